@@ -1,0 +1,328 @@
+"""Plain fp64 CPU oracle of one FlashMemory LSA + KV_SWAP decode step.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline / reference legs of ``bench.py`` may import or run this module. It
+shares no code with the CUDA path: it does not import the product package and
+the product package does not import it. Inputs come from the seeded
+generator in ``srh_workload`` (random draws only) or from hand-made cases.
+
+The step, as the pages state it:
+  1. score every compressed chunk by dotting 3 memory-indexer query sets
+     against the frozen compressed indexer keys (PocketLLM
+     "FlashMemory 1M 上下文显存优化使用文档", section "技术细节 / 架构概览", box
+     "FlashMemory Runtime Scoring", steps 1-2; FlashMemory-DeepSeek-V4 summary,
+     section "LSA 让模型预判 KV chunk");
+  2. ensemble the three scores by max (OR-mode) or mean (same box, step 3;
+     summary section "Memory Indexer 放哪里");
+  3. select by top-k (index_topk = 512) or by a sigmoid threshold
+     (same box, step 3; summary section "LSA 让模型预判 KV chunk");
+  4. per sparse layer, resolve the selected chunks against the GPU staging
+     slots with the pages' LRU (section "KV_SWAP 实现细节", the
+     GgufKvSwapLayerState structure and the Swap-in flow);
+  5. attention over the 128-row window plus the selected chunks
+     (section "架构概览", box "Per-layer Sparse Attention", step 3, and
+     "Memory Layout").
+
+Readings taken where the pages are silent (each one is a choice, listed with
+its reason in the design notes):
+  * the 8 query heads of one indexer combine by max; logit = scale*max + b_i,
+    scale = 1/sqrt(128);
+  * MEAN ensembles logits (max is domain-free because the sigmoid is monotone);
+  * the threshold test is strict and taken in the logit domain:
+    sigmoid(s) > tau  <=>  s > ln(tau/(1-tau));
+  * order and tie-break everywhere: score descending, then chunk index ascending;
+    a threshold set larger than the clamp keeps its first ``clamp`` entries;
+  * a layer of ratio r reuses the global selection through
+    c -> floor(c*src_ratio/r), first occurrence kept;
+  * the LRU list starts with every slot free, slot 0 at the back;
+  * attention is MQA over the 512-wide latent (K = V = row), scale 1/sqrt(512).
+
+Parity pins (checks that do not reuse this code) live in ``tests/test_oracle_*.py``.
+"""
+from __future__ import annotations
+
+import math
+from collections import OrderedDict
+from dataclasses import dataclass, field
+from typing import Callable, Dict, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+KV_DIM = 512
+WINDOW = 128
+N_INDEXERS = 3
+INDEXER_HEADS = 8
+INDEXER_DIM = 128
+
+ENSEMBLE_MAX = 0
+ENSEMBLE_MEAN = 1
+SELECT_TOPK = 0
+SELECT_THRESH = 1
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns (uint16) to float64; exact."""
+    b = np.asarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ----------------------------------------------------------------------------
+# Pinned host memory (section "关键参数调优", item 2, PINNED_MIB: the formula
+#   required_pinned_mib = sum(layer_compressed_cap * kv_dim * sizeof(float)) / 2^20
+#   layer_compressed_cap = (context_length + ratio - 1) / ratio )
+# ----------------------------------------------------------------------------
+def compressed_cap(context_len: int, ratio: int) -> int:
+    return (context_len + ratio - 1) // ratio
+
+
+def layer_pinned_bytes(context_len: int, ratio: int, kv_dim: int = KV_DIM) -> int:
+    return compressed_cap(context_len, ratio) * kv_dim * 4
+
+
+def required_pinned_bytes(context_len: int, ratios: Sequence[int], kv_dim: int = KV_DIM) -> int:
+    return sum(layer_pinned_bytes(context_len, r, kv_dim) for r in ratios)
+
+
+def swap_enabled(compressed_cap_: int, gpu_chunks: int) -> bool:
+    """A layer swaps only if its chunks do not all fit in the staging slots
+    (section "故障排查", the note on ``reason=no_layer_with_compressed_cap_gt_gpu_chunks``)."""
+    return compressed_cap_ > gpu_chunks
+
+
+# ----------------------------------------------------------------------------
+# 1-2. Scoring and ensemble
+# ----------------------------------------------------------------------------
+def head_dots(keys_bits: np.ndarray, q_bits: np.ndarray) -> np.ndarray:
+    """s_{i,h}(c) = <Q[i,h,:], K[c,:]> for every chunk c: ``[n][3][8]``."""
+    k = bf16_to_f64(keys_bits)                       # [n][128]
+    q = bf16_to_f64(q_bits).reshape(N_INDEXERS * INDEXER_HEADS, INDEXER_DIM)
+    return (k @ q.T).reshape(k.shape[0], N_INDEXERS, INDEXER_HEADS)
+
+
+def indexer_logits(keys_bits, q_bits, scale: float, bias: Sequence[float]) -> np.ndarray:
+    """s_i(c) = scale * max_h s_{i,h}(c) + b_i: ``[3][n]``."""
+    d = head_dots(keys_bits, q_bits)
+    per = d.max(axis=2)                              # max over the 8 heads
+    b = np.asarray(bias, dtype=np.float64).reshape(1, N_INDEXERS)
+    return (scale * per + b).T
+
+
+def ensemble(logits: np.ndarray, mode: int) -> np.ndarray:
+    """MAX: s = max_i s_i (OR-mode routing); MEAN: s = (s_0 + s_1 + s_2) / 3."""
+    if mode == ENSEMBLE_MAX:
+        return logits.max(axis=0)
+    if mode == ENSEMBLE_MEAN:
+        return logits.sum(axis=0) / N_INDEXERS
+    raise ValueError(mode)
+
+
+def score(keys_bits, q_bits, scale, bias, mode) -> np.ndarray:
+    return ensemble(indexer_logits(keys_bits, q_bits, scale, bias), mode)
+
+
+# ----------------------------------------------------------------------------
+# 3. Selection
+# ----------------------------------------------------------------------------
+def threshold_logit(tau: float) -> float:
+    """sigmoid(s) > tau  <=>  s > ln(tau / (1 - tau))."""
+    return math.log(tau / (1.0 - tau))
+
+
+def order_desc(s: np.ndarray) -> np.ndarray:
+    """Chunk indices ordered by (score descending, index ascending)."""
+    s = np.asarray(s, dtype=np.float64)
+    return np.lexsort((np.arange(s.shape[0]), -s))
+
+
+def select_topk(s: np.ndarray, k: int) -> np.ndarray:
+    return order_desc(s)[:min(k, s.shape[0])].astype(np.int64)
+
+
+def select_threshold(s: np.ndarray, tau: float, clamp: int) -> np.ndarray:
+    t = threshold_logit(tau)
+    o = order_desc(s)
+    o = o[np.asarray(s)[o] > t]
+    return o[:clamp].astype(np.int64)
+
+
+def select(s, mode: int, k: int, tau: float, clamp: int) -> np.ndarray:
+    if mode == SELECT_TOPK:
+        return select_topk(s, k)
+    if mode == SELECT_THRESH:
+        return select_threshold(s, tau, clamp)
+    raise ValueError(mode)
+
+
+# ----------------------------------------------------------------------------
+# 4a. All sparse layers reuse the one global selection (section "技术细节",
+#     "FlashMemory vs Native Indexer": selection granularity is global).
+# ----------------------------------------------------------------------------
+def layer_chunks(sel: Sequence[int], src_ratio: int, layer_ratio: int) -> List[int]:
+    out: List[int] = []
+    seen = set()
+    for c in sel:
+        m = (int(c) * src_ratio) // layer_ratio
+        if m not in seen:
+            seen.add(m)
+            out.append(m)
+    return out
+
+
+# ----------------------------------------------------------------------------
+# 4b. KV_SWAP: GgufKvSwapLayerState and gguf_kv_swap_in_selected
+#     (section "KV_SWAP 实现细节", data structure and Swap-in flow)
+# ----------------------------------------------------------------------------
+class NotStoredError(RuntimeError):
+    """A selected chunk has not been stored to the host cache yet
+    (section "故障排查", error 4)."""
+
+
+@dataclass
+class SwapResult:
+    phys: List[int]                       # window + slot (or window + chunk when resident)
+    misses: List[Tuple[int, int]]         # (logical chunk, slot) in processing order
+    hits: int
+
+
+class KvSwapLayerState:
+    """One (layer, sequence) of the swap state.
+
+    ``slot_lru`` is the pages' ``std::list<int>`` with front = most recently
+    used; it is held as an ordered dict whose LAST item is the front and whose
+    FIRST item is the back, so ``pop_back`` = ``popitem(last=False)``. All slots
+    start free at the back, slot 0 outermost, so the first misses fill slots
+    0, 1, 2, ...
+    """
+
+    def __init__(self, compressed_cap_: int, gpu_chunks: int, window: int = WINDOW):
+        self.compressed_cap = compressed_cap_
+        self.gpu_chunks = gpu_chunks
+        self.window = window
+        self.swap_enabled = swap_enabled(compressed_cap_, gpu_chunks)
+        self.host_ready = np.zeros(compressed_cap_, dtype=np.uint8)
+        self.gpu_slot_logical = [-1] * gpu_chunks
+        self.slot_by_logical: Dict[int, int] = {}
+        self.slot_lru: "OrderedDict[int, None]" = OrderedDict((s, None) for s in range(gpu_chunks))
+        self.hits = 0
+        self.misses = 0
+
+    def store(self, logical: int) -> None:
+        """Store flow: the chunk now exists in the host cache; a resident copy stays."""
+        self.host_ready[logical] = 1
+
+    def swap_in_selected(self, logical_ids: Sequence[int]) -> SwapResult:
+        phys: List[int] = []
+        misses: List[Tuple[int, int]] = []
+        hits = 0
+        if not self.swap_enabled:
+            # swap disabled: every chunk is resident at its own index
+            for c in logical_ids:
+                if not self.host_ready[c]:
+                    raise NotStoredError(f"chunk {c} selected before it was stored")
+                phys.append(self.window + int(c))
+            return SwapResult(phys, misses, 0)
+        for c in logical_ids:
+            c = int(c)
+            slot = self.slot_by_logical.get(c)
+            if slot is not None:
+                self.slot_lru.move_to_end(slot)          # LRU touch: move to front
+                hits += 1
+            else:
+                if not self.host_ready[c]:
+                    raise NotStoredError(f"chunk {c} selected before it was stored")
+                slot, _ = self.slot_lru.popitem(last=False)   # LRU evict: pop_back
+                old = self.gpu_slot_logical[slot]
+                if old >= 0:
+                    del self.slot_by_logical[old]
+                self.gpu_slot_logical[slot] = c
+                self.slot_by_logical[c] = slot
+                self.slot_lru[slot] = None               # the filled slot is the front
+                misses.append((c, slot))                 # H2D h_compressed_kv[c] -> slot
+            phys.append(self.window + slot)
+        self.hits += hits
+        self.misses += len(misses)
+        return SwapResult(phys, misses, hits)
+
+
+# ----------------------------------------------------------------------------
+# 5. Attention over window + selected chunks (K = V = the 512-wide latent row)
+# ----------------------------------------------------------------------------
+def attend(q_bits: np.ndarray, rows: np.ndarray) -> np.ndarray:
+    """o_h = sum_j softmax_j(<q_h, e_j> / sqrt(D)) e_j, all in fp64. ``[H][D]``."""
+    q = bf16_to_f64(q_bits)
+    e = np.asarray(rows, dtype=np.float64)
+    z = (q @ e.T) / math.sqrt(e.shape[1])
+    z = z - z.max(axis=1, keepdims=True)
+    p = np.exp(z)
+    return (p @ e) / p.sum(axis=1, keepdims=True)
+
+
+# ----------------------------------------------------------------------------
+# The decode step
+# ----------------------------------------------------------------------------
+@dataclass
+class StepResult:
+    scores: List[np.ndarray]              # [B] of [n] fp64
+    sel: List[np.ndarray]                 # [B] of selected chunk ids, in order
+    lists: List[List[List[int]]]          # [L][B] per-layer ordered chunk lists
+    swap: List[List[SwapResult]]          # [L][B]
+    out: Dict[Tuple[int, int], np.ndarray] = field(default_factory=dict)  # (l, b) -> [H][512]
+
+
+class DecodeOracle:
+    """Holds the per-(layer, sequence) swap state across decode steps."""
+
+    def __init__(self, *, context_len: int, layer_ratios: Sequence[int], gpu_chunks: int,
+                 index_topk: int, batch: int, scale: float, bias: Sequence[float],
+                 ensemble_mode: int, select_mode: int, tau: float, clamp: int,
+                 src_ratio: int = 4, window: int = WINDOW):
+        self.context_len = context_len
+        self.layer_ratios = list(layer_ratios)
+        self.gpu_chunks = gpu_chunks
+        self.index_topk = index_topk
+        self.batch = batch
+        self.scale = scale
+        self.bias = list(bias)
+        self.ensemble_mode = ensemble_mode
+        self.select_mode = select_mode
+        self.tau = tau
+        self.clamp = clamp
+        self.src_ratio = src_ratio
+        self.window = window
+        self.caps = [compressed_cap(context_len, r) for r in self.layer_ratios]
+        self.states = [[KvSwapLayerState(cap, gpu_chunks, window) for _ in range(batch)]
+                       for cap in self.caps]
+
+    def mark_all_stored(self) -> None:
+        for row in self.states:
+            for st in row:
+                st.host_ready[:] = 1
+
+    def step(self, keys_of: Callable[[int], np.ndarray], fm_q_of: Callable[[int], np.ndarray],
+             attn_q_of: Optional[Callable[[int, int], np.ndarray]] = None,
+             window_of: Optional[Callable[[int, int], np.ndarray]] = None,
+             pool_rows_of: Optional[Callable[[int, int, Sequence[int]], np.ndarray]] = None,
+             attend_pairs: Optional[Sequence[Tuple[int, int]]] = None) -> StepResult:
+        scores, sels = [], []
+        for b in range(self.batch):
+            s = score(keys_of(b), fm_q_of(b), self.scale, self.bias, self.ensemble_mode)
+            scores.append(s)
+            sels.append(select(s, self.select_mode, self.index_topk, self.tau, self.clamp))
+        lists, swaps = [], []
+        for l, ratio in enumerate(self.layer_ratios):
+            row_l, row_s = [], []
+            for b in range(self.batch):
+                lst = layer_chunks(sels[b], self.src_ratio, ratio)
+                row_l.append(lst)
+                row_s.append(self.states[l][b].swap_in_selected(lst))
+            lists.append(row_l)
+            swaps.append(row_s)
+        res = StepResult(scores, sels, lists, swaps)
+        if attend_pairs is None and attn_q_of is not None:
+            attend_pairs = [(l, b) for l in range(len(self.layer_ratios)) for b in range(self.batch)]
+        for (l, b) in attend_pairs or []:
+            rows = np.concatenate([np.asarray(window_of(l, b), dtype=np.float64),
+                                   np.asarray(pool_rows_of(l, b, lists[l][b]), dtype=np.float64)
+                                   .reshape(-1, KV_DIM)], axis=0)
+            res.out[(l, b)] = attend(attn_q_of(l, b), rows)
+        return res

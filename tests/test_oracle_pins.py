@@ -1,0 +1,420 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle itself.
+
+Each test checks one oracle function against what the pages print, a closed
+form, an invariant, an independent brute-force formulation, or a library
+routine. A plausible slip in the oracle (a dropped term, a wrong sign or
+index, a transposed operand, a wrong tie-break) fails at least one of them.
+"""
+import math
+import os
+import random
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import srh_oracle as O
+from srh_workload import configs as C
+from srh_workload import generate as G
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(line.split())
+    return rows
+
+
+# --------------------------------------------------------------------------- pinned sizes
+def _printed_close(value_mb: float, printed: str) -> bool:
+    """True if ``value_mb`` rounds to the printed figure (its last printed digit)."""
+    digits = len(printed.split(".")[1]) if "." in printed else 0
+    p = float(printed)
+    if digits == 0:
+        # integers such as "134" or "2680" carry 2-3 significant digits on the page
+        sig = len(printed.rstrip("0")) or 1
+        unit = 10 ** (len(printed) - sig)
+        return abs(value_mb - p) <= 0.5 * unit + 1e-9
+    return abs(value_mb - p) <= 0.5 * 10 ** (-digits) + 1e-9
+
+
+def test_pinned_formula_matches_page_examples():
+    """Section "关键参数调优" item 2: per-layer pinned bytes and per-ratio totals."""
+    n = 0
+    for row in _golden_rows("pinned_sizes.txt"):
+        if row[0] == "total":
+            continue
+        ctx, ratio, layers, cap = (int(x) for x in row[:4])
+        per_mb, total_mb = row[4], row[5]
+        assert O.compressed_cap(ctx, ratio) == cap
+        per = O.layer_pinned_bytes(ctx, ratio)
+        assert per == cap * 512 * 4
+        assert _printed_close(per / 1e6, per_mb), (ctx, ratio, per / 1e6, per_mb)
+        exact_total = O.required_pinned_bytes(ctx, [ratio] * layers) / 1e6
+        # the page multiplies its rounded per-layer figure by the layer count
+        assert abs(float(per_mb) * layers - float(total_mb)) <= 0.02 * float(total_mb) + 0.05
+        assert abs(exact_total - float(total_mb)) <= 0.02 * float(total_mb) + 0.05
+        n += 1
+    assert n == 6
+
+
+def test_pinned_grand_totals():
+    """Grand totals ~87 MB / ~2.77 GB / ~11 GB for 20 ratio-4 + 21 ratio-128 layers."""
+    ratios = [4] * 20 + [128] * 21
+    for row in _golden_rows("pinned_sizes.txt"):
+        if row[0] != "total":
+            continue
+        ctx, printed = int(row[1]), float(row[2])
+        got = O.required_pinned_bytes(ctx, ratios) / 1e6
+        assert abs(got - printed) <= 0.01 * printed + 0.5, (ctx, got, printed)
+
+
+def test_compressed_cap_rounds_up():
+    assert O.compressed_cap(64, 4) == 16
+    assert O.compressed_cap(65, 4) == 17
+    assert O.compressed_cap(1, 128) == 1
+    assert O.compressed_cap(128, 128) == 1
+    assert O.compressed_cap(129, 128) == 2
+    assert O.compressed_cap(0, 4) == 0
+
+
+def test_log_example_numbers():
+    """Section "使用示例", 示例 1: pinned_mib=84, max_capacity=640, stats totals."""
+    g = {r[0]: int(r[1]) for r in _golden_rows("log_example.txt")}
+    cap = O.compressed_cap(g["context_len"], g["ratio"])
+    n = g["swapped_layers"]
+    assert O.swap_enabled(cap, g["gpu_chunks"])
+    assert O.required_pinned_bytes(g["context_len"], [g["ratio"]] * n) // 2**20 == g["pinned_mib"]
+    assert g["window"] + g["gpu_chunks"] == g["max_capacity"]
+    assert n * g["gpu_chunks"] == g["gpu_chunks_total"]
+    assert n * cap == g["compressed_cap_total"]
+    # section "故障排查": 64-token context, ratio 4
+    short = O.compressed_cap(g["short_context_len"], 4)
+    assert short == g["short_compressed_cap"]
+    assert not O.swap_enabled(short, g["short_gpu_chunks_disabled"])
+    assert O.swap_enabled(short, g["short_gpu_chunks_enabled"])
+
+
+# --------------------------------------------------------------------------- scoring
+def _bf16_exact(bits: int) -> Fraction:
+    """bf16 value as an exact rational, decoded field by field."""
+    s, e, m = (bits >> 15) & 1, (bits >> 7) & 0xFF, bits & 0x7F
+    assert e != 0xFF
+    if e == 0:
+        v = Fraction(m, 128) * Fraction(1, 2 ** 126)
+    else:
+        v = Fraction(128 + m, 128) * (Fraction(2) ** (e - 127))
+    return -v if s else v
+
+
+def test_head_dots_exact_against_rational_arithmetic():
+    rng = np.random.default_rng(7)
+    keys = G.f32_to_bf16_bits(rng.standard_normal((9, 128), dtype=np.float32))
+    q = G.f32_to_bf16_bits(2.0 * rng.standard_normal((3, 8, 128), dtype=np.float32))
+    d = O.head_dots(keys, q)
+    assert d.shape == (9, 3, 8)
+    for c in range(9):
+        for i in range(3):
+            for h in range(8):
+                exact = sum(_bf16_exact(int(a)) * _bf16_exact(int(b))
+                            for a, b in zip(keys[c], q[i, h]))
+                assert Fraction(d[c, i, h]) == exact, (c, i, h)
+
+
+def _bits(x):
+    return G.f32_to_bf16_bits(np.asarray(x, dtype=np.float32))
+
+
+def test_logit_is_scaled_max_over_heads_plus_indexer_bias():
+    # one chunk whose key is 2*e_0; head h of indexer i carries (i*8 + h + 1) * e_0
+    key = np.zeros((1, 128), np.float32)
+    key[0, 0] = 2.0
+    q = np.zeros((3, 8, 128), np.float32)
+    for i in range(3):
+        for h in range(8):
+            q[i, h, 0] = (-1.0) ** h * (i * 8 + h + 1)
+    bias = [0.25, -1.0, 3.0]
+    lg = O.indexer_logits(_bits(key), _bits(q), 0.5, bias)
+    # largest head of indexer i: h = 6 (positive, even) -> 2 * (8i + 7)
+    want = [0.5 * 2 * (8 * i + 7) + bias[i] for i in range(3)]
+    assert np.array_equal(lg[:, 0], np.array(want))
+    assert O.ensemble(lg, O.ENSEMBLE_MAX)[0] == max(want)
+    assert O.ensemble(lg, O.ENSEMBLE_MEAN)[0] == pytest.approx(sum(want) / 3, abs=0)
+
+
+def test_or_mode_max_threshold_is_union_of_indexers():
+    """Summary section "Memory Indexer 放哪里": a chunk is recalled if ANY indexer recalls it."""
+    rng = np.random.default_rng(3)
+    keys = G.f32_to_bf16_bits(rng.standard_normal((500, 128), dtype=np.float32))
+    q = G.f32_to_bf16_bits(rng.standard_normal((3, 8, 128), dtype=np.float32))
+    lg = O.indexer_logits(keys, q, 128 ** -0.5, [-2.0, -2.5, -1.5])
+    s = O.ensemble(lg, O.ENSEMBLE_MAX)
+    for tau in (0.3, 0.5, 0.8):
+        t = O.threshold_logit(tau)
+        union = set(np.nonzero((lg > t).any(axis=0))[0].tolist())
+        got = set(O.select_threshold(s, tau, 10 ** 9).tolist())
+        assert got == union
+
+
+def test_sigmoid_threshold_equivalence():
+    rng = np.random.default_rng(11)
+    s = rng.normal(0, 3, 4000)
+    for tau in (0.1, 0.5, 0.9):
+        t = O.threshold_logit(tau)
+        keep = np.abs(s - t) > 1e-9
+        sig = 1.0 / (1.0 + np.exp(-s))
+        assert np.array_equal((sig > tau)[keep], (s > t)[keep])
+    assert O.threshold_logit(0.5) == 0.0
+
+
+# --------------------------------------------------------------------------- selection
+def _rank_bruteforce(s):
+    n = len(s)
+    return [sum(1 for j in range(n) if s[j] > s[i] or (s[j] == s[i] and j < i)) for i in range(n)]
+
+
+@pytest.mark.parametrize("n,k", [(1, 1), (7, 3), (33, 8), (64, 17), (64, 64), (20, 50)])
+def test_topk_matches_rank_definition(n, k):
+    rng = np.random.default_rng(n * 100 + k)
+    s = rng.choice([-1.5, 0.0, 0.25, 2.0, 3.0], size=n) + rng.choice([0.0, 1e-3], size=n)
+    rank = _rank_bruteforce(list(s))
+    want = [i for _, i in sorted((r, i) for i, r in enumerate(rank))][:min(k, n)]
+    assert O.select_topk(s, k).tolist() == want
+
+
+def test_topk_k_at_least_n_selects_everything_in_order():
+    s = np.array([0.5, 2.0, 0.5, -1.0, 2.0])
+    assert O.select_topk(s, 5).tolist() == [1, 4, 0, 2, 3]
+    assert O.select_topk(s, 99).tolist() == [1, 4, 0, 2, 3]
+
+
+def test_threshold_is_strict_ordered_and_clamped():
+    s = np.array([0.0, 1.0, -0.5, 3.0, 1.0, 1e-12, -1e-12])
+    assert O.select_threshold(s, 0.5, 100).tolist() == [3, 1, 4, 5]
+    assert O.select_threshold(s, 0.5, 2).tolist() == [3, 1]
+    assert O.select_threshold(s, 0.5, 0).tolist() == []
+    rng = np.random.default_rng(5)
+    s = rng.choice([-1.0, 0.5, 0.75, 1.5], size=40)
+    rank = _rank_bruteforce(list(s))
+    over = sorted((rank[i], i) for i in range(40) if s[i] > 0.0)
+    assert O.select_threshold(s, 0.5, 9).tolist() == [i for _, i in over][:9]
+
+
+# --------------------------------------------------------------------------- ratio mapping
+def test_layer_chunks_ratio_mapping():
+    assert O.layer_chunks([5, 37, 33, 64, 3], 4, 4) == [5, 37, 33, 64, 3]
+    assert O.layer_chunks([5, 37, 33, 64, 3], 4, 128) == [0, 1, 2]
+    assert O.layer_chunks([40, 8, 9, 41], 4, 8) == [20, 4]
+    assert O.layer_chunks([], 4, 128) == []
+
+
+# --------------------------------------------------------------------------- LRU
+def _lru_textbook(steps, G_):
+    """Textbook LRU by timestamps: hit iff fewer than G other distinct chunks were
+    referenced since the last reference (stack distance); a miss fills the lowest
+    free slot, else the slot of the chunk referenced longest ago."""
+    last, slot_of, out, t = {}, {}, [], 0
+    for refs in steps:
+        res = []
+        for c in refs:
+            if c in last:
+                since = {x for x, tt in last.items() if tt > last[c]}
+                hit_sd = len(since) < G_
+            else:
+                hit_sd = False
+            hit = c in slot_of
+            assert hit == hit_sd
+            if hit:
+                slot = slot_of[c]
+            elif len(slot_of) < G_:
+                slot = min(set(range(G_)) - set(slot_of.values()))
+                slot_of[c] = slot
+            else:
+                victim = min(slot_of, key=lambda x: last[x])
+                slot = slot_of.pop(victim)
+                slot_of[c] = slot
+            last[c] = t
+            t += 1
+            res.append((hit, slot))
+        out.append(res)
+    return out, slot_of
+
+
+def _random_trace(seed, G_, universe, n_steps):
+    r = random.Random(seed)
+    steps, prev = [], []
+    for _ in range(n_steps):
+        m = r.randint(0, G_)
+        keep = [c for c in prev if r.random() < 0.7]
+        pool = [c for c in range(universe) if c not in keep]
+        new = r.sample(pool, max(0, min(m - len(keep), len(pool))))
+        refs = (keep + new)[:m]
+        r.shuffle(refs)
+        steps.append(refs)
+        prev = refs
+    return steps
+
+
+@pytest.mark.parametrize("seed,G_,universe", [(0, 4, 9), (1, 8, 30), (2, 16, 40), (3, 5, 6), (4, 32, 200)])
+def test_lru_matches_textbook_stack_distance(seed, G_, universe):
+    steps = _random_trace(seed, G_, universe, 40)
+    st = O.KvSwapLayerState(universe + G_ + 1, G_, window=128)
+    st.host_ready[:] = 1
+    want, resident = _lru_textbook(steps, G_)
+    for refs, exp in zip(steps, want):
+        r = st.swap_in_selected(refs)
+        got = []
+        miss_slots = dict(r.misses)
+        for c, p in zip(refs, r.phys):
+            got.append((c not in miss_slots, p - 128))
+        assert got == exp
+        assert r.hits + len(r.misses) == len(refs)
+    assert {c: s for c, s in st.slot_by_logical.items()} == resident
+    assert sorted(s for s in st.gpu_slot_logical if s >= 0) == sorted(resident)
+
+
+def test_lru_evicts_a_chunk_selected_later_in_the_same_step():
+    """The Swap-in flow walks the list in order: a miss may pop a slot whose chunk
+    is selected further down the same list (then that chunk misses too)."""
+    st = O.KvSwapLayerState(10, 2)
+    st.host_ready[:] = 1
+    r1 = st.swap_in_selected([1, 2])          # 1 -> slot 0, 2 -> slot 1; 1 is least recent
+    assert r1.phys == [128, 129] and r1.hits == 0
+    r2 = st.swap_in_selected([3, 1])          # 3 pops slot 0 (chunk 1); then 1 pops slot 1
+    assert r2.misses == [(3, 0), (1, 1)] and r2.hits == 0
+    assert r2.phys == [128, 129]
+
+
+def test_lru_invariants_constant_selection_all_hits():
+    st = O.KvSwapLayerState(5000, 1024)
+    st.host_ready[:] = 1
+    sel = list(np.random.default_rng(0).permutation(5000)[:512])
+    r = st.swap_in_selected(sel)
+    assert r.hits == 0 and len(r.misses) == 512
+    assert [s for _, s in r.misses] == list(range(512))     # free slots fill in order
+    for _ in range(3):
+        r = st.swap_in_selected(sel)
+        assert r.hits == 512 and not r.misses
+    assert len(set(r.phys)) == 512
+
+
+def test_lru_not_stored_error():
+    st = O.KvSwapLayerState(10, 4)
+    st.store(3)
+    st.swap_in_selected([3])
+    with pytest.raises(O.NotStoredError):
+        st.swap_in_selected([3, 7])
+
+
+def test_swap_disabled_layer_is_identity_mapped():
+    st = O.KvSwapLayerState(16, 16)
+    st.host_ready[:] = 1
+    assert not st.swap_enabled
+    r = st.swap_in_selected([9, 0, 15])
+    assert r.phys == [137, 128, 143] and r.hits == 0 and not r.misses
+
+
+# --------------------------------------------------------------------------- attention
+def test_attention_matches_torch_sdpa_float64():
+    rng = np.random.default_rng(1)
+    q = G.f32_to_bf16_bits(rng.standard_normal((16, 512), dtype=np.float32))
+    rows = rng.standard_normal((200, 512))
+    got = O.attend(q, rows)
+    qt = torch.from_numpy(O.bf16_to_f64(q))[None, None]
+    et = torch.from_numpy(rows)[None, None]
+    want = torch.nn.functional.scaled_dot_product_attention(qt, et, et)[0, 0].numpy()
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-13)
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(2)
+    rows = rng.standard_normal((1, 512))
+    q = G.f32_to_bf16_bits(rng.standard_normal((4, 512), dtype=np.float32))
+    np.testing.assert_allclose(O.attend(q, rows), np.repeat(rows, 4, axis=0), rtol=0, atol=1e-15)
+    rows = rng.standard_normal((37, 512))
+    zero_q = np.zeros((3, 512), np.uint16)
+    np.testing.assert_allclose(O.attend(zero_q, rows), np.repeat(rows.mean(0, keepdims=True), 3, 0),
+                               rtol=1e-13, atol=1e-14)
+    # two rows, logits differing by exactly ln 3 -> weights 3/4, 1/4
+    e = np.zeros((2, 512))
+    e[0, 0] = math.sqrt(512) * math.log(3.0)
+    q1 = np.zeros((1, 512), np.float32)
+    q1[0, 0] = 1.0
+    o = O.attend(G.f32_to_bf16_bits(q1), e)
+    assert o[0, 0] == pytest.approx(0.75 * e[0, 0], rel=1e-13)
+
+
+# --------------------------------------------------------------------------- whole step
+def _small_workload(**kw):
+    base = dict(name="pin", code=99, context_len=256, layer_ratios=(4, 128), gpu_chunks=64,
+                index_topk=64, ensemble=C.ENSEMBLE_MAX, select_mode=C.SELECT_TOPK, tau=0.5,
+                bias=0.0, n_heads=16, batch=2, steps=6, lookahead=2, n_needles=4)
+    base.update(kw)
+    return C.Workload(**base)
+
+
+def _run(w, attend=True):
+    ora = O.DecodeOracle(context_len=w.context_len, layer_ratios=w.layer_ratios,
+                         gpu_chunks=w.gpu_chunks, index_topk=w.index_topk, batch=w.batch,
+                         scale=w.scale, bias=[w.bias] * 3, ensemble_mode=w.ensemble,
+                         select_mode=w.select_mode, tau=w.tau, clamp=w.clamp)
+    ora.mark_all_stored()
+    keys = [G.keys(w, b) for b in range(w.batch)]
+    pools = {(l, b): G.pool(w, l, b) for l in range(w.n_layers) for b in range(w.batch)}
+    res = []
+    for t in range(w.steps):
+        res.append(ora.step(lambda b: keys[b], lambda b: G.fm_queries(w, t, b),
+                            (lambda l, b: G.attn_q(w, t, l, b)) if attend else None,
+                            lambda l, b: G.window(w, l, b),
+                            lambda l, b, idx: pools[(l, b)][np.asarray(idx, dtype=np.int64)]))
+    return ora, res, keys, pools
+
+
+def test_topk_covering_all_chunks_is_dense_attention():
+    w = _small_workload(index_topk=64, gpu_chunks=64)      # n = 64 chunks, all selected
+    _, res, _, pools = _run(w)
+    for t, r in enumerate(res):
+        for b in range(w.batch):
+            assert sorted(r.sel[b].tolist()) == list(range(64))
+            rows = np.concatenate([G.window(w, 0, b), pools[(0, b)]]).astype(np.float64)
+            qt = torch.from_numpy(O.bf16_to_f64(G.attn_q(w, t, 0, b)))[None, None]
+            et = torch.from_numpy(rows)[None, None]
+            want = torch.nn.functional.scaled_dot_product_attention(qt, et, et)[0, 0].numpy()
+            np.testing.assert_allclose(r.out[(0, b)], want, rtol=1e-12, atol=1e-13)
+
+
+def test_residency_changes_slots_never_outputs():
+    """kestrel-llm-cuda 06, section 3.4: residency changes occupancy, never outputs."""
+    swapped = _small_workload(index_topk=16, gpu_chunks=24)    # cap 64 > 24 -> swap
+    resident = swapped.with_(gpu_chunks=64)                     # cap 64 <= 64 -> resident
+    _, rs, _, _ = _run(swapped)
+    _, rr, _, _ = _run(resident)
+    saw_miss_after_start = False
+    for t, (a, b) in enumerate(zip(rs, rr)):
+        for key in a.out:
+            assert np.array_equal(a.out[key], b.out[key])
+        for bb in range(swapped.batch):
+            assert a.swap[0][bb].phys != b.swap[0][bb].phys or not a.sel[bb].size
+            if t > 0 and a.swap[0][bb].misses:
+                saw_miss_after_start = True
+    assert saw_miss_after_start
+
+
+def test_needles_are_selected_by_every_ensemble():
+    """The planted needles score far above the noise chunks, so top-k and the
+    threshold selector (bias -7, tau 0.5) both recall them."""
+    for w in (_small_workload(context_len=8192, index_topk=32, gpu_chunks=64, n_needles=8,
+                              layer_ratios=(4,), steps=2, batch=1),
+              _small_workload(context_len=8192, ensemble=C.ENSEMBLE_MEAN, select_mode=C.SELECT_THRESH,
+                              bias=-7.0, gpu_chunks=512, n_needles=32, layer_ratios=(4,), steps=2,
+                              batch=1)):
+        _, res, _, _ = _run(w, attend=False)
+        for t, r in enumerate(res):
+            nd = set(G.step_needles(w, t, 0).tolist())
+            assert nd <= set(r.sel[0].tolist())
