@@ -1,0 +1,433 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark of the FlashMemory LSA + KV_SWAP hot path on GB300.
+
+One "step" is one pass of the whole hot path -- fm_score, fm_select,
+kvswap_stage (LRU resolve + miss gather) and lsa_attend over all sparse
+layers -- for one batch of synthetic input, with inputs already resident in
+HBM. Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config ctx8k]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, timed on the host
+
+Timing: W warm-up steps, then K timed steps; the L2 is flushed (a 256 MiB
+write) before every timed step and each step is bracketed by CUDA events on
+its stream, so the flush is outside the timed spans. Multi-GPU (N > 1 under
+torchrun) runs N independent replicas (weak scaling, no collective on the
+data path); value = steps of all ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from srh_workload import configs as C  # noqa: E402
+from srh_workload import generate as G  # noqa: E402
+
+KERNELS_PER_STEP = 5          # score, select, lru, gather, attend
+Q_CYCLE = 16                  # distinct attention-query sets cycled through the steps
+FLUSH_BYTES = 256 << 20       # > 2x the 126 MiB L2
+METRIC = "decode steps/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="ctx8k", choices=sorted(C.ALL))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-steps", type=int, default=0, help="0 = auto")
+    ap.add_argument("--quiet", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- distributed
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("SRH_DIST_BACKEND", "nccl")
+        dist.init_process_group(backend)
+        return dist, rank, world, local
+    return None, 0, 1, 0
+
+
+def aggregate(dist, local_seconds: float, local_steps: int, device=None):
+    """Max of the timed seconds and sum of the steps over ranks."""
+    if dist is None:
+        return local_seconds, local_steps
+    import torch
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=device)
+    s = torch.tensor([float(local_steps)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(s, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(s.item())
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 8:
+                continue
+            try:
+                sm.append(float(p[0]))
+                mx.append(float(p[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, p[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- peaks
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def traffic_record(kernel: str):
+    """Measured DRAM bytes per launch from an ncu capture, if the kernel source
+    is unchanged since (profiles/traffic.json keys it by a hash of the source)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "sparse_retrieval_host_gb300", "csrc", rec["source"])
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return rec if h == rec.get("source_sha") else None
+
+
+# --------------------------------------------------------------------------- setup
+def setup(w, device):
+    import torch
+    from sparse_retrieval_host_gb300.runtime import DecodeStep, StepSpec, bits_to_i16
+    ds = DecodeStep(batch=w.batch, layer_ratios=w.layer_ratios, gpu_chunks=w.gpu_chunks,
+                    index_topk=w.index_topk, context_len=w.context_len, n_heads=w.n_heads,
+                    max_select=w.clamp)
+    for l in range(w.n_layers):
+        for b in range(w.batch):
+            G.fill_pool(w, l, b, ds.pool_view(l, b))
+            ds.mark_stored(l, b)
+            ds.window[l, b] = torch.from_numpy(G.window(w, l, b))
+    for b in range(w.batch):
+        ds.keys[b] = bits_to_i16(G.keys(w, b))
+    n_win = (w.steps + w.lookahead - 1) // w.lookahead
+    fmq = np.stack([np.stack([G.fm_queries(w, i * w.lookahead, b) for b in range(w.batch)])
+                    for i in range(n_win)])
+    fm_q_all = bits_to_i16(fmq).to(device)
+    nq = min(Q_CYCLE, w.steps)
+    qs = np.stack([np.stack([np.stack([G.attn_q(w, t, l, b) for b in range(w.batch)])
+                             for l in range(w.n_layers)]) for t in range(nq)])
+    q_all = bits_to_i16(qs).to(device)
+    spec = StepSpec(w.scale, [w.bias] * 3, w.ensemble, w.select_mode, w.index_topk, w.tau, w.clamp)
+    return ds, spec, fm_q_all, q_all
+
+
+def attn_bytes(w, count_l):
+    """Algorithmic bytes of one lsa_attend launch: rows read + q read + out written."""
+    rows = count_l.sum() + w.n_layers * w.batch * C.WINDOW
+    return int(rows) * C.KV_DIM * 4 + w.n_layers * w.batch * w.n_heads * C.KV_DIM * (2 + 4)
+
+
+def score_bytes(w):
+    return w.batch * w.n_chunks * (C.INDEXER_DIM * 2 + 4)
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args, dist, rank, world, local):
+    import torch
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    w = C.get(args.config)
+    ds, spec, fm_q_all, q_all = setup(w, device)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def do_step(t):
+        ds.step(spec, stream, fm_q=fm_q_all[(t % w.steps) // w.lookahead],
+                q=q_all[t % q_all.shape[0]])
+
+    for t in range(args.warmup):
+        do_step(t)
+    torch.cuda.synchronize()
+    assert ds.check_error() == 0, "device error during warm-up"
+    ds.reset_stats()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    counts = []
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with ClockSampler(local) as clk:
+        for i in range(K):
+            t = args.warmup + i
+            flush.zero_()
+            e0, e1, e2, e3 = ev[i]
+            e0.record(stream)
+            ds.score(spec, stream, fm_q_all[(t % w.steps) // w.lookahead])
+            e1.record(stream)
+            ds.select(spec, stream)
+            ds.stage(-1, stream)
+            e2.record(stream)
+            ds.attend(-1, stream, q_all[t % q_all.shape[0]])
+            e3.record(stream)
+            e3.synchronize()
+            counts.append(ds.count_l.cpu().numpy().copy())
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    assert ds.check_error() == 0, "device error during the timed steps"
+    step_ms = [ev[i][0].elapsed_time(ev[i][3]) for i in range(K)]
+    score_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    attn_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
+    local_s = sum(step_ms) / 1e3
+    tot_s, tot_steps = aggregate(dist, local_s, K, device)
+    st = ds.stats()
+
+    result = None
+    if rank == 0:
+        peak, peak_kind = measured_peaks()
+        a_bytes = [attn_bytes(w, c) for c in counts]
+        a_avg_ms = statistics.mean(attn_ms)
+        achieved = statistics.mean(a_bytes) / (a_avg_ms / 1e3) / 1e9
+        sel_total = st["hits"] + st["misses"]
+        step_bytes = statistics.mean(a_bytes) + score_bytes(w)
+        traffic = traffic_record("attend")
+        result = {
+            "metric": METRIC,
+            "value": tot_steps / tot_s,
+            "unit": "steps/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": args.warmup,
+            "ms_per_step": statistics.mean(step_ms),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "precision": "bf16 keys/queries, f32 latents; tf32 attention MMA operands, f32 accumulate",
+            "data": "synthetic (seeded PCG64; shapes of the pages' workloads)",
+            "config": {
+                "workload": w.name, "context_len": w.context_len,
+                "layers": f"{sum(1 for r in w.layer_ratios if r == 4)}x ratio-4 + "
+                          f"{sum(1 for r in w.layer_ratios if r == 128)}x ratio-128",
+                "n_chunks": w.n_chunks, "gpu_chunks": w.gpu_chunks, "index_topk": w.index_topk,
+                "select": "topk" if w.select_mode == C.SELECT_TOPK else f"threshold tau={w.tau}",
+                "ensemble": "max" if w.ensemble == C.ENSEMBLE_MAX else "mean",
+                "heads": w.n_heads, "batch": w.batch, "lookahead": w.lookahead,
+                "l2": "flushed before every timed step (256 MiB write, outside the timed span)",
+                "parallelism": f"replicas x{world}",
+            },
+            "gpu_launches": KERNELS_PER_STEP * K,
+            "roofline": {
+                "kernel": "attend_kernel (lsa_attend)",
+                "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_kind": peak_kind,
+                "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
+                "algorithmic_bytes_per_launch": statistics.mean(a_bytes),
+                "avg_launch_us": a_avg_ms * 1e3,
+            },
+            "kernels_us": {"fm_score": statistics.mean(score_ms) * 1e3,
+                           "fm_select+kvswap_stage": statistics.mean(
+                               [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]) * 1e3,
+                           "lsa_attend": a_avg_ms * 1e3},
+            "score_gbs": score_bytes(w) / (statistics.mean(score_ms) / 1e3) / 1e9,
+            "step_hbm_gbs": step_bytes / (statistics.mean(step_ms) / 1e3) / 1e9,
+            "lru_hit_rate": (st["hits"] / sel_total) if sel_total else None,
+            "staged_bytes_per_step": st["h2d_bytes"] / K,
+            "selected_per_step": st["selected"] / K,
+            "wall_s": wall,
+        }
+        clk_sum = clk.summary()
+        result["clocks"] = clk_sum
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, ds, spec, device)
+        if result is not None:
+            result["e2e"] = e2e
+    ds.close()
+    return result
+
+
+def run_e2e(args, w, ds, spec, device):
+    """Same steps through the public API with host buffers: every step copies its
+    queries H2D from pinned memory and reads the attention output and the
+    selection back D2H, inside the timed region."""
+    import torch
+    from sparse_retrieval_host_gb300.runtime import bits_to_i16
+    stream = torch.cuda.current_stream()
+    nq = min(Q_CYCLE, w.steps)
+    h_fmq = [bits_to_i16(np.stack([G.fm_queries(w, t, b) for b in range(w.batch)])).pin_memory()
+             for t in range(0, w.steps, w.lookahead)]
+    h_q = [bits_to_i16(np.stack([np.stack([G.attn_q(w, t, l, b) for b in range(w.batch)])
+                                 for l in range(w.n_layers)])).pin_memory() for t in range(nq)]
+    h_out = torch.empty(ds.out.shape, dtype=torch.float32).pin_memory()
+    h_sel = torch.empty(ds.sel.shape, dtype=torch.int32).pin_memory()
+    h_cnt = torch.empty(ds.count.shape, dtype=torch.int32).pin_memory()
+    K = max(3, args.steps // 2)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(K):
+        t = args.warmup + args.steps + i
+        ds.fm_q.copy_(h_fmq[(t % w.steps) // w.lookahead], non_blocking=True)
+        ds.q.copy_(h_q[t % nq], non_blocking=True)
+        ds.step(spec, stream)
+        h_out.copy_(ds.out, non_blocking=True)
+        h_sel.copy_(ds.sel, non_blocking=True)
+        h_cnt.copy_(ds.count, non_blocking=True)
+        stream.synchronize()
+    end.record(stream)
+    end.synchronize()
+    ms = start.elapsed_time(end) / K
+    h2d = ds.fm_q.numel() * 2 + ds.q.numel() * 2
+    d2h = ds.out.numel() * 4 + ds.sel.numel() * 4 + ds.count.numel() * 4
+    return {"value": 1e3 / ms, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms, "steps": K}
+
+
+# --------------------------------------------------------------------------- the oracle
+def oracle_sample(w, n_steps):
+    """Time the fp64 oracle on the first ``n_steps`` steps of workload ``w``."""
+    from oracle import srh_oracle as O
+    ora = O.DecodeOracle(context_len=w.context_len, layer_ratios=w.layer_ratios,
+                         gpu_chunks=w.gpu_chunks, index_topk=w.index_topk, batch=w.batch,
+                         scale=w.scale, bias=[w.bias] * 3, ensemble_mode=w.ensemble,
+                         select_mode=w.select_mode, tau=w.tau, clamp=w.clamp)
+    ora.mark_all_stored()
+    keys = [G.keys(w, b) for b in range(w.batch)]
+    small = w.n_chunks <= 8192
+    pools = {(l, b): G.pool(w, l, b) for l in range(w.n_layers) for b in range(w.batch)} if small else None
+    wins = {(l, b): G.window(w, l, b) for l in range(w.n_layers) for b in range(w.batch)}
+    fmq = {t: [G.fm_queries(w, t, b) for b in range(w.batch)] for t in range(n_steps)}
+    qs = {t: {(l, b): G.attn_q(w, t, l, b) for l in range(w.n_layers) for b in range(w.batch)}
+          for t in range(n_steps)}
+    rows = (lambda l, b, idx: pools[(l, b)][np.asarray(idx, dtype=np.int64)]) if small else \
+        (lambda l, b, idx: G.pool_rows(w, l, b, idx))
+    t0 = time.perf_counter()
+    for t in range(n_steps):
+        ora.step(lambda b: keys[b], lambda b: fmq[t][b], lambda l, b: qs[t][(l, b)],
+                 lambda l, b: wins[(l, b)], rows)
+    return time.perf_counter() - t0
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        n = max((i.get("num_threads", 1) for i in info), default=1)
+        return int(n)
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, sample_steps=0):
+    n = sample_steps or {"tiny": 256, "ctx8k": 128}.get(w.name, 8)
+    secs = oracle_sample(w, n)
+    return {"value": n / secs, "unit": "steps/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"first {n} decode steps of {w.name} (fp64 numpy oracle, host cores; "
+                      f"input generation excluded)", "seconds": secs}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return None
+    w = C.get(args.config)
+    n = max(1, min(args.steps, args.cpu_sample_steps or {"tiny": 1000, "ctx8k": 200}.get(w.name, 8)))
+    # warm-up: one step, untimed
+    if args.warmup > 0:
+        oracle_sample(w, 1)
+    secs = oracle_sample(w, n)
+    v = n / secs
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": 1,
+            "steps": n, "warmup": args.warmup, "ms_per_step": secs / n * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name},
+            "cpu_baseline": {"value": v, "unit": "steps/s", "cores": blas_threads(), "kind": "oracle",
+                             "sample": f"{n} decode steps of {w.name} per timed run"},
+            "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    dist, rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        res = run_reference(args, rank)
+    else:
+        res = run_ours(args, dist, rank, world, local)
+        if rank == 0 and res is not None and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(C.get(args.config), args.cpu_sample_steps)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,273 @@
+/*
+ * srh.h -- C ABI of the FlashMemory lookahead-sparse-attention + KV_SWAP
+ * decode-step hot path, for one NVIDIA GB300 (sm_103a).
+ *
+ * One decode step is four calls, in this order:
+ *
+ *   fm_score      score every compressed chunk with 3 memory-indexer query
+ *                 sets against the frozen bf16 indexer keys and ensemble the
+ *                 three per-indexer logits (max = OR-mode, or mean);
+ *   fm_select     pick chunks by top-k or by sigmoid threshold, ordered by
+ *                 (score descending, chunk index ascending);
+ *   kvswap_stage  per sparse layer, map the global selection to the layer's
+ *                 chunks, resolve them against the GPU staging slots with the
+ *                 LRU of the Swap-in flow, and gather the misses from the
+ *                 pinned host pool;
+ *   lsa_attend    per sparse layer, attention of every head over the
+ *                 128-row window plus the staged selected chunks.
+ *
+ * Sources (the pages this interface restates):
+ *   [P1] PocketLLM, "FlashMemory 1M 上下文显存优化使用文档": sections
+ *        "配置说明" (flags), "关键参数调优" (GPU_CHUNKS rule, pinned-size
+ *        formula), "故障排查" (the four errors and swap auto-disable),
+ *        "技术细节 / 架构概览" (scoring box and per-layer attention box,
+ *        memory layout), "KV_SWAP 实现细节" (GgufKvSwapLayerState, Swap-in
+ *        and Store flows).
+ *   [P2] FlashMemory-DeepSeek-V4 summary (wmrh.cn/news/1094): sections
+ *        "LSA 让模型预判 KV chunk" (cold pool, indexer queries vs compressed
+ *        indexer keys, sigmoid threshold recall), "Memory Indexer 放哪里"
+ *        (3 indexers, OR-mode routing).
+ *
+ * Conventions
+ *   - "d_" pointers are device memory owned by the caller; "h_" pointers
+ *     are host memory. bf16 tensors are passed as their uint16_t bit
+ *     patterns. All device arrays are dense, row-major, with the shapes
+ *     given at each call.
+ *   - Streams are cudaStream_t values passed as srh_stream_t (void*); NULL
+ *     means the legacy default stream.
+ *   - Every call returns SRH_OK (0) or a negative SRH_ERR_* code, and
+ *     validates its arguments before it launches anything. Kernel work is
+ *     asynchronous: errors found on the device (a selected chunk not yet
+ *     stored, an index out of range) are recorded in a sticky device error
+ *     word and reported by srh_check_error(). No kernel traps or waits
+ *     without bound.
+ *   - Nothing is allocated in the per-step calls: srh_create() allocates
+ *     the pinned host pools, the device slot tables and all scratch.
+ *   - A context is not thread-safe; calls on one context must be issued
+ *     from one host thread. Streams passed to consecutive calls of one
+ *     step must be ordered by the caller (the usual case is one stream).
+ */
+#ifndef SRH_H
+#define SRH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SRH_KV_DIM 512        /* latent row width, fp32 ([P1] 关键参数调优: kv_dim = 512) */
+#define SRH_WINDOW 128        /* sliding-window rows ([P1] 概述, item 3) */
+#define SRH_N_INDEXERS 3      /* memory indexers (layers 10/12/20) ([P2] Memory Indexer 放哪里) */
+#define SRH_INDEXER_HEADS 8   /* query heads per indexer */
+#define SRH_INDEXER_DIM 128   /* indexer key width, bf16 */
+#define SRH_MAX_HEADS 64      /* largest attention head count lsa_attend accepts */
+
+/* Return codes. */
+#define SRH_OK 0
+#define SRH_ERR_INVALID -1     /* bad argument or shape; GPU_CHUNKS < index_topk without
+                                  allow_topk_reduction ([P1] 故障排查, error 2) */
+#define SRH_ERR_PINNED_CAP -2  /* pinned pools would exceed pinned_cap_bytes ([P1] 故障排查,
+                                  error 3; srh_last_error() gives required_mib / cap_mib) */
+#define SRH_ERR_NOT_STORED -3  /* a selected chunk was never stored to the host pool
+                                  ([P1] 故障排查, error 4); reported by srh_check_error() */
+#define SRH_ERR_CUDA -4        /* a CUDA runtime call failed */
+#define SRH_ERR_TIMEOUT -5     /* a bounded device-side wait gave up */
+#define SRH_ERR_NOMEM -6       /* host or device allocation failed */
+#define SRH_ERR_BOUNDS -7      /* a device kernel met an index outside its buffer (the
+                                  access was skipped); reported by srh_check_error() */
+
+#define SRH_ENSEMBLE_MAX 0     /* s = max_i s_i: OR-mode ([P1] 配置说明 ENSEMBLE=max; [P2]) */
+#define SRH_ENSEMBLE_MEAN 1    /* s = (s_0 + s_1 + s_2) / 3 */
+
+#define SRH_SELECT_TOPK 0      /* top-k by (score desc, index asc) ([P1] 架构概览 step 3) */
+#define SRH_SELECT_THRESH 1    /* sigmoid(s) > tau, taken as s > ln(tau/(1-tau)) ([P2] LSA) */
+
+/* srh_config.flags */
+#define SRH_FLAG_TEST_FAIL_HOST_ALLOC 1u  /* testing only: make the pinned allocation fail */
+
+typedef void* srh_stream_t;
+typedef struct srh_ctx srh_ctx;
+
+/*
+ * Static shape of one decode loop ([P1] 配置说明 and 关键参数调优).
+ *   batch            B, independent sequences
+ *   n_layers         L, sparse layers
+ *   kv_dim           must be SRH_KV_DIM
+ *   window           must be SRH_WINDOW
+ *   gpu_chunks       G, staging slots per (layer, sequence) (KV_SWAP_GPU_CHUNKS)
+ *   index_topk       k, the top-k size (512 on the pages)
+ *   src_ratio        compression ratio of the scored chunks (4)
+ *   layer_ratio      [n_layers] host array, each a multiple of src_ratio;
+ *                    copied by srh_create
+ *   context_len      tokens; a layer of ratio r holds cap = ceil(context_len / r)
+ *                    chunks ([P1] 关键参数调优, layer_compressed_cap)
+ *   pinned_cap_bytes upper bound of the pinned host pools (KV_SWAP_PINNED_MIB
+ *                    in bytes); 0 = no bound
+ *   allow_topk_reduction  accept gpu_chunks < index_topk
+ *                    (KV_SWAP_TEST_ALLOW_TOPK_REDUCTION, tests only)
+ *   max_select       S, the row stride of every selection-shaped array
+ *                    ([B][S] and [L][B][S]); 0 means max(index_topk, gpu_chunks).
+ *                    Must be >= index_topk and <= 4096.
+ *   flags            SRH_FLAG_* bits; 0 normally
+ */
+typedef struct {
+    int batch;
+    int n_layers;
+    int kv_dim;
+    int window;
+    int gpu_chunks;
+    int index_topk;
+    int src_ratio;
+    const int* layer_ratio;
+    long long context_len;
+    size_t pinned_cap_bytes;
+    int allow_topk_reduction;
+    int max_select;
+    unsigned flags;
+} srh_config;
+
+/* Swap counters, summed over swapped layers and sequences since creation or the
+ * last srh_reset_stats() ([P1] 使用示例: gguf_kv_swap_stats hits/misses/h2d_mib/d2h_mib). */
+typedef struct {
+    unsigned long long hits;                 /* selected chunks found in a staging slot */
+    unsigned long long misses;               /* selected chunks gathered from the host pool */
+    unsigned long long h2d_bytes;            /* misses * kv_dim * 4 */
+    unsigned long long d2h_bytes;            /* bytes written to the host pool by the store path */
+    unsigned long long resident_fill_bytes;  /* one-time fills of swap-disabled layers */
+    unsigned long long stage_calls;          /* kvswap_stage calls */
+    unsigned long long selected;             /* chunks resolved, all layers and sequences */
+    int swapped_layers;                      /* layers with cap > gpu_chunks */
+    int n_layers;
+} srh_stats;
+
+/*
+ * Create a context: validates the config (GPU_CHUNKS >= index_topk unless
+ * allow_topk_reduction, [P1] 故障排查 error 2; required pinned bytes <=
+ * pinned_cap_bytes, error 3), allocates one mapped pinned pool per layer of
+ * [batch][cap][kv_dim] fp32 (the host "full compressed cache", [P1] Memory
+ * Layout), the device slot tables (all slots free), and the scratch of every
+ * kernel. The pools start zeroed and unstored. Uses the current CUDA device.
+ * On success *out owns everything; release it with srh_destroy().
+ * Errors: SRH_ERR_INVALID, SRH_ERR_PINNED_CAP, SRH_ERR_NOMEM, SRH_ERR_CUDA.
+ */
+int srh_create(const srh_config* cfg, srh_ctx** out);
+
+/* Free everything the context owns. Waits for the device first. NULL is a no-op. */
+void srh_destroy(srh_ctx* ctx);
+
+/* Bytes of pinned host memory a config needs: sum over layers of
+ * batch * ceil(context_len / ratio) * kv_dim * 4 ([P1] 关键参数调优, item 2). */
+int srh_pinned_required_bytes(const srh_config* cfg, unsigned long long* out);
+
+/* Host pointer to the pinned pool of (layer, seq): [cap][kv_dim] fp32, owned by
+ * the context, valid until srh_destroy(). The caller writes chunks here and then
+ * calls srh_mark_stored(). NULL on a bad argument. */
+float* srh_pool_host_ptr(srh_ctx* ctx, int layer, int seq);
+
+/* Store flow ([P1] KV_SWAP 实现细节, Store): mark chunks [c0, c0+n) of (layer, seq)
+ * as present in the host pool (host_ready = 1). Synchronous. Swap-disabled
+ * layers re-copy those chunks into their staging rows on the next kvswap_stage. */
+int srh_mark_stored(srh_ctx* ctx, int layer, int seq, long long c0, long long n);
+
+/* Layer facts: chunk capacity and whether the layer swaps (cap > gpu_chunks,
+ * [P1] 故障排查, the swap auto-disable note). */
+int srh_layer_info(srh_ctx* ctx, int layer, long long* cap, int* swap_enabled);
+
+/* Row stride S of selection-shaped arrays. */
+int srh_max_select(srh_ctx* ctx);
+
+/*
+ * a1+a2: indexer scoring + ensemble ([P1] 架构概览, scoring box steps 1-3; [P2] LSA,
+ * Memory Indexer 放哪里).
+ *   d_keys   [batch][n][128] bf16, the frozen compressed indexer keys of one
+ *            shared source layer (n <= the ratio-src_ratio capacity)
+ *   d_q      [batch][3][8][128] bf16, the memory-indexer query sets
+ *   scale    logit scale applied to the per-indexer max over heads
+ *   bias3    host [3], per-indexer logit bias b_i
+ *   ensemble SRH_ENSEMBLE_MAX or SRH_ENSEMBLE_MEAN
+ *   d_scores [batch][n] fp32 output: s(c), where
+ *            s_i(c) = scale * max_h <Q[i,h], K[c]> + b_i and s = max_i or mean_i.
+ * Also fills a per-sequence score histogram inside the context that fm_select
+ * uses when it is called on the same d_scores.
+ */
+int fm_score(srh_ctx* ctx, const uint16_t* d_keys, int n, const uint16_t* d_q, float scale,
+             const float* bias3, int ensemble, float* d_scores, srh_stream_t stream);
+
+/*
+ * a3: selection ([P1] 架构概览 step 3: global top-k; [P2] LSA: sigmoid threshold).
+ *   d_scores [batch][n] fp32
+ *   mode     SRH_SELECT_TOPK: the min(k, n) best chunks;
+ *            SRH_SELECT_THRESH: chunks with s > ln(tau/(1-tau)), at most clamp
+ *            of them (the best ones) -- clamp must be <= gpu_chunks;
+ *   d_sel    [batch][S] int32 output: chunk ids in (score desc, index asc) order;
+ *            entries past the count are left unspecified
+ *   d_count  [batch] int32 output: how many ids each sequence selected
+ * Requires k <= S (TOPK) and clamp <= S.
+ */
+int fm_select(srh_ctx* ctx, const float* d_scores, int n, int mode, int k, float tau, int clamp,
+              int32_t* d_sel, int32_t* d_count, srh_stream_t stream);
+
+/*
+ * a4+a5: KV_SWAP staging ([P1] KV_SWAP 实现细节, Swap-in flow).
+ *   layer      one sparse layer, or -1 for all layers
+ *   d_sel, d_count  the fm_select outputs ([batch][S], [batch])
+ *   d_staging  [L][batch][G][kv_dim] fp32: the GPU staging slots. This buffer is
+ *              part of the cache state: pass the same buffer to every call on a
+ *              context (a different one is rejected with SRH_ERR_INVALID).
+ *              Swap-disabled layers keep their chunk c in row c.
+ *   d_phys     [L][batch][S] int32 output: physical row of each selected chunk of
+ *              the layer, window + slot (window + c when the layer does not swap)
+ *   d_count_l  [L][batch] int32 output: chunks of the layer's list. A layer of
+ *              ratio r uses the list c -> floor(c * src_ratio / r), first
+ *              occurrence kept, in selection order.
+ *   main       stream of the LRU resolve; side: stream of the miss gathers (may
+ *              equal main). On return, work queued later on main sees the
+ *              staged rows.
+ * The LRU is the sequential list of the Swap-in flow: the selected ids are
+ * taken in order; a hit moves its slot to the front, a miss pops the back slot
+ * (all slots start free, slot 0 first) and copies h_compressed_kv[c] into it.
+ */
+int kvswap_stage(srh_ctx* ctx, int layer, const int32_t* d_sel, const int32_t* d_count,
+                 float* d_staging, int32_t* d_phys, int32_t* d_count_l, srh_stream_t main,
+                 srh_stream_t side);
+
+/*
+ * a6: sparse attention ([P1] 架构概览, per-layer box step 3; Memory Layout).
+ *   layer      one sparse layer, or -1 for all layers
+ *   d_q        [L][batch][n_heads][kv_dim] bf16 queries
+ *   n_heads    16, 32 or 64
+ *   d_window   [L][batch][128][kv_dim] fp32 window rows
+ *   d_staging, d_phys, d_count_l  as written by kvswap_stage
+ *   d_out      [L][batch][n_heads][kv_dim] fp32 output:
+ *              o_h = sum_j softmax_j(<q_h, e_j> / sqrt(kv_dim)) e_j over the 128
+ *              window rows and the layer's staged rows (K = V = the latent row).
+ */
+int lsa_attend(srh_ctx* ctx, int layer, const uint16_t* d_q, int n_heads, const float* d_window,
+               const float* d_staging, const int32_t* d_phys, const int32_t* d_count_l,
+               float* d_out, srh_stream_t stream);
+
+/* Copy the swap counters out (waits for the device). */
+int srh_get_stats(srh_ctx* ctx, srh_stats* out);
+
+/* Zero the swap counters (waits for the device). */
+int srh_reset_stats(srh_ctx* ctx);
+
+/* Wait for the device and report the sticky device error word: SRH_OK,
+ * SRH_ERR_NOT_STORED or SRH_ERR_BOUNDS (first match in that order), or
+ * SRH_ERR_CUDA. The word is cleared after it is read. */
+int srh_check_error(srh_ctx* ctx);
+
+/* Static text for a return code. */
+const char* srh_error_string(int code);
+
+/* Detail of the last failing call on the context (or of the last failing
+ * srh_create when ctx is NULL), e.g. "required_mib=84 cap_mib=64". */
+const char* srh_last_error(srh_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SRH_H */

@@ -35,6 +35,8 @@ its reason in the design notes):
   * a layer of ratio r reuses the global selection through
     c -> floor(c*src_ratio/r), first occurrence kept;
   * the LRU list starts with every slot free, slot 0 at the back;
+  * with GPU_CHUNKS below the selected count (allowed only by the test flag),
+    a swapped layer keeps the first GPU_CHUNKS chunks of its list;
   * attention is MQA over the 512-wide latent (K = V = row), scale 1/sqrt(512).
 
 Parity pins (checks that do not reuse this code) live in ``tests/test_oracle_*.py``.
@@ -313,6 +315,10 @@ class DecodeOracle:
             row_l, row_s = [], []
             for b in range(self.batch):
                 lst = layer_chunks(sels[b], self.src_ratio, ratio)
+                if self.states[l][b].swap_enabled and len(lst) > self.gpu_chunks:
+                    # GPU_CHUNKS < index_topk (a test-only setting): the layer keeps
+                    # the first GPU_CHUNKS chunks of its list
+                    lst = lst[:self.gpu_chunks]
                 row_l.append(lst)
                 row_s.append(self.states[l][b].swap_in_selected(lst))
             lists.append(row_l)

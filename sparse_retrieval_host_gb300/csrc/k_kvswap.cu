@@ -1,0 +1,397 @@
+// K-lru + K-gather: the KV_SWAP Swap-in flow on the device.
+//
+// PocketLLM "FlashMemory 1M 上下文显存优化使用文档", section "KV_SWAP 实现细节":
+// GgufKvSwapLayerState keeps, per sparse layer, the GPU slot of each logical
+// chunk, the chunk of each slot and an LRU list of slots (front = most recently
+// used). gguf_kv_swap_in_selected walks the selected logical ids in order: a hit
+// moves its slot to the front; a miss pops the back slot, copies
+// h_compressed_kv[logical] into it (H2D) and the slot becomes the front; the
+// indices are then rewritten to physical = window + slot for the attention.
+//
+// Here that state lives in device memory and one CTA resolves one
+// (layer, sequence) with no host round trip:
+//   * slot_of[c]        chunk -> slot (-1 if absent), a direct map over the cap;
+//   * slot_logical[s]   slot -> chunk (-1 if free);
+//   * lru_order[q]      slots from least (q = 0) to most recently used.
+// The walk is sequential on the pages, so a miss may pop the slot of a chunk
+// that is selected later in the same list. The kernel first assumes that never
+// happens (hits are the resident chunks; the i-th miss takes the i-th non-hit
+// slot in LRU order), checks that assumption exactly in parallel, and replays
+// the list one id at a time in shared memory only when it fails. Both paths
+// produce the state and outputs of the sequential list.
+//
+// The miss gather reads the mapped pinned pool directly (zero-copy over the
+// host link), one warp per 2 KiB chunk, 16-byte loads.
+#include <climits>
+
+#include "srh_internal.cuh"
+
+namespace srh {
+namespace {
+
+constexpr int kLruThreads = 1024;
+
+__device__ int block_scan_incl(int v, int* warp_buf) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+    }
+    if (lane == 31) warp_buf[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < nwarps ? warp_buf[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += u;
+        }
+        warp_buf[lane] = w;
+    }
+    __syncthreads();
+    const int r = v + (warp > 0 ? warp_buf[warp - 1] : 0);
+    __syncthreads();
+    return r;
+}
+
+// In-place exclusive scan of a[0..len) in shared memory; returns the total.
+__device__ int block_scan_excl_array(int* a, int len, int* warp_buf, int* total_buf) {
+    const int per = (len + blockDim.x - 1) / blockDim.x;
+    const int beg = threadIdx.x * per;
+    const int end = min(beg + per, len);
+    int local = 0;
+    for (int i = beg; i < end; ++i) local += a[i];
+    const int incl = block_scan_incl(local, warp_buf);
+    int run = incl - local;
+    for (int i = beg; i < end; ++i) {
+        const int v = a[i];
+        a[i] = run;
+        run += v;
+    }
+    if (threadIdx.x == blockDim.x - 1) *total_buf = incl;
+    __syncthreads();
+    const int total = *total_buf;
+    __syncthreads();
+    return total;
+}
+
+struct LruShared {
+    int warp_buf[32];
+    int total;
+    int m;
+    int nmiss;
+    int conflict;
+};
+
+__global__ void __launch_bounds__(kLruThreads)
+lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int src_ratio,
+           const int32_t* __restrict__ sel, const int32_t* __restrict__ count,
+           int32_t* __restrict__ phys, int32_t* __restrict__ count_l, int2* __restrict__ miss,
+           int* __restrict__ miss_count, unsigned long long* __restrict__ stats,
+           uint32_t* __restrict__ err) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    LruShared& sh = *reinterpret_cast<LruShared*>(smem_raw);
+    int* r = reinterpret_cast<int*>(smem_raw + sizeof(LruShared));  // [S] layer list
+    int* init_slot = r + S;      // [S]
+    int* assign = init_slot + S; // [S]
+    int* mr = assign + S;        // [S] miss rank / keep flags
+    int* tk = mr + S;            // [S] position of the k-th miss
+    int* is_miss = tk + S;       // [S]
+    int* queue = is_miss + S;    // [G] lru order
+    int* qpos = queue + G;       // [G]
+    int* hit_time = qpos + G;    // [G]
+    int* nh = hit_time + G;      // [G]
+    int* victim = nh + G;        // [G]
+    int* flag = victim + G;      // [G]
+
+    const int tid = threadIdx.x;
+    const int l = l0 + blockIdx.x / B;
+    const int b = blockIdx.x % B;
+    const LayerDev ld = layers[l];
+    const long long cap = ld.cap;
+    const size_t lb = (size_t)l * B + b;
+
+    // ---- 1. the layer's ordered chunk list: c -> floor(c * src_ratio / ratio), first kept
+    int m0 = count[b];
+    if (m0 < 0 || m0 > S) {
+        if (tid == 0) atomicOr(err, kErrBounds);
+        m0 = m0 < 0 ? 0 : S;
+    }
+    const int32_t* sel_b = sel + (size_t)b * S;
+    for (int p = tid; p < m0; p += blockDim.x) {
+        long long c = sel_b[p];
+        long long v = (c * src_ratio) / ld.ratio;
+        if (c < 0 || v >= cap) {
+            // out-of-range id: flagged, then clamped so every access stays in bounds
+            atomicOr(err, kErrBounds);
+            v = 0;
+        }
+        r[p] = (int)v;
+    }
+    __syncthreads();
+    int m;
+    if (ld.ratio == src_ratio) {
+        m = m0;
+    } else {
+        for (int p = tid; p < m0; p += blockDim.x) {
+            const int v = r[p];
+            int keep = 1;
+            for (int q = 0; q < p; ++q)
+                if (r[q] == v) {
+                    keep = 0;
+                    break;
+                }
+            mr[p] = keep;
+        }
+        __syncthreads();
+        // stable compaction (read all, scan, then write)
+        for (int p = tid; p < m0; p += blockDim.x) tk[p] = mr[p];
+        __syncthreads();
+        m = block_scan_excl_array(mr, m0, sh.warp_buf, &sh.total);
+        for (int p = tid; p < m0; p += blockDim.x) is_miss[p] = r[p];
+        __syncthreads();
+        for (int p = tid; p < m0; p += blockDim.x)
+            if (tk[p]) r[mr[p]] = is_miss[p];
+        __syncthreads();
+    }
+
+    int32_t* phys_lb = phys + lb * S;
+    if (!ld.swap) {
+        // swap disabled: every chunk is resident at its own row
+        for (int p = tid; p < m; p += blockDim.x) {
+            const int c = r[p];
+            if (!ld.host_ready[(size_t)b * cap + c]) atomicOr(err, kErrNotStored);
+            phys_lb[p] = kWindow + c;
+        }
+        if (tid == 0) {
+            count_l[lb] = m;
+            miss_count[lb] = 0;
+            atomicAdd(&stats[kStatSelected], (unsigned long long)m);
+        }
+        return;
+    }
+
+    // a swapped layer stages at most G chunks per step (only reachable with
+    // allow_topk_reduction): it keeps the first G of its list
+    if (m > G) m = G;
+
+    int* slot_of = ld.slot_of + (size_t)b * cap;
+    int* slot_logical = ld.slot_logical + (size_t)b * G;
+    int* lru = ld.lru_order + (size_t)b * G;
+
+    // ---- 2. resident lookups and the LRU queue
+    for (int p = tid; p < m; p += blockDim.x) {
+        const int c = r[p];
+        int s = slot_of[c];
+        if (s >= G) {
+            atomicOr(err, kErrBounds);
+            s = -1;
+        }
+        init_slot[p] = s;
+    }
+    for (int q = tid; q < G; q += blockDim.x) {
+        int s = lru[q];
+        if (s < 0 || s >= G) {
+            atomicOr(err, kErrBounds);
+            s = q;
+        }
+        queue[q] = s;
+        hit_time[q] = INT_MAX;
+    }
+    __syncthreads();
+    for (int q = tid; q < G; q += blockDim.x) qpos[queue[q]] = q;
+    for (int p = tid; p < m; p += blockDim.x)
+        if (init_slot[p] >= 0) hit_time[init_slot[p]] = p;
+    if (tid == 0) sh.conflict = 0;
+    __syncthreads();
+
+    // ---- 3. optimistic two-phase assignment
+    for (int q = tid; q < G; q += blockDim.x) nh[q] = hit_time[queue[q]] == INT_MAX ? 1 : 0;
+    for (int p = tid; p < m; p += blockDim.x) {
+        is_miss[p] = init_slot[p] < 0 ? 1 : 0;
+        mr[p] = is_miss[p];
+    }
+    __syncthreads();
+    block_scan_excl_array(nh, G, sh.warp_buf, &sh.total);
+    const int nmiss0 = block_scan_excl_array(mr, m, sh.warp_buf, &sh.total);
+    for (int p = tid; p < m; p += blockDim.x)
+        if (is_miss[p]) tk[mr[p]] = p;
+    for (int q = tid; q < G; q += blockDim.x)
+        if (hit_time[queue[q]] == INT_MAX) victim[nh[q]] = queue[q];
+    __syncthreads();
+    // a hit slot j lying before the kj-th non-hit slot is reached by that pop if
+    // the pop happens before j is touched: the sequential list would take j
+    for (int p = tid; p < m; p += blockDim.x) {
+        const int j = init_slot[p];
+        if (j >= 0) {
+            const int kj = nh[qpos[j]];
+            if (kj < nmiss0 && tk[kj] < p) sh.conflict = 1;
+        }
+    }
+    __syncthreads();
+    if (!sh.conflict) {
+        for (int p = tid; p < m; p += blockDim.x)
+            assign[p] = init_slot[p] >= 0 ? init_slot[p] : victim[mr[p]];
+        if (tid == 0) sh.nmiss = nmiss0;
+        __syncthreads();
+    } else {
+        // replay the list one id at a time (flag: 0 untouched, 1 hit, 2 refilled)
+        for (int q = tid; q < G; q += blockDim.x) flag[q] = 0;
+        __syncthreads();
+        if (tid == 0) {
+            int ptr = 0, nm = 0;
+            for (int p = 0; p < m; ++p) {
+                const int j = init_slot[p];
+                if (j >= 0 && flag[j] != 2) {
+                    flag[j] = 1;
+                    assign[p] = j;
+                    is_miss[p] = 0;
+                } else {
+                    while (ptr < G && flag[queue[ptr]] != 0) ++ptr;
+                    const int s = ptr < G ? queue[ptr++] : 0;
+                    flag[s] = 2;
+                    assign[p] = s;
+                    is_miss[p] = 1;
+                    ++nm;
+                }
+            }
+            sh.nmiss = nm;
+        }
+        __syncthreads();
+        for (int p = tid; p < m; p += blockDim.x) mr[p] = is_miss[p];
+        __syncthreads();
+        block_scan_excl_array(mr, m, sh.warp_buf, &sh.total);
+    }
+    const int nmiss = sh.nmiss;
+
+    // ---- 4. new LRU order: untouched slots in old order, then touched ones by position
+    for (int q = tid; q < G; q += blockDim.x) flag[q] = 0;
+    __syncthreads();
+    for (int p = tid; p < m; p += blockDim.x) flag[assign[p]] = 1;
+    __syncthreads();
+    for (int q = tid; q < G; q += blockDim.x) nh[q] = flag[queue[q]] ? 0 : 1;
+    __syncthreads();
+    block_scan_excl_array(nh, G, sh.warp_buf, &sh.total);
+    for (int q = tid; q < G; q += blockDim.x)
+        if (!flag[queue[q]]) lru[nh[q]] = queue[q];
+    for (int p = tid; p < m; p += blockDim.x) lru[G - m + p] = assign[p];
+
+    // ---- 5. slot maps: clear evicted chunks first, then record the new ones
+    for (int p = tid; p < m; p += blockDim.x)
+        if (is_miss[p]) {
+            const int old = slot_logical[assign[p]];
+            if (old >= 0 && old < cap) slot_of[old] = -1;
+        }
+    __syncthreads();
+    int2* miss_lb = miss + lb * S;
+    for (int p = tid; p < m; p += blockDim.x) {
+        const int s = assign[p];
+        phys_lb[p] = kWindow + s;
+        if (is_miss[p]) {
+            const int c = r[p];
+            slot_of[c] = s;
+            slot_logical[s] = c;
+            miss_lb[mr[p]] = make_int2(c, s);
+            if (!ld.host_ready[(size_t)b * cap + c]) atomicOr(err, kErrNotStored);
+        }
+    }
+    if (tid == 0) {
+        count_l[lb] = m;
+        miss_count[lb] = nmiss;
+        atomicAdd(&stats[kStatHits], (unsigned long long)(m - nmiss));
+        atomicAdd(&stats[kStatMisses], (unsigned long long)nmiss);
+        atomicAdd(&stats[kStatSelected], (unsigned long long)m);
+    }
+}
+
+constexpr int kGatherWarps = 8;
+
+__device__ __forceinline__ void copy_row(float* __restrict__ dst, const float* __restrict__ src, int lane) {
+    const float4* s = reinterpret_cast<const float4*>(src);
+    float4* d = reinterpret_cast<float4*>(dst);
+    float4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = s[k * 32 + lane];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) d[k * 32 + lane] = v[k];
+}
+
+__global__ void __launch_bounds__(kGatherWarps * 32)
+gather_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S,
+              const int2* __restrict__ miss, const int* __restrict__ miss_count,
+              float* __restrict__ staging, uint32_t* __restrict__ err) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t lb = (size_t)l0 * B + blockIdx.y;
+    const int l = (int)(lb / B), b = (int)(lb % B);
+    const int nm = miss_count[lb];
+    const LayerDev ld = layers[l];
+    const int2* ml = miss + lb * S;
+    for (int i = blockIdx.x * kGatherWarps + warp; i < nm; i += gridDim.x * kGatherWarps) {
+        const int2 e = ml[i];
+        if (e.x < 0 || e.x >= ld.cap || e.y < 0 || e.y >= G) {
+            if (lane == 0) atomicOr(err, kErrBounds);
+            continue;
+        }
+        copy_row(staging + (((size_t)l * B + b) * G + e.y) * kKvDim,
+                 ld.pool + ((size_t)b * ld.cap + e.x) * kKvDim, lane);
+    }
+}
+
+__global__ void __launch_bounds__(kGatherWarps * 32)
+resident_fill_kernel(const float* __restrict__ pool, const uint8_t* __restrict__ ready,
+                     long long cap, int layer, int B, int G, float* __restrict__ staging) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.y;
+    for (long long c = (long long)blockIdx.x * kGatherWarps + warp; c < cap;
+         c += (long long)gridDim.x * kGatherWarps) {
+        if (!ready[(size_t)b * cap + c]) continue;
+        copy_row(staging + (((size_t)layer * B + b) * G + c) * kKvDim,
+                 pool + ((size_t)b * cap + c) * kKvDim, lane);
+    }
+}
+
+}  // namespace
+
+size_t lru_smem_bytes(int S, int G) {
+    return sizeof(LruShared) + sizeof(int) * (6 * (size_t)S + 6 * (size_t)G);
+}
+
+cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int S, int src_ratio,
+                       const int32_t* sel, const int32_t* count, int32_t* phys, int32_t* count_l,
+                       int2* miss, int* miss_count, unsigned long long* stats, uint32_t* err,
+                       cudaStream_t st) {
+    const size_t smem = lru_smem_bytes(S, G);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(lru_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    lru_kernel<<<nl * B, kLruThreads, smem, st>>>(layers, l0, B, G, S, src_ratio, sel, count, phys,
+                                                  count_l, miss, miss_count, stats, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, int S,
+                          const int2* miss, const int* miss_count, float* staging, uint32_t* err,
+                          int sm_count, cudaStream_t st) {
+    int bx = (4 * sm_count + nl * B - 1) / (nl * B);
+    if (bx < 1) bx = 1;
+    if (bx > 64) bx = 64;
+    gather_kernel<<<dim3(bx, nl * B), kGatherWarps * 32, 0, st>>>(layers, l0, B, G, S, miss,
+                                                                   miss_count, staging, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_resident_fill(const float* pool_dev, const uint8_t* ready, long long cap,
+                                 int layer, int B, int G, float* staging, cudaStream_t st) {
+    long long bx = (cap + kGatherWarps - 1) / kGatherWarps;
+    if (bx > 256) bx = 256;
+    if (bx < 1) bx = 1;
+    resident_fill_kernel<<<dim3((unsigned)bx, B), kGatherWarps * 32, 0, st>>>(pool_dev, ready, cap,
+                                                                              layer, B, G, staging);
+    return cudaGetLastError();
+}
+
+}  // namespace srh

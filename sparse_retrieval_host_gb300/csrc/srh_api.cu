@@ -1,0 +1,479 @@
+// Host side of the C ABI: context creation, validation, pinned pools, launches.
+//
+// Guards restated from PocketLLM "FlashMemory 1M 上下文显存优化使用文档":
+//   * section 关键参数调优 item 1 and 故障排查 error 2: GPU_CHUNKS must be >=
+//     index_topk unless the test-only reduction flag is set;
+//   * section 关键参数调优 item 2 and 故障排查 error 3: the pinned pools must fit
+//     the cap, reported as "required_mib=... cap_mib=...";
+//   * section 故障排查, the swap auto-disable note: a layer whose capacity fits in
+//     the staging slots does not swap (its chunk c lives in staging row c);
+//   * section 故障排查 error 4: a selected chunk that was never stored is an error
+//     (raised on the device, reported by srh_check_error).
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "srh_internal.cuh"
+
+using namespace srh;
+
+namespace {
+
+std::string g_create_error;
+
+const char* kErrText[] = {
+    "ok",
+    "invalid argument",
+    "pinned cache exceeds cap",
+    "selected chunk before it was stored",
+    "CUDA error",
+    "device wait timed out",
+    "out of memory",
+    "index out of bounds on the device",
+};
+
+int fail(srh_ctx* ctx, int code, const std::string& msg) {
+    if (ctx) ctx->last_error = msg;
+    else g_create_error = msg;
+    return code;
+}
+
+int cuda_fail(srh_ctx* ctx, cudaError_t e, const char* where) {
+    std::string m = std::string(where) + ": " + cudaGetErrorString(e);
+    return fail(ctx, SRH_ERR_CUDA, m);
+}
+
+#define SRH_CUDA(ctx, call)                                   \
+    do {                                                      \
+        cudaError_t e_ = (call);                              \
+        if (e_ != cudaSuccess) return cuda_fail(ctx, e_, #call); \
+    } while (0)
+
+long long cap_of(long long ctx_len, int ratio) { return (ctx_len + ratio - 1) / ratio; }
+
+int validate_config(const srh_config* c, std::string* why) {
+    if (!c) { *why = "config is NULL"; return SRH_ERR_INVALID; }
+    if (c->batch < 1) { *why = "batch must be >= 1"; return SRH_ERR_INVALID; }
+    if (c->n_layers < 1) { *why = "n_layers must be >= 1"; return SRH_ERR_INVALID; }
+    if (c->kv_dim != SRH_KV_DIM) { *why = "kv_dim must be 512"; return SRH_ERR_INVALID; }
+    if (c->window != SRH_WINDOW) { *why = "window must be 128"; return SRH_ERR_INVALID; }
+    if (c->gpu_chunks < 1 || c->gpu_chunks > kMaxGpuChunks) {
+        *why = "gpu_chunks must be in [1, 4096]"; return SRH_ERR_INVALID;
+    }
+    if (c->index_topk < 1 || c->index_topk > kMaxSelect) {
+        *why = "index_topk must be in [1, 4096]"; return SRH_ERR_INVALID;
+    }
+    if (c->gpu_chunks < c->index_topk && !c->allow_topk_reduction) {
+        *why = "POCKETLLM_GGUF_KV_SWAP_GPU_CHUNKS must be >= index_topk";
+        return SRH_ERR_INVALID;
+    }
+    if (c->src_ratio < 1) { *why = "src_ratio must be >= 1"; return SRH_ERR_INVALID; }
+    if (!c->layer_ratio) { *why = "layer_ratio is NULL"; return SRH_ERR_INVALID; }
+    if (c->context_len < 1) { *why = "context_len must be >= 1"; return SRH_ERR_INVALID; }
+    const long long n_src = cap_of(c->context_len, c->src_ratio);
+    if (n_src > (1LL << 30)) { *why = "context too long"; return SRH_ERR_INVALID; }
+    for (int l = 0; l < c->n_layers; ++l) {
+        const int r = c->layer_ratio[l];
+        if (r < c->src_ratio || r % c->src_ratio != 0) {
+            *why = "every layer ratio must be a multiple of src_ratio";
+            return SRH_ERR_INVALID;
+        }
+    }
+    const int S = c->max_select > 0 ? c->max_select : c->index_topk;
+    if (S < c->index_topk || S > kMaxSelect) {
+        *why = "max_select must be in [index_topk, 4096]"; return SRH_ERR_INVALID;
+    }
+    if (lru_smem_bytes(S, c->gpu_chunks) > 227 * 1024) {
+        *why = "max_select + gpu_chunks too large for one LRU block"; return SRH_ERR_INVALID;
+    }
+    return SRH_OK;
+}
+
+unsigned long long pinned_bytes(const srh_config* c) {
+    unsigned long long t = 0;
+    for (int l = 0; l < c->n_layers; ++l)
+        t += (unsigned long long)c->batch * cap_of(c->context_len, c->layer_ratio[l]) *
+             SRH_KV_DIM * sizeof(float);
+    return t;
+}
+
+void free_ctx(srh_ctx* ctx) {
+    if (!ctx) return;
+    cudaDeviceSynchronize();
+    for (float* p : ctx->pool_host) if (p) cudaFreeHost(p);
+    for (auto& ld : ctx->h_layers) {
+        cudaFree(ld.host_ready);
+        cudaFree(ld.slot_of);
+        cudaFree(ld.slot_logical);
+        cudaFree(ld.lru_order);
+    }
+    cudaFree(ctx->d_layers);
+    cudaFree(ctx->d_stats);
+    cudaFree(ctx->d_err);
+    cudaFree(ctx->d_hist);
+    cudaFree(ctx->d_miss);
+    cudaFree(ctx->d_miss_count);
+    cudaFree(ctx->d_items);
+    cudaFree(ctx->d_part_o);
+    cudaFree(ctx->d_part_ml);
+    cudaFree(ctx->d_attn_counter);
+    if (ctx->ev_resolved) cudaEventDestroy(ctx->ev_resolved);
+    if (ctx->ev_gathered) cudaEventDestroy(ctx->ev_gathered);
+    delete ctx;
+}
+
+// Split every (layer, sequence) row range into equal splits so the whole
+// attention launch is about one CTA per SM (it holds ~200 KB of shared memory).
+void plan_attention(srh_ctx* ctx, std::vector<AttnItem>* items) {
+    long long total = 0;
+    std::vector<int> max_rows(ctx->L);
+    for (int l = 0; l < ctx->L; ++l) {
+        max_rows[l] = kWindow + (int)std::min<long long>(ctx->S, ctx->caps[l]);
+        total += (long long)ctx->B * max_rows[l];
+    }
+    long long sr = (total + ctx->sm_count - 1) / ctx->sm_count;
+    sr = ((sr + kAttnTile - 1) / kAttnTile) * kAttnTile;
+    sr = std::max<long long>(sr, 2 * kAttnTile);
+    ctx->split_rows = (int)sr;
+    ctx->item_begin.assign(ctx->L + 1, 0);
+    for (int l = 0; l < ctx->L; ++l) {
+        ctx->item_begin[l] = (int)items->size();
+        const int ns = (max_rows[l] + ctx->split_rows - 1) / ctx->split_rows;
+        for (int b = 0; b < ctx->B; ++b)
+            for (int s = 0; s < ns; ++s) items->push_back(AttnItem{l, b, s, ns});
+    }
+    ctx->item_begin[ctx->L] = (int)items->size();
+    ctx->n_items = (int)items->size();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* srh_error_string(int code) {
+    if (code > 0 || code < -7) return "unknown error";
+    return kErrText[-code];
+}
+
+const char* srh_last_error(srh_ctx* ctx) {
+    return ctx ? ctx->last_error.c_str() : g_create_error.c_str();
+}
+
+int srh_pinned_required_bytes(const srh_config* cfg, unsigned long long* out) {
+    std::string why;
+    if (!out) return SRH_ERR_INVALID;
+    const int rc = validate_config(cfg, &why);
+    if (rc != SRH_OK) return fail(nullptr, rc, why);
+    *out = pinned_bytes(cfg);
+    return SRH_OK;
+}
+
+int srh_create(const srh_config* cfg, srh_ctx** out) {
+    if (!out) return fail(nullptr, SRH_ERR_INVALID, "out is NULL");
+    *out = nullptr;
+    std::string why;
+    int rc = validate_config(cfg, &why);
+    if (rc != SRH_OK) return fail(nullptr, rc, why);
+
+    const unsigned long long need = pinned_bytes(cfg);
+    if (cfg->pinned_cap_bytes && need > cfg->pinned_cap_bytes) {
+        char buf[160];
+        std::snprintf(buf, sizeof buf,
+                      "POCKETLLM_GGUF_KV_SWAP pinned cache exceeds cap: required_mib=%llu cap_mib=%llu",
+                      (need + (1ull << 20) - 1) >> 20,
+                      (unsigned long long)(cfg->pinned_cap_bytes >> 20));
+        return fail(nullptr, SRH_ERR_PINNED_CAP, buf);
+    }
+
+    srh_ctx* ctx = new (std::nothrow) srh_ctx();
+    if (!ctx) return fail(nullptr, SRH_ERR_NOMEM, "host allocation failed");
+    ctx->cfg = *cfg;
+    ctx->B = cfg->batch;
+    ctx->L = cfg->n_layers;
+    ctx->G = cfg->gpu_chunks;
+    ctx->S = cfg->max_select > 0 ? cfg->max_select : cfg->index_topk;
+    ctx->n_src = cap_of(cfg->context_len, cfg->src_ratio);
+    ctx->ratios.assign(cfg->layer_ratio, cfg->layer_ratio + cfg->n_layers);
+    ctx->cfg.layer_ratio = nullptr;
+
+    auto bail = [&](int code, const std::string& msg) {
+        g_create_error = msg;
+        free_ctx(ctx);
+        return code;
+    };
+    cudaError_t e = cudaGetDevice(&ctx->device);
+    if (e != cudaSuccess) return bail(SRH_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+    e = cudaDeviceGetAttribute(&ctx->sm_count, cudaDevAttrMultiProcessorCount, ctx->device);
+    if (e != cudaSuccess) return bail(SRH_ERR_CUDA, cudaGetErrorString(e));
+
+    const int B = ctx->B, G = ctx->G;
+    ctx->h_layers.resize(ctx->L);
+    ctx->pool_host.assign(ctx->L, nullptr);
+    ctx->pool_dev.assign(ctx->L, nullptr);
+    ctx->ready_host.resize(ctx->L);
+    ctx->resident_dirty.assign(ctx->L, 0);
+    for (int l = 0; l < ctx->L; ++l) {
+        const long long cap = cap_of(cfg->context_len, ctx->ratios[l]);
+        ctx->caps.push_back(cap);
+        ctx->swap.push_back(cap > G ? 1 : 0);
+        LayerDev& ld = ctx->h_layers[l];
+        ld = LayerDev{};
+        ld.cap = cap;
+        ld.ratio = ctx->ratios[l];
+        ld.swap = cap > G ? 1 : 0;
+        const size_t pool_bytes = (size_t)B * cap * kKvDim * sizeof(float);
+        void* hp = nullptr;
+        if (cfg->flags & SRH_FLAG_TEST_FAIL_HOST_ALLOC) {
+            return bail(SRH_ERR_NOMEM, "cudaHostAlloc failed (injected by SRH_FLAG_TEST_FAIL_HOST_ALLOC)");
+        }
+        e = cudaHostAlloc(&hp, pool_bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+        if (e != cudaSuccess) {
+            return bail(SRH_ERR_NOMEM, std::string("cudaHostAlloc: ") + cudaGetErrorString(e));
+        }
+        ctx->pool_host[l] = static_cast<float*>(hp);
+        void* dp = nullptr;
+        e = cudaHostGetDevicePointer(&dp, hp, 0);
+        if (e != cudaSuccess) return bail(SRH_ERR_CUDA, std::string("cudaHostGetDevicePointer: ") + cudaGetErrorString(e));
+        ctx->pool_dev[l] = static_cast<float*>(dp);
+        ld.pool = ctx->pool_dev[l];
+        ctx->ready_host[l].assign((size_t)B * cap, 0);
+        e = cudaMalloc(&ld.host_ready, (size_t)B * cap);
+        if (e == cudaSuccess) e = cudaMemset(ld.host_ready, 0, (size_t)B * cap);
+        if (e == cudaSuccess && ld.swap) {
+            e = cudaMalloc(&ld.slot_of, sizeof(int) * (size_t)B * cap);
+            if (e == cudaSuccess) e = cudaMemset(ld.slot_of, 0xff, sizeof(int) * (size_t)B * cap);
+            if (e == cudaSuccess) e = cudaMalloc(&ld.slot_logical, sizeof(int) * (size_t)B * G);
+            if (e == cudaSuccess) e = cudaMemset(ld.slot_logical, 0xff, sizeof(int) * (size_t)B * G);
+            if (e == cudaSuccess) e = cudaMalloc(&ld.lru_order, sizeof(int) * (size_t)B * G);
+            if (e == cudaSuccess) {
+                std::vector<int> order((size_t)B * G);
+                for (int b = 0; b < B; ++b)
+                    for (int q = 0; q < G; ++q) order[(size_t)b * G + q] = q;   // slot 0 at the back
+                e = cudaMemcpy(ld.lru_order, order.data(), sizeof(int) * order.size(), cudaMemcpyHostToDevice);
+            }
+        }
+        if (e != cudaSuccess) return bail(SRH_ERR_NOMEM, std::string("device state: ") + cudaGetErrorString(e));
+    }
+
+    e = cudaMalloc(&ctx->d_layers, sizeof(LayerDev) * ctx->L);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(ctx->d_layers, ctx->h_layers.data(), sizeof(LayerDev) * ctx->L, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_stats, sizeof(unsigned long long) * kStatCount);
+    if (e == cudaSuccess) e = cudaMemset(ctx->d_stats, 0, sizeof(unsigned long long) * kStatCount);
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_err, sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMemset(ctx->d_err, 0, sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_hist, sizeof(uint32_t) * kHistBins * B);
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_miss, sizeof(int2) * (size_t)ctx->L * B * ctx->S);
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_miss_count, sizeof(int) * (size_t)ctx->L * B);
+    if (e == cudaSuccess) e = cudaMemset(ctx->d_miss_count, 0, sizeof(int) * (size_t)ctx->L * B);
+    if (e != cudaSuccess) return bail(SRH_ERR_NOMEM, std::string("device scratch: ") + cudaGetErrorString(e));
+
+    std::vector<AttnItem> items;
+    plan_attention(ctx, &items);
+    e = cudaMalloc(&ctx->d_items, sizeof(AttnItem) * items.size());
+    if (e == cudaSuccess)
+        e = cudaMemcpy(ctx->d_items, items.data(), sizeof(AttnItem) * items.size(), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_part_o, sizeof(float) * (size_t)ctx->n_items * SRH_MAX_HEADS * kKvDim);
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_part_ml, sizeof(float) * (size_t)ctx->n_items * 2 * SRH_MAX_HEADS);
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_attn_counter, sizeof(unsigned) * (size_t)ctx->L * B);
+    if (e == cudaSuccess) e = cudaMemset(ctx->d_attn_counter, 0, sizeof(unsigned) * (size_t)ctx->L * B);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_resolved, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_gathered, cudaEventDisableTiming);
+    if (e != cudaSuccess) return bail(SRH_ERR_NOMEM, std::string("attention scratch: ") + cudaGetErrorString(e));
+    *out = ctx;
+    return SRH_OK;
+}
+
+void srh_destroy(srh_ctx* ctx) { free_ctx(ctx); }
+
+float* srh_pool_host_ptr(srh_ctx* ctx, int layer, int seq) {
+    if (!ctx || layer < 0 || layer >= ctx->L || seq < 0 || seq >= ctx->B) return nullptr;
+    return ctx->pool_host[layer] + (size_t)seq * ctx->caps[layer] * kKvDim;
+}
+
+int srh_mark_stored(srh_ctx* ctx, int layer, int seq, long long c0, long long n) {
+    if (!ctx) return SRH_ERR_INVALID;
+    if (layer < 0 || layer >= ctx->L || seq < 0 || seq >= ctx->B)
+        return fail(ctx, SRH_ERR_INVALID, "layer or seq out of range");
+    const long long cap = ctx->caps[layer];
+    if (c0 < 0 || n < 0 || c0 + n > cap) return fail(ctx, SRH_ERR_INVALID, "chunk range out of bounds");
+    if (n == 0) return SRH_OK;
+    uint8_t* hr = ctx->ready_host[layer].data() + (size_t)seq * cap;
+    std::memset(hr + c0, 1, (size_t)n);
+    SRH_CUDA(ctx, cudaMemcpy(ctx->h_layers[layer].host_ready + (size_t)seq * cap + c0, hr + c0, (size_t)n,
+                             cudaMemcpyHostToDevice));
+    if (!ctx->swap[layer]) ctx->resident_dirty[layer] = 1;
+    return SRH_OK;
+}
+
+int srh_layer_info(srh_ctx* ctx, int layer, long long* cap, int* swap_enabled) {
+    if (!ctx || layer < 0 || layer >= ctx->L) return SRH_ERR_INVALID;
+    if (cap) *cap = ctx->caps[layer];
+    if (swap_enabled) *swap_enabled = ctx->swap[layer];
+    return SRH_OK;
+}
+
+int srh_max_select(srh_ctx* ctx) { return ctx ? ctx->S : SRH_ERR_INVALID; }
+
+int fm_score(srh_ctx* ctx, const uint16_t* d_keys, int n, const uint16_t* d_q, float scale,
+             const float* bias3, int ensemble, float* d_scores, srh_stream_t stream) {
+    if (!ctx) return SRH_ERR_INVALID;
+    if (!d_keys || !d_q || !bias3 || !d_scores) return fail(ctx, SRH_ERR_INVALID, "NULL pointer");
+    if (n < 1 || n > ctx->n_src) return fail(ctx, SRH_ERR_INVALID, "n must be in [1, source capacity]");
+    if (ensemble != SRH_ENSEMBLE_MAX && ensemble != SRH_ENSEMBLE_MEAN)
+        return fail(ctx, SRH_ERR_INVALID, "unknown ensemble");
+    if (((uintptr_t)d_keys | (uintptr_t)d_q) & 15) return fail(ctx, SRH_ERR_INVALID, "keys/queries must be 16-byte aligned");
+    if (!std::isfinite(scale)) return fail(ctx, SRH_ERR_INVALID, "scale must be finite");
+    const cudaError_t e = launch_score(d_keys, n, ctx->B, d_q, scale, bias3, ensemble, d_scores, ctx->d_hist,
+                                       ctx->sm_count, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "fm_score launch");
+    ctx->hist_scores = d_scores;
+    ctx->hist_n = n;
+    return SRH_OK;
+}
+
+int fm_select(srh_ctx* ctx, const float* d_scores, int n, int mode, int k, float tau, int clamp,
+              int32_t* d_sel, int32_t* d_count, srh_stream_t stream) {
+    if (!ctx) return SRH_ERR_INVALID;
+    if (!d_scores || !d_sel || !d_count) return fail(ctx, SRH_ERR_INVALID, "NULL pointer");
+    if (n < 1 || n > ctx->n_src) return fail(ctx, SRH_ERR_INVALID, "n must be in [1, source capacity]");
+    float thresh = 0.f;
+    if (mode == SRH_SELECT_TOPK) {
+        if (k < 1 || k > ctx->S) return fail(ctx, SRH_ERR_INVALID, "k must be in [1, max_select]");
+    } else if (mode == SRH_SELECT_THRESH) {
+        if (!(tau > 0.f && tau < 1.f)) return fail(ctx, SRH_ERR_INVALID, "tau must be in (0, 1)");
+        if (clamp < 0 || clamp > ctx->S || clamp > ctx->G)
+            return fail(ctx, SRH_ERR_INVALID, "clamp must be in [0, min(max_select, gpu_chunks)]");
+        thresh = (float)std::log((double)tau / (1.0 - (double)tau));
+    } else {
+        return fail(ctx, SRH_ERR_INVALID, "unknown selection mode");
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    const uint32_t* hist = nullptr;
+    if (mode == SRH_SELECT_TOPK || clamp > 0) {
+        if (ctx->hist_scores == d_scores && ctx->hist_n == n) {
+            hist = ctx->d_hist;
+        } else {
+            const cudaError_t e = launch_hist(d_scores, n, ctx->B, ctx->d_hist, st);
+            if (e != cudaSuccess) return cuda_fail(ctx, e, "fm_select histogram");
+            hist = ctx->d_hist;
+        }
+    }
+    ctx->hist_scores = nullptr;   // one use per scoring pass
+    ctx->hist_n = -1;
+    const cudaError_t e = launch_select(d_scores, n, ctx->B, mode, k, thresh, clamp, ctx->S, hist, d_sel,
+                                        d_count, st);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "fm_select launch");
+    return SRH_OK;
+}
+
+int kvswap_stage(srh_ctx* ctx, int layer, const int32_t* d_sel, const int32_t* d_count,
+                 float* d_staging, int32_t* d_phys, int32_t* d_count_l, srh_stream_t main,
+                 srh_stream_t side) {
+    if (!ctx) return SRH_ERR_INVALID;
+    if (!d_sel || !d_count || !d_staging || !d_phys || !d_count_l) return fail(ctx, SRH_ERR_INVALID, "NULL pointer");
+    if (layer < -1 || layer >= ctx->L) return fail(ctx, SRH_ERR_INVALID, "layer out of range");
+    if (((uintptr_t)d_staging) & 15) return fail(ctx, SRH_ERR_INVALID, "staging must be 16-byte aligned");
+    if (ctx->staging && ctx->staging != d_staging)
+        return fail(ctx, SRH_ERR_INVALID, "d_staging differs from the buffer bound on the first call");
+    ctx->staging = d_staging;
+    cudaStream_t sm = (cudaStream_t)main, ss = (cudaStream_t)side;
+    const int l0 = layer < 0 ? 0 : layer;
+    const int nl = layer < 0 ? ctx->L : 1;
+    // swap-disabled layers: (re)copy their stored chunks once
+    for (int l = l0; l < l0 + nl; ++l) {
+        if (ctx->swap[l] || !ctx->resident_dirty[l]) continue;
+        cudaError_t e = launch_resident_fill(ctx->pool_dev[l], ctx->h_layers[l].host_ready, ctx->caps[l], l,
+                                             ctx->B, ctx->G, d_staging, sm);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "resident fill");
+        ctx->resident_dirty[l] = 0;
+        unsigned long long ready = 0;
+        for (uint8_t v : ctx->ready_host[l]) ready += v;
+        ctx->resident_fill_bytes += ready * kKvDim * sizeof(float);
+    }
+    cudaError_t e = launch_lru(ctx->d_layers, l0, nl, ctx->B, ctx->G, ctx->S, ctx->cfg.src_ratio, d_sel, d_count,
+                               d_phys, d_count_l, ctx->d_miss, ctx->d_miss_count, ctx->d_stats, ctx->d_err, sm);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "kvswap_stage LRU launch");
+    if (ss && ss != sm) {
+        SRH_CUDA(ctx, cudaEventRecord(ctx->ev_resolved, sm));
+        SRH_CUDA(ctx, cudaStreamWaitEvent(ss, ctx->ev_resolved, 0));
+    } else {
+        ss = sm;
+    }
+    e = launch_gather(ctx->d_layers, l0, nl, ctx->B, ctx->G, ctx->S, ctx->d_miss, ctx->d_miss_count, d_staging,
+                      ctx->d_err, ctx->sm_count, ss);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "kvswap_stage gather launch");
+    if (ss != sm) {
+        SRH_CUDA(ctx, cudaEventRecord(ctx->ev_gathered, ss));
+        SRH_CUDA(ctx, cudaStreamWaitEvent(sm, ctx->ev_gathered, 0));
+    }
+    ++ctx->stage_calls;
+    return SRH_OK;
+}
+
+int lsa_attend(srh_ctx* ctx, int layer, const uint16_t* d_q, int n_heads, const float* d_window,
+               const float* d_staging, const int32_t* d_phys, const int32_t* d_count_l, float* d_out,
+               srh_stream_t stream) {
+    if (!ctx) return SRH_ERR_INVALID;
+    if (!d_q || !d_window || !d_staging || !d_phys || !d_count_l || !d_out)
+        return fail(ctx, SRH_ERR_INVALID, "NULL pointer");
+    if (layer < -1 || layer >= ctx->L) return fail(ctx, SRH_ERR_INVALID, "layer out of range");
+    if (n_heads != 16 && n_heads != 32 && n_heads != 64)
+        return fail(ctx, SRH_ERR_INVALID, "n_heads must be 16, 32 or 64");
+    if (((uintptr_t)d_q | (uintptr_t)d_window | (uintptr_t)d_staging | (uintptr_t)d_out) & 15)
+        return fail(ctx, SRH_ERR_INVALID, "q/window/staging/out must be 16-byte aligned");
+    const int i0 = layer < 0 ? 0 : ctx->item_begin[layer];
+    const int i1 = layer < 0 ? ctx->n_items : ctx->item_begin[layer + 1];
+    const cudaError_t e = launch_attend(ctx->d_items, i0, i1 - i0, ctx->split_rows, n_heads, ctx->B, ctx->G,
+                                        ctx->S, d_q, d_window, d_staging, d_phys, d_count_l, d_out,
+                                        ctx->d_part_o, ctx->d_part_ml, ctx->d_attn_counter, ctx->d_err,
+                                        (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "lsa_attend launch");
+    return SRH_OK;
+}
+
+int srh_get_stats(srh_ctx* ctx, srh_stats* out) {
+    if (!ctx || !out) return SRH_ERR_INVALID;
+    SRH_CUDA(ctx, cudaDeviceSynchronize());
+    unsigned long long s[kStatCount];
+    SRH_CUDA(ctx, cudaMemcpy(s, ctx->d_stats, sizeof s, cudaMemcpyDeviceToHost));
+    std::memset(out, 0, sizeof *out);
+    out->hits = s[kStatHits];
+    out->misses = s[kStatMisses];
+    out->h2d_bytes = s[kStatMisses] * kKvDim * sizeof(float);
+    out->d2h_bytes = 0;
+    out->resident_fill_bytes = ctx->resident_fill_bytes;
+    out->stage_calls = ctx->stage_calls;
+    out->selected = s[kStatSelected];
+    int sw = 0;
+    for (int v : ctx->swap) sw += v;
+    out->swapped_layers = sw;
+    out->n_layers = ctx->L;
+    return SRH_OK;
+}
+
+int srh_reset_stats(srh_ctx* ctx) {
+    if (!ctx) return SRH_ERR_INVALID;
+    SRH_CUDA(ctx, cudaDeviceSynchronize());
+    SRH_CUDA(ctx, cudaMemset(ctx->d_stats, 0, sizeof(unsigned long long) * kStatCount));
+    SRH_CUDA(ctx, cudaDeviceSynchronize());
+    ctx->stage_calls = 0;
+    return SRH_OK;
+}
+
+int srh_check_error(srh_ctx* ctx) {
+    if (!ctx) return SRH_ERR_INVALID;
+    SRH_CUDA(ctx, cudaDeviceSynchronize());
+    uint32_t w = 0;
+    SRH_CUDA(ctx, cudaMemcpy(&w, ctx->d_err, sizeof w, cudaMemcpyDeviceToHost));
+    SRH_CUDA(ctx, cudaMemset(ctx->d_err, 0, sizeof w));
+    SRH_CUDA(ctx, cudaDeviceSynchronize());
+    if (w & kErrNotStored) return fail(ctx, SRH_ERR_NOT_STORED, "GGUF KV swap selected chunk before it was stored");
+    if (w & kErrBounds) return fail(ctx, SRH_ERR_BOUNDS, "a device index was out of bounds");
+    if (w & kErrTimeout) return fail(ctx, SRH_ERR_TIMEOUT, "a device wait timed out");
+    return SRH_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,145 @@
+// Internal declarations shared by the translation units of libsrh.so.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/srh.h"
+
+namespace srh {
+
+constexpr int kKvDim = SRH_KV_DIM;
+constexpr int kWindow = SRH_WINDOW;
+constexpr int kIdx = SRH_N_INDEXERS;
+constexpr int kIdxHeads = SRH_INDEXER_HEADS;
+constexpr int kIdxDim = SRH_INDEXER_DIM;
+constexpr int kHistBins = 4096;        // score histogram: top 12 bits of the ordered key
+constexpr int kMaxSelect = 4096;       // largest S
+constexpr int kMaxGpuChunks = 4096;    // largest G
+constexpr int kAttnTile = 32;          // rows per attention tile
+
+// Bits of the sticky device error word.
+enum : uint32_t {
+    kErrNotStored = 1u,
+    kErrBounds = 2u,
+    kErrTimeout = 4u,
+};
+
+// Device-side counters (one array of unsigned long long).
+enum : int {
+    kStatHits = 0,
+    kStatMisses,
+    kStatSelected,
+    kStatResidentFill,
+    kStatCount
+};
+
+// Per-layer facts and state pointers, kept in device memory ([L] array).
+struct LayerDev {
+    long long cap;           // chunks of this layer
+    int ratio;               // compression ratio
+    int swap;                // 1 if cap > G
+    const float* pool;       // device alias of the mapped pinned pool [B][cap][D]
+    uint8_t* host_ready;     // [B][cap]
+    int* slot_of;            // [B][cap]: slot holding chunk c, -1 if none (swap layers)
+    int* slot_logical;       // [B][G]: chunk in slot s, -1 if free (swap layers)
+    int* lru_order;          // [B][G]: slots from least (0) to most recently used
+};
+
+// One attention work item: rows [split*split_rows, ...) of (layer, seq).
+struct AttnItem {
+    int layer;
+    int seq;
+    int split;
+    int n_splits;
+};
+
+struct Ctx {
+    srh_config cfg{};
+    std::vector<int> ratios;
+    std::vector<long long> caps;
+    std::vector<int> swap;
+    int S = 0;           // selection row stride
+    int G = 0;
+    int B = 0;
+    int L = 0;
+    long long n_src = 0; // scored chunks (ratio src_ratio)
+    int device = 0;
+    int sm_count = 0;
+
+    // pinned pools: one per layer, [B][cap][D]
+    std::vector<float*> pool_host;
+    std::vector<float*> pool_dev;
+    // host_ready mirror (host) per layer [B][cap]
+    std::vector<std::vector<uint8_t>> ready_host;
+    // swap-disabled layers whose staging rows need a (re)fill, per layer
+    std::vector<uint8_t> resident_dirty;
+
+    // device state
+    LayerDev* d_layers = nullptr;
+    std::vector<LayerDev> h_layers;
+    unsigned long long* d_stats = nullptr;
+    uint32_t* d_err = nullptr;
+    uint32_t* d_hist = nullptr;         // [B][kHistBins]
+    const float* hist_scores = nullptr; // the d_scores the histogram describes
+    int hist_n = -1;
+    int2* d_miss = nullptr;             // [L][B][S] (chunk, slot)
+    int* d_miss_count = nullptr;        // [L][B]
+    // attention scratch
+    AttnItem* d_items = nullptr;        // all items, grouped by layer
+    std::vector<int> item_begin;        // [L+1] offsets into d_items
+    int split_rows = 0;
+    int n_items = 0;
+    float* d_part_o = nullptr;          // [n_items][SRH_MAX_HEADS][D]
+    float* d_part_ml = nullptr;         // [n_items][2][SRH_MAX_HEADS]
+    unsigned* d_attn_counter = nullptr; // [L][B]
+    // bookkeeping
+    float* staging = nullptr;           // the staging buffer bound to this context
+    cudaEvent_t ev_resolved = nullptr;
+    cudaEvent_t ev_gathered = nullptr;
+    unsigned long long stage_calls = 0;
+    unsigned long long resident_fill_bytes = 0;
+    std::string last_error;
+};
+
+#ifdef __CUDACC__
+// Order-preserving 32-bit key of a score: a larger score gives a larger key and
+// -0 maps like +0, so equal scores give equal keys.
+__device__ __forceinline__ uint32_t ordered_key(float s) {
+    s = (s == 0.0f) ? 0.0f : s;
+    const uint32_t u = __float_as_uint(s);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+#endif
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_score(const uint16_t* keys, int n, int B, const uint16_t* q, float scale,
+                         const float* bias3, int ensemble, float* scores, uint32_t* hist,
+                         int sm_count, cudaStream_t st);
+cudaError_t launch_hist(const float* scores, int n, int B, uint32_t* hist, cudaStream_t st);
+cudaError_t launch_select(const float* scores, int n, int B, int mode, int k, float thresh,
+                          int clamp, int S, const uint32_t* hist, int32_t* sel, int32_t* count,
+                          cudaStream_t st);
+cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int S, int src_ratio,
+                       const int32_t* sel, const int32_t* count, int32_t* phys, int32_t* count_l,
+                       int2* miss, int* miss_count, unsigned long long* stats, uint32_t* err,
+                       cudaStream_t st);
+cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, int S,
+                          const int2* miss, const int* miss_count, float* staging,
+                          uint32_t* err, int sm_count, cudaStream_t st);
+cudaError_t launch_resident_fill(const float* pool_dev, const uint8_t* ready, long long cap,
+                                 int layer, int B, int G, float* staging, cudaStream_t st);
+cudaError_t launch_attend(const AttnItem* items, int item0, int n_items, int split_rows,
+                          int n_heads, int B, int G, int S, const uint16_t* q, const float* window,
+                          const float* staging, const int32_t* phys, const int32_t* count_l,
+                          float* out, float* part_o, float* part_ml, unsigned* counters,
+                          uint32_t* err, cudaStream_t st);
+size_t lru_smem_bytes(int S, int G);
+int attend_max_splits();
+
+}  // namespace srh
+
+struct srh_ctx : public srh::Ctx {};

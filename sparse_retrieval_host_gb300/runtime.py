@@ -1,0 +1,127 @@
+"""Device buffers for one decode loop and the four-call decode step.
+
+``DecodeStep`` owns a library context (pinned pools, slot tables, scratch) and
+the caller-side device tensors the C ABI reads and writes. ``step()`` issues
+fm_score -> fm_select -> kvswap_stage -> lsa_attend on one stream (the miss
+gathers go to a side stream when one is given). PyTorch is used only to
+allocate device memory and to name streams.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import abi
+
+INDEXERS, IDX_HEADS, IDX_DIM = 3, 8, 128
+
+
+@dataclass
+class StepSpec:
+    scale: float
+    bias: Sequence[float]
+    ensemble: int
+    select_mode: int
+    k: int
+    tau: float
+    clamp: int
+
+
+class DecodeStep:
+    def __init__(self, *, batch: int, layer_ratios: Sequence[int], gpu_chunks: int, index_topk: int,
+                 context_len: int, n_heads: int, max_select: int = 0, src_ratio: int = 4,
+                 pinned_cap_bytes: int = 0, allow_topk_reduction: bool = False,
+                 device: str = "cuda", flags: int = 0):
+        self.cfg = abi.make_config(batch=batch, layer_ratios=list(layer_ratios), gpu_chunks=gpu_chunks,
+                                   index_topk=index_topk, context_len=context_len, src_ratio=src_ratio,
+                                   pinned_cap_bytes=pinned_cap_bytes,
+                                   allow_topk_reduction=allow_topk_reduction, max_select=max_select,
+                                   flags=flags)
+        self.ctx = abi.srh_create(self.cfg)
+        self.B, self.L, self.G, self.H = batch, len(layer_ratios), gpu_chunks, n_heads
+        self.layer_ratios = list(layer_ratios)
+        self.S = abi.srh_max_select(self.ctx)
+        self.n = (context_len + src_ratio - 1) // src_ratio
+        self.caps = [abi.srh_layer_info(self.ctx, l)[0] for l in range(self.L)]
+        self.swap = [abi.srh_layer_info(self.ctx, l)[1] for l in range(self.L)]
+        dev = torch.device(device)
+        B, L, G, H, S, n = self.B, self.L, self.G, self.H, self.S, self.n
+        i16, f32, i32 = torch.int16, torch.float32, torch.int32
+        self.keys = torch.zeros((B, n, IDX_DIM), dtype=i16, device=dev)
+        self.fm_q = torch.zeros((B, INDEXERS, IDX_HEADS, IDX_DIM), dtype=i16, device=dev)
+        self.scores = torch.zeros((B, n), dtype=f32, device=dev)
+        self.sel = torch.zeros((B, S), dtype=i32, device=dev)
+        self.count = torch.zeros((B,), dtype=i32, device=dev)
+        self.staging = torch.zeros((L, B, G, abi.KV_DIM), dtype=f32, device=dev)
+        self.phys = torch.zeros((L, B, S), dtype=i32, device=dev)
+        self.count_l = torch.zeros((L, B), dtype=i32, device=dev)
+        self.window = torch.zeros((L, B, abi.WINDOW, abi.KV_DIM), dtype=f32, device=dev)
+        self.q = torch.zeros((L, B, H, abi.KV_DIM), dtype=i16, device=dev)
+        self.out = torch.zeros((L, B, H, abi.KV_DIM), dtype=f32, device=dev)
+
+    # ------------------------------------------------------------------ host pools
+    def pool_view(self, layer: int, seq: int) -> np.ndarray:
+        """numpy view of the pinned pool of (layer, seq): ``[cap][512]`` fp32."""
+        addr = abi.srh_pool_host_ptr(self.ctx, layer, seq)
+        cap = self.caps[layer]
+        buf = (ctypes.c_float * (cap * abi.KV_DIM)).from_address(addr)
+        return np.ctypeslib.as_array(buf).reshape(cap, abi.KV_DIM)
+
+    def mark_stored(self, layer: int, seq: int, c0: int = 0, n: Optional[int] = None) -> None:
+        if n is None:
+            n = self.caps[layer] - c0
+        abi.srh_mark_stored(self.ctx, layer, seq, c0, n)
+
+    # ------------------------------------------------------------------ the step
+    def score(self, spec: StepSpec, stream=None, fm_q=None) -> None:
+        abi.fm_score(self.ctx, self.keys, self.n, self.fm_q if fm_q is None else fm_q, spec.scale,
+                     spec.bias, spec.ensemble, self.scores, stream)
+
+    def select(self, spec: StepSpec, stream=None) -> None:
+        abi.fm_select(self.ctx, self.scores, self.n, spec.select_mode, spec.k, spec.tau, spec.clamp,
+                      self.sel, self.count, stream)
+
+    def stage(self, layer: int = -1, stream=None, side=None) -> None:
+        abi.kvswap_stage(self.ctx, layer, self.sel, self.count, self.staging, self.phys, self.count_l,
+                         stream, side)
+
+    def attend(self, layer: int = -1, stream=None, q=None, out=None) -> None:
+        abi.lsa_attend(self.ctx, layer, self.q if q is None else q, self.H, self.window, self.staging,
+                       self.phys, self.count_l, self.out if out is None else out, stream)
+
+    def step(self, spec: StepSpec, stream=None, side=None, fm_q=None, q=None, out=None) -> None:
+        """One decode step: the four C entry points in order (5 kernels)."""
+        self.score(spec, stream, fm_q)
+        self.select(spec, stream)
+        self.stage(-1, stream, side)
+        self.attend(-1, stream, q, out)
+
+    # ------------------------------------------------------------------ status
+    def stats(self) -> dict:
+        return abi.srh_get_stats(self.ctx)
+
+    def reset_stats(self) -> None:
+        abi.srh_reset_stats(self.ctx)
+
+    def check_error(self) -> int:
+        return abi.srh_check_error(self.ctx)
+
+    def close(self) -> None:
+        if getattr(self, "ctx", None):
+            abi.srh_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):  # pragma: no cover
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def bits_to_i16(a: np.ndarray) -> torch.Tensor:
+    """uint16 bf16 bit patterns as an int16 tensor (same bytes)."""
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16))

@@ -1,0 +1,186 @@
+"""End-to-end decode steps through the C ABI against the fp64 oracle, the
+residency invariant, and the swap counters."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from srh_workload import configs as C
+from srh_workload import generate as G
+
+from helpers import (ATTN_TOL, attn_err, check_selection, fill, load_step_inputs, make_ds,
+                     make_oracle, spec_of)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def _run_decode(w, steps, attend_layers=None, pools=None):
+    """Run ``steps`` decode steps on GPU and oracle; returns (n_matched_steps, worst_attn_rel)."""
+    ds = make_ds(w)
+    try:
+        if pools is None and w.n_chunks <= 8192:
+            pools = {(l, b): G.pool(w, l, b) for l in range(w.n_layers) for b in range(w.batch)}
+        keys = fill(ds, w, pools)
+        ora = make_oracle(w)
+        spec = spec_of(w)
+        in_sync = True
+        worst = 0.0
+        matched = 0
+        hits = misses = 0
+        if pools is not None:
+            rows_of = lambda l, b, idx: pools[(l, b)][np.asarray(idx, dtype=np.int64)]
+        else:
+            rows_of = lambda l, b, idx: G.pool_rows(w, l, b, idx)
+        layers = range(w.n_layers) if attend_layers is None else attend_layers
+        for t in range(steps):
+            load_step_inputs(ds, w, t)
+            ds.step(spec)
+            torch.cuda.synchronize()
+            pairs = [(l, b) for l in layers for b in range(w.batch)]
+            ref = ora.step(lambda b: keys[b], lambda b: G.fm_queries(w, t, b),
+                           lambda l, b: G.attn_q(w, t, l, b), lambda l, b: G.window(w, l, b),
+                           rows_of, attend_pairs=pairs)
+            scores = ds.scores.double().cpu().numpy()
+            sel = ds.sel.cpu().numpy()
+            cnt = ds.count.cpu().numpy()
+            same = True
+            for b in range(w.batch):
+                same &= check_selection(w, ref.scores[b], ref.sel[b], sel[b, :cnt[b]], scores[b])
+            in_sync &= same
+            phys = ds.phys.cpu().numpy()
+            cl = ds.count_l.cpu().numpy()
+            for l in range(w.n_layers):
+                for b in range(w.batch):
+                    if in_sync:
+                        assert cl[l, b] == len(ref.lists[l][b])
+                        assert phys[l, b, :cl[l, b]].tolist() == ref.swap[l][b].phys, (t, l, b)
+                        if ds.swap[l]:
+                            hits += ref.swap[l][b].hits
+                            misses += len(ref.swap[l][b].misses)
+            # staged rows always hold the pool rows of the GPU's own selection
+            stg = ds.staging
+            for l in list(layers)[:3]:
+                for b in range(w.batch):
+                    n_l = int(cl[l, b])
+                    got = stg[l, b][torch.from_numpy(phys[l, b, :n_l] - 128).long().cuda()].cpu().numpy()
+                    lst = np.asarray(sorted(set(sel[b, :cnt[b]] * 4 // w.layer_ratios[l])), dtype=np.int64)
+                    want_rows = rows_of(l, b, lst)
+                    assert sorted(map(bytes, got)) == sorted(map(bytes, want_rows))
+            if in_sync:
+                matched += 1
+                out = ds.out.cpu().numpy()
+                for (l, b), r in ref.out.items():
+                    _, rel = attn_err(out[l, b], r)
+                    worst = max(worst, rel)
+        if matched == steps:
+            st = ds.stats()
+            assert st["hits"] == hits and st["misses"] == misses
+        assert ds.check_error() == 0
+        return matched, worst
+    finally:
+        ds.close()
+
+
+def test_decode_tiny_all_steps():
+    w = C.TINY
+    matched, worst = _run_decode(w, w.steps)
+    assert matched == w.steps
+    assert worst <= ATTN_TOL, worst
+
+
+def test_decode_ctx8k_full_stack():
+    w = C.CTX8K
+    matched, worst = _run_decode(w, 40)
+    assert matched == 40
+    assert worst <= ATTN_TOL, worst
+
+
+def test_decode_batch_sweep_b4():
+    w = C.batch_sweep(4)
+    matched, worst = _run_decode(w, 20, attend_layers=[0, 7, 19])
+    assert matched == 20
+    assert worst <= ATTN_TOL, worst
+
+
+@pytest.mark.skipif(os.environ.get("SRH_SKIP_LARGE") == "1", reason="large configs skipped")
+def test_decode_ctx256k_sampled():
+    w = C.CTX256K
+    matched, worst = _run_decode(w, 20, attend_layers=[0, 19, 20, 40])
+    assert matched == 20
+    assert worst <= ATTN_TOL, worst
+
+
+@pytest.mark.skipif(os.environ.get("SRH_SKIP_LARGE") == "1", reason="large configs skipped")
+def test_decode_ctx1m_sampled():
+    w = C.CTX1M
+    matched, worst = _run_decode(w, 12, attend_layers=[0, 20, 40])
+    assert matched == 12
+    assert worst <= ATTN_TOL, worst
+
+
+def test_residency_changes_slots_never_outputs():
+    """kestrel-llm-cuda 06, section 3.4 and the FlashMemory doc's 验证状态: swapping
+    changes which slots hold a chunk, never the outputs (bitwise)."""
+    swapped = C.TINY
+    resident = swapped.with_(gpu_chunks=2048)
+    outs = []
+    for w in (swapped, resident):
+        ds = make_ds(w)
+        try:
+            fill(ds, w)
+            spec = spec_of(w)
+            seq = []
+            for t in range(w.steps):
+                load_step_inputs(ds, w, t)
+                ds.step(spec)
+                seq.append(ds.out.clone())
+            st = ds.stats()
+            outs.append((torch.stack(seq).cpu(), st, ds.swap[0]))
+        finally:
+            ds.close()
+    (a, sa, swa), (b, sb, swb) = outs
+    assert swa and not swb
+    assert sa["misses"] > 0 and sb["misses"] == 0
+    assert torch.equal(a, b)
+
+
+def test_ties_follow_index_order():
+    """Duplicated keys give exactly equal scores; both sides break ties by index."""
+    from sparse_retrieval_host_gb300.runtime import bits_to_i16
+    from oracle import srh_oracle as O
+    w = C.TINY
+    ds = make_ds(w)
+    try:
+        base = G.keys(w, 0)
+        keys = base[np.arange(w.n_chunks) % 100]
+        ds.keys[0] = bits_to_i16(keys)
+        for t in (0, 8):
+            ds.fm_q[0] = bits_to_i16(G.fm_queries(w, t, 0))
+            ds.score(spec_of(w))
+            ds.select(spec_of(w))
+            ref_s = O.score(keys, G.fm_queries(w, t, 0), w.scale, [0.0] * 3, w.ensemble)
+            ref = O.select_topk(ref_s, w.index_topk)
+            got = ds.sel[0, :int(ds.count[0])].cpu().numpy()
+            assert np.array_equal(np.sort(got), np.sort(ref))
+            g = ds.scores[0].double().cpu().numpy()
+            assert all(g[c] == g[c % 100] for c in range(w.n_chunks))
+    finally:
+        ds.close()
+
+
+def test_max_sizes_select_and_stage():
+    """Largest supported S and G (4096) on one layer."""
+    w = C.Workload(name="max", code=60, context_len=4 * 20000, layer_ratios=(4,), gpu_chunks=4096,
+                   index_topk=4096, ensemble=C.ENSEMBLE_MAX, select_mode=C.SELECT_TOPK, tau=0.5,
+                   bias=0.0, n_heads=64, batch=1, steps=3, lookahead=1)
+    matched, worst = _run_decode(w, 3)
+    assert matched == 3
+    assert worst <= ATTN_TOL

@@ -1,0 +1,285 @@
+"""GPU parity of each C-ABI call against the fp64 oracle on seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import srh_oracle as O
+from srh_workload import configs as C
+from srh_workload import generate as G
+
+from helpers import (ATTN_TOL, attn_err, fill, load_step_inputs, make_ds, spec_of)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def _w(**kw):
+    base = dict(name="unit", code=50, context_len=8192, layer_ratios=(4,), gpu_chunks=512,
+                index_topk=512, ensemble=C.ENSEMBLE_MAX, select_mode=C.SELECT_TOPK, tau=0.5,
+                bias=0.0, n_heads=16, batch=1, steps=4, lookahead=2)
+    base.update(kw)
+    return C.Workload(**base)
+
+
+# ----------------------------------------------------------------------------- fm_score
+@pytest.mark.parametrize("w", [
+    C.TINY,
+    _w(context_len=4 * 1001 + 3, code=51),                          # ragged tail: n = 1002
+    _w(context_len=4, code=52, index_topk=1, gpu_chunks=1),         # n = 1
+    _w(context_len=131072, batch=3, code=53, ensemble=C.ENSEMBLE_MEAN, bias=-7.0),
+], ids=["tiny", "ragged", "n1", "b3_mean"])
+def test_fm_score_matches_oracle(w):
+    from sparse_retrieval_host_gb300.runtime import bits_to_i16
+    ds = make_ds(w, layer_ratios=(4,))
+    try:
+        keys = [G.keys(w, b) for b in range(w.batch)]
+        for b in range(w.batch):
+            ds.keys[b] = bits_to_i16(keys[b])
+        for t in (0, w.lookahead):
+            for b in range(w.batch):
+                ds.fm_q[b] = bits_to_i16(G.fm_queries(w, t, b))
+            ds.score(spec_of(w))
+            got = ds.scores.double().cpu().numpy()
+            for b in range(w.batch):
+                ref = O.score(keys[b], G.fm_queries(w, t, b), w.scale, [w.bias] * 3, w.ensemble)
+                err = np.abs(got[b] - ref).max()
+                assert err <= 1e-5, err
+    finally:
+        ds.close()
+
+
+# ----------------------------------------------------------------------------- fm_select
+def _select_case(name, n, rng):
+    if name == "random":
+        return rng.standard_normal(n).astype(np.float32)
+    if name == "ties":
+        return rng.choice(np.float32([-2.0, -0.0, 0.0, 0.5, 1.0, 1.0000001, 3.0]), size=n)
+    if name == "equal":
+        return np.zeros(n, np.float32)
+    if name == "one_bin":     # everything in one 12-bit histogram bin: forces deeper radix passes
+        return (1.0 + rng.random(n) * 1e-3).astype(np.float32)
+    if name == "neg":
+        return -np.abs(rng.standard_normal(n)).astype(np.float32)
+    raise ValueError(name)
+
+
+@pytest.mark.parametrize("n", [1, 37, 2048, 65536, 262144])
+@pytest.mark.parametrize("case", ["random", "ties", "equal", "one_bin", "neg"])
+def test_fm_select_topk_exact(n, case):
+    from sparse_retrieval_host_gb300 import abi
+    rng = np.random.default_rng(n + len(case))
+    s = _select_case(case, n, rng)
+    k = 512
+    w = _w(context_len=4 * n, code=54)
+    ds = make_ds(w, layer_ratios=(4,))
+    try:
+        ds.scores[0, :n] = torch.from_numpy(s)
+        abi.fm_select(ds.ctx, ds.scores, n, abi.SRH_SELECT_TOPK, k, 0.5, 0, ds.sel, ds.count)
+        cnt = int(ds.count[0])
+        got = ds.sel[0, :cnt].cpu().numpy()
+        ref = O.select_topk(s.astype(np.float64), k)
+        assert cnt == len(ref)
+        assert np.array_equal(got, ref)
+    finally:
+        ds.close()
+
+
+@pytest.mark.parametrize("n,clamp,case", [(2048, 512, "random"), (262144, 512, "random"),
+                                          (262144, 512, "neg"), (5000, 4, "ties"), (70000, 300, "ties"),
+                                          (2048, 0, "random")])
+def test_fm_select_threshold_exact(n, clamp, case):
+    from sparse_retrieval_host_gb300 import abi
+    rng = np.random.default_rng(n + clamp)
+    s = _select_case(case, n, rng) - np.float32(2.5 if case == "random" else 0.0)
+    w = _w(context_len=4 * n, code=55)
+    ds = make_ds(w, layer_ratios=(4,))
+    try:
+        ds.scores[0, :n] = torch.from_numpy(s)
+        abi.fm_select(ds.ctx, ds.scores, n, abi.SRH_SELECT_THRESH, 512, 0.5, clamp, ds.sel, ds.count)
+        cnt = int(ds.count[0])
+        got = ds.sel[0, :cnt].cpu().numpy()
+        ref = O.select_threshold(s.astype(np.float64), 0.5, clamp)
+        assert np.array_equal(got, ref)
+    finally:
+        ds.close()
+
+
+def test_fm_select_uses_fresh_histogram_after_scores_change():
+    """The scoring pass's histogram is used once; a second selection over other
+    scores in the same buffer must rebuild it."""
+    from sparse_retrieval_host_gb300 import abi
+    from sparse_retrieval_host_gb300.runtime import bits_to_i16
+    w = C.TINY
+    ds = make_ds(w)
+    try:
+        keys = G.keys(w, 0)
+        ds.keys[0] = bits_to_i16(keys)
+        ds.fm_q[0] = bits_to_i16(G.fm_queries(w, 0, 0))
+        ds.score(spec_of(w))
+        ds.select(spec_of(w))
+        s = np.random.default_rng(3).standard_normal(w.n_chunks).astype(np.float32)
+        ds.scores[0] = torch.from_numpy(s)
+        ds.select(spec_of(w))
+        got = ds.sel[0, :int(ds.count[0])].cpu().numpy()
+        assert np.array_equal(got, O.select_topk(s.astype(np.float64), w.index_topk))
+    finally:
+        ds.close()
+
+
+# ----------------------------------------------------------------------------- kvswap_stage
+def _trace(rng, n_steps, n, m_max, G_):
+    """Selections (distinct ids) mixing repeats, fresh ids and returns of old ids,
+    so some steps pop a slot whose chunk is selected later in the same list."""
+    steps, hist = [], []
+    for t in range(n_steps):
+        m = int(rng.integers(0, m_max + 1))
+        kind = t % 4
+        if kind == 0 or not hist:
+            ids = rng.choice(n, size=m, replace=False)
+        elif kind == 1:
+            prev = hist[-1]
+            keep = prev[rng.random(len(prev)) < 0.7]
+            fresh = rng.choice(n, size=m, replace=False)
+            ids = np.concatenate([keep, fresh])
+        elif kind == 2:
+            old = np.concatenate(hist[-4:])
+            ids = np.concatenate([rng.choice(n, size=m // 2, replace=False), old[::-1]])
+        else:
+            ids = np.concatenate([hist[0][::-1], rng.choice(n, size=m, replace=False)])
+        _, first = np.unique(ids, return_index=True)
+        ids = ids[np.sort(first)][:m_max]
+        steps.append(ids.astype(np.int64))
+        hist.append(ids)
+    return steps
+
+
+@pytest.mark.parametrize("G_,k,ctx_len", [(64, 48, 4 * 600), (512, 512, 8192), (40, 40, 4 * 90)])
+def test_kvswap_stage_matches_list_lru(G_, k, ctx_len):
+    ratios = (4, 128, 4, 8)
+    w = _w(context_len=ctx_len, layer_ratios=ratios, gpu_chunks=G_, index_topk=k, batch=2, code=56)
+    ds = make_ds(w, max_select=k)
+    try:
+        pools = {(l, b): G.pool(w, l, b) for l in range(w.n_layers) for b in range(w.batch)}
+        fill(ds, w, pools)
+        states = [[O.KvSwapLayerState(w.layer_cap(l), G_) for b in range(w.batch)] for l in range(w.n_layers)]
+        for row in states:
+            for st in row:
+                st.host_ready[:] = 1
+        rng = np.random.default_rng(G_ + k)
+        traces = [_trace(rng, 24, w.n_chunks, k, G_) for _ in range(w.batch)]
+        hits = misses = 0
+        for t in range(24):
+            sel = np.zeros((w.batch, ds.S), np.int32)
+            cnt = np.zeros(w.batch, np.int32)
+            for b in range(w.batch):
+                ids = traces[b][t]
+                sel[b, :len(ids)] = ids
+                cnt[b] = len(ids)
+            ds.sel.copy_(torch.from_numpy(sel))
+            ds.count.copy_(torch.from_numpy(cnt))
+            ds.stage()
+            torch.cuda.synchronize()
+            phys = ds.phys.cpu().numpy()
+            cl = ds.count_l.cpu().numpy()
+            staging = ds.staging.cpu().numpy()
+            for l in range(w.n_layers):
+                for b in range(w.batch):
+                    lst = O.layer_chunks(traces[b][t], 4, ratios[l])
+                    r = states[l][b].swap_in_selected(lst)
+                    if states[l][b].swap_enabled:
+                        hits += r.hits
+                        misses += len(r.misses)
+                    assert cl[l, b] == len(lst)
+                    assert phys[l, b, :len(lst)].tolist() == r.phys, (t, l, b)
+                    rows = staging[l, b][phys[l, b, :len(lst)] - 128]
+                    assert np.array_equal(rows, pools[(l, b)][lst]), (t, l, b)
+        st = ds.stats()
+        assert st["hits"] == hits and st["misses"] == misses
+        assert st["h2d_bytes"] == misses * 2048
+        assert ds.check_error() == 0
+    finally:
+        ds.close()
+
+
+def test_kvswap_not_stored_is_reported():
+    """Section 故障排查, error 4: a selected chunk that was never stored."""
+    from sparse_retrieval_host_gb300 import abi
+    w = _w(context_len=4 * 300, layer_ratios=(4, 128), gpu_chunks=64, index_topk=32, code=57)
+    ds = make_ds(w, max_select=32)
+    try:
+        ds.mark_stored(0, 0, 0, 100)
+        ds.mark_stored(1, 0)
+        sel = torch.zeros((1, ds.S), dtype=torch.int32)
+        sel[0, :3] = torch.tensor([5, 7, 99])
+        ds.sel.copy_(sel)
+        ds.count.fill_(3)
+        ds.stage()
+        assert ds.check_error() == abi.SRH_OK
+        sel[0, :3] = torch.tensor([5, 150, 99])
+        ds.sel.copy_(sel)
+        ds.stage()
+        assert ds.check_error() == abi.SRH_ERR_NOT_STORED
+        assert ds.check_error() == abi.SRH_OK       # the word clears after it is read
+    finally:
+        ds.close()
+
+
+def test_kvswap_rejects_a_second_staging_buffer():
+    from sparse_retrieval_host_gb300 import abi
+    w = _w(context_len=4 * 300, gpu_chunks=64, index_topk=32, code=58)
+    ds = make_ds(w, max_select=32)
+    try:
+        ds.mark_stored(0, 0)
+        ds.count.fill_(0)
+        ds.stage()
+        other = torch.zeros_like(ds.staging)
+        with pytest.raises(abi.SrhError):
+            abi.kvswap_stage(ds.ctx, -1, ds.sel, ds.count, other, ds.phys, ds.count_l)
+    finally:
+        ds.close()
+
+
+# ----------------------------------------------------------------------------- lsa_attend
+@pytest.mark.parametrize("H", [16, 32, 64])
+@pytest.mark.parametrize("counts,batch_layers", [((0, 1, 31, 32), 1), ((33, 200, 512, 97), 1),
+                                                 ((512,) * 8, 20)])
+def test_lsa_attend_matches_oracle(H, counts, batch_layers):
+    from sparse_retrieval_host_gb300.runtime import bits_to_i16
+    B = len(counts)
+    L = batch_layers
+    w = _w(context_len=8192, layer_ratios=(4,) * L, gpu_chunks=600, index_topk=512, n_heads=H,
+           batch=B, code=59)
+    ds = make_ds(w, max_select=512)
+    try:
+        rng = np.random.default_rng(H * 7 + B + L)
+        stg = rng.standard_normal((L, B, 600, 512), dtype=np.float32)
+        win = rng.standard_normal((L, B, 128, 512), dtype=np.float32)
+        q = G.f32_to_bf16_bits(rng.standard_normal((L, B, H, 512), dtype=np.float32))
+        phys = np.zeros((L, B, ds.S), np.int32)
+        for l in range(L):
+            for b in range(B):
+                phys[l, b, :counts[b]] = 128 + rng.choice(600, size=counts[b], replace=False)
+        ds.staging.copy_(torch.from_numpy(stg))
+        ds.window.copy_(torch.from_numpy(win))
+        ds.q.copy_(bits_to_i16(q))
+        ds.phys.copy_(torch.from_numpy(phys))
+        ds.count_l.copy_(torch.from_numpy(np.tile(np.int32(counts), (L, 1))))
+        ds.attend()
+        out = ds.out.cpu().numpy()
+        worst = 0.0
+        for l in range(L):
+            for b in range(B):
+                rows = np.concatenate([win[l, b], stg[l, b][phys[l, b, :counts[b]] - 128]])
+                ref = O.attend(q[l, b], rows)
+                _, rel = attn_err(out[l, b], ref)
+                worst = max(worst, rel)
+        assert worst <= ATTN_TOL, worst
+        assert ds.check_error() == 0
+    finally:
+        ds.close()
