@@ -86,7 +86,7 @@ struct LruShared {
 };
 
 __global__ void __launch_bounds__(kLruThreads)
-lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int src_ratio,
+lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int src_ratio, int dedup_tbl,
            const int32_t* __restrict__ sel, const int32_t* __restrict__ count,
            int32_t* __restrict__ phys, int32_t* __restrict__ count_l, int2* __restrict__ miss,
            int* __restrict__ miss_count, unsigned long long* __restrict__ stats,
@@ -105,6 +105,7 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
     int* nh = hit_time + G;      // [G]
     int* victim = nh + G;        // [G]
     int* flag = victim + G;      // [G]
+    int* first = flag + G;       // [dedup_tbl]: first list position of each mapped chunk
 
     const int tid = threadIdx.x;
     const int l = l0 + blockIdx.x / B;
@@ -135,15 +136,24 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
     if (ld.ratio == src_ratio) {
         m = m0;
     } else {
-        for (int p = tid; p < m0; p += blockDim.x) {
-            const int v = r[p];
-            int keep = 1;
-            for (int q = 0; q < p; ++q)
-                if (r[q] == v) {
-                    keep = 0;
-                    break;
-                }
-            mr[p] = keep;
+        if (cap <= dedup_tbl) {
+            // keep the first position of each mapped chunk: min position per chunk
+            for (int v = tid; v < cap; v += blockDim.x) first[v] = INT_MAX;
+            __syncthreads();
+            for (int p = tid; p < m0; p += blockDim.x) atomicMin(&first[r[p]], p);
+            __syncthreads();
+            for (int p = tid; p < m0; p += blockDim.x) mr[p] = first[r[p]] == p ? 1 : 0;
+        } else {
+            for (int p = tid; p < m0; p += blockDim.x) {
+                const int v = r[p];
+                int keep = 1;
+                for (int q = 0; q < p; ++q)
+                    if (r[q] == v) {
+                        keep = 0;
+                        break;
+                    }
+                mr[p] = keep;
+            }
         }
         __syncthreads();
         // stable compaction (read all, scan, then write)
@@ -359,17 +369,23 @@ size_t lru_smem_bytes(int S, int G) {
 }
 
 cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int S, int src_ratio,
-                       const int32_t* sel, const int32_t* count, int32_t* phys, int32_t* count_l,
-                       int2* miss, int* miss_count, unsigned long long* stats, uint32_t* err,
-                       cudaStream_t st) {
-    const size_t smem = lru_smem_bytes(S, G);
+                       long long max_dedup_cap, const int32_t* sel, const int32_t* count,
+                       int32_t* phys, int32_t* count_l, int2* miss, int* miss_count,
+                       unsigned long long* stats, uint32_t* err, cudaStream_t st) {
+    // a shared-memory table of first positions for layers whose ratio differs from
+    // src_ratio, when it fits; otherwise those layers fall back to pairwise checks
+    int tbl = 0;
+    if (max_dedup_cap > 0 &&
+        lru_smem_bytes(S, G) + sizeof(int) * (size_t)max_dedup_cap <= 227 * 1024)
+        tbl = (int)max_dedup_cap;
+    const size_t smem = lru_smem_bytes(S, G) + sizeof(int) * (size_t)tbl;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(lru_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
         if (e != cudaSuccess) return e;
     }
-    lru_kernel<<<nl * B, kLruThreads, smem, st>>>(layers, l0, B, G, S, src_ratio, sel, count, phys,
-                                                  count_l, miss, miss_count, stats, err);
+    lru_kernel<<<nl * B, kLruThreads, smem, st>>>(layers, l0, B, G, S, src_ratio, tbl, sel, count,
+                                                  phys, count_l, miss, miss_count, stats, err);
     return cudaGetLastError();
 }
 

@@ -80,6 +80,37 @@ __device__ void bitonic_sort_desc(unsigned long long* a, int m) {
     }
 }
 
+// Descending bitonic sort of one element per thread over the first m2 threads
+// (m2 a power of two <= blockDim.x); returns the element now at position tid.
+// Strides below a warp use shuffles, larger ones go through `xchg` in shared
+// memory. Threads past m2 sort their own padding. All threads must call it.
+__device__ unsigned long long reg_bitonic_desc(unsigned long long v, int m2, unsigned long long* xchg) {
+    const int tid = threadIdx.x;
+    for (int size = 2; size <= m2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            unsigned long long o;
+            if (stride >= 32) {
+                xchg[tid] = v;
+                __syncthreads();
+                o = xchg[tid ^ stride];
+                __syncthreads();
+            } else {
+                o = __shfl_xor_sync(0xffffffffu, v, stride);
+            }
+            const bool up = (tid & size) == 0;
+            const bool lower = (tid & stride) == 0;
+            v = (lower == up) ? (v > o ? v : o) : (v < o ? v : o);
+        }
+    }
+    return v;
+}
+
+__device__ __forceinline__ int pow2_at_least(int m) {
+    int m2 = 32;
+    while (m2 < m) m2 <<= 1;
+    return m2;
+}
+
 struct SelShared {
     uint32_t hist[kHistBins];
     int warp_buf[32];
@@ -122,8 +153,15 @@ select_kernel(const float* __restrict__ scores, int n, int mode, int k, float th
         __syncthreads();
         const int total = sh.n_cand;
         if (total <= clamp) {
-            bitonic_sort_desc(cand, total);
-            for (int i = tid; i < total; i += kSelThreads) sel_b[i] = (int32_t)(~(uint32_t)cand[i]);
+            if (total <= kSelThreads) {
+                unsigned long long v = tid < total ? cand[tid] : 0ull;
+                __syncthreads();
+                v = reg_bitonic_desc(v, pow2_at_least(total), outk);
+                if (tid < total) sel_b[tid] = (int32_t)(~(uint32_t)v);
+            } else {
+                bitonic_sort_desc(cand, total);
+                for (int i = tid; i < total; i += kSelThreads) sel_b[i] = (int32_t)(~(uint32_t)cand[i]);
+            }
             if (tid == 0) count[b] = total;
             return;
         }
@@ -214,6 +252,15 @@ select_kernel(const float* __restrict__ scores, int n, int mode, int k, float th
     // histogram from writing outside the arrays
     const int n_above = sh.n_out < K ? sh.n_out : K;
     const int n_cls = sh.n_cand < kCandCap ? sh.n_cand : kCandCap;
+    if (n_above + n_cls <= kSelThreads) {
+        // one register sort of everything at or above the class; keep the first K
+        unsigned long long v = tid < n_above ? outk[tid] : (tid < n_above + n_cls ? cand[tid - n_above] : 0ull);
+        __syncthreads();
+        v = reg_bitonic_desc(v, pow2_at_least(n_above + n_cls), outk);
+        if (tid < K) sel_b[tid] = (int32_t)(~(uint32_t)v);
+        if (tid == 0) count[b] = K;
+        return;
+    }
     bitonic_sort_desc(cand, n_cls);
     for (int i = tid; i < remaining && n_above + i < K; i += kSelThreads) outk[n_above + i] = cand[i];
     __syncthreads();

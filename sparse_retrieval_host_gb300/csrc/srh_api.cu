@@ -135,7 +135,7 @@ void plan_attention(srh_ctx* ctx, std::vector<AttnItem>* items) {
     }
     long long sr = (total + ctx->sm_count - 1) / ctx->sm_count;
     sr = ((sr + kAttnTile - 1) / kAttnTile) * kAttnTile;
-    sr = std::max<long long>(sr, 2 * kAttnTile);
+    sr = std::max<long long>(sr, kAttnTile);
     ctx->split_rows = (int)sr;
     ctx->item_begin.assign(ctx->L + 1, 0);
     for (int l = 0; l < ctx->L; ++l) {
@@ -393,8 +393,12 @@ int kvswap_stage(srh_ctx* ctx, int layer, const int32_t* d_sel, const int32_t* d
         for (uint8_t v : ctx->ready_host[l]) ready += v;
         ctx->resident_fill_bytes += ready * kKvDim * sizeof(float);
     }
-    cudaError_t e = launch_lru(ctx->d_layers, l0, nl, ctx->B, ctx->G, ctx->S, ctx->cfg.src_ratio, d_sel, d_count,
-                               d_phys, d_count_l, ctx->d_miss, ctx->d_miss_count, ctx->d_stats, ctx->d_err, sm);
+    long long dedup_cap = 0;
+    for (int l = l0; l < l0 + nl; ++l)
+        if (ctx->ratios[l] != ctx->cfg.src_ratio) dedup_cap = std::max(dedup_cap, ctx->caps[l]);
+    cudaError_t e = launch_lru(ctx->d_layers, l0, nl, ctx->B, ctx->G, ctx->S, ctx->cfg.src_ratio, dedup_cap,
+                               d_sel, d_count, d_phys, d_count_l, ctx->d_miss, ctx->d_miss_count, ctx->d_stats,
+                               ctx->d_err, sm);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "kvswap_stage LRU launch");
     if (ss && ss != sm) {
         SRH_CUDA(ctx, cudaEventRecord(ctx->ev_resolved, sm));
@@ -426,7 +430,7 @@ int lsa_attend(srh_ctx* ctx, int layer, const uint16_t* d_q, int n_heads, const 
         return fail(ctx, SRH_ERR_INVALID, "q/window/staging/out must be 16-byte aligned");
     const int i0 = layer < 0 ? 0 : ctx->item_begin[layer];
     const int i1 = layer < 0 ? ctx->n_items : ctx->item_begin[layer + 1];
-    const cudaError_t e = launch_attend(ctx->d_items, i0, i1 - i0, ctx->split_rows, n_heads, ctx->B, ctx->G,
+    const cudaError_t e = launch_attend(ctx->d_items, i0, i1 - i0, ctx->split_rows, n_heads, ctx->L, ctx->B, ctx->G,
                                         ctx->S, d_q, d_window, d_staging, d_phys, d_count_l, d_out,
                                         ctx->d_part_o, ctx->d_part_ml, ctx->d_attn_counter, ctx->d_err,
                                         (cudaStream_t)stream);

@@ -19,7 +19,7 @@ constexpr int kIdxDim = SRH_INDEXER_DIM;
 constexpr int kHistBins = 4096;        // score histogram: top 12 bits of the ordered key
 constexpr int kMaxSelect = 4096;       // largest S
 constexpr int kMaxGpuChunks = 4096;    // largest G
-constexpr int kAttnTile = 32;          // rows per attention tile
+constexpr int kAttnTile = 128;         // rows per attention tile
 
 // Bits of the sticky device error word.
 enum : uint32_t {
@@ -124,16 +124,16 @@ cudaError_t launch_select(const float* scores, int n, int B, int mode, int k, fl
                           int clamp, int S, const uint32_t* hist, int32_t* sel, int32_t* count,
                           cudaStream_t st);
 cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int S, int src_ratio,
-                       const int32_t* sel, const int32_t* count, int32_t* phys, int32_t* count_l,
-                       int2* miss, int* miss_count, unsigned long long* stats, uint32_t* err,
-                       cudaStream_t st);
+                       long long max_dedup_cap, const int32_t* sel, const int32_t* count,
+                       int32_t* phys, int32_t* count_l, int2* miss, int* miss_count,
+                       unsigned long long* stats, uint32_t* err, cudaStream_t st);
 cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, int S,
                           const int2* miss, const int* miss_count, float* staging,
                           uint32_t* err, int sm_count, cudaStream_t st);
 cudaError_t launch_resident_fill(const float* pool_dev, const uint8_t* ready, long long cap,
                                  int layer, int B, int G, float* staging, cudaStream_t st);
 cudaError_t launch_attend(const AttnItem* items, int item0, int n_items, int split_rows,
-                          int n_heads, int B, int G, int S, const uint16_t* q, const float* window,
+                          int n_heads, int L, int B, int G, int S, const uint16_t* q, const float* window,
                           const float* staging, const int32_t* phys, const int32_t* count_l,
                           float* out, float* part_o, float* part_ml, unsigned* counters,
                           uint32_t* err, cudaStream_t st);

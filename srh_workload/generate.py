@@ -155,11 +155,12 @@ def attn_q(w: Workload, step: int, layer: int, seq: int) -> np.ndarray:
 
 def _needle_plan(w: Workload, window_idx: int, seq: int):
     g = _rng(w, KIND_NEEDLES, window_idx, seq)
-    nd = np.sort(g.choice(w.n_chunks, size=w.n_needles, replace=False)).astype(np.int64)
+    n_nd = min(w.n_needles, w.n_chunks)
+    nd = np.sort(g.choice(w.n_chunks, size=n_nd, replace=False)).astype(np.int64)
     per_head = INDEXER_HEADS * SLOTS_PER_HEAD
     plan = np.empty((N_INDEXERS, INDEXER_HEADS, SLOTS_PER_HEAD), dtype=np.int64)
     for i in range(N_INDEXERS):
-        perm = g.permutation(w.n_needles)
+        perm = g.permutation(n_nd)
         # every needle appears in each indexer; extra slots wrap around the set
         take = np.resize(perm, per_head)
         plan[i] = nd[take].reshape(INDEXER_HEADS, SLOTS_PER_HEAD)

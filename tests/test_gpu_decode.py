@@ -31,7 +31,11 @@ def _run_decode(w, steps, attend_layers=None, pools=None):
         keys = fill(ds, w, pools)
         ora = make_oracle(w)
         spec = spec_of(w)
-        in_sync = True
+        # Exact slot/LRU comparisons need the same selection ORDER on both sides
+        # since the first step; the order of chunks whose scores differ by less
+        # than the fp32 scoring error is not unique, so once it differs only the
+        # order-free facts are compared (sets, staged rows, attention outputs).
+        order_sync = True
         worst = 0.0
         matched = 0
         hits = misses = 0
@@ -54,12 +58,16 @@ def _run_decode(w, steps, attend_layers=None, pools=None):
             same = True
             for b in range(w.batch):
                 same &= check_selection(w, ref.scores[b], ref.sel[b], sel[b, :cnt[b]], scores[b])
-            in_sync &= same
+                order_sync &= np.array_equal(sel[b, :cnt[b]], ref.sel[b])
+            order_sync &= same
             phys = ds.phys.cpu().numpy()
             cl = ds.count_l.cpu().numpy()
             for l in range(w.n_layers):
                 for b in range(w.batch):
-                    if in_sync:
+                    if same:
+                        assert sorted(ref.lists[l][b]) == sorted(
+                            set((sel[b, :cnt[b]].astype(np.int64) * 4 // w.layer_ratios[l]).tolist()))
+                    if order_sync:
                         assert cl[l, b] == len(ref.lists[l][b])
                         assert phys[l, b, :cl[l, b]].tolist() == ref.swap[l][b].phys, (t, l, b)
                         if ds.swap[l]:
@@ -74,13 +82,13 @@ def _run_decode(w, steps, attend_layers=None, pools=None):
                     lst = np.asarray(sorted(set(sel[b, :cnt[b]] * 4 // w.layer_ratios[l])), dtype=np.int64)
                     want_rows = rows_of(l, b, lst)
                     assert sorted(map(bytes, got)) == sorted(map(bytes, want_rows))
-            if in_sync:
+            if same:
                 matched += 1
                 out = ds.out.cpu().numpy()
                 for (l, b), r in ref.out.items():
                     _, rel = attn_err(out[l, b], r)
                     worst = max(worst, rel)
-        if matched == steps:
+        if order_sync:
             st = ds.stats()
             assert st["hits"] == hits and st["misses"] == misses
         assert ds.check_error() == 0

@@ -47,9 +47,18 @@ def test_fm_score_matches_oracle(w):
             ds.score(spec_of(w))
             got = ds.scores.double().cpu().numpy()
             for b in range(w.batch):
-                ref = O.score(keys[b], G.fm_queries(w, t, b), w.scale, [w.bias] * 3, w.ensemble)
-                err = np.abs(got[b] - ref).max()
-                assert err <= 1e-5, err
+                q = G.fm_queries(w, t, b)
+                ref = O.score(keys[b], q, w.scale, [w.bias] * 3, w.ensemble)
+                # a-priori bound of an fp32 dot product of 128 terms in any order
+                # (unit roundoff 2^-23 allows truncating adders), then scale, bias
+                # and the ensemble in fp32
+                absdot = np.abs(O.bf16_to_f64(keys[b])) @ np.abs(O.bf16_to_f64(q)).reshape(24, 128).T
+                bound = (w.scale * 128 * 2.0 ** -23 * absdot.max(axis=1)
+                         + 8 * 2.0 ** -24 * (np.abs(ref) + abs(w.bias)))
+                err = np.abs(got[b] - ref)
+                assert np.all(err <= bound), (err.max(), bound[err.argmax()])
+                if len(err) >= 100:
+                    assert np.median(err) <= 1e-6
     finally:
         ds.close()
 
