@@ -210,6 +210,46 @@ int fm_select(srh_ctx* ctx, const float* d_scores, int n, int mode, int k, float
               int32_t* d_sel, int32_t* d_count, srh_stream_t stream);
 
 /*
+ * fm_select without a context and without any device allocation. The pages
+ * have no counterpart: this is a library entry point for callers that may not
+ * allocate GPU memory themselves -- an engine that has already reserved the
+ * whole device for its own pool (a stray cudaMalloc would fail or fragment it),
+ * or code on a latency-critical path where cudaMalloc/cudaFree would stall
+ * other streams by synchronizing the device. Creating an srh_ctx allocates, so
+ * such a caller uses this instead of fm_select.
+ *
+ * It computes exactly what fm_select computes (same kernels, same results).
+ * The caller owns every input and output buffer; the only scratch is the
+ * per-sequence first-digit histogram, held in a fixed array compiled into the
+ * library: SRH_NOALLOC_MAX_BATCH x 4096 uint32 (1 MiB). Every GPU that loads
+ * the library keeps that array until the process exits.
+ *
+ *   d_scores   [batch][n] fp32 (device)
+ *   batch      1 .. SRH_NOALLOC_MAX_BATCH; larger values are rejected with
+ *              SRH_ERR_INVALID before any GPU work
+ *   n          1 .. SRH_NOALLOC_MAX_N
+ *   mode, k, tau, clamp   as for fm_select; k and clamp must be <= max_select
+ *   max_select row stride of d_sel, 1 .. 4096
+ *   d_sel      [batch][max_select] int32 output, d_count [batch] int32 output
+ *   err, err_len  optional (may be NULL/0): receives a NUL-terminated message
+ *              when the call fails
+ * Returns SRH_OK, SRH_ERR_INVALID or SRH_ERR_CUDA.
+ *
+ * The first call on each device looks up the device address of the scratch
+ * array on the current device; make that first call before any stream capture
+ * begins. Every call on a device shares the one array, and the array keeps the
+ * last call's histogram (each call clears it first on its stream). Calls whose
+ * GPU work overlaps -- on different streams, or from threads that do not order
+ * them -- race on the array and may return wrong selections: order them on
+ * one stream.
+ */
+#define SRH_NOALLOC_MAX_BATCH 64
+#define SRH_NOALLOC_MAX_N (1 << 30)
+int fm_select_noalloc(const float* d_scores, int batch, int n, int mode, int k, float tau, int clamp,
+                      int max_select, int32_t* d_sel, int32_t* d_count, srh_stream_t stream, char* err,
+                      size_t err_len);
+
+/*
  * a4+a5: KV_SWAP staging ([P1] KV_SWAP 实现细节, Swap-in flow).
  *   layer      one sparse layer, or -1 for all layers
  *   d_sel, d_count  the fm_select outputs ([batch][S], [batch])

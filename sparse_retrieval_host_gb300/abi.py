@@ -31,6 +31,8 @@ SRH_SELECT_THRESH = 1
 SRH_FLAG_TEST_FAIL_HOST_ALLOC = 1
 KV_DIM = 512
 WINDOW = 128
+SRH_NOALLOC_MAX_BATCH = 64
+SRH_NOALLOC_MAX_N = 1 << 30
 
 
 class SrhConfig(ctypes.Structure):
@@ -90,6 +92,7 @@ SIGNATURES = [
     ("srh_max_select", _i, [_vp]),
     ("fm_score", _i, [_vp, _vp, _i, _vp, _f, ctypes.POINTER(_f), _i, _vp, _vp]),
     ("fm_select", _i, [_vp, _vp, _i, _i, _i, _f, _i, _vp, _vp, _vp]),
+    ("fm_select_noalloc", _i, [_vp, _i, _i, _i, _i, _f, _i, _i, _vp, _vp, _vp, ctypes.c_char_p, ctypes.c_size_t]),
     ("kvswap_stage", _i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     ("lsa_attend", _i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp]),
     ("srh_get_stats", _i, [_vp, ctypes.POINTER(SrhStats)]),
@@ -208,6 +211,16 @@ def fm_score(ctx, keys, n, q, scale, bias3, ensemble, scores, stream=None) -> No
 def fm_select(ctx, scores, n, mode, k, tau, clamp, sel, count, stream=None) -> None:
     _check(load().fm_select(ctx, _ptr(scores), n, mode, k, float(tau), clamp, _ptr(sel), _ptr(count),
                             _stream(stream)), "fm_select", ctx)
+
+
+def fm_select_noalloc(scores, batch, n, mode, k, tau, clamp, max_select, sel, count, stream=None) -> None:
+    """fm_select with no context and no device allocation (scratch is a fixed
+    array inside the library; see include/srh.h for the limits and sharing)."""
+    buf = ctypes.create_string_buffer(256)
+    rc = load().fm_select_noalloc(_ptr(scores), batch, n, mode, k, float(tau), clamp, max_select, _ptr(sel),
+                                  _ptr(count), _stream(stream), buf, len(buf))
+    if rc != SRH_OK:
+        raise SrhError(rc, "fm_select_noalloc", buf.value.decode(errors="replace"))
 
 
 def kvswap_stage(ctx, layer, sel, count, staging, phys, count_l, main=None, side=None) -> None:
