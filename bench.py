@@ -9,9 +9,11 @@ HBM. Prints ONE JSON line on rank 0.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config ctx8k]
   python bench.py --impl reference ...   # the fp64 CPU oracle, timed on the host
 
-Timing: W warm-up steps, then K timed steps; the L2 is flushed (a 256 MiB
-write) before every timed step and each step is bracketed by CUDA events on
-its stream, so the flush is outside the timed spans. Multi-GPU (N > 1 under
+Timing: W warm-up steps, then K timed steps; the L2 is flushed before every
+timed step (a 256 MiB buffer is written, then read back, so the L2 holds only
+clean lines of it and the timed kernels pay no write-back of the flush), and
+each step is bracketed by CUDA events on its stream, so the flush is outside
+the timed spans. Multi-GPU (N > 1 under
 torchrun) runs N independent replicas (weak scaling, no collective on the
 data path); value = steps of all ranks / the slowest rank's time.
 """
@@ -35,7 +37,7 @@ import numpy as np  # noqa: E402
 from srh_workload import configs as C  # noqa: E402
 from srh_workload import generate as G  # noqa: E402
 
-KERNELS_PER_STEP = 5          # score, select, lru, gather, attend
+BASE_KERNELS = 5              # score, select, lru, gather, attend (+ merge when a layer has splits)
 Q_CYCLE = 16                  # distinct attention-query sets cycled through the steps
 FLUSH_BYTES = 256 << 20       # > 2x the 126 MiB L2
 METRIC = "decode steps/s"
@@ -193,6 +195,15 @@ def attn_bytes(w, count_l):
     return int(rows) * C.KV_DIM * 4 + w.n_layers * w.batch * w.n_heads * C.KV_DIM * (2 + 4)
 
 
+def launches_per_step(w, sm_count):
+    """Our kernels per step. lsa_attend adds its merge kernel when some layer's
+    rows are cut into more than one split; the split rule is the planner's
+    (split rows = rows of all layers / SM count, rounded up to 128)."""
+    rows = [C.WINDOW + min(w.clamp, -(-w.context_len // r)) for r in w.layer_ratios]
+    split = max(128, -(-(-(-w.batch * sum(rows) // sm_count)) // 128) * 128)
+    return BASE_KERNELS + (1 if any(-(-r // split) > 1 for r in rows) else 0)
+
+
 def score_bytes(w):
     return w.batch * w.n_chunks * (C.INDEXER_DIM * 2 + 4)
 
@@ -209,47 +220,67 @@ def run_ours(args, dist, rank, world, local):
     stream = torch.cuda.current_stream()
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
-    def do_step(t):
-        ds.step(spec, stream, fm_q=fm_q_all[(t % w.steps) // w.lookahead],
-                q=q_all[t % q_all.shape[0]])
+    def bind(t):
+        # the step's inputs into the buffers the graphs read (outside the timed span)
+        ds.fm_q.copy_(fm_q_all[(t % w.steps) // w.lookahead])
+        ds.q.copy_(q_all[t % q_all.shape[0]])
+
+    def flush_l2():
+        flush.zero_()
+        flush.sum()
 
     for t in range(args.warmup):
-        do_step(t)
+        bind(t)
+        ds.step(spec, stream)
     torch.cuda.synchronize()
     assert ds.check_error() == 0, "device error during warm-up"
+    (graph,) = ds.capture(spec)
+    parts = ds.capture(spec, parts=True)
     ds.reset_stats()
 
+    # headline: K steps, each one graph launch, timed on the stream
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    counts = []
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     with ClockSampler(local) as clk:
         for i in range(K):
-            t = args.warmup + i
-            flush.zero_()
-            e0, e1, e2, e3 = ev[i]
-            e0.record(stream)
-            ds.score(spec, stream, fm_q_all[(t % w.steps) // w.lookahead])
-            e1.record(stream)
-            ds.select(spec, stream)
-            ds.stage(-1, stream)
-            e2.record(stream)
-            ds.attend(-1, stream, q_all[t % q_all.shape[0]])
-            e3.record(stream)
-            e3.synchronize()
-            counts.append(ds.count_l.cpu().numpy().copy())
-    torch.cuda.synchronize()
+            bind(args.warmup + i)
+            flush_l2()
+            ev[i][0].record(stream)
+            graph.replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     assert ds.check_error() == 0, "device error during the timed steps"
-    step_ms = [ev[i][0].elapsed_time(ev[i][3]) for i in range(K)]
-    score_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    attn_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    st = ds.stats()
+
+    # breakdown: the same steps as three graphs with events between the phases
+    KB = min(K, 20)
+    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(KB)]
+    counts = []
+    for i in range(KB):
+        bind(args.warmup + K + i)
+        flush_l2()
+        e0, e1, e2, e3 = evb[i]
+        e0.record(stream)
+        parts[0].replay()
+        e1.record(stream)
+        parts[1].replay()
+        e2.record(stream)
+        parts[2].replay()
+        e3.record(stream)
+        e3.synchronize()
+        counts.append(ds.count_l.cpu().numpy().copy())
+    assert ds.check_error() == 0, "device error during the breakdown steps"
+    score_ms = [e[0].elapsed_time(e[1]) for e in evb]
+    stage_ms = [e[1].elapsed_time(e[2]) for e in evb]
+    attn_ms = [e[2].elapsed_time(e[3]) for e in evb]
     local_s = sum(step_ms) / 1e3
     tot_s, tot_steps = aggregate(dist, local_s, K, device)
-    st = ds.stats()
 
     result = None
     if rank == 0:
@@ -272,7 +303,7 @@ def run_ours(args, dist, rank, world, local):
             "scaling": "weak",
             "vs_baseline": None,
             "dtype": "f32",
-            "precision": "bf16 keys/queries, f32 latents; tf32 attention MMA operands, f32 accumulate",
+            "precision": "bf16 keys/queries, f32 latents; fp16 attention MMA operands (tcgen05 kind::f16), f32 accumulate",
             "data": "synthetic (seeded PCG64; shapes of the pages' workloads)",
             "config": {
                 "workload": w.name, "context_len": w.context_len,
@@ -282,12 +313,12 @@ def run_ours(args, dist, rank, world, local):
                 "select": "topk" if w.select_mode == C.SELECT_TOPK else f"threshold tau={w.tau}",
                 "ensemble": "max" if w.ensemble == C.ENSEMBLE_MAX else "mean",
                 "heads": w.n_heads, "batch": w.batch, "lookahead": w.lookahead,
-                "l2": "flushed before every timed step (256 MiB write, outside the timed span)",
+                "l2": "flushed before every timed step (256 MiB written then read back, outside the timed span)",
                 "parallelism": f"replicas x{world}",
             },
-            "gpu_launches": KERNELS_PER_STEP * K,
+            "gpu_launches": launches_per_step(w, torch.cuda.get_device_properties(device).multi_processor_count) * K,
             "roofline": {
-                "kernel": "attend_kernel (lsa_attend)",
+                "kernel": "lsa_attend (attend_tc_kernel + merge_kernel)",
                 "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind,
                 "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
@@ -295,9 +326,9 @@ def run_ours(args, dist, rank, world, local):
                 "avg_launch_us": a_avg_ms * 1e3,
             },
             "kernels_us": {"fm_score": statistics.mean(score_ms) * 1e3,
-                           "fm_select+kvswap_stage": statistics.mean(
-                               [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]) * 1e3,
-                           "lsa_attend": a_avg_ms * 1e3},
+                           "fm_select+kvswap_stage": statistics.mean(stage_ms) * 1e3,
+                           "lsa_attend": a_avg_ms * 1e3,
+                           "note": f"phase spans of {KB} further steps replayed as three graphs"},
             "score_gbs": score_bytes(w) / (statistics.mean(score_ms) / 1e3) / 1e9,
             "step_hbm_gbs": step_bytes / (statistics.mean(step_ms) / 1e3) / 1e9,
             "lru_hit_rate": (st["hits"] / sel_total) if sel_total else None,
@@ -308,17 +339,18 @@ def run_ours(args, dist, rank, world, local):
         clk_sum = clk.summary()
         result["clocks"] = clk_sum
     if not args.no_e2e:
-        e2e = run_e2e(args, w, ds, spec, device)
+        e2e = run_e2e(args, w, ds, spec, graph)
         if result is not None:
             result["e2e"] = e2e
     ds.close()
     return result
 
 
-def run_e2e(args, w, ds, spec, device):
+def run_e2e(args, w, ds, spec, graph):
     """Same steps through the public API with host buffers: every step copies its
-    queries H2D from pinned memory and reads the attention output and the
-    selection back D2H, inside the timed region."""
+    queries H2D from pinned memory into the bound input buffers, replays the
+    captured step and reads the attention output and the selection back D2H,
+    all inside the timed region."""
     import torch
     from sparse_retrieval_host_gb300.runtime import bits_to_i16
     stream = torch.cuda.current_stream()
@@ -338,7 +370,7 @@ def run_e2e(args, w, ds, spec, device):
         t = args.warmup + args.steps + i
         ds.fm_q.copy_(h_fmq[(t % w.steps) // w.lookahead], non_blocking=True)
         ds.q.copy_(h_q[t % nq], non_blocking=True)
-        ds.step(spec, stream)
+        graph.replay()
         h_out.copy_(ds.out, non_blocking=True)
         h_sel.copy_(ds.sel, non_blocking=True)
         h_cnt.copy_(ds.count, non_blocking=True)

@@ -1,4 +1,4 @@
-// K-attend + K-combine: split-K flash-decode on the 5th-generation tensor cores.
+// K-attend + K-merge: split-K flash-decode on the 5th-generation tensor cores.
 //
 // PocketLLM "FlashMemory 1M 上下文显存优化使用文档", section 技术细节 / 架构概览,
 // per-layer box step 3 (indexed_cached_attention over window + selected rows)
@@ -10,41 +10,35 @@
 // Work: the rows of one (layer, sequence) -- the 128 window rows, then the
 // layer's staged rows in selection order -- are cut into fixed splits of
 // `split_rows` (a multiple of 128); one CTA runs one split for all heads, in
-// tiles of 128 rows. Per tile:
-//   pass 1  S^T[r, h] = E[r, :] . Q[h, :]   (M = 128 rows, N = heads, K = 512)
-//           over 8 pieces [128 rows x 64 d];
-//   softmax (4 warps, one TMEM lane = one row): base-2 online softmax with a
+// tiles of 128 rows. Each row is read from HBM once per step:
+//   load    all 8 warps stream the tile's fp32 rows (warp w: rows 16w..16w+15,
+//           whole 2 KiB rows, 512 contiguous bytes per load instruction) into
+//           registers, convert to fp16 and store them into one resident
+//           128B-swizzled tile E [128 rows x 512 d] (8 d-blocks of 64);
+//   pass 1  S^T[r, h] = E[r, :] . Q[h, :]   (M = 128 rows, N = heads, K = 512),
+//           E and Q K-major;
+//   softmax (warps 0-3, one TMEM lane = one row): base-2 online softmax with a
 //           lazily moved reference max per head (moved only when the tile max
 //           exceeds it by 2^8), warp butterfly transpose-reductions for the
 //           per-head max and sum; P written as fp16 [rows x heads];
-//   pass 2  O^T[d, h] += E^T[d, r] P[r, h]   (M = 128 d, N = heads, K = rows)
-//           over 8 pieces [64 rows x 128 d]; the tile's rows are read a second
-//           time, from L2.
-// Both products run as tcgen05 kind::f16 MMAs with fp32 accumulation in TMEM.
-// The fp32 rows are gathered by bulk copies into a landing ring, then
-// converted to fp16 into a 128B-swizzled operand ring (K-major for pass 1,
-// MN-major for pass 2: 32-bit operands must be K-major, and pass 2 contracts
-// over rows). fp16 keeps 11 significant bits, as tf32 does; the latents are
-// O(1), p <= 2^8 by construction, and bf16 queries of normal fp16 range
-// convert exactly.
+//   pass 2  O^T[d, h] += E^T[d, r] P[r, h]   (M = 128 d, N = heads, K = rows),
+//           the SAME smem tile read MN-major (a 128B-swizzled atom of 8 rows x
+//           64 d serves both views), so no row is fetched twice.
+// Both products are tcgen05 kind::f16 MMAs with fp32 accumulation in TMEM,
+// issued by thread 0. fp16 keeps 11 significant bits, as tf32 does; 32-bit
+// operands cannot be MN-major, which pass 2 needs. The latents are O(1),
+// p <= 2^8 by construction, and bf16 queries of normal fp16 range convert
+// exactly.
 //
-// Roles: warps 4-7 only issue the gathers: one 256-byte bulk copy (TMA) per
-// thread and piece, counted on the piece's mbarrier as transaction bytes, so
-// they never wait on their own copies. Warps 0-3 convert landed pieces, run the softmax (TMEM lanes
-// 0-127) and write the output with warps 4-7; they issue no copies, so the
-// proxy fence that publishes each converted piece to the tensor core stays
-// cheap. Warp 0 allocates TMEM and its lane 0 issues the MMAs, each piece as
-// soon as all four converter warps have published it. Every wait is bounded;
-// on a timeout the CTA records kErrTimeout, drains its copies and MMAs, frees
-// TMEM and returns.
+// With more than one tile per split, warps 4-7 issue the loads of the next
+// tile while warps 0-3 run the softmax; every warp waits for the previous
+// tile's pass 2 before it overwrites E. Every wait is bounded; on a timeout
+// the CTA records kErrTimeout, drains its MMAs, frees TMEM and returns.
 //
-// A split writes (m, l, O) partials; the last CTA of a (layer, sequence) to
-// finish (an atomic ticket, no waiting) merges them in split order. The split
-// layout depends only on the row count, so identical rows give identical bits
-// whatever slots hold them.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
+// A multi-split (layer, sequence) writes (m, l, O) partials per split; a
+// second kernel merges them in split order. The split layout depends only on
+// the row count, so identical rows give identical bits whatever slots hold
+// them.
 #include <cmath>
 
 #include "srh_internal.cuh"
@@ -55,41 +49,30 @@ namespace {
 
 using namespace umma;
 
-constexpr int kTileRows = kAttnTile;    // 128
-constexpr int kSoftWarps = 4;
-constexpr int kLoadWarps = 4;
-constexpr int kThreads = (kSoftWarps + kLoadWarps) * 32;   // 256: two warps per SM sub-partition
-constexpr int kLoads = 16;                                  // landing loads per tile (8 per pass)
-constexpr int kNLand = 3;                                   // fp32 landing slots
-constexpr int kNOp = 3;                                     // fp16 operand slots (shared with the MMA)
-constexpr int kLand = 32768;                                // [128 rows x 64 d] or [64 rows x 128 d] fp32
-constexpr int kOp = 16384;                                  // the same piece in fp16
-constexpr int kOffQ = 0;                                    // 8 K-blocks [64 heads x 64 d] fp16
-constexpr int kOffLand = kOffQ + 8 * 8192;
-constexpr int kOffOp = kOffLand + kNLand * kLand;
-constexpr int kOffP = kOffOp + kNOp * kOp;                  // fp16 [128 rows x 64 heads]
+constexpr int kTileRows = kAttnTile;                // 128
+constexpr int kThreads = 256;                       // 8 warps
+constexpr int kSoftThreads = 128;                   // warps 0-3: softmax, TMEM lanes 0-127
+constexpr int kOffQ = 0;                            // 8 d-blocks x 8 KB: fp16 Q, K-major, row h
+constexpr int kDBlockE = kTileRows * 128;           // 16 KB: one d-block of E
+constexpr int kOffE = kOffQ + 8 * 8192;             // 8 d-blocks: fp16 E, row r
+constexpr int kOffP = kOffE + 8 * kDBlockE;         // fp16 P [128 rows x 64 heads], heads contiguous
 constexpr int kOffMisc = kOffP + kTileRows * 128;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;                               // S^T: 64 columns
-constexpr uint32_t kColO = 64;                              // O^T[mb]: 64 columns each
-constexpr float kLazy = 8.0f;                               // reference max moves past 2^8 growth
+constexpr uint32_t kColS = 0;                       // S^T: up to 64 columns
+constexpr uint32_t kColO = 64;                      // O^T[mb]: 64 columns each
+constexpr float kLazy = 8.0f;                       // reference max moves past 2^8 growth
 constexpr int kMaxSplits = (kWindow + kMaxSelect + kTileRows - 1) / kTileRows;
 
 struct Misc {
-    uint64_t lfull[kNLand];
-    uint64_t lempty[kNLand];
-    uint64_t opfull[kNOp];
-    uint64_t opempty[kNOp];
-    uint64_t s_full, p_full, o_full, drain;
+    uint64_t s_full, o_full, drain;
     uint32_t tmem_base;
-    uint32_t ticket;
     int abort;
     int rescale;
     int epi_ok;
     float m_used[64];
     float l_run[64];
     float alpha[64];        // per-tile rescale factors; 1 / l after the last tile
-    float red[kSoftWarps][64];
+    float red[4][64];
 };
 constexpr int kSmemBytes = kOffMisc + (int)sizeof(Misc) + 1024;   // + base alignment slack
 static_assert(kSmemBytes <= 232448, "attention shared memory exceeds 227 KB");
@@ -99,12 +82,6 @@ __host__ __device__ constexpr uint32_t idesc_f16(int a_mn, int b_mn, int n) {
     return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(n >> 3) << 17) |
            ((uint32_t)(128 >> 4) << 24);
 }
-
-// Gather maps: window [L*B*128 rows][512] and staging [L*B*G rows][512] fp32,
-// each with a 64- and a 128-column box one row high.
-struct AttnMaps {
-    CUtensorMap win64, win128, stg64, stg128;
-};
 
 struct AttnArgs {
     const AttnItem* items;
@@ -119,12 +96,11 @@ struct AttnArgs {
     float* out;
     float* part_o;
     float* part_ml;
-    unsigned* counters;
     uint32_t* err;
     float sl2;   // log2(e) / sqrt(kv_dim)
 };
 
-// Bounded wait that also gives up when another role has aborted the CTA.
+// Bounded wait that also gives up when another thread has aborted the CTA.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
                                               uint32_t* err) {
     for (uint32_t i = 0; i < (1u << 26); ++i) {
@@ -161,6 +137,15 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return r;
 }
 
+// Read-only streaming load of 16 bytes (no L1 allocation).
+__device__ __forceinline__ float4 ldg_stream(const float4* p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 // Max / sum over the 32 lanes of a warp for 32 per-lane values at once: after
 // the call, lane l holds the reduction of column l. Each step hands half of
 // the columns to the partner lane, so 31 shuffles do all 32 reductions.
@@ -183,8 +168,7 @@ __device__ __forceinline__ float butterfly32(float (&v)[32], int lane) {
 }
 
 template <int H>
-__global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_constant__ AttnArgs a,
-                                                                 const __grid_constant__ AttnMaps maps) {
+__global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_constant__ AttnArgs a) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     Misc& ms = *reinterpret_cast<Misc*>(sm + kOffMisc);
@@ -207,16 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
 
     // ---------------------------------------------------------------- set-up
     if (tid == 0) {
-        for (int s = 0; s < kNLand; ++s) {
-            mbar_init(&ms.lfull[s], 1);
-            mbar_init(&ms.lempty[s], kSoftWarps * 32);
-        }
-        for (int s = 0; s < kNOp; ++s) {
-            mbar_init(&ms.opfull[s], kSoftWarps * 32);
-            mbar_init(&ms.opempty[s], 1);
-        }
         mbar_init(&ms.s_full, 1);
-        mbar_init(&ms.p_full, kSoftWarps * 32);
         mbar_init(&ms.o_full, 1);
         mbar_init(&ms.drain, 1);
         ms.abort = 0;
@@ -230,295 +205,233 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         ms.alpha[tid] = 1.f;
     }
     if (warp == 0 && n_tiles > 0) tmem_alloc(&ms.tmem_base, kTmemCols);
-    if (n_tiles > 0) {
-        // queries: bf16 [H][512] -> fp16 K-major; K-block d / 64 at (d / 64) * 8192, row h.
-        // All loads first, then the conversions.
-        constexpr int kPer = H * 64 / kThreads;          // 16-byte chunks per thread
-        const uint16_t* qg = a.q + lb * H * kKvDim;
-        uint4 qv[kPer];
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int i = tid + k * kThreads;
-            qv[k] = *reinterpret_cast<const uint4*>(qg + (i >> 6) * kKvDim + (i & 63) * 8);
-        }
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int i = tid + k * kThreads, h = i >> 6, c8 = i & 63;
-            const uint4 v = qv[k];
-            uint4 w;
-            w.x = pack_f16x2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
-            w.y = pack_f16x2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
-            w.z = pack_f16x2(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u));
-            w.w = pack_f16x2(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
-            *reinterpret_cast<uint4*>(sm + kOffQ + (c8 >> 3) * 8192 + sw128(h, c8 & 7)) = w;
-        }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = ms.tmem_base;
 
-    if (n_tiles > 0 && warp == kSoftWarps) {
-        // ------------------------------------------------------------ loader warp
-        // Load g (g = 16 * tile + x) lands in landing slot g % 3. x < 8: pass-1
-        // piece of d-block x, [128 rows x 64 d], as 32 gathers of 4 rows; x >= 8:
-        // pass-2 piece y = x - 8, [64 rows x 128 d] of rows 64 (y >> 2).. and
-        // columns 128 (y & 3).., as 16 gathers. Lane j owns tile rows 4j..4j+3.
-        // Tile 0 is the window; later tiles are staged rows. Rows past the
-        // split end repeat its last row (finite data the softmax masks).
-        bool ok = true;
-        int g = 0;
-        const uint64_t lb_rows_win = lb * kWindow;
-        const uint64_t lb_rows_stg = lb * (uint64_t)a.G;
-        for (int tile = 0; tile < n_tiles && ok; ++tile) {
-            const int tr0 = row0 + tile * kTileRows;
-            int rq[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int row = min(tr0 + 4 * lane + k, row1 - 1);   // row1 > tr0 for every tile
-                if (row < kWindow) {
-                    rq[k] = (int)(lb_rows_win + row);
-                } else {
-                    int slot = ph[row - kWindow] - kWindow;
-                    if (slot < 0 || slot >= a.G) {
-                        atomicOr(a.err, kErrBounds);
-                        slot = 0;
-                    }
-                    rq[k] = (int)(lb_rows_stg + slot);
-                }
-            }
-            const bool in_win = tr0 < kWindow;          // tile 0: window rows only (tiles are 128 = W)
-            const void* m64 = in_win ? (const void*)&maps.win64 : (const void*)&maps.stg64;
-            const void* m128 = in_win ? (const void*)&maps.win128 : (const void*)&maps.stg128;
-            for (int x = 0; x < kLoads; ++x) {
-                const int ls = g % kNLand;
-                if (!wait_or_abort(&ms.lempty[ls], ((g / kNLand) & 1) ^ 1, abort, a.err)) { ok = false; break; }
-                if (lane == 0) mbar_arrive_expect_tx(&ms.lfull[ls], kLand);
-                __syncwarp();
-                const uint32_t land = smem_u32(sm + kOffLand + ls * kLand);
-                if (x < 8) {
-                    tma_gather4(land + lane * 1024, m64, 64 * x, rq[0], rq[1], rq[2], rq[3], &ms.lfull[ls]);
-                } else {
-                    const int y = x - 8, src = 16 * (y >> 2) + (lane & 15);
-                    const int q0 = __shfl_sync(0xffffffffu, rq[0], src), q1 = __shfl_sync(0xffffffffu, rq[1], src);
-                    const int q2 = __shfl_sync(0xffffffffu, rq[2], src), q3 = __shfl_sync(0xffffffffu, rq[3], src);
-                    if (lane < 16) tma_gather4(land + lane * 2048, m128, 128 * (y & 3), q0, q1, q2, q3, &ms.lfull[ls]);
-                }
-                ++g;
-            }
+    // Source of tile row tr: window rows first, then the staged rows in list
+    // order; rows past the split end repeat its last row (finite data that the
+    // softmax masks).
+    auto row_src = [&](int tr0, int tr) -> const float4* {
+        const int row = min(tr0 + tr, row1 - 1);
+        if (row < kWindow) return reinterpret_cast<const float4*>(a.window + (lb * kWindow + row) * kKvDim);
+        int slot = ph[row - kWindow] - kWindow;
+        if (slot < 0 || slot >= a.G) {
+            atomicOr(a.err, kErrBounds);
+            slot = 0;
         }
-        // after an abort, wait (bounded) for the copies of the last pieces issued
-        if (!ok && lane == 0)
-            for (int k = g > kNLand ? g - kNLand : 0; k < g; ++k)
-                mbar_wait(&ms.lfull[k % kNLand], (k / kNLand) & 1, 1u << 20);
-        __syncwarp();
-    } else if (n_tiles > 0 && warp > kSoftWarps) {
-        // warps 5-7 join for the output
-    } else if (n_tiles > 0) {
-        // ------------------------------------------------------------ converters + MMA issue
-        constexpr uint32_t id1 = idesc_f16(0, 0, H);   // pass 1: K-major E and Q
-        constexpr uint32_t id2 = idesc_f16(1, 1, H);   // pass 2: MN-major E^T and P
-        bool cv_ok = true;
-        int g = 0;                                       // pieces converted (all four warps in step)
-        // convert landed piece g into operand slot g % 3 (this thread's 16 units)
-        auto convert = [&]() {
-            const int x = g & 15, ls = g % kNLand, s = g % kNOp;
-            if (!wait_or_abort(&ms.lfull[ls], (g / kNLand) & 1, abort, a.err) ||
-                !wait_or_abort(&ms.opempty[s], ((g / kNOp) & 1) ^ 1, abort, a.err)) {
-                cv_ok = false;
-                return;
-            }
-            const unsigned char* land = sm + kOffLand + ls * kLand;
-            unsigned char* op = sm + kOffOp + s * kOp;
-            const int u = tid;                           // unit owner index, 0..127
-            if (x < 8) {
-                // K-major [128 rows x 64 d] fp16: row r, 16-byte chunk d4 >> 1, half d4 & 1
-                const int d4 = u & 15;
+        return reinterpret_cast<const float4*>(a.staging + (lb * (size_t)a.G + slot) * kKvDim);
+    };
+    // Four rows of this warp: lane holds float4 lane + 32 j of each (d = 4 (lane + 32 j)).
+    auto load4 = [&](float4 (&v)[4][4], int tr0, int rbase) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float4 f = *reinterpret_cast<const float4*>(land + 16 * u + 2048 * i);
-                    const int r = (u >> 4) + 8 * i;
-                    *reinterpret_cast<uint2*>(op + sw128(r, d4 >> 1) + 8 * (d4 & 1)) =
-                        make_uint2(pack_f16x2(f.x, f.y), pack_f16x2(f.z, f.w));
-                }
-            } else {
-                // MN-major [64 rows x 128 d] fp16: atom d4 >> 4 (64 d) at 8 KB, row r, chunk (d4 & 15) >> 1
-                const int d4 = u & 31;
+        for (int i = 0; i < 4; ++i) {
+            const float4* src = row_src(tr0, rbase + i);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float4 f = *reinterpret_cast<const float4*>(land + 16 * u + 2048 * i);
-                    const int r = (u >> 5) + 4 * i;
-                    *reinterpret_cast<uint2*>(op + (d4 >> 4) * 8192 + sw128(r, (d4 & 15) >> 1) + 8 * (d4 & 1)) =
-                        make_uint2(pack_f16x2(f.x, f.y), pack_f16x2(f.z, f.w));
+            for (int j = 0; j < 4; ++j) v[i][j] = ldg_stream(src + lane + 32 * j);
+        }
+    };
+    // ... as fp16 into E: d-block (lane >> 4) + 2 j, 16-byte chunk (lane & 15) >> 1, half lane & 1.
+    auto store4 = [&](const float4 (&v)[4][4], int rbase) {
+        unsigned char* e = sm + kOffE + (lane >> 4) * kDBlockE + 8 * (lane & 1);
+        const int chunk = (lane & 15) >> 1;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint2*>(e + 2 * j * kDBlockE + sw128(rbase + i, chunk)) =
+                    make_uint2(pack_f16x2(v[i][j].x, v[i][j].y), pack_f16x2(v[i][j].z, v[i][j].w));
+    };
+
+    constexpr uint32_t id1 = idesc_f16(0, 0, H);   // pass 1: K-major E and Q
+    constexpr uint32_t id2 = idesc_f16(1, 1, H);   // pass 2: MN-major E^T and P
+    const int rw = 16 * warp;                       // this warp's first tile row
+    bool ok = true;
+
+    for (int tile = 0; tile < n_tiles; ++tile) {
+        // ------------------------------------------------------------ load E (all warps)
+        const int tr0 = row0 + tile * kTileRows;
+        float4 b0[4][4], b1[4][4];
+        if (ok) {
+            if (tile == 0) {
+                // queries: bf16 [H][512] -> fp16 K-major; d-block d / 64 at (d / 64) * 8192, row h
+                constexpr int kPer = H * 64 / kThreads;          // 16-byte chunks per thread
+                const uint16_t* qg = a.q + lb * H * kKvDim;
+                uint4 qv[kPer];
+#pragma unroll
+                for (int k = 0; k < kPer; ++k) {
+                    const int i = tid + k * kThreads;
+                    qv[k] = *reinterpret_cast<const uint4*>(qg + (i >> 6) * kKvDim + (i & 63) * 8);
+                }
+#pragma unroll
+                for (int k = 0; k < kPer; ++k) {
+                    const int i = tid + k * kThreads, h = i >> 6, c8 = i & 63;
+                    const uint4 v = qv[k];
+                    uint4 w;
+                    w.x = pack_f16x2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
+                    w.y = pack_f16x2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+                    w.z = pack_f16x2(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u));
+                    w.w = pack_f16x2(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
+                    *reinterpret_cast<uint4*>(sm + kOffQ + (c8 >> 3) * 8192 + sw128(h, c8 & 7)) = w;
                 }
             }
-            mbar_arrive(&ms.lempty[ls]);
-            fence_async_smem();
-            mbar_arrive(&ms.opfull[s]);
-        };
-        // lane 0 of warp 0: MMAs of piece g once all four warps have published it
-        auto mma_piece = [&](int tile) {
-            const int x = g & 15, s = g % kNOp;
-            if (!wait_or_abort(&ms.opfull[s], (g / kNOp) & 1, abort, a.err)) {
-                cv_ok = false;
-                return;
-            }
-            tc_fence_after();
-            const uint32_t sa = smem_u32(sm + kOffOp + s * kOp);
-            if (x < 8) {
-                const uint32_t sb = smem_u32(sm + kOffQ + x * 8192);
+            load4(b0, tr0, rw);
+            load4(b1, tr0, rw + 4);
+            // the previous tile's pass 2 reads E: wait for it before overwriting
+            if (tile > 0 && !wait_or_abort(&ms.o_full, (tile - 1) & 1, abort, a.err)) ok = false;
+        }
+        if (ok) {
+            store4(b0, rw);
+            load4(b0, tr0, rw + 8);
+            store4(b1, rw + 4);
+            load4(b1, tr0, rw + 12);
+            store4(b0, rw + 8);
+            store4(b1, rw + 12);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        if (__syncthreads_or(!ok)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        const uint32_t tmem = ms.tmem_base;
+
+        // ------------------------------------------------------------ pass 1 (thread 0)
+        if (tid == 0) {
+            const uint32_t e0 = smem_u32(sm + kOffE), q0 = smem_u32(sm + kOffQ);
+#pragma unroll 1
+            for (int x = 0; x < 8; ++x)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_f16kind(tmem + kColS, desc_sw128(sa + kk * 32, 16, 1024), desc_sw128(sb + kk * 32, 16, 1024),
-                                id1, (x | kk) != 0);
-            } else {
-                const int y = x - 8, rb = y >> 2, mb = y & 3;
-                const uint32_t sb = smem_u32(sm + kOffP + (64 * rb) * 128);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_f16kind(tmem + kColO + 64 * mb, desc_sw128(sa + kk * 2048, 8192, 1024),
-                                desc_sw128(sb + kk * 2048, 8192, 1024), id2,
-                                (tile > 0 || rb > 0 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(&ms.opempty[s]);
-            if (x == 7) mma_commit(&ms.s_full);
-            if (x == 15) mma_commit(&ms.o_full);
-        };
-        // the eight pieces of one pass: convert, then (warp 0) issue
-        auto run_pass = [&](int tile) {
-            for (int k = 0; k < 8; ++k) {
-                if (cv_ok) convert();
-                if (warp == 0) {
-                    __syncwarp();
-                    if (lane == 0 && cv_ok) mma_piece(tile);
-                    __syncwarp();
-                }
-                ++g;
-            }
-        };
+                    mma_f16kind(tmem + kColS, desc_sw128(e0 + x * kDBlockE + kk * 32, 16, 1024),
+                                desc_sw128(q0 + x * 8192 + kk * 32, 16, 1024), id1, (x | kk) != 0);
+            mma_commit(&ms.s_full);
+        }
+        if (tid >= kSoftThreads) continue;   // warps 4-7: on to the next tile's loads
 
-        // ------------------------------------------------------------ softmax
+        // ------------------------------------------------------------ softmax (warps 0-3)
         const int r = tid;                                // tile row = TMEM lane
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        bool ok = true;
-        for (int tile = 0; tile < n_tiles && ok; ++tile) {
-            run_pass(tile);                              // pass 1
-            const bool got = cv_ok && wait_or_abort(&ms.s_full, tile & 1, abort, a.err);
-            if (named_sync_or(1, kSoftWarps * 32, !got)) { ok = false; break; }
-            tc_fence_after();
-            float v[64];
+        const bool got = wait_or_abort(&ms.s_full, tile & 1, abort, a.err);
+        if (named_sync_or(1, kSoftThreads, !got)) {
+            ok = false;
+            *abort = 1;
+            continue;                                     // leaves at the next block barrier
+        }
+        tc_fence_after();
+        float v[64];
 #pragma unroll
-            for (int c = 0; c < H; c += 16) {
-                float t16[16];
-                tmem_ld16(tmem + lane_base + kColS + c, t16);
+        for (int c = 0; c < H; c += 16) {
+            float t16[16];
+            tmem_ld16(tmem + lane_base + kColS + c, t16);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[c + i] = t16[i];
+            for (int i = 0; i < 16; ++i) v[c + i] = t16[i];
+        }
+        tmem_ld_wait();
+        const bool valid = tr0 + r < row1;
+#pragma unroll
+        for (int h = 0; h < 64; ++h) v[h] = (h < H && valid) ? v[h] * a.sl2 : -INFINITY;
+        // per-head tile max over the 128 rows: warp butterflies, then the 4 warps
+#pragma unroll
+        for (int hh = 0; hh < H; hh += 32) {
+            float red[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) red[i] = hh + i < H ? v[hh + i] : -INFINITY;
+            ms.red[warp][hh + lane] = butterfly32<true>(red, lane);
+        }
+        named_sync(1, kSoftThreads);
+        if (tid < H) {
+            const int h = tid;
+            const float mt = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
+            const float mu = ms.m_used[h];
+            float al = 1.f;
+            if (mt > mu + kLazy || (mu == -INFINITY && mt > -INFINITY)) {
+                al = exp2f(mu - mt);                      // 0 when mu = -inf
+                ms.m_used[h] = mt;
+                ms.l_run[h] *= al;
+                if (tile > 0 && al != 1.f) ms.rescale = 1;
             }
-            tmem_ld_wait();
-            const bool valid = row0 + tile * kTileRows + r < row1;
+            ms.alpha[h] = al;
+        }
+        named_sync(1, kSoftThreads);
 #pragma unroll
-            for (int h = 0; h < 64; ++h) v[h] = (h < H && valid) ? v[h] * a.sl2 : -INFINITY;
-            // per-head tile max over the 128 rows: warp butterflies, then the 4 warps
+        for (int h = 0; h < 64; ++h) v[h] = (h < H) ? exp2f(v[h] - ms.m_used[h]) : 0.f;
 #pragma unroll
-            for (int hh = 0; hh < H; hh += 32) {
-                float red[32];
+        for (int hh = 0; hh < H; hh += 32) {
+            float red[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) red[i] = hh + i < H ? v[hh + i] : -INFINITY;
-                ms.red[warp][hh + lane] = butterfly32<true>(red, lane);
-            }
-            named_sync(1, kSoftWarps * 32);
-            if (tid < H) {
-                const int h = tid;
-                const float mt = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
-                const float mu = ms.m_used[h];
-                float al = 1.f;
-                if (mt > mu + kLazy || (mu == -INFINITY && mt > -INFINITY)) {
-                    al = exp2f(mu - mt);                  // 0 when mu = -inf
-                    ms.m_used[h] = mt;
-                    ms.l_run[h] *= al;
-                    if (tile > 0 && al != 1.f) ms.rescale = 1;
-                }
-                ms.alpha[h] = al;
-            }
-            named_sync(1, kSoftWarps * 32);
-#pragma unroll
-            for (int h = 0; h < 64; ++h) v[h] = (h < H) ? exp2f(v[h] - ms.m_used[h]) : 0.f;
-#pragma unroll
-            for (int hh = 0; hh < H; hh += 32) {
-                float red[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) red[i] = v[hh + i];
-                ms.red[warp][hh + lane] = butterfly32<false>(red, lane);
-            }
-            // the previous tile's pass 2 still reads P and writes O: wait for it
-            const bool prev = tile == 0 || wait_or_abort(&ms.o_full, (tile - 1) & 1, abort, a.err);
-            if (named_sync_or(1, kSoftWarps * 32, !prev)) { ok = false; break; }
-            if (tid < H)
-                ms.l_run[tid] += (ms.red[0][tid] + ms.red[1][tid]) + (ms.red[2][tid] + ms.red[3][tid]);
-            if (ms.rescale) {
-                // O^T[d, h] *= alpha[h]: this thread owns TMEM lane r of each d-block
-                tc_fence_after();
+            for (int i = 0; i < 32; ++i) red[i] = v[hh + i];
+            ms.red[warp][hh + lane] = butterfly32<false>(red, lane);
+        }
+        named_sync(1, kSoftThreads);
+        if (tid < H) ms.l_run[tid] += (ms.red[0][tid] + ms.red[1][tid]) + (ms.red[2][tid] + ms.red[3][tid]);
+        // pass 2 of the previous tile completed before E was overwritten, so O
+        // and P are free here
+        if (ms.rescale) {
+            // O^T[d, h] *= alpha[h]: this thread owns TMEM lane r of each d-block
 #pragma unroll 1
-                for (int mb = 0; mb < 4; ++mb) {
+            for (int mb = 0; mb < 4; ++mb) {
 #pragma unroll
-                    for (int c = 0; c < H; c += 16) {
-                        float t16[16];
-                        const uint32_t ta = tmem + lane_base + kColO + 64 * mb + c;
-                        tmem_ld16(ta, t16);
-                        tmem_ld_wait();
+                for (int c = 0; c < H; c += 16) {
+                    float t16[16];
+                    const uint32_t ta = tmem + lane_base + kColO + 64 * mb + c;
+                    tmem_ld16(ta, t16);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) t16[i] *= ms.alpha[c + i];
-                        tmem_st16(ta, t16);
-                    }
+                    for (int i = 0; i < 16; ++i) t16[i] *= ms.alpha[c + i];
+                    tmem_st16(ta, t16);
                 }
-                tmem_st_wait();
             }
-            // P row r: 64 fp16 heads = 128 B, MN-major (heads contiguous), swizzled
-            unsigned char* prow = sm + kOffP;
+            tmem_st_wait();
+        }
+        // P row r: 64 fp16 heads = 128 B, MN-major (heads contiguous), swizzled
+        unsigned char* prow = sm + kOffP;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint4 w;
-                w.x = pack_f16x2(v[8 * c + 0], v[8 * c + 1]);
-                w.y = pack_f16x2(v[8 * c + 2], v[8 * c + 3]);
-                w.z = pack_f16x2(v[8 * c + 4], v[8 * c + 5]);
-                w.w = pack_f16x2(v[8 * c + 6], v[8 * c + 7]);
-                *reinterpret_cast<uint4*>(prow + sw128(r, c)) = w;
-            }
-            fence_async_smem();
-            tc_fence_before();
-            named_sync(1, kSoftWarps * 32);
-            if (tid == 0) ms.rescale = 0;
-            mbar_arrive(&ms.p_full);
-            if (warp == 0) {
-                // the pass-2 MMAs read P: every softmax thread must have written it
-                if (lane == 0 && !wait_or_abort(&ms.p_full, tile & 1, abort, a.err)) cv_ok = false;
-                __syncwarp();
-                tc_fence_after();
-            }
-            run_pass(tile);                              // pass 2
+        for (int c = 0; c < 8; ++c) {
+            uint4 w;
+            w.x = pack_f16x2(v[8 * c + 0], v[8 * c + 1]);
+            w.y = pack_f16x2(v[8 * c + 2], v[8 * c + 3]);
+            w.z = pack_f16x2(v[8 * c + 4], v[8 * c + 5]);
+            w.w = pack_f16x2(v[8 * c + 6], v[8 * c + 7]);
+            *reinterpret_cast<uint4*>(prow + sw128(r, c)) = w;
         }
-        if (warp == 0) {
-            // drain: completes once every MMA issued above has completed
-            if (lane == 0) {
-                mma_commit(&ms.drain);
-                if (!mbar_wait(&ms.drain, 0, 1u << 26)) atomicOr(a.err, kErrTimeout);
-            }
-            __syncwarp();
+        fence_async_smem();
+        tc_fence_before();
+        named_sync(1, kSoftThreads);
+        if (tid == 0) {
+            // ------------------------------------------------------------ pass 2 (thread 0)
+            ms.rescale = 0;
+            tc_fence_after();
+            const uint32_t e0 = smem_u32(sm + kOffE), p0 = smem_u32(sm + kOffP);
+#pragma unroll 1
+            for (int mb = 0; mb < 4; ++mb)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_f16kind(tmem + kColO + 64 * mb, desc_sw128(e0 + 2 * mb * kDBlockE + kk * 2048, kDBlockE, 1024),
+                                desc_sw128(p0 + kk * 2048, 8192, 1024), id2, (tile > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&ms.o_full);
         }
-        const bool got = ok && wait_or_abort(&ms.o_full, (n_tiles - 1) & 1, abort, a.err);
-        ok = !named_sync_or(1, kSoftWarps * 32, !got);    // the same verdict in all 128 threads
-        if (tid < H) ms.alpha[tid] = 1.f / ms.l_run[tid];
-        if (tid == 0) ms.epi_ok = ok ? 1 : 0;
     }
 
-    // ---------------------------------------------------------------- epilogue: all 8 warps
+    // ---------------------------------------------------------------- drain
+    if (tid == 0 && n_tiles > 0) {
+        // completes once every MMA issued above has completed
+        mma_commit(&ms.drain);
+        if (!mbar_wait(&ms.drain, 0, 1u << 26)) {
+            atomicOr(a.err, kErrTimeout);
+            ok = false;
+        }
+    }
     tc_fence_before();
-    __syncthreads();
+    const bool failed = __syncthreads_or(!ok);
     tc_fence_after();
+    if (tid < H) ms.alpha[tid] = 1.f / ms.l_run[tid];
+    if (tid == 0) ms.epi_ok = failed ? 0 : 1;
+    __syncthreads();
+
+    // ---------------------------------------------------------------- epilogue: all 8 warps
     const bool single = it.n_splits == 1;
     float* dst = single ? a.out + lb * H * kKvDim : a.part_o + (size_t)item_idx * H * kKvDim;
     if (n_tiles > 0 && ms.epi_ok) {
+        const uint32_t tmem = ms.tmem_base;
         // warp w reads TMEM lanes 32 (w & 3).. of d-blocks 2 (w >> 2) and 2 (w >> 2) + 1
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 #pragma unroll 1
@@ -552,58 +465,70 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     __syncthreads();
     if (warp == 0 && n_tiles > 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(ms.tmem_base, kTmemCols);
     }
-    if (it.n_splits == 1) return;
+}
 
-    // ---------------------------------------------------------------- last CTA merges the splits
-    __threadfence();
+// Merge the split partials of one (layer, sequence), one head per CTA (thread
+// i owns float4 i of the head's 512 values):
+//     o_h = sum_s w_s O_s[h] / sum_s w_s l_s,   w_s = 2^(m_s - max_s m_s),
+// over the splits with l_s > 0, in split order. A split with l_s = 0 (no rows,
+// or a failed CTA) wrote zeros and gets weight 0.
+template <int H>
+__global__ void __launch_bounds__(kKvDim / 4) merge_kernel(const MergeItem* __restrict__ merges, int merge0,
+                                                           const float* __restrict__ part_o,
+                                                           const float* __restrict__ part_ml,
+                                                           float* __restrict__ out) {
+    __shared__ float m_s[kMaxSplits], l_s[kMaxSplits], w_s[kMaxSplits];
+    const MergeItem mi = merges[merge0 + blockIdx.x];
+    const int h = blockIdx.y;
+    const int ns = min(mi.ns, kMaxSplits);
+    const int t = threadIdx.x;
+    if (t < ns) {
+        const float* ml = part_ml + (size_t)(mi.first + t) * 2 * H;
+        m_s[t] = __ldcg(&ml[h]);
+        l_s[t] = __ldcg(&ml[H + h]);
+    }
     __syncthreads();
-    if (tid == 0) ms.ticket = atomicAdd(&a.counters[lb], 1u);
-    __syncthreads();
-    if (ms.ticket != (unsigned)(it.n_splits - 1)) return;
-    __threadfence();
-    const int ns = it.n_splits;
-    const int base = item_idx - it.split;
-    float* wts = reinterpret_cast<float*>(sm + kOffLand);   // [ns][H]
-    for (int h = tid; h < H; h += kThreads) {
+    if (t == 0) {
         float M = -INFINITY;
-        for (int s = 0; s < ns; ++s) {
-            const float* ml = a.part_ml + (size_t)(base + s) * 2 * H;
-            if (__ldcg(&ml[H + h]) > 0.f) M = fmaxf(M, __ldcg(&ml[h]));
-        }
+        for (int s = 0; s < ns; ++s)
+            if (l_s[s] > 0.f) M = fmaxf(M, m_s[s]);
         float L = 0.f;
         for (int s = 0; s < ns; ++s) {
-            const float* ml = a.part_ml + (size_t)(base + s) * 2 * H;
-            const float ls = __ldcg(&ml[H + h]);
-            const float w = ls > 0.f ? exp2f(__ldcg(&ml[h]) - M) : 0.f;
-            wts[s * H + h] = w;
-            L += w * ls;
+            const float w = l_s[s] > 0.f ? exp2f(m_s[s] - M) : 0.f;
+            w_s[s] = w;
+            L += w * l_s[s];
         }
         const float inv = 1.f / L;
-        for (int s = 0; s < ns; ++s) wts[s * H + h] *= inv;
+        for (int s = 0; s < ns; ++s) w_s[s] *= inv;
     }
     __syncthreads();
-    float* o = a.out + lb * H * kKvDim;
-    for (int i = tid; i < H * kKvDim / 4; i += kThreads) {
-        const int h = (i * 4) / kKvDim;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s = 0; s < ns; ++s) {
-            const float w = wts[s * H + h];
-            if (w == 0.f) continue;
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_o + (size_t)(base + s) * H * kKvDim) + i);
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
+    const float4* src = reinterpret_cast<const float4*>(part_o + ((size_t)mi.first * H + h) * kKvDim) + t;
+    const size_t split_stride = (size_t)H * kKvDim / 4;   // float4s between consecutive splits
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < ns; s0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (s0 + j < ns) v[j] = __ldcg(src + (size_t)(s0 + j) * split_stride);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (s0 + j < ns) {
+                const float w = w_s[s0 + j];
+                acc.x += w * v[j].x;
+                acc.y += w * v[j].y;
+                acc.z += w * v[j].z;
+                acc.w += w * v[j].w;
+            }
         }
-        reinterpret_cast<float4*>(o)[i] = acc;
     }
-    if (tid == 0) a.counters[lb] = 0u;
+    reinterpret_cast<float4*>(out + ((size_t)mi.lb * H + h) * kKvDim)[t] = acc;
 }
 
 template <int H>
-cudaError_t launch_h(const AttnArgs& args, const AttnMaps& maps, int n_items, cudaStream_t st) {
+cudaError_t launch_h(const AttnArgs& args, int n_items, const MergeItem* merges, int merge0, int n_merges,
+                     cudaStream_t st) {
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -611,7 +536,11 @@ cudaError_t launch_h(const AttnArgs& args, const AttnMaps& maps, int n_items, cu
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    attend_tc_kernel<H><<<n_items, kThreads, kSmemBytes, st>>>(args, maps);
+    attend_tc_kernel<H><<<n_items, kThreads, kSmemBytes, st>>>(args);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || n_merges <= 0) return e;
+    merge_kernel<H><<<dim3((unsigned)n_merges, H), kKvDim / 4, 0, st>>>(merges, merge0, args.part_o, args.part_ml,
+                                                                        args.out);
     return cudaGetLastError();
 }
 
@@ -619,46 +548,19 @@ cudaError_t launch_h(const AttnArgs& args, const AttnMaps& maps, int n_items, cu
 
 int attend_max_splits() { return kMaxSplits; }
 
-// 2-D fp32 map over [rows][512] with a box of `box` columns x 1 row, no swizzle.
-static cudaError_t encode_rows_map(CUtensorMap* m, const float* base, unsigned long long rows, unsigned box) {
-    static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
-    if (!enc) {
-        cudaDriverEntryPointQueryResult qr;
-        cudaError_t e = cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", (void**)&enc, cudaEnableDefault, &qr);
-        if (e != cudaSuccess || qr != cudaDriverEntryPointSuccess || !enc) return cudaErrorNotSupported;
-    }
-    cuuint64_t dims[2] = {(cuuint64_t)kKvDim, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)kKvDim * sizeof(float)};
-    cuuint32_t boxd[2] = {box, 1};
-    cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, boxd,
-                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-cudaError_t launch_attend(const AttnItem* items, int item0, int n_items, int split_rows,
-                          int n_heads, int L, int B, int G, int S, const uint16_t* q, const float* window,
-                          const float* staging, const int32_t* phys, const int32_t* count_l,
-                          float* out, float* part_o, float* part_ml, unsigned* counters,
-                          uint32_t* err, cudaStream_t st) {
+cudaError_t launch_attend(const AttnItem* items, int item0, int n_items, const MergeItem* merges, int merge0,
+                          int n_merges, int split_rows, int n_heads, int B, int G, int S, const uint16_t* q,
+                          const float* window, const float* staging, const int32_t* phys,
+                          const int32_t* count_l, float* out, float* part_o, float* part_ml, uint32_t* err,
+                          cudaStream_t st) {
     if (n_items <= 0) return cudaSuccess;
     if (split_rows % kTileRows != 0) return cudaErrorInvalidValue;
-    AttnMaps maps;
-    const unsigned long long win_rows = (unsigned long long)L * B * kWindow;
-    const unsigned long long stg_rows = (unsigned long long)L * B * G;
-    cudaError_t e = encode_rows_map(&maps.win64, window, win_rows, 64);
-    if (e == cudaSuccess) e = encode_rows_map(&maps.win128, window, win_rows, 128);
-    if (e == cudaSuccess) e = encode_rows_map(&maps.stg64, staging, stg_rows, 64);
-    if (e == cudaSuccess) e = encode_rows_map(&maps.stg128, staging, stg_rows, 128);
-    if (e != cudaSuccess) return e;
     AttnArgs args{items, item0, split_rows, B, G, S, q, window, staging, phys, count_l,
-                  out, part_o, part_ml, counters, err,
-                  (float)(1.4426950408889634 / std::sqrt((double)kKvDim))};
+                  out, part_o, part_ml, err, (float)(1.4426950408889634 / std::sqrt((double)kKvDim))};
     switch (n_heads) {
-        case 16: return launch_h<16>(args, maps, n_items, st);
-        case 32: return launch_h<32>(args, maps, n_items, st);
-        case 64: return launch_h<64>(args, maps, n_items, st);
+        case 16: return launch_h<16>(args, n_items, merges, merge0, n_merges, st);
+        case 32: return launch_h<32>(args, n_items, merges, merge0, n_merges, st);
+        case 64: return launch_h<64>(args, n_items, merges, merge0, n_merges, st);
         default: return cudaErrorInvalidValue;
     }
 }

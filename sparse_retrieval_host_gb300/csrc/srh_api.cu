@@ -118,7 +118,7 @@ void free_ctx(srh_ctx* ctx) {
     cudaFree(ctx->d_items);
     cudaFree(ctx->d_part_o);
     cudaFree(ctx->d_part_ml);
-    cudaFree(ctx->d_attn_counter);
+    cudaFree(ctx->d_merges);
     if (ctx->ev_resolved) cudaEventDestroy(ctx->ev_resolved);
     if (ctx->ev_gathered) cudaEventDestroy(ctx->ev_gathered);
     delete ctx;
@@ -126,7 +126,7 @@ void free_ctx(srh_ctx* ctx) {
 
 // Split every (layer, sequence) row range into equal splits so the whole
 // attention launch is about one CTA per SM (it holds ~200 KB of shared memory).
-void plan_attention(srh_ctx* ctx, std::vector<AttnItem>* items) {
+void plan_attention(srh_ctx* ctx, std::vector<AttnItem>* items, std::vector<MergeItem>* merges) {
     long long total = 0;
     std::vector<int> max_rows(ctx->L);
     for (int l = 0; l < ctx->L; ++l) {
@@ -138,14 +138,20 @@ void plan_attention(srh_ctx* ctx, std::vector<AttnItem>* items) {
     sr = std::max<long long>(sr, kAttnTile);
     ctx->split_rows = (int)sr;
     ctx->item_begin.assign(ctx->L + 1, 0);
+    ctx->merge_begin.assign(ctx->L + 1, 0);
     for (int l = 0; l < ctx->L; ++l) {
         ctx->item_begin[l] = (int)items->size();
+        ctx->merge_begin[l] = (int)merges->size();
         const int ns = (max_rows[l] + ctx->split_rows - 1) / ctx->split_rows;
-        for (int b = 0; b < ctx->B; ++b)
+        for (int b = 0; b < ctx->B; ++b) {
+            if (ns > 1) merges->push_back(MergeItem{l * ctx->B + b, (int)items->size(), ns, 0});
             for (int s = 0; s < ns; ++s) items->push_back(AttnItem{l, b, s, ns});
+        }
     }
     ctx->item_begin[ctx->L] = (int)items->size();
+    ctx->merge_begin[ctx->L] = (int)merges->size();
     ctx->n_items = (int)items->size();
+    ctx->n_merges = (int)merges->size();
 }
 
 }  // namespace
@@ -271,14 +277,16 @@ int srh_create(const srh_config* cfg, srh_ctx** out) {
     if (e != cudaSuccess) return bail(SRH_ERR_NOMEM, std::string("device scratch: ") + cudaGetErrorString(e));
 
     std::vector<AttnItem> items;
-    plan_attention(ctx, &items);
+    std::vector<MergeItem> merges;
+    plan_attention(ctx, &items, &merges);
     e = cudaMalloc(&ctx->d_items, sizeof(AttnItem) * items.size());
     if (e == cudaSuccess)
         e = cudaMemcpy(ctx->d_items, items.data(), sizeof(AttnItem) * items.size(), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_part_o, sizeof(float) * (size_t)ctx->n_items * SRH_MAX_HEADS * kKvDim);
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_part_ml, sizeof(float) * (size_t)ctx->n_items * 2 * SRH_MAX_HEADS);
-    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_attn_counter, sizeof(unsigned) * (size_t)ctx->L * B);
-    if (e == cudaSuccess) e = cudaMemset(ctx->d_attn_counter, 0, sizeof(unsigned) * (size_t)ctx->L * B);
+    if (e == cudaSuccess && !merges.empty()) e = cudaMalloc(&ctx->d_merges, sizeof(MergeItem) * merges.size());
+    if (e == cudaSuccess && !merges.empty())
+        e = cudaMemcpy(ctx->d_merges, merges.data(), sizeof(MergeItem) * merges.size(), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_resolved, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_gathered, cudaEventDisableTiming);
     if (e != cudaSuccess) return bail(SRH_ERR_NOMEM, std::string("attention scratch: ") + cudaGetErrorString(e));
@@ -430,9 +438,11 @@ int lsa_attend(srh_ctx* ctx, int layer, const uint16_t* d_q, int n_heads, const 
         return fail(ctx, SRH_ERR_INVALID, "q/window/staging/out must be 16-byte aligned");
     const int i0 = layer < 0 ? 0 : ctx->item_begin[layer];
     const int i1 = layer < 0 ? ctx->n_items : ctx->item_begin[layer + 1];
-    const cudaError_t e = launch_attend(ctx->d_items, i0, i1 - i0, ctx->split_rows, n_heads, ctx->L, ctx->B, ctx->G,
-                                        ctx->S, d_q, d_window, d_staging, d_phys, d_count_l, d_out,
-                                        ctx->d_part_o, ctx->d_part_ml, ctx->d_attn_counter, ctx->d_err,
+    const int m0 = layer < 0 ? 0 : ctx->merge_begin[layer];
+    const int m1 = layer < 0 ? ctx->n_merges : ctx->merge_begin[layer + 1];
+    const cudaError_t e = launch_attend(ctx->d_items, i0, i1 - i0, ctx->d_merges, m0, m1 - m0, ctx->split_rows,
+                                        n_heads, ctx->B, ctx->G, ctx->S, d_q, d_window, d_staging, d_phys,
+                                        d_count_l, d_out, ctx->d_part_o, ctx->d_part_ml, ctx->d_err,
                                         (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "lsa_attend launch");
     return SRH_OK;

@@ -57,6 +57,15 @@ struct AttnItem {
     int n_splits;
 };
 
+// One (layer, seq) whose rows were cut into ns > 1 splits: the merge pass
+// combines the partials of items first .. first + ns - 1 into its output.
+struct MergeItem {
+    int lb;      // layer * B + seq
+    int first;   // index of its split 0 in the item list
+    int ns;
+    int pad;
+};
+
 struct Ctx {
     srh_config cfg{};
     std::vector<int> ratios;
@@ -95,7 +104,9 @@ struct Ctx {
     int n_items = 0;
     float* d_part_o = nullptr;          // [n_items][SRH_MAX_HEADS][D]
     float* d_part_ml = nullptr;         // [n_items][2][SRH_MAX_HEADS]
-    unsigned* d_attn_counter = nullptr; // [L][B]
+    MergeItem* d_merges = nullptr;      // the multi-split (layer, seq) pairs, grouped by layer
+    std::vector<int> merge_begin;       // [L+1] offsets into d_merges
+    int n_merges = 0;
     // bookkeeping
     float* staging = nullptr;           // the staging buffer bound to this context
     cudaEvent_t ev_resolved = nullptr;
@@ -132,11 +143,11 @@ cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, 
                           uint32_t* err, int sm_count, cudaStream_t st);
 cudaError_t launch_resident_fill(const float* pool_dev, const uint8_t* ready, long long cap,
                                  int layer, int B, int G, float* staging, cudaStream_t st);
-cudaError_t launch_attend(const AttnItem* items, int item0, int n_items, int split_rows,
-                          int n_heads, int L, int B, int G, int S, const uint16_t* q, const float* window,
-                          const float* staging, const int32_t* phys, const int32_t* count_l,
-                          float* out, float* part_o, float* part_ml, unsigned* counters,
-                          uint32_t* err, cudaStream_t st);
+cudaError_t launch_attend(const AttnItem* items, int item0, int n_items, const MergeItem* merges, int merge0,
+                          int n_merges, int split_rows, int n_heads, int B, int G, int S, const uint16_t* q,
+                          const float* window, const float* staging, const int32_t* phys,
+                          const int32_t* count_l, float* out, float* part_o, float* part_ml, uint32_t* err,
+                          cudaStream_t st);
 size_t lru_smem_bytes(int S, int G);
 int attend_max_splits();
 

@@ -94,11 +94,45 @@ class DecodeStep:
                        self.phys, self.count_l, self.out if out is None else out, stream)
 
     def step(self, spec: StepSpec, stream=None, side=None, fm_q=None, q=None, out=None) -> None:
-        """One decode step: the four C entry points in order (5 kernels)."""
+        """One decode step: the four C entry points in order."""
         self.score(spec, stream, fm_q)
         self.select(spec, stream)
         self.stage(-1, stream, side)
         self.attend(-1, stream, q, out)
+
+    # ------------------------------------------------------------------ CUDA graphs
+    def capture(self, spec: StepSpec, parts: bool = False):
+        """Record the decode step into CUDA graphs and return them.
+
+        The graphs read the bound inputs (``fm_q``, ``q``) and write the bound
+        outputs, so a caller copies each step's queries into those buffers and
+        calls ``replay()``: one launch per step instead of one host call per
+        kernel. Replays advance the LRU state like eager steps. Capture after at
+        least one eager step (one-time set-up -- kernel attributes, resident
+        fills of layers that do not swap -- happens there), and capture again
+        after ``mark_stored`` on a layer that does not swap. With ``parts`` the
+        step is recorded as three graphs (score; select + stage; attend) so the
+        phases can be timed separately.
+        """
+        dev = self.keys.device
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        graphs = []
+
+        def rec(fn):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                fn()
+            graphs.append(g)
+
+        if parts:
+            rec(lambda: self.score(spec))
+            rec(lambda: (self.select(spec), self.stage(-1)))
+            rec(lambda: self.attend(-1))
+        else:
+            rec(lambda: self.step(spec))
+        torch.cuda.current_stream(dev).wait_stream(s)
+        return graphs
 
     # ------------------------------------------------------------------ status
     def stats(self) -> dict:

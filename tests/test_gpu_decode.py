@@ -160,6 +160,43 @@ def test_residency_changes_slots_never_outputs():
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("parts", [False, True], ids=["one_graph", "three_graphs"])
+def test_graph_replay_equals_eager_steps(parts):
+    """Steps replayed from captured CUDA graphs give the same bits as eager
+    calls: selections, slots, staged rows, outputs and the swap counters."""
+    w = C.TINY.with_(steps=12)
+    runs = []
+    for mode in ("eager", "graph"):
+        ds = make_ds(w)
+        try:
+            fill(ds, w)
+            spec = spec_of(w)
+            load_step_inputs(ds, w, 0)
+            ds.step(spec)                       # one eager step before capture
+            graphs = ds.capture(spec, parts=parts) if mode == "graph" else None
+            seq = []
+            for t in range(1, w.steps):
+                load_step_inputs(ds, w, t)
+                if graphs is None:
+                    ds.step(spec)
+                else:
+                    for g in graphs:
+                        g.replay()
+                torch.cuda.synchronize()
+                seq.append([x.clone() for x in (ds.sel, ds.count, ds.phys, ds.count_l, ds.out)])
+            st = ds.stats()
+            runs.append((seq, st["hits"], st["misses"], ds.staging.clone()))
+            assert ds.check_error() == 0
+        finally:
+            ds.close()
+    (sa, ha, ma, ga), (sb, hb, mb, gb) = runs
+    assert (ha, ma) == (hb, mb)
+    assert torch.equal(ga, gb)
+    for xa, xb in zip(sa, sb):
+        for a, b in zip(xa, xb):
+            assert torch.equal(a, b)
+
+
 def test_ties_follow_index_order():
     """Duplicated keys give exactly equal scores; both sides break ties by index."""
     from sparse_retrieval_host_gb300.runtime import bits_to_i16
