@@ -40,6 +40,11 @@ its reason in the design notes):
   * attention is MQA over the 512-wide latent (K = V = row), scale 1/sqrt(512).
 
 Parity pins (checks that do not reuse this code) live in ``tests/test_oracle_*.py``.
+
+Parity unpinned against the method: the head reduction (max over the 8
+heads), the logit scale and bias, and the MEAN domain (logits, not sigmoids).
+The pages do not fix them; hand-worked cases pin the code only to the readings
+stated above. Every other step has a pin fixed by the pages or by mathematics.
 """
 from __future__ import annotations
 
