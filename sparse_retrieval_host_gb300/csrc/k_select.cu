@@ -18,6 +18,18 @@
 // Threshold mode (s > ln(tau/(1-tau)), strict) collects the passing chunks in
 // one pass; if more than `clamp` pass, the best `clamp` of them are exactly the
 // global top-`clamp`, so it falls through to the top-k path with k = clamp.
+//
+// Two accelerations, both exact:
+//   * for large n, a multi-CTA collect pass first appends the chunks that can
+//     be selected (first digit at or above the cut-off digit of the k-th key,
+//     or above the threshold) to a candidate list; the per-sequence CTA then
+//     works on that list instead of all n scores (if the list overflows its
+//     capacity, the CTA scans all n scores as before);
+//   * when the first digit already isolates the selection and every digit
+//     bucket at or above the cut-off is small, the output is placed without a
+//     sort: candidates are scattered into their buckets (buckets are ordered by
+//     digit), and each one's position is its bucket's start plus the number of
+//     larger keys inside its bucket.
 #include "srh_internal.cuh"
 
 namespace srh {
@@ -26,6 +38,10 @@ namespace {
 constexpr int kSelThreads = 1024;
 constexpr int kCandCap = 8192;
 constexpr int kDigit = 12;
+constexpr int kArr = kCandCap + kMaxSelect;             // cand + outk, contiguous in shared memory
+constexpr long long kBucketWork = 256LL * kSelThreads;  // bound on sum of squared bucket sizes
+constexpr int kCollectThreads = 256;
+constexpr int kCollectPer = 16;                         // scores per collect thread
 
 __device__ __forceinline__ unsigned long long composite(uint32_t key, uint32_t idx) {
     return ((unsigned long long)key << 32) | (unsigned long long)(~idx);
@@ -113,16 +129,30 @@ __device__ __forceinline__ int pow2_at_least(int m) {
 
 struct SelShared {
     uint32_t hist[kHistBins];
+    int bbase[kHistBins];    // first level: keys in higher digits (then: bucket ends)
     int warp_buf[32];
     int n_out;
     int n_cand;
     int found_digit;
     int found_above;
+    unsigned long long sq;   // sum of squared bucket sizes at or above the cut-off
+};
+
+// The keys the selection runs over: all n scores of the sequence, or a
+// candidate list of composites made by collect_kernel.
+struct Src {
+    const float* sc;
+    const unsigned long long* cl;
+    int n;
+    __device__ __forceinline__ unsigned long long get(int j) const {
+        return cl ? cl[j] : composite(ordered_key(sc[j]), (uint32_t)j);
+    }
 };
 
 __global__ void __launch_bounds__(kSelThreads)
 select_kernel(const float* __restrict__ scores, int n, int mode, int k, float thresh, int clamp,
-              int S, const uint32_t* __restrict__ hist_in, int32_t* __restrict__ sel,
+              int S, const uint32_t* __restrict__ hist_in, const unsigned long long* __restrict__ cand_in,
+              const int* __restrict__ cand_cnt, int cand_cap, int32_t* __restrict__ sel,
               int32_t* __restrict__ count) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
@@ -131,23 +161,33 @@ select_kernel(const float* __restrict__ scores, int n, int mode, int k, float th
 
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
-    const float* sc = scores + (size_t)b * n;
     int32_t* sel_b = sel + (size_t)b * S;
+
+    // the key universe: a candidate list when one was made and did not overflow
+    Src src{scores + (size_t)b * n, nullptr, n};
+    if (cand_in) {
+        const int nc = cand_cnt[b];
+        if (nc >= 0 && nc <= cand_cap) {
+            src.cl = cand_in + (size_t)b * cand_cap;
+            src.n = nc;
+        }
+    }
 
     if (tid == 0) {
         sh.n_out = 0;
         sh.n_cand = 0;
+        sh.sq = 0ull;
     }
     __syncthreads();
 
     int K;
     if (mode == SRH_SELECT_THRESH) {
         const uint32_t kt = ordered_key(thresh);
-        for (int i = tid; i < n; i += kSelThreads) {
-            const uint32_t key = ordered_key(sc[i]);
-            if (key > kt) {
+        for (int i = tid; i < src.n; i += kSelThreads) {
+            const unsigned long long c = src.get(i);
+            if ((uint32_t)(c >> 32) > kt) {
                 const int pos = atomicAdd(&sh.n_cand, 1);
-                if (pos < kCandCap) cand[pos] = composite(key, (uint32_t)i);
+                if (pos < kCandCap) cand[pos] = c;
             }
         }
         __syncthreads();
@@ -192,8 +232,8 @@ select_kernel(const float* __restrict__ scores, int n, int mode, int k, float th
         } else {
             for (int i = tid; i < kHistBins; i += kSelThreads) sh.hist[i] = 0;
             __syncthreads();
-            for (int i = tid; i < n; i += kSelThreads) {
-                const unsigned long long c = composite(ordered_key(sc[i]), (uint32_t)i);
+            for (int i = tid; i < src.n; i += kSelThreads) {
+                const unsigned long long c = src.get(i);
                 if (pbits == 0 || (c >> (64 - pbits)) == (prefix >> (64 - pbits)))
                     atomicAdd(&sh.hist[(c >> shift) & mask], 1u);
             }
@@ -209,6 +249,7 @@ select_kernel(const float* __restrict__ scores, int n, int mode, int k, float th
         for (int j = 0; j < 4; ++j) {
             const int bin = kHistBins - 1 - 4 * tid - j;
             const int c = (int)sh.hist[bin];
+            sh.bbase[bin] = cum;
             if (c > 0 && cum < remaining && remaining <= cum + c) {
                 sh.found_digit = bin;
                 sh.found_above = cum;
@@ -235,9 +276,53 @@ select_kernel(const float* __restrict__ scores, int n, int mode, int k, float th
         if (cls <= kCandCap || pbits >= 64) break;
     }
 
+    if (pbits == kDigit && mode == SRH_SELECT_TOPK) {
+        // ---- first digit decided: try placing by buckets (no sort)
+        const int digit = (int)(prefix >> (64 - kDigit));
+        unsigned long long sq = 0ull;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int bin = kHistBins - 1 - 4 * tid - j;
+            if (bin >= digit) sq += (unsigned long long)sh.hist[bin] * sh.hist[bin];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        if ((tid & 31) == 0 && sq) atomicAdd(&sh.sq, sq);
+        __syncthreads();
+        const int total = (K - remaining) + (int)sh.hist[digit];
+        if (sh.sq <= (unsigned long long)kBucketWork && total <= kArr) {
+            unsigned long long* arr = cand;               // cand and outk: kArr entries
+            for (int i = tid; i < src.n; i += kSelThreads) {
+                const unsigned long long c = src.get(i);
+                const int bin = (int)(c >> (64 - kDigit));
+                if (bin >= digit) {
+                    const int slot = atomicAdd(&sh.bbase[bin], 1);
+                    if (slot < kArr) arr[slot] = c;
+                }
+            }
+            __syncthreads();
+            // bucket of digit d: [bbase[d] - hist[d], bbase[d]); keys in higher
+            // buckets are larger, so a key's position is its bucket start plus
+            // the number of larger keys in its bucket
+            for (int j = tid; j < total; j += kSelThreads) {
+                const unsigned long long c = arr[j];
+                const int bin = (int)(c >> (64 - kDigit));
+                const int e = min(sh.bbase[bin], total);
+                const int s0 = max(e - (int)sh.hist[bin], 0);
+                int rank = 0;
+#pragma unroll 4
+                for (int q = s0; q < e; ++q) rank += arr[q] > c ? 1 : 0;
+                const int pos = s0 + rank;
+                if (pos < K) sel_b[pos] = (int32_t)(~(uint32_t)c);
+            }
+            if (tid == 0) count[b] = K;
+            return;
+        }
+    }
+
     // ---- collect: keys above the class go out directly, class members to cand
-    for (int i = tid; i < n; i += kSelThreads) {
-        const unsigned long long c = composite(ordered_key(sc[i]), (uint32_t)i);
+    for (int i = tid; i < src.n; i += kSelThreads) {
+        const unsigned long long c = src.get(i);
         const unsigned long long top = c >> (64 - pbits), pre = prefix >> (64 - pbits);
         if (top > pre) {
             const int pos = atomicAdd(&sh.n_out, 1);
@@ -269,12 +354,84 @@ select_kernel(const float* __restrict__ scores, int n, int mode, int k, float th
     if (tid == 0) count[b] = K;
 }
 
+// Candidate pass for large n, grid (ceil(n / 4096), B): append every chunk that
+// can be selected to the sequence's list -- keys above the threshold, or keys
+// whose first digit is at or above the digit holding the K-th largest key (from
+// the first-digit histogram). Each CTA finds that digit itself, while its score
+// loads are in flight, and reserves room for its keys with one atomic. The
+// count keeps growing past the capacity so the select kernel can tell an
+// overflow.
+__global__ void __launch_bounds__(kCollectThreads)
+collect_kernel(const float* __restrict__ scores, int n, int mode, int K, float thresh,
+               const uint32_t* __restrict__ hist_in, unsigned long long* __restrict__ cand,
+               int* __restrict__ cand_cnt, int cap) {
+    __shared__ int warp_buf[32];
+    __shared__ int cut_s, base_s;
+    const int b = blockIdx.y, tid = threadIdx.x;
+    const float* sc = scores + (size_t)b * n;
+    const int i0 = blockIdx.x * (kCollectThreads * kCollectPer) + tid;
+    float v[kCollectPer];
+#pragma unroll
+    for (int j = 0; j < kCollectPer; ++j) {
+        const int i = i0 + j * kCollectThreads;
+        v[j] = i < n ? __ldg(sc + i) : 0.f;
+    }
+    uint32_t kt = 0, cut = 0;
+    if (mode == SRH_SELECT_THRESH) {
+        kt = ordered_key(thresh);
+    } else {
+        // thread t owns bins 4095-16t .. 4080-16t (descending)
+        const uint32_t* h = hist_in + (size_t)b * kHistBins;
+        uint32_t hv[16];
+        int local = 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            hv[j] = __ldg(h + kHistBins - 1 - 16 * tid - j);
+            local += (int)hv[j];
+        }
+        if (tid == 0) cut_s = 0;
+        const int incl = block_inclusive_scan(local, warp_buf);
+        int cum = incl - local;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int c = (int)hv[j];
+            if (c > 0 && cum < K && K <= cum + c) cut_s = kHistBins - 1 - 16 * tid - j;
+            cum += c;
+        }
+        __syncthreads();
+        cut = (uint32_t)cut_s;
+    }
+    uint32_t keys[kCollectPer];
+    unsigned pass = 0;
+    int np = 0;
+#pragma unroll
+    for (int j = 0; j < kCollectPer; ++j) {
+        const int i = i0 + j * kCollectThreads;
+        keys[j] = ordered_key(v[j]);
+        const bool p = i < n && (mode == SRH_SELECT_THRESH ? keys[j] > kt : (keys[j] >> 20) >= cut);
+        pass |= (p ? 1u : 0u) << j;
+        np += p ? 1 : 0;
+    }
+    const int incl = block_inclusive_scan(np, warp_buf);
+    if (tid == kCollectThreads - 1) base_s = incl ? atomicAdd(&cand_cnt[b], incl) : 0;
+    __syncthreads();
+    int pos = base_s + incl - np;
+    unsigned long long* out = cand + (size_t)b * cap;
+#pragma unroll
+    for (int j = 0; j < kCollectPer; ++j) {
+        if (pass & (1u << j)) {
+            if (pos < cap) out[pos] = composite(keys[j], (uint32_t)(i0 + j * kCollectThreads));
+            ++pos;
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_select(const float* scores, int n, int B, int mode, int k, float thresh,
                           int clamp, int S, const uint32_t* hist, int32_t* sel, int32_t* count,
-                          cudaStream_t st) {
-    const size_t smem = sizeof(SelShared) + sizeof(unsigned long long) * (kCandCap + kMaxSelect);
+                          cudaStream_t st, const unsigned long long* cand, const int* cand_cnt, int cand_cap) {
+    const size_t smem = sizeof(SelShared) + sizeof(unsigned long long) * kArr;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -282,7 +439,22 @@ cudaError_t launch_select(const float* scores, int n, int B, int mode, int k, fl
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    select_kernel<<<B, kSelThreads, smem, st>>>(scores, n, mode, k, thresh, clamp, S, hist, sel, count);
+    select_kernel<<<B, kSelThreads, smem, st>>>(scores, n, mode, k, thresh, clamp, S, hist, cand, cand_cnt,
+                                                cand_cap, sel, count);
+    return cudaGetLastError();
+}
+
+int select_cand_cap() { return kCandCap; }
+
+cudaError_t launch_collect(const float* scores, int n, int B, int mode, int K, float thresh,
+                           const uint32_t* hist, unsigned long long* cand, int* cand_cnt, int cap,
+                           cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(cand_cnt, 0, sizeof(int) * B, st);
+    if (e != cudaSuccess) return e;
+    const int per_cta = kCollectThreads * kCollectPer;
+    const int bx = (n + per_cta - 1) / per_cta;
+    collect_kernel<<<dim3((unsigned)bx, (unsigned)B), kCollectThreads, 0, st>>>(scores, n, mode, K, thresh,
+                                                                              hist, cand, cand_cnt, cap);
     return cudaGetLastError();
 }
 

@@ -113,6 +113,8 @@ void free_ctx(srh_ctx* ctx) {
     cudaFree(ctx->d_stats);
     cudaFree(ctx->d_err);
     cudaFree(ctx->d_hist);
+    cudaFree(ctx->d_cand);
+    cudaFree(ctx->d_cand_cnt);
     cudaFree(ctx->d_miss);
     cudaFree(ctx->d_miss_count);
     cudaFree(ctx->d_items);
@@ -271,6 +273,8 @@ int srh_create(const srh_config* cfg, srh_ctx** out) {
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_err, sizeof(uint32_t));
     if (e == cudaSuccess) e = cudaMemset(ctx->d_err, 0, sizeof(uint32_t));
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_hist, sizeof(uint32_t) * kHistBins * B);
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_cand, sizeof(unsigned long long) * select_cand_cap() * B);
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_cand_cnt, sizeof(int) * B);
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_miss, sizeof(int2) * (size_t)ctx->L * B * ctx->S);
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_miss_count, sizeof(int) * (size_t)ctx->L * B);
     if (e == cudaSuccess) e = cudaMemset(ctx->d_miss_count, 0, sizeof(int) * (size_t)ctx->L * B);
@@ -371,8 +375,16 @@ int fm_select(srh_ctx* ctx, const float* d_scores, int n, int mode, int k, float
     }
     ctx->hist_scores = nullptr;   // one use per scoring pass
     ctx->hist_n = -1;
+    const unsigned long long* cand = nullptr;
+    if (n > kCollectMinN) {
+        const int K = mode == SRH_SELECT_TOPK ? std::min(k, n) : clamp;
+        const cudaError_t ec = launch_collect(d_scores, n, ctx->B, mode, K, thresh, hist, ctx->d_cand,
+                                              ctx->d_cand_cnt, select_cand_cap(), st);
+        if (ec != cudaSuccess) return cuda_fail(ctx, ec, "fm_select candidate pass");
+        cand = ctx->d_cand;
+    }
     const cudaError_t e = launch_select(d_scores, n, ctx->B, mode, k, thresh, clamp, ctx->S, hist, d_sel,
-                                        d_count, st);
+                                        d_count, st, cand, ctx->d_cand_cnt, select_cand_cap());
     if (e != cudaSuccess) return cuda_fail(ctx, e, "fm_select launch");
     return SRH_OK;
 }

@@ -93,6 +93,8 @@ struct Ctx {
     unsigned long long* d_stats = nullptr;
     uint32_t* d_err = nullptr;
     uint32_t* d_hist = nullptr;         // [B][kHistBins]
+    unsigned long long* d_cand = nullptr; // [B][select_cand_cap()] candidate composites
+    int* d_cand_cnt = nullptr;          // [B]
     const float* hist_scores = nullptr; // the d_scores the histogram describes
     int hist_n = -1;
     int2* d_miss = nullptr;             // [L][B][S] (chunk, slot)
@@ -131,9 +133,16 @@ cudaError_t launch_score(const uint16_t* keys, int n, int B, const uint16_t* q, 
                          const float* bias3, int ensemble, float* scores, uint32_t* hist,
                          int sm_count, cudaStream_t st);
 cudaError_t launch_hist(const float* scores, int n, int B, uint32_t* hist, cudaStream_t st);
+// Candidate pass for large n: zeroes cand_cnt, then appends the selectable keys.
+cudaError_t launch_collect(const float* scores, int n, int B, int mode, int K, float thresh,
+                           const uint32_t* hist, unsigned long long* cand, int* cand_cnt, int cap,
+                           cudaStream_t st);
+int select_cand_cap();
+constexpr int kCollectMinN = 16384;    // fm_select runs the candidate pass above this n
 cudaError_t launch_select(const float* scores, int n, int B, int mode, int k, float thresh,
                           int clamp, int S, const uint32_t* hist, int32_t* sel, int32_t* count,
-                          cudaStream_t st);
+                          cudaStream_t st, const unsigned long long* cand = nullptr,
+                          const int* cand_cnt = nullptr, int cand_cap = 0);
 cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int S, int src_ratio,
                        long long max_dedup_cap, const int32_t* sel, const int32_t* count,
                        int32_t* phys, int32_t* count_l, int2* miss, int* miss_count,
