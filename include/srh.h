@@ -288,6 +288,20 @@ int lsa_attend(srh_ctx* ctx, int layer, const uint16_t* d_q, int n_heads, const 
                const float* d_staging, const int32_t* d_phys, const int32_t* d_count_l,
                float* d_out, srh_stream_t stream);
 
+/*
+ * Chained launches (no counterpart on the pages: a launch-latency option).
+ * With on != 0, the calls that follow on this context may start their kernels
+ * before the previous kernel on the stream has finished (programmatic
+ * dependent launch): each kernel waits for the previous one before it reads
+ * anything an earlier kernel wrote, and reads only the call's own inputs
+ * (queries, window rows) before that. Turn it on only around calls issued back
+ * to back on one stream -- fm_score, fm_select, kvswap_stage, lsa_attend --
+ * whose inputs were written before the first of them was issued; turn it off
+ * (the default) before issuing calls after other kernels of your own.
+ * Returns SRH_OK or SRH_ERR_INVALID (NULL context).
+ */
+int srh_set_chained(srh_ctx* ctx, int on);
+
 /* Copy the swap counters out (waits for the device). */
 int srh_get_stats(srh_ctx* ctx, srh_stats* out);
 

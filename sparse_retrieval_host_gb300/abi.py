@@ -95,6 +95,7 @@ SIGNATURES = [
     ("fm_select_noalloc", _i, [_vp, _i, _i, _i, _i, _f, _i, _i, _vp, _vp, _vp, ctypes.c_char_p, ctypes.c_size_t]),
     ("kvswap_stage", _i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     ("lsa_attend", _i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp]),
+    ("srh_set_chained", _i, [_vp, _i]),
     ("srh_get_stats", _i, [_vp, ctypes.POINTER(SrhStats)]),
     ("srh_reset_stats", _i, [_vp]),
     ("srh_check_error", _i, [_vp]),
@@ -233,6 +234,10 @@ def kvswap_stage(ctx, layer, sel, count, staging, phys, count_l, main=None, side
 def lsa_attend(ctx, layer, q, n_heads, window, staging, phys, count_l, out, stream=None) -> None:
     _check(load().lsa_attend(ctx, layer, _ptr(q), n_heads, _ptr(window), _ptr(staging), _ptr(phys),
                              _ptr(count_l), _ptr(out), _stream(stream)), "lsa_attend", ctx)
+
+
+def srh_set_chained(ctx, on: bool) -> None:
+    _check(load().srh_set_chained(ctx, 1 if on else 0), "srh_set_chained", ctx)
 
 
 def srh_get_stats(ctx) -> dict:

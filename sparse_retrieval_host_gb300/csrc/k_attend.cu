@@ -176,20 +176,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     const int item_idx = a.item0 + blockIdx.x;
-    const AttnItem it = a.items[item_idx];
+    const AttnItem it = a.items[item_idx];       // the work plan: written once, at creation
     const size_t lb = (size_t)it.layer * a.B + it.seq;
-    int cnt = a.count_l[lb];
-    if (cnt < 0 || cnt > a.S) {
-        if (tid == 0) atomicOr(a.err, kErrBounds);
-        cnt = cnt < 0 ? 0 : a.S;
-    }
-    const int R = kWindow + cnt;
-    const int row0 = it.split * a.split_rows;
-    const int row1 = min(R, row0 + a.split_rows);
-    const int n_tiles = row1 > row0 ? (row1 - row0 + kTileRows - 1) / kTileRows : 0;
-    const int32_t* ph = a.phys + lb * a.S;
+    pdl_trigger();
 
     // ---------------------------------------------------------------- set-up
+    // Everything up to the dependency wait reads only this call's inputs (the
+    // queries), so with chained launches it overlaps the kernels that resolve
+    // and gather the staged rows.
     if (tid == 0) {
         mbar_init(&ms.s_full, 1);
         mbar_init(&ms.o_full, 1);
@@ -204,7 +198,58 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         ms.l_run[tid] = 0.f;
         ms.alpha[tid] = 1.f;
     }
-    if (warp == 0 && n_tiles > 0) tmem_alloc(&ms.tmem_base, kTmemCols);
+    if (warp == 0) tmem_alloc(&ms.tmem_base, kTmemCols);
+    {
+        // queries: bf16 [H][512] -> fp16 K-major; d-block d / 64 at (d / 64) * 8192, row h
+        constexpr int kPer = H * 64 / kThreads;          // 16-byte chunks per thread
+        const uint16_t* qg = a.q + lb * H * kKvDim;
+        uint4 qv[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = tid + k * kThreads;
+            qv[k] = *reinterpret_cast<const uint4*>(qg + (i >> 6) * kKvDim + (i & 63) * 8);
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = tid + k * kThreads, h = i >> 6, c8 = i & 63;
+            const uint4 v = qv[k];
+            uint4 w;
+            w.x = pack_f16x2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
+            w.y = pack_f16x2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+            w.z = pack_f16x2(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u));
+            w.w = pack_f16x2(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
+            *reinterpret_cast<uint4*>(sm + kOffQ + (c8 >> 3) * 8192 + sw128(h, c8 & 7)) = w;
+        }
+    }
+
+    // ... as fp16 into E: d-block (lane >> 4) + 2 j, 16-byte chunk (lane & 15) >> 1, half lane & 1.
+    auto store4 = [&](const float4 (&v)[4][4], int rbase) {
+        unsigned char* e = sm + kOffE + (lane >> 4) * kDBlockE + 8 * (lane & 1);
+        const int chunk = (lane & 15) >> 1;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint2*>(e + 2 * j * kDBlockE + sw128(rbase + i, chunk)) =
+                    make_uint2(pack_f16x2(v[i][j].x, v[i][j].y), pack_f16x2(v[i][j].z, v[i][j].w));
+    };
+
+    constexpr uint32_t id1 = idesc_f16(0, 0, H);   // pass 1: K-major E and Q
+    constexpr uint32_t id2 = idesc_f16(1, 1, H);   // pass 2: MN-major E^T and P
+    const int rw = 16 * warp;                       // this warp's first tile row
+    bool ok = true;
+
+    pdl_wait();   // slots, counts and staged rows come from earlier kernels
+    int cnt = a.count_l[lb];
+    if (cnt < 0 || cnt > a.S) {
+        if (tid == 0) atomicOr(a.err, kErrBounds);
+        cnt = cnt < 0 ? 0 : a.S;
+    }
+    const int R = kWindow + cnt;
+    const int row0 = it.split * a.split_rows;
+    const int row1 = min(R, row0 + a.split_rows);
+    const int n_tiles = row1 > row0 ? (row1 - row0 + kTileRows - 1) / kTileRows : 0;
+    const int32_t* ph = a.phys + lb * a.S;
 
     // Source of tile row tr: window rows first, then the staged rows in list
     // order; rows past the split end repeat its last row (finite data that the
@@ -228,50 +273,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
             for (int j = 0; j < 4; ++j) v[i][j] = ldg_stream(src + lane + 32 * j);
         }
     };
-    // ... as fp16 into E: d-block (lane >> 4) + 2 j, 16-byte chunk (lane & 15) >> 1, half lane & 1.
-    auto store4 = [&](const float4 (&v)[4][4], int rbase) {
-        unsigned char* e = sm + kOffE + (lane >> 4) * kDBlockE + 8 * (lane & 1);
-        const int chunk = (lane & 15) >> 1;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                *reinterpret_cast<uint2*>(e + 2 * j * kDBlockE + sw128(rbase + i, chunk)) =
-                    make_uint2(pack_f16x2(v[i][j].x, v[i][j].y), pack_f16x2(v[i][j].z, v[i][j].w));
-    };
-
-    constexpr uint32_t id1 = idesc_f16(0, 0, H);   // pass 1: K-major E and Q
-    constexpr uint32_t id2 = idesc_f16(1, 1, H);   // pass 2: MN-major E^T and P
-    const int rw = 16 * warp;                       // this warp's first tile row
-    bool ok = true;
 
     for (int tile = 0; tile < n_tiles; ++tile) {
         // ------------------------------------------------------------ load E (all warps)
         const int tr0 = row0 + tile * kTileRows;
         float4 b0[4][4], b1[4][4];
         if (ok) {
-            if (tile == 0) {
-                // queries: bf16 [H][512] -> fp16 K-major; d-block d / 64 at (d / 64) * 8192, row h
-                constexpr int kPer = H * 64 / kThreads;          // 16-byte chunks per thread
-                const uint16_t* qg = a.q + lb * H * kKvDim;
-                uint4 qv[kPer];
-#pragma unroll
-                for (int k = 0; k < kPer; ++k) {
-                    const int i = tid + k * kThreads;
-                    qv[k] = *reinterpret_cast<const uint4*>(qg + (i >> 6) * kKvDim + (i & 63) * 8);
-                }
-#pragma unroll
-                for (int k = 0; k < kPer; ++k) {
-                    const int i = tid + k * kThreads, h = i >> 6, c8 = i & 63;
-                    const uint4 v = qv[k];
-                    uint4 w;
-                    w.x = pack_f16x2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
-                    w.y = pack_f16x2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
-                    w.z = pack_f16x2(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u));
-                    w.w = pack_f16x2(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
-                    *reinterpret_cast<uint4*>(sm + kOffQ + (c8 >> 3) * 8192 + sw128(h, c8 & 7)) = w;
-                }
-            }
             load4(b0, tr0, rw);
             load4(b1, tr0, rw + 4);
             // the previous tile's pass 2 reads E: wait for it before overwriting
@@ -463,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == 0 && n_tiles > 0) {
+    if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(ms.tmem_base, kTmemCols);
     }
@@ -480,6 +487,7 @@ __global__ void __launch_bounds__(kKvDim / 4) merge_kernel(const MergeItem* __re
                                                            const float* __restrict__ part_ml,
                                                            float* __restrict__ out) {
     __shared__ float m_s[kMaxSplits], l_s[kMaxSplits], w_s[kMaxSplits];
+    pdl_wait();   // the partials come from the attention kernel
     const MergeItem mi = merges[merge0 + blockIdx.x];
     const int h = blockIdx.y;
     const int ns = min(mi.ns, kMaxSplits);
@@ -528,7 +536,7 @@ __global__ void __launch_bounds__(kKvDim / 4) merge_kernel(const MergeItem* __re
 
 template <int H>
 cudaError_t launch_h(const AttnArgs& args, int n_items, const MergeItem* merges, int merge0, int n_merges,
-                     cudaStream_t st) {
+                     cudaStream_t st, bool chained) {
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -536,12 +544,11 @@ cudaError_t launch_h(const AttnArgs& args, int n_items, const MergeItem* merges,
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    attend_tc_kernel<H><<<n_items, kThreads, kSmemBytes, st>>>(args);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_k(attend_tc_kernel<H>, dim3(n_items), dim3(kThreads), kSmemBytes, st, chained, args);
     if (e != cudaSuccess || n_merges <= 0) return e;
-    merge_kernel<H><<<dim3((unsigned)n_merges, H), kKvDim / 4, 0, st>>>(merges, merge0, args.part_o, args.part_ml,
-                                                                        args.out);
-    return cudaGetLastError();
+    // the merge follows its own attention kernel: always chained
+    return launch_k(merge_kernel<H>, dim3((unsigned)n_merges, H), dim3(kKvDim / 4), 0, st, true, merges, merge0,
+                    (const float*)args.part_o, (const float*)args.part_ml, args.out);
 }
 
 }  // namespace
@@ -552,15 +559,15 @@ cudaError_t launch_attend(const AttnItem* items, int item0, int n_items, const M
                           int n_merges, int split_rows, int n_heads, int B, int G, int S, const uint16_t* q,
                           const float* window, const float* staging, const int32_t* phys,
                           const int32_t* count_l, float* out, float* part_o, float* part_ml, uint32_t* err,
-                          cudaStream_t st) {
+                          cudaStream_t st, bool chained) {
     if (n_items <= 0) return cudaSuccess;
     if (split_rows % kTileRows != 0) return cudaErrorInvalidValue;
     AttnArgs args{items, item0, split_rows, B, G, S, q, window, staging, phys, count_l,
                   out, part_o, part_ml, err, (float)(1.4426950408889634 / std::sqrt((double)kKvDim))};
     switch (n_heads) {
-        case 16: return launch_h<16>(args, n_items, merges, merge0, n_merges, st);
-        case 32: return launch_h<32>(args, n_items, merges, merge0, n_merges, st);
-        case 64: return launch_h<64>(args, n_items, merges, merge0, n_merges, st);
+        case 16: return launch_h<16>(args, n_items, merges, merge0, n_merges, st, chained);
+        case 32: return launch_h<32>(args, n_items, merges, merge0, n_merges, st, chained);
+        case 64: return launch_h<64>(args, n_items, merges, merge0, n_merges, st, chained);
         default: return cudaErrorInvalidValue;
     }
 }

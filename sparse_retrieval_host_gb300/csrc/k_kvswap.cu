@@ -110,9 +110,11 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
     const int tid = threadIdx.x;
     const int l = l0 + blockIdx.x / B;
     const int b = blockIdx.x % B;
-    const LayerDev ld = layers[l];
+    pdl_trigger();
+    const LayerDev ld = layers[l];     // written once, at creation
     const long long cap = ld.cap;
     const size_t lb = (size_t)l * B + b;
+    pdl_wait();                        // the selection comes from earlier kernels
 
     // ---- 1. the layer's ordered chunk list: c -> floor(c * src_ratio / ratio), first kept
     int m0 = count[b];
@@ -333,6 +335,8 @@ gather_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S,
               const int2* __restrict__ miss, const int* __restrict__ miss_count,
               float* __restrict__ staging, uint32_t* __restrict__ err) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();
+    pdl_wait();                        // the miss lists come from the resolve kernel
     const size_t lb = (size_t)l0 * B + blockIdx.y;
     const int l = (int)(lb / B), b = (int)(lb % B);
     const int nm = miss_count[lb];
@@ -371,7 +375,7 @@ size_t lru_smem_bytes(int S, int G) {
 cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int S, int src_ratio,
                        long long max_dedup_cap, const int32_t* sel, const int32_t* count,
                        int32_t* phys, int32_t* count_l, int2* miss, int* miss_count,
-                       unsigned long long* stats, uint32_t* err, cudaStream_t st) {
+                       unsigned long long* stats, uint32_t* err, cudaStream_t st, bool chained) {
     // a shared-memory table of first positions for layers whose ratio differs from
     // src_ratio, when it fits; otherwise those layers fall back to pairwise checks
     int tbl = 0;
@@ -384,20 +388,18 @@ cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int
                                              (int)smem);
         if (e != cudaSuccess) return e;
     }
-    lru_kernel<<<nl * B, kLruThreads, smem, st>>>(layers, l0, B, G, S, src_ratio, tbl, sel, count,
-                                                  phys, count_l, miss, miss_count, stats, err);
-    return cudaGetLastError();
+    return launch_k(lru_kernel, dim3(nl * B), dim3(kLruThreads), smem, st, chained, layers, l0, B, G, S, src_ratio,
+                    tbl, sel, count, phys, count_l, miss, miss_count, stats, err);
 }
 
 cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, int S,
                           const int2* miss, const int* miss_count, float* staging, uint32_t* err,
-                          int sm_count, cudaStream_t st) {
+                          int sm_count, cudaStream_t st, bool chained) {
     int bx = (4 * sm_count + nl * B - 1) / (nl * B);
     if (bx < 1) bx = 1;
     if (bx > 64) bx = 64;
-    gather_kernel<<<dim3(bx, nl * B), kGatherWarps * 32, 0, st>>>(layers, l0, B, G, S, miss,
-                                                                   miss_count, staging, err);
-    return cudaGetLastError();
+    return launch_k(gather_kernel, dim3(bx, nl * B), dim3(kGatherWarps * 32), 0, st, chained, layers, l0, B, G, S,
+                    miss, miss_count, staging, err);
 }
 
 cudaError_t launch_resident_fill(const float* pool_dev, const uint8_t* ready, long long cap,

@@ -71,6 +71,7 @@ score_kernel(const uint16_t* __restrict__ keys, int n, const uint16_t* __restric
              float b0, float b1, float b2, int ensemble, float* __restrict__ scores,
              uint32_t* __restrict__ hist) {
     __shared__ uint32_t h_s[kHistBins];
+    pdl_trigger();
     const int b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -158,6 +159,7 @@ score_kernel(const uint16_t* __restrict__ keys, int n, const uint16_t* __restric
 
 __global__ void hist_kernel(const float* __restrict__ scores, int n, uint32_t* __restrict__ hist) {
     __shared__ uint32_t h_s[kHistBins];
+    pdl_trigger();
     const int b = blockIdx.y;
     for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h_s[i] = 0;
     __syncthreads();

@@ -162,6 +162,8 @@ select_kernel(const float* __restrict__ scores, int n, int mode, int k, float th
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
     int32_t* sel_b = sel + (size_t)b * S;
+    pdl_trigger();
+    pdl_wait();   // scores, histogram and candidates come from earlier kernels
 
     // the key universe: a candidate list when one was made and did not overflow
     Src src{scores + (size_t)b * n, nullptr, n};
@@ -367,6 +369,8 @@ collect_kernel(const float* __restrict__ scores, int n, int mode, int K, float t
                int* __restrict__ cand_cnt, int cap) {
     __shared__ int warp_buf[32];
     __shared__ int cut_s, base_s;
+    pdl_trigger();
+    pdl_wait();
     const int b = blockIdx.y, tid = threadIdx.x;
     const float* sc = scores + (size_t)b * n;
     const int i0 = blockIdx.x * (kCollectThreads * kCollectPer) + tid;
@@ -430,7 +434,8 @@ collect_kernel(const float* __restrict__ scores, int n, int mode, int K, float t
 
 cudaError_t launch_select(const float* scores, int n, int B, int mode, int k, float thresh,
                           int clamp, int S, const uint32_t* hist, int32_t* sel, int32_t* count,
-                          cudaStream_t st, const unsigned long long* cand, const int* cand_cnt, int cand_cap) {
+                          cudaStream_t st, const unsigned long long* cand, const int* cand_cnt, int cand_cap,
+                          bool chained) {
     const size_t smem = sizeof(SelShared) + sizeof(unsigned long long) * kArr;
     static bool attr_set = false;
     if (!attr_set) {
@@ -439,9 +444,8 @@ cudaError_t launch_select(const float* scores, int n, int B, int mode, int k, fl
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    select_kernel<<<B, kSelThreads, smem, st>>>(scores, n, mode, k, thresh, clamp, S, hist, cand, cand_cnt,
-                                                cand_cap, sel, count);
-    return cudaGetLastError();
+    return launch_k(select_kernel, dim3(B), dim3(kSelThreads), smem, st, chained, scores, n, mode, k, thresh, clamp, S,
+                    hist, cand, cand_cnt, cand_cap, sel, count);
 }
 
 int select_cand_cap() { return kCandCap; }

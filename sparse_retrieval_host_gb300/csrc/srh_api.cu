@@ -364,6 +364,7 @@ int fm_select(srh_ctx* ctx, const float* d_scores, int n, int mode, int k, float
     }
     cudaStream_t st = (cudaStream_t)stream;
     const uint32_t* hist = nullptr;
+    bool chained = ctx->chained;   // the select kernel follows a kernel of this call or of fm_score
     if (mode == SRH_SELECT_TOPK || clamp > 0) {
         if (ctx->hist_scores == d_scores && ctx->hist_n == n) {
             hist = ctx->d_hist;
@@ -371,6 +372,7 @@ int fm_select(srh_ctx* ctx, const float* d_scores, int n, int mode, int k, float
             const cudaError_t e = launch_hist(d_scores, n, ctx->B, ctx->d_hist, st);
             if (e != cudaSuccess) return cuda_fail(ctx, e, "fm_select histogram");
             hist = ctx->d_hist;
+            chained = true;
         }
     }
     ctx->hist_scores = nullptr;   // one use per scoring pass
@@ -382,9 +384,10 @@ int fm_select(srh_ctx* ctx, const float* d_scores, int n, int mode, int k, float
                                               ctx->d_cand_cnt, select_cand_cap(), st);
         if (ec != cudaSuccess) return cuda_fail(ctx, ec, "fm_select candidate pass");
         cand = ctx->d_cand;
+        chained = true;
     }
     const cudaError_t e = launch_select(d_scores, n, ctx->B, mode, k, thresh, clamp, ctx->S, hist, d_sel,
-                                        d_count, st, cand, ctx->d_cand_cnt, select_cand_cap());
+                                        d_count, st, cand, ctx->d_cand_cnt, select_cand_cap(), chained);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "fm_select launch");
     return SRH_OK;
 }
@@ -418,7 +421,7 @@ int kvswap_stage(srh_ctx* ctx, int layer, const int32_t* d_sel, const int32_t* d
         if (ctx->ratios[l] != ctx->cfg.src_ratio) dedup_cap = std::max(dedup_cap, ctx->caps[l]);
     cudaError_t e = launch_lru(ctx->d_layers, l0, nl, ctx->B, ctx->G, ctx->S, ctx->cfg.src_ratio, dedup_cap,
                                d_sel, d_count, d_phys, d_count_l, ctx->d_miss, ctx->d_miss_count, ctx->d_stats,
-                               ctx->d_err, sm);
+                               ctx->d_err, sm, ctx->chained);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "kvswap_stage LRU launch");
     if (ss && ss != sm) {
         SRH_CUDA(ctx, cudaEventRecord(ctx->ev_resolved, sm));
@@ -426,8 +429,9 @@ int kvswap_stage(srh_ctx* ctx, int layer, const int32_t* d_sel, const int32_t* d
     } else {
         ss = sm;
     }
+    // on the main stream the gather directly follows the resolve kernel: chained
     e = launch_gather(ctx->d_layers, l0, nl, ctx->B, ctx->G, ctx->S, ctx->d_miss, ctx->d_miss_count, d_staging,
-                      ctx->d_err, ctx->sm_count, ss);
+                      ctx->d_err, ctx->sm_count, ss, ss == sm);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "kvswap_stage gather launch");
     if (ss != sm) {
         SRH_CUDA(ctx, cudaEventRecord(ctx->ev_gathered, ss));
@@ -455,8 +459,14 @@ int lsa_attend(srh_ctx* ctx, int layer, const uint16_t* d_q, int n_heads, const 
     const cudaError_t e = launch_attend(ctx->d_items, i0, i1 - i0, ctx->d_merges, m0, m1 - m0, ctx->split_rows,
                                         n_heads, ctx->B, ctx->G, ctx->S, d_q, d_window, d_staging, d_phys,
                                         d_count_l, d_out, ctx->d_part_o, ctx->d_part_ml, ctx->d_err,
-                                        (cudaStream_t)stream);
+                                        (cudaStream_t)stream, ctx->chained);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "lsa_attend launch");
+    return SRH_OK;
+}
+
+int srh_set_chained(srh_ctx* ctx, int on) {
+    if (!ctx) return SRH_ERR_INVALID;
+    ctx->chained = on != 0;
     return SRH_OK;
 }
 

@@ -11,6 +11,30 @@
 
 namespace srh {
 
+// Programmatic dependent launch. A kernel launched with `chained` may start
+// while the previous kernel on the stream is still running: it must call
+// pdl_wait() before it reads anything that kernel (or an earlier one) wrote.
+// pdl_trigger() lets the next chained kernel start as soon as every CTA of
+// this one has issued it. Both are no-ops for a normal launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            bool chained, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = chained ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 constexpr int kKvDim = SRH_KV_DIM;
 constexpr int kWindow = SRH_WINDOW;
 constexpr int kIdx = SRH_N_INDEXERS;
@@ -92,6 +116,7 @@ struct Ctx {
     std::vector<LayerDev> h_layers;
     unsigned long long* d_stats = nullptr;
     uint32_t* d_err = nullptr;
+    bool chained = false;               // srh_set_chained: step kernels may launch early
     uint32_t* d_hist = nullptr;         // [B][kHistBins]
     unsigned long long* d_cand = nullptr; // [B][select_cand_cap()] candidate composites
     int* d_cand_cnt = nullptr;          // [B]
@@ -142,21 +167,21 @@ constexpr int kCollectMinN = 16384;    // fm_select runs the candidate pass abov
 cudaError_t launch_select(const float* scores, int n, int B, int mode, int k, float thresh,
                           int clamp, int S, const uint32_t* hist, int32_t* sel, int32_t* count,
                           cudaStream_t st, const unsigned long long* cand = nullptr,
-                          const int* cand_cnt = nullptr, int cand_cap = 0);
+                          const int* cand_cnt = nullptr, int cand_cap = 0, bool chained = false);
 cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int S, int src_ratio,
                        long long max_dedup_cap, const int32_t* sel, const int32_t* count,
                        int32_t* phys, int32_t* count_l, int2* miss, int* miss_count,
-                       unsigned long long* stats, uint32_t* err, cudaStream_t st);
+                       unsigned long long* stats, uint32_t* err, cudaStream_t st, bool chained);
 cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, int S,
                           const int2* miss, const int* miss_count, float* staging,
-                          uint32_t* err, int sm_count, cudaStream_t st);
+                          uint32_t* err, int sm_count, cudaStream_t st, bool chained);
 cudaError_t launch_resident_fill(const float* pool_dev, const uint8_t* ready, long long cap,
                                  int layer, int B, int G, float* staging, cudaStream_t st);
 cudaError_t launch_attend(const AttnItem* items, int item0, int n_items, const MergeItem* merges, int merge0,
                           int n_merges, int split_rows, int n_heads, int B, int G, int S, const uint16_t* q,
                           const float* window, const float* staging, const int32_t* phys,
                           const int32_t* count_l, float* out, float* part_o, float* part_ml, uint32_t* err,
-                          cudaStream_t st);
+                          cudaStream_t st, bool chained);
 size_t lru_smem_bytes(int S, int G);
 int attend_max_splits();
 

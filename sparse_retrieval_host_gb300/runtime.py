@@ -94,11 +94,17 @@ class DecodeStep:
                        self.phys, self.count_l, self.out if out is None else out, stream)
 
     def step(self, spec: StepSpec, stream=None, side=None, fm_q=None, q=None, out=None) -> None:
-        """One decode step: the four C entry points in order."""
-        self.score(spec, stream, fm_q)
-        self.select(spec, stream)
-        self.stage(-1, stream, side)
-        self.attend(-1, stream, q, out)
+        """One decode step: the four C entry points in order, issued back to back
+        on one stream, so their kernels are launched chained (each may start
+        while the previous one finishes; see srh_set_chained)."""
+        abi.srh_set_chained(self.ctx, True)
+        try:
+            self.score(spec, stream, fm_q)
+            self.select(spec, stream)
+            self.stage(-1, stream, side)
+            self.attend(-1, stream, q, out)
+        finally:
+            abi.srh_set_chained(self.ctx, False)
 
     # ------------------------------------------------------------------ CUDA graphs
     def capture(self, spec: StepSpec, parts: bool = False):

@@ -163,10 +163,11 @@ def test_residency_changes_slots_never_outputs():
 @pytest.mark.parametrize("parts", [False, True], ids=["one_graph", "three_graphs"])
 def test_graph_replay_equals_eager_steps(parts):
     """Steps replayed from captured CUDA graphs give the same bits as eager
-    calls: selections, slots, staged rows, outputs and the swap counters."""
+    calls (chained, through step(), and unchained, call by call): selections,
+    slots, staged rows, outputs and the swap counters."""
     w = C.TINY.with_(steps=12)
     runs = []
-    for mode in ("eager", "graph"):
+    for mode in ("eager", "graph", "unchained"):
         ds = make_ds(w)
         try:
             fill(ds, w)
@@ -177,7 +178,12 @@ def test_graph_replay_equals_eager_steps(parts):
             seq = []
             for t in range(1, w.steps):
                 load_step_inputs(ds, w, t)
-                if graphs is None:
+                if mode == "unchained":
+                    ds.score(spec)
+                    ds.select(spec)
+                    ds.stage(-1)
+                    ds.attend(-1)
+                elif graphs is None:
                     ds.step(spec)
                 else:
                     for g in graphs:
@@ -189,12 +195,13 @@ def test_graph_replay_equals_eager_steps(parts):
             assert ds.check_error() == 0
         finally:
             ds.close()
-    (sa, ha, ma, ga), (sb, hb, mb, gb) = runs
-    assert (ha, ma) == (hb, mb)
-    assert torch.equal(ga, gb)
-    for xa, xb in zip(sa, sb):
-        for a, b in zip(xa, xb):
-            assert torch.equal(a, b)
+    (sa, ha, ma, ga) = runs[0]
+    for (sb, hb, mb, gb) in runs[1:]:
+        assert (ha, ma) == (hb, mb)
+        assert torch.equal(ga, gb)
+        for xa, xb in zip(sa, sb):
+            for a, b in zip(xa, xb):
+                assert torch.equal(a, b)
 
 
 def test_ties_follow_index_order():
