@@ -37,7 +37,8 @@ import numpy as np  # noqa: E402
 from srh_workload import configs as C  # noqa: E402
 from srh_workload import generate as G  # noqa: E402
 
-BASE_KERNELS = 5              # score, select, lru, gather, attend (+ merge when a layer has splits)
+BASE_KERNELS = 5              # score, select, lru, gather, attend (+ merge, + candidate pass)
+COLLECT_MIN_N = 16384         # fm_select runs its candidate pass above this many chunks
 Q_CYCLE = 16                  # distinct attention-query sets cycled through the steps
 FLUSH_BYTES = 256 << 20       # > 2x the 126 MiB L2
 METRIC = "decode steps/s"
@@ -201,7 +202,9 @@ def launches_per_step(w, sm_count):
     (split rows = rows of all layers / SM count, rounded up to 128)."""
     rows = [C.WINDOW + min(w.clamp, -(-w.context_len // r)) for r in w.layer_ratios]
     split = max(128, -(-(-(-w.batch * sum(rows) // sm_count)) // 128) * 128)
-    return BASE_KERNELS + (1 if any(-(-r // split) > 1 for r in rows) else 0)
+    merge = 1 if any(-(-r // split) > 1 for r in rows) else 0
+    collect = 1 if w.n_chunks > COLLECT_MIN_N else 0      # fm_select's candidate pass
+    return BASE_KERNELS + merge + collect
 
 
 def score_bytes(w):
