@@ -333,6 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
             for (int i = 0; i < 16; ++i) v[c + i] = t16[i];
         }
         tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < H; c += 16) tmem_regs_ready(v + c);
         const bool valid = tr0 + r < row1;
 #pragma unroll
         for (int h = 0; h < 64; ++h) v[h] = (h < H && valid) ? v[h] * a.sl2 : -INFINITY;
@@ -382,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
                     const uint32_t ta = tmem + lane_base + kColO + 64 * mb + c;
                     tmem_ld16(ta, t16);
                     tmem_ld_wait();
+                    tmem_regs_ready(t16);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) t16[i] *= ms.alpha[c + i];
                     tmem_st16(ta, t16);
@@ -445,17 +448,17 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         for (int mm = 0; mm < 2; ++mm) {
             const int mb = 2 * (warp >> 2) + mm;
             const int d = mb * 128 + (warp & 3) * 32 + lane;
+            // all H columns of this d-block in one TMEM round trip
+            float t[H];
 #pragma unroll
-            for (int c = 0; c < H; c += 16) {
-                float t16[16];
-                tmem_ld16(tmem + lane_base + kColO + 64 * mb + c, t16);
-                tmem_ld_wait();
+            for (int c = 0; c < H; c += 16) tmem_ld16(tmem + lane_base + kColO + 64 * mb + c, *reinterpret_cast<float(*)[16]>(t + c));
+            tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int h = c + i;
-                    if (single) dst[h * kKvDim + d] = t16[i] * ms.alpha[h];
-                    else __stcg(&dst[h * kKvDim + d], t16[i]);
-                }
+            for (int c = 0; c < H; c += 16) tmem_regs_ready(t + c);
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                if (single) dst[h * kKvDim + d] = t[h] * ms.alpha[h];
+                else __stcg(&dst[h * kKvDim + d], t[h]);
             }
         }
     } else if (!single) {

@@ -105,7 +105,8 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
     int* nh = hit_time + G;      // [G]
     int* victim = nh + G;        // [G]
     int* flag = victim + G;      // [G]
-    int* first = flag + G;       // [dedup_tbl]: first list position of each mapped chunk
+    int* ready = flag + G;       // [S] host_ready of each listed chunk
+    int* first = ready + S;      // [dedup_tbl]: first list position of each mapped chunk
 
     const int tid = threadIdx.x;
     const int l = l0 + blockIdx.x / B;
@@ -197,6 +198,7 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
     for (int p = tid; p < m; p += blockDim.x) {
         const int c = r[p];
         int s = slot_of[c];
+        ready[p] = ld.host_ready[(size_t)b * cap + c];   // read with the slot, used for misses
         if (s >= G) {
             atomicOr(err, kErrBounds);
             s = -1;
@@ -306,7 +308,7 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
             slot_of[c] = s;
             slot_logical[s] = c;
             miss_lb[mr[p]] = make_int2(c, s);
-            if (!ld.host_ready[(size_t)b * cap + c]) atomicOr(err, kErrNotStored);
+            if (!ready[p]) atomicOr(err, kErrNotStored);
         }
     }
     if (tid == 0) {
@@ -369,7 +371,7 @@ resident_fill_kernel(const float* __restrict__ pool, const uint8_t* __restrict__
 }  // namespace
 
 size_t lru_smem_bytes(int S, int G) {
-    return sizeof(LruShared) + sizeof(int) * (6 * (size_t)S + 6 * (size_t)G);
+    return sizeof(LruShared) + sizeof(int) * (7 * (size_t)S + 6 * (size_t)G);
 }
 
 cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int S, int src_ratio,

@@ -155,6 +155,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+// After tmem_ld_wait(): make every later use of these registers depend on a
+// point after the wait, so the compiler cannot move arithmetic on them above it.
+__device__ __forceinline__ void tmem_regs_ready(float* v) {
+    asm volatile("" : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]),
+                 "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]),
+                 "+f"(v[14]), "+f"(v[15]));
+}
 
 // ---------------------------------------------------------------- bulk copies (TMA, async proxy)
 // Arrive on `bar` and raise its expected transaction bytes by `bytes`.
