@@ -171,6 +171,24 @@ float* srh_pool_host_ptr(srh_ctx* ctx, int layer, int seq);
  * layers re-copy those chunks into their staging rows on the next kvswap_stage. */
 int srh_mark_stored(srh_ctx* ctx, int layer, int seq, long long c0, long long n);
 
+/*
+ * Store flow on the device ([P1] KV_SWAP 实现细节, Store: the compressor made a
+ * new chunk; D2H it to h_compressed_kv[logical], set host_ready[logical], and a
+ * chunk that is in a GPU staging slot stays there).
+ *   layer, seq  the (layer, sequence) the chunks belong to
+ *   c0, n       chunks [c0, c0+n) of that layer, 0 <= c0, c0 + n <= cap
+ *   d_rows      [n][kv_dim] fp32 device rows, read by the call's kernel
+ * One kernel copies each row into the pinned host pool (zero-copy writes),
+ * sets host_ready, and keeps the staging consistent: a chunk that currently
+ * holds a staging slot keeps it and its staged row gets the new content; on a
+ * layer that does not swap, staging row c gets it. Nothing is evicted.
+ * Asynchronous on `stream`: issue it before the kvswap_stage that may select
+ * these chunks, on the same stream. Counts n * kv_dim * 4 bytes in d2h_bytes.
+ * Errors: SRH_ERR_INVALID (range, pointers), SRH_ERR_CUDA.
+ */
+int kvswap_store(srh_ctx* ctx, int layer, int seq, long long c0, int n, const float* d_rows,
+                 srh_stream_t stream);
+
 /* Layer facts: chunk capacity and whether the layer swaps (cap > gpu_chunks,
  * [P1] 故障排查, the swap auto-disable note). */
 int srh_layer_info(srh_ctx* ctx, int layer, long long* cap, int* swap_enabled);

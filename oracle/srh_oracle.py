@@ -305,16 +305,32 @@ class DecodeOracle:
             for st in row:
                 st.host_ready[:] = 1
 
+    def store(self, layer: int, seq: int, c0: int, n: int) -> None:
+        """Store flow (section "KV_SWAP 实现细节", Store): chunks [c0, c0+n) of
+        (layer, seq) now exist in the host cache. The swap state is untouched: a
+        chunk already in a staging slot keeps it. The new content itself is
+        whatever the caller's ``pool_rows_of`` returns from now on."""
+        for c in range(c0, c0 + n):
+            self.states[layer][seq].store(c)
+
     def step(self, keys_of: Callable[[int], np.ndarray], fm_q_of: Callable[[int], np.ndarray],
              attn_q_of: Optional[Callable[[int, int], np.ndarray]] = None,
              window_of: Optional[Callable[[int, int], np.ndarray]] = None,
              pool_rows_of: Optional[Callable[[int, int, Sequence[int]], np.ndarray]] = None,
-             attend_pairs: Optional[Sequence[Tuple[int, int]]] = None) -> StepResult:
-        scores, sels = [], []
-        for b in range(self.batch):
-            s = score(keys_of(b), fm_q_of(b), self.scale, self.bias, self.ensemble_mode)
-            scores.append(s)
-            sels.append(select(s, self.select_mode, self.index_topk, self.tau, self.clamp))
+             attend_pairs: Optional[Sequence[Tuple[int, int]]] = None, rescore: bool = True) -> StepResult:
+        """One decode step. With ``rescore=False`` the step reuses the previous
+        step's scores and selection (the memory indexer fires periodically,
+        summary section "LSA 让模型预判 KV chunk"): only the swap-in and the
+        attention run."""
+        if rescore or not hasattr(self, "_last"):
+            scores, sels = [], []
+            for b in range(self.batch):
+                s = score(keys_of(b), fm_q_of(b), self.scale, self.bias, self.ensemble_mode)
+                scores.append(s)
+                sels.append(select(s, self.select_mode, self.index_topk, self.tau, self.clamp))
+            self._last = (scores, sels)
+        else:
+            scores, sels = self._last
         lists, swaps = [], []
         for l, ratio in enumerate(self.layer_ratios):
             row_l, row_s = [], []

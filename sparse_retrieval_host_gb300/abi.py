@@ -88,6 +88,7 @@ SIGNATURES = [
     ("srh_pinned_required_bytes", _i, [ctypes.POINTER(SrhConfig), ctypes.POINTER(ctypes.c_ulonglong)]),
     ("srh_pool_host_ptr", ctypes.POINTER(_f), [_vp, _i, _i]),
     ("srh_mark_stored", _i, [_vp, _i, _i, _ll, _ll]),
+    ("kvswap_store", _i, [_vp, _i, _i, _ll, _i, _vp, _vp]),
     ("srh_layer_info", _i, [_vp, _i, ctypes.POINTER(_ll), ctypes.POINTER(_i)]),
     ("srh_max_select", _i, [_vp]),
     ("fm_score", _i, [_vp, _vp, _i, _vp, _f, ctypes.POINTER(_f), _i, _vp, _vp]),
@@ -191,6 +192,10 @@ def srh_pool_host_ptr(ctx: int, layer: int, seq: int) -> int:
 
 def srh_mark_stored(ctx: int, layer: int, seq: int, c0: int, n: int) -> None:
     _check(load().srh_mark_stored(ctx, layer, seq, c0, n), "srh_mark_stored", ctx)
+
+
+def kvswap_store(ctx, layer, seq, c0, n, rows, stream=None) -> None:
+    _check(load().kvswap_store(ctx, layer, seq, c0, n, _ptr(rows), _stream(stream)), "kvswap_store", ctx)
 
 
 def srh_layer_info(ctx: int, layer: int):

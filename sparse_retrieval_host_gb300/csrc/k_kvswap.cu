@@ -368,6 +368,41 @@ resident_fill_kernel(const float* __restrict__ pool, const uint8_t* __restrict__
     }
 }
 
+
+// Store flow: rows [n][512] of chunks c0.. of (layer, seq) go to the pinned pool
+// (zero-copy writes over the host link), host_ready is set, and the staging
+// stays consistent: a staged chunk keeps its slot with the new row; a layer
+// that does not swap gets row c. One warp per row.
+__global__ void __launch_bounds__(kGatherWarps * 32)
+store_kernel(const LayerDev* __restrict__ layers, int l, int B, int G, int seq, long long c0, int n,
+             const float* __restrict__ rows, float* __restrict__ staging, uint32_t* __restrict__ err) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const LayerDev ld = layers[l];
+    float* pool = const_cast<float*>(ld.pool) + (size_t)seq * ld.cap * kKvDim;
+    float* stg = staging ? staging + ((size_t)l * B + seq) * G * kKvDim : nullptr;
+    for (int i = blockIdx.x * kGatherWarps + warp; i < n; i += gridDim.x * kGatherWarps) {
+        const long long c = c0 + i;
+        if (c < 0 || c >= ld.cap) {
+            if (lane == 0) atomicOr(err, kErrBounds);
+            continue;
+        }
+        const float* src = rows + (size_t)i * kKvDim;
+        copy_row(pool + c * kKvDim, src, lane);
+        if (stg) {
+            long long row = -1;
+            if (ld.swap) {
+                const int s = ld.slot_of[(size_t)seq * ld.cap + c];
+                if (s >= 0 && s < G) row = s;
+            } else if (c < G) {
+                row = c;
+            }
+            if (row >= 0) copy_row(stg + row * kKvDim, src, lane);
+        }
+        __syncwarp();
+        if (lane == 0) ld.host_ready[(size_t)seq * ld.cap + c] = 1;
+    }
+    __threadfence_system();   // the pool rows are host memory read by later kernels
+}
 }  // namespace
 
 size_t lru_smem_bytes(int S, int G) {
@@ -402,6 +437,14 @@ cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, 
     if (bx > 64) bx = 64;
     return launch_k(gather_kernel, dim3(bx, nl * B), dim3(kGatherWarps * 32), 0, st, chained, layers, l0, B, G, S,
                     miss, miss_count, staging, err);
+}
+
+cudaError_t launch_store(const LayerDev* layers, int l, int B, int G, int seq, long long c0, int n,
+                         const float* rows, float* staging, uint32_t* err, cudaStream_t st) {
+    int bx = (n + kGatherWarps - 1) / kGatherWarps;
+    if (bx > 1024) bx = 1024;
+    store_kernel<<<bx, kGatherWarps * 32, 0, st>>>(layers, l, B, G, seq, c0, n, rows, staging, err);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_resident_fill(const float* pool_dev, const uint8_t* ready, long long cap,

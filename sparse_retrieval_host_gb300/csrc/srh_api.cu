@@ -320,6 +320,27 @@ int srh_mark_stored(srh_ctx* ctx, int layer, int seq, long long c0, long long n)
     return SRH_OK;
 }
 
+int kvswap_store(srh_ctx* ctx, int layer, int seq, long long c0, int n, const float* d_rows,
+                 srh_stream_t stream) {
+    if (!ctx) return SRH_ERR_INVALID;
+    if (!d_rows) return fail(ctx, SRH_ERR_INVALID, "NULL pointer");
+    if (layer < 0 || layer >= ctx->L || seq < 0 || seq >= ctx->B)
+        return fail(ctx, SRH_ERR_INVALID, "layer or seq out of range");
+    const long long cap = ctx->caps[layer];
+    if (c0 < 0 || n < 0 || c0 + n > cap) return fail(ctx, SRH_ERR_INVALID, "chunk range out of bounds");
+    if (((uintptr_t)d_rows) & 15) return fail(ctx, SRH_ERR_INVALID, "rows must be 16-byte aligned");
+    if (n == 0) return SRH_OK;
+    // a layer that does not swap gets its staging rows written directly once the
+    // staging is bound; before that, the next kvswap_stage fills them
+    if (!ctx->swap[layer] && !ctx->staging) ctx->resident_dirty[layer] = 1;
+    const cudaError_t e = launch_store(ctx->d_layers, layer, ctx->B, ctx->G, seq, c0, n, d_rows, ctx->staging,
+                                       ctx->d_err, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "kvswap_store launch");
+    std::memset(ctx->ready_host[layer].data() + (size_t)seq * cap + c0, 1, (size_t)n);
+    ctx->stored_bytes += (unsigned long long)n * kKvDim * sizeof(float);
+    return SRH_OK;
+}
+
 int srh_layer_info(srh_ctx* ctx, int layer, long long* cap, int* swap_enabled) {
     if (!ctx || layer < 0 || layer >= ctx->L) return SRH_ERR_INVALID;
     if (cap) *cap = ctx->caps[layer];
@@ -479,7 +500,7 @@ int srh_get_stats(srh_ctx* ctx, srh_stats* out) {
     out->hits = s[kStatHits];
     out->misses = s[kStatMisses];
     out->h2d_bytes = s[kStatMisses] * kKvDim * sizeof(float);
-    out->d2h_bytes = 0;
+    out->d2h_bytes = ctx->stored_bytes;
     out->resident_fill_bytes = ctx->resident_fill_bytes;
     out->stage_calls = ctx->stage_calls;
     out->selected = s[kStatSelected];
@@ -496,6 +517,7 @@ int srh_reset_stats(srh_ctx* ctx) {
     SRH_CUDA(ctx, cudaMemset(ctx->d_stats, 0, sizeof(unsigned long long) * kStatCount));
     SRH_CUDA(ctx, cudaDeviceSynchronize());
     ctx->stage_calls = 0;
+    ctx->stored_bytes = 0;
     return SRH_OK;
 }
 

@@ -140,6 +140,7 @@ struct Ctx {
     cudaEvent_t ev_gathered = nullptr;
     unsigned long long stage_calls = 0;
     unsigned long long resident_fill_bytes = 0;
+    unsigned long long stored_bytes = 0;   // kvswap_store: rows written to the host pool
     std::string last_error;
 };
 
@@ -175,6 +176,8 @@ cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int
 cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, int S,
                           const int2* miss, const int* miss_count, float* staging,
                           uint32_t* err, int sm_count, cudaStream_t st, bool chained);
+cudaError_t launch_store(const LayerDev* layers, int l, int B, int G, int seq, long long c0, int n,
+                         const float* rows, float* staging, uint32_t* err, cudaStream_t st);
 cudaError_t launch_resident_fill(const float* pool_dev, const uint8_t* ready, long long cap,
                                  int layer, int B, int G, float* staging, cudaStream_t st);
 cudaError_t launch_attend(const AttnItem* items, int item0, int n_items, const MergeItem* merges, int merge0,

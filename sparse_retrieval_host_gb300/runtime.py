@@ -76,6 +76,12 @@ class DecodeStep:
             n = self.caps[layer] - c0
         abi.srh_mark_stored(self.ctx, layer, seq, c0, n)
 
+    def store(self, layer: int, seq: int, c0: int, rows: torch.Tensor, stream=None) -> None:
+        """Store flow on the device: ``rows`` [n][512] fp32 (CUDA) become chunks
+        c0.. of (layer, seq) in the host pool (see kvswap_store)."""
+        rows = rows.contiguous()
+        abi.kvswap_store(self.ctx, layer, seq, c0, rows.shape[0], rows, stream)
+
     # ------------------------------------------------------------------ the step
     def score(self, spec: StepSpec, stream=None, fm_q=None) -> None:
         abi.fm_score(self.ctx, self.keys, self.n, self.fm_q if fm_q is None else fm_q, spec.scale,
@@ -93,21 +99,33 @@ class DecodeStep:
         abi.lsa_attend(self.ctx, layer, self.q if q is None else q, self.H, self.window, self.staging,
                        self.phys, self.count_l, self.out if out is None else out, stream)
 
-    def step(self, spec: StepSpec, stream=None, side=None, fm_q=None, q=None, out=None) -> None:
+    def step(self, spec: StepSpec, stream=None, side=None, fm_q=None, q=None, out=None,
+             rescore: bool = True) -> None:
         """One decode step: the four C entry points in order, issued back to back
         on one stream, so their kernels are launched chained (each may start
-        while the previous one finishes; see srh_set_chained)."""
-        abi.srh_set_chained(self.ctx, True)
+        while the previous one finishes; see srh_set_chained).
+
+        With ``rescore=False`` the step keeps the current selection (``sel``,
+        ``count``) and runs only the swap-in and the attention: the memory
+        indexer fires periodically, once per lookahead window (summary section
+        "LSA 让模型预判 KV chunk"), not at every step."""
+        # the step's first kernel waits for all earlier work on the stream; the
+        # ones after it are chained
         try:
-            self.score(spec, stream, fm_q)
-            self.select(spec, stream)
-            self.stage(-1, stream, side)
+            if rescore:
+                self.score(spec, stream, fm_q)
+                abi.srh_set_chained(self.ctx, True)
+                self.select(spec, stream)
+                self.stage(-1, stream, side)
+            else:
+                self.stage(-1, stream, side)
+                abi.srh_set_chained(self.ctx, True)
             self.attend(-1, stream, q, out)
         finally:
             abi.srh_set_chained(self.ctx, False)
 
     # ------------------------------------------------------------------ CUDA graphs
-    def capture(self, spec: StepSpec, parts: bool = False):
+    def capture(self, spec: StepSpec, parts: bool = False, rescore: bool = True):
         """Record the decode step into CUDA graphs and return them.
 
         The graphs read the bound inputs (``fm_q``, ``q``) and write the bound
@@ -136,7 +154,7 @@ class DecodeStep:
             rec(lambda: (self.select(spec), self.stage(-1)))
             rec(lambda: self.attend(-1))
         else:
-            rec(lambda: self.step(spec))
+            rec(lambda: self.step(spec, rescore=rescore))
         torch.cuda.current_stream(dev).wait_stream(s)
         return graphs
 

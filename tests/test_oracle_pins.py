@@ -312,6 +312,46 @@ def test_lru_not_stored_error():
         st.swap_in_selected([3, 7])
 
 
+def test_store_keeps_a_staged_chunk_and_enables_a_new_one():
+    """Store flow (KV_SWAP 实现细节, Store): storing sets host_ready; a chunk that
+    is already in a staging slot stays there (the store evicts nothing)."""
+    st = O.KvSwapLayerState(10, 2)
+    for c in (1, 2):
+        st.store(c)
+    r1 = st.swap_in_selected([1, 2])
+    before = (dict(st.slot_by_logical), list(st.slot_lru), list(st.gpu_slot_logical))
+    st.store(1)                                   # re-store a staged chunk
+    st.store(5)                                   # a new chunk
+    assert (dict(st.slot_by_logical), list(st.slot_lru), list(st.gpu_slot_logical)) == before
+    r2 = st.swap_in_selected([1])                 # still staged: a hit in its old slot
+    assert r2.hits == 1 and r2.phys == [r1.phys[0]]
+    r3 = st.swap_in_selected([5])                 # now allowed; takes the least recent slot (chunk 2's)
+    assert r3.misses == [(5, 1)]
+
+
+def test_decode_oracle_store_and_periodic_selection():
+    """DecodeOracle.store marks chunks of one (layer, seq) only; a step with
+    rescore=False reuses the previous selection, so a repeated selection is all
+    hits (the indexer fires once per lookahead window)."""
+    w = C.TINY
+    ora = O.DecodeOracle(context_len=w.context_len, layer_ratios=(4, 4), gpu_chunks=w.gpu_chunks,
+                         index_topk=w.index_topk, batch=2, scale=w.scale, bias=[0.0] * 3,
+                         ensemble_mode=w.ensemble, select_mode=w.select_mode, tau=w.tau, clamp=w.clamp)
+    ora.store(1, 0, 10, 5)
+    assert ora.states[1][0].host_ready[10:15].all() and not ora.states[1][0].host_ready[15]
+    assert not ora.states[0][0].host_ready.any() and not ora.states[1][1].host_ready.any()
+    ora.mark_all_stored()
+    keys = [G.keys(w, b) for b in range(2)]
+    r0 = ora.step(lambda b: keys[b], lambda b: G.fm_queries(w, 0, b))
+    other = lambda b: G.fm_queries(w, 8, b)       # would change the selection if it were scored
+    r1 = ora.step(lambda b: keys[b], other, rescore=False)
+    for b in range(2):
+        assert np.array_equal(r1.sel[b], r0.sel[b])
+        assert r1.swap[0][b].hits == len(r1.lists[0][b]) and not r1.swap[0][b].misses
+    r2 = ora.step(lambda b: keys[b], other)       # rescored: a new needle set
+    assert not all(np.array_equal(r2.sel[b], r0.sel[b]) for b in range(2))
+
+
 def test_swap_disabled_layer_is_identity_mapped():
     st = O.KvSwapLayerState(16, 16)
     st.host_ready[:] = 1
