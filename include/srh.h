@@ -214,6 +214,17 @@ int fm_score(srh_ctx* ctx, const uint16_t* d_keys, int n, const uint16_t* d_q, f
              const float* bias3, int ensemble, float* d_scores, srh_stream_t stream);
 
 /*
+ * fm_score with one key set per memory indexer ([P1] 限制与未来工作,
+ * "Multi-layer compressed_k": each FlashMemory scorer reads the indexer keys of
+ * its own layer, l10/l12/l20, instead of one shared source layer).
+ *   d_keys3  [3][batch][n][128] bf16: key set i is scored by indexer i
+ * Everything else as fm_score, with s_i(c) = scale * max_h <Q[i,h], K_i[c]> + b_i;
+ * the key stream is three times that of fm_score.
+ */
+int fm_score_multi(srh_ctx* ctx, const uint16_t* d_keys3, int n, const uint16_t* d_q, float scale,
+                   const float* bias3, int ensemble, float* d_scores, srh_stream_t stream);
+
+/*
  * a3: selection ([P1] 架构概览 step 3: global top-k; [P2] LSA: sigmoid threshold).
  *   d_scores [batch][n] fp32
  *   mode     SRH_SELECT_TOPK: the min(k, n) best chunks;

@@ -127,6 +127,22 @@ def score(keys_bits, q_bits, scale, bias, mode) -> np.ndarray:
     return ensemble(indexer_logits(keys_bits, q_bits, scale, bias), mode)
 
 
+def indexer_logits_multi(keys3_bits, q_bits, scale: float, bias: Sequence[float]) -> np.ndarray:
+    """One key set per indexer (section "限制与未来工作", Multi-layer compressed_k:
+    each scorer reads its own layer's indexer keys):
+    s_i(c) = scale * max_h <Q[i,h,:], K_i[c,:]> + b_i: ``[3][n]``."""
+    q = bf16_to_f64(q_bits).reshape(N_INDEXERS, INDEXER_HEADS, INDEXER_DIM)
+    rows = []
+    for i in range(N_INDEXERS):
+        k = bf16_to_f64(np.asarray(keys3_bits)[i])   # [n][128]
+        rows.append(scale * (k @ q[i].T).max(axis=1) + float(bias[i]))
+    return np.stack(rows)
+
+
+def score_multi(keys3_bits, q_bits, scale, bias, mode) -> np.ndarray:
+    return ensemble(indexer_logits_multi(keys3_bits, q_bits, scale, bias), mode)
+
+
 # ----------------------------------------------------------------------------
 # 3. Selection
 # ----------------------------------------------------------------------------
@@ -325,7 +341,9 @@ class DecodeOracle:
         if rescore or not hasattr(self, "_last"):
             scores, sels = [], []
             for b in range(self.batch):
-                s = score(keys_of(b), fm_q_of(b), self.scale, self.bias, self.ensemble_mode)
+                k = np.asarray(keys_of(b))
+                sc = score_multi if k.ndim == 3 else score   # [3][n][128]: per-indexer key sets
+                s = sc(k, fm_q_of(b), self.scale, self.bias, self.ensemble_mode)
                 scores.append(s)
                 sels.append(select(s, self.select_mode, self.index_topk, self.tau, self.clamp))
             self._last = (scores, sels)

@@ -92,6 +92,7 @@ SIGNATURES = [
     ("srh_layer_info", _i, [_vp, _i, ctypes.POINTER(_ll), ctypes.POINTER(_i)]),
     ("srh_max_select", _i, [_vp]),
     ("fm_score", _i, [_vp, _vp, _i, _vp, _f, ctypes.POINTER(_f), _i, _vp, _vp]),
+    ("fm_score_multi", _i, [_vp, _vp, _i, _vp, _f, ctypes.POINTER(_f), _i, _vp, _vp]),
     ("fm_select", _i, [_vp, _vp, _i, _i, _i, _f, _i, _vp, _vp, _vp]),
     ("fm_select_noalloc", _i, [_vp, _i, _i, _i, _i, _f, _i, _i, _vp, _vp, _vp, ctypes.c_char_p, ctypes.c_size_t]),
     ("kvswap_stage", _i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
@@ -212,6 +213,12 @@ def fm_score(ctx, keys, n, q, scale, bias3, ensemble, scores, stream=None) -> No
     b = (ctypes.c_float * 3)(*[float(x) for x in bias3])
     _check(load().fm_score(ctx, _ptr(keys), n, _ptr(q), float(scale), b, ensemble, _ptr(scores),
                            _stream(stream)), "fm_score", ctx)
+
+
+def fm_score_multi(ctx, keys3, n, q, scale, bias3, ensemble, scores, stream=None) -> None:
+    b = (ctypes.c_float * 3)(*[float(x) for x in bias3])
+    _check(load().fm_score_multi(ctx, _ptr(keys3), n, _ptr(q), float(scale), b, ensemble, _ptr(scores),
+                                 _stream(stream)), "fm_score_multi", ctx)
 
 
 def fm_select(ctx, scores, n, mode, k, tau, clamp, sel, count, stream=None) -> None:

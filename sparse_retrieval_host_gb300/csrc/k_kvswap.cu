@@ -403,6 +403,17 @@ store_kernel(const LayerDev* __restrict__ layers, int l, int B, int G, int seq, 
     }
     __threadfence_system();   // the pool rows are host memory read by later kernels
 }
+
+// One read per 4 KiB of a pool range, so the device side of the host page
+// mappings is set up before the first miss gathers need them (random rows of
+// pages the GPU has never read are several times slower to fetch).
+__global__ void touch_kernel(const float* __restrict__ p, long long n_pages, uint32_t* __restrict__ sink) {
+    uint32_t acc = 0;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_pages;
+         i += (long long)gridDim.x * blockDim.x)
+        acc ^= __float_as_uint(p[i * 1024]);
+    if (acc == 0x9e3779b9u) *sink = acc;   // keeps the loads; practically never taken
+}
 }  // namespace
 
 size_t lru_smem_bytes(int S, int G) {
@@ -437,6 +448,15 @@ cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, 
     if (bx > 64) bx = 64;
     return launch_k(gather_kernel, dim3(bx, nl * B), dim3(kGatherWarps * 32), 0, st, chained, layers, l0, B, G, S,
                     miss, miss_count, staging, err);
+}
+
+cudaError_t launch_touch(const float* p, long long n_floats, uint32_t* sink, int sm_count, cudaStream_t st) {
+    const long long pages = (n_floats + 1023) / 1024;
+    if (pages <= 0) return cudaSuccess;
+    long long bx = (pages + 255) / 256;
+    if (bx > 8LL * sm_count) bx = 8LL * sm_count;
+    touch_kernel<<<(unsigned)bx, 256, 0, st>>>(p, pages, sink);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_store(const LayerDev* layers, int l, int B, int G, int seq, long long c0, int n,

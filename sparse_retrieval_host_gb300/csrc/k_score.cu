@@ -66,9 +66,12 @@ __device__ __forceinline__ void load_tile(KeyTile& kt, const uint16_t* keys_b, l
     }
 }
 
-__global__ void __launch_bounds__(kScoreWarps * 32)
-score_kernel(const uint16_t* __restrict__ keys, int n, const uint16_t* __restrict__ q, float scale,
-             float b0, float b1, float b2, int ensemble, float* __restrict__ scores,
+// kSets = 1: one key set shared by the three indexers; kSets = 3: indexer i
+// scores against its own key set i (key sets `set_stride` elements apart).
+template <int kSets>
+__global__ void __launch_bounds__(kScoreWarps * 32, kSets == 1 ? 2 : 1)
+score_kernel(const uint16_t* __restrict__ keys, long long set_stride, int n, const uint16_t* __restrict__ q,
+             float scale, float b0, float b1, float b2, int ensemble, float* __restrict__ scores,
              uint32_t* __restrict__ hist) {
     __shared__ uint32_t h_s[kHistBins];
     pdl_trigger();
@@ -101,24 +104,30 @@ score_kernel(const uint16_t* __restrict__ keys, int n, const uint16_t* __restric
     long long tile = (long long)blockIdx.x * kScoreWarps + warp;
     const float bias[3] = {b0, b1, b2};
 
+    // one unit = (tile, key set); the next unit's keys load while this one's MMAs run
     KeyTile cur, nxt;
     if (tile < n_tiles) load_tile(cur, keys_b, tile * 16, n, g, t);
     for (; tile < n_tiles; tile += stride) {
         const long long next = tile + stride;
-        if (next < n_tiles) load_tile(nxt, keys_b, next * 16, n, g, t);
-
         float acc[kIdx][4];
 #pragma unroll
         for (int i = 0; i < kIdx; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int u = 0; u < kSets; ++u) {
+            if (u + 1 < kSets) load_tile(nxt, keys_b + (u + 1) * set_stride, tile * 16, n, g, t);
+            else if (next < n_tiles) load_tile(nxt, keys_b, next * 16, n, g, t);
 #pragma unroll
-            for (int i = 0; i < kIdx; ++i) {
-                mma_bf16(acc[i], cur.r0[j].x, cur.r1[j].x, cur.r0[j].y, cur.r1[j].y,
-                         bq[i][2 * j][0], bq[i][2 * j][1]);
-                mma_bf16(acc[i], cur.r0[j].z, cur.r1[j].z, cur.r0[j].w, cur.r1[j].w,
-                         bq[i][2 * j + 1][0], bq[i][2 * j + 1][1]);
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                for (int i = 0; i < kIdx; ++i) {
+                    if (kSets != 1 && i != u) continue;   // per-set keys: indexer u only
+                    mma_bf16(acc[i], cur.r0[j].x, cur.r1[j].x, cur.r0[j].y, cur.r1[j].y,
+                             bq[i][2 * j][0], bq[i][2 * j][1]);
+                    mma_bf16(acc[i], cur.r0[j].z, cur.r1[j].z, cur.r0[j].w, cur.r1[j].w,
+                             bq[i][2 * j + 1][0], bq[i][2 * j + 1][1]);
+                }
             }
+            if (u + 1 < kSets) cur = nxt;
         }
         // max over the 8 heads of each indexer: 2 in-thread, 4 lanes of the quad
         float sa[kIdx], sb[kIdx];
@@ -177,7 +186,7 @@ __global__ void hist_kernel(const float* __restrict__ scores, int n, uint32_t* _
 
 cudaError_t launch_score(const uint16_t* keys, int n, int B, const uint16_t* q, float scale,
                          const float* bias3, int ensemble, float* scores, uint32_t* hist,
-                         int sm_count, cudaStream_t st) {
+                         int sm_count, cudaStream_t st, int key_sets) {
     cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(uint32_t) * kHistBins * B, st);
     if (e != cudaSuccess) return e;
     const long long tiles = (n + 15) / 16;
@@ -186,8 +195,13 @@ cudaError_t launch_score(const uint16_t* keys, int n, int B, const uint16_t* q, 
     if (bx > cap) bx = cap;
     if (bx < 1) bx = 1;
     dim3 grid((unsigned)bx, (unsigned)B);
-    score_kernel<<<grid, kScoreWarps * 32, 0, st>>>(keys, n, q, scale, bias3[0], bias3[1],
-                                                    bias3[2], ensemble, scores, hist);
+    const long long set_stride = (long long)B * n * kIdxDim;
+    if (key_sets == 3)
+        score_kernel<3><<<grid, kScoreWarps * 32, 0, st>>>(keys, set_stride, n, q, scale, bias3[0], bias3[1],
+                                                           bias3[2], ensemble, scores, hist);
+    else
+        score_kernel<1><<<grid, kScoreWarps * 32, 0, st>>>(keys, 0, n, q, scale, bias3[0], bias3[1], bias3[2],
+                                                           ensemble, scores, hist);
     return cudaGetLastError();
 }
 

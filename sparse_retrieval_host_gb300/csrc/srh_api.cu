@@ -53,6 +53,7 @@ int cuda_fail(srh_ctx* ctx, cudaError_t e, const char* where) {
 
 long long cap_of(long long ctx_len, int ratio) { return (ctx_len + ratio - 1) / ratio; }
 
+
 int validate_config(const srh_config* c, std::string* why) {
     if (!c) { *why = "config is NULL"; return SRH_ERR_INVALID; }
     if (c->batch < 1) { *why = "batch must be >= 1"; return SRH_ERR_INVALID; }
@@ -117,6 +118,7 @@ void free_ctx(srh_ctx* ctx) {
     cudaFree(ctx->d_cand_cnt);
     cudaFree(ctx->d_miss);
     cudaFree(ctx->d_miss_count);
+    cudaFree(ctx->d_sink);
     cudaFree(ctx->d_items);
     cudaFree(ctx->d_part_o);
     cudaFree(ctx->d_part_ml);
@@ -277,6 +279,7 @@ int srh_create(const srh_config* cfg, srh_ctx** out) {
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_cand_cnt, sizeof(int) * B);
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_miss, sizeof(int2) * (size_t)ctx->L * B * ctx->S);
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_miss_count, sizeof(int) * (size_t)ctx->L * B);
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_sink, sizeof(uint32_t));
     if (e == cudaSuccess) e = cudaMemset(ctx->d_miss_count, 0, sizeof(int) * (size_t)ctx->L * B);
     if (e != cudaSuccess) return bail(SRH_ERR_NOMEM, std::string("device scratch: ") + cudaGetErrorString(e));
 
@@ -317,6 +320,12 @@ int srh_mark_stored(srh_ctx* ctx, int layer, int seq, long long c0, long long n)
     SRH_CUDA(ctx, cudaMemcpy(ctx->h_layers[layer].host_ready + (size_t)seq * cap + c0, hr + c0, (size_t)n,
                              cudaMemcpyHostToDevice));
     if (!ctx->swap[layer]) ctx->resident_dirty[layer] = 1;
+    // read each stored page once from the device: the first reads of a host
+    // page are the slow ones, and this keeps them out of the decode steps
+    const cudaError_t e = launch_touch(ctx->pool_dev[layer] + ((size_t)seq * cap + c0) * kKvDim, n * kKvDim,
+                                       ctx->d_sink, ctx->sm_count, 0);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "srh_mark_stored touch");
+    SRH_CUDA(ctx, cudaStreamSynchronize(0));
     return SRH_OK;
 }
 
@@ -350,8 +359,9 @@ int srh_layer_info(srh_ctx* ctx, int layer, long long* cap, int* swap_enabled) {
 
 int srh_max_select(srh_ctx* ctx) { return ctx ? ctx->S : SRH_ERR_INVALID; }
 
-int fm_score(srh_ctx* ctx, const uint16_t* d_keys, int n, const uint16_t* d_q, float scale,
-             const float* bias3, int ensemble, float* d_scores, srh_stream_t stream) {
+namespace {
+int score_impl(srh_ctx* ctx, const uint16_t* d_keys, int key_sets, int n, const uint16_t* d_q, float scale,
+               const float* bias3, int ensemble, float* d_scores, srh_stream_t stream) {
     if (!ctx) return SRH_ERR_INVALID;
     if (!d_keys || !d_q || !bias3 || !d_scores) return fail(ctx, SRH_ERR_INVALID, "NULL pointer");
     if (n < 1 || n > ctx->n_src) return fail(ctx, SRH_ERR_INVALID, "n must be in [1, source capacity]");
@@ -360,11 +370,22 @@ int fm_score(srh_ctx* ctx, const uint16_t* d_keys, int n, const uint16_t* d_q, f
     if (((uintptr_t)d_keys | (uintptr_t)d_q) & 15) return fail(ctx, SRH_ERR_INVALID, "keys/queries must be 16-byte aligned");
     if (!std::isfinite(scale)) return fail(ctx, SRH_ERR_INVALID, "scale must be finite");
     const cudaError_t e = launch_score(d_keys, n, ctx->B, d_q, scale, bias3, ensemble, d_scores, ctx->d_hist,
-                                       ctx->sm_count, (cudaStream_t)stream);
+                                       ctx->sm_count, (cudaStream_t)stream, key_sets);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "fm_score launch");
     ctx->hist_scores = d_scores;
     ctx->hist_n = n;
     return SRH_OK;
+}
+}  // namespace
+
+int fm_score(srh_ctx* ctx, const uint16_t* d_keys, int n, const uint16_t* d_q, float scale,
+             const float* bias3, int ensemble, float* d_scores, srh_stream_t stream) {
+    return score_impl(ctx, d_keys, 1, n, d_q, scale, bias3, ensemble, d_scores, stream);
+}
+
+int fm_score_multi(srh_ctx* ctx, const uint16_t* d_keys3, int n, const uint16_t* d_q, float scale,
+                   const float* bias3, int ensemble, float* d_scores, srh_stream_t stream) {
+    return score_impl(ctx, d_keys3, 3, n, d_q, scale, bias3, ensemble, d_scores, stream);
 }
 
 int fm_select(srh_ctx* ctx, const float* d_scores, int n, int mode, int k, float tau, int clamp,

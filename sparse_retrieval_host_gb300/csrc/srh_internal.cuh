@@ -124,6 +124,7 @@ struct Ctx {
     int hist_n = -1;
     int2* d_miss = nullptr;             // [L][B][S] (chunk, slot)
     int* d_miss_count = nullptr;        // [L][B]
+    uint32_t* d_sink = nullptr;         // write target that keeps the page-touch loads alive
     // attention scratch
     AttnItem* d_items = nullptr;        // all items, grouped by layer
     std::vector<int> item_begin;        // [L+1] offsets into d_items
@@ -157,7 +158,7 @@ __device__ __forceinline__ uint32_t ordered_key(float s) {
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_score(const uint16_t* keys, int n, int B, const uint16_t* q, float scale,
                          const float* bias3, int ensemble, float* scores, uint32_t* hist,
-                         int sm_count, cudaStream_t st);
+                         int sm_count, cudaStream_t st, int key_sets = 1);
 cudaError_t launch_hist(const float* scores, int n, int B, uint32_t* hist, cudaStream_t st);
 // Candidate pass for large n: zeroes cand_cnt, then appends the selectable keys.
 cudaError_t launch_collect(const float* scores, int n, int B, int mode, int K, float thresh,
@@ -176,6 +177,7 @@ cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int
 cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, int S,
                           const int2* miss, const int* miss_count, float* staging,
                           uint32_t* err, int sm_count, cudaStream_t st, bool chained);
+cudaError_t launch_touch(const float* p, long long n_floats, uint32_t* sink, int sm_count, cudaStream_t st);
 cudaError_t launch_store(const LayerDev* layers, int l, int B, int G, int seq, long long c0, int n,
                          const float* rows, float* staging, uint32_t* err, cudaStream_t st);
 cudaError_t launch_resident_fill(const float* pool_dev, const uint8_t* ready, long long cap,

@@ -35,7 +35,7 @@ class DecodeStep:
     def __init__(self, *, batch: int, layer_ratios: Sequence[int], gpu_chunks: int, index_topk: int,
                  context_len: int, n_heads: int, max_select: int = 0, src_ratio: int = 4,
                  pinned_cap_bytes: int = 0, allow_topk_reduction: bool = False,
-                 device: str = "cuda", flags: int = 0):
+                 device: str = "cuda", flags: int = 0, key_sets: int = 1):
         self.cfg = abi.make_config(batch=batch, layer_ratios=list(layer_ratios), gpu_chunks=gpu_chunks,
                                    index_topk=index_topk, context_len=context_len, src_ratio=src_ratio,
                                    pinned_cap_bytes=pinned_cap_bytes,
@@ -51,7 +51,12 @@ class DecodeStep:
         dev = torch.device(device)
         B, L, G, H, S, n = self.B, self.L, self.G, self.H, self.S, self.n
         i16, f32, i32 = torch.int16, torch.float32, torch.int32
-        self.keys = torch.zeros((B, n, IDX_DIM), dtype=i16, device=dev)
+        # key_sets = 3: each memory indexer scores its own layer's keys (fm_score_multi)
+        if key_sets not in (1, 3):
+            raise ValueError("key_sets must be 1 or 3")
+        self.key_sets = key_sets
+        shape = (B, n, IDX_DIM) if key_sets == 1 else (3, B, n, IDX_DIM)
+        self.keys = torch.zeros(shape, dtype=i16, device=dev)
         self.fm_q = torch.zeros((B, INDEXERS, IDX_HEADS, IDX_DIM), dtype=i16, device=dev)
         self.scores = torch.zeros((B, n), dtype=f32, device=dev)
         self.sel = torch.zeros((B, S), dtype=i32, device=dev)
@@ -84,8 +89,9 @@ class DecodeStep:
 
     # ------------------------------------------------------------------ the step
     def score(self, spec: StepSpec, stream=None, fm_q=None) -> None:
-        abi.fm_score(self.ctx, self.keys, self.n, self.fm_q if fm_q is None else fm_q, spec.scale,
-                     spec.bias, spec.ensemble, self.scores, stream)
+        fn = abi.fm_score if self.key_sets == 1 else abi.fm_score_multi
+        fn(self.ctx, self.keys, self.n, self.fm_q if fm_q is None else fm_q, spec.scale, spec.bias, spec.ensemble,
+           self.scores, stream)
 
     def select(self, spec: StepSpec, stream=None) -> None:
         abi.fm_select(self.ctx, self.scores, self.n, spec.select_mode, spec.k, spec.tau, spec.clamp,

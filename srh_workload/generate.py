@@ -40,6 +40,7 @@ KIND_POOL = 2
 KIND_WINDOW = 3
 KIND_ATTNQ = 4
 KIND_NEEDLES = 5
+KIND_KEY_SET = 6       # key sets 1 and 2 of the per-indexer-keys variant
 
 KEY_BLOCK = 1024     # key rows per generator
 POOL_BLOCK = 32      # pool rows per generator
@@ -90,6 +91,39 @@ def key_rows(w: Workload, seq: int, idx: Sequence[int]) -> np.ndarray:
         b = int(c) // KEY_BLOCK
         if b not in cache:
             cache[b] = key_block(w, seq, b)
+        out[j] = cache[b][int(c) - b * KEY_BLOCK]
+    return out
+
+
+def key_set_block(w: Workload, i: int, seq: int, block: int) -> np.ndarray:
+    """Block of key set i (set 0 is the shared key set of ``keys``)."""
+    if i == 0:
+        return key_block(w, seq, block)
+    n = w.n_chunks
+    lo = block * KEY_BLOCK
+    rows = min(KEY_BLOCK, n - lo)
+    g = _rng(w, KIND_KEY_SET, i, seq, block)
+    return f32_to_bf16_bits(g.standard_normal((rows, INDEXER_DIM), dtype=np.float32))
+
+
+def keys_multi(w: Workload, seq: int) -> np.ndarray:
+    """bf16 bits ``[3][n][128]``: one key set per memory indexer (set 0 = ``keys``)."""
+    n = w.n_chunks
+    out = np.empty((N_INDEXERS, n, INDEXER_DIM), dtype=np.uint16)
+    for i in range(N_INDEXERS):
+        for b in range((n + KEY_BLOCK - 1) // KEY_BLOCK):
+            out[i, b * KEY_BLOCK:(b + 1) * KEY_BLOCK] = key_set_block(w, i, seq, b)
+    return out
+
+
+def _key_set_rows(w: Workload, i: int, seq: int, idx) -> np.ndarray:
+    idx = np.asarray(idx, dtype=np.int64)
+    out = np.empty((len(idx), INDEXER_DIM), dtype=np.uint16)
+    cache = {}
+    for j, c in enumerate(idx):
+        b = int(c) // KEY_BLOCK
+        if b not in cache:
+            cache[b] = key_set_block(w, i, seq, b)
         out[j] = cache[b][int(c) - b * KEY_BLOCK]
     return out
 
@@ -176,6 +210,19 @@ def fm_queries(w: Workload, step: int, seq: int) -> np.ndarray:
     k = bf16_bits_to_f32(key_rows(w, seq, flat)).reshape(N_INDEXERS, INDEXER_HEADS,
                                                           SLOTS_PER_HEAD, INDEXER_DIM)
     q = k.sum(axis=2, dtype=np.float32) + np.float32(NOISE_STD) * noise
+    return f32_to_bf16_bits(q)
+
+
+def fm_queries_multi(w: Workload, step: int, seq: int) -> np.ndarray:
+    """Like ``fm_queries`` for per-indexer key sets: indexer i's needle
+    directions are taken from key set i."""
+    window_idx = step // w.lookahead
+    _, plan, noise = _needle_plan(w, window_idx, seq)
+    q = np.empty((N_INDEXERS, INDEXER_HEADS, INDEXER_DIM), dtype=np.float32)
+    for i in range(N_INDEXERS):
+        k = bf16_bits_to_f32(_key_set_rows(w, i, seq, plan[i].reshape(-1))).reshape(
+            INDEXER_HEADS, SLOTS_PER_HEAD, INDEXER_DIM)
+        q[i] = k.sum(axis=1, dtype=np.float32) + np.float32(NOISE_STD) * noise[i]
     return f32_to_bf16_bits(q)
 
 

@@ -63,6 +63,43 @@ def test_fm_score_matches_oracle(w):
         ds.close()
 
 
+@pytest.mark.parametrize("w", [
+    C.TINY,
+    _w(context_len=4 * 1001 + 3, code=56),                          # ragged tail: n = 1002
+    _w(context_len=131072, batch=2, code=57, ensemble=C.ENSEMBLE_MEAN, bias=-7.0),
+], ids=["tiny", "ragged", "b2_mean"])
+def test_fm_score_multi_matches_oracle(w):
+    """One key set per memory indexer: indexer i scores key set i."""
+    from sparse_retrieval_host_gb300.runtime import bits_to_i16
+    ds = make_ds(w, layer_ratios=(4,), key_sets=3)
+    try:
+        keys = [G.keys_multi(w, b) for b in range(w.batch)]
+        for b in range(w.batch):
+            for i in range(3):
+                ds.keys[i, b] = bits_to_i16(keys[b][i])
+        for t in (0, w.lookahead):
+            for b in range(w.batch):
+                ds.fm_q[b] = bits_to_i16(G.fm_queries_multi(w, t, b))
+            ds.score(spec_of(w))
+            got = ds.scores.double().cpu().numpy()
+            for b in range(w.batch):
+                q = G.fm_queries_multi(w, t, b)
+                ref = O.score_multi(keys[b], q, w.scale, [w.bias] * 3, w.ensemble)
+                qf = np.abs(O.bf16_to_f64(q)).reshape(3, 8, 128)
+                absdot = np.stack([np.abs(O.bf16_to_f64(keys[b][i])) @ qf[i].T for i in range(3)])
+                bound = (w.scale * 128 * 2.0 ** -23 * absdot.max(axis=(0, 2))
+                         + 8 * 2.0 ** -24 * (np.abs(ref) + abs(w.bias)))
+                err = np.abs(got[b] - ref)
+                assert np.all(err <= bound), (err.max(), bound[err.argmax()])
+                if len(err) >= 100:
+                    assert np.median(err) <= 1e-6
+                # the needles of every indexer's own key set are found
+                top = O.select_topk(ref, w.index_topk)
+                assert np.isin(G.step_needles(w, t, b), top).all()
+    finally:
+        ds.close()
+
+
 # ----------------------------------------------------------------------------- fm_select
 def _select_case(name, n, rng):
     if name == "random":

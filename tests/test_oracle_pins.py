@@ -148,6 +148,29 @@ def test_logit_is_scaled_max_over_heads_plus_indexer_bias():
     assert O.ensemble(lg, O.ENSEMBLE_MEAN)[0] == pytest.approx(sum(want) / 3, abs=0)
 
 
+def test_per_indexer_keys_exact_and_isolated():
+    """Multi-layer compressed_k (限制与未来工作): indexer i scores key set i only.
+    Exact against rational arithmetic; three equal sets give the shared-key
+    score; changing set 1 moves only indexer 1's logits."""
+    rng = np.random.default_rng(21)
+    keys3 = G.f32_to_bf16_bits(rng.standard_normal((3, 7, 128), dtype=np.float32))
+    q = G.f32_to_bf16_bits(rng.standard_normal((3, 8, 128), dtype=np.float32))
+    bias = [0.5, -0.25, 1.0]
+    lg = O.indexer_logits_multi(keys3, q, 0.5, bias)
+    for i in range(3):
+        for c in range(7):
+            best = max(sum(_bf16_exact(int(a)) * _bf16_exact(int(b)) for a, b in zip(keys3[i, c], q[i, h]))
+                       for h in range(8))
+            assert Fraction(lg[i, c]) == Fraction(1, 2) * best + Fraction(bias[i]), (i, c)
+    same = np.stack([keys3[0]] * 3)
+    assert np.array_equal(O.indexer_logits_multi(same, q, 0.5, bias), O.indexer_logits(keys3[0], q, 0.5, bias))
+    other = keys3.copy()
+    other[1] = G.f32_to_bf16_bits(rng.standard_normal((7, 128), dtype=np.float32))
+    lg2 = O.indexer_logits_multi(other, q, 0.5, bias)
+    assert np.array_equal(lg2[0], lg[0]) and np.array_equal(lg2[2], lg[2])
+    assert not np.array_equal(lg2[1], lg[1])
+
+
 def test_or_mode_max_threshold_is_union_of_indexers():
     """Summary section "Memory Indexer 放哪里": a chunk is recalled if ANY indexer recalls it."""
     rng = np.random.default_rng(3)
