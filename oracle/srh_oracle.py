@@ -144,6 +144,79 @@ def score_multi(keys3_bits, q_bits, scale, bias, mode) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------
+# 1'. fp8 indexer keys (section "限制与未来工作": quantize the indexer keys to
+#     fp8/int8 to cut the key stream; the scorer kernel has to change with it).
+#     Reading: e4m3 codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits;
+#     largest finite value 448; 0x7F/0xFF are NaN) with one fp32 scale per
+#     chunk, scale_c = amax_c / 448; code = e4m3(K / scale_c), rounded to nearest
+#     (ties to even) and saturated to +-448. The scale and the division are fp32
+#     operations, the same ones the kernel performs, because they decide codes.
+# ----------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    """Value of each e4m3 code (uint8) as float64; NaN for 0x7F / 0xFF."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    val = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    val = np.where((c & 0x7F) == 0x7F, np.nan, val)
+    return sign * val
+
+
+def _e4m3_table():
+    codes = np.arange(0x7F, dtype=np.uint8)          # non-negative finite codes, increasing values
+    return codes, e4m3_decode(codes)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Round each finite value to the nearest e4m3 value, ties to the even code,
+    saturating at +-448, keeping the sign (a negative value that rounds to zero
+    gives 0x80); fp32/fp64 inputs, NaN is not expected."""
+    x = np.asarray(x, dtype=np.float64)
+    codes, vals = _e4m3_table()
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    hi = np.searchsorted(vals, a, side="left")       # first value >= a
+    hi = np.minimum(hi, len(vals) - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = a - vals[lo]
+    d_hi = vals[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & ((codes[hi] & 1) == 0))
+    out = np.where(pick_hi, codes[hi], codes[lo]).astype(np.uint8)
+    out = np.where(vals[hi] == a, codes[hi], out).astype(np.uint8)
+    return np.where(np.signbit(x), out | 0x80, out).astype(np.uint8)   # the sign is kept, -0 included
+
+
+def quantize_keys_fp8(keys_bits: np.ndarray):
+    """bf16 keys [n][128] -> (e4m3 codes [n][128] uint8, fp32 scale [n])."""
+    k = (np.asarray(keys_bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+    amax = np.abs(k).max(axis=1).astype(np.float32)
+    scale = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    ratio = (k / safe[:, None]).astype(np.float32)     # fp32 division, as on the device
+    codes = e4m3_encode(ratio)
+    codes[scale == 0] = 0
+    return codes, scale
+
+
+def indexer_logits_fp8(codes: np.ndarray, kscale: np.ndarray, q_bits, scale: float,
+                       bias: Sequence[float]) -> np.ndarray:
+    """s_i(c) = scale * kscale_c * max_h <Q[i,h,:], e4m3(K8[c,:])> + b_i: ``[3][n]``."""
+    k = e4m3_decode(codes)                            # [n][128], exact
+    q = bf16_to_f64(q_bits).reshape(N_INDEXERS * INDEXER_HEADS, INDEXER_DIM)
+    d = (k @ q.T).reshape(k.shape[0], N_INDEXERS, INDEXER_HEADS).max(axis=2)
+    per = d * np.asarray(kscale, dtype=np.float64)[:, None]
+    b = np.asarray(bias, dtype=np.float64).reshape(1, N_INDEXERS)
+    return (scale * per + b).T
+
+
+def score_fp8(codes, kscale, q_bits, scale, bias, mode) -> np.ndarray:
+    return ensemble(indexer_logits_fp8(codes, kscale, q_bits, scale, bias), mode)
+
+
+# ----------------------------------------------------------------------------
 # 3. Selection
 # ----------------------------------------------------------------------------
 def threshold_logit(tau: float) -> float:

@@ -171,6 +171,63 @@ def test_per_indexer_keys_exact_and_isolated():
     assert not np.array_equal(lg2[1], lg[1])
 
 
+def test_e4m3_decode_follows_the_format():
+    """e4m3: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits, no infinities,
+    0x7F / 0xFF NaN; subnormals m * 2^-9."""
+    want = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0, 0x39: 1.125,
+            0x7E: 448.0, 0xB8: -1.0, 0xFE: -448.0}
+    got = O.e4m3_decode(np.array(list(want), np.uint8))
+    assert np.array_equal(got, np.array(list(want.values())))
+    assert np.isnan(O.e4m3_decode(np.array([0x7F, 0xFF], np.uint8))).all()
+    pos = O.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    assert np.all(np.diff(pos) > 0)                       # 127 distinct, increasing values
+
+
+def test_e4m3_encode_rounds_to_nearest_even_and_saturates():
+    codes = np.arange(0x7F, dtype=np.uint8)
+    vals = O.e4m3_decode(codes)
+    assert np.array_equal(O.e4m3_encode(vals), codes)      # every value is its own code
+    assert np.array_equal(O.e4m3_encode(-vals[1:]), codes[1:] | 0x80)
+    mid = (vals[:-1] + vals[1:]) / 2                      # exact midpoints go to the even code
+    even = np.where(codes[:-1] % 2 == 0, codes[:-1], codes[1:])
+    assert np.array_equal(O.e4m3_encode(mid), even)
+    assert np.array_equal(O.e4m3_encode(np.nextafter(mid, np.inf)), codes[1:])
+    assert np.array_equal(O.e4m3_encode(np.nextafter(mid, -np.inf)), codes[:-1])
+    assert list(O.e4m3_encode([449.0, 1e9, -1e9])) == [0x7E, 0x7E, 0xFE]
+    assert list(O.e4m3_encode([-0.0, -2.0 ** -12])) == [0x80, 0x80]
+
+
+def test_fp8_key_quantization_and_score():
+    rng = np.random.default_rng(17)
+    keys = G.f32_to_bf16_bits(rng.standard_normal((64, 128), dtype=np.float32))
+    keys[5] = 0                                           # an all-zero key
+    codes, ks = O.quantize_keys_fp8(keys)
+    k = O.bf16_to_f64(keys)
+    assert ks.dtype == np.float32 and ks[5] == 0 and not codes[5].any()
+    amax_at = np.abs(k).argmax(axis=1)
+    for c in range(64):
+        if c == 5:
+            continue
+        assert codes[c, amax_at[c]] & 0x7F == 0x7E          # the largest element maps to +-448
+        deq = O.e4m3_decode(codes[c]) * float(ks[c])
+        assert np.all(np.abs(deq - k[c]) <= np.maximum(2.0 ** -4 * np.abs(k[c]), 2.0 ** -10 * float(ks[c])))
+    q = G.f32_to_bf16_bits(rng.standard_normal((3, 8, 128), dtype=np.float32))
+    lg = O.indexer_logits_fp8(codes, ks, q, 0.25, [0.5, 0.0, -1.0])
+    deq = O.e4m3_decode(codes) * ks.astype(np.float64)[:, None]
+    qq = O.bf16_to_f64(q)
+    for i in range(3):
+        want = 0.25 * np.max(deq @ qq[i].T, axis=1) + [0.5, 0.0, -1.0][i]
+        assert np.allclose(lg[i], want, rtol=1e-13, atol=1e-13)
+
+
+def test_fp8_keys_still_find_the_needles():
+    w = C.TINY
+    codes, ks = O.quantize_keys_fp8(G.keys(w, 0))
+    for t in (0, 8, 16):
+        s = O.score_fp8(codes, ks, G.fm_queries(w, t, 0), w.scale, [0.0] * 3, w.ensemble)
+        assert np.isin(G.step_needles(w, t, 0), O.select_topk(s, w.index_topk)).all()
+
+
 def test_or_mode_max_threshold_is_union_of_indexers():
     """Summary section "Memory Indexer 放哪里": a chunk is recalled if ANY indexer recalls it."""
     rng = np.random.default_rng(3)
