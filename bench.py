@@ -312,6 +312,23 @@ def run_ours(args, dist, rank, world, local):
         if i >= 1:
             multi_ms.append(m0.elapsed_time(m1))
     del keys3
+
+    # fp8 (e4m3) indexer keys with per-chunk scales (fm_score_fp8): the scoring call alone
+    codes = torch.empty(tuple(ds.keys.shape), dtype=torch.uint8, device=device)
+    kscale = torch.empty(tuple(ds.keys.shape[:2]), dtype=torch.float32, device=device)
+    abi.fm_quantize_keys(ds.ctx, ds.keys, ds.n, codes, kscale, stream)
+    fp8_ms = []
+    for i in range(6):
+        flush_l2()
+        m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        m0.record(stream)
+        abi.fm_score_fp8(ds.ctx, codes, kscale, ds.n, ds.fm_q, spec.scale, spec.bias, spec.ensemble, ds.scores,
+                         stream)
+        m1.record(stream)
+        m1.synchronize()
+        if i >= 1:
+            fp8_ms.append(m0.elapsed_time(m1))
+    del codes, kscale
     stage_ms = [e[1].elapsed_time(e[2]) for e in evb]
     attn_ms = [e[2].elapsed_time(e[3]) for e in evb]
     local_s = sum(step_ms) / 1e3
@@ -365,6 +382,11 @@ def run_ours(args, dist, rank, world, local):
                            "lsa_attend": a_avg_ms * 1e3,
                            "note": f"phase spans of {KB} further steps replayed as three graphs"},
             "score_gbs": score_bytes(w) / (statistics.mean(score_ms) / 1e3) / 1e9,
+            "score_fp8_keys": {
+                "us": statistics.median(fp8_ms) * 1e3,
+                "gbs": w.batch * w.n_chunks * (C.INDEXER_DIM + 4 + 4) / (statistics.median(fp8_ms) / 1e3) / 1e9,
+                "note": "fm_score_fp8: e4m3 codes + fp32 scale per chunk (132 B read, 4 B written), L2 flushed, "
+                        "memset + kernel"},
             "score_per_indexer_keys": {
                 "us": statistics.median(multi_ms) * 1e3,
                 "gbs": w.batch * w.n_chunks * (3 * C.INDEXER_DIM * 2 + 4) / (statistics.median(multi_ms) / 1e3) / 1e9,

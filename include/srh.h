@@ -225,6 +225,26 @@ int fm_score_multi(srh_ctx* ctx, const uint16_t* d_keys3, int n, const uint16_t*
                    const float* bias3, int ensemble, float* d_scores, srh_stream_t stream);
 
 /*
+ * fp8 indexer keys ([P1] 限制与未来工作: quantize the indexer keys to fp8 to cut
+ * the scoring pass's key stream; the scorer kernel reads them directly).
+ *
+ * fm_quantize_keys: d_keys [batch][n][128] bf16 -> d_codes [batch][n][128] e4m3
+ * codes (uint8) and d_kscale [batch][n] fp32, per chunk
+ *     kscale_c = amax_c / 448,  code = e4m3(K / kscale_c)
+ * in IEEE fp32 division, rounded to nearest (ties to even), saturated; an
+ * all-zero chunk gets kscale 0 and zero codes. Run once for frozen keys.
+ *
+ * fm_score_fp8: as fm_score on those codes,
+ *     s_i(c) = scale * kscale_c * max_h <Q[i,h], e4m3(K8[c])> + b_i,
+ * reading 132 bytes per chunk instead of 256. Fills the same histogram for
+ * fm_select. Errors as fm_score.
+ */
+int fm_quantize_keys(srh_ctx* ctx, const uint16_t* d_keys, int n, uint8_t* d_codes, float* d_kscale,
+                     srh_stream_t stream);
+int fm_score_fp8(srh_ctx* ctx, const uint8_t* d_codes, const float* d_kscale, int n, const uint16_t* d_q,
+                 float scale, const float* bias3, int ensemble, float* d_scores, srh_stream_t stream);
+
+/*
  * a3: selection ([P1] 架构概览 step 3: global top-k; [P2] LSA: sigmoid threshold).
  *   d_scores [batch][n] fp32
  *   mode     SRH_SELECT_TOPK: the min(k, n) best chunks;

@@ -93,6 +93,8 @@ SIGNATURES = [
     ("srh_max_select", _i, [_vp]),
     ("fm_score", _i, [_vp, _vp, _i, _vp, _f, ctypes.POINTER(_f), _i, _vp, _vp]),
     ("fm_score_multi", _i, [_vp, _vp, _i, _vp, _f, ctypes.POINTER(_f), _i, _vp, _vp]),
+    ("fm_quantize_keys", _i, [_vp, _vp, _i, _vp, _vp, _vp]),
+    ("fm_score_fp8", _i, [_vp, _vp, _vp, _i, _vp, _f, ctypes.POINTER(_f), _i, _vp, _vp]),
     ("fm_select", _i, [_vp, _vp, _i, _i, _i, _f, _i, _vp, _vp, _vp]),
     ("fm_select_noalloc", _i, [_vp, _i, _i, _i, _i, _f, _i, _i, _vp, _vp, _vp, ctypes.c_char_p, ctypes.c_size_t]),
     ("kvswap_stage", _i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
@@ -219,6 +221,17 @@ def fm_score_multi(ctx, keys3, n, q, scale, bias3, ensemble, scores, stream=None
     b = (ctypes.c_float * 3)(*[float(x) for x in bias3])
     _check(load().fm_score_multi(ctx, _ptr(keys3), n, _ptr(q), float(scale), b, ensemble, _ptr(scores),
                                  _stream(stream)), "fm_score_multi", ctx)
+
+
+def fm_quantize_keys(ctx, keys, n, codes, kscale, stream=None) -> None:
+    _check(load().fm_quantize_keys(ctx, _ptr(keys), n, _ptr(codes), _ptr(kscale), _stream(stream)),
+           "fm_quantize_keys", ctx)
+
+
+def fm_score_fp8(ctx, codes, kscale, n, q, scale, bias3, ensemble, scores, stream=None) -> None:
+    b = (ctypes.c_float * 3)(*[float(x) for x in bias3])
+    _check(load().fm_score_fp8(ctx, _ptr(codes), _ptr(kscale), n, _ptr(q), float(scale), b, ensemble,
+                               _ptr(scores), _stream(stream)), "fm_score_fp8", ctx)
 
 
 def fm_select(ctx, scores, n, mode, k, tau, clamp, sel, count, stream=None) -> None:

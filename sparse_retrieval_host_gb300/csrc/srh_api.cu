@@ -388,6 +388,37 @@ int fm_score_multi(srh_ctx* ctx, const uint16_t* d_keys3, int n, const uint16_t*
     return score_impl(ctx, d_keys3, 3, n, d_q, scale, bias3, ensemble, d_scores, stream);
 }
 
+int fm_quantize_keys(srh_ctx* ctx, const uint16_t* d_keys, int n, uint8_t* d_codes, float* d_kscale,
+                     srh_stream_t stream) {
+    if (!ctx) return SRH_ERR_INVALID;
+    if (!d_keys || !d_codes || !d_kscale) return fail(ctx, SRH_ERR_INVALID, "NULL pointer");
+    if (n < 1 || n > ctx->n_src) return fail(ctx, SRH_ERR_INVALID, "n must be in [1, source capacity]");
+    if (((uintptr_t)d_keys | (uintptr_t)d_codes | (uintptr_t)d_kscale) & 15)
+        return fail(ctx, SRH_ERR_INVALID, "keys/codes/scales must be 16-byte aligned");
+    const cudaError_t e = launch_quantize_keys(d_keys, (long long)ctx->B * n, d_codes, d_kscale, ctx->sm_count,
+                                               (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "fm_quantize_keys launch");
+    return SRH_OK;
+}
+
+int fm_score_fp8(srh_ctx* ctx, const uint8_t* d_codes, const float* d_kscale, int n, const uint16_t* d_q,
+                 float scale, const float* bias3, int ensemble, float* d_scores, srh_stream_t stream) {
+    if (!ctx) return SRH_ERR_INVALID;
+    if (!d_codes || !d_kscale || !d_q || !bias3 || !d_scores) return fail(ctx, SRH_ERR_INVALID, "NULL pointer");
+    if (n < 1 || n > ctx->n_src) return fail(ctx, SRH_ERR_INVALID, "n must be in [1, source capacity]");
+    if (ensemble != SRH_ENSEMBLE_MAX && ensemble != SRH_ENSEMBLE_MEAN)
+        return fail(ctx, SRH_ERR_INVALID, "unknown ensemble");
+    if (((uintptr_t)d_codes | (uintptr_t)d_q) & 15) return fail(ctx, SRH_ERR_INVALID, "codes/queries must be 16-byte aligned");
+    if (((uintptr_t)d_kscale) & 3) return fail(ctx, SRH_ERR_INVALID, "scales must be 4-byte aligned");
+    if (!std::isfinite(scale)) return fail(ctx, SRH_ERR_INVALID, "scale must be finite");
+    const cudaError_t e = launch_score_fp8(d_codes, d_kscale, n, ctx->B, d_q, scale, bias3, ensemble, d_scores,
+                                           ctx->d_hist, ctx->sm_count, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "fm_score_fp8 launch");
+    ctx->hist_scores = d_scores;
+    ctx->hist_n = n;
+    return SRH_OK;
+}
+
 int fm_select(srh_ctx* ctx, const float* d_scores, int n, int mode, int k, float tau, int clamp,
               int32_t* d_sel, int32_t* d_count, srh_stream_t stream) {
     if (!ctx) return SRH_ERR_INVALID;

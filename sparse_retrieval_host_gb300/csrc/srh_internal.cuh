@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <cuda_fp8.h>
 
 #include <cstdint>
 #include <string>
@@ -160,6 +161,11 @@ cudaError_t launch_score(const uint16_t* keys, int n, int B, const uint16_t* q, 
                          const float* bias3, int ensemble, float* scores, uint32_t* hist,
                          int sm_count, cudaStream_t st, int key_sets = 1);
 cudaError_t launch_hist(const float* scores, int n, int B, uint32_t* hist, cudaStream_t st);
+cudaError_t launch_quantize_keys(const uint16_t* keys, long long total, uint8_t* codes, float* kscale,
+                                 int sm_count, cudaStream_t st);
+cudaError_t launch_score_fp8(const uint8_t* codes, const float* kscale, int n, int B, const uint16_t* q, float scale,
+                             const float* bias3, int ensemble, float* scores, uint32_t* hist, int sm_count,
+                             cudaStream_t st);
 // Candidate pass for large n: zeroes cand_cnt, then appends the selectable keys.
 cudaError_t launch_collect(const float* scores, int n, int B, int mode, int K, float thresh,
                            const uint32_t* hist, unsigned long long* cand, int* cand_cnt, int cap,

@@ -35,7 +35,7 @@ class DecodeStep:
     def __init__(self, *, batch: int, layer_ratios: Sequence[int], gpu_chunks: int, index_topk: int,
                  context_len: int, n_heads: int, max_select: int = 0, src_ratio: int = 4,
                  pinned_cap_bytes: int = 0, allow_topk_reduction: bool = False,
-                 device: str = "cuda", flags: int = 0, key_sets: int = 1):
+                 device: str = "cuda", flags: int = 0, key_sets: int = 1, key_format: str = "bf16"):
         self.cfg = abi.make_config(batch=batch, layer_ratios=list(layer_ratios), gpu_chunks=gpu_chunks,
                                    index_topk=index_topk, context_len=context_len, src_ratio=src_ratio,
                                    pinned_cap_bytes=pinned_cap_bytes,
@@ -57,6 +57,13 @@ class DecodeStep:
         self.key_sets = key_sets
         shape = (B, n, IDX_DIM) if key_sets == 1 else (3, B, n, IDX_DIM)
         self.keys = torch.zeros(shape, dtype=i16, device=dev)
+        # key_format = "fp8": score e4m3 codes made by quantize_keys() from ``keys``
+        if key_format not in ("bf16", "fp8") or (key_format == "fp8" and key_sets != 1):
+            raise ValueError("key_format must be bf16, or fp8 with one key set")
+        self.key_format = key_format
+        if key_format == "fp8":
+            self.codes = torch.zeros((B, n, IDX_DIM), dtype=torch.uint8, device=dev)
+            self.kscale = torch.zeros((B, n), dtype=f32, device=dev)
         self.fm_q = torch.zeros((B, INDEXERS, IDX_HEADS, IDX_DIM), dtype=i16, device=dev)
         self.scores = torch.zeros((B, n), dtype=f32, device=dev)
         self.sel = torch.zeros((B, S), dtype=i32, device=dev)
@@ -88,7 +95,15 @@ class DecodeStep:
         abi.kvswap_store(self.ctx, layer, seq, c0, rows.shape[0], rows, stream)
 
     # ------------------------------------------------------------------ the step
+    def quantize_keys(self, stream=None) -> None:
+        """e4m3 codes and per-chunk scales of ``keys`` (once, for frozen keys)."""
+        abi.fm_quantize_keys(self.ctx, self.keys, self.n, self.codes, self.kscale, stream)
+
     def score(self, spec: StepSpec, stream=None, fm_q=None) -> None:
+        if self.key_format == "fp8":
+            abi.fm_score_fp8(self.ctx, self.codes, self.kscale, self.n, self.fm_q if fm_q is None else fm_q,
+                             spec.scale, spec.bias, spec.ensemble, self.scores, stream)
+            return
         fn = abi.fm_score if self.key_sets == 1 else abi.fm_score_multi
         fn(self.ctx, self.keys, self.n, self.fm_q if fm_q is None else fm_q, spec.scale, spec.bias, spec.ensemble,
            self.scores, stream)

@@ -7,7 +7,7 @@ from oracle import srh_oracle as O
 from srh_workload import configs as C
 from srh_workload import generate as G
 
-from helpers import (ATTN_TOL, attn_err, fill, load_step_inputs, make_ds, spec_of)
+from helpers import (ATTN_TOL, attn_err, check_selection, fill, load_step_inputs, make_ds, spec_of)
 
 pytestmark = pytest.mark.gpu
 
@@ -96,6 +96,62 @@ def test_fm_score_multi_matches_oracle(w):
                 # the needles of every indexer's own key set are found
                 top = O.select_topk(ref, w.index_topk)
                 assert np.isin(G.step_needles(w, t, b), top).all()
+    finally:
+        ds.close()
+
+
+def _crafted_keys(n, rng):
+    """Random keys plus chunks that exercise the quantizer's corners."""
+    k = rng.standard_normal((n, 128)).astype(np.float32)
+    k[0] = 0.0                                            # all zero: scale 0, zero codes
+    k[1, :] = 1e-6 * (-1.0) ** np.arange(128)             # +-tiny: zero codes, the negative ones signed
+    k[1, 7] = -3e4                                        # large amax, tiny negatives -> signed zeros
+    k[2, ::2] = -k[2, ::2] * 1e-3                         # wide dynamic range, subnormal codes
+    return G.f32_to_bf16_bits(k)
+
+
+@pytest.mark.parametrize("w", [
+    C.TINY,
+    _w(context_len=4 * 1001 + 3, code=58),                          # ragged tail: n = 1002
+    _w(context_len=131072, batch=2, code=59, ensemble=C.ENSEMBLE_MEAN, bias=-7.0),
+], ids=["tiny", "ragged", "b2_mean"])
+def test_fp8_keys_quantize_exactly_and_score_within_bound(w):
+    from sparse_retrieval_host_gb300.runtime import bits_to_i16
+    ds = make_ds(w, layer_ratios=(4,), key_format="fp8")
+    try:
+        keys = [G.keys(w, b) for b in range(w.batch)]
+        keys[0] = np.concatenate([_crafted_keys(3, np.random.default_rng(5)), keys[0][3:]])
+        for b in range(w.batch):
+            ds.keys[b] = bits_to_i16(keys[b])
+        ds.quantize_keys()
+        codes = ds.codes.cpu().numpy()
+        ks = ds.kscale.cpu().numpy()
+        ref = [O.quantize_keys_fp8(keys[b]) for b in range(w.batch)]
+        for b in range(w.batch):
+            assert np.array_equal(ks[b], ref[b][1]), np.nonzero(ks[b] != ref[b][1])[0][:5]
+            bad = np.nonzero(codes[b] != ref[b][0])
+            assert bad[0].size == 0, (bad[0][:5], bad[1][:5], codes[b][bad][:5], ref[b][0][bad][:5])
+        for t in (0, w.lookahead):
+            for b in range(w.batch):
+                ds.fm_q[b] = bits_to_i16(G.fm_queries(w, t, b))
+            ds.score(spec_of(w))
+            ds.select(spec_of(w))
+            got = ds.scores.double().cpu().numpy()
+            for b in range(w.batch):
+                q = G.fm_queries(w, t, b)
+                c8, k8 = ref[b]
+                s_ref = O.score_fp8(c8, k8, q, w.scale, [w.bias] * 3, w.ensemble)
+                deq = np.abs(O.e4m3_decode(c8))
+                absdot = (deq @ np.abs(O.bf16_to_f64(q)).reshape(24, 128).T).max(axis=1) * k8.astype(np.float64)
+                bound = w.scale * 130 * 2.0 ** -23 * absdot + 8 * 2.0 ** -24 * (np.abs(s_ref) + abs(w.bias))
+                err = np.abs(got[b] - s_ref)
+                assert np.all(err <= bound), (err.max(), bound[err.argmax()])
+                sel_ref = O.select(s_ref, w.select_mode, w.index_topk, w.tau, w.clamp)
+                cnt = int(ds.count[b])
+                check_selection(w, s_ref, sel_ref, ds.sel[b, :cnt].cpu().numpy(), got[b])
+                nd = G.step_needles(w, t, b)
+                nd = nd[nd >= 3] if b == 0 else nd          # chunks 0-2 of sequence 0 were replaced
+                assert np.isin(nd, ds.sel[b, :cnt].cpu().numpy()).all()
     finally:
         ds.close()
 
