@@ -37,6 +37,9 @@ its reason in the design notes):
   * the LRU list starts with every slot free, slot 0 at the back;
   * with GPU_CHUNKS below the selected count (allowed only by the test flag),
     a swapped layer keeps the first GPU_CHUNKS chunks of its list;
+  * adaptive GPU_CHUNKS (listed by the pages as a future direction) resizes the
+    slot range in use from the hit rate of a window of steps, by the rule of
+    section 4c; slots are never moved, dropped slots forget their chunks;
   * attention is MQA over the 512-wide latent (K = V = row), scale 1/sqrt(512).
 
 Parity pins (checks that do not reuse this code) live in ``tests/test_oracle_*.py``.
@@ -301,6 +304,67 @@ class KvSwapLayerState:
         self.slot_lru: "OrderedDict[int, None]" = OrderedDict((s, None) for s in range(gpu_chunks))
         self.hits = 0
         self.misses = 0
+        # adaptive capacity (section 4c below): slots [0, capacity) are in use
+        self.capacity = gpu_chunks
+        self.next_capacity = gpu_chunks
+        self.policy: Optional["AdaptivePolicy"] = None
+        self.ep_steps = self.ep_hits = self.ep_sel = 0
+
+    # -- adaptive capacity -------------------------------------------------
+    def install_policy(self, policy: Optional["AdaptivePolicy"]) -> None:
+        """The next swap step runs with ``policy.g_init`` slots (all
+        ``gpu_chunks`` when ``policy`` is None); the hit-rate window restarts."""
+        if policy is not None:
+            policy.check(self.gpu_chunks)
+        self.policy = policy
+        self.next_capacity = policy.g_init if policy is not None else self.gpu_chunks
+        self.ep_steps = self.ep_hits = self.ep_sel = 0
+
+    def set_capacity(self, g: int) -> None:
+        """Resize the slot range in use to [0, g) without moving any row.
+        Growing adds the new slots, empty, at the back of the LRU list (lowest
+        index outermost), so they are taken before any slot that holds a
+        chunk. Shrinking drops slots [g, capacity): their chunks are no longer
+        staged; the kept slots keep their chunks and their LRU order."""
+        assert 1 <= g <= self.gpu_chunks
+        cur = self.capacity
+        if g > cur:
+            order = list(range(cur, g)) + list(self.slot_lru)
+            self.slot_lru = OrderedDict((s, None) for s in order)
+        elif g < cur:
+            for s in range(g, cur):
+                c = self.gpu_slot_logical[s]
+                if c >= 0:
+                    del self.slot_by_logical[c]
+                    self.gpu_slot_logical[s] = -1
+                del self.slot_lru[s]
+        self.capacity = g
+        self.next_capacity = g
+
+    def active_capacity(self) -> int:
+        """Slots the next swap step uses (a pending resize is applied first)."""
+        if self.swap_enabled and self.next_capacity != self.capacity:
+            self.set_capacity(self.next_capacity)
+        return self.capacity if self.swap_enabled else self.gpu_chunks
+
+    def _account(self, hits: int, selected: int) -> None:
+        """Hit-rate window of the policy: after ``epoch`` swap steps the window's
+        hits/selected decides the capacity of the steps that follow."""
+        p = self.policy
+        if p is None:
+            return
+        self.ep_steps += 1
+        self.ep_hits += hits
+        self.ep_sel += selected
+        if self.ep_steps < p.epoch:
+            return
+        g = self.capacity
+        if self.ep_hits * 1000 < p.lo_permille * self.ep_sel:
+            g = min(p.g_max, g + p.delta)
+        elif self.ep_hits * 1000 > p.hi_permille * self.ep_sel:
+            g = max(p.g_min, g - p.delta)
+        self.next_capacity = g
+        self.ep_steps = self.ep_hits = self.ep_sel = 0
 
     def store(self, logical: int) -> None:
         """Store flow: the chunk now exists in the host cache; a resident copy stays."""
@@ -317,6 +381,7 @@ class KvSwapLayerState:
                     raise NotStoredError(f"chunk {c} selected before it was stored")
                 phys.append(self.window + int(c))
             return SwapResult(phys, misses, 0)
+        self.active_capacity()
         for c in logical_ids:
             c = int(c)
             slot = self.slot_by_logical.get(c)
@@ -337,7 +402,35 @@ class KvSwapLayerState:
             phys.append(self.window + slot)
         self.hits += hits
         self.misses += len(misses)
+        self._account(hits, len(logical_ids))
         return SwapResult(phys, misses, hits)
+
+
+# ----------------------------------------------------------------------------
+# 4c. Adaptive GPU_CHUNKS from the runtime LRU hit rate (section "未来优化方向",
+#     item 4: the staging capacity follows the measured hit rate). The pages
+#     name the direction only; the rule below is this implementation's reading.
+# ----------------------------------------------------------------------------
+@dataclass(frozen=True)
+class AdaptivePolicy:
+    """Per (layer, sequence) of a swapped layer: every ``epoch`` swap steps the
+    hit rate h = hits/selected of those steps sets the capacity of the next
+    steps: h < lo_permille/1000 grows it by ``delta`` (up to ``g_max``),
+    h > hi_permille/1000 shrinks it by ``delta`` (down to ``g_min``), otherwise
+    it stays. The comparisons are exact integers (hits*1000 against
+    permille*selected), so a window with nothing selected changes nothing."""
+    g_min: int
+    g_max: int
+    g_init: int
+    epoch: int
+    lo_permille: int
+    hi_permille: int
+    delta: int
+
+    def check(self, gpu_chunks: int) -> None:
+        assert 1 <= self.g_min <= self.g_init <= self.g_max <= gpu_chunks
+        assert self.epoch >= 1 and self.delta >= 1
+        assert 0 <= self.lo_permille <= self.hi_permille <= 1000
 
 
 # ----------------------------------------------------------------------------
@@ -389,6 +482,13 @@ class DecodeOracle:
         self.states = [[KvSwapLayerState(cap, gpu_chunks, window) for _ in range(batch)]
                        for cap in self.caps]
 
+    def install_policy(self, policy: Optional[AdaptivePolicy]) -> None:
+        """Adaptive capacity (section 4c) for every swapped (layer, sequence)."""
+        for row in self.states:
+            for st in row:
+                if st.swap_enabled:
+                    st.install_policy(policy)
+
     def mark_all_stored(self) -> None:
         for row in self.states:
             for st in row:
@@ -427,10 +527,12 @@ class DecodeOracle:
             row_l, row_s = [], []
             for b in range(self.batch):
                 lst = layer_chunks(sels[b], self.src_ratio, ratio)
-                if self.states[l][b].swap_enabled and len(lst) > self.gpu_chunks:
-                    # GPU_CHUNKS < index_topk (a test-only setting): the layer keeps
-                    # the first GPU_CHUNKS chunks of its list
-                    lst = lst[:self.gpu_chunks]
+                g = self.states[l][b].active_capacity()
+                if self.states[l][b].swap_enabled and len(lst) > g:
+                    # fewer slots in use than chunks listed (GPU_CHUNKS < index_topk,
+                    # a test-only setting, or a small adaptive capacity): the layer
+                    # keeps the first chunks of its list, as many as it has slots
+                    lst = lst[:g]
                 row_l.append(lst)
                 row_s.append(self.states[l][b].swap_in_selected(lst))
             lists.append(row_l)

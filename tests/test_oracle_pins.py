@@ -432,6 +432,126 @@ def test_decode_oracle_store_and_periodic_selection():
     assert not all(np.array_equal(r2.sel[b], r0.sel[b]) for b in range(2))
 
 
+# --------------------------------------------------------------------------- adaptive capacity
+def _stamp_lru_resizable(steps, caps, G_):
+    """LRU by last-use keys over a slot range that can shrink or grow, written
+    independently of the list form: a slot's key is (step, position) of its
+    last use; slots free from the start have (-1, slot); slots added when the
+    range grows at step t have (-(t + 2), slot), below every other key. A miss
+    takes the slot in range with the smallest key; a dropped slot forgets its
+    chunk."""
+    key = {s: (-1, s) for s in range(G_)}
+    chunk = {}
+    g, out = G_, []
+    for t, (refs, gt) in enumerate(zip(steps, caps)):
+        if gt > g:
+            for s in range(g, gt):
+                key[s] = (-(t + 2), s)
+        for s in range(gt, g):
+            chunk.pop(s, None)
+        g = gt
+        res = []
+        for p, c in enumerate(refs):
+            where = [s for s in range(g) if chunk.get(s) == c]
+            if where:
+                s, hit = where[0], True
+            else:
+                s, hit = min(range(g), key=lambda x: key[x]), False
+                chunk[s] = c
+            key[s] = (t, p)
+            res.append((hit, s))
+        out.append(res)
+    return out
+
+
+@pytest.mark.parametrize("seed,G_,universe", [(0, 8, 20), (1, 16, 40), (2, 6, 9), (3, 32, 100)])
+def test_adaptive_resize_matches_stamp_model(seed, G_, universe):
+    r = random.Random(100 + seed)
+    caps, g = [], G_
+    for _ in range(60):
+        if r.random() < 0.3:
+            g = r.randint(1, G_)
+        caps.append(g)
+    steps = []
+    prev = []
+    for g in caps:
+        m = r.randint(0, g)
+        keep = [c for c in prev if r.random() < 0.6]
+        pool = [c for c in range(universe) if c not in keep]
+        refs = (keep + r.sample(pool, max(0, min(m - len(keep), len(pool)))))[:m]
+        r.shuffle(refs)
+        steps.append(refs)
+        prev = refs
+    want = _stamp_lru_resizable(steps, caps, G_)
+    st = O.KvSwapLayerState(universe + G_ + 1, G_)
+    st.host_ready[:] = 1
+    for refs, g, exp in zip(steps, caps, want):
+        st.set_capacity(g)
+        res = st.swap_in_selected(refs)
+        miss = dict(res.misses)
+        assert [(c not in miss, p - 128) for c, p in zip(refs, res.phys)] == exp
+        assert all(s < g for s in st.slot_by_logical.values())
+        assert sorted(st.slot_lru) == list(range(g))
+
+
+def test_adaptive_policy_hand_worked():
+    """Capacity 8 slots, policy: start at 4, decide every 2 steps, grow below a
+    50 % hit rate, shrink above 90 %, by 2 slots, within [2, 8]."""
+    st = O.KvSwapLayerState(100, 8)
+    st.host_ready[:] = 1
+    st.install_policy(O.AdaptivePolicy(g_min=2, g_max=8, g_init=4, epoch=2, lo_permille=500,
+                                       hi_permille=900, delta=2))
+    trace = [
+        # refs, capacity used, phys, hits
+        ([0, 1, 2], 4, [128, 129, 130], 0),
+        ([0, 1, 2], 4, [128, 129, 130], 3),   # window 3/6 = 50 %: neither below 50 % nor above 90 %
+        ([0, 1, 2], 4, [128, 129, 130], 3),
+        ([0, 1, 2], 4, [128, 129, 130], 3),   # window 6/6: shrink to 2
+        ([0, 1], 2, [128, 129], 2),           # slots 2, 3 dropped with chunk 2
+        ([5, 6], 2, [128, 129], 0),           # window 2/4 = 50 %: stays
+        ([7, 8], 2, [128, 129], 0),
+        ([9], 2, [128], 0),                   # window 0/3: grow to 4
+        ([10], 4, [130], 0),                  # the new empty slots go first, lowest first
+        ([8, 11, 12], 4, [129, 131, 128], 1), # 12 takes the least recent slot (chunk 9's); 1/4: grow to 6
+        ([], 6, [], 0),
+    ]
+    for refs, g, phys, hits in trace:
+        res = st.swap_in_selected(refs)
+        assert (st.capacity, res.phys, res.hits) == (g, phys, hits), refs
+    assert st.next_capacity == 6 and st.capacity == 6
+
+
+def test_adaptive_fixed_range_is_plain_lru():
+    """A policy pinned to the full range (or one that never fires) leaves the
+    plain list LRU unchanged, step for step."""
+    steps = _random_trace(9, 16, 50, 40)
+    for pol in (O.AdaptivePolicy(16, 16, 16, 1, 0, 1000, 4), O.AdaptivePolicy(4, 16, 16, 3, 0, 1000, 4)):
+        a = O.KvSwapLayerState(70, 16)
+        b = O.KvSwapLayerState(70, 16)
+        a.host_ready[:] = 1
+        b.host_ready[:] = 1
+        b.install_policy(pol)
+        for refs in steps:
+            ra, rb = a.swap_in_selected(refs), b.swap_in_selected(refs)
+            assert (ra.phys, ra.misses, ra.hits) == (rb.phys, rb.misses, rb.hits)
+        assert b.capacity == 16
+
+
+def test_decode_oracle_keeps_list_prefix_under_small_capacity():
+    """A step whose list is longer than the slots in use keeps the first chunks
+    of the list, as many as the slots (and the attention uses those)."""
+    w = C.TINY
+    ora = O.DecodeOracle(context_len=w.context_len, layer_ratios=(4,), gpu_chunks=w.gpu_chunks,
+                         index_topk=w.index_topk, batch=1, scale=w.scale, bias=[0.0] * 3,
+                         ensemble_mode=w.ensemble, select_mode=w.select_mode, tau=w.tau, clamp=w.clamp)
+    ora.mark_all_stored()
+    ora.install_policy(O.AdaptivePolicy(100, w.gpu_chunks, 100, 1, 0, 1000, 1))
+    keys = G.keys(w, 0)
+    r = ora.step(lambda b: keys, lambda b: G.fm_queries(w, 0, b))
+    assert len(r.lists[0][0]) == 100 and r.lists[0][0] == list(r.sel[0][:100])
+    assert sorted(p - 128 for p in r.swap[0][0].phys) == list(range(100))
+
+
 def test_swap_disabled_layer_is_identity_mapped():
     st = O.KvSwapLayerState(16, 16)
     st.host_ready[:] = 1
