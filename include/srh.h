@@ -351,6 +351,53 @@ int lsa_attend(srh_ctx* ctx, int layer, const uint16_t* d_q, int n_heads, const 
  */
 int srh_set_chained(srh_ctx* ctx, int on);
 
+/*
+ * Adaptive staging capacity ([P1] 未来优化方向, item 4: size the staging from
+ * the runtime LRU hit rate; the pages give the direction, not a rule).
+ * Each swapped (layer, sequence) uses slots [0, g) of its gpu_chunks staging
+ * rows; kvswap_stage resolves against those g slots only. Every `epoch` swap
+ * steps of that (layer, sequence) the hit rate h = hits / selected of those
+ * steps sets g for the steps that follow:
+ *   hits*1000 <  lo_permille*selected  -> g = min(g_max, g + delta)
+ *   hits*1000 >  hi_permille*selected  -> g = max(g_min, g - delta)
+ *   otherwise g stays (so does it when nothing was selected).
+ * A resize moves no row: growing adds the new slots, empty, at the
+ * least-recently-used end (lowest slot first), so they fill before any held
+ * slot is evicted; shrinking drops slots [g_new, g) and forgets their chunks
+ * (a later selection of one is a miss). A step whose layer list is longer
+ * than g keeps the first g chunks of the list (as with gpu_chunks < index_topk).
+ * The decisions are taken on the device by the resolve kernel, so they also
+ * run inside a captured CUDA graph.
+ */
+typedef struct {
+    int enabled;        /* 0: every swapped layer uses all gpu_chunks slots (the default) */
+    int g_min;          /* >= index_topk (>= 1 with allow_topk_reduction) */
+    int g_max;          /* <= gpu_chunks */
+    int g_init;         /* slots in use from the next kvswap_stage on; g_min <= g_init <= g_max */
+    int epoch;          /* swap steps per decision, >= 1 */
+    int lo_permille;    /* grow below this hit rate (per mille), 0..1000 */
+    int hi_permille;    /* shrink above this hit rate, lo_permille..1000 */
+    int delta;          /* slots added or removed per decision, >= 1 */
+} srh_adaptive;
+
+/*
+ * Install (policy->enabled != 0) or remove (policy NULL or enabled == 0) the
+ * adaptive capacity of every swapped (layer, sequence). Waits for the device.
+ * The next kvswap_stage resizes each swapped (layer, sequence) to g_init
+ * (to gpu_chunks on removal) and restarts its hit-rate window; the staged
+ * rows of the kept slots stay valid. Returns SRH_OK or SRH_ERR_INVALID (bad
+ * bounds, recorded in srh_last_error) or SRH_ERR_CUDA.
+ */
+int srh_set_adaptive(srh_ctx* ctx, const srh_adaptive* policy);
+
+/*
+ * Slots in use per (layer, sequence): out is a host array [n_layers][batch];
+ * a swapped layer reports the g of its last kvswap_stage (gpu_chunks before
+ * the first), a swap-disabled layer its cap (its chunks are staged at their
+ * own rows). Waits for the device. Returns SRH_OK, SRH_ERR_INVALID or SRH_ERR_CUDA.
+ */
+int srh_get_active_slots(srh_ctx* ctx, int* out);
+
 /* Copy the swap counters out (waits for the device). */
 int srh_get_stats(srh_ctx* ctx, srh_stats* out);
 

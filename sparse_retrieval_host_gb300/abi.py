@@ -70,6 +70,12 @@ class SrhStats(ctypes.Structure):
         return {k: getattr(self, k) for k, _ in self._fields_}
 
 
+class SrhAdaptive(ctypes.Structure):
+    """srh_adaptive: the hit-rate policy of the staging capacity."""
+    _fields_ = [(name, ctypes.c_int) for name in
+                ("enabled", "g_min", "g_max", "g_init", "epoch", "lo_permille", "hi_permille", "delta")]
+
+
 class SrhError(RuntimeError):
     def __init__(self, code: int, where: str, detail: str = ""):
         self.code = code
@@ -100,6 +106,8 @@ SIGNATURES = [
     ("kvswap_stage", _i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     ("lsa_attend", _i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp]),
     ("srh_set_chained", _i, [_vp, _i]),
+    ("srh_set_adaptive", _i, [_vp, ctypes.POINTER(SrhAdaptive)]),
+    ("srh_get_active_slots", _i, [_vp, ctypes.POINTER(ctypes.c_int)]),
     ("srh_get_stats", _i, [_vp, ctypes.POINTER(SrhStats)]),
     ("srh_reset_stats", _i, [_vp]),
     ("srh_check_error", _i, [_vp]),
@@ -263,6 +271,24 @@ def lsa_attend(ctx, layer, q, n_heads, window, staging, phys, count_l, out, stre
 
 def srh_set_chained(ctx, on: bool) -> None:
     _check(load().srh_set_chained(ctx, 1 if on else 0), "srh_set_chained", ctx)
+
+
+def srh_set_adaptive(ctx, policy=None) -> None:
+    """policy: None (remove) or a mapping with the srh_adaptive fields except
+    ``enabled``."""
+    if policy is None:
+        rc = load().srh_set_adaptive(ctx, None)
+    else:
+        p = SrhAdaptive(enabled=1, **dict(policy))
+        rc = load().srh_set_adaptive(ctx, ctypes.byref(p))
+    _check(rc, "srh_set_adaptive", ctx)
+
+
+def srh_get_active_slots(ctx, n_layers: int, batch: int):
+    """Slots in use per (layer, sequence), as a list of lists."""
+    buf = (ctypes.c_int * (n_layers * batch))()
+    _check(load().srh_get_active_slots(ctx, buf), "srh_get_active_slots", ctx)
+    return [[buf[l * batch + b] for b in range(batch)] for l in range(n_layers)]
 
 
 def srh_get_stats(ctx) -> dict:

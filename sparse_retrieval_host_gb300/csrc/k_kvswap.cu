@@ -90,7 +90,7 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
            const int32_t* __restrict__ sel, const int32_t* __restrict__ count,
            int32_t* __restrict__ phys, int32_t* __restrict__ count_l, int2* __restrict__ miss,
            int* __restrict__ miss_count, unsigned long long* __restrict__ stats,
-           uint32_t* __restrict__ err) {
+           uint32_t* __restrict__ err, AdaptParams ap) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     LruShared& sh = *reinterpret_cast<LruShared*>(smem_raw);
     int* r = reinterpret_cast<int*>(smem_raw + sizeof(LruShared));  // [S] layer list
@@ -186,53 +186,107 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
         return;
     }
 
-    // a swapped layer stages at most G chunks per step (only reachable with
-    // allow_topk_reduction): it keeps the first G of its list
-    if (m > G) m = G;
-
     int* slot_of = ld.slot_of + (size_t)b * cap;
     int* slot_logical = ld.slot_logical + (size_t)b * G;
     int* lru = ld.lru_order + (size_t)b * G;
+    AdaptState* as = ld.adapt + b;
 
-    // ---- 2. resident lookups and the LRU queue
+    // ---- 2a. slots in use: the last step's range g0, resized to g when the
+    // hit-rate policy (or the host) asked for it. No staged row moves.
+    int g0 = as->g, g = as->g_next;
+    if (g0 < 1 || g0 > G || g < 1 || g > G) {
+        if (tid == 0) atomicOr(err, kErrBounds);
+        g0 = (g0 < 1 || g0 > G) ? G : g0;
+        g = (g < 1 || g > G) ? g0 : g;
+    }
+    if (g > g0) {
+        // the new slots, empty, go to the least recently used end, lowest first
+        const int add = g - g0;
+        for (int q = tid; q < add; q += blockDim.x) {
+            const int s = g0 + q;
+            const int c = slot_logical[s];
+            if (c >= 0 && c < cap && slot_of[c] == s) slot_of[c] = -1;
+            slot_logical[s] = -1;
+            queue[q] = s;
+        }
+        for (int q = tid; q < g0; q += blockDim.x) {
+            int s = lru[q];
+            if (s < 0 || s >= g0) {
+                atomicOr(err, kErrBounds);
+                s = q;
+            }
+            queue[add + q] = s;
+        }
+        __syncthreads();
+    } else if (g < g0) {
+        // keep the slots below g in their order; the others forget their chunks
+        for (int q = tid; q < g0; q += blockDim.x) {
+            int s = lru[q];
+            if (s < 0 || s >= g0) {
+                atomicOr(err, kErrBounds);
+                s = q;
+            }
+            victim[q] = s;
+            nh[q] = s < g ? 1 : 0;
+        }
+        __syncthreads();
+        block_scan_excl_array(nh, g0, sh.warp_buf, &sh.total);
+        for (int q = tid; q < g0; q += blockDim.x) {
+            const int s = victim[q];
+            if (s < g) {
+                queue[nh[q]] = s;
+            } else {
+                const int c = slot_logical[s];
+                if (c >= 0 && c < cap && slot_of[c] == s) slot_of[c] = -1;
+                slot_logical[s] = -1;
+            }
+        }
+        __syncthreads();
+    } else {
+        for (int q = tid; q < g; q += blockDim.x) {
+            int s = lru[q];
+            if (s < 0 || s >= g) {
+                atomicOr(err, kErrBounds);
+                s = q;
+            }
+            queue[q] = s;
+        }
+    }
+    // a swapped layer stages at most g chunks per step (reachable with
+    // allow_topk_reduction or a small adaptive range): it keeps the first g
+    if (m > g) m = g;
+
+    // ---- 2b. resident lookups and the LRU queue
     for (int p = tid; p < m; p += blockDim.x) {
         const int c = r[p];
         int s = slot_of[c];
         ready[p] = ld.host_ready[(size_t)b * cap + c];   // read with the slot, used for misses
-        if (s >= G) {
+        if (s >= g) {
             atomicOr(err, kErrBounds);
             s = -1;
         }
         init_slot[p] = s;
     }
-    for (int q = tid; q < G; q += blockDim.x) {
-        int s = lru[q];
-        if (s < 0 || s >= G) {
-            atomicOr(err, kErrBounds);
-            s = q;
-        }
-        queue[q] = s;
-        hit_time[q] = INT_MAX;
-    }
+    for (int q = tid; q < g; q += blockDim.x) hit_time[q] = INT_MAX;
     __syncthreads();
-    for (int q = tid; q < G; q += blockDim.x) qpos[queue[q]] = q;
+    for (int q = tid; q < g; q += blockDim.x) qpos[queue[q]] = q;
     for (int p = tid; p < m; p += blockDim.x)
         if (init_slot[p] >= 0) hit_time[init_slot[p]] = p;
     if (tid == 0) sh.conflict = 0;
     __syncthreads();
 
     // ---- 3. optimistic two-phase assignment
-    for (int q = tid; q < G; q += blockDim.x) nh[q] = hit_time[queue[q]] == INT_MAX ? 1 : 0;
+    for (int q = tid; q < g; q += blockDim.x) nh[q] = hit_time[queue[q]] == INT_MAX ? 1 : 0;
     for (int p = tid; p < m; p += blockDim.x) {
         is_miss[p] = init_slot[p] < 0 ? 1 : 0;
         mr[p] = is_miss[p];
     }
     __syncthreads();
-    block_scan_excl_array(nh, G, sh.warp_buf, &sh.total);
+    block_scan_excl_array(nh, g, sh.warp_buf, &sh.total);
     const int nmiss0 = block_scan_excl_array(mr, m, sh.warp_buf, &sh.total);
     for (int p = tid; p < m; p += blockDim.x)
         if (is_miss[p]) tk[mr[p]] = p;
-    for (int q = tid; q < G; q += blockDim.x)
+    for (int q = tid; q < g; q += blockDim.x)
         if (hit_time[queue[q]] == INT_MAX) victim[nh[q]] = queue[q];
     __syncthreads();
     // a hit slot j lying before the kj-th non-hit slot is reached by that pop if
@@ -252,7 +306,7 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
         __syncthreads();
     } else {
         // replay the list one id at a time (flag: 0 untouched, 1 hit, 2 refilled)
-        for (int q = tid; q < G; q += blockDim.x) flag[q] = 0;
+        for (int q = tid; q < g; q += blockDim.x) flag[q] = 0;
         __syncthreads();
         if (tid == 0) {
             int ptr = 0, nm = 0;
@@ -263,8 +317,8 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
                     assign[p] = j;
                     is_miss[p] = 0;
                 } else {
-                    while (ptr < G && flag[queue[ptr]] != 0) ++ptr;
-                    const int s = ptr < G ? queue[ptr++] : 0;
+                    while (ptr < g && flag[queue[ptr]] != 0) ++ptr;
+                    const int s = ptr < g ? queue[ptr++] : 0;
                     flag[s] = 2;
                     assign[p] = s;
                     is_miss[p] = 1;
@@ -281,16 +335,16 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
     const int nmiss = sh.nmiss;
 
     // ---- 4. new LRU order: untouched slots in old order, then touched ones by position
-    for (int q = tid; q < G; q += blockDim.x) flag[q] = 0;
+    for (int q = tid; q < g; q += blockDim.x) flag[q] = 0;
     __syncthreads();
     for (int p = tid; p < m; p += blockDim.x) flag[assign[p]] = 1;
     __syncthreads();
-    for (int q = tid; q < G; q += blockDim.x) nh[q] = flag[queue[q]] ? 0 : 1;
+    for (int q = tid; q < g; q += blockDim.x) nh[q] = flag[queue[q]] ? 0 : 1;
     __syncthreads();
-    block_scan_excl_array(nh, G, sh.warp_buf, &sh.total);
-    for (int q = tid; q < G; q += blockDim.x)
+    block_scan_excl_array(nh, g, sh.warp_buf, &sh.total);
+    for (int q = tid; q < g; q += blockDim.x)
         if (!flag[queue[q]]) lru[nh[q]] = queue[q];
-    for (int p = tid; p < m; p += blockDim.x) lru[G - m + p] = assign[p];
+    for (int p = tid; p < m; p += blockDim.x) lru[g - m + p] = assign[p];
 
     // ---- 5. slot maps: clear evicted chunks first, then record the new ones
     for (int p = tid; p < m; p += blockDim.x)
@@ -317,6 +371,28 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
         atomicAdd(&stats[kStatHits], (unsigned long long)(m - nmiss));
         atomicAdd(&stats[kStatMisses], (unsigned long long)nmiss);
         atomicAdd(&stats[kStatSelected], (unsigned long long)m);
+        // ---- 6. hit-rate window of the adaptive policy
+        as->g = g;
+        if (ap.on) {
+            int en = as->ep_steps + 1;
+            long long eh = as->ep_hits + (m - nmiss);
+            long long es = as->ep_sel + m;
+            int gn = g;
+            if (en >= ap.epoch) {
+                if (eh * 1000 < (long long)ap.lo_pm * es)
+                    gn = min(ap.g_max, g + ap.delta);
+                else if (eh * 1000 > (long long)ap.hi_pm * es)
+                    gn = max(ap.g_min, g - ap.delta);
+                en = 0;
+                eh = es = 0;
+            }
+            as->ep_steps = en;
+            as->ep_hits = eh;
+            as->ep_sel = es;
+            as->g_next = gn;
+        } else {
+            as->g_next = g;
+        }
     }
 }
 
@@ -423,7 +499,8 @@ size_t lru_smem_bytes(int S, int G) {
 cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int S, int src_ratio,
                        long long max_dedup_cap, const int32_t* sel, const int32_t* count,
                        int32_t* phys, int32_t* count_l, int2* miss, int* miss_count,
-                       unsigned long long* stats, uint32_t* err, cudaStream_t st, bool chained) {
+                       unsigned long long* stats, uint32_t* err, AdaptParams ap, cudaStream_t st,
+                       bool chained) {
     // a shared-memory table of first positions for layers whose ratio differs from
     // src_ratio, when it fits; otherwise those layers fall back to pairwise checks
     int tbl = 0;
@@ -437,7 +514,7 @@ cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int
         if (e != cudaSuccess) return e;
     }
     return launch_k(lru_kernel, dim3(nl * B), dim3(kLruThreads), smem, st, chained, layers, l0, B, G, S, src_ratio,
-                    tbl, sel, count, phys, count_l, miss, miss_count, stats, err);
+                    tbl, sel, count, phys, count_l, miss, miss_count, stats, err, ap);
 }
 
 cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, int S,

@@ -109,6 +109,7 @@ void free_ctx(srh_ctx* ctx) {
         cudaFree(ld.slot_of);
         cudaFree(ld.slot_logical);
         cudaFree(ld.lru_order);
+        cudaFree(ld.adapt);
     }
     cudaFree(ctx->d_layers);
     cudaFree(ctx->d_stats);
@@ -262,6 +263,11 @@ int srh_create(const srh_config* cfg, srh_ctx** out) {
                 for (int b = 0; b < B; ++b)
                     for (int q = 0; q < G; ++q) order[(size_t)b * G + q] = q;   // slot 0 at the back
                 e = cudaMemcpy(ld.lru_order, order.data(), sizeof(int) * order.size(), cudaMemcpyHostToDevice);
+            }
+            if (e == cudaSuccess) e = cudaMalloc(&ld.adapt, sizeof(AdaptState) * (size_t)B);
+            if (e == cudaSuccess) {
+                std::vector<AdaptState> st((size_t)B, AdaptState{G, G, 0, 0, 0, 0});   // all slots in use
+                e = cudaMemcpy(ld.adapt, st.data(), sizeof(AdaptState) * st.size(), cudaMemcpyHostToDevice);
             }
         }
         if (e != cudaSuccess) return bail(SRH_ERR_NOMEM, std::string("device state: ") + cudaGetErrorString(e));
@@ -494,7 +500,7 @@ int kvswap_stage(srh_ctx* ctx, int layer, const int32_t* d_sel, const int32_t* d
         if (ctx->ratios[l] != ctx->cfg.src_ratio) dedup_cap = std::max(dedup_cap, ctx->caps[l]);
     cudaError_t e = launch_lru(ctx->d_layers, l0, nl, ctx->B, ctx->G, ctx->S, ctx->cfg.src_ratio, dedup_cap,
                                d_sel, d_count, d_phys, d_count_l, ctx->d_miss, ctx->d_miss_count, ctx->d_stats,
-                               ctx->d_err, sm, ctx->chained);
+                               ctx->d_err, ctx->adapt, sm, ctx->chained);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "kvswap_stage LRU launch");
     if (ss && ss != sm) {
         SRH_CUDA(ctx, cudaEventRecord(ctx->ev_resolved, sm));
@@ -534,6 +540,58 @@ int lsa_attend(srh_ctx* ctx, int layer, const uint16_t* d_q, int n_heads, const 
                                         d_count_l, d_out, ctx->d_part_o, ctx->d_part_ml, ctx->d_err,
                                         (cudaStream_t)stream, ctx->chained);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "lsa_attend launch");
+    return SRH_OK;
+}
+
+int srh_set_adaptive(srh_ctx* ctx, const srh_adaptive* p) {
+    if (!ctx) return SRH_ERR_INVALID;
+    AdaptParams ap{};
+    const int G = ctx->G;
+    int g_next = G;
+    if (p && p->enabled) {
+        const int lo_g = ctx->cfg.allow_topk_reduction ? 1 : ctx->cfg.index_topk;
+        if (p->g_max < 1 || p->g_max > G) return fail(ctx, SRH_ERR_INVALID, "g_max must be in [1, gpu_chunks]");
+        if (p->g_min < lo_g || p->g_min > p->g_max)
+            return fail(ctx, SRH_ERR_INVALID, "g_min must be in [index_topk, g_max]");
+        if (p->g_init < p->g_min || p->g_init > p->g_max)
+            return fail(ctx, SRH_ERR_INVALID, "g_init must be in [g_min, g_max]");
+        if (p->epoch < 1 || p->delta < 1) return fail(ctx, SRH_ERR_INVALID, "epoch and delta must be >= 1");
+        if (p->lo_permille < 0 || p->lo_permille > p->hi_permille || p->hi_permille > 1000)
+            return fail(ctx, SRH_ERR_INVALID, "need 0 <= lo_permille <= hi_permille <= 1000");
+        ap = AdaptParams{1, p->g_min, p->g_max, p->epoch, p->lo_permille, p->hi_permille, p->delta};
+        g_next = p->g_init;
+    }
+    SRH_CUDA(ctx, cudaDeviceSynchronize());
+    std::vector<AdaptState> st((size_t)ctx->B);
+    for (int l = 0; l < ctx->L; ++l) {
+        if (!ctx->swap[l]) continue;
+        AdaptState* d = ctx->h_layers[l].adapt;
+        SRH_CUDA(ctx, cudaMemcpy(st.data(), d, sizeof(AdaptState) * st.size(), cudaMemcpyDeviceToHost));
+        for (auto& a : st) {
+            a.g_next = g_next;
+            a.ep_steps = 0;
+            a.ep_hits = a.ep_sel = 0;
+        }
+        SRH_CUDA(ctx, cudaMemcpy(d, st.data(), sizeof(AdaptState) * st.size(), cudaMemcpyHostToDevice));
+    }
+    ctx->adapt = ap;
+    return SRH_OK;
+}
+
+int srh_get_active_slots(srh_ctx* ctx, int* out) {
+    if (!ctx) return SRH_ERR_INVALID;
+    if (!out) return fail(ctx, SRH_ERR_INVALID, "NULL pointer");
+    SRH_CUDA(ctx, cudaDeviceSynchronize());
+    std::vector<AdaptState> st((size_t)ctx->B);
+    for (int l = 0; l < ctx->L; ++l) {
+        if (ctx->swap[l]) {
+            SRH_CUDA(ctx, cudaMemcpy(st.data(), ctx->h_layers[l].adapt, sizeof(AdaptState) * st.size(),
+                                     cudaMemcpyDeviceToHost));
+            for (int b = 0; b < ctx->B; ++b) out[(size_t)l * ctx->B + b] = st[b].g;
+        } else {
+            for (int b = 0; b < ctx->B; ++b) out[(size_t)l * ctx->B + b] = (int)ctx->caps[l];
+        }
+    }
     return SRH_OK;
 }
 

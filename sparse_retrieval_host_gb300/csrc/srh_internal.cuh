@@ -62,6 +62,25 @@ enum : int {
     kStatCount
 };
 
+// Adaptive capacity of one swapped (layer, sequence): slots [0, g) are in use.
+struct AdaptState {
+    int g;               // slots used by the last resolve
+    int g_next;          // slots the next resolve uses (policy decision or host setting)
+    int ep_steps;        // swap steps in the current hit-rate window
+    int pad;
+    long long ep_hits;   // hits in the window
+    long long ep_sel;    // chunks resolved in the window
+};
+
+// The hit-rate policy, passed by value to the resolve kernel (on == 0: none).
+struct AdaptParams {
+    int on;
+    int g_min, g_max;
+    int epoch;
+    int lo_pm, hi_pm;
+    int delta;
+};
+
 // Per-layer facts and state pointers, kept in device memory ([L] array).
 struct LayerDev {
     long long cap;           // chunks of this layer
@@ -71,7 +90,8 @@ struct LayerDev {
     uint8_t* host_ready;     // [B][cap]
     int* slot_of;            // [B][cap]: slot holding chunk c, -1 if none (swap layers)
     int* slot_logical;       // [B][G]: chunk in slot s, -1 if free (swap layers)
-    int* lru_order;          // [B][G]: slots from least (0) to most recently used
+    int* lru_order;          // [B][G]: slots in use from least (0) to most recently used
+    AdaptState* adapt;       // [B] (swap layers)
 };
 
 // One attention work item: rows [split*split_rows, ...) of (layer, seq).
@@ -118,6 +138,7 @@ struct Ctx {
     unsigned long long* d_stats = nullptr;
     uint32_t* d_err = nullptr;
     bool chained = false;               // srh_set_chained: step kernels may launch early
+    AdaptParams adapt{};                // srh_set_adaptive
     uint32_t* d_hist = nullptr;         // [B][kHistBins]
     unsigned long long* d_cand = nullptr; // [B][select_cand_cap()] candidate composites
     int* d_cand_cnt = nullptr;          // [B]
@@ -179,7 +200,8 @@ cudaError_t launch_select(const float* scores, int n, int B, int mode, int k, fl
 cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int S, int src_ratio,
                        long long max_dedup_cap, const int32_t* sel, const int32_t* count,
                        int32_t* phys, int32_t* count_l, int2* miss, int* miss_count,
-                       unsigned long long* stats, uint32_t* err, cudaStream_t st, bool chained);
+                       unsigned long long* stats, uint32_t* err, AdaptParams ap, cudaStream_t st,
+                       bool chained);
 cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, int S,
                           const int2* miss, const int* miss_count, float* staging,
                           uint32_t* err, int sm_count, cudaStream_t st, bool chained);

@@ -180,6 +180,15 @@ class DecodeStep:
         return graphs
 
     # ------------------------------------------------------------------ status
+    def set_adaptive(self, policy=None) -> None:
+        """Adaptive staging capacity (srh_set_adaptive); ``policy`` is a mapping
+        of g_min, g_max, g_init, epoch, lo_permille, hi_permille, delta, or None."""
+        abi.srh_set_adaptive(self.ctx, policy)
+
+    def active_slots(self):
+        """Slots in use per (layer, sequence) (srh_get_active_slots)."""
+        return abi.srh_get_active_slots(self.ctx, self.L, self.B)
+
     def stats(self) -> dict:
         return abi.srh_get_stats(self.ctx)
 

@@ -22,14 +22,20 @@ def _built():
     torch.cuda.set_device(0)
 
 
-def _run_decode(w, steps, attend_layers=None, pools=None):
-    """Run ``steps`` decode steps on GPU and oracle; returns (n_matched_steps, worst_attn_rel)."""
+def _run_decode(w, steps, attend_layers=None, pools=None, policy=None):
+    """Run ``steps`` decode steps on GPU and oracle; returns (n_matched_steps, worst_attn_rel).
+    With ``policy`` both sides run the adaptive staging capacity."""
     ds = make_ds(w)
     try:
         if pools is None and w.n_chunks <= 8192:
             pools = {(l, b): G.pool(w, l, b) for l in range(w.n_layers) for b in range(w.batch)}
         keys = fill(ds, w, pools)
         ora = make_oracle(w)
+        caps_seen = set()
+        if policy is not None:
+            ds.set_adaptive(policy)
+            from oracle import srh_oracle as O
+            ora.install_policy(O.AdaptivePolicy(**policy))
         spec = spec_of(w)
         # Exact slot/LRU comparisons need the same selection ORDER on both sides
         # since the first step; the order of chunks whose scores differ by less
@@ -62,8 +68,12 @@ def _run_decode(w, steps, attend_layers=None, pools=None):
             order_sync &= same
             phys = ds.phys.cpu().numpy()
             cl = ds.count_l.cpu().numpy()
+            active = ds.active_slots() if policy is not None else None
             for l in range(w.n_layers):
                 for b in range(w.batch):
+                    if active is not None and order_sync and ds.swap[l]:
+                        assert active[l][b] == ora.states[l][b].capacity, (t, l, b)
+                        caps_seen.add(active[l][b])
                     if same:
                         assert sorted(ref.lists[l][b]) == sorted(
                             set((sel[b, :cnt[b]].astype(np.int64) * 4 // w.layer_ratios[l]).tolist()))
@@ -91,6 +101,8 @@ def _run_decode(w, steps, attend_layers=None, pools=None):
         if order_sync:
             st = ds.stats()
             assert st["hits"] == hits and st["misses"] == misses
+        if policy is not None:
+            assert len(caps_seen) > 1, caps_seen     # compared while the orders agreed
         assert ds.check_error() == 0
         return matched, worst
     finally:
@@ -115,6 +127,16 @@ def test_decode_batch_sweep_b4():
     w = C.batch_sweep(4)
     matched, worst = _run_decode(w, 20, attend_layers=[0, 7, 19])
     assert matched == 20
+    assert worst <= ATTN_TOL, worst
+
+
+def test_decode_ctx8k_adaptive_capacity():
+    """Adaptive staging capacity over the full 8K stack: per step the capacity
+    in use, the slots and the outputs match the oracle under the same policy."""
+    w = C.CTX8K
+    policy = dict(g_min=512, g_max=1024, g_init=1024, epoch=4, lo_permille=800, hi_permille=950, delta=128)
+    matched, worst = _run_decode(w, 40, attend_layers=[0, 19, 20, 40], policy=policy)
+    assert matched == 40
     assert worst <= ATTN_TOL, worst
 
 
@@ -160,18 +182,26 @@ def test_residency_changes_slots_never_outputs():
     assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("parts", [False, True], ids=["one_graph", "three_graphs"])
-def test_graph_replay_equals_eager_steps(parts):
+@pytest.mark.parametrize("parts,adaptive", [(False, False), (True, False), (False, True)],
+                         ids=["one_graph", "three_graphs", "one_graph_adaptive"])
+def test_graph_replay_equals_eager_steps(parts, adaptive):
     """Steps replayed from captured CUDA graphs give the same bits as eager
     calls (chained, through step(), and unchained, call by call): selections,
-    slots, staged rows, outputs and the swap counters."""
+    slots, staged rows, outputs and the swap counters; with the adaptive
+    capacity also the capacity decided on the device each step."""
     w = C.TINY.with_(steps=12)
+    policy = None
+    if adaptive:
+        w = w.with_(gpu_chunks=1024, lookahead=4)
+        policy = dict(g_min=512, g_max=1024, g_init=768, epoch=2, lo_permille=700, hi_permille=900, delta=128)
     runs = []
     for mode in ("eager", "graph", "unchained"):
         ds = make_ds(w)
         try:
             fill(ds, w)
             spec = spec_of(w)
+            if policy is not None:
+                ds.set_adaptive(policy)
             load_step_inputs(ds, w, 0)
             ds.step(spec)                       # one eager step before capture
             graphs = ds.capture(spec, parts=parts) if mode == "graph" else None
@@ -190,6 +220,8 @@ def test_graph_replay_equals_eager_steps(parts):
                         g.replay()
                 torch.cuda.synchronize()
                 seq.append([x.clone() for x in (ds.sel, ds.count, ds.phys, ds.count_l, ds.out)])
+                if policy is not None:
+                    seq[-1].append(torch.tensor(ds.active_slots()))
             st = ds.stats()
             runs.append((seq, st["hits"], st["misses"], ds.staging.clone()))
             assert ds.check_error() == 0

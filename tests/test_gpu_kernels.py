@@ -311,6 +311,76 @@ def test_kvswap_stage_matches_list_lru(G_, k, ctx_len):
         ds.close()
 
 
+@pytest.mark.parametrize("G_,k,policy", [
+    (64, 24, dict(g_min=24, g_max=64, g_init=32, epoch=2, lo_permille=600, hi_permille=850, delta=8)),
+    (96, 32, dict(g_min=32, g_max=80, g_init=80, epoch=1, lo_permille=300, hi_permille=500, delta=16)),
+    (512, 128, dict(g_min=128, g_max=512, g_init=128, epoch=3, lo_permille=700, hi_permille=900, delta=64)),
+])
+def test_kvswap_stage_adaptive_capacity_matches_oracle(G_, k, policy):
+    """Adaptive staging capacity: per step the slots, misses, staged rows and
+    the capacity in use match the oracle's resizable LRU under the same policy;
+    removing the policy restores every slot."""
+    ratios = (4, 128, 4, 8)
+    w = _w(context_len=4 * 700, layer_ratios=ratios, gpu_chunks=G_, index_topk=k, batch=2, code=58)
+    ds = make_ds(w, max_select=k)
+    try:
+        pools = {(l, b): G.pool(w, l, b) for l in range(w.n_layers) for b in range(w.batch)}
+        fill(ds, w, pools)
+        states = [[O.KvSwapLayerState(w.layer_cap(l), G_) for b in range(w.batch)] for l in range(w.n_layers)]
+        pol = O.AdaptivePolicy(**policy)
+        for row in states:
+            for st in row:
+                st.host_ready[:] = 1
+                if st.swap_enabled:
+                    st.install_policy(pol)
+        ds.set_adaptive(policy)
+        rng = np.random.default_rng(G_ + 7 * k)
+        n_steps = 30
+        traces = [_trace(rng, n_steps, w.n_chunks, k, G_) for _ in range(w.batch)]
+        seen = set()
+        for t in range(n_steps):
+            if t == n_steps - 6:
+                ds.set_adaptive(None)
+                for row in states:
+                    for st in row:
+                        if st.swap_enabled:
+                            st.install_policy(None)
+            sel = np.zeros((w.batch, ds.S), np.int32)
+            cnt = np.zeros(w.batch, np.int32)
+            for b in range(w.batch):
+                ids = traces[b][t]
+                sel[b, :len(ids)] = ids
+                cnt[b] = len(ids)
+            ds.sel.copy_(torch.from_numpy(sel))
+            ds.count.copy_(torch.from_numpy(cnt))
+            ds.stage()
+            torch.cuda.synchronize()
+            phys = ds.phys.cpu().numpy()
+            cl = ds.count_l.cpu().numpy()
+            staging = ds.staging.cpu().numpy()
+            active = ds.active_slots()
+            for l in range(w.n_layers):
+                for b in range(w.batch):
+                    st = states[l][b]
+                    lst = O.layer_chunks(traces[b][t], 4, ratios[l])
+                    g = st.active_capacity()
+                    if st.swap_enabled:
+                        lst = lst[:g]
+                    r = st.swap_in_selected(lst)
+                    assert cl[l, b] == len(lst), (t, l, b)
+                    assert phys[l, b, :len(lst)].tolist() == r.phys, (t, l, b)
+                    rows = staging[l, b][phys[l, b, :len(lst)] - 128]
+                    assert np.array_equal(rows, pools[(l, b)][lst]), (t, l, b)
+                    assert active[l][b] == (st.capacity if st.swap_enabled else w.layer_cap(l)), (t, l, b)
+                    if st.swap_enabled:
+                        seen.add(st.capacity)
+        assert len(seen) > 1, "the policy never changed the capacity"
+        assert all(active[l][b] == G_ for l in range(w.n_layers) for b in range(w.batch) if states[l][b].swap_enabled)
+        assert ds.check_error() == 0
+    finally:
+        ds.close()
+
+
 def test_kvswap_not_stored_is_reported():
     """Section 故障排查, error 4: a selected chunk that was never stored."""
     from sparse_retrieval_host_gb300 import abi
