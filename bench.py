@@ -207,6 +207,17 @@ def launches_per_step(w, sm_count):
     return BASE_KERNELS + merge + collect
 
 
+def adaptive_policy(w):
+    """Hit-rate policy for the adaptive-capacity run: from GPU_CHUNKS down to
+    index_topk slots, one decision per lookahead window, shrink above a 90 %
+    hit rate, grow below 80 %. None when the workload leaves no room."""
+    swapped = any(-(-w.context_len // r) > w.gpu_chunks for r in w.layer_ratios)
+    if not swapped or w.gpu_chunks <= w.index_topk:
+        return None
+    return dict(g_min=w.index_topk, g_max=w.gpu_chunks, g_init=w.gpu_chunks, epoch=w.lookahead,
+                lo_permille=800, hi_permille=900, delta=max(1, w.gpu_chunks // 8))
+
+
 def score_bytes(w):
     return w.batch * w.n_chunks * (C.INDEXER_DIM * 2 + 4)
 
@@ -276,6 +287,47 @@ def run_ours(args, dist, rank, world, local):
     torch.cuda.synchronize()
     assert ds.check_error() == 0, "device error during the periodic-selection steps"
     periodic_ms = [e0.elapsed_time(e1) for e0, e1 in evp]
+
+    # adaptive staging capacity: the same steps with the hit-rate policy deciding
+    # on the device; the policy is a launch argument, so the step is captured again
+    adaptive = None
+    policy = adaptive_policy(w)
+    if policy is not None:
+        ds.set_adaptive(policy)
+        (graph_ad,) = ds.capture(spec)
+        t0 = args.warmup + K + KP
+        settle = 6 * policy["epoch"]
+        for i in range(settle):                       # let the capacity settle (untimed)
+            bind(t0 + i)
+            graph_ad.replay()
+        torch.cuda.synchronize()
+        ds.reset_stats()
+        eva = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        for i in range(K):
+            bind(t0 + settle + i)
+            flush_l2()
+            eva[i][0].record(stream)
+            graph_ad.replay()
+            eva[i][1].record(stream)
+        torch.cuda.synchronize()
+        assert ds.check_error() == 0, "device error during the adaptive-capacity steps"
+        sta = ds.stats()
+        act = ds.active_slots()
+        swapped = [act[l][b] for l in range(ds.L) for b in range(ds.B) if ds.swap[l]]
+        ada_ms = [e0.elapsed_time(e1) for e0, e1 in eva]
+        sel_a = sta["hits"] + sta["misses"]
+        adaptive = {
+            "value": K / (sum(ada_ms) / 1e3), "unit": "steps/s", "ms_per_step": statistics.mean(ada_ms),
+            "policy": policy,
+            "lru_hit_rate": (sta["hits"] / sel_a) if sel_a else None,
+            "staged_bytes_per_step": sta["h2d_bytes"] / K,
+            "mean_active_slots": statistics.mean(swapped),
+            "gpu_chunks": w.gpu_chunks,
+            "staging_bytes_in_use": sum(swapped) * C.KV_DIM * 4,
+            "staging_bytes_allocated": len(swapped) * w.gpu_chunks * C.KV_DIM * 4,
+            "note": f"srh_set_adaptive; {settle} settling steps, then {K} timed steps of one graph each; "
+                    "slots in use read after the timed steps"}
+        ds.set_adaptive(None)
 
     # breakdown: the same steps as three graphs with events between the phases
     KB = min(K, 20)
@@ -396,6 +448,7 @@ def run_ours(args, dist, rank, world, local):
             "staged_bytes_per_step": st["h2d_bytes"] / K,
             "selected_per_step": st["selected"] / K,
             "wall_s": wall,
+            "adaptive_capacity": adaptive,
             "periodic_selection": {
                 "value": KP / (sum(periodic_ms) / 1e3), "unit": "steps/s",
                 "ms_per_step": statistics.mean(periodic_ms),
