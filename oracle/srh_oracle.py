@@ -546,3 +546,34 @@ class DecodeOracle:
                                    .reshape(-1, KV_DIM)], axis=0)
             res.out[(l, b)] = attend(attn_q_of(l, b), rows)
         return res
+
+    def lookahead_step(self, keys_of, fm_q_of, attn_q_of=None, window_of=None, pool_rows_of=None,
+                       attend_pairs=None, trigger: bool = True) -> StepResult:
+        """One step of the lookahead schedule (summary section "LSA 让模型预判 KV
+        chunk": the indexer predicts, from the current token, the chunks the
+        coming window of steps needs; PocketLLM doc, section "未来优化方向",
+        item 2: take the scoring off the step's critical path). At a trigger
+        step the indexer scores and selects and the selection is swapped in,
+        while the step's attention still reads the selection in force; the new
+        selection is in force from the next step on. Other steps only attend.
+        Before the first trigger no chunk is in force (window rows only).
+        ``lists`` and ``out`` describe the selection in force during the step;
+        ``sel``, ``scores`` and ``swap`` the new selection (trigger steps)."""
+        cur = getattr(self, "_in_force", None)
+        if cur is None:
+            cur = [[[] for _ in range(self.batch)] for _ in self.layer_ratios]
+        if trigger:
+            new = self.step(keys_of, fm_q_of)
+            res = StepResult(new.scores, new.sel, cur, new.swap)
+            self._in_force = new.lists
+        else:
+            res = StepResult([], [], cur, [])
+        if attend_pairs is None and attn_q_of is not None:
+            attend_pairs = [(l, b) for l in range(len(self.layer_ratios)) for b in range(self.batch)]
+        for (l, b) in attend_pairs or []:
+            rows = np.asarray(window_of(l, b), dtype=np.float64)
+            if cur[l][b]:
+                rows = np.concatenate([rows, np.asarray(pool_rows_of(l, b, cur[l][b]), dtype=np.float64)
+                                       .reshape(-1, KV_DIM)], axis=0)
+            res.out[(l, b)] = attend(attn_q_of(l, b), rows)
+        return res

@@ -552,6 +552,68 @@ def test_decode_oracle_keeps_list_prefix_under_small_capacity():
     assert sorted(p - 128 for p in r.swap[0][0].phys) == list(range(100))
 
 
+def _small_oracle(w):
+    ora = O.DecodeOracle(context_len=w.context_len, layer_ratios=w.layer_ratios, gpu_chunks=w.gpu_chunks,
+                         index_topk=w.index_topk, batch=1, scale=w.scale, bias=[0.0] * 3,
+                         ensemble_mode=w.ensemble, select_mode=w.select_mode, tau=w.tau, clamp=w.clamp)
+    ora.mark_all_stored()
+    return ora
+
+
+def test_lookahead_schedule_is_the_plain_step_one_step_late():
+    """Triggered at every step, the lookahead schedule attends at step t over
+    the chunks that the indexer picked from step t-1's queries: the plain step
+    fed step t-1's indexer queries and step t's attention queries gives the
+    same output. Step 0 attends over the window rows alone (checked against
+    torch's attention)."""
+    w = C.TINY.with_(gpu_chunks=1024, lookahead=1, layer_ratios=(4, 128))
+    keys = G.keys(w, 0)
+    pools = {l: G.pool(w, l, 0) for l in range(2)}
+    rows_of = lambda l, b, idx: pools[l][np.asarray(idx, dtype=np.int64)]
+    win = lambda l, b: G.window(w, l, b)
+    la, plain = _small_oracle(w), _small_oracle(w)
+    for t in range(4):
+        q_t = lambda l, b, t=t: G.attn_q(w, t, l, b)
+        r = la.lookahead_step(lambda b: keys, lambda b, t=t: G.fm_queries(w, t, b), q_t, win, rows_of,
+                              attend_pairs=[(0, 0), (1, 0)], trigger=True)
+        if t == 0:
+            for l in range(2):
+                q = torch.from_numpy(O.bf16_to_f64(G.attn_q(w, 0, l, 0)))[None, :, None, :].transpose(1, 2)
+                e = torch.from_numpy(win(l, 0).astype(np.float64))[None, None]
+                ref = torch.nn.functional.scaled_dot_product_attention(q.transpose(1, 2), e, e)[0]
+                assert np.allclose(r.out[(l, 0)], ref.numpy().reshape(r.out[(l, 0)].shape), rtol=1e-12, atol=1e-12)
+            continue
+        p = plain.step(lambda b: keys, lambda b, t=t: G.fm_queries(w, t - 1, b), q_t, win, rows_of,
+                       attend_pairs=[(0, 0), (1, 0)])
+        for l in range(2):
+            assert r.lists[l][0] == p.lists[l][0]
+            assert np.allclose(r.out[(l, 0)], p.out[(l, 0)], rtol=1e-13, atol=1e-13)
+
+
+def test_lookahead_schedule_swaps_like_periodic_selection():
+    """Between triggers the lookahead schedule resolves nothing; the periodic
+    schedule resolves the same list again (all hits). Touching a list that was
+    just resolved leaves the LRU order as it was, so both schedules stage the
+    same slots at every trigger and end in the same state."""
+    w = C.TINY.with_(gpu_chunks=1024, lookahead=3, layer_ratios=(4, 128))
+    keys = G.keys(w, 0)
+    la, per = _small_oracle(w), _small_oracle(w)
+    for t in range(9):
+        fq = lambda b, t=t: G.fm_queries(w, t, b)
+        trig = t % w.lookahead == 0
+        r = la.lookahead_step(lambda b: keys, fq, trigger=trig)
+        p = per.step(lambda b: keys, fq, rescore=trig)
+        if trig:
+            for l in range(2):
+                assert r.swap[l][0].phys == p.swap[l][0].phys and r.swap[l][0].misses == p.swap[l][0].misses
+        else:
+            assert all(p.swap[l][0].hits == len(p.lists[l][0]) for l in range(2) if per.states[l][0].swap_enabled)
+    for l in range(2):
+        a, b = la.states[l][0], per.states[l][0]
+        assert (a.slot_by_logical, list(a.slot_lru), a.gpu_slot_logical) == \
+               (b.slot_by_logical, list(b.slot_lru), b.gpu_slot_logical)
+
+
 def test_swap_disabled_layer_is_identity_mapped():
     st = O.KvSwapLayerState(16, 16)
     st.host_ready[:] = 1
