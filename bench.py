@@ -288,6 +288,37 @@ def run_ours(args, dist, rank, world, local):
     assert ds.check_error() == 0, "device error during the periodic-selection steps"
     periodic_ms = [e0.elapsed_time(e1) for e0, e1 in evp]
 
+    # lookahead schedule: a trigger step swaps in its new selection on a side
+    # stream while its attention reads the selection in force (not the headline:
+    # the selection takes effect one step later)
+    lookahead = None
+    m_sel = w.index_topk if w.select_mode == C.SELECT_TOPK else w.clamp
+    if w.gpu_chunks >= 2 * m_sel or not any(ds.swap):
+        t0 = args.warmup + K + KP
+        ds.lookahead_step(spec, True)             # eager first step (buffers, set-up)
+        torch.cuda.synchronize()
+        lgraphs = ds.capture_lookahead(spec)
+        evl = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        for i in range(K):
+            t = t0 + 1 + i
+            bind(t)
+            flush_l2()
+            evl[i][0].record(stream)
+            ds.replay_lookahead(lgraphs, t % w.lookahead == 0)
+            evl[i][1].record(stream)
+        torch.cuda.synchronize()
+        assert ds.check_error() == 0, "device error during the lookahead-schedule steps"
+        la_ms = [e0.elapsed_time(e1) for e0, e1 in evl]
+        trig_ms = [m for i, m in enumerate(la_ms) if (t0 + 1 + i) % w.lookahead == 0]
+        lookahead = {
+            "value": K / (sum(la_ms) / 1e3), "unit": "steps/s", "ms_per_step": statistics.mean(la_ms),
+            "trigger_step_us": statistics.mean(trig_ms) * 1e3 if trig_ms else None,
+            "note": f"indexer fires every {w.lookahead} steps; at a trigger step score + select + swap-in "
+                    "run on a side stream beside the attention over the selection in force; the other "
+                    "steps run the attention alone; one graph per step"}
+    else:
+        lookahead = {"value": None, "note": f"needs gpu_chunks >= {2 * m_sel} (two selections in flight)"}
+
     # adaptive staging capacity: the same steps with the hit-rate policy deciding
     # on the device; the policy is a launch argument, so the step is captured again
     adaptive = None
@@ -449,6 +480,7 @@ def run_ours(args, dist, rank, world, local):
             "selected_per_step": st["selected"] / K,
             "wall_s": wall,
             "adaptive_capacity": adaptive,
+            "lookahead_schedule": lookahead,
             "periodic_selection": {
                 "value": KP / (sum(periodic_ms) / 1e3), "unit": "steps/s",
                 "ms_per_step": statistics.mean(periodic_ms),

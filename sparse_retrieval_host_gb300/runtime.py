@@ -74,6 +74,7 @@ class DecodeStep:
         self.window = torch.zeros((L, B, abi.WINDOW, abi.KV_DIM), dtype=f32, device=dev)
         self.q = torch.zeros((L, B, H, abi.KV_DIM), dtype=i16, device=dev)
         self.out = torch.zeros((L, B, H, abi.KV_DIM), dtype=f32, device=dev)
+        self._adaptive = None
 
     # ------------------------------------------------------------------ host pools
     def pool_view(self, layer: int, seq: int) -> np.ndarray:
@@ -179,11 +180,87 @@ class DecodeStep:
         torch.cuda.current_stream(dev).wait_stream(s)
         return graphs
 
+    # ------------------------------------------------------------------ lookahead schedule
+    def _lookahead_setup(self, spec: StepSpec) -> None:
+        """Two phys/count_l buffers (the selection in force and the one being
+        staged) and the capacity check that makes the overlap safe."""
+        m = spec.k if spec.select_mode == abi.SRH_SELECT_TOPK else spec.clamp
+        g_lo = self.G if self._adaptive is None else self._adaptive["g_min"]
+        if any(self.swap) and g_lo < 2 * m:
+            raise ValueError(f"the lookahead schedule needs >= {2 * m} slots in use per swapped layer "
+                             f"(two selections of up to {m} chunks); the capacity can drop to {g_lo}")
+        if not hasattr(self, "phys2"):
+            dev = self.keys.device
+            self.phys2 = torch.zeros((2,) + tuple(self.phys.shape), dtype=torch.int32, device=dev)
+            self.count_l2 = torch.zeros((2,) + tuple(self.count_l.shape), dtype=torch.int32, device=dev)
+            self.in_force = 0
+            self.side = torch.cuda.Stream(device=dev)
+
+    def lookahead_step(self, spec: StepSpec, trigger: bool, stream=None, fm_q=None, q=None, out=None) -> None:
+        """One step of the lookahead schedule. At a trigger step the memory
+        indexer scores and selects from this step's queries and the selection
+        is swapped in on a side stream, while the attention on ``stream`` reads
+        the selection in force (staged at the previous trigger); the new one is
+        in force from the next step on. Other steps run the attention alone.
+        Before the first trigger no chunk is in force (window rows only).
+
+        Safe because a swapped layer keeps at least two selections' worth of
+        slots: the LRU then evicts only slots outside the selection in force,
+        whose slots are the most recently used (checked on the first call)."""
+        self._lookahead_setup(spec)
+        dev = self.keys.device
+        main = stream if stream is not None else torch.cuda.current_stream(dev)
+        cur, nxt = self.in_force, 1 - self.in_force
+        try:
+            if trigger:
+                self.side.wait_stream(main)
+                self.score(spec, self.side, fm_q)
+                abi.srh_set_chained(self.ctx, True)
+                self.select(spec, self.side)
+                abi.kvswap_stage(self.ctx, -1, self.sel, self.count, self.staging, self.phys2[nxt],
+                                 self.count_l2[nxt], self.side, None)
+                abi.srh_set_chained(self.ctx, False)
+            abi.lsa_attend(self.ctx, -1, self.q if q is None else q, self.H, self.window, self.staging,
+                           self.phys2[cur], self.count_l2[cur], self.out if out is None else out, main)
+            if trigger:
+                main.wait_stream(self.side)
+        finally:
+            abi.srh_set_chained(self.ctx, False)
+        if trigger:
+            self.in_force = nxt
+
+    def capture_lookahead(self, spec: StepSpec):
+        """CUDA graphs of the lookahead schedule: ``{(trigger, in_force): graph}``
+        for the four combinations (the buffers alternate). Replay with
+        ``replay_lookahead``. Capture after at least one eager step."""
+        self._lookahead_setup(spec)
+        dev = self.keys.device
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        keep = self.in_force
+        graphs = {}
+        for trig in (True, False):
+            for cur in (0, 1):
+                self.in_force = cur
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=s):
+                    self.lookahead_step(spec, trig, stream=s)
+                graphs[(trig, cur)] = g
+        self.in_force = keep
+        torch.cuda.current_stream(dev).wait_stream(s)
+        return graphs
+
+    def replay_lookahead(self, graphs, trigger: bool) -> None:
+        graphs[(bool(trigger), self.in_force)].replay()
+        if trigger:
+            self.in_force = 1 - self.in_force
+
     # ------------------------------------------------------------------ status
     def set_adaptive(self, policy=None) -> None:
         """Adaptive staging capacity (srh_set_adaptive); ``policy`` is a mapping
         of g_min, g_max, g_init, epoch, lo_permille, hi_permille, delta, or None."""
         abi.srh_set_adaptive(self.ctx, policy)
+        self._adaptive = dict(policy) if policy is not None else None
 
     def active_slots(self):
         """Slots in use per (layer, sequence) (srh_get_active_slots)."""

@@ -268,3 +268,86 @@ def test_max_sizes_select_and_stage():
     matched, worst = _run_decode(w, 3)
     assert matched == 3
     assert worst <= ATTN_TOL
+
+
+def _lookahead_run(w, steps, attend_layers, graph):
+    """The lookahead schedule on the GPU (eager or graph replays) beside the
+    oracle's; returns per-step outputs and the number of steps compared."""
+    ds = make_ds(w)
+    try:
+        pools = {(l, b): G.pool(w, l, b) for l in range(w.n_layers) for b in range(w.batch)}
+        keys = fill(ds, w, pools)
+        ora = make_oracle(w)
+        spec = spec_of(w)
+        rows_of = lambda l, b, idx: pools[(l, b)][np.asarray(idx, dtype=np.int64)]
+        graphs = None
+        outs, compared = [], 0
+        in_force_same = True           # the GPU's selection in force has the oracle's set
+        order_sync = True
+        for t in range(steps):
+            trig = t % w.lookahead == 0
+            load_step_inputs(ds, w, t)
+            if graph and graphs is None and t >= 1:
+                graphs = ds.capture_lookahead(spec)
+            if graphs is not None:
+                ds.replay_lookahead(graphs, trig)
+            else:
+                ds.lookahead_step(spec, trig)
+            torch.cuda.synchronize()
+            outs.append(ds.out.clone())
+            pairs = [(l, b) for l in attend_layers for b in range(w.batch)]
+            ref = ora.lookahead_step(lambda b: keys[b], lambda b: G.fm_queries(w, t, b),
+                                     lambda l, b: G.attn_q(w, t, l, b), lambda l, b: G.window(w, l, b),
+                                     rows_of, attend_pairs=pairs, trigger=trig)
+            if in_force_same:
+                out = ds.out.cpu().numpy()
+                for (l, b), r in ref.out.items():
+                    _, rel = attn_err(out[l, b], r)
+                    assert rel <= ATTN_TOL, (t, l, b, rel)
+                compared += 1
+            if trig:
+                scores = ds.scores.double().cpu().numpy()
+                sel = ds.sel.cpu().numpy()
+                cnt = ds.count.cpu().numpy()
+                same = True
+                for b in range(w.batch):
+                    same &= check_selection(w, ref.scores[b], ref.sel[b], sel[b, :cnt[b]], scores[b])
+                    order_sync &= np.array_equal(sel[b, :cnt[b]], ref.sel[b])
+                order_sync &= same
+                in_force_same = same
+                nxt = ds.in_force                 # the buffer the new selection was staged into
+                phys = ds.phys2[nxt].cpu().numpy()
+                cl = ds.count_l2[nxt].cpu().numpy()
+                for l in range(w.n_layers):
+                    for b in range(w.batch):
+                        if order_sync:
+                            assert cl[l, b] == len(ref.swap[l][b].phys)
+                            assert phys[l, b, :cl[l, b]].tolist() == ref.swap[l][b].phys, (t, l, b)
+        assert ds.check_error() == 0
+        return outs, compared
+    finally:
+        ds.close()
+
+
+def test_lookahead_schedule_matches_oracle():
+    """Lookahead schedule over the 8K stack: the step's attention reads the
+    selection in force while the new one is swapped in on a side stream; the
+    outputs and the new slots match the oracle's schedule, and graph replays
+    give the same bits as eager steps."""
+    w = C.CTX8K.with_(lookahead=4)
+    eager, n_cmp = _lookahead_run(w, 14, [0, 19, 20, 40], graph=False)
+    assert n_cmp >= 10
+    replay, _ = _lookahead_run(w, 14, [0, 40], graph=True)
+    for a, b in zip(eager, replay):
+        assert torch.equal(a, b)
+
+
+def test_lookahead_needs_two_selections_of_slots():
+    w = C.TINY                                     # GPU_CHUNKS = index_topk = 512
+    ds = make_ds(w)
+    try:
+        fill(ds, w)
+        with pytest.raises(ValueError):
+            ds.lookahead_step(spec_of(w), True)
+    finally:
+        ds.close()
