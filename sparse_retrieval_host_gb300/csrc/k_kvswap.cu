@@ -77,6 +77,32 @@ __device__ int block_scan_excl_array(int* a, int len, int* warp_buf, int* total_
     return total;
 }
 
+__device__ __forceinline__ void copy_row(float* __restrict__ dst, const float* __restrict__ src, int lane) {
+    const float4* s = reinterpret_cast<const float4*>(src);
+    float4* d = reinterpret_cast<float4*>(dst);
+    float4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = s[k * 32 + lane];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) d[k * 32 + lane] = v[k];
+}
+
+// Two rows per warp in flight: 16 float4 loads issued before the first store.
+__device__ __forceinline__ void copy_rows2(float* __restrict__ d0, const float* __restrict__ s0,
+                                           float* __restrict__ d1, const float* __restrict__ s1, int lane) {
+    const float4* a = reinterpret_cast<const float4*>(s0);
+    const float4* b = reinterpret_cast<const float4*>(s1);
+    float4 va[4], vb[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) va[k] = a[k * 32 + lane];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) vb[k] = b[k * 32 + lane];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) reinterpret_cast<float4*>(d0)[k * 32 + lane] = va[k];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) reinterpret_cast<float4*>(d1)[k * 32 + lane] = vb[k];
+}
+
 struct LruShared {
     int warp_buf[32];
     int total;
@@ -90,7 +116,7 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
            const int32_t* __restrict__ sel, const int32_t* __restrict__ count,
            int32_t* __restrict__ phys, int32_t* __restrict__ count_l, int2* __restrict__ miss,
            int* __restrict__ miss_count, unsigned long long* __restrict__ stats,
-           uint32_t* __restrict__ err, AdaptParams ap) {
+           uint32_t* __restrict__ err, AdaptParams ap, float* __restrict__ staging) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     LruShared& sh = *reinterpret_cast<LruShared*>(smem_raw);
     int* r = reinterpret_cast<int*>(smem_raw + sizeof(LruShared));  // [S] layer list
@@ -111,7 +137,6 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
     const int tid = threadIdx.x;
     const int l = l0 + blockIdx.x / B;
     const int b = blockIdx.x % B;
-    pdl_trigger();
     const LayerDev ld = layers[l];     // written once, at creation
     const long long cap = ld.cap;
     const size_t lb = (size_t)l * B + b;
@@ -361,8 +386,31 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
             const int c = r[p];
             slot_of[c] = s;
             slot_logical[s] = c;
-            miss_lb[mr[p]] = make_int2(c, s);
+            if (staging) tk[mr[p]] = p;            // compact list of the misses, in list order
+            else miss_lb[mr[p]] = make_int2(c, s);
             if (!ready[p]) atomicOr(err, kErrNotStored);
+        }
+    }
+    // The attention may launch now (its CTAs take the SMs this grid leaves
+    // free). Releasing it any earlier parks its CTAs for the whole resolve,
+    // which measured slower than this.
+    pdl_trigger();
+    if (staging) {
+        // ---- 5b. the miss gather, in this kernel: warp per pair of 2 KiB rows,
+        // zero-copy reads of the mapped pinned pool
+        __syncthreads();
+        const int warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+        float* stg = staging + lb * (size_t)G * kKvDim;
+        const float* pool = ld.pool + (size_t)b * cap * kKvDim;
+        for (int k = 2 * warp; k < nmiss; k += 2 * nw) {
+            const int p0 = tk[k];
+            if (k + 1 < nmiss) {
+                const int p1 = tk[k + 1];
+                copy_rows2(stg + (size_t)assign[p0] * kKvDim, pool + (size_t)r[p0] * kKvDim,
+                           stg + (size_t)assign[p1] * kKvDim, pool + (size_t)r[p1] * kKvDim, lane);
+            } else {
+                copy_row(stg + (size_t)assign[p0] * kKvDim, pool + (size_t)r[p0] * kKvDim, lane);
+            }
         }
     }
     if (tid == 0) {
@@ -398,15 +446,6 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
 
 constexpr int kGatherWarps = 8;
 
-__device__ __forceinline__ void copy_row(float* __restrict__ dst, const float* __restrict__ src, int lane) {
-    const float4* s = reinterpret_cast<const float4*>(src);
-    float4* d = reinterpret_cast<float4*>(dst);
-    float4 v[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) v[k] = s[k * 32 + lane];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) d[k * 32 + lane] = v[k];
-}
 
 __global__ void __launch_bounds__(kGatherWarps * 32)
 gather_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S,
@@ -499,8 +538,8 @@ size_t lru_smem_bytes(int S, int G) {
 cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int S, int src_ratio,
                        long long max_dedup_cap, const int32_t* sel, const int32_t* count,
                        int32_t* phys, int32_t* count_l, int2* miss, int* miss_count,
-                       unsigned long long* stats, uint32_t* err, AdaptParams ap, cudaStream_t st,
-                       bool chained) {
+                       unsigned long long* stats, uint32_t* err, AdaptParams ap, float* staging,
+                       cudaStream_t st, bool chained) {
     // a shared-memory table of first positions for layers whose ratio differs from
     // src_ratio, when it fits; otherwise those layers fall back to pairwise checks
     int tbl = 0;
@@ -514,7 +553,7 @@ cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int
         if (e != cudaSuccess) return e;
     }
     return launch_k(lru_kernel, dim3(nl * B), dim3(kLruThreads), smem, st, chained, layers, l0, B, G, S, src_ratio,
-                    tbl, sel, count, phys, count_l, miss, miss_count, stats, err, ap);
+                    tbl, sel, count, phys, count_l, miss, miss_count, stats, err, ap, staging);
 }
 
 cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, int S,

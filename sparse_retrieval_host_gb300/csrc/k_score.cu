@@ -186,9 +186,11 @@ __global__ void hist_kernel(const float* __restrict__ scores, int n, uint32_t* _
 
 cudaError_t launch_score(const uint16_t* keys, int n, int B, const uint16_t* q, float scale,
                          const float* bias3, int ensemble, float* scores, uint32_t* hist,
-                         int sm_count, cudaStream_t st, int key_sets) {
-    cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(uint32_t) * kHistBins * B, st);
-    if (e != cudaSuccess) return e;
+                         int sm_count, cudaStream_t st, int key_sets, bool clear_hist) {
+    if (clear_hist) {
+        const cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(uint32_t) * kHistBins * B, st);
+        if (e != cudaSuccess) return e;
+    }
     const long long tiles = (n + 15) / 16;
     long long bx = (tiles + kScoreWarps - 1) / kScoreWarps;
     const long long cap = (2LL * sm_count + B - 1) / B;
@@ -205,9 +207,11 @@ cudaError_t launch_score(const uint16_t* keys, int n, int B, const uint16_t* q, 
     return cudaGetLastError();
 }
 
-cudaError_t launch_hist(const float* scores, int n, int B, uint32_t* hist, cudaStream_t st) {
-    cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(uint32_t) * kHistBins * B, st);
-    if (e != cudaSuccess) return e;
+cudaError_t launch_hist(const float* scores, int n, int B, uint32_t* hist, cudaStream_t st, bool clear_hist) {
+    if (clear_hist) {
+        const cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(uint32_t) * kHistBins * B, st);
+        if (e != cudaSuccess) return e;
+    }
     long long bx = (n + 4095) / 4096;
     if (bx > 64) bx = 64;
     if (bx < 1) bx = 1;

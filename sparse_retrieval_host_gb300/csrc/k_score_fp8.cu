@@ -228,9 +228,11 @@ cudaError_t launch_quantize_keys(const uint16_t* keys, long long total, uint8_t*
 
 cudaError_t launch_score_fp8(const uint8_t* codes, const float* kscale, int n, int B, const uint16_t* q, float scale,
                              const float* bias3, int ensemble, float* scores, uint32_t* hist, int sm_count,
-                             cudaStream_t st) {
-    cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(uint32_t) * kHistBins * B, st);
-    if (e != cudaSuccess) return e;
+                             cudaStream_t st, bool clear_hist) {
+    if (clear_hist) {
+        const cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(uint32_t) * kHistBins * B, st);
+        if (e != cudaSuccess) return e;
+    }
     const long long tiles = (n + 15) / 16;
     long long bx = (tiles + kWarps - 1) / kWarps;
     const long long cap = (2LL * sm_count + B - 1) / B;

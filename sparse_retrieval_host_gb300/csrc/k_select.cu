@@ -40,6 +40,7 @@ constexpr int kCandCap = 8192;
 constexpr int kDigit = 12;
 constexpr int kArr = kCandCap + kMaxSelect;             // cand + outk, contiguous in shared memory
 constexpr long long kBucketWork = 256LL * kSelThreads;  // bound on sum of squared bucket sizes
+constexpr int kPre = 8;                                 // keys per thread held in registers
 constexpr int kCollectThreads = 256;
 constexpr int kCollectPer = 16;                         // scores per collect thread
 
@@ -135,6 +136,7 @@ struct SelShared {
     int n_cand;
     int found_digit;
     int found_above;
+    int hist_total;          // sum of the handed-in histogram row
     unsigned long long sq;   // sum of squared bucket sizes at or above the cut-off
 };
 
@@ -151,7 +153,7 @@ struct Src {
 
 __global__ void __launch_bounds__(kSelThreads)
 select_kernel(const float* __restrict__ scores, int n, int mode, int k, float thresh, int clamp,
-              int S, const uint32_t* __restrict__ hist_in, const unsigned long long* __restrict__ cand_in,
+              int S, uint32_t* __restrict__ hist_in, const unsigned long long* __restrict__ cand_in,
               const int* __restrict__ cand_cnt, int cand_cap, int32_t* __restrict__ sel,
               int32_t* __restrict__ count) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -165,6 +167,17 @@ select_kernel(const float* __restrict__ scores, int n, int mode, int k, float th
     pdl_trigger();
     pdl_wait();   // scores, histogram and candidates come from earlier kernels
 
+    // The handed-in first-digit histogram is read once and left zeroed, so the
+    // next scoring pass can add into it without clearing it first. Its loads
+    // and the first keys of every thread are issued together: one round trip.
+    constexpr int kHv = kHistBins / kSelThreads;
+    uint32_t* hb = hist_in ? hist_in + (size_t)b * kHistBins : nullptr;
+    uint32_t hv[kHv];
+    if (hb) {
+#pragma unroll
+        for (int k = 0; k < kHv; ++k) hv[k] = hb[tid + k * kSelThreads];
+    }
+
     // the key universe: a candidate list when one was made and did not overflow
     Src src{scores + (size_t)b * n, nullptr, n};
     if (cand_in) {
@@ -172,6 +185,26 @@ select_kernel(const float* __restrict__ scores, int n, int mode, int k, float th
         if (nc >= 0 && nc <= cand_cap) {
             src.cl = cand_in + (size_t)b * cand_cap;
             src.n = nc;
+        }
+    }
+    // keys tid + k * kSelThreads, k < kPre, stay in registers for every pass
+    unsigned long long pre[kPre];
+#pragma unroll
+    for (int k = 0; k < kPre; ++k) {
+        const int i = tid + k * kSelThreads;
+        pre[k] = i < src.n ? src.get(i) : 0ull;
+    }
+    auto each_key = [&](auto&& body) {
+#pragma unroll
+        for (int k = 0; k < kPre; ++k)
+            if (tid + k * kSelThreads < src.n) body(pre[k]);
+        for (int i = tid + kPre * kSelThreads; i < src.n; i += kSelThreads) body(src.get(i));
+    };
+    if (hb) {
+#pragma unroll
+        for (int k = 0; k < kHv; ++k) {
+            sh.hist[tid + k * kSelThreads] = hv[k];
+            hb[tid + k * kSelThreads] = 0u;
         }
     }
 
@@ -185,13 +218,12 @@ select_kernel(const float* __restrict__ scores, int n, int mode, int k, float th
     int K;
     if (mode == SRH_SELECT_THRESH) {
         const uint32_t kt = ordered_key(thresh);
-        for (int i = tid; i < src.n; i += kSelThreads) {
-            const unsigned long long c = src.get(i);
+        each_key([&](unsigned long long c) {
             if ((uint32_t)(c >> 32) > kt) {
                 const int pos = atomicAdd(&sh.n_cand, 1);
                 if (pos < kCandCap) cand[pos] = c;
             }
-        }
+        });
         __syncthreads();
         const int total = sh.n_cand;
         if (total <= clamp) {
@@ -230,15 +262,14 @@ select_kernel(const float* __restrict__ scores, int n, int mode, int k, float th
         const unsigned long long mask = (1ull << D) - 1ull;
         if (tid == 0) sh.found_digit = -1;
         if (pbits == 0 && use_hist_in) {
-            for (int i = tid; i < kHistBins; i += kSelThreads) sh.hist[i] = hist_in[(size_t)b * kHistBins + i];
+            // sh.hist holds the handed-in histogram (copied at the start)
         } else {
             for (int i = tid; i < kHistBins; i += kSelThreads) sh.hist[i] = 0;
             __syncthreads();
-            for (int i = tid; i < src.n; i += kSelThreads) {
-                const unsigned long long c = src.get(i);
+            each_key([&](unsigned long long c) {
                 if (pbits == 0 || (c >> (64 - pbits)) == (prefix >> (64 - pbits)))
                     atomicAdd(&sh.hist[(c >> shift) & mask], 1u);
-            }
+            });
         }
         __syncthreads();
         // thread tid owns bins 4095-4*tid .. 4092-4*tid (descending)
@@ -246,6 +277,7 @@ select_kernel(const float* __restrict__ scores, int n, int mode, int k, float th
 #pragma unroll
         for (int j = 0; j < 4; ++j) local += (int)sh.hist[kHistBins - 1 - 4 * tid - j];
         const int incl = block_inclusive_scan(local, sh.warp_buf);
+        if (tid == kSelThreads - 1) sh.hist_total = incl;
         int cum = incl - local;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -260,8 +292,9 @@ select_kernel(const float* __restrict__ scores, int n, int mode, int k, float th
         }
         __syncthreads();
         const int digit = sh.found_digit;
-        if (digit < 0) {
-            // the histogram handed in does not describe these scores: rebuild it
+        if (digit < 0 || (pbits == 0 && use_hist_in && sh.hist_total != n)) {
+            // the histogram handed in does not describe these scores (a count
+            // that is not n means it was not cleared or not filled): rebuild it
             if (pbits == 0 && use_hist_in) {
                 use_hist_in = false;
                 __syncthreads();
@@ -294,14 +327,13 @@ select_kernel(const float* __restrict__ scores, int n, int mode, int k, float th
         const int total = (K - remaining) + (int)sh.hist[digit];
         if (sh.sq <= (unsigned long long)kBucketWork && total <= kArr) {
             unsigned long long* arr = cand;               // cand and outk: kArr entries
-            for (int i = tid; i < src.n; i += kSelThreads) {
-                const unsigned long long c = src.get(i);
+            each_key([&](unsigned long long c) {
                 const int bin = (int)(c >> (64 - kDigit));
                 if (bin >= digit) {
                     const int slot = atomicAdd(&sh.bbase[bin], 1);
                     if (slot < kArr) arr[slot] = c;
                 }
-            }
+            });
             __syncthreads();
             // bucket of digit d: [bbase[d] - hist[d], bbase[d]); keys in higher
             // buckets are larger, so a key's position is its bucket start plus
@@ -323,17 +355,16 @@ select_kernel(const float* __restrict__ scores, int n, int mode, int k, float th
     }
 
     // ---- collect: keys above the class go out directly, class members to cand
-    for (int i = tid; i < src.n; i += kSelThreads) {
-        const unsigned long long c = src.get(i);
-        const unsigned long long top = c >> (64 - pbits), pre = prefix >> (64 - pbits);
-        if (top > pre) {
+    each_key([&](unsigned long long c) {
+        const unsigned long long top = c >> (64 - pbits), cls = prefix >> (64 - pbits);
+        if (top > cls) {
             const int pos = atomicAdd(&sh.n_out, 1);
             if (pos < K) outk[pos] = c;
-        } else if (top == pre) {
+        } else if (top == cls) {
             const int pos = atomicAdd(&sh.n_cand, 1);
             if (pos < kCandCap) cand[pos] = c;
         }
-    }
+    });
     __syncthreads();
     // consistent inputs give n_above == K - remaining; the clamps keep a stale
     // histogram from writing outside the arrays
@@ -368,7 +399,7 @@ collect_kernel(const float* __restrict__ scores, int n, int mode, int K, float t
                const uint32_t* __restrict__ hist_in, unsigned long long* __restrict__ cand,
                int* __restrict__ cand_cnt, int cap) {
     __shared__ int warp_buf[32];
-    __shared__ int cut_s, base_s;
+    __shared__ int cut_s, base_s, total_s;
     pdl_trigger();
     pdl_wait();
     const int b = blockIdx.y, tid = threadIdx.x;
@@ -395,6 +426,7 @@ collect_kernel(const float* __restrict__ scores, int n, int mode, int K, float t
         }
         if (tid == 0) cut_s = 0;
         const int incl = block_inclusive_scan(local, warp_buf);
+        if (tid == kCollectThreads - 1) total_s = incl;
         int cum = incl - local;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -403,7 +435,9 @@ collect_kernel(const float* __restrict__ scores, int n, int mode, int K, float t
             cum += c;
         }
         __syncthreads();
-        cut = (uint32_t)cut_s;
+        // a histogram that does not count n keys is stale: keep every key, so
+        // the list overflows and the select kernel works on all the scores
+        cut = total_s == n ? (uint32_t)cut_s : 0u;
     }
     uint32_t keys[kCollectPer];
     unsigned pass = 0;
@@ -433,7 +467,7 @@ collect_kernel(const float* __restrict__ scores, int n, int mode, int K, float t
 }  // namespace
 
 cudaError_t launch_select(const float* scores, int n, int B, int mode, int k, float thresh,
-                          int clamp, int S, const uint32_t* hist, int32_t* sel, int32_t* count,
+                          int clamp, int S, uint32_t* hist, int32_t* sel, int32_t* count,
                           cudaStream_t st, const unsigned long long* cand, const int* cand_cnt, int cand_cap,
                           bool chained) {
     const size_t smem = sizeof(SelShared) + sizeof(unsigned long long) * kArr;

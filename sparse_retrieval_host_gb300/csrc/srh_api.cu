@@ -281,6 +281,7 @@ int srh_create(const srh_config* cfg, srh_ctx** out) {
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_err, sizeof(uint32_t));
     if (e == cudaSuccess) e = cudaMemset(ctx->d_err, 0, sizeof(uint32_t));
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_hist, sizeof(uint32_t) * kHistBins * B);
+    if (e == cudaSuccess) e = cudaMemset(ctx->d_hist, 0, sizeof(uint32_t) * kHistBins * B);
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_cand, sizeof(unsigned long long) * select_cand_cap() * B);
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_cand_cnt, sizeof(int) * B);
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_miss, sizeof(int2) * (size_t)ctx->L * B * ctx->S);
@@ -376,8 +377,9 @@ int score_impl(srh_ctx* ctx, const uint16_t* d_keys, int key_sets, int n, const 
     if (((uintptr_t)d_keys | (uintptr_t)d_q) & 15) return fail(ctx, SRH_ERR_INVALID, "keys/queries must be 16-byte aligned");
     if (!std::isfinite(scale)) return fail(ctx, SRH_ERR_INVALID, "scale must be finite");
     const cudaError_t e = launch_score(d_keys, n, ctx->B, d_q, scale, bias3, ensemble, d_scores, ctx->d_hist,
-                                       ctx->sm_count, (cudaStream_t)stream, key_sets);
+                                       ctx->sm_count, (cudaStream_t)stream, key_sets, !ctx->hist_clean);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "fm_score launch");
+    ctx->hist_clean = false;
     ctx->hist_scores = d_scores;
     ctx->hist_n = n;
     return SRH_OK;
@@ -418,8 +420,9 @@ int fm_score_fp8(srh_ctx* ctx, const uint8_t* d_codes, const float* d_kscale, in
     if (((uintptr_t)d_kscale) & 3) return fail(ctx, SRH_ERR_INVALID, "scales must be 4-byte aligned");
     if (!std::isfinite(scale)) return fail(ctx, SRH_ERR_INVALID, "scale must be finite");
     const cudaError_t e = launch_score_fp8(d_codes, d_kscale, n, ctx->B, d_q, scale, bias3, ensemble, d_scores,
-                                           ctx->d_hist, ctx->sm_count, (cudaStream_t)stream);
+                                           ctx->d_hist, ctx->sm_count, (cudaStream_t)stream, !ctx->hist_clean);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "fm_score_fp8 launch");
+    ctx->hist_clean = false;
     ctx->hist_scores = d_scores;
     ctx->hist_n = n;
     return SRH_OK;
@@ -442,13 +445,14 @@ int fm_select(srh_ctx* ctx, const float* d_scores, int n, int mode, int k, float
         return fail(ctx, SRH_ERR_INVALID, "unknown selection mode");
     }
     cudaStream_t st = (cudaStream_t)stream;
-    const uint32_t* hist = nullptr;
+    uint32_t* hist = nullptr;
     bool chained = ctx->chained;   // the select kernel follows a kernel of this call or of fm_score
     if (mode == SRH_SELECT_TOPK || clamp > 0) {
         if (ctx->hist_scores == d_scores && ctx->hist_n == n) {
             hist = ctx->d_hist;
         } else {
-            const cudaError_t e = launch_hist(d_scores, n, ctx->B, ctx->d_hist, st);
+            const cudaError_t e = launch_hist(d_scores, n, ctx->B, ctx->d_hist, st, !ctx->hist_clean);
+            ctx->hist_clean = false;
             if (e != cudaSuccess) return cuda_fail(ctx, e, "fm_select histogram");
             hist = ctx->d_hist;
             chained = true;
@@ -468,6 +472,7 @@ int fm_select(srh_ctx* ctx, const float* d_scores, int n, int mode, int k, float
     const cudaError_t e = launch_select(d_scores, n, ctx->B, mode, k, thresh, clamp, ctx->S, hist, d_sel,
                                         d_count, st, cand, ctx->d_cand_cnt, select_cand_cap(), chained);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "fm_select launch");
+    if (hist) ctx->hist_clean = true;   // the select kernel zeroes the rows it reads
     return SRH_OK;
 }
 
@@ -498,21 +503,19 @@ int kvswap_stage(srh_ctx* ctx, int layer, const int32_t* d_sel, const int32_t* d
     long long dedup_cap = 0;
     for (int l = l0; l < l0 + nl; ++l)
         if (ctx->ratios[l] != ctx->cfg.src_ratio) dedup_cap = std::max(dedup_cap, ctx->caps[l]);
+    // one stream: the resolve kernel gathers its own misses; with a side stream
+    // the gather is a kernel of its own there, joined back by an event
+    const bool split = ss && ss != sm;
     cudaError_t e = launch_lru(ctx->d_layers, l0, nl, ctx->B, ctx->G, ctx->S, ctx->cfg.src_ratio, dedup_cap,
                                d_sel, d_count, d_phys, d_count_l, ctx->d_miss, ctx->d_miss_count, ctx->d_stats,
-                               ctx->d_err, ctx->adapt, sm, ctx->chained);
+                               ctx->d_err, ctx->adapt, split ? nullptr : d_staging, sm, ctx->chained);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "kvswap_stage LRU launch");
-    if (ss && ss != sm) {
+    if (split) {
         SRH_CUDA(ctx, cudaEventRecord(ctx->ev_resolved, sm));
         SRH_CUDA(ctx, cudaStreamWaitEvent(ss, ctx->ev_resolved, 0));
-    } else {
-        ss = sm;
-    }
-    // on the main stream the gather directly follows the resolve kernel: chained
-    e = launch_gather(ctx->d_layers, l0, nl, ctx->B, ctx->G, ctx->S, ctx->d_miss, ctx->d_miss_count, d_staging,
-                      ctx->d_err, ctx->sm_count, ss, ss == sm);
-    if (e != cudaSuccess) return cuda_fail(ctx, e, "kvswap_stage gather launch");
-    if (ss != sm) {
+        e = launch_gather(ctx->d_layers, l0, nl, ctx->B, ctx->G, ctx->S, ctx->d_miss, ctx->d_miss_count,
+                          d_staging, ctx->d_err, ctx->sm_count, ss, false);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "kvswap_stage gather launch");
         SRH_CUDA(ctx, cudaEventRecord(ctx->ev_gathered, ss));
         SRH_CUDA(ctx, cudaStreamWaitEvent(sm, ctx->ev_gathered, 0));
     }

@@ -140,6 +140,7 @@ struct Ctx {
     bool chained = false;               // srh_set_chained: step kernels may launch early
     AdaptParams adapt{};                // srh_set_adaptive
     uint32_t* d_hist = nullptr;         // [B][kHistBins]
+    bool hist_clean = true;             // d_hist is all zeros (cleared, or consumed by a selection)
     unsigned long long* d_cand = nullptr; // [B][select_cand_cap()] candidate composites
     int* d_cand_cnt = nullptr;          // [B]
     const float* hist_scores = nullptr; // the d_scores the histogram describes
@@ -178,15 +179,18 @@ __device__ __forceinline__ uint32_t ordered_key(float s) {
 #endif
 
 // ---------------------------------------------------------------- launchers
+// The scoring launchers add into the first-digit histogram `hist`; with
+// `clear_hist` they zero it first (the select kernel leaves the rows it reads
+// zeroed, so a histogram consumed by a selection needs no clearing).
 cudaError_t launch_score(const uint16_t* keys, int n, int B, const uint16_t* q, float scale,
                          const float* bias3, int ensemble, float* scores, uint32_t* hist,
-                         int sm_count, cudaStream_t st, int key_sets = 1);
-cudaError_t launch_hist(const float* scores, int n, int B, uint32_t* hist, cudaStream_t st);
+                         int sm_count, cudaStream_t st, int key_sets, bool clear_hist);
+cudaError_t launch_hist(const float* scores, int n, int B, uint32_t* hist, cudaStream_t st, bool clear_hist);
 cudaError_t launch_quantize_keys(const uint16_t* keys, long long total, uint8_t* codes, float* kscale,
                                  int sm_count, cudaStream_t st);
 cudaError_t launch_score_fp8(const uint8_t* codes, const float* kscale, int n, int B, const uint16_t* q, float scale,
                              const float* bias3, int ensemble, float* scores, uint32_t* hist, int sm_count,
-                             cudaStream_t st);
+                             cudaStream_t st, bool clear_hist);
 // Candidate pass for large n: zeroes cand_cnt, then appends the selectable keys.
 cudaError_t launch_collect(const float* scores, int n, int B, int mode, int K, float thresh,
                            const uint32_t* hist, unsigned long long* cand, int* cand_cnt, int cap,
@@ -194,14 +198,16 @@ cudaError_t launch_collect(const float* scores, int n, int B, int mode, int K, f
 int select_cand_cap();
 constexpr int kCollectMinN = 16384;    // fm_select runs the candidate pass above this n
 cudaError_t launch_select(const float* scores, int n, int B, int mode, int k, float thresh,
-                          int clamp, int S, const uint32_t* hist, int32_t* sel, int32_t* count,
+                          int clamp, int S, uint32_t* hist, int32_t* sel, int32_t* count,
                           cudaStream_t st, const unsigned long long* cand = nullptr,
                           const int* cand_cnt = nullptr, int cand_cap = 0, bool chained = false);
+// With staging != nullptr the resolve kernel also copies its misses into the
+// staging rows (no separate gather kernel); otherwise it writes the miss lists.
 cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int S, int src_ratio,
                        long long max_dedup_cap, const int32_t* sel, const int32_t* count,
                        int32_t* phys, int32_t* count_l, int2* miss, int* miss_count,
-                       unsigned long long* stats, uint32_t* err, AdaptParams ap, cudaStream_t st,
-                       bool chained);
+                       unsigned long long* stats, uint32_t* err, AdaptParams ap, float* staging,
+                       cudaStream_t st, bool chained);
 cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, int S,
                           const int2* miss, const int* miss_count, float* staging,
                           uint32_t* err, int sm_count, cudaStream_t st, bool chained);

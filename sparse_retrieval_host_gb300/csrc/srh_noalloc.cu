@@ -108,10 +108,10 @@ extern "C" int fm_select_noalloc(const float* d_scores, int batch, int n, int mo
     if (!hist) return code;
 
     cudaStream_t st = (cudaStream_t)stream;
-    const uint32_t* hist_in = nullptr;
+    uint32_t* hist_in = nullptr;
     if (mode == SRH_SELECT_TOPK || clamp > 0) {
         // launch_hist zeroes the batch rows of the scratch on `st`, then fills them.
-        const cudaError_t e = srh::launch_hist(d_scores, n, batch, hist, st);
+        const cudaError_t e = srh::launch_hist(d_scores, n, batch, hist, st, true);
         if (e != cudaSuccess)
             return report(err, err_len, SRH_ERR_CUDA, "fm_select_noalloc histogram: %s", cudaGetErrorString(e));
         hist_in = hist;

@@ -351,3 +351,37 @@ def test_lookahead_needs_two_selections_of_slots():
             ds.lookahead_step(spec_of(w), True)
     finally:
         ds.close()
+
+
+@pytest.mark.parametrize("ctx_len", [8192, 4 * 32768], ids=["n2048", "n32768_candidates"])
+def test_replay_after_unconsumed_scoring_selects_right(ctx_len):
+    """A graph captured while the score histogram was clean has no clearing
+    step. If an eager scoring pass that no selection consumed runs before the
+    replay, the replay's histogram counts keys twice; the select kernel (and
+    the candidate pass) must notice and rebuild rather than select wrongly."""
+    from sparse_retrieval_host_gb300 import abi
+    w = C.TINY.with_(context_len=ctx_len)
+    ds = make_ds(w)
+    try:
+        fill(ds, w)
+        spec = spec_of(w)
+        load_step_inputs(ds, w, 0)
+        ds.step(spec)
+        (g,) = ds.capture(spec)
+        load_step_inputs(ds, w, 9)
+        ds.score(spec)                      # scored, never selected
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        sel, cnt = ds.sel.clone(), ds.count.clone()
+        ref_sel = torch.zeros_like(ds.sel)
+        ref_cnt = torch.zeros_like(ds.count)
+        abi.fm_select_noalloc(ds.scores, w.batch, ds.n, spec.select_mode, spec.k, spec.tau, spec.clamp, ds.S,
+                              ref_sel, ref_cnt)
+        torch.cuda.synchronize()
+        assert torch.equal(cnt, ref_cnt)
+        for b in range(w.batch):
+            assert torch.equal(sel[b, :cnt[b]], ref_sel[b, :cnt[b]])
+        assert ds.check_error() == 0
+    finally:
+        ds.close()
