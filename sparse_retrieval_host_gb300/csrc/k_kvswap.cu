@@ -140,24 +140,52 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
     const LayerDev ld = layers[l];     // written once, at creation
     const long long cap = ld.cap;
     const size_t lb = (size_t)l * B + b;
+    const int32_t* sel_b = sel + (size_t)b * S;
+    int* lru = ld.swap ? ld.lru_order + (size_t)b * G : nullptr;   // swap layers only
+    AdaptState* as = ld.swap ? ld.adapt + b : nullptr;
     pdl_wait();                        // the selection comes from earlier kernels
 
-    // ---- 1. the layer's ordered chunk list: c -> floor(c * src_ratio / ratio), first kept
+    // One round of independent loads: the count, the whole selection row
+    // (entries past the count are ignored) and, for a swapped layer, its
+    // capacity state and LRU order. Thread t holds entries t + k * 1024.
+    constexpr int kPer = kMaxGpuChunks / kLruThreads;
+    static_assert(kMaxSelect <= kMaxGpuChunks, "selection entries per thread");
+    int selv[kPer], lruv[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int p = tid + k * kLruThreads;
+        selv[k] = p < S ? sel_b[p] : 0;
+    }
+    int g0 = G, g = G;
+    if (ld.swap) {
+        g0 = as->g;
+        g = as->g_next;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int q = tid + k * kLruThreads;
+            lruv[k] = q < G ? lru[q] : 0;
+        }
+    }
     int m0 = count[b];
+
+    // ---- 1. the layer's ordered chunk list: c -> floor(c * src_ratio / ratio), first kept
     if (m0 < 0 || m0 > S) {
         if (tid == 0) atomicOr(err, kErrBounds);
         m0 = m0 < 0 ? 0 : S;
     }
-    const int32_t* sel_b = sel + (size_t)b * S;
-    for (int p = tid; p < m0; p += blockDim.x) {
-        long long c = sel_b[p];
-        long long v = (c * src_ratio) / ld.ratio;
-        if (c < 0 || v >= cap) {
-            // out-of-range id: flagged, then clamped so every access stays in bounds
-            atomicOr(err, kErrBounds);
-            v = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int p = tid + k * kLruThreads;
+        if (p < m0) {
+            const long long c = selv[k];
+            long long v = (c * src_ratio) / ld.ratio;
+            if (c < 0 || v >= cap) {
+                // out-of-range id: flagged, then clamped so every access stays in bounds
+                atomicOr(err, kErrBounds);
+                v = 0;
+            }
+            r[p] = (int)v;
         }
-        r[p] = (int)v;
     }
     __syncthreads();
     int m;
@@ -213,12 +241,9 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
 
     int* slot_of = ld.slot_of + (size_t)b * cap;
     int* slot_logical = ld.slot_logical + (size_t)b * G;
-    int* lru = ld.lru_order + (size_t)b * G;
-    AdaptState* as = ld.adapt + b;
 
     // ---- 2a. slots in use: the last step's range g0, resized to g when the
     // hit-rate policy (or the host) asked for it. No staged row moves.
-    int g0 = as->g, g = as->g_next;
     if (g0 < 1 || g0 > G || g < 1 || g > G) {
         if (tid == 0) atomicOr(err, kErrBounds);
         g0 = (g0 < 1 || g0 > G) ? G : g0;
@@ -234,25 +259,33 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
             slot_logical[s] = -1;
             queue[q] = s;
         }
-        for (int q = tid; q < g0; q += blockDim.x) {
-            int s = lru[q];
-            if (s < 0 || s >= g0) {
-                atomicOr(err, kErrBounds);
-                s = q;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int q = tid + k * kLruThreads;
+            if (q < g0) {
+                int s = lruv[k];
+                if (s < 0 || s >= g0) {
+                    atomicOr(err, kErrBounds);
+                    s = q;
+                }
+                queue[add + q] = s;
             }
-            queue[add + q] = s;
         }
         __syncthreads();
     } else if (g < g0) {
         // keep the slots below g in their order; the others forget their chunks
-        for (int q = tid; q < g0; q += blockDim.x) {
-            int s = lru[q];
-            if (s < 0 || s >= g0) {
-                atomicOr(err, kErrBounds);
-                s = q;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int q = tid + k * kLruThreads;
+            if (q < g0) {
+                int s = lruv[k];
+                if (s < 0 || s >= g0) {
+                    atomicOr(err, kErrBounds);
+                    s = q;
+                }
+                victim[q] = s;
+                nh[q] = s < g ? 1 : 0;
             }
-            victim[q] = s;
-            nh[q] = s < g ? 1 : 0;
         }
         __syncthreads();
         block_scan_excl_array(nh, g0, sh.warp_buf, &sh.total);
@@ -268,13 +301,17 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
         }
         __syncthreads();
     } else {
-        for (int q = tid; q < g; q += blockDim.x) {
-            int s = lru[q];
-            if (s < 0 || s >= g) {
-                atomicOr(err, kErrBounds);
-                s = q;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int q = tid + k * kLruThreads;
+            if (q < g) {
+                int s = lruv[k];
+                if (s < 0 || s >= g) {
+                    atomicOr(err, kErrBounds);
+                    s = q;
+                }
+                queue[q] = s;
             }
-            queue[q] = s;
         }
     }
     // a swapped layer stages at most g chunks per step (reachable with
