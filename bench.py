@@ -197,12 +197,24 @@ def attn_bytes(w, count_l):
 
 
 def launches_per_step(w, sm_count):
-    """Our kernels per step. lsa_attend adds its merge kernel when some layer's
-    rows are cut into more than one split; the split rule is the planner's
-    (split rows = rows of all layers / SM count, rounded up to 128)."""
-    rows = [C.WINDOW + min(w.clamp, -(-w.context_len // r)) for r in w.layer_ratios]
-    split = max(128, -(-(-(-w.batch * sum(rows) // sm_count)) // 128) * 128)
-    merge = 1 if any(-(-r // split) > 1 for r in rows) else 0
+    """Our kernels per step. lsa_attend adds its merge kernel when its plan
+    spreads some (layer, sequence) over more than one CTA. The rule is the
+    planner's: T tiles of 128 rows (window + min(clamp, cap) rows per pair);
+    pairs cut into chunks of ceil(T / SMs) tiles when that fits one wave, else
+    contiguous tile ranges over min(SMs, T) CTAs."""
+    tiles = [-(-(C.WINDOW + min(w.clamp, -(-w.context_len // r))) // 128) for r in w.layer_ratios] * w.batch
+    T = sum(tiles)
+    m = -(-T // sm_count)
+    if sum(-(-t // m) for t in tiles) <= sm_count:
+        merge = 1 if any(t > m for t in tiles) else 0
+    else:
+        n = min(sm_count, T)
+        bounds = {k * T // n for k in range(1, n)}
+        starts, acc = [], 0
+        for t in tiles:
+            starts.append((acc, acc + t))
+            acc += t
+        merge = 1 if any(any(a < x < b for x in bounds) for a, b in starts) else 0
     collect = 1 if w.n_chunks > COLLECT_MIN_N else 0      # fm_select's candidate pass
     return BASE_KERNELS + merge + collect
 

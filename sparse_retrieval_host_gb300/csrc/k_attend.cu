@@ -84,9 +84,8 @@ __host__ __device__ constexpr uint32_t idesc_f16(int a_mn, int b_mn, int n) {
 }
 
 struct AttnArgs {
-    const AttnItem* items;
-    int item0;
-    int split_rows;
+    const AttnSeg* segs;
+    const int* cta_begin;   // CTA k runs segs[cta_begin[k] .. cta_begin[k + 1])
     int B, G, S;
     const uint16_t* q;
     const float* window;
@@ -175,9 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     volatile int* abort = &ms.abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    const int item_idx = a.item0 + blockIdx.x;
-    const AttnItem it = a.items[item_idx];       // the work plan: written once, at creation
-    const size_t lb = (size_t)it.layer * a.B + it.seq;
+    // this CTA's segments of the static plan (written once, at creation)
+    const int sb = a.cta_begin[blockIdx.x], se = a.cta_begin[blockIdx.x + 1];
     pdl_trigger();
 
     // ---------------------------------------------------------------- set-up
@@ -199,10 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         ms.alpha[tid] = 1.f;
     }
     if (warp == 0) tmem_alloc(&ms.tmem_base, kTmemCols);
-    {
-        // queries: bf16 [H][512] -> fp16 K-major; d-block d / 64 at (d / 64) * 8192, row h
+    // queries of (layer, sequence) lb: bf16 [H][512] -> fp16 K-major; d-block d / 64
+    // at (d / 64) * 8192, row h
+    auto convert_q = [&](int lbq) {
         constexpr int kPer = H * 64 / kThreads;          // 16-byte chunks per thread
-        const uint16_t* qg = a.q + lb * H * kKvDim;
+        const uint16_t* qg = a.q + (size_t)lbq * H * kKvDim;
         uint4 qv[kPer];
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
@@ -220,7 +219,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
             w.w = pack_f16x2(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
             *reinterpret_cast<uint4*>(sm + kOffQ + (c8 >> 3) * 8192 + sw128(h, c8 & 7)) = w;
         }
-    }
+    };
+    int q_lb = sb < se ? a.segs[sb].lb : 0;
+    if (sb < se) convert_q(q_lb);
+    // the barriers, the abort flag, the softmax state and the TMEM address are
+    // set: every thread sees them from here on
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
 
     // ... as fp16 into E: d-block (lane >> 4) + 2 j, 16-byte chunk (lane & 15) >> 1, half lane & 1.
     auto store4 = [&](const float4 (&v)[4][4], int rbase) {
@@ -240,14 +246,35 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     bool ok = true;
 
     pdl_wait();   // slots, counts and staged rows come from earlier kernels
+
+    uint32_t gt0 = 0;     // tiles this CTA ran before the current segment (mbarrier phases)
+    uint32_t n_drain = 0; // drains this CTA ran (phases of ms.drain)
+    for (int si = sb; si < se && !*abort; ++si) {
+    const AttnSeg sg = a.segs[si];
+    const size_t lb = (size_t)sg.lb;
+    if (si > sb) {
+        // a new segment: the previous one drained its MMAs and wrote its
+        // epilogue; reset the running softmax and, for a new pair, load its queries
+        if (sg.lb != q_lb) {
+            convert_q(sg.lb);
+            q_lb = sg.lb;
+        }
+        if (tid < 64) {
+            ms.m_used[tid] = -INFINITY;
+            ms.l_run[tid] = 0.f;
+            ms.alpha[tid] = 1.f;
+        }
+        if (tid == 0) ms.rescale = 0;
+        __syncthreads();
+    }
     int cnt = a.count_l[lb];
     if (cnt < 0 || cnt > a.S) {
         if (tid == 0) atomicOr(a.err, kErrBounds);
         cnt = cnt < 0 ? 0 : a.S;
     }
     const int R = kWindow + cnt;
-    const int row0 = it.split * a.split_rows;
-    const int row1 = min(R, row0 + a.split_rows);
+    const int row0 = sg.tile0 * kTileRows;
+    const int row1 = min(R, sg.tile1 * kTileRows);
     const int n_tiles = row1 > row0 ? (row1 - row0 + kTileRows - 1) / kTileRows : 0;
     const int32_t* ph = a.phys + lb * a.S;
 
@@ -282,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
             load4(b0, tr0, rw);
             load4(b1, tr0, rw + 4);
             // the previous tile's pass 2 reads E: wait for it before overwriting
-            if (tile > 0 && !wait_or_abort(&ms.o_full, (tile - 1) & 1, abort, a.err)) ok = false;
+            if (tile > 0 && !wait_or_abort(&ms.o_full, (gt0 + tile - 1) & 1, abort, a.err)) ok = false;
         }
         if (ok) {
             store4(b0, rw);
@@ -317,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         // ------------------------------------------------------------ softmax (warps 0-3)
         const int r = tid;                                // tile row = TMEM lane
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        const bool got = wait_or_abort(&ms.s_full, tile & 1, abort, a.err);
+        const bool got = wait_or_abort(&ms.s_full, (gt0 + tile) & 1, abort, a.err);
         if (named_sync_or(1, kSoftThreads, !got)) {
             ok = false;
             *abort = 1;
@@ -425,11 +452,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     if (tid == 0 && n_tiles > 0) {
         // completes once every MMA issued above has completed
         mma_commit(&ms.drain);
-        if (!mbar_wait(&ms.drain, 0, 1u << 26)) {
+        if (!mbar_wait(&ms.drain, n_drain & 1, 1u << 26)) {
             atomicOr(a.err, kErrTimeout);
             ok = false;
         }
     }
+    if (n_tiles > 0) ++n_drain;
+    gt0 += (uint32_t)n_tiles;
     tc_fence_before();
     const bool failed = __syncthreads_or(!ok);
     tc_fence_after();
@@ -438,8 +467,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     __syncthreads();
 
     // ---------------------------------------------------------------- epilogue: all 8 warps
-    const bool single = it.n_splits == 1;
-    float* dst = single ? a.out + lb * H * kKvDim : a.part_o + (size_t)item_idx * H * kKvDim;
+    const bool single = sg.slot < 0;
+    float* dst = single ? a.out + lb * H * kKvDim : a.part_o + (size_t)sg.slot * H * kKvDim;
     if (n_tiles > 0 && ms.epi_ok) {
         const uint32_t tmem = ms.tmem_base;
         // warp w reads TMEM lanes 32 (w & 3).. of d-blocks 2 (w >> 2) and 2 (w >> 2) + 1
@@ -465,10 +494,17 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         for (int i = tid; i < H * kKvDim; i += kThreads) __stcg(&dst[i], 0.f);
     }
     if (!single && tid < H) {
-        float* pml = a.part_ml + (size_t)item_idx * 2 * H;
+        float* pml = a.part_ml + (size_t)sg.slot * 2 * H;
         __stcg(&pml[tid], ms.m_used[tid]);
         __stcg(&pml[H + tid], n_tiles > 0 && ms.epi_ok ? ms.l_run[tid] : 0.f);
     }
+    // the next segment overwrites O, S, E, P and the softmax state: every
+    // thread is done with this one's TMEM reads and shared values first
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (!ms.epi_ok && n_tiles > 0) *abort = 1;
+    }   // segments
 
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
@@ -538,7 +574,7 @@ __global__ void __launch_bounds__(kKvDim / 4) merge_kernel(const MergeItem* __re
 }
 
 template <int H>
-cudaError_t launch_h(const AttnArgs& args, int n_items, const MergeItem* merges, int merge0, int n_merges,
+cudaError_t launch_h(const AttnArgs& args, int n_ctas, const MergeItem* merges, int n_merges,
                      cudaStream_t st, bool chained) {
     static bool attr_set = false;
     if (!attr_set) {
@@ -547,10 +583,10 @@ cudaError_t launch_h(const AttnArgs& args, int n_items, const MergeItem* merges,
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    cudaError_t e = launch_k(attend_tc_kernel<H>, dim3(n_items), dim3(kThreads), kSmemBytes, st, chained, args);
+    cudaError_t e = launch_k(attend_tc_kernel<H>, dim3(n_ctas), dim3(kThreads), kSmemBytes, st, chained, args);
     if (e != cudaSuccess || n_merges <= 0) return e;
     // the merge follows its own attention kernel: always chained
-    return launch_k(merge_kernel<H>, dim3((unsigned)n_merges, H), dim3(kKvDim / 4), 0, st, true, merges, merge0,
+    return launch_k(merge_kernel<H>, dim3((unsigned)n_merges, H), dim3(kKvDim / 4), 0, st, true, merges, 0,
                     (const float*)args.part_o, (const float*)args.part_ml, args.out);
 }
 
@@ -558,19 +594,17 @@ cudaError_t launch_h(const AttnArgs& args, int n_items, const MergeItem* merges,
 
 int attend_max_splits() { return kMaxSplits; }
 
-cudaError_t launch_attend(const AttnItem* items, int item0, int n_items, const MergeItem* merges, int merge0,
-                          int n_merges, int split_rows, int n_heads, int B, int G, int S, const uint16_t* q,
-                          const float* window, const float* staging, const int32_t* phys,
-                          const int32_t* count_l, float* out, float* part_o, float* part_ml, uint32_t* err,
-                          cudaStream_t st, bool chained) {
-    if (n_items <= 0) return cudaSuccess;
-    if (split_rows % kTileRows != 0) return cudaErrorInvalidValue;
-    AttnArgs args{items, item0, split_rows, B, G, S, q, window, staging, phys, count_l,
+cudaError_t launch_attend(const AttnSeg* segs, const int* cta_begin, int n_ctas, const MergeItem* merges,
+                          int n_merges, int n_heads, int B, int G, int S, const uint16_t* q, const float* window,
+                          const float* staging, const int32_t* phys, const int32_t* count_l, float* out,
+                          float* part_o, float* part_ml, uint32_t* err, cudaStream_t st, bool chained) {
+    if (n_ctas <= 0) return cudaSuccess;
+    AttnArgs args{segs, cta_begin, B, G, S, q, window, staging, phys, count_l,
                   out, part_o, part_ml, err, (float)(1.4426950408889634 / std::sqrt((double)kKvDim))};
     switch (n_heads) {
-        case 16: return launch_h<16>(args, n_items, merges, merge0, n_merges, st, chained);
-        case 32: return launch_h<32>(args, n_items, merges, merge0, n_merges, st, chained);
-        case 64: return launch_h<64>(args, n_items, merges, merge0, n_merges, st, chained);
+        case 16: return launch_h<16>(args, n_ctas, merges, n_merges, st, chained);
+        case 32: return launch_h<32>(args, n_ctas, merges, n_merges, st, chained);
+        case 64: return launch_h<64>(args, n_ctas, merges, n_merges, st, chained);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -87,22 +87,6 @@ __device__ __forceinline__ void copy_row(float* __restrict__ dst, const float* _
     for (int k = 0; k < 4; ++k) d[k * 32 + lane] = v[k];
 }
 
-// Two rows per warp in flight: 16 float4 loads issued before the first store.
-__device__ __forceinline__ void copy_rows2(float* __restrict__ d0, const float* __restrict__ s0,
-                                           float* __restrict__ d1, const float* __restrict__ s1, int lane) {
-    const float4* a = reinterpret_cast<const float4*>(s0);
-    const float4* b = reinterpret_cast<const float4*>(s1);
-    float4 va[4], vb[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) va[k] = a[k * 32 + lane];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) vb[k] = b[k * 32 + lane];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) reinterpret_cast<float4*>(d0)[k * 32 + lane] = va[k];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) reinterpret_cast<float4*>(d1)[k * 32 + lane] = vb[k];
-}
-
 struct LruShared {
     int warp_buf[32];
     int total;
@@ -116,7 +100,7 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
            const int32_t* __restrict__ sel, const int32_t* __restrict__ count,
            int32_t* __restrict__ phys, int32_t* __restrict__ count_l, int2* __restrict__ miss,
            int* __restrict__ miss_count, unsigned long long* __restrict__ stats,
-           uint32_t* __restrict__ err, AdaptParams ap, float* __restrict__ staging) {
+           uint32_t* __restrict__ err, AdaptParams ap) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     LruShared& sh = *reinterpret_cast<LruShared*>(smem_raw);
     int* r = reinterpret_cast<int*>(smem_raw + sizeof(LruShared));  // [S] layer list
@@ -143,6 +127,7 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
     const int32_t* sel_b = sel + (size_t)b * S;
     int* lru = ld.swap ? ld.lru_order + (size_t)b * G : nullptr;   // swap layers only
     AdaptState* as = ld.swap ? ld.adapt + b : nullptr;
+    pdl_trigger();                     // the gather kernel may launch (it waits for this one)
     pdl_wait();                        // the selection comes from earlier kernels
 
     // One round of independent loads: the count, the whole selection row
@@ -423,31 +408,8 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
             const int c = r[p];
             slot_of[c] = s;
             slot_logical[s] = c;
-            if (staging) tk[mr[p]] = p;            // compact list of the misses, in list order
-            else miss_lb[mr[p]] = make_int2(c, s);
+            miss_lb[mr[p]] = make_int2(c, s);
             if (!ready[p]) atomicOr(err, kErrNotStored);
-        }
-    }
-    // The attention may launch now (its CTAs take the SMs this grid leaves
-    // free). Releasing it any earlier parks its CTAs for the whole resolve,
-    // which measured slower than this.
-    pdl_trigger();
-    if (staging) {
-        // ---- 5b. the miss gather, in this kernel: warp per pair of 2 KiB rows,
-        // zero-copy reads of the mapped pinned pool
-        __syncthreads();
-        const int warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
-        float* stg = staging + lb * (size_t)G * kKvDim;
-        const float* pool = ld.pool + (size_t)b * cap * kKvDim;
-        for (int k = 2 * warp; k < nmiss; k += 2 * nw) {
-            const int p0 = tk[k];
-            if (k + 1 < nmiss) {
-                const int p1 = tk[k + 1];
-                copy_rows2(stg + (size_t)assign[p0] * kKvDim, pool + (size_t)r[p0] * kKvDim,
-                           stg + (size_t)assign[p1] * kKvDim, pool + (size_t)r[p1] * kKvDim, lane);
-            } else {
-                copy_row(stg + (size_t)assign[p0] * kKvDim, pool + (size_t)r[p0] * kKvDim, lane);
-            }
         }
     }
     if (tid == 0) {
@@ -575,8 +537,8 @@ size_t lru_smem_bytes(int S, int G) {
 cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int S, int src_ratio,
                        long long max_dedup_cap, const int32_t* sel, const int32_t* count,
                        int32_t* phys, int32_t* count_l, int2* miss, int* miss_count,
-                       unsigned long long* stats, uint32_t* err, AdaptParams ap, float* staging,
-                       cudaStream_t st, bool chained) {
+                       unsigned long long* stats, uint32_t* err, AdaptParams ap, cudaStream_t st,
+                       bool chained) {
     // a shared-memory table of first positions for layers whose ratio differs from
     // src_ratio, when it fits; otherwise those layers fall back to pairwise checks
     int tbl = 0;
@@ -590,7 +552,7 @@ cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int
         if (e != cudaSuccess) return e;
     }
     return launch_k(lru_kernel, dim3(nl * B), dim3(kLruThreads), smem, st, chained, layers, l0, B, G, S, src_ratio,
-                    tbl, sel, count, phys, count_l, miss, miss_count, stats, err, ap, staging);
+                    tbl, sel, count, phys, count_l, miss, miss_count, stats, err, ap);
 }
 
 cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, int S,

@@ -120,7 +120,8 @@ void free_ctx(srh_ctx* ctx) {
     cudaFree(ctx->d_miss);
     cudaFree(ctx->d_miss_count);
     cudaFree(ctx->d_sink);
-    cudaFree(ctx->d_items);
+    cudaFree(ctx->d_segs);
+    cudaFree(ctx->d_cta_begin);
     cudaFree(ctx->d_part_o);
     cudaFree(ctx->d_part_ml);
     cudaFree(ctx->d_merges);
@@ -129,34 +130,106 @@ void free_ctx(srh_ctx* ctx) {
     delete ctx;
 }
 
-// Split every (layer, sequence) row range into equal splits so the whole
-// attention launch is about one CTA per SM (it holds ~200 KB of shared memory).
-void plan_attention(srh_ctx* ctx, std::vector<AttnItem>* items, std::vector<MergeItem>* merges) {
-    long long total = 0;
-    std::vector<int> max_rows(ctx->L);
-    for (int l = 0; l < ctx->L; ++l) {
-        max_rows[l] = kWindow + (int)std::min<long long>(ctx->S, ctx->caps[l]);
-        total += (long long)ctx->B * max_rows[l];
+// The static attention plan of one lsa_attend scope (the pairs (layer, seq)
+// of `layers`). A pair holds 128 window rows plus at most min(S, cap) staged
+// rows, in 128-row tiles; a CTA holds ~200 KB of shared memory, so one runs
+// per SM. With T tiles in the scope, no plan can give a CTA fewer than
+// ceil(T / SMs) tiles; when cutting every pair into chunks of that many tiles
+// fits one wave, each CTA runs one chunk; otherwise the T tiles, in (layer,
+// seq, row) order, are cut into min(SMs, T) contiguous ranges of equal size
+// (+-1 tile), one CTA each. A pair spread over several CTAs is merged
+// afterwards from their partials. The plan depends only on the configuration,
+// so the same rows give the same bits whichever slots hold them.
+void plan_scope(srh_ctx* ctx, const std::vector<int>& layers, std::vector<AttnSeg>* segs,
+                std::vector<int>* cta_begin, std::vector<MergeItem>* merges, AttnPlan* plan) {
+    const int B = ctx->B;
+    std::vector<int> lbs, tiles;
+    long long T = 0;
+    for (int l : layers)
+        for (int b = 0; b < B; ++b) {
+            const long long rows = kWindow + std::min<long long>(ctx->S, ctx->caps[l]);
+            lbs.push_back(l * B + b);
+            tiles.push_back((int)((rows + kAttnTile - 1) / kAttnTile));
+            T += tiles.back();
+        }
+    plan->seg0 = (int)segs->size();
+    plan->cta0 = (int)cta_begin->size();
+    plan->merge0 = (int)merges->size();
+    std::vector<int> first_slot(lbs.size(), -1), n_parts(lbs.size(), 0);
+    int slot = 0;
+    // Pair-aligned when it fits one wave: each pair is cut into chunks of at
+    // most m = ceil(T / SMs) tiles, one CTA per chunk, so no CTA starts a second
+    // pair (which would cost it a second query load and epilogue).
+    const long long m = (T + ctx->sm_count - 1) / ctx->sm_count;
+    long long n_chunks = 0;
+    for (int t : tiles) n_chunks += (t + m - 1) / m;
+    if (n_chunks <= ctx->sm_count) {
+        for (size_t r = 0; r < lbs.size(); ++r) {
+            const int nc = (int)((tiles[r] + m - 1) / m);
+            for (int c = 0; c < nc; ++c) {
+                cta_begin->push_back((int)segs->size() - plan->seg0);
+                int sl = -1;
+                if (nc > 1) {
+                    sl = slot++;
+                    if (first_slot[r] < 0) first_slot[r] = sl;
+                    ++n_parts[r];
+                }
+                segs->push_back(AttnSeg{lbs[r], (int)(c * m), (int)std::min<long long>((c + 1) * m, tiles[r]), sl});
+            }
+        }
+        plan->n_ctas = (int)n_chunks;
+        cta_begin->push_back((int)segs->size() - plan->seg0);
+        for (size_t r = 0; r < lbs.size(); ++r)
+            if (n_parts[r] > 0) merges->push_back(MergeItem{lbs[r], first_slot[r], n_parts[r], 0});
+        plan->n_segs = (int)segs->size() - plan->seg0;
+        plan->n_merges = (int)merges->size() - plan->merge0;
+        plan->n_slots = slot;
+        return;
     }
-    long long sr = (total + ctx->sm_count - 1) / ctx->sm_count;
-    sr = ((sr + kAttnTile - 1) / kAttnTile) * kAttnTile;
-    sr = std::max<long long>(sr, kAttnTile);
-    ctx->split_rows = (int)sr;
-    ctx->item_begin.assign(ctx->L + 1, 0);
-    ctx->merge_begin.assign(ctx->L + 1, 0);
-    for (int l = 0; l < ctx->L; ++l) {
-        ctx->item_begin[l] = (int)items->size();
-        ctx->merge_begin[l] = (int)merges->size();
-        const int ns = (max_rows[l] + ctx->split_rows - 1) / ctx->split_rows;
-        for (int b = 0; b < ctx->B; ++b) {
-            if (ns > 1) merges->push_back(MergeItem{l * ctx->B + b, (int)items->size(), ns, 0});
-            for (int s = 0; s < ns; ++s) items->push_back(AttnItem{l, b, s, ns});
+    // Otherwise stream-K: min(SMs, T) CTAs over contiguous tile ranges.
+    const int n = (int)std::min<long long>(ctx->sm_count, T);
+    plan->n_ctas = n;
+    size_t q = 0;
+    long long qs = 0;                           // first tile of pair q
+    for (int k = 0; k < n; ++k) {
+        cta_begin->push_back((int)segs->size() - plan->seg0);
+        const long long t0 = (long long)k * T / n, t1 = (long long)(k + 1) * T / n;
+        while (qs + tiles[q] <= t0) qs += tiles[q++];
+        long long t = t0;
+        size_t r = q;
+        long long rs = qs;
+        while (t < t1) {
+            const long long re = rs + tiles[r];
+            const long long e = std::min(re, t1);
+            int sl = -1;
+            if (!(t == rs && e == re)) {        // part of the pair: a partial
+                sl = slot++;
+                if (first_slot[r] < 0) first_slot[r] = sl;
+                ++n_parts[r];
+            }
+            segs->push_back(AttnSeg{lbs[r], (int)(t - rs), (int)(e - rs), sl});
+            t = e;
+            if (e == re) rs += tiles[r++];
         }
     }
-    ctx->item_begin[ctx->L] = (int)items->size();
-    ctx->merge_begin[ctx->L] = (int)merges->size();
-    ctx->n_items = (int)items->size();
-    ctx->n_merges = (int)merges->size();
+    cta_begin->push_back((int)segs->size() - plan->seg0);
+    for (size_t r = 0; r < lbs.size(); ++r)
+        if (n_parts[r] > 0) merges->push_back(MergeItem{lbs[r], first_slot[r], n_parts[r], 0});
+    plan->n_segs = (int)segs->size() - plan->seg0;
+    plan->n_merges = (int)merges->size() - plan->merge0;
+    plan->n_slots = slot;
+}
+
+// Plans [0] for all layers and [1 + l] for layer l alone.
+void plan_attention(srh_ctx* ctx, std::vector<AttnSeg>* segs, std::vector<int>* cta_begin,
+                    std::vector<MergeItem>* merges) {
+    ctx->plans.assign(ctx->L + 1, AttnPlan{});
+    std::vector<int> all(ctx->L);
+    for (int l = 0; l < ctx->L; ++l) all[l] = l;
+    plan_scope(ctx, all, segs, cta_begin, merges, &ctx->plans[0]);
+    for (int l = 0; l < ctx->L; ++l) plan_scope(ctx, {l}, segs, cta_begin, merges, &ctx->plans[1 + l]);
+    ctx->max_slots = 0;
+    for (const AttnPlan& p : ctx->plans) ctx->max_slots = std::max(ctx->max_slots, p.n_slots);
 }
 
 }  // namespace
@@ -290,14 +363,19 @@ int srh_create(const srh_config* cfg, srh_ctx** out) {
     if (e == cudaSuccess) e = cudaMemset(ctx->d_miss_count, 0, sizeof(int) * (size_t)ctx->L * B);
     if (e != cudaSuccess) return bail(SRH_ERR_NOMEM, std::string("device scratch: ") + cudaGetErrorString(e));
 
-    std::vector<AttnItem> items;
+    std::vector<AttnSeg> segs;
+    std::vector<int> cta_begin;
     std::vector<MergeItem> merges;
-    plan_attention(ctx, &items, &merges);
-    e = cudaMalloc(&ctx->d_items, sizeof(AttnItem) * items.size());
+    plan_attention(ctx, &segs, &cta_begin, &merges);
+    e = cudaMalloc(&ctx->d_segs, sizeof(AttnSeg) * segs.size());
     if (e == cudaSuccess)
-        e = cudaMemcpy(ctx->d_items, items.data(), sizeof(AttnItem) * items.size(), cudaMemcpyHostToDevice);
-    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_part_o, sizeof(float) * (size_t)ctx->n_items * SRH_MAX_HEADS * kKvDim);
-    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_part_ml, sizeof(float) * (size_t)ctx->n_items * 2 * SRH_MAX_HEADS);
+        e = cudaMemcpy(ctx->d_segs, segs.data(), sizeof(AttnSeg) * segs.size(), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_cta_begin, sizeof(int) * cta_begin.size());
+    if (e == cudaSuccess)
+        e = cudaMemcpy(ctx->d_cta_begin, cta_begin.data(), sizeof(int) * cta_begin.size(), cudaMemcpyHostToDevice);
+    const size_t slots = (size_t)std::max(ctx->max_slots, 1);
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_part_o, sizeof(float) * slots * SRH_MAX_HEADS * kKvDim);
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_part_ml, sizeof(float) * slots * 2 * SRH_MAX_HEADS);
     if (e == cudaSuccess && !merges.empty()) e = cudaMalloc(&ctx->d_merges, sizeof(MergeItem) * merges.size());
     if (e == cudaSuccess && !merges.empty())
         e = cudaMemcpy(ctx->d_merges, merges.data(), sizeof(MergeItem) * merges.size(), cudaMemcpyHostToDevice);
@@ -503,19 +581,24 @@ int kvswap_stage(srh_ctx* ctx, int layer, const int32_t* d_sel, const int32_t* d
     long long dedup_cap = 0;
     for (int l = l0; l < l0 + nl; ++l)
         if (ctx->ratios[l] != ctx->cfg.src_ratio) dedup_cap = std::max(dedup_cap, ctx->caps[l]);
-    // one stream: the resolve kernel gathers its own misses; with a side stream
-    // the gather is a kernel of its own there, joined back by an event
-    const bool split = ss && ss != sm;
     cudaError_t e = launch_lru(ctx->d_layers, l0, nl, ctx->B, ctx->G, ctx->S, ctx->cfg.src_ratio, dedup_cap,
                                d_sel, d_count, d_phys, d_count_l, ctx->d_miss, ctx->d_miss_count, ctx->d_stats,
-                               ctx->d_err, ctx->adapt, split ? nullptr : d_staging, sm, ctx->chained);
+                               ctx->d_err, ctx->adapt, sm, ctx->chained);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "kvswap_stage LRU launch");
-    if (split) {
+    // The gather is a wide kernel of its own: a boundary step's misses are rows
+    // of host pages the GPU may not have read recently, so many must be in
+    // flight at once. On the main stream it directly follows the resolve
+    // kernel (chained); with a side stream it runs there, joined by events.
+    if (ss && ss != sm) {
         SRH_CUDA(ctx, cudaEventRecord(ctx->ev_resolved, sm));
         SRH_CUDA(ctx, cudaStreamWaitEvent(ss, ctx->ev_resolved, 0));
-        e = launch_gather(ctx->d_layers, l0, nl, ctx->B, ctx->G, ctx->S, ctx->d_miss, ctx->d_miss_count,
-                          d_staging, ctx->d_err, ctx->sm_count, ss, false);
-        if (e != cudaSuccess) return cuda_fail(ctx, e, "kvswap_stage gather launch");
+    } else {
+        ss = sm;
+    }
+    e = launch_gather(ctx->d_layers, l0, nl, ctx->B, ctx->G, ctx->S, ctx->d_miss, ctx->d_miss_count, d_staging,
+                      ctx->d_err, ctx->sm_count, ss, ss == sm);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "kvswap_stage gather launch");
+    if (ss != sm) {
         SRH_CUDA(ctx, cudaEventRecord(ctx->ev_gathered, ss));
         SRH_CUDA(ctx, cudaStreamWaitEvent(sm, ctx->ev_gathered, 0));
     }
@@ -534,14 +617,11 @@ int lsa_attend(srh_ctx* ctx, int layer, const uint16_t* d_q, int n_heads, const 
         return fail(ctx, SRH_ERR_INVALID, "n_heads must be 16, 32 or 64");
     if (((uintptr_t)d_q | (uintptr_t)d_window | (uintptr_t)d_staging | (uintptr_t)d_out) & 15)
         return fail(ctx, SRH_ERR_INVALID, "q/window/staging/out must be 16-byte aligned");
-    const int i0 = layer < 0 ? 0 : ctx->item_begin[layer];
-    const int i1 = layer < 0 ? ctx->n_items : ctx->item_begin[layer + 1];
-    const int m0 = layer < 0 ? 0 : ctx->merge_begin[layer];
-    const int m1 = layer < 0 ? ctx->n_merges : ctx->merge_begin[layer + 1];
-    const cudaError_t e = launch_attend(ctx->d_items, i0, i1 - i0, ctx->d_merges, m0, m1 - m0, ctx->split_rows,
-                                        n_heads, ctx->B, ctx->G, ctx->S, d_q, d_window, d_staging, d_phys,
-                                        d_count_l, d_out, ctx->d_part_o, ctx->d_part_ml, ctx->d_err,
-                                        (cudaStream_t)stream, ctx->chained);
+    const AttnPlan& pl = ctx->plans[layer + 1];
+    const cudaError_t e = launch_attend(ctx->d_segs + pl.seg0, ctx->d_cta_begin + pl.cta0, pl.n_ctas,
+                                        ctx->d_merges + pl.merge0, pl.n_merges, n_heads, ctx->B, ctx->G, ctx->S,
+                                        d_q, d_window, d_staging, d_phys, d_count_l, d_out, ctx->d_part_o,
+                                        ctx->d_part_ml, ctx->d_err, (cudaStream_t)stream, ctx->chained);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "lsa_attend launch");
     return SRH_OK;
 }

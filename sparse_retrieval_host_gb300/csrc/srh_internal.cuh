@@ -94,21 +94,32 @@ struct LayerDev {
     AdaptState* adapt;       // [B] (swap layers)
 };
 
-// One attention work item: rows [split*split_rows, ...) of (layer, seq).
-struct AttnItem {
-    int layer;
-    int seq;
-    int split;
-    int n_splits;
+// One segment of the attention plan: tiles [tile0, tile1) (128 rows each) of
+// one (layer, seq). A CTA runs a contiguous range of the plan's tiles, so its
+// segments are the pairs that range touches. A segment holding every tile of
+// its pair writes the output; the others write partials to `slot`.
+struct AttnSeg {
+    int lb;      // layer * B + seq
+    int tile0;
+    int tile1;
+    int slot;    // partial slot, or -1
 };
 
-// One (layer, seq) whose rows were cut into ns > 1 splits: the merge pass
-// combines the partials of items first .. first + ns - 1 into its output.
+// One (layer, seq) whose tiles were cut across ns > 1 CTAs: the merge pass
+// combines partial slots first .. first + ns - 1, in row order.
 struct MergeItem {
     int lb;      // layer * B + seq
-    int first;   // index of its split 0 in the item list
+    int first;
     int ns;
     int pad;
+};
+
+// The static attention plan of one lsa_attend scope (all layers, or one).
+struct AttnPlan {
+    int seg0, n_segs;      // into Ctx::d_segs
+    int cta0, n_ctas;      // into Ctx::d_cta_begin (n_ctas + 1 entries from cta0)
+    int merge0, n_merges;  // into Ctx::d_merges
+    int n_slots;
 };
 
 struct Ctx {
@@ -148,16 +159,14 @@ struct Ctx {
     int2* d_miss = nullptr;             // [L][B][S] (chunk, slot)
     int* d_miss_count = nullptr;        // [L][B]
     uint32_t* d_sink = nullptr;         // write target that keeps the page-touch loads alive
-    // attention scratch
-    AttnItem* d_items = nullptr;        // all items, grouped by layer
-    std::vector<int> item_begin;        // [L+1] offsets into d_items
-    int split_rows = 0;
-    int n_items = 0;
-    float* d_part_o = nullptr;          // [n_items][SRH_MAX_HEADS][D]
-    float* d_part_ml = nullptr;         // [n_items][2][SRH_MAX_HEADS]
-    MergeItem* d_merges = nullptr;      // the multi-split (layer, seq) pairs, grouped by layer
-    std::vector<int> merge_begin;       // [L+1] offsets into d_merges
-    int n_merges = 0;
+    // attention plans: [0] all layers, [1 + l] layer l alone
+    std::vector<AttnPlan> plans;
+    AttnSeg* d_segs = nullptr;
+    int* d_cta_begin = nullptr;
+    MergeItem* d_merges = nullptr;
+    int max_slots = 0;
+    float* d_part_o = nullptr;          // [max_slots][SRH_MAX_HEADS][D]
+    float* d_part_ml = nullptr;         // [max_slots][2][SRH_MAX_HEADS]
     // bookkeeping
     float* staging = nullptr;           // the staging buffer bound to this context
     cudaEvent_t ev_resolved = nullptr;
@@ -201,13 +210,11 @@ cudaError_t launch_select(const float* scores, int n, int B, int mode, int k, fl
                           int clamp, int S, uint32_t* hist, int32_t* sel, int32_t* count,
                           cudaStream_t st, const unsigned long long* cand = nullptr,
                           const int* cand_cnt = nullptr, int cand_cap = 0, bool chained = false);
-// With staging != nullptr the resolve kernel also copies its misses into the
-// staging rows (no separate gather kernel); otherwise it writes the miss lists.
 cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int S, int src_ratio,
                        long long max_dedup_cap, const int32_t* sel, const int32_t* count,
                        int32_t* phys, int32_t* count_l, int2* miss, int* miss_count,
-                       unsigned long long* stats, uint32_t* err, AdaptParams ap, float* staging,
-                       cudaStream_t st, bool chained);
+                       unsigned long long* stats, uint32_t* err, AdaptParams ap, cudaStream_t st,
+                       bool chained);
 cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, int S,
                           const int2* miss, const int* miss_count, float* staging,
                           uint32_t* err, int sm_count, cudaStream_t st, bool chained);
@@ -216,11 +223,10 @@ cudaError_t launch_store(const LayerDev* layers, int l, int B, int G, int seq, l
                          const float* rows, float* staging, uint32_t* err, cudaStream_t st);
 cudaError_t launch_resident_fill(const float* pool_dev, const uint8_t* ready, long long cap,
                                  int layer, int B, int G, float* staging, cudaStream_t st);
-cudaError_t launch_attend(const AttnItem* items, int item0, int n_items, const MergeItem* merges, int merge0,
-                          int n_merges, int split_rows, int n_heads, int B, int G, int S, const uint16_t* q,
-                          const float* window, const float* staging, const int32_t* phys,
-                          const int32_t* count_l, float* out, float* part_o, float* part_ml, uint32_t* err,
-                          cudaStream_t st, bool chained);
+cudaError_t launch_attend(const AttnSeg* segs, const int* cta_begin, int n_ctas, const MergeItem* merges,
+                          int n_merges, int n_heads, int B, int G, int S, const uint16_t* q, const float* window,
+                          const float* staging, const int32_t* phys, const int32_t* count_l, float* out,
+                          float* part_o, float* part_ml, uint32_t* err, cudaStream_t st, bool chained);
 size_t lru_smem_bytes(int S, int G);
 int attend_max_splits();
 
