@@ -287,6 +287,71 @@ class DecodeStep:
             pass
 
 
+class HostLoop:
+    """Decode steps fed from pinned host memory and read back into it, with the
+    copies of neighbouring steps overlapping the step in flight.
+
+    Two sets of device input/output buffers alternate. Step i's queries are
+    copied in on one stream while step i-1 runs, and step i-1's outputs
+    (attention output, selection, count) are copied out on another while step
+    i runs; each step is one graph replay on the compute stream, so the LRU
+    state still advances in step order. A set is refilled only after the step
+    that read it finished and its outputs left the device (stream events).
+    """
+
+    def __init__(self, ds: "DecodeStep", spec: StepSpec):
+        self.ds = ds
+        dev = ds.keys.device
+        self.fm_q = [torch.zeros_like(ds.fm_q) for _ in range(2)]
+        self.q = [torch.zeros_like(ds.q) for _ in range(2)]
+        self.out = [torch.zeros_like(ds.out) for _ in range(2)]
+        self.sel = [torch.zeros_like(ds.sel) for _ in range(2)]
+        self.count = [torch.zeros_like(ds.count) for _ in range(2)]
+        self.s_comp = torch.cuda.Stream(device=dev)
+        self.s_in = torch.cuda.Stream(device=dev)
+        self.s_out = torch.cuda.Stream(device=dev)
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]
+        self.ev_done = [torch.cuda.Event() for _ in range(2)]
+        self.ev_out = [torch.cuda.Event() for _ in range(2)]
+        self.s_comp.wait_stream(torch.cuda.current_stream(dev))
+        self.graphs = []
+        for k in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.s_comp):
+                ds.step(spec, self.s_comp, fm_q=self.fm_q[k], q=self.q[k], out=self.out[k])
+                self.sel[k].copy_(ds.sel)
+                self.count[k].copy_(ds.count)
+            self.graphs.append(g)
+        torch.cuda.current_stream(dev).wait_stream(self.s_comp)
+
+    def step(self, i: int, h_fm_q: torch.Tensor, h_q: torch.Tensor, h_out: torch.Tensor, h_sel: torch.Tensor,
+             h_count: torch.Tensor) -> None:
+        """Issue step i: inputs from pinned ``h_fm_q``/``h_q``, outputs into pinned
+        ``h_out``/``h_sel``/``h_count`` (ready once ``synchronize()`` returns, or
+        two steps later). Asynchronous."""
+        k = i & 1
+        self.s_in.wait_event(self.ev_done[k])          # step i-2 finished reading set k
+        with torch.cuda.stream(self.s_in):
+            self.fm_q[k].copy_(h_fm_q, non_blocking=True)
+            self.q[k].copy_(h_q, non_blocking=True)
+        self.ev_in[k].record(self.s_in)
+        self.s_comp.wait_event(self.ev_in[k])
+        self.s_comp.wait_event(self.ev_out[k])         # step i-2's outputs left set k
+        with torch.cuda.stream(self.s_comp):
+            self.graphs[k].replay()
+        self.ev_done[k].record(self.s_comp)
+        self.s_out.wait_event(self.ev_done[k])
+        with torch.cuda.stream(self.s_out):
+            h_out.copy_(self.out[k], non_blocking=True)
+            h_sel.copy_(self.sel[k], non_blocking=True)
+            h_count.copy_(self.count[k], non_blocking=True)
+        self.ev_out[k].record(self.s_out)
+
+    def synchronize(self) -> None:
+        for s in (self.s_in, self.s_comp, self.s_out):
+            s.synchronize()
+
+
 def bits_to_i16(a: np.ndarray) -> torch.Tensor:
     """uint16 bf16 bit patterns as an int16 tensor (same bytes)."""
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16))

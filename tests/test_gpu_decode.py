@@ -385,3 +385,45 @@ def test_replay_after_unconsumed_scoring_selects_right(ctx_len):
         assert ds.check_error() == 0
     finally:
         ds.close()
+
+
+def test_host_loop_matches_eager_steps():
+    """runtime.HostLoop (pinned host inputs and outputs, copies of neighbouring
+    steps overlapping the step in flight) gives, step for step, the bits of
+    eager steps fed through the bound buffers."""
+    from sparse_retrieval_host_gb300.runtime import HostLoop, bits_to_i16
+    w = C.TINY.with_(steps=10)
+    n = 9
+    h_fmq = [bits_to_i16(np.stack([G.fm_queries(w, t, b) for b in range(w.batch)])).pin_memory() for t in range(n)]
+    h_q = [bits_to_i16(np.stack([np.stack([G.attn_q(w, t, l, b) for b in range(w.batch)])
+                                 for l in range(w.n_layers)])).pin_memory() for t in range(n)]
+    runs = []
+    for mode in ("eager", "loop"):
+        ds = make_ds(w)
+        try:
+            fill(ds, w)
+            spec = spec_of(w)
+            load_step_inputs(ds, w, 0)
+            ds.step(spec)                                   # set-up step
+            outs = []
+            if mode == "eager":
+                for t in range(1, n):
+                    ds.fm_q.copy_(h_fmq[t])
+                    ds.q.copy_(h_q[t])
+                    ds.step(spec)
+                    outs.append((ds.out.cpu(), ds.sel.cpu(), ds.count.cpu()))
+            else:
+                loop = HostLoop(ds, spec)
+                bufs = [(torch.empty(ds.out.shape).pin_memory(), torch.empty(ds.sel.shape, dtype=torch.int32).pin_memory(),
+                         torch.empty(ds.count.shape, dtype=torch.int32).pin_memory()) for _ in range(1, n)]
+                for i, t in enumerate(range(1, n)):
+                    loop.step(i, h_fmq[t], h_q[t], *bufs[i])
+                loop.synchronize()
+                outs = bufs
+            assert ds.check_error() == 0
+            runs.append(outs)
+        finally:
+            ds.close()
+    for a, b in zip(*runs):
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
