@@ -505,8 +505,62 @@ def run_ours(args, dist, rank, world, local):
         e2e = run_e2e(args, w, ds, spec, graph)
         if result is not None:
             result["e2e"] = e2e
+    gather = run_miss_gather(w, ds, stream)
+    if result is not None:
+        result["miss_gather"] = gather
     ds.close()
     return result
+
+
+def run_miss_gather(w, ds, stream):
+    """Host-link roofline of the miss gather: kvswap_stage calls in which every
+    selected chunk of a swapped layer misses (disjoint chunk sets in turn, so the
+    LRU always evicts a set staged earlier), timed after every row's host pages
+    were read once, against a plain pinned H2D copy of 256 MiB in the same run."""
+    import torch
+    if not any(ds.swap):
+        return None
+    m = w.index_topk if w.select_mode == C.SELECT_TOPK else w.clamp
+    n_sets = 3 if w.gpu_chunks >= 2 * m else 2
+    if w.n_chunks < n_sets * m:
+        return None
+    sets = [torch.arange(i * m, (i + 1) * m, dtype=torch.int32, device=ds.sel.device) for i in range(n_sets)]
+
+    def select_set(i):
+        ds.sel[:, :m] = sets[i % n_sets]
+        ds.count.fill_(m)
+
+    for i in range(2 * n_sets):                         # fill the slots, then read every row once more
+        select_set(i)
+        ds.stage(-1, stream)
+    torch.cuda.synchronize()
+    ds.reset_stats()
+    R = 6
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(R)]
+    for i in range(R):
+        select_set(2 * n_sets + i)                      # outside the timed span
+        ev[i][0].record(stream)
+        ds.stage(-1, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert ds.check_error() == 0, "device error during the miss-gather measurement"
+    st = ds.stats()
+    secs = sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3
+    src = torch.empty(64 << 20, dtype=torch.float32).pin_memory()
+    dst = torch.empty(src.shape, dtype=torch.float32, device=ds.sel.device)
+    link = 0.0
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dst.copy_(src, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        link = max(link, src.numel() * 4 / (a.elapsed_time(b) / 1e3) / 1e9)
+    gbs = st["h2d_bytes"] / secs / 1e9
+    return {"gbs": gbs, "host_link_gbs": link, "frac": gbs / link, "misses_per_call": st["misses"] / R,
+            "hits": st["hits"], "us_per_call": secs / R * 1e6,
+            "note": f"kvswap_stage (resolve + zero-copy gather) of {m} chunks per sequence, all missing in every "
+                    f"swapped layer, rows read once before; host link = pinned cudaMemcpyAsync H2D of 256 MiB"}
 
 
 def run_e2e(args, w, ds, spec, graph):
