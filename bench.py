@@ -37,6 +37,7 @@ import numpy as np  # noqa: E402
 from srh_workload import configs as C  # noqa: E402
 from srh_workload import generate as G  # noqa: E402
 
+HOLD_CYCLES = 400_000          # ~0.2 ms device-side wait before eagerly timed calls
 BASE_KERNELS = 5              # score, select, lru, gather, attend (+ merge, + candidate pass)
 COLLECT_MIN_N = 16384         # fm_select runs its candidate pass above this many chunks
 Q_CYCLE = 16                  # distinct attention-query sets cycled through the steps
@@ -230,6 +231,12 @@ def adaptive_policy(w):
                 lo_permille=800, hi_permille=900, delta=max(1, w.gpu_chunks // 8))
 
 
+def pass_bytes(w):
+    """Algorithmic bytes of the scoring + selection pass: keys, the score write and
+    up to two reads of the scores by the selection."""
+    return w.batch * w.n_chunks * (C.INDEXER_DIM * 2 + 12)
+
+
 def score_bytes(w):
     return w.batch * w.n_chunks * (C.INDEXER_DIM * 2 + 4)
 
@@ -392,6 +399,25 @@ def run_ours(args, dist, rank, world, local):
     assert ds.check_error() == 0, "device error during the breakdown steps"
     score_ms = [e[0].elapsed_time(e[1]) for e in evb]
 
+    # the scoring + selection pass alone, eager calls queued behind the L2 flush and
+    # a short device-side wait (the device is still busy when they are issued, so
+    # the event spans are device time, without host or graph-launch latency)
+    sp_score, sp_select = [], []
+    for i in range(8):
+        bind(args.warmup + K + KP + KB + i)
+        flush_l2()
+        torch.cuda._sleep(HOLD_CYCLES)                  # the calls below are all queued before the GPU gets to them
+        q0, q1, q2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        q0.record(stream)
+        ds.score(spec, stream)
+        q1.record(stream)
+        ds.select(spec, stream)
+        q2.record(stream)
+        q2.synchronize()
+        if i >= 2:
+            sp_score.append(q0.elapsed_time(q1))
+            sp_select.append(q1.elapsed_time(q2))
+
     # one key set per memory indexer (fm_score_multi): the scoring call alone
     from sparse_retrieval_host_gb300 import abi
     keys3 = torch.empty((3,) + tuple(ds.keys.shape), dtype=ds.keys.dtype, device=device)
@@ -399,6 +425,7 @@ def run_ours(args, dist, rank, world, local):
     multi_ms = []
     for i in range(6):
         flush_l2()
+        torch.cuda._sleep(HOLD_CYCLES)
         m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         m0.record(stream)
         abi.fm_score_multi(ds.ctx, keys3, ds.n, ds.fm_q, spec.scale, spec.bias, spec.ensemble, ds.scores, stream)
@@ -415,6 +442,7 @@ def run_ours(args, dist, rank, world, local):
     fp8_ms = []
     for i in range(6):
         flush_l2()
+        torch.cuda._sleep(HOLD_CYCLES)
         m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         m0.record(stream)
         abi.fm_score_fp8(ds.ctx, codes, kscale, ds.n, ds.fm_q, spec.scale, spec.bias, spec.ensemble, ds.scores,
@@ -477,15 +505,25 @@ def run_ours(args, dist, rank, world, local):
                            "lsa_attend": a_avg_ms * 1e3,
                            "note": f"phase spans of {KB} further steps replayed as three graphs"},
             "score_gbs": score_bytes(w) / (statistics.mean(score_ms) / 1e3) / 1e9,
+            "score_select_pass": {
+                "score_us": statistics.median(sp_score) * 1e3, "select_us": statistics.median(sp_select) * 1e3,
+                "bytes": pass_bytes(w),
+                "gbs": pass_bytes(w) / ((statistics.median(sp_score) + statistics.median(sp_select)) / 1e3) / 1e9,
+                "score_kernel_gbs": score_bytes(w) / (statistics.median(sp_score) / 1e3) / 1e9,
+                "frac": pass_bytes(w) / ((statistics.median(sp_score) + statistics.median(sp_select)) / 1e3) / 1e9
+                / peak,
+                "note": "fm_score then fm_select, eager, queued behind the L2 flush; bytes = keys + score write + "
+                        "selection reads (256 + 12 per chunk and sequence)"},
             "score_fp8_keys": {
                 "us": statistics.median(fp8_ms) * 1e3,
                 "gbs": w.batch * w.n_chunks * (C.INDEXER_DIM + 4 + 4) / (statistics.median(fp8_ms) / 1e3) / 1e9,
                 "note": "fm_score_fp8: e4m3 codes + fp32 scale per chunk (132 B read, 4 B written), L2 flushed, "
-                        "memset + kernel"},
+                        "eager call queued behind a device-side wait"},
             "score_per_indexer_keys": {
                 "us": statistics.median(multi_ms) * 1e3,
                 "gbs": w.batch * w.n_chunks * (3 * C.INDEXER_DIM * 2 + 4) / (statistics.median(multi_ms) / 1e3) / 1e9,
-                "note": "fm_score_multi, three key sets (one per memory indexer), L2 flushed, memset + kernel"},
+                "note": "fm_score_multi, three key sets (one per memory indexer), L2 flushed, eager call queued "
+                        "behind a device-side wait"},
             "step_hbm_gbs": step_bytes / (statistics.mean(step_ms) / 1e3) / 1e9,
             "lru_hit_rate": (st["hits"] / sel_total) if sel_total else None,
             "staged_bytes_per_step": st["h2d_bytes"] / K,
