@@ -154,7 +154,7 @@ struct Src {
 __global__ void __launch_bounds__(kSelThreads)
 select_kernel(const float* __restrict__ scores, int n, int mode, int k, float thresh, int clamp,
               int S, uint32_t* __restrict__ hist_in, const unsigned long long* __restrict__ cand_in,
-              const int* __restrict__ cand_cnt, int cand_cap, int32_t* __restrict__ sel,
+              int* __restrict__ cand_cnt, int cand_cap, int32_t* __restrict__ sel,
               int32_t* __restrict__ count) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
@@ -214,6 +214,9 @@ select_kernel(const float* __restrict__ scores, int n, int mode, int k, float th
         sh.sq = 0ull;
     }
     __syncthreads();
+    // every thread has read the candidate count: leave it zeroed for the next
+    // candidate pass (which adds into it)
+    if (cand_in && tid == 0) cand_cnt[b] = 0;
 
     int K;
     if (mode == SRH_SELECT_THRESH) {
@@ -468,7 +471,7 @@ collect_kernel(const float* __restrict__ scores, int n, int mode, int K, float t
 
 cudaError_t launch_select(const float* scores, int n, int B, int mode, int k, float thresh,
                           int clamp, int S, uint32_t* hist, int32_t* sel, int32_t* count,
-                          cudaStream_t st, const unsigned long long* cand, const int* cand_cnt, int cand_cap,
+                          cudaStream_t st, const unsigned long long* cand, int* cand_cnt, int cand_cap,
                           bool chained) {
     const size_t smem = sizeof(SelShared) + sizeof(unsigned long long) * kArr;
     static bool attr_set = false;
@@ -486,14 +489,15 @@ int select_cand_cap() { return kCandCap; }
 
 cudaError_t launch_collect(const float* scores, int n, int B, int mode, int K, float thresh,
                            const uint32_t* hist, unsigned long long* cand, int* cand_cnt, int cap,
-                           cudaStream_t st) {
-    cudaError_t e = cudaMemsetAsync(cand_cnt, 0, sizeof(int) * B, st);
-    if (e != cudaSuccess) return e;
+                           cudaStream_t st, bool clear_count, bool chained) {
+    if (clear_count) {
+        const cudaError_t e = cudaMemsetAsync(cand_cnt, 0, sizeof(int) * B, st);
+        if (e != cudaSuccess) return e;
+    }
     const int per_cta = kCollectThreads * kCollectPer;
     const int bx = (n + per_cta - 1) / per_cta;
-    collect_kernel<<<dim3((unsigned)bx, (unsigned)B), kCollectThreads, 0, st>>>(scores, n, mode, K, thresh,
-                                                                              hist, cand, cand_cnt, cap);
-    return cudaGetLastError();
+    return launch_k(collect_kernel, dim3((unsigned)bx, (unsigned)B), dim3(kCollectThreads), 0, st, chained, scores,
+                    n, mode, K, thresh, hist, cand, cand_cnt, cap);
 }
 
 }  // namespace srh

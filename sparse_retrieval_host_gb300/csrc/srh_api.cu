@@ -357,6 +357,7 @@ int srh_create(const srh_config* cfg, srh_ctx** out) {
     if (e == cudaSuccess) e = cudaMemset(ctx->d_hist, 0, sizeof(uint32_t) * kHistBins * B);
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_cand, sizeof(unsigned long long) * select_cand_cap() * B);
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_cand_cnt, sizeof(int) * B);
+    if (e == cudaSuccess) e = cudaMemset(ctx->d_cand_cnt, 0, sizeof(int) * B);
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_miss, sizeof(int2) * (size_t)ctx->L * B * ctx->S);
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_miss_count, sizeof(int) * (size_t)ctx->L * B);
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_sink, sizeof(uint32_t));
@@ -542,7 +543,8 @@ int fm_select(srh_ctx* ctx, const float* d_scores, int n, int mode, int k, float
     if (n > kCollectMinN) {
         const int K = mode == SRH_SELECT_TOPK ? std::min(k, n) : clamp;
         const cudaError_t ec = launch_collect(d_scores, n, ctx->B, mode, K, thresh, hist, ctx->d_cand,
-                                              ctx->d_cand_cnt, select_cand_cap(), st);
+                                              ctx->d_cand_cnt, select_cand_cap(), st, !ctx->cand_clean, chained);
+        ctx->cand_clean = false;
         if (ec != cudaSuccess) return cuda_fail(ctx, ec, "fm_select candidate pass");
         cand = ctx->d_cand;
         chained = true;
@@ -551,6 +553,7 @@ int fm_select(srh_ctx* ctx, const float* d_scores, int n, int mode, int k, float
                                         d_count, st, cand, ctx->d_cand_cnt, select_cand_cap(), chained);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "fm_select launch");
     if (hist) ctx->hist_clean = true;   // the select kernel zeroes the rows it reads
+    if (cand) ctx->cand_clean = true;   // ... and the candidate counts
     return SRH_OK;
 }
 

@@ -154,6 +154,7 @@ struct Ctx {
     bool hist_clean = true;             // d_hist is all zeros (cleared, or consumed by a selection)
     unsigned long long* d_cand = nullptr; // [B][select_cand_cap()] candidate composites
     int* d_cand_cnt = nullptr;          // [B]
+    bool cand_clean = true;             // d_cand_cnt is zero (cleared, or consumed by a selection)
     const float* hist_scores = nullptr; // the d_scores the histogram describes
     int hist_n = -1;
     int2* d_miss = nullptr;             // [L][B][S] (chunk, slot)
@@ -200,16 +201,17 @@ cudaError_t launch_quantize_keys(const uint16_t* keys, long long total, uint8_t*
 cudaError_t launch_score_fp8(const uint8_t* codes, const float* kscale, int n, int B, const uint16_t* q, float scale,
                              const float* bias3, int ensemble, float* scores, uint32_t* hist, int sm_count,
                              cudaStream_t st, bool clear_hist);
-// Candidate pass for large n: zeroes cand_cnt, then appends the selectable keys.
+// Candidate pass for large n: appends the selectable keys to cand, counting in
+// cand_cnt (zeroed first with clear_count; the select kernel leaves it zeroed).
 cudaError_t launch_collect(const float* scores, int n, int B, int mode, int K, float thresh,
                            const uint32_t* hist, unsigned long long* cand, int* cand_cnt, int cap,
-                           cudaStream_t st);
+                           cudaStream_t st, bool clear_count, bool chained);
 int select_cand_cap();
 constexpr int kCollectMinN = 16384;    // fm_select runs the candidate pass above this n
 cudaError_t launch_select(const float* scores, int n, int B, int mode, int k, float thresh,
                           int clamp, int S, uint32_t* hist, int32_t* sel, int32_t* count,
                           cudaStream_t st, const unsigned long long* cand = nullptr,
-                          const int* cand_cnt = nullptr, int cand_cap = 0, bool chained = false);
+                          int* cand_cnt = nullptr, int cand_cap = 0, bool chained = false);
 cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int S, int src_ratio,
                        long long max_dedup_cap, const int32_t* sel, const int32_t* count,
                        int32_t* phys, int32_t* count_l, int2* miss, int* miss_count,
