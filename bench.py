@@ -150,15 +150,16 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def traffic_record(kernel: str):
-    """Measured DRAM bytes per launch from an ncu capture, if the kernel source
-    is unchanged since (profiles/traffic.json keys it by a hash of the source)."""
+def traffic_record(kernel: str, workload: str):
+    """Measured DRAM bytes per launch from an ncu capture of this workload, if the
+    kernel source is unchanged since (profiles/traffic.json keys it by a hash of
+    the source and names the workload it was taken on)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         rec = json.load(f).get(kernel)
-    if not rec:
+    if not rec or rec.get("workload") != workload:
         return None
     src = os.path.join(ROOT, "sparse_retrieval_host_gb300", "csrc", rec["source"])
     h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
@@ -402,21 +403,30 @@ def run_ours(args, dist, rank, world, local):
     # the scoring + selection pass alone, eager calls queued behind the L2 flush and
     # a short device-side wait (the device is still busy when they are issued, so
     # the event spans are device time, without host or graph-launch latency)
-    sp_score, sp_select = [], []
-    for i in range(8):
+    # The same for the whole step, call by call: these spans are the per-call
+    # device times; the attention call's is the roofline's launch duration.
+    sp_score, sp_select, sp_stage, sp_attn, sp_counts = [], [], [], [], []
+    for i in range(10):
         bind(args.warmup + K + KP + KB + i)
         flush_l2()
         torch.cuda._sleep(HOLD_CYCLES)                  # the calls below are all queued before the GPU gets to them
-        q0, q1, q2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-        q0.record(stream)
+        q = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        q[0].record(stream)
         ds.score(spec, stream)
-        q1.record(stream)
+        q[1].record(stream)
         ds.select(spec, stream)
-        q2.record(stream)
-        q2.synchronize()
+        q[2].record(stream)
+        ds.stage(-1, stream)
+        q[3].record(stream)
+        ds.attend(-1, stream)
+        q[4].record(stream)
+        q[4].synchronize()
         if i >= 2:
-            sp_score.append(q0.elapsed_time(q1))
-            sp_select.append(q1.elapsed_time(q2))
+            sp_score.append(q[0].elapsed_time(q[1]))
+            sp_select.append(q[1].elapsed_time(q[2]))
+            sp_stage.append(q[2].elapsed_time(q[3]))
+            sp_attn.append(q[3].elapsed_time(q[4]))
+            sp_counts.append(ds.count_l.cpu().numpy().copy())
 
     # one key set per memory indexer (fm_score_multi): the scoring call alone
     from sparse_retrieval_host_gb300 import abi
@@ -460,12 +470,12 @@ def run_ours(args, dist, rank, world, local):
     result = None
     if rank == 0:
         peak, peak_kind = measured_peaks()
-        a_bytes = [attn_bytes(w, c) for c in counts]
-        a_avg_ms = statistics.mean(attn_ms)
+        a_bytes = [attn_bytes(w, c) for c in sp_counts]
+        a_avg_ms = statistics.mean(sp_attn)
         achieved = statistics.mean(a_bytes) / (a_avg_ms / 1e3) / 1e9
         sel_total = st["hits"] + st["misses"]
         step_bytes = statistics.mean(a_bytes) + score_bytes(w)
-        traffic = traffic_record("attend")
+        traffic = traffic_record("attend", w.name)
         result = {
             "metric": METRIC,
             "value": tot_steps / tot_s,
@@ -493,7 +503,7 @@ def run_ours(args, dist, rank, world, local):
             },
             "gpu_launches": launches_per_step(w, torch.cuda.get_device_properties(device).multi_processor_count) * K,
             "roofline": {
-                "kernel": "lsa_attend (attend_tc_kernel + merge_kernel)",
+                "kernel": "lsa_attend (attend_tc_kernel + merge_kernel), device time per call",
                 "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind,
                 "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
@@ -502,8 +512,15 @@ def run_ours(args, dist, rank, world, local):
             },
             "kernels_us": {"fm_score": statistics.mean(score_ms) * 1e3,
                            "fm_select+kvswap_stage": statistics.mean(stage_ms) * 1e3,
-                           "lsa_attend": a_avg_ms * 1e3,
-                           "note": f"phase spans of {KB} further steps replayed as three graphs"},
+                           "lsa_attend": statistics.mean(attn_ms) * 1e3,
+                           "note": f"phase spans of {KB} further steps replayed as three graphs (each span "
+                                   "includes its graph launch)"},
+            "calls_us": {"fm_score": statistics.median(sp_score) * 1e3,
+                         "fm_select": statistics.median(sp_select) * 1e3,
+                         "kvswap_stage": statistics.median(sp_stage) * 1e3,
+                         "lsa_attend": statistics.median(sp_attn) * 1e3,
+                         "note": "device time per call: eager calls queued behind the L2 flush and a device-side "
+                                 "wait, unchained"},
             "score_gbs": score_bytes(w) / (statistics.mean(score_ms) / 1e3) / 1e9,
             "score_select_pass": {
                 "score_us": statistics.median(sp_score) * 1e3, "select_us": statistics.median(sp_select) * 1e3,
