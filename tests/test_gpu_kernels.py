@@ -421,9 +421,15 @@ def test_kvswap_rejects_a_second_staging_buffer():
 
 # ----------------------------------------------------------------------------- lsa_attend
 @pytest.mark.parametrize("H", [16, 32, 64])
-@pytest.mark.parametrize("counts,batch_layers", [((0, 1, 31, 32), 1), ((33, 200, 512, 97), 1),
-                                                 ((512,) * 8, 20)])
-def test_lsa_attend_matches_oracle(H, counts, batch_layers):
+@pytest.mark.parametrize("counts,batch_layers,per_layer", [((0, 1, 31, 32), 1, False),
+                                                           ((33, 200, 512, 97), 1, False),
+                                                           ((512,) * 8, 20, False),
+                                                           ((0, 1, 300, 512, 77, 130, 511, 2), 20, False),
+                                                           ((5, 512, 260, 0), 6, True)])
+def test_lsa_attend_matches_oracle(H, counts, batch_layers, per_layer):
+    """All layers in one call (one wave of pair chunks, or stream-K tile ranges
+    when the pairs do not fit one wave, with counts below the planned rows) or one
+    call per layer (the single-layer plans)."""
     from sparse_retrieval_host_gb300.runtime import bits_to_i16
     B = len(counts)
     L = batch_layers
@@ -444,7 +450,11 @@ def test_lsa_attend_matches_oracle(H, counts, batch_layers):
         ds.q.copy_(bits_to_i16(q))
         ds.phys.copy_(torch.from_numpy(phys))
         ds.count_l.copy_(torch.from_numpy(np.tile(np.int32(counts), (L, 1))))
-        ds.attend()
+        if per_layer:
+            for l in range(L):
+                ds.attend(l)
+        else:
+            ds.attend()
         out = ds.out.cpu().numpy()
         worst = 0.0
         for l in range(L):
