@@ -31,7 +31,10 @@ namespace {
 
 constexpr int kLruThreads = 1024;
 
-__device__ int block_scan_incl(int v, int* warp_buf) {
+// Inclusive block scan of one int per thread; *total receives the block total.
+// Two barriers; warp_buf must not be written again before the caller's next
+// barrier.
+__device__ __forceinline__ int block_scan_incl(int v, int* warp_buf, int* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
 #pragma unroll
@@ -51,28 +54,26 @@ __device__ int block_scan_incl(int v, int* warp_buf) {
         warp_buf[lane] = w;
     }
     __syncthreads();
-    const int r = v + (warp > 0 ? warp_buf[warp - 1] : 0);
-    __syncthreads();
-    return r;
+    *total = warp_buf[nwarps - 1];
+    return v + (warp > 0 ? warp_buf[warp - 1] : 0);
 }
 
 // In-place exclusive scan of a[0..len) in shared memory; returns the total.
-__device__ int block_scan_excl_array(int* a, int len, int* warp_buf, int* total_buf) {
+// Three barriers; on return every thread sees the whole scanned array.
+__device__ int block_scan_excl_array(int* a, int len, int* warp_buf) {
     const int per = (len + blockDim.x - 1) / blockDim.x;
     const int beg = threadIdx.x * per;
     const int end = min(beg + per, len);
     int local = 0;
     for (int i = beg; i < end; ++i) local += a[i];
-    const int incl = block_scan_incl(local, warp_buf);
+    int total;
+    const int incl = block_scan_incl(local, warp_buf, &total);
     int run = incl - local;
     for (int i = beg; i < end; ++i) {
         const int v = a[i];
         a[i] = run;
         run += v;
     }
-    if (threadIdx.x == blockDim.x - 1) *total_buf = incl;
-    __syncthreads();
-    const int total = *total_buf;
     __syncthreads();
     return total;
 }
@@ -89,8 +90,6 @@ __device__ __forceinline__ void copy_row(float* __restrict__ dst, const float* _
 
 struct LruShared {
     int warp_buf[32];
-    int total;
-    int m;
     int nmiss;
     int conflict;
 };
@@ -200,7 +199,7 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
         // stable compaction (read all, scan, then write)
         for (int p = tid; p < m0; p += blockDim.x) tk[p] = mr[p];
         __syncthreads();
-        m = block_scan_excl_array(mr, m0, sh.warp_buf, &sh.total);
+        m = block_scan_excl_array(mr, m0, sh.warp_buf);
         for (int p = tid; p < m0; p += blockDim.x) is_miss[p] = r[p];
         __syncthreads();
         for (int p = tid; p < m0; p += blockDim.x)
@@ -273,7 +272,7 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
             }
         }
         __syncthreads();
-        block_scan_excl_array(nh, g0, sh.warp_buf, &sh.total);
+        block_scan_excl_array(nh, g0, sh.warp_buf);
         for (int q = tid; q < g0; q += blockDim.x) {
             const int s = victim[q];
             if (s < g) {
@@ -329,8 +328,8 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
         mr[p] = is_miss[p];
     }
     __syncthreads();
-    block_scan_excl_array(nh, g, sh.warp_buf, &sh.total);
-    const int nmiss0 = block_scan_excl_array(mr, m, sh.warp_buf, &sh.total);
+    block_scan_excl_array(nh, g, sh.warp_buf);
+    const int nmiss0 = block_scan_excl_array(mr, m, sh.warp_buf);
     for (int p = tid; p < m; p += blockDim.x)
         if (is_miss[p]) tk[mr[p]] = p;
     for (int q = tid; q < g; q += blockDim.x)
@@ -377,7 +376,7 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
         __syncthreads();
         for (int p = tid; p < m; p += blockDim.x) mr[p] = is_miss[p];
         __syncthreads();
-        block_scan_excl_array(mr, m, sh.warp_buf, &sh.total);
+        block_scan_excl_array(mr, m, sh.warp_buf);
     }
     const int nmiss = sh.nmiss;
 
@@ -388,7 +387,7 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
     __syncthreads();
     for (int q = tid; q < g; q += blockDim.x) nh[q] = flag[queue[q]] ? 0 : 1;
     __syncthreads();
-    block_scan_excl_array(nh, g, sh.warp_buf, &sh.total);
+    block_scan_excl_array(nh, g, sh.warp_buf);
     for (int q = tid; q < g; q += blockDim.x)
         if (!flag[queue[q]]) lru[nh[q]] = queue[q];
     for (int p = tid; p < m; p += blockDim.x) lru[g - m + p] = assign[p];
