@@ -221,6 +221,11 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         }
     };
     int q_lb = sb < se ? a.segs[sb].lb : 0;
+    // The window rows are this call's own input: the first segment's (when it
+    // starts at tile 0) are requested from HBM before the dependency wait.
+    if (sb < se && a.segs[sb].tile0 == 0 && tid < kWindow)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(a.window + ((size_t)q_lb * kWindow + tid) * kKvDim),
+                     "r"(kKvDim * 4) : "memory");
     if (sb < se) convert_q(q_lb);
     // the barriers, the abort flag, the softmax state and the TMEM address are
     // set: every thread sees them from here on
@@ -291,6 +296,23 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         }
         return reinterpret_cast<const float4*>(a.staging + (lb * (size_t)a.G + slot) * kKvDim);
     };
+    // Ask L2 for the rows of the tile at tr0: one 2 KiB bulk prefetch per row,
+    // issued by threads 0-127. It holds no registers or shared memory, so the
+    // whole tile is requested from HBM at once and the loads below find it in L2.
+    auto prefetch_tile = [&](int tr0) {
+        const int row = tr0 + tid;
+        if (tid >= kTileRows || row >= row1) return;
+        if (si == sb && row < kWindow) return;             // requested before the wait
+        const float* p;
+        if (row < kWindow) {
+            p = a.window + (lb * kWindow + row) * kKvDim;
+        } else {
+            const int slot = ph[row - kWindow] - kWindow;
+            if (slot < 0 || slot >= a.G) return;            // reported by the loads
+            p = a.staging + (lb * (size_t)a.G + slot) * kKvDim;
+        }
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(kKvDim * 4) : "memory");
+    };
     // Four rows of this warp: lane holds float4 lane + 32 j of each (d = 4 (lane + 32 j)).
     auto load4 = [&](float4 (&v)[4][4], int tr0, int rbase) {
 #pragma unroll
@@ -301,9 +323,11 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         }
     };
 
+    if (n_tiles > 0) prefetch_tile(row0);
     for (int tile = 0; tile < n_tiles; ++tile) {
         // ------------------------------------------------------------ load E (all warps)
         const int tr0 = row0 + tile * kTileRows;
+        if (tile + 1 < n_tiles) prefetch_tile(tr0 + kTileRows);   // the next tile's rows, during this one
         float4 b0[4][4], b1[4][4];
         if (ok) {
             load4(b0, tr0, rw);
