@@ -317,6 +317,11 @@ int fm_select_noalloc(const float* d_scores, int batch, int n, int mode, int k, 
  * The LRU is the sequential list of the Swap-in flow: the selected ids are
  * taken in order; a hit moves its slot to the front, a miss pops the back slot
  * (all slots start free, slot 0 first) and copies h_compressed_kv[c] into it.
+ * Overlap: a call may run on another stream while an lsa_attend still reads
+ * the rows the previous call staged (the lookahead schedule), provided it
+ * writes other d_phys/d_count_l buffers and every swapped layer has at least
+ * as many slots in use as the two selections' list lengths together: the
+ * previous list's slots are then the most recently used and none is evicted.
  */
 int kvswap_stage(srh_ctx* ctx, int layer, const int32_t* d_sel, const int32_t* d_count,
                  float* d_staging, int32_t* d_phys, int32_t* d_count_l, srh_stream_t main,

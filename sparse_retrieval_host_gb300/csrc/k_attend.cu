@@ -8,9 +8,13 @@
 //     o_h = sum_j softmax_j(<q_h, e_j> / sqrt(512)) e_j.
 //
 // Work: the rows of one (layer, sequence) -- the 128 window rows, then the
-// layer's staged rows in selection order -- are cut into fixed splits of
-// `split_rows` (a multiple of 128); one CTA runs one split for all heads, in
-// tiles of 128 rows. Each row is read from HBM once per step:
+// layer's staged rows in selection order -- form tiles of 128 rows. A static
+// plan built at context creation gives each CTA a list of segments (a range
+// of tiles of one pair): one chunk of one pair when every pair's chunks fit
+// one wave, otherwise a contiguous range of the whole call's tiles. A CTA runs
+// its segments for all heads, tile by tile. Each row is read from HBM once per
+// step; a tile's rows are requested into L2 with bulk prefetches before the
+// loads below:
 //   load    all 8 warps stream the tile's fp32 rows (warp w: rows 16w..16w+15,
 //           whole 2 KiB rows, 512 contiguous bytes per load instruction) into
 //           registers, convert to fp16 and store them into one resident
@@ -30,14 +34,14 @@
 // p <= 2^8 by construction, and bf16 queries of normal fp16 range convert
 // exactly.
 //
-// With more than one tile per split, warps 4-7 issue the loads of the next
+// With more than one tile in a segment, warps 4-7 issue the loads of the next
 // tile while warps 0-3 run the softmax; every warp waits for the previous
 // tile's pass 2 before it overwrites E. Every wait is bounded; on a timeout
 // the CTA records kErrTimeout, drains its MMAs, frees TMEM and returns.
 //
-// A multi-split (layer, sequence) writes (m, l, O) partials per split; a
-// second kernel merges them in split order. The split layout depends only on
-// the row count, so identical rows give identical bits whatever slots hold
+// A pair spread over several segments writes (m, l, O) partials per segment;
+// a second kernel merges them in row order. The plan depends only on the
+// configuration, so identical rows give identical bits whatever slots hold
 // them.
 #include <cmath>
 
