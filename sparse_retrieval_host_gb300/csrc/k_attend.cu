@@ -106,13 +106,9 @@ struct AttnArgs {
 // Bounded wait that also gives up when another thread has aborted the CTA.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
                                               uint32_t* err) {
-    for (uint32_t i = 0; i < (1u << 26); ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 63u && *abort) return false;
-    }
-    *abort = 1;
-    atomicOr(err, kErrTimeout);
-    return false;
+    const int r = mbar_wait_abort(bar, parity, abort);
+    if (r < 0) atomicOr(err, kErrTimeout);
+    return r > 0;
 }
 
 __device__ __forceinline__ void named_sync(int id, int n) {
@@ -480,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     if (tid == 0 && n_tiles > 0) {
         // completes once every MMA issued above has completed
         mma_commit(&ms.drain);
-        if (!mbar_wait(&ms.drain, n_drain & 1, 1u << 26)) {
+        if (!mbar_wait(&ms.drain, n_drain & 1)) {
             atomicOr(a.err, kErrTimeout);
             ok = false;
         }

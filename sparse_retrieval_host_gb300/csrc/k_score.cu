@@ -1,4 +1,7 @@
-// K-score: memory-indexer scoring + ensemble for every compressed chunk.
+// K-score: memory-indexer scoring + ensemble for every compressed chunk, with
+// mma.sync: the path for per-indexer key sets (indexer i scores its own key
+// set i; three key streams). One key set shared by the indexers runs on the
+// tensor-core stream of k_score_tc.cu.
 //
 // PocketLLM "FlashMemory 1M 上下文显存优化使用文档", section 技术细节 / 架构概览,
 // scoring box steps 1-3, and the FlashMemory-DeepSeek-V4 summary, sections
@@ -185,12 +188,15 @@ __global__ void hist_kernel(const float* __restrict__ scores, int n, uint32_t* _
 }  // namespace
 
 cudaError_t launch_score(const uint16_t* keys, int n, int B, const uint16_t* q, float scale,
-                         const float* bias3, int ensemble, float* scores, uint32_t* hist,
+                         const float* bias3, int ensemble, float* scores, uint32_t* hist, uint32_t* err,
                          int sm_count, cudaStream_t st, int key_sets, bool clear_hist) {
     if (clear_hist) {
         const cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(uint32_t) * kHistBins * B, st);
         if (e != cudaSuccess) return e;
     }
+    // one key set: the tensor-core stream (k_score_tc.cu)
+    if (key_sets == 1)
+        return launch_score_tc(keys, n, B, q, scale, bias3, ensemble, scores, hist, err, sm_count, st);
     const long long tiles = (n + 15) / 16;
     long long bx = (tiles + kScoreWarps - 1) / kScoreWarps;
     const long long cap = (2LL * sm_count + B - 1) / B;
@@ -198,12 +204,8 @@ cudaError_t launch_score(const uint16_t* keys, int n, int B, const uint16_t* q, 
     if (bx < 1) bx = 1;
     dim3 grid((unsigned)bx, (unsigned)B);
     const long long set_stride = (long long)B * n * kIdxDim;
-    if (key_sets == 3)
-        score_kernel<3><<<grid, kScoreWarps * 32, 0, st>>>(keys, set_stride, n, q, scale, bias3[0], bias3[1],
-                                                           bias3[2], ensemble, scores, hist);
-    else
-        score_kernel<1><<<grid, kScoreWarps * 32, 0, st>>>(keys, 0, n, q, scale, bias3[0], bias3[1], bias3[2],
-                                                           ensemble, scores, hist);
+    score_kernel<3><<<grid, kScoreWarps * 32, 0, st>>>(keys, set_stride, n, q, scale, bias3[0], bias3[1],
+                                                       bias3[2], ensemble, scores, hist);
     return cudaGetLastError();
 }
 

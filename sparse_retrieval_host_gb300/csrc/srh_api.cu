@@ -456,7 +456,7 @@ int score_impl(srh_ctx* ctx, const uint16_t* d_keys, int key_sets, int n, const 
     if (((uintptr_t)d_keys | (uintptr_t)d_q) & 15) return fail(ctx, SRH_ERR_INVALID, "keys/queries must be 16-byte aligned");
     if (!std::isfinite(scale)) return fail(ctx, SRH_ERR_INVALID, "scale must be finite");
     const cudaError_t e = launch_score(d_keys, n, ctx->B, d_q, scale, bias3, ensemble, d_scores, ctx->d_hist,
-                                       ctx->sm_count, (cudaStream_t)stream, key_sets, !ctx->hist_clean);
+                                       ctx->d_err, ctx->sm_count, (cudaStream_t)stream, key_sets, !ctx->hist_clean);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "fm_score launch");
     ctx->hist_clean = false;
     ctx->hist_scores = d_scores;

@@ -193,8 +193,12 @@ __device__ __forceinline__ uint32_t ordered_key(float s) {
 // `clear_hist` they zero it first (the select kernel leaves the rows it reads
 // zeroed, so a histogram consumed by a selection needs no clearing).
 cudaError_t launch_score(const uint16_t* keys, int n, int B, const uint16_t* q, float scale,
-                         const float* bias3, int ensemble, float* scores, uint32_t* hist,
+                         const float* bias3, int ensemble, float* scores, uint32_t* hist, uint32_t* err,
                          int sm_count, cudaStream_t st, int key_sets, bool clear_hist);
+// One key set on the tensor cores (TMA-streamed key tiles, tcgen05, TMEM).
+cudaError_t launch_score_tc(const uint16_t* keys, int n, int B, const uint16_t* q, float scale, const float* bias3,
+                            int ensemble, float* scores, uint32_t* hist, uint32_t* err, int sm_count,
+                            cudaStream_t st);
 cudaError_t launch_hist(const float* scores, int n, int B, uint32_t* hist, cudaStream_t st, bool clear_hist);
 cudaError_t launch_quantize_keys(const uint16_t* keys, long long total, uint8_t* codes, float* kscale,
                                  int sm_count, cudaStream_t st);

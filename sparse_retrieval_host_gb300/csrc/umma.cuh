@@ -66,11 +66,42 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait: gives up after `limit` polls and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit = (1u << 22)) {
-    for (uint32_t i = 0; i < limit; ++i)
+// Nanoseconds of the GPU's global timer.
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+// Wall-clock limit of every device wait: far above any legitimate wait (a
+// poll of try_wait may itself suspend the thread, so a poll count is no bound).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+
+// Bounded wait: gives up after `limit_ns` nanoseconds and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-    return false;
+        if ((i & 63u) == 0 && global_ns() - t0 > limit_ns) return false;
+    }
+}
+// Bounded wait that also leaves when another thread of the CTA sets *abort.
+// Returns 1 when the phase completed, 0 when another thread aborted, -1 on a
+// timeout (after which *abort is set, so the CTA's other waits leave too).
+__device__ __forceinline__ int mbar_wait_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait(bar, parity)) return 1;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return 1;
+        if ((i & 63u) == 0) {
+            if (*abort) return 0;
+            if (global_ns() - t0 > limit_ns) {
+                *abort = 1;
+                return -1;
+            }
+        }
+    }
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
@@ -175,6 +206,18 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// TMA tile load of a 3-D tensor: the box at (x, y, z) (x innermost, in elements;
+// x times the element size a multiple of 16 bytes) into shared memory at `dst`,
+// laid out as the tensor map's swizzle says; elements outside the tensor read as
+// zero. `map` points to a CUtensorMap in kernel-parameter (grid-constant) memory.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
 }
 
