@@ -272,6 +272,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         if (tid == 0) ms.rescale = 0;
         __syncthreads();
     }
+    const int32_t* ph = a.phys + lb * a.S;
+    // the slot of this thread's row of the first tile, loaded beside the count
+    // (a slot past the count is never used)
+    int ph0 = -1;
+    {
+        const int rr = sg.tile0 * kTileRows + tid - kWindow;
+        if (tid < kTileRows && rr >= 0 && rr < a.S) ph0 = ph[rr];
+    }
     int cnt = a.count_l[lb];
     if (cnt < 0 || cnt > a.S) {
         if (tid == 0) atomicOr(a.err, kErrBounds);
@@ -281,7 +289,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     const int row0 = sg.tile0 * kTileRows;
     const int row1 = min(R, sg.tile1 * kTileRows);
     const int n_tiles = row1 > row0 ? (row1 - row0 + kTileRows - 1) / kTileRows : 0;
-    const int32_t* ph = a.phys + lb * a.S;
 
     // Source of tile row tr: window rows first, then the staged rows in list
     // order; rows past the split end repeat its last row (finite data that the
@@ -299,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     // Ask L2 for the rows of the tile at tr0: one 2 KiB bulk prefetch per row,
     // issued by threads 0-127. It holds no registers or shared memory, so the
     // whole tile is requested from HBM at once and the loads below find it in L2.
-    auto prefetch_tile = [&](int tr0) {
+    // `first`: the segment's first tile, whose slots are already in ph0.
+    auto prefetch_tile = [&](int tr0, bool first) {
         const int row = tr0 + tid;
         if (tid >= kTileRows || row >= row1) return;
         if (si == sb && row < kWindow) return;             // requested before the wait
@@ -307,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         if (row < kWindow) {
             p = a.window + (lb * kWindow + row) * kKvDim;
         } else {
-            const int slot = ph[row - kWindow] - kWindow;
+            const int slot = (first ? ph0 : ph[row - kWindow]) - kWindow;
             if (slot < 0 || slot >= a.G) return;            // reported by the loads
             p = a.staging + (lb * (size_t)a.G + slot) * kKvDim;
         }
@@ -323,11 +331,11 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         }
     };
 
-    if (n_tiles > 0) prefetch_tile(row0);
+    if (n_tiles > 0) prefetch_tile(row0, true);
     for (int tile = 0; tile < n_tiles; ++tile) {
         // ------------------------------------------------------------ load E (all warps)
         const int tr0 = row0 + tile * kTileRows;
-        if (tile + 1 < n_tiles) prefetch_tile(tr0 + kTileRows);   // the next tile's rows, during this one
+        if (tile + 1 < n_tiles) prefetch_tile(tr0 + kTileRows, false);   // the next tile's rows, during this one
         float4 b0[4][4], b1[4][4];
         if (ok) {
             load4(b0, tr0, rw);
@@ -543,56 +551,89 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
 // i owns float4 i of the head's 512 values):
 //     o_h = sum_s w_s O_s[h] / sum_s w_s l_s,   w_s = 2^(m_s - max_s m_s),
 // over the splits with l_s > 0, in split order. A split with l_s = 0 (no rows,
-// or a failed CTA) wrote zeros and gets weight 0.
+// or a failed CTA) wrote zeros and gets weight 0. Every thread loads the
+// splits' statistics itself, together with its values of the first splits, so
+// the merge costs one round of loads and no barrier.
+// L2 loads of data an earlier kernel wrote: volatile with a memory clobber, so
+// the compiler keeps them after pdl_wait().
+__device__ __forceinline__ float ld_dep(const float* p) {
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];\n" : "=f"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 ld_dep4(const float4* p) {
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
 template <int H>
 __global__ void __launch_bounds__(kKvDim / 4) merge_kernel(const MergeItem* __restrict__ merges, int merge0,
-                                                           const float* __restrict__ part_o,
-                                                           const float* __restrict__ part_ml,
+                                                           const float* part_o, const float* part_ml,
                                                            float* __restrict__ out) {
-    __shared__ float m_s[kMaxSplits], l_s[kMaxSplits], w_s[kMaxSplits];
-    pdl_wait();   // the partials come from the attention kernel
-    const MergeItem mi = merges[merge0 + blockIdx.x];
+    constexpr int kFirst = 5;   // splits loaded in the first round (a 640-row pair has 5)
+    const MergeItem mi = merges[merge0 + blockIdx.x];   // the plan: written once, at creation
     const int h = blockIdx.y;
     const int ns = min(mi.ns, kMaxSplits);
     const int t = threadIdx.x;
-    if (t < ns) {
-        const float* ml = part_ml + (size_t)(mi.first + t) * 2 * H;
-        m_s[t] = __ldcg(&ml[h]);
-        l_s[t] = __ldcg(&ml[H + h]);
-    }
-    __syncthreads();
-    if (t == 0) {
-        float M = -INFINITY;
-        for (int s = 0; s < ns; ++s)
-            if (l_s[s] > 0.f) M = fmaxf(M, m_s[s]);
-        float L = 0.f;
-        for (int s = 0; s < ns; ++s) {
-            const float w = l_s[s] > 0.f ? exp2f(m_s[s] - M) : 0.f;
-            w_s[s] = w;
-            L += w * l_s[s];
-        }
-        const float inv = 1.f / L;
-        for (int s = 0; s < ns; ++s) w_s[s] *= inv;
-    }
-    __syncthreads();
+    const float* ml = part_ml + (size_t)mi.first * 2 * H;
     const float4* src = reinterpret_cast<const float4*>(part_o + ((size_t)mi.first * H + h) * kKvDim) + t;
     const size_t split_stride = (size_t)H * kKvDim / 4;   // float4s between consecutive splits
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < ns; s0 += 8) {
-        float4 v[8];
+    pdl_wait();   // the partials come from the attention kernel
+    float4 v[kFirst];
+    float mv[kFirst], lv[kFirst];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (s0 + j < ns) v[j] = __ldcg(src + (size_t)(s0 + j) * split_stride);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (s0 + j < ns) {
-                const float w = w_s[s0 + j];
-                acc.x += w * v[j].x;
-                acc.y += w * v[j].y;
-                acc.z += w * v[j].z;
-                acc.w += w * v[j].w;
-            }
+    for (int j = 0; j < kFirst; ++j) {
+        if (j < ns) {
+            v[j] = ld_dep4(src + (size_t)j * split_stride);
+            mv[j] = ld_dep(&ml[(size_t)j * 2 * H + h]);
+            lv[j] = ld_dep(&ml[(size_t)j * 2 * H + H + h]);
         }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kFirst; ++j)
+        if (j < ns && lv[j] > 0.f) M = fmaxf(M, mv[j]);
+    for (int s = kFirst; s < ns; ++s) {
+        const float ls = ld_dep(&ml[(size_t)s * 2 * H + H + h]);
+        if (ls > 0.f) M = fmaxf(M, ld_dep(&ml[(size_t)s * 2 * H + h]));
+    }
+    float L = 0.f;
+#pragma unroll
+    for (int j = 0; j < kFirst; ++j) {
+        if (j < ns) {
+            mv[j] = lv[j] > 0.f ? exp2f(mv[j] - M) : 0.f;   // the weight w_j
+            L += mv[j] * lv[j];
+        }
+    }
+    for (int s = kFirst; s < ns; ++s) {
+        const float ls = ld_dep(&ml[(size_t)s * 2 * H + H + h]);
+        const float w = ls > 0.f ? exp2f(ld_dep(&ml[(size_t)s * 2 * H + h]) - M) : 0.f;
+        L += w * ls;
+    }
+    const float inv = 1.f / L;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < kFirst; ++j) {
+        if (j < ns) {
+            const float w = mv[j] * inv;
+            acc.x += w * v[j].x;
+            acc.y += w * v[j].y;
+            acc.z += w * v[j].z;
+            acc.w += w * v[j].w;
+        }
+    }
+    for (int s = kFirst; s < ns; ++s) {
+        const float ls = ld_dep(&ml[(size_t)s * 2 * H + H + h]);
+        const float w = (ls > 0.f ? exp2f(ld_dep(&ml[(size_t)s * 2 * H + h]) - M) : 0.f) * inv;
+        const float4 x = ld_dep4(src + (size_t)s * split_stride);
+        acc.x += w * x.x;
+        acc.y += w * x.y;
+        acc.z += w * x.z;
+        acc.w += w * x.w;
     }
     reinterpret_cast<float4*>(out + ((size_t)mi.lb * H + h) * kKvDim)[t] = acc;
 }
@@ -600,13 +641,6 @@ __global__ void __launch_bounds__(kKvDim / 4) merge_kernel(const MergeItem* __re
 template <int H>
 cudaError_t launch_h(const AttnArgs& args, int n_ctas, const MergeItem* merges, int n_merges,
                      cudaStream_t st, bool chained) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
     cudaError_t e = launch_k(attend_tc_kernel<H>, dim3(n_ctas), dim3(kThreads), kSmemBytes, st, chained, args);
     if (e != cudaSuccess || n_merges <= 0) return e;
     // the merge follows its own attention kernel: always chained
@@ -617,6 +651,15 @@ cudaError_t launch_h(const AttnArgs& args, int n_ctas, const MergeItem* merges, 
 }  // namespace
 
 int attend_max_splits() { return kMaxSplits; }
+
+cudaError_t set_attend_attrs() {
+    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(attend_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(attend_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    return e;
+}
 
 cudaError_t launch_attend(const AttnSeg* segs, const int* cta_begin, int n_ctas, const MergeItem* merges,
                           int n_merges, int n_heads, int B, int G, int S, const uint16_t* q, const float* window,

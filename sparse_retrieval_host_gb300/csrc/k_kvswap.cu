@@ -96,7 +96,7 @@ struct LruShared {
 
 __global__ void __launch_bounds__(kLruThreads)
 lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int src_ratio, int dedup_tbl,
-           const int32_t* __restrict__ sel, const int32_t* __restrict__ count,
+           const int32_t* sel, const int32_t* count,
            int32_t* __restrict__ phys, int32_t* __restrict__ count_l, int2* __restrict__ miss,
            int* __restrict__ miss_count, unsigned long long* __restrict__ stats,
            uint32_t* __restrict__ err, AdaptParams ap) {
@@ -115,7 +115,8 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
     int* victim = nh + G;        // [G]
     int* flag = victim + G;      // [G]
     int* ready = flag + G;       // [S] host_ready of each listed chunk
-    int* first = ready + S;      // [dedup_tbl]: first list position of each mapped chunk
+    int* sls = ready + S;        // [G] chunk held by each slot before this step
+    int* first = sls + G;        // [dedup_tbl]: first list position of each mapped chunk
 
     const int tid = threadIdx.x;
     const int l = l0 + blockIdx.x / B;
@@ -127,14 +128,17 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
     int* lru = ld.swap ? ld.lru_order + (size_t)b * G : nullptr;   // swap layers only
     AdaptState* as = ld.swap ? ld.adapt + b : nullptr;
     pdl_trigger();                     // the gather kernel may launch (it waits for this one)
+    // shared state that needs no input: set while the earlier kernels finish
+    for (int q = tid; q < G; q += blockDim.x) hit_time[q] = INT_MAX;
+    __syncthreads();
     pdl_wait();                        // the selection comes from earlier kernels
 
     // One round of independent loads: the count, the whole selection row
     // (entries past the count are ignored) and, for a swapped layer, its
-    // capacity state and LRU order. Thread t holds entries t + k * 1024.
+    // capacity state, LRU order and slot contents. Thread t holds entries t + k * 1024.
     constexpr int kPer = kMaxGpuChunks / kLruThreads;
     static_assert(kMaxSelect <= kMaxGpuChunks, "selection entries per thread");
-    int selv[kPer], lruv[kPer];
+    int selv[kPer], lruv[kPer], slv[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
         const int p = tid + k * kLruThreads;
@@ -144,13 +148,23 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
     if (ld.swap) {
         g0 = as->g;
         g = as->g_next;
+        const int* slg = ld.slot_logical + (size_t)b * G;
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
             const int q = tid + k * kLruThreads;
             lruv[k] = q < G ? lru[q] : 0;
+            slv[k] = q < G ? slg[q] : -1;
         }
     }
     int m0 = count[b];
+    if (ld.swap) {
+        // visible to every thread after the barrier of step 1
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int q = tid + k * kLruThreads;
+            if (q < G) sls[q] = slv[k];
+        }
+    }
 
     // ---- 1. the layer's ordered chunk list: c -> floor(c * src_ratio / ratio), first kept
     if (m0 < 0 || m0 > S) {
@@ -238,9 +252,10 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
         const int add = g - g0;
         for (int q = tid; q < add; q += blockDim.x) {
             const int s = g0 + q;
-            const int c = slot_logical[s];
+            const int c = sls[s];
             if (c >= 0 && c < cap && slot_of[c] == s) slot_of[c] = -1;
             slot_logical[s] = -1;
+            sls[s] = -1;
             queue[q] = s;
         }
 #pragma unroll
@@ -278,7 +293,7 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
             if (s < g) {
                 queue[nh[q]] = s;
             } else {
-                const int c = slot_logical[s];
+                const int c = sls[s];
                 if (c >= 0 && c < cap && slot_of[c] == s) slot_of[c] = -1;
                 slot_logical[s] = -1;
             }
@@ -302,7 +317,7 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
     // allow_topk_reduction or a small adaptive range): it keeps the first g
     if (m > g) m = g;
 
-    // ---- 2b. resident lookups and the LRU queue
+    // ---- 2b. resident lookups (hit_time was set to INT_MAX before the wait)
     for (int p = tid; p < m; p += blockDim.x) {
         const int c = r[p];
         int s = slot_of[c];
@@ -312,44 +327,65 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
             s = -1;
         }
         init_slot[p] = s;
+        if (s >= 0) hit_time[s] = p;
     }
-    for (int q = tid; q < g; q += blockDim.x) hit_time[q] = INT_MAX;
-    __syncthreads();
     for (int q = tid; q < g; q += blockDim.x) qpos[queue[q]] = q;
-    for (int p = tid; p < m; p += blockDim.x)
-        if (init_slot[p] >= 0) hit_time[init_slot[p]] = p;
     if (tid == 0) sh.conflict = 0;
     __syncthreads();
 
-    // ---- 3. optimistic two-phase assignment
-    for (int q = tid; q < g; q += blockDim.x) nh[q] = hit_time[queue[q]] == INT_MAX ? 1 : 0;
-    for (int p = tid; p < m; p += blockDim.x) {
-        is_miss[p] = init_slot[p] < 0 ? 1 : 0;
-        mr[p] = is_miss[p];
-    }
+    // ---- 3. optimistic assignment: hits keep their slots, the i-th miss takes
+    // the i-th non-hit slot in LRU order. One scan ranks both: the non-hit slots
+    // (high 16 bits) and the misses (low 16 bits); both counts are <= 4096.
+    const int nk = max(g, m);
+    for (int i = tid; i < nk; i += blockDim.x)
+        nh[i] = ((i < g && hit_time[queue[i]] == INT_MAX) ? (1 << 16) : 0) | ((i < m && init_slot[i] < 0) ? 1 : 0);
     __syncthreads();
-    block_scan_excl_array(nh, g, sh.warp_buf);
-    const int nmiss0 = block_scan_excl_array(mr, m, sh.warp_buf);
-    for (int p = tid; p < m; p += blockDim.x)
-        if (is_miss[p]) tk[mr[p]] = p;
+    const int both = block_scan_excl_array(nh, nk, sh.warp_buf);
+    const int nmiss0 = both & 0xffff;
     for (int q = tid; q < g; q += blockDim.x)
-        if (hit_time[queue[q]] == INT_MAX) victim[nh[q]] = queue[q];
+        if (hit_time[queue[q]] == INT_MAX) victim[nh[q] >> 16] = queue[q];
+    for (int p = tid; p < m; p += blockDim.x)
+        if (init_slot[p] < 0) tk[nh[p] & 0xffff] = p;
     __syncthreads();
     // a hit slot j lying before the kj-th non-hit slot is reached by that pop if
     // the pop happens before j is touched: the sequential list would take j
     for (int p = tid; p < m; p += blockDim.x) {
         const int j = init_slot[p];
         if (j >= 0) {
-            const int kj = nh[qpos[j]];
+            const int kj = nh[qpos[j]] >> 16;
             if (kj < nmiss0 && tk[kj] < p) sh.conflict = 1;
         }
     }
     __syncthreads();
+    int nmiss;
+    int2* miss_lb = miss + lb * S;
     if (!sh.conflict) {
-        for (int p = tid; p < m; p += blockDim.x)
-            assign[p] = init_slot[p] >= 0 ? init_slot[p] : victim[mr[p]];
-        if (tid == 0) sh.nmiss = nmiss0;
-        __syncthreads();
+        nmiss = nmiss0;
+        // ---- 4+5 (no conflict). The victims are the first nmiss non-hit slots,
+        // so the untouched slots are the other non-hit ones, in their old order;
+        // the touched slots follow by list position. A victim's old chunk is not
+        // listed (it would have been a hit), so clearing it never meets a new entry.
+        for (int q = tid; q < g; q += blockDim.x) {
+            const int s = queue[q];
+            const int k = nh[q] >> 16;
+            if (hit_time[s] == INT_MAX && k >= nmiss) lru[k - nmiss] = s;
+        }
+        for (int p = tid; p < m; p += blockDim.x) {
+            int s = init_slot[p];
+            if (s < 0) {
+                const int i = nh[p] & 0xffff;
+                s = victim[i];
+                const int c = r[p];
+                const int old = sls[s];
+                if (old >= 0 && old < cap) slot_of[old] = -1;
+                slot_of[c] = s;
+                slot_logical[s] = c;
+                miss_lb[i] = make_int2(c, s);
+                if (!ready[p]) atomicOr(err, kErrNotStored);
+            }
+            phys_lb[p] = kWindow + s;
+            lru[g - m + p] = s;
+        }
     } else {
         // replay the list one id at a time (flag: 0 untouched, 1 hit, 2 refilled)
         for (int q = tid; q < g; q += blockDim.x) flag[q] = 0;
@@ -374,41 +410,40 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
             sh.nmiss = nm;
         }
         __syncthreads();
+        nmiss = sh.nmiss;
         for (int p = tid; p < m; p += blockDim.x) mr[p] = is_miss[p];
         __syncthreads();
         block_scan_excl_array(mr, m, sh.warp_buf);
-    }
-    const int nmiss = sh.nmiss;
 
-    // ---- 4. new LRU order: untouched slots in old order, then touched ones by position
-    for (int q = tid; q < g; q += blockDim.x) flag[q] = 0;
-    __syncthreads();
-    for (int p = tid; p < m; p += blockDim.x) flag[assign[p]] = 1;
-    __syncthreads();
-    for (int q = tid; q < g; q += blockDim.x) nh[q] = flag[queue[q]] ? 0 : 1;
-    __syncthreads();
-    block_scan_excl_array(nh, g, sh.warp_buf);
-    for (int q = tid; q < g; q += blockDim.x)
-        if (!flag[queue[q]]) lru[nh[q]] = queue[q];
-    for (int p = tid; p < m; p += blockDim.x) lru[g - m + p] = assign[p];
+        // ---- 4. new LRU order: untouched slots in old order, then touched ones by position
+        for (int q = tid; q < g; q += blockDim.x) flag[q] = 0;
+        __syncthreads();
+        for (int p = tid; p < m; p += blockDim.x) flag[assign[p]] = 1;
+        __syncthreads();
+        for (int q = tid; q < g; q += blockDim.x) nh[q] = flag[queue[q]] ? 0 : 1;
+        __syncthreads();
+        block_scan_excl_array(nh, g, sh.warp_buf);
+        for (int q = tid; q < g; q += blockDim.x)
+            if (!flag[queue[q]]) lru[nh[q]] = queue[q];
+        for (int p = tid; p < m; p += blockDim.x) lru[g - m + p] = assign[p];
 
-    // ---- 5. slot maps: clear evicted chunks first, then record the new ones
-    for (int p = tid; p < m; p += blockDim.x)
-        if (is_miss[p]) {
-            const int old = slot_logical[assign[p]];
-            if (old >= 0 && old < cap) slot_of[old] = -1;
-        }
-    __syncthreads();
-    int2* miss_lb = miss + lb * S;
-    for (int p = tid; p < m; p += blockDim.x) {
-        const int s = assign[p];
-        phys_lb[p] = kWindow + s;
-        if (is_miss[p]) {
-            const int c = r[p];
-            slot_of[c] = s;
-            slot_logical[s] = c;
-            miss_lb[mr[p]] = make_int2(c, s);
-            if (!ready[p]) atomicOr(err, kErrNotStored);
+        // ---- 5. slot maps: clear evicted chunks first, then record the new ones
+        for (int p = tid; p < m; p += blockDim.x)
+            if (is_miss[p]) {
+                const int old = sls[assign[p]];
+                if (old >= 0 && old < cap) slot_of[old] = -1;
+            }
+        __syncthreads();
+        for (int p = tid; p < m; p += blockDim.x) {
+            const int s = assign[p];
+            phys_lb[p] = kWindow + s;
+            if (is_miss[p]) {
+                const int c = r[p];
+                slot_of[c] = s;
+                slot_logical[s] = c;
+                miss_lb[mr[p]] = make_int2(c, s);
+                if (!ready[p]) atomicOr(err, kErrNotStored);
+            }
         }
     }
     if (tid == 0) {
@@ -447,7 +482,7 @@ constexpr int kGatherWarps = 8;
 
 __global__ void __launch_bounds__(kGatherWarps * 32)
 gather_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S,
-              const int2* __restrict__ miss, const int* __restrict__ miss_count,
+              const int2* miss, const int* miss_count,
               float* __restrict__ staging, uint32_t* __restrict__ err) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
@@ -529,8 +564,12 @@ __global__ void touch_kernel(const float* __restrict__ p, long long n_pages, uin
 }
 }  // namespace
 
+cudaError_t set_lru_attrs() {
+    return cudaFuncSetAttribute(lru_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+}
+
 size_t lru_smem_bytes(int S, int G) {
-    return sizeof(LruShared) + sizeof(int) * (7 * (size_t)S + 6 * (size_t)G);
+    return sizeof(LruShared) + sizeof(int) * (7 * (size_t)S + 7 * (size_t)G);
 }
 
 cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int S, int src_ratio,
@@ -544,12 +583,7 @@ cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int
     if (max_dedup_cap > 0 &&
         lru_smem_bytes(S, G) + sizeof(int) * (size_t)max_dedup_cap <= 227 * 1024)
         tbl = (int)max_dedup_cap;
-    const size_t smem = lru_smem_bytes(S, G) + sizeof(int) * (size_t)tbl;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(lru_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-    }
+    const size_t smem = lru_smem_bytes(S, G) + sizeof(int) * (size_t)tbl;   // <= 227 KB (set_lru_attrs)
     return launch_k(lru_kernel, dim3(nl * B), dim3(kLruThreads), smem, st, chained, layers, l0, B, G, S, src_ratio,
                     tbl, sel, count, phys, count_l, miss, miss_count, stats, err, ap);
 }

@@ -256,16 +256,13 @@ bool encode_rows(CUtensorMap* m, const void* base, long long dim1, long long dim
 
 }  // namespace
 
+cudaError_t set_score_tc_attrs() {
+    return cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
+}
+
 cudaError_t launch_score_tc(const uint16_t* keys, int n, int B, const uint16_t* q, float scale, const float* bias3,
                             int ensemble, float* scores, uint32_t* hist, uint32_t* err, int sm_count,
                             cudaStream_t st) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
     CUtensorMap kmap, qmap;
     if (!encode_rows(&kmap, keys, n, B, kTile) || !encode_rows(&qmap, q, kIdx * kIdxHeads, B, kN))
         return cudaErrorNotSupported;

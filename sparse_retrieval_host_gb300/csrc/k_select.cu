@@ -152,9 +152,9 @@ struct Src {
 };
 
 __global__ void __launch_bounds__(kSelThreads)
-select_kernel(const float* __restrict__ scores, int n, int mode, int k, float thresh, int clamp,
-              int S, uint32_t* __restrict__ hist_in, const unsigned long long* __restrict__ cand_in,
-              int* __restrict__ cand_cnt, int cand_cap, int32_t* __restrict__ sel,
+select_kernel(const float* scores, int n, int mode, int k, float thresh, int clamp,
+              int S, uint32_t* hist_in, const unsigned long long* cand_in,
+              int* cand_cnt, int cand_cap, int32_t* __restrict__ sel,
               int32_t* __restrict__ count) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
@@ -398,8 +398,8 @@ select_kernel(const float* __restrict__ scores, int n, int mode, int k, float th
 // count keeps growing past the capacity so the select kernel can tell an
 // overflow.
 __global__ void __launch_bounds__(kCollectThreads)
-collect_kernel(const float* __restrict__ scores, int n, int mode, int K, float thresh,
-               const uint32_t* __restrict__ hist_in, unsigned long long* __restrict__ cand,
+collect_kernel(const float* scores, int n, int mode, int K, float thresh,
+               const uint32_t* hist_in, unsigned long long* __restrict__ cand,
                int* __restrict__ cand_cnt, int cap) {
     __shared__ int warp_buf[32];
     __shared__ int cut_s, base_s, total_s;
@@ -474,18 +474,16 @@ cudaError_t launch_select(const float* scores, int n, int B, int mode, int k, fl
                           cudaStream_t st, const unsigned long long* cand, int* cand_cnt, int cand_cap,
                           bool chained) {
     const size_t smem = sizeof(SelShared) + sizeof(unsigned long long) * kArr;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
     return launch_k(select_kernel, dim3(B), dim3(kSelThreads), smem, st, chained, scores, n, mode, k, thresh, clamp, S,
                     hist, cand, cand_cnt, cand_cap, sel, count);
 }
 
 int select_cand_cap() { return kCandCap; }
+
+cudaError_t set_select_attrs() {
+    return cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)(sizeof(SelShared) + sizeof(unsigned long long) * kArr));
+}
 
 cudaError_t launch_collect(const float* scores, int n, int B, int mode, int K, float thresh,
                            const uint32_t* hist, unsigned long long* cand, int* cand_cnt, int cap,

@@ -291,6 +291,11 @@ int srh_create(const srh_config* cfg, srh_ctx** out) {
     if (e != cudaSuccess) return bail(SRH_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
     e = cudaDeviceGetAttribute(&ctx->sm_count, cudaDevAttrMultiProcessorCount, ctx->device);
     if (e != cudaSuccess) return bail(SRH_ERR_CUDA, cudaGetErrorString(e));
+    e = set_select_attrs();
+    if (e == cudaSuccess) e = set_lru_attrs();
+    if (e == cudaSuccess) e = set_attend_attrs();
+    if (e == cudaSuccess) e = set_score_tc_attrs();
+    if (e != cudaSuccess) return bail(SRH_ERR_CUDA, std::string("kernel attributes: ") + cudaGetErrorString(e));
 
     const int B = ctx->B, G = ctx->G;
     ctx->h_layers.resize(ctx->L);

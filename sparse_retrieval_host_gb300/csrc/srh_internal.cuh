@@ -236,6 +236,16 @@ cudaError_t launch_attend(const AttnSeg* segs, const int* cta_begin, int n_ctas,
 size_t lru_smem_bytes(int S, int G);
 int attend_max_splits();
 
+// Shared-memory limits of the kernels that need more than the default 48 KB,
+// set on the current device once, outside any launch sequence: changing a
+// kernel's limit between two chained launches let the second start before the
+// first had finished (seen with the resolve kernel). srh_create sets all of
+// them; fm_select_noalloc sets the select kernel's in its per-device set-up.
+cudaError_t set_select_attrs();
+cudaError_t set_lru_attrs();
+cudaError_t set_attend_attrs();
+cudaError_t set_score_tc_attrs();
+
 }  // namespace srh
 
 struct srh_ctx : public srh::Ctx {};

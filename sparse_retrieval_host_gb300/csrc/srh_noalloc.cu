@@ -66,6 +66,12 @@ uint32_t* scratch_on_current_device(char* err, size_t err_len, int* code) {
                            dev, cudaGetErrorString(e));
             return nullptr;
         }
+        e = srh::set_select_attrs();
+        if (e != cudaSuccess) {
+            *code = report(err, err_len, SRH_ERR_CUDA, "fm_select_noalloc: kernel attributes on device %d: %s", dev,
+                           cudaGetErrorString(e));
+            return nullptr;
+        }
         g_hist_dev[dev] = static_cast<uint32_t*>(p);
     }
     return g_hist_dev[dev];
