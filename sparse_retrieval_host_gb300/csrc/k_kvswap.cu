@@ -30,6 +30,8 @@ namespace srh {
 namespace {
 
 constexpr int kLruThreads = 1024;
+constexpr long long kPrefetchCap = 1 << 16;   // slot maps of at most this many chunks are prefetched whole
+constexpr uintptr_t kPrefetchChunk = 1 << 14;  // bytes per bulk prefetch
 
 // Inclusive block scan of one int per thread; *total receives the block total.
 // Two barriers; warp_buf must not be written again before the caller's next
@@ -128,8 +130,35 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
     int* lru = ld.swap ? ld.lru_order + (size_t)b * G : nullptr;   // swap layers only
     AdaptState* as = ld.swap ? ld.adapt + b : nullptr;
     pdl_trigger();                     // the gather kernel may launch (it waits for this one)
-    // shared state that needs no input: set while the earlier kernels finish
+    // While the earlier kernels finish: shared state that needs no input, and
+    // L2 prefetches of this layer's tables (a prefetch reads nothing into the
+    // kernel, so it is safe whoever writes the tables; the loads after the wait
+    // then find them in L2). slot_of is prefetched only when it is small.
     for (int q = tid; q < G; q += blockDim.x) hit_time[q] = INT_MAX;
+    if (ld.swap && tid < 4) {
+        const void* base = nullptr;
+        long long bytes = 0;
+        if (tid == 0) {
+            base = lru;
+            bytes = 4LL * G;
+        } else if (tid == 1) {
+            base = ld.slot_logical + (size_t)b * G;
+            bytes = 4LL * G;
+        } else if (tid == 2 && cap <= kPrefetchCap) {
+            base = ld.slot_of + (size_t)b * cap;
+            bytes = 4LL * cap;
+        } else if (tid == 3 && cap <= kPrefetchCap) {
+            base = ld.host_ready + (size_t)b * cap;
+            bytes = cap;
+        }
+        // whole 16-byte units inside the range, from its first 16-byte boundary
+        const uintptr_t a0 = ((uintptr_t)base + 15) & ~(uintptr_t)15;
+        const uintptr_t a1 = ((uintptr_t)base + (uintptr_t)bytes) & ~(uintptr_t)15;
+        for (uintptr_t a = a0; base && a < a1; a += kPrefetchChunk) {
+            const uint32_t len = (uint32_t)min((uintptr_t)kPrefetchChunk, a1 - a);
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(a), "r"(len) : "memory");
+        }
+    }
     __syncthreads();
     pdl_wait();                        // the selection comes from earlier kernels
 
