@@ -1,7 +1,8 @@
 // K-score: memory-indexer scoring + ensemble for every compressed chunk, with
 // mma.sync: the path for per-indexer key sets (indexer i scores its own key
-// set i; three key streams). One key set shared by the indexers runs on the
-// tensor-core stream of k_score_tc.cu.
+// set i; three key streams) and for one key set below kTcMinChunks chunks per
+// call. Longer single-set streams run on the tensor-core kernel of
+// k_score_tc.cu.
 //
 // PocketLLM "FlashMemory 1M 上下文显存优化使用文档", section 技术细节 / 架构概览,
 // scoring box steps 1-3, and the FlashMemory-DeepSeek-V4 summary, sections
@@ -194,8 +195,11 @@ cudaError_t launch_score(const uint16_t* keys, int n, int B, const uint16_t* q, 
         const cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(uint32_t) * kHistBins * B, st);
         if (e != cudaSuccess) return e;
     }
-    // one key set: the tensor-core stream (k_score_tc.cu)
-    if (key_sets == 1)
+    // One key set over many tiles: the tensor-core stream (k_score_tc.cu). Its
+    // fixed cost (TMEM, barriers, tensor maps) is about 1.5 us more per call than
+    // this kernel's, which its higher streaming rate repays only on long streams:
+    // measured 16.8 against 15.0 us at 2^18 chunks, 47 against 60 us at 2^20.
+    if (key_sets == 1 && (long long)B * n >= kTcMinChunks)
         return launch_score_tc(keys, n, B, q, scale, bias3, ensemble, scores, hist, err, sm_count, st);
     const long long tiles = (n + 15) / 16;
     long long bx = (tiles + kScoreWarps - 1) / kScoreWarps;
@@ -204,8 +208,12 @@ cudaError_t launch_score(const uint16_t* keys, int n, int B, const uint16_t* q, 
     if (bx < 1) bx = 1;
     dim3 grid((unsigned)bx, (unsigned)B);
     const long long set_stride = (long long)B * n * kIdxDim;
-    score_kernel<3><<<grid, kScoreWarps * 32, 0, st>>>(keys, set_stride, n, q, scale, bias3[0], bias3[1],
-                                                       bias3[2], ensemble, scores, hist);
+    if (key_sets == 3)
+        score_kernel<3><<<grid, kScoreWarps * 32, 0, st>>>(keys, set_stride, n, q, scale, bias3[0], bias3[1],
+                                                           bias3[2], ensemble, scores, hist);
+    else
+        score_kernel<1><<<grid, kScoreWarps * 32, 0, st>>>(keys, 0, n, q, scale, bias3[0], bias3[1], bias3[2],
+                                                           ensemble, scores, hist);
     return cudaGetLastError();
 }
 

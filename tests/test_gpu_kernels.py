@@ -33,7 +33,11 @@ def _w(**kw):
     _w(context_len=4 * 1001 + 3, code=51),                          # ragged tail: n = 1002
     _w(context_len=4, code=52, index_topk=1, gpu_chunks=1),         # n = 1
     _w(context_len=131072, batch=3, code=53, ensemble=C.ENSEMBLE_MEAN, bias=-7.0),
-], ids=["tiny", "ragged", "n1", "b3_mean"])
+    # 2^19 chunks in one call: the tensor-core kernel (smaller calls use the mma.sync one)
+    _w(context_len=131072, batch=16, code=61, layer_ratios=(128,)),
+    _w(context_len=4 * (4 * 32768 + 37), batch=4, code=62, layer_ratios=(128,), ensemble=C.ENSEMBLE_MEAN,
+       bias=-7.0),
+], ids=["tiny", "ragged", "n1", "b3_mean", "b16_tc", "b4_ragged_tc"])
 def test_fm_score_matches_oracle(w):
     from sparse_retrieval_host_gb300.runtime import bits_to_i16
     ds = make_ds(w, layer_ratios=(4,))
