@@ -39,8 +39,8 @@
  *     validates its arguments before it launches anything. Kernel work is
  *     asynchronous: errors found on the device (a selected chunk not yet
  *     stored, an index out of range) are recorded in a sticky device error
- *     word and reported by srh_check_error(). No kernel traps or waits
- *     without bound.
+ *     word and reported by srh_check_error(). No kernel traps; every
+ *     device-side wait gives up after 2 s (SRH_ERR_TIMEOUT).
  *   - Nothing is allocated in the per-step calls: srh_create() allocates
  *     the pinned host pools, the device slot tables and all scratch.
  *   - A context is not thread-safe; calls on one context must be issued
