@@ -410,9 +410,22 @@ int srh_get_stats(srh_ctx* ctx, srh_stats* out);
 int srh_reset_stats(srh_ctx* ctx);
 
 /* Wait for the device and report the sticky device error word: SRH_OK,
- * SRH_ERR_NOT_STORED or SRH_ERR_BOUNDS (first match in that order), or
- * SRH_ERR_CUDA. The word is cleared after it is read. */
+ * SRH_ERR_NOT_STORED, SRH_ERR_BOUNDS or SRH_ERR_TIMEOUT (first match in that
+ * order), or SRH_ERR_CUDA. The word is cleared after it is read. */
 int srh_check_error(srh_ctx* ctx);
+
+/*
+ * Self-test of the device-side bounded waits (failure detection without a
+ * fault; the pages have no counterpart, their errors are host-side guards,
+ * [P1] 故障排查). Launches one CTA on `stream` that waits on an mbarrier phase
+ * nothing completes, with a limit of `limit_us` microseconds in [1, 2000000]
+ * (the kernels' own waits use 2 s); when the limit passes, the wait gives up
+ * and records the timeout in the context's sticky error word, exactly as a
+ * stuck wait in a step kernel would. The next srh_check_error() then returns
+ * SRH_ERR_TIMEOUT and the context stays usable. Asynchronous; returns SRH_OK,
+ * SRH_ERR_INVALID (NULL context, limit out of range) or SRH_ERR_CUDA.
+ */
+int srh_selftest_wait_timeout(srh_ctx* ctx, int limit_us, srh_stream_t stream);
 
 /* Static text for a return code. */
 const char* srh_error_string(int code);

@@ -111,6 +111,7 @@ SIGNATURES = [
     ("srh_get_stats", _i, [_vp, ctypes.POINTER(SrhStats)]),
     ("srh_reset_stats", _i, [_vp]),
     ("srh_check_error", _i, [_vp]),
+    ("srh_selftest_wait_timeout", _i, [_vp, _i, _vp]),
     ("srh_error_string", ctypes.c_char_p, [_i]),
     ("srh_last_error", ctypes.c_char_p, [_vp]),
 ]
@@ -302,8 +303,12 @@ def srh_reset_stats(ctx) -> None:
 
 
 def srh_check_error(ctx) -> int:
-    """Returns the code (does not raise): SRH_OK, SRH_ERR_NOT_STORED or SRH_ERR_BOUNDS."""
+    """Returns the code (does not raise): SRH_OK, SRH_ERR_NOT_STORED, SRH_ERR_BOUNDS or SRH_ERR_TIMEOUT."""
     return load().srh_check_error(ctx)
+
+
+def srh_selftest_wait_timeout(ctx, limit_us: int, stream=None) -> None:
+    _check(load().srh_selftest_wait_timeout(ctx, int(limit_us), _stream(stream)), "srh_selftest_wait_timeout", ctx)
 
 
 def srh_last_error(ctx) -> str:

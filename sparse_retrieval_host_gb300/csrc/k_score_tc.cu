@@ -256,6 +256,25 @@ bool encode_rows(CUtensorMap* m, const void* base, long long dim1, long long dim
 
 }  // namespace
 
+namespace {
+// The bounded-wait path of the kernels above, on its own: the barrier expects
+// one arrival that never comes, so mbar_wait gives up after limit_ns.
+__global__ void wait_selftest_kernel(uint32_t* err, unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0, limit_ns)) atomicOr(err, kErrTimeout);
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(uint32_t* err, unsigned long long limit_ns, cudaStream_t st) {
+    wait_selftest_kernel<<<1, 32, 0, st>>>(err, limit_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t set_score_tc_attrs() {
     return cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
 }

@@ -722,6 +722,15 @@ int srh_reset_stats(srh_ctx* ctx) {
     return SRH_OK;
 }
 
+int srh_selftest_wait_timeout(srh_ctx* ctx, int limit_us, srh_stream_t stream) {
+    if (!ctx) return SRH_ERR_INVALID;
+    if (limit_us < 1 || limit_us > 2000000) return fail(ctx, SRH_ERR_INVALID, "limit_us must be in [1, 2000000]");
+    const cudaError_t e = launch_wait_selftest(ctx->d_err, (unsigned long long)limit_us * 1000ull,
+                                               (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "srh_selftest_wait_timeout launch");
+    return SRH_OK;
+}
+
 int srh_check_error(srh_ctx* ctx) {
     if (!ctx) return SRH_ERR_INVALID;
     SRH_CUDA(ctx, cudaDeviceSynchronize());

@@ -237,6 +237,9 @@ cudaError_t launch_attend(const AttnSeg* segs, const int* cta_begin, int n_ctas,
                           float* part_o, float* part_ml, uint32_t* err, cudaStream_t st, bool chained);
 size_t lru_smem_bytes(int S, int G);
 int attend_max_splits();
+// One CTA waits (limit_ns) on an mbarrier phase nothing completes and records
+// kErrTimeout in err: the self-test of the kernels' bounded waits.
+cudaError_t launch_wait_selftest(uint32_t* err, unsigned long long limit_ns, cudaStream_t st);
 
 // Shared-memory limits of the kernels that need more than the default 48 KB,
 // set on the current device once, outside any launch sequence: changing a

@@ -92,6 +92,7 @@ def test_bad_kv_dim_is_invalid(abi):
 def test_null_context_calls_are_invalid(abi):
     lib = abi.load()
     assert lib.srh_check_error(None) == abi.SRH_ERR_INVALID
+    assert lib.srh_selftest_wait_timeout(None, 1000, None) == abi.SRH_ERR_INVALID
     assert lib.fm_score(None, None, 1, None, ctypes.c_float(1.0), None, 0, None, None) == abi.SRH_ERR_INVALID
     assert lib.lsa_attend(None, -1, None, 64, None, None, None, None, None, None) == abi.SRH_ERR_INVALID
     lib.srh_destroy(None)

@@ -260,6 +260,39 @@ def test_ties_follow_index_order():
         ds.close()
 
 
+def test_device_wait_timeout_is_reported_and_context_stays_usable():
+    """The kernels' bounded-wait path on its own: a wait that nothing completes gives
+    up after its limit (wall-clock), the host reads SRH_ERR_TIMEOUT once, and the
+    context's later steps equal, bit for bit, those of a context that never timed out."""
+    import time
+    from sparse_retrieval_host_gb300 import abi
+    w = C.TINY
+    results = []
+    for inject in (False, True):
+        ds = make_ds(w)
+        try:
+            fill(ds, w)
+            spec = spec_of(w)
+            for t in range(3):
+                load_step_inputs(ds, w, t)
+                if inject and t == 1:
+                    torch.cuda.synchronize()
+                    t0 = time.perf_counter()
+                    abi.srh_selftest_wait_timeout(ds.ctx, 20000)
+                    assert ds.check_error() == abi.SRH_ERR_TIMEOUT
+                    waited = time.perf_counter() - t0
+                    assert 0.015 <= waited < 5.0, waited
+                    assert ds.check_error() == abi.SRH_OK   # the word was cleared
+                ds.step(spec)
+                torch.cuda.synchronize()
+            assert ds.check_error() == abi.SRH_OK
+            results.append([x.clone() for x in (ds.out, ds.sel, ds.count, ds.phys, ds.count_l)])
+        finally:
+            ds.close()
+    for a, b in zip(*results):
+        assert torch.equal(a, b)
+
+
 def test_max_sizes_select_and_stage():
     """Largest supported S and G (4096) on one layer."""
     w = C.Workload(name="max", code=60, context_len=4 * 20000, layer_ratios=(4,), gpu_chunks=4096,
