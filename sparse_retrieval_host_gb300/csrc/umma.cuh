@@ -1,14 +1,15 @@
 // Thin inline-PTX wrappers for the sm_100-family tensor-core path used by the
 // kernels of this library: tcgen05 (TMEM allocation, MMA, commit, loads),
-// mbarriers with bounded waits, and shared-memory matrix descriptors.
+// mbarriers with bounded waits, TMA tile loads, and shared-memory matrix
+// descriptors.
 //
 // Shared-memory operands use the 128-byte swizzle: a matrix is stored as rows
 // of 128 bytes in which the 16-byte chunk c of row r sits at chunk c ^ (r & 7);
 // a group of 8 rows (1024 bytes, 1024-byte aligned) is one swizzle atom.
-//   * K-major operand (rows = M or N, 128 B = 32 tf32 / 64 bf16 along K): atoms
+//   * K-major operand (rows = M or N, 128 B = 64 fp16/bf16 along K): atoms
 //     stacked along M/N every 1024 B (the stride byte offset); a K step inside
 //     the 128-byte row advances the start address by its byte width.
-//   * MN-major operand (rows = K, 128 B = 32 tf32 along M/N): 8-row groups along
+//   * MN-major operand (rows = K, 128 B = 64 fp16 along M/N): 8-row groups along
 //     K every 1024 B (stride byte offset) and 128-byte-wide column blocks along
 //     M/N every `lbo` bytes (leading byte offset).
 #pragma once
@@ -36,7 +37,7 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo_byte
 }
 
 // Instruction descriptor of a dense MMA with fp32 accumulation.
-//   ab_fmt: 1 = bf16 (kind::f16), 2 = tf32 (kind::tf32)
+//   ab_fmt: 0 = fp16, 1 = bf16 (kind::f16)
 //   a_mn / b_mn: 1 if that operand is MN-major
 __device__ __forceinline__ constexpr uint32_t idesc_f32acc(int ab_fmt, int a_mn, int b_mn, int M, int N) {
     return (1u << 4)                          // D format f32
@@ -131,17 +132,8 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 }
 
 // ---------------------------------------------------------------- MMA
-// D[tmem] (+)= A[smem] * B[smem]; issued by one thread.
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n"
-        " setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// kind::f16 covers fp16 and bf16 inputs (the instruction descriptor says which).
+// D[tmem] (+)= A[smem] * B[smem], issued by one thread. kind::f16 covers fp16
+// and bf16 inputs (the instruction descriptor says which).
 __device__ __forceinline__ void mma_f16kind(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
     asm volatile(
@@ -200,15 +192,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
 }
-// Copy `bytes` (multiple of 16, both addresses 16-byte aligned) from global to
-// shared memory; completion is counted on `bar` as transaction bytes.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
 // TMA tile load of a 3-D tensor: the box at (x, y, z) (x innermost, in elements;
 // x times the element size a multiple of 16 bytes) into shared memory at `dst`,
 // laid out as the tensor map's swizzle says; elements outside the tensor read as
@@ -219,34 +202,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, int x
         "[%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
         "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
-}
-
-// TMA gather of 4 rows (row0..row3) of a 2-D tensor, columns [col, col + box)
-// of each, into consecutive rows at `dst`; `map` points to a CUtensorMap kept in
-// kernel-parameter (grid-constant) memory whose box is one row high.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, int col, int r0, int r1, int r2, int r3,
-                                            uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(dst),
-        "l"(map), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// ---------------------------------------------------------------- cp.async
-__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* gmem, int src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(saddr), "l"(gmem), "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-// Arrive on `bar` once all of this thread's earlier cp.async copies have landed,
-// without blocking the thread (the barrier's expected count is not raised).
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar)) : "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
 // Byte offset of the 16-byte chunk `c` (0..7) of row `r` inside a 128-byte-swizzled
