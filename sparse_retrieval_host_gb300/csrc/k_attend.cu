@@ -199,17 +199,18 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     if (warp == 0) tmem_alloc(&ms.tmem_base, kTmemCols);
     // queries of (layer, sequence) lb: bf16 [H][512] -> fp16 K-major; d-block d / 64
     // at (d / 64) * 8192, row h
-    auto convert_q = [&](int lbq) {
-        constexpr int kPer = H * 64 / kThreads;          // 16-byte chunks per thread
+    constexpr int kQPer = H * 64 / kThreads;             // 16-byte chunks per thread
+    auto load_q = [&](int lbq, uint4 (&qv)[kQPer]) {
         const uint16_t* qg = a.q + (size_t)lbq * H * kKvDim;
-        uint4 qv[kPer];
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) {
+        for (int k = 0; k < kQPer; ++k) {
             const int i = tid + k * kThreads;
             qv[k] = *reinterpret_cast<const uint4*>(qg + (i >> 6) * kKvDim + (i & 63) * 8);
         }
+    };
+    auto store_q = [&](const uint4 (&qv)[kQPer]) {
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) {
+        for (int k = 0; k < kQPer; ++k) {
             const int i = tid + k * kThreads, h = i >> 6, c8 = i & 63;
             const uint4 v = qv[k];
             uint4 w;
@@ -220,13 +221,24 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
             *reinterpret_cast<uint4*>(sm + kOffQ + (c8 >> 3) * 8192 + sw128(h, c8 & 7)) = w;
         }
     };
+    auto convert_q = [&](int lbq) {
+        uint4 qv[kQPer];
+        load_q(lbq, qv);
+        store_q(qv);
+    };
     int q_lb = sb < se ? a.segs[sb].lb : 0;
     // The window rows are this call's own input: the first segment's (when it
     // starts at tile 0) are requested from HBM before the dependency wait.
     if (sb < se && a.segs[sb].tile0 == 0 && tid < kWindow)
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(a.window + ((size_t)q_lb * kWindow + tid) * kKvDim),
                      "r"(kKvDim * 4) : "memory");
-    if (sb < se) convert_q(q_lb);
+    // The first pair's queries are loaded after the dependency wait (below);
+    // L2 is asked for them now.
+    constexpr int kQChunk = 16384;
+    if (sb < se && tid < H * kKvDim * 2 / kQChunk)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(
+                         reinterpret_cast<const unsigned char*>(a.q + (size_t)q_lb * H * kKvDim) + tid * kQChunk),
+                     "r"(kQChunk) : "memory");
     // the barriers, the abort flag, the softmax state and the TMEM address are
     // set: every thread sees them from here on
     tc_fence_before();
@@ -252,6 +264,18 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
 
     pdl_wait();   // slots, counts and staged rows come from earlier kernels
 
+    // The first segment's row count and first-tile slots, then its queries:
+    // all in flight together (one round trip for a CTA that starts once the
+    // earlier kernels are done, as most do: an attention CTA needs a whole SM).
+    int pre_cnt = 0, pre_ph0 = -1;
+    if (sb < se) {
+        const AttnSeg s0 = a.segs[sb];
+        const int rr = s0.tile0 * kTileRows + tid - kWindow;
+        if (tid < kTileRows && rr >= 0 && rr < a.S) pre_ph0 = a.phys[(size_t)s0.lb * a.S + rr];
+        pre_cnt = a.count_l[s0.lb];
+        convert_q(q_lb);   // read by pass 1 after the tile loop's barrier
+    }
+
     uint32_t gt0 = 0;     // tiles this CTA ran before the current segment (mbarrier phases)
     uint32_t n_drain = 0; // drains this CTA ran (phases of ms.drain)
     for (int si = sb; si < se && !*abort; ++si) {
@@ -274,13 +298,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     }
     const int32_t* ph = a.phys + lb * a.S;
     // the slot of this thread's row of the first tile, loaded beside the count
-    // (a slot past the count is never used)
-    int ph0 = -1;
-    {
+    // (a slot past the count is never used); the first segment's were loaded
+    // after the dependency wait, beside its queries
+    int ph0 = pre_ph0, cnt = pre_cnt;
+    if (si > sb) {
+        ph0 = -1;
         const int rr = sg.tile0 * kTileRows + tid - kWindow;
         if (tid < kTileRows && rr >= 0 && rr < a.S) ph0 = ph[rr];
+        cnt = a.count_l[lb];
     }
-    int cnt = a.count_l[lb];
     if (cnt < 0 || cnt > a.S) {
         if (tid == 0) atomicOr(a.err, kErrBounds);
         cnt = cnt < 0 ? 0 : a.S;
