@@ -37,6 +37,7 @@ import numpy as np  # noqa: E402
 from srh_workload import configs as C  # noqa: E402
 from srh_workload import generate as G  # noqa: E402
 
+TC_SCORE_MIN_CHUNKS = 1 << 19  # fm_score's tensor-core kernel from this many chunks per call (all sequences)
 HOLD_CYCLES = 400_000          # ~0.2 ms device-side wait before eagerly timed calls
 BASE_KERNELS = 5              # score, select, lru, gather, attend (+ merge, + candidate pass)
 COLLECT_MIN_N = 16384         # fm_select runs its candidate pass above this many chunks
@@ -196,6 +197,13 @@ def attn_bytes(w, count_l):
     """Algorithmic bytes of one lsa_attend launch: rows read + q read + out written."""
     rows = count_l.sum() + w.n_layers * w.batch * C.WINDOW
     return int(rows) * C.KV_DIM * 4 + w.n_layers * w.batch * w.n_heads * C.KV_DIM * (2 + 4)
+
+
+def scoring_kernel(w) -> str:
+    """Which fm_score kernel a call of this workload runs (one key set)."""
+    if w.batch * w.n_chunks >= TC_SCORE_MIN_CHUNKS:
+        return "score_tc_kernel (TMA + tcgen05)"
+    return "score_kernel<1> (mma.sync)"
 
 
 def launches_per_step(w, sm_count):
@@ -527,6 +535,7 @@ def run_ours(args, dist, rank, world, local):
                 "bytes": pass_bytes(w),
                 "gbs": pass_bytes(w) / ((statistics.median(sp_score) + statistics.median(sp_select)) / 1e3) / 1e9,
                 "score_kernel_gbs": score_bytes(w) / (statistics.median(sp_score) / 1e3) / 1e9,
+                "score_kernel": scoring_kernel(w),
                 "frac": pass_bytes(w) / ((statistics.median(sp_score) + statistics.median(sp_select)) / 1e3) / 1e9
                 / peak,
                 "note": "fm_score then fm_select, eager, queued behind the L2 flush; bytes = keys + score write + "
