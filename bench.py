@@ -391,7 +391,7 @@ def run_ours(args, dist, rank, world, local):
     # breakdown: the same steps as three graphs with events between the phases
     KB = min(K, 20)
     evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(KB)]
-    counts = []
+    counts, sel_counts = [], []
     for i in range(KB):
         bind(args.warmup + K + KP + i)
         flush_l2()
@@ -405,6 +405,7 @@ def run_ours(args, dist, rank, world, local):
         e3.record(stream)
         e3.synchronize()
         counts.append(ds.count_l.cpu().numpy().copy())
+        sel_counts.extend(int(c) for c in ds.count.cpu().numpy())
     assert ds.check_error() == 0, "device error during the breakdown steps"
     score_ms = [e[0].elapsed_time(e[1]) for e in evb]
 
@@ -554,6 +555,10 @@ def run_ours(args, dist, rank, world, local):
             "lru_hit_rate": (st["hits"] / sel_total) if sel_total else None,
             "staged_bytes_per_step": st["h2d_bytes"] / K,
             "selected_per_step": st["selected"] / K,
+            "selected_count": {
+                "min": min(sel_counts), "median": statistics.median(sel_counts), "max": max(sel_counts),
+                "hist": {str(c): sel_counts.count(c) for c in sorted(set(sel_counts))},
+                "note": f"fm_select's count per sequence over {KB} breakdown steps"},
             "wall_s": wall,
             "adaptive_capacity": adaptive,
             "lookahead_schedule": lookahead,
