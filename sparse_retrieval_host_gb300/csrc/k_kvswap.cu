@@ -30,7 +30,10 @@ namespace srh {
 namespace {
 
 constexpr int kLruThreads = 1024;
-constexpr long long kPrefetchCap = 1 << 16;   // slot maps of at most this many chunks are prefetched whole
+// Slot maps of at most this many chunks (32 KB) are prefetched whole; a larger
+// map would cost far more DRAM reads than its 512 or so lookups (at 128K x 32
+// sequences, 80 MB a step).
+constexpr long long kPrefetchCap = 1 << 13;
 constexpr uintptr_t kPrefetchChunk = 1 << 14;  // bytes per bulk prefetch
 
 // Inclusive block scan of one int per thread; *total receives the block total.
