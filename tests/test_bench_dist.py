@@ -44,3 +44,23 @@ def test_aggregate_two_gloo_ranks():
 def test_single_process_aggregate_is_identity():
     import bench
     assert bench.aggregate(None, 3.5, 7) == (3.5, 7)
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` (the oracle on the host cores) prints one JSON
+    line with the metric, the reference tag, its CPU baseline and a host-only e2e."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--config", "tiny",
+                        "--steps", "3", "--warmup", "1"], capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == "decode steps/s" and line["unit"] == "steps/s"
+    assert line["value"] > 0 and line["steps"] == 3 and line["higher_is_better"] is True
+    assert line["config"]["workload"] == "tiny"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "steps/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
