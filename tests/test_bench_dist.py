@@ -64,3 +64,17 @@ def test_reference_arm_prints_the_contract_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
     assert line["e2e"] == {"value": line["value"], "unit": "steps/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_bench_names_the_scoring_kernel_the_library_picks():
+    """bench.py reports which fm_score kernel a workload runs; its threshold is the
+    library's (the tensor-core kernel from kTcMinChunks chunks per call)."""
+    import re
+    import bench
+    from srh_workload import configs as C
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    txt = open(os.path.join(root, "sparse_retrieval_host_gb300", "csrc", "srh_internal.cuh")).read()
+    m = re.search(r"kTcMinChunks\s*=\s*1LL\s*<<\s*(\d+)", txt)
+    assert m and bench.TC_SCORE_MIN_CHUNKS == 1 << int(m.group(1))
+    assert "mma.sync" in bench.scoring_kernel(C.CTX8K) and "mma.sync" in bench.scoring_kernel(C.CTX1M)
+    assert "tcgen05" in bench.scoring_kernel(C.batch_sweep(16))
