@@ -220,6 +220,86 @@ def test_fp8_key_quantization_and_score():
         assert np.allclose(lg[i], want, rtol=1e-13, atol=1e-13)
 
 
+def _e4m3_exact(code: int) -> Fraction:
+    """e4m3 value as an exact rational, from the format's fields: sign, 4
+    exponent bits with bias 7, 3 mantissa bits; subnormals m * 2^-9."""
+    s, e, m = (code >> 7) & 1, (code >> 3) & 0xF, code & 0x7
+    assert (code & 0x7F) != 0x7F
+    v = Fraction(m, 512) if e == 0 else Fraction(8 + m, 8) * Fraction(2) ** (e - 7)
+    return -v if s else v
+
+
+def _rne_f32(x: Fraction) -> Fraction:
+    """Round a rational to the nearest binary32 value, ties to the even
+    significand (normal and subnormal range; no overflow in these cases)."""
+    if x == 0:
+        return Fraction(0)
+    a = abs(x)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1                                            # now 2^e <= a < 2^(e+1)
+    ulp = Fraction(2) ** (max(e, -126) - 23)
+    n, rem = divmod(a, ulp)
+    n = int(n)
+    if rem * 2 > ulp or (rem * 2 == ulp and n % 2 == 1):
+        n += 1
+    return n * ulp if x > 0 else -(n * ulp)
+
+
+def _e4m3_rne(x: Fraction) -> int:
+    """Nearest e4m3 code of a rational, ties to the even code, saturated at
+    +-448, sign kept (searched over all 127 finite magnitudes)."""
+    a = min(abs(x), Fraction(448))
+    best = min(range(0x7F), key=lambda c: (abs(_e4m3_exact(c) - a), c & 1))
+    return best | (0x80 if x < 0 else 0)
+
+
+def test_fp8_quantizer_divides_in_fp32():
+    """The codes are decided by the fp32 quotient K / kscale (the reading the
+    device kernel follows): a crafted row whose fp32 quotient lands exactly on
+    an e4m3 midpoint, where an fp64 quotient lies just above it and would give
+    the next code. Expected codes come from exact rational arithmetic: kscale =
+    rn32(amax / 448), quotient = rn32(K / kscale), code = the e4m3 value nearest
+    to it (ties to even)."""
+    row = np.zeros((1, 128), np.float32)
+    vals = [7.5, 0.001373291015625, 0.0006866455078125, 0.00034332275390625, -0.001373291015625, 0.30078125, -2.0]
+    row[0, :len(vals)] = vals
+    bits = G.f32_to_bf16_bits(row)
+    assert np.array_equal(G.bf16_bits_to_f32(bits), row)          # every value is a bf16 value
+    codes, ks = O.quantize_keys_fp8(bits)
+    kscale = _rne_f32(Fraction(7.5) / 448)
+    assert Fraction(float(ks[0])) == kscale
+    fp64_differs = 0
+    for d in range(128):
+        x = Fraction(float(row[0, d]))
+        want = _e4m3_rne(_rne_f32(x / kscale))
+        assert int(codes[0, d]) == want, (d, hex(int(codes[0, d])), hex(want))
+        fp64_differs += _e4m3_rne(Fraction(float(x) / float(kscale))) != want
+    assert int(codes[0, 1]) == 0x1A and int(codes[0, 4]) == 0x9A   # the midpoint 0.08203125 rounds to even
+    assert fp64_differs >= 3                                        # an fp64 division gives other codes here
+
+
+def test_fp8_logits_exact_against_rational_arithmetic():
+    """s_i(c) = scale * kscale_c * max_h <Q[i,h], e4m3(K8[c])> + b_i, checked
+    against exact rationals built from the code and bf16 bit fields. A dropped
+    chunk scale, a scale applied inside the max, a wrong head or indexer index,
+    or a missing bias fails it."""
+    rng = np.random.default_rng(29)
+    keys = G.f32_to_bf16_bits((rng.standard_normal((6, 128)) * rng.uniform(0.05, 20, (6, 1))).astype(np.float32))
+    codes, ks = O.quantize_keys_fp8(keys)
+    q = G.f32_to_bf16_bits(rng.standard_normal((3, 8, 128), dtype=np.float32))
+    scale, bias = 128 ** -0.5, [0.75, -3.0, 0.0]
+    lg = O.indexer_logits_fp8(codes, ks, q, scale, bias)
+    for c in range(6):
+        k = [_e4m3_exact(int(v)) for v in codes[c]]
+        for i in range(3):
+            best = max(sum(a * _bf16_exact(int(b)) for a, b in zip(k, q[i, h])) for h in range(8))
+            term = Fraction(scale) * Fraction(float(ks[c])) * best
+            exact = term + Fraction(bias[i])
+            err = abs(Fraction(float(lg[i, c])) - exact)
+            assert err <= (abs(term) + abs(Fraction(bias[i]))) * Fraction(1, 2 ** 50), (i, c)
+
+
 def test_fp8_keys_still_find_the_needles():
     w = C.TINY
     codes, ks = O.quantize_keys_fp8(G.keys(w, 0))
@@ -550,6 +630,46 @@ def test_decode_oracle_keeps_list_prefix_under_small_capacity():
     r = ora.step(lambda b: keys, lambda b: G.fm_queries(w, 0, b))
     assert len(r.lists[0][0]) == 100 and r.lists[0][0] == list(r.sel[0][:100])
     assert sorted(p - 128 for p in r.swap[0][0].phys) == list(range(100))
+
+
+def test_gpu_chunks_below_topk_keeps_the_list_head_hand_trace():
+    """GPU_CHUNKS < index_topk (rejected by default, [P1] 故障排查 error 2;
+    allowed by the reduction flag): a swapped layer stages only the first
+    GPU_CHUNKS chunks of its list. Hand-worked trace: 10 chunks whose key c is
+    (c+1)*e_0, every query head e_0 (step 0) or -e_0 (step 1), so the top-5 is
+    [9, 8, 7, 6, 5] then [0, 1, 2, 3, 4]; G = 3; layers of ratio 4 (cap 10) and
+    ratio 8 (cap 5, list c -> c // 2), both swapped."""
+    keys = np.zeros((10, 128), np.float32)
+    keys[:, 0] = np.arange(1, 11)
+    qa = np.zeros((3, 8, 128), np.float32)
+    qa[:, :, 0] = 1.0
+    kb, qpos, qneg = _bits(keys), _bits(qa), _bits(-qa)
+    ora = O.DecodeOracle(context_len=40, layer_ratios=(4, 8), gpu_chunks=3, index_topk=5, batch=1,
+                         scale=1.0, bias=[0.0] * 3, ensemble_mode=O.ENSEMBLE_MAX,
+                         select_mode=O.SELECT_TOPK, tau=0.5, clamp=5)
+    ora.mark_all_stored()
+    win = np.zeros((128, 512))
+    pool = np.arange(10 * 512, dtype=np.float64).reshape(10, 512) / 5000.0
+    qa_bits = _bits(np.ones((16, 512), np.float32))
+    rows_of = lambda l, b, idx: pool[np.asarray(idx, dtype=np.int64)] if len(idx) else np.zeros((0, 512))
+    r0 = ora.step(lambda b: kb, lambda b: qpos, lambda l, b: qa_bits, lambda l, b: win, rows_of)
+    assert list(r0.sel[0]) == [9, 8, 7, 6, 5]
+    assert r0.lists[0][0] == [9, 8, 7]                      # ratio 4: the first three of five
+    assert r0.lists[1][0] == [4, 3, 2]                      # ratio 8: [4,4,3,3,2] deduplicated, fits
+    assert r0.swap[0][0].phys == [128, 129, 130] and r0.swap[0][0].misses == [(9, 0), (8, 1), (7, 2)]
+    assert r0.swap[1][0].misses == [(4, 0), (3, 1), (2, 2)]
+    # the attention reads the window and exactly the staged chunks
+    want = O.attend(qa_bits, np.concatenate([win, pool[[9, 8, 7]]]))
+    assert np.array_equal(r0.out[(0, 0)], want)
+    r1 = ora.step(lambda b: kb, lambda b: qneg, lambda l, b: qa_bits, lambda l, b: win, rows_of)
+    assert list(r1.sel[0]) == [0, 1, 2, 3, 4]
+    assert r1.lists[0][0] == [0, 1, 2]
+    assert r1.swap[0][0].misses == [(0, 0), (1, 1), (2, 2)] and r1.swap[0][0].hits == 0
+    # ratio 8: [0,0,1,1,2] -> [0, 1, 2]; chunk 2 is still in slot 2 (a hit),
+    # 0 and 1 take the least recent slots 0 (chunk 4) and 1 (chunk 3)
+    assert r1.lists[1][0] == [0, 1, 2]
+    assert r1.swap[1][0].misses == [(0, 0), (1, 1)] and r1.swap[1][0].hits == 1
+    assert r1.swap[1][0].phys == [128, 129, 130]
 
 
 def _small_oracle(w):
