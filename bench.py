@@ -39,7 +39,7 @@ from srh_workload import generate as G  # noqa: E402
 
 TC_SCORE_MIN_CHUNKS = 1 << 19  # fm_score's tensor-core kernel from this many chunks per call (all sequences)
 HOLD_CYCLES = 400_000          # ~0.2 ms device-side wait before eagerly timed calls
-BASE_KERNELS = 5              # score, select, lru, gather, attend (+ merge, + candidate pass)
+BASE_KERNELS = 5              # score, select, lru, gather, attend (+ the candidate pass)
 COLLECT_MIN_N = 16384         # fm_select runs its candidate pass above this many chunks
 Q_CYCLE = 16                  # distinct attention-query sets cycled through the steps
 FLUSH_BYTES = 256 << 20       # > 2x the 126 MiB L2
@@ -207,26 +207,11 @@ def scoring_kernel(w) -> str:
 
 
 def launches_per_step(w, sm_count):
-    """Our kernels per step. lsa_attend adds its merge kernel when its plan
-    spreads some (layer, sequence) over more than one CTA. The rule is the
-    planner's: T tiles of 128 rows (window + min(clamp, cap) rows per pair);
-    pairs cut into chunks of ceil(T / SMs) tiles when that fits one wave, else
-    contiguous tile ranges over min(SMs, T) CTAs."""
-    tiles = [-(-(C.WINDOW + min(w.clamp, -(-w.context_len // r))) // 128) for r in w.layer_ratios] * w.batch
-    T = sum(tiles)
-    m = -(-T // sm_count)
-    if sum(-(-t // m) for t in tiles) <= sm_count:
-        merge = 1 if any(t > m for t in tiles) else 0
-    else:
-        n = min(sm_count, T)
-        bounds = {k * T // n for k in range(1, n)}
-        starts, acc = [], 0
-        for t in tiles:
-            starts.append((acc, acc + t))
-            acc += t
-        merge = 1 if any(any(a < x < b for x in bounds) for a, b in starts) else 0
-    collect = 1 if w.n_chunks > COLLECT_MIN_N else 0      # fm_select's candidate pass
-    return BASE_KERNELS + merge + collect
+    """Our kernels per step: score, select, resolve, gather and attend (the
+    attention kernel merges split pairs itself), plus fm_select's candidate
+    pass when the workload scores more than COLLECT_MIN_N chunks."""
+    collect = 1 if w.n_chunks > COLLECT_MIN_N else 0
+    return BASE_KERNELS + collect
 
 
 def adaptive_policy(w):
@@ -512,7 +497,7 @@ def run_ours(args, dist, rank, world, local):
             },
             "gpu_launches": launches_per_step(w, torch.cuda.get_device_properties(device).multi_processor_count) * K,
             "roofline": {
-                "kernel": "lsa_attend (attend_tc_kernel + merge_kernel), device time per call",
+                "kernel": "lsa_attend (attend_kernel, split pairs merged in the same kernel), device time per call",
                 "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind,
                 "traffic": traffic["dram_bytes_per_launch"] if traffic else None,

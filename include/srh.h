@@ -77,6 +77,9 @@ extern "C" {
 #define SRH_ERR_NOMEM -6       /* host or device allocation failed */
 #define SRH_ERR_BOUNDS -7      /* a device kernel met an index outside its buffer (the
                                   access was skipped); reported by srh_check_error() */
+#define SRH_ERR_RANGE -8       /* lsa_attend met a query or latent value beyond +-65504, the
+                                  finite range of its fp16 tensor-core operands; that call's
+                                  outputs are not valid; reported by srh_check_error() */
 
 #define SRH_ENSEMBLE_MAX 0     /* s = max_i s_i: OR-mode ([P1] 配置说明 ENSEMBLE=max; [P2]) */
 #define SRH_ENSEMBLE_MEAN 1    /* s = (s_0 + s_1 + s_2) / 3 */
@@ -337,6 +340,15 @@ int kvswap_stage(srh_ctx* ctx, int layer, const int32_t* d_sel, const int32_t* d
  *   d_out      [L][batch][n_heads][kv_dim] fp32 output:
  *              o_h = sum_j softmax_j(<q_h, e_j> / sqrt(kv_dim)) e_j over the 128
  *              window rows and the layer's staged rows (K = V = the latent row).
+ * Precision: the products run on the tensor cores with fp16 operands (11
+ * significant bits) and fp32 accumulation; a pair split over several CTAs is
+ * combined from fp16 partial outputs (each a softmax-weighted mean of rows).
+ * Query and latent values must lie within +-65504 (else SRH_ERR_RANGE at the
+ * next srh_check_error); values below 2^-14 (about 6.1e-5) in magnitude keep
+ * an absolute precision of 2^-25 instead of 11 significant bits.
+ * Calls on one context must not overlap in time: they share the context's
+ * partial buffers and arrival counters. Asynchronous; returns SRH_OK,
+ * SRH_ERR_INVALID or SRH_ERR_CUDA.
  */
 int lsa_attend(srh_ctx* ctx, int layer, const uint16_t* d_q, int n_heads, const float* d_window,
                const float* d_staging, const int32_t* d_phys, const int32_t* d_count_l,
@@ -410,8 +422,8 @@ int srh_get_stats(srh_ctx* ctx, srh_stats* out);
 int srh_reset_stats(srh_ctx* ctx);
 
 /* Wait for the device and report the sticky device error word: SRH_OK,
- * SRH_ERR_NOT_STORED, SRH_ERR_BOUNDS or SRH_ERR_TIMEOUT (first match in that
- * order), or SRH_ERR_CUDA. The word is cleared after it is read. */
+ * SRH_ERR_NOT_STORED, SRH_ERR_BOUNDS, SRH_ERR_TIMEOUT or SRH_ERR_RANGE (first
+ * match in that order), or SRH_ERR_CUDA. The word is cleared after it is read. */
 int srh_check_error(srh_ctx* ctx);
 
 /*

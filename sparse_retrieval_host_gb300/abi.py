@@ -24,6 +24,7 @@ SRH_ERR_CUDA = -4
 SRH_ERR_TIMEOUT = -5
 SRH_ERR_NOMEM = -6
 SRH_ERR_BOUNDS = -7
+SRH_ERR_RANGE = -8
 SRH_ENSEMBLE_MAX = 0
 SRH_ENSEMBLE_MEAN = 1
 SRH_SELECT_TOPK = 0
@@ -303,7 +304,7 @@ def srh_reset_stats(ctx) -> None:
 
 
 def srh_check_error(ctx) -> int:
-    """Returns the code (does not raise): SRH_OK, SRH_ERR_NOT_STORED, SRH_ERR_BOUNDS or SRH_ERR_TIMEOUT."""
+    """Returns the code (does not raise): SRH_OK, SRH_ERR_NOT_STORED, SRH_ERR_BOUNDS, SRH_ERR_TIMEOUT or SRH_ERR_RANGE."""
     return load().srh_check_error(ctx)
 
 

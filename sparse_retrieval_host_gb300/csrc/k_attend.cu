@@ -1,4 +1,5 @@
-// K-attend + K-merge: split-K flash-decode on the 5th-generation tensor cores.
+// K-attend: split-K flash-decode on the 5th-generation tensor cores, with the
+// split merge inside the same (cooperative) kernel.
 //
 // PocketLLM "FlashMemory 1M 上下文显存优化使用文档", section 技术细节 / 架构概览,
 // per-layer box step 3 (indexed_cached_attention over window + selected rows)
@@ -11,36 +12,46 @@
 // layer's staged rows in selection order -- form tiles of 128 rows. A static
 // plan built at context creation gives each CTA a list of segments (a range
 // of tiles of one pair): one chunk of one pair when every pair's chunks fit
-// one wave, otherwise a contiguous range of the whole call's tiles. A CTA runs
-// its segments for all heads, tile by tile. Each row is read from HBM once per
-// step; a tile's rows are requested into L2 with bulk prefetches before the
-// loads below:
-//   load    all 8 warps stream the tile's fp32 rows (warp w: rows 16w..16w+15,
-//           whole 2 KiB rows, 512 contiguous bytes per load instruction) into
-//           registers, convert to fp16 and store them into one resident
-//           128B-swizzled tile E [128 rows x 512 d] (8 d-blocks of 64);
+// one wave, otherwise a contiguous range of the whole call's tiles. Each row
+// is read from HBM once per call.
+//
+// One CTA of 32 warps per SM. A CTA's row stream is bound by the bytes it
+// keeps in flight, so every warp streams rows: warp w owns tile rows w, w+32,
+// w+64, w+96 and loads two whole 2 KiB rows at a time (512 contiguous bytes
+// per load instruction, 128 KB in flight per CTA), converts them to fp16 and
+// stores them into one resident 128B-swizzled tile E [128 rows x 512 d]
+// (8 d-blocks of 64). Rows past the segment's end are zero-filled, not loaded.
 //   pass 1  S^T[r, h] = E[r, :] . Q[h, :]   (M = 128 rows, N = heads, K = 512),
 //           E and Q K-major;
-//   softmax (warps 0-3, one TMEM lane = one row): base-2 online softmax with a
-//           lazily moved reference max per head (moved only when the tile max
-//           exceeds it by 2^8), warp butterfly transpose-reductions for the
-//           per-head max and sum; P written as fp16 [rows x heads];
+//   softmax every warp: warp w reads TMEM lanes 32 (w % 4) (its rows) and the
+//           H/8 head columns of group w / 4; per-head tile max and sum by warp
+//           butterflies and a 4-warp exchange in shared memory; base-2 online
+//           softmax with a lazily moved reference max (moved only when the tile
+//           max exceeds it by 2^8); P written as fp16 [rows x heads];
 //   pass 2  O^T[d, h] += E^T[d, r] P[r, h]   (M = 128 d, N = heads, K = rows),
 //           the SAME smem tile read MN-major (a 128B-swizzled atom of 8 rows x
 //           64 d serves both views), so no row is fetched twice.
 // Both products are tcgen05 kind::f16 MMAs with fp32 accumulation in TMEM,
 // issued by thread 0. fp16 keeps 11 significant bits, as tf32 does; 32-bit
-// operands cannot be MN-major, which pass 2 needs. The latents are O(1),
-// p <= 2^8 by construction, and bf16 queries of normal fp16 range convert
-// exactly.
+// operands cannot be MN-major, which pass 2 needs. A latent or query value
+// beyond fp16's finite range (65504) sets kErrRange; the results of that call
+// are then not to be used. p <= 2^8 by construction, and bf16 queries of
+// normal fp16 range convert exactly.
 //
-// With more than one tile in a segment, warps 4-7 issue the loads of the next
-// tile while warps 0-3 run the softmax; every warp waits for the previous
-// tile's pass 2 before it overwrites E. Every wait is bounded; on a timeout
-// the CTA records kErrTimeout, drains its MMAs, frees TMEM and returns.
+// With more than one tile in a segment, the next tile's rows are requested
+// into L2 (one 2 KiB bulk prefetch per row) when a tile starts, so HBM keeps
+// streaming while the tile's products and softmax run; its loads then find the
+// rows in L2. Every wait is bounded; on a timeout the CTA records kErrTimeout,
+// drains its MMAs, frees TMEM and returns.
 //
-// A pair spread over several segments writes (m, l, O) partials per segment;
-// a second kernel merges them in row order. The plan depends only on the
+// A pair spread over several segments: each segment writes its normalized
+// output O / l as fp16 with its (m, l) statistics, and raises the pair's
+// arrival counter. When a CTA has run all its segments, it waits (bounded) for
+// the counters of the split pairs it took part in and merges its share of each
+// such pair's output, in split order:
+//     o_h = sum_s w_s O_s[h] / l_s,   w_s = l_s 2^(m_s - M) / sum_s' l_s' 2^(m_s' - M).
+// The CTAs of the grid wait on one another only there, so the kernel is
+// launched cooperatively (every CTA resident). The plan depends only on the
 // configuration, so identical rows give identical bits whatever slots hold
 // them.
 #include <cmath>
@@ -54,8 +65,9 @@ namespace {
 using namespace umma;
 
 constexpr int kTileRows = kAttnTile;                // 128
-constexpr int kThreads = 256;                       // 8 warps
-constexpr int kSoftThreads = 128;                   // warps 0-3: softmax, TMEM lanes 0-127
+constexpr int kThreads = 512;                       // 16 warps
+constexpr int kWarps = kThreads / 32;
+constexpr int kRowsPerWarp = kTileRows / kWarps;    // 8 tile rows per warp
 constexpr int kOffQ = 0;                            // 8 d-blocks x 8 KB: fp16 Q, K-major, row h
 constexpr int kDBlockE = kTileRows * 128;           // 16 KB: one d-block of E
 constexpr int kOffE = kOffQ + 8 * 8192;             // 8 d-blocks: fp16 E, row r
@@ -66,17 +78,23 @@ constexpr uint32_t kColS = 0;                       // S^T: up to 64 columns
 constexpr uint32_t kColO = 64;                      // O^T[mb]: 64 columns each
 constexpr float kLazy = 8.0f;                       // reference max moves past 2^8 growth
 constexpr int kMaxSplits = (kWindow + kMaxSelect + kTileRows - 1) / kTileRows;
+constexpr int kMaxDuties = 4;                       // split pairs one CTA takes part in
+constexpr int kMergeBatch = 5;                      // splits whose values a merging thread loads at once
 
 struct Misc {
-    uint64_t s_full, o_full, drain;
+    uint64_t s_full, o_full, drain, q_full;
     uint32_t tmem_base;
     int abort;
-    int rescale;
-    int epi_ok;
-    float m_used[64];
-    float l_run[64];
-    float alpha[64];        // per-tile rescale factors; 1 / l after the last tile
-    float red[4][64];
+    int n_duties;
+    int duty_merge[kMaxDuties];
+    int duty_part[kMaxDuties];
+    unsigned long long duty_target[kMaxDuties];
+    float m_used[2][64];    // reference max per head (parity of the segment's tile)
+    float l_run[2][64];     // running sum per head
+    float red[4][64];       // per-quadrant tile maxima
+    float red2[4][64];      // per-quadrant tile sums
+    float alpha[64];        // this tile's rescale factor per head
+    float inv_l[64];        // 1 / l per head at a segment's end
 };
 constexpr int kSmemBytes = kOffMisc + (int)sizeof(Misc) + 1024;   // + base alignment slack
 static_assert(kSmemBytes <= 232448, "attention shared memory exceeds 227 KB");
@@ -90,6 +108,8 @@ __host__ __device__ constexpr uint32_t idesc_f16(int a_mn, int b_mn, int n) {
 struct AttnArgs {
     const AttnSeg* segs;
     const int* cta_begin;   // CTA k runs segs[cta_begin[k] .. cta_begin[k + 1])
+    const MergeItem* merges;
+    unsigned long long* merge_cnt;   // arrivals per split pair (monotonic across calls)
     int B, G, S;
     const uint16_t* q;
     const float* window;
@@ -97,37 +117,14 @@ struct AttnArgs {
     const int32_t* phys;
     const int32_t* count_l;
     float* out;
-    float* part_o;
-    float* part_ml;
+    uint16_t* part_o;       // fp16 [slot][H][512]: O / l of one segment
+    float* part_ml;         // [slot][2][H]: m, l
     uint32_t* err;
-    float sl2;   // log2(e) / sqrt(kv_dim)
+    float sl2;              // log2(e) / sqrt(kv_dim)
 };
-
-// Bounded wait that also gives up when another thread has aborted the CTA.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                              uint32_t* err) {
-    const int r = mbar_wait_abort(bar, parity, abort);
-    if (r < 0) atomicOr(err, kErrTimeout);
-    return r > 0;
-}
 
 __device__ __forceinline__ void named_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
-}
-
-// Named barrier that also ORs a predicate over the participating threads, so a
-// failed wait in any of them makes all of them leave together.
-__device__ __forceinline__ bool named_sync_or(int id, int n, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n .reg .pred pi, po;\n"
-        " setp.ne.u32 pi, %1, 0;\n"
-        " bar.red.or.pred po, %2, %3, pi;\n"
-        " selp.u32 %0, 1, 0, po;\n}\n"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(id), "r"(n)
-        : "memory");
-    return r != 0;
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -145,15 +142,51 @@ __device__ __forceinline__ float4 ldg_stream(const float4* p) {
     return v;
 }
 
-// Max / sum over the 32 lanes of a warp for 32 per-lane values at once: after
-// the call, lane l holds the reduction of column l. Each step hands half of
-// the columns to the partner lane, so 31 shuffles do all 32 reductions.
-template <bool kMax>
-__device__ __forceinline__ float butterfly32(float (&v)[32], int lane) {
+// Loads of data written earlier in this kernel by other CTAs (partials) or by
+// an earlier kernel: L2, and volatile so they stay after the waits.
+__device__ __forceinline__ uint4 ld_cg_u4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ float ld_cg_f(const float* p) {
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];\n" : "=f"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];\n" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// 2^x by the hardware's approximate exponential (relative error about 2^-22,
+// far below the fp16 rounding that every weight p gets next); subnormal
+// results flush to zero. ex2(-inf) = 0.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float f16_to_f32(uint32_t h) {
+    float f;
+    asm("{\n .reg .f16 t;\n mov.b16 t, %1;\n cvt.f32.f16 %0, t;\n}\n" : "=f"(f) : "h"((unsigned short)h));
+    return f;
+}
+
+// Max / sum over the 32 lanes of a warp for N per-lane columns at once. The
+// first log2(N) steps hand half of the columns to the partner lane; afterwards
+// lane l holds column l / (32 / N), reduced over every lane.
+template <int N, bool kMax>
+__device__ __forceinline__ float reduce_cols(float (&v)[N], int lane) {
 #pragma unroll
-    for (int step = 0; step < 5; ++step) {
-        const int bit = 16 >> step;
-        const int half = 16 >> step;
+    for (int s = 0; (1 << s) < N; ++s) {
+        const int bit = 16 >> s;
+        const int half = N >> (s + 1);
         const bool upper = (lane & bit) != 0;
 #pragma unroll
         for (int i = 0; i < half; ++i) {
@@ -163,408 +196,579 @@ __device__ __forceinline__ float butterfly32(float (&v)[32], int lane) {
             v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
         }
     }
+#pragma unroll
+    for (int bit = 16 / N; bit >= 1; bit >>= 1) {
+        const float recv = __shfl_xor_sync(0xffffffffu, v[0], bit);
+        v[0] = kMax ? fmaxf(v[0], recv) : v[0] + recv;
+    }
     return v[0];
 }
 
 template <int H>
-__global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_constant__ AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_constant__ AttnArgs a) {
+    constexpr int HPG = H / 4;                       // heads per softmax group (4 groups of 4 warps)
+    constexpr int kQPer = H * 64 / kThreads;         // 16-byte query chunks per thread
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     Misc& ms = *reinterpret_cast<Misc*>(sm + kOffMisc);
     volatile int* abort = &ms.abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, grp = warp >> 2;      // TMEM lane quadrant; softmax / epilogue group
 
     // this CTA's segments of the static plan (written once, at creation)
     const int sb = a.cta_begin[blockIdx.x], se = a.cta_begin[blockIdx.x + 1];
     pdl_trigger();
 
     // ---------------------------------------------------------------- set-up
-    // Everything up to the dependency wait reads only this call's inputs (the
-    // queries), so with chained launches it overlaps the kernels that resolve
-    // and gather the staged rows.
     if (tid == 0) {
         mbar_init(&ms.s_full, 1);
         mbar_init(&ms.o_full, 1);
         mbar_init(&ms.drain, 1);
+        mbar_init(&ms.q_full, 1);
         ms.abort = 0;
-        ms.rescale = 0;
-        ms.epi_ok = 0;
+        ms.n_duties = 0;
         fence_mbar_init();
     }
-    if (tid < 64) {
-        ms.m_used[tid] = -INFINITY;
-        ms.l_run[tid] = 0.f;
-        ms.alpha[tid] = 1.f;
-    }
     if (warp == 0) tmem_alloc(&ms.tmem_base, kTmemCols);
-    // queries of (layer, sequence) lb: bf16 [H][512] -> fp16 K-major; d-block d / 64
-    // at (d / 64) * 8192, row h
-    constexpr int kQPer = H * 64 / kThreads;             // 16-byte chunks per thread
-    auto load_q = [&](int lbq, uint4 (&qv)[kQPer]) {
-        const uint16_t* qg = a.q + (size_t)lbq * H * kKvDim;
-#pragma unroll
-        for (int k = 0; k < kQPer; ++k) {
-            const int i = tid + k * kThreads;
-            qv[k] = *reinterpret_cast<const uint4*>(qg + (i >> 6) * kKvDim + (i & 63) * 8);
+    float amax = 0.f;   // largest |value| converted to fp16 by this thread (range guard)
+
+    // Wait for an mbarrier phase: thread 0 polls, every other thread waits at
+    // the block barrier that follows (a waiting warp issues nothing). Returns
+    // true, block-uniformly, if the CTA has failed.
+    auto block_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (tid == 0 && !mbar_wait(bar, parity)) {
+            atomicOr(a.err, kErrTimeout);
+            ms.abort = 1;
         }
+        const bool f = __syncthreads_or(*abort != 0);
+        tc_fence_after();
+        return f;
     };
-    auto store_q = [&](const uint4 (&qv)[kQPer]) {
+    // Queries of pair lbq: bf16 [H][512], copied as they are into the E area
+    // (free between segments) by one bulk copy per 16 KiB, then converted to
+    // fp16 K-major in the Q area: d-block d / 64 at (d / 64) * 8192, row h.
+    uint32_t q_uses = 0;                             // phases of q_full
+    auto fetch_q = [&](int lbq) {                    // thread 0
+        const unsigned char* qg = reinterpret_cast<const unsigned char*>(a.q + (size_t)lbq * H * kKvDim);
+        constexpr uint32_t kBytes = H * kKvDim * 2, kPiece = 16384;
+        mbar_arrive_expect_tx(&ms.q_full, kBytes);
+#pragma unroll 1
+        for (uint32_t o = 0; o < kBytes; o += kPiece)
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                    smem_u32(sm + kOffE + o)),
+                "l"(qg + o), "r"(kPiece), "r"(smem_u32(&ms.q_full))
+                : "memory");
+    };
+    // after q_full's phase and a block barrier: every thread converts its chunks
+    auto convert_q = [&]() {
 #pragma unroll
         for (int k = 0; k < kQPer; ++k) {
             const int i = tid + k * kThreads, h = i >> 6, c8 = i & 63;
-            const uint4 v = qv[k];
-            uint4 w;
-            w.x = pack_f16x2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
-            w.y = pack_f16x2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
-            w.z = pack_f16x2(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u));
-            w.w = pack_f16x2(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
+            const uint4 v = *reinterpret_cast<const uint4*>(sm + kOffE + (size_t)i * 16);
+            const float f[8] = {__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                                __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u),
+                                __uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u),
+                                __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u)};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+            const uint4 w = make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
+                                       pack_f16x2(f[6], f[7]));
             *reinterpret_cast<uint4*>(sm + kOffQ + (c8 >> 3) * 8192 + sw128(h, c8 & 7)) = w;
         }
     };
-    auto convert_q = [&](int lbq) {
-        uint4 qv[kQPer];
-        load_q(lbq, qv);
-        store_q(qv);
-    };
-    int q_lb = sb < se ? a.segs[sb].lb : 0;
-    // The window rows are this call's own input: the first segment's (when it
-    // starts at tile 0) are requested from HBM before the dependency wait.
-    if (sb < se && a.segs[sb].tile0 == 0 && tid < kWindow)
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(a.window + ((size_t)q_lb * kWindow + tid) * kKvDim),
-                     "r"(kKvDim * 4) : "memory");
-    // The first pair's queries are loaded after the dependency wait (below);
-    // L2 is asked for them now.
-    constexpr int kQChunk = 16384;
-    if (sb < se && tid < H * kKvDim * 2 / kQChunk)
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(
-                         reinterpret_cast<const unsigned char*>(a.q + (size_t)q_lb * H * kKvDim) + tid * kQChunk),
-                     "r"(kQChunk) : "memory");
-    // the barriers, the abort flag, the softmax state and the TMEM address are
-    // set: every thread sees them from here on
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    // ... as fp16 into E: d-block (lane >> 4) + 2 j, 16-byte chunk (lane & 15) >> 1, half lane & 1.
-    auto store4 = [&](const float4 (&v)[4][4], int rbase) {
-        unsigned char* e = sm + kOffE + (lane >> 4) * kDBlockE + 8 * (lane & 1);
-        const int chunk = (lane & 15) >> 1;
+    // Half h2 (d 256 h2 .. +255) of a tile row: this lane's float4s lane + 32 j
+    // (j = 0, 1) of that half, as fp16 into E row r: d-block (lane >> 4) + 2 j
+    // + 4 h2, 16-byte chunk (lane & 15) >> 1, 8-byte half lane & 1.
+    auto store_half = [&](const float4 (&v)[2], int r, int h2) {
+        unsigned char* e = sm + kOffE + ((lane >> 4) + 4 * h2) * kDBlockE + 8 * (lane & 1) + sw128(r, (lane & 15) >> 1);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int j = 0; j < 2; ++j) {
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+            *reinterpret_cast<uint2*>(e + 2 * j * kDBlockE) =
+                make_uint2(pack_f16x2(v[j].x, v[j].y), pack_f16x2(v[j].z, v[j].w));
+        }
+    };
+    auto zero_half = [&](int r, int h2) {
+        unsigned char* e = sm + kOffE + ((lane >> 4) + 4 * h2) * kDBlockE + 8 * (lane & 1) + sw128(r, (lane & 15) >> 1);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                *reinterpret_cast<uint2*>(e + 2 * j * kDBlockE + sw128(rbase + i, chunk)) =
-                    make_uint2(pack_f16x2(v[i][j].x, v[i][j].y), pack_f16x2(v[i][j].z, v[i][j].w));
+        for (int j = 0; j < 2; ++j) *reinterpret_cast<uint2*>(e + 2 * j * kDBlockE) = make_uint2(0u, 0u);
     };
 
-    constexpr uint32_t id1 = idesc_f16(0, 0, H);   // pass 1: K-major E and Q
-    constexpr uint32_t id2 = idesc_f16(1, 1, H);   // pass 2: MN-major E^T and P
-    const int rw = 16 * warp;                       // this warp's first tile row
-    bool ok = true;
-
-    pdl_wait();   // slots, counts and staged rows come from earlier kernels
-
-    // The first segment's row count and first-tile slots, then its queries:
-    // all in flight together (one round trip for a CTA that starts once the
-    // earlier kernels are done, as most do: an attention CTA needs a whole SM).
-    int pre_cnt = 0, pre_ph0 = -1;
-    if (sb < se) {
-        const AttnSeg s0 = a.segs[sb];
-        const int rr = s0.tile0 * kTileRows + tid - kWindow;
-        if (tid < kTileRows && rr >= 0 && rr < a.S) pre_ph0 = a.phys[(size_t)s0.lb * a.S + rr];
-        pre_cnt = a.count_l[s0.lb];
-        convert_q(q_lb);   // read by pass 1 after the tile loop's barrier
-    }
-
-    uint32_t gt0 = 0;     // tiles this CTA ran before the current segment (mbarrier phases)
-    uint32_t n_drain = 0; // drains this CTA ran (phases of ms.drain)
-    for (int si = sb; si < se && !*abort; ++si) {
-    const AttnSeg sg = a.segs[si];
-    const size_t lb = (size_t)sg.lb;
-    if (si > sb) {
-        // a new segment: the previous one drained its MMAs and wrote its
-        // epilogue; reset the running softmax and, for a new pair, load its queries
-        if (sg.lb != q_lb) {
-            convert_q(sg.lb);
-            q_lb = sg.lb;
+    // Rows [row0, row1) of segment sg: the count comes from the resolve kernel.
+    auto seg_rows = [&](const AttnSeg& sg, int& row0, int& row1) {
+        int cnt = a.count_l[sg.lb];
+        if (cnt < 0 || cnt > a.S) {
+            if (tid == 0) atomicOr(a.err, kErrBounds);
+            cnt = cnt < 0 ? 0 : a.S;
         }
-        if (tid < 64) {
-            ms.m_used[tid] = -INFINITY;
-            ms.l_run[tid] = 0.f;
-            ms.alpha[tid] = 1.f;
-        }
-        if (tid == 0) ms.rescale = 0;
-        __syncthreads();
-    }
-    const int32_t* ph = a.phys + lb * a.S;
-    // the slot of this thread's row of the first tile, loaded beside the count
-    // (a slot past the count is never used); the first segment's were loaded
-    // after the dependency wait, beside its queries
-    int ph0 = pre_ph0, cnt = pre_cnt;
-    if (si > sb) {
-        ph0 = -1;
-        const int rr = sg.tile0 * kTileRows + tid - kWindow;
-        if (tid < kTileRows && rr >= 0 && rr < a.S) ph0 = ph[rr];
-        cnt = a.count_l[lb];
-    }
-    if (cnt < 0 || cnt > a.S) {
-        if (tid == 0) atomicOr(a.err, kErrBounds);
-        cnt = cnt < 0 ? 0 : a.S;
-    }
-    const int R = kWindow + cnt;
-    const int row0 = sg.tile0 * kTileRows;
-    const int row1 = min(R, sg.tile1 * kTileRows);
-    const int n_tiles = row1 > row0 ? (row1 - row0 + kTileRows - 1) / kTileRows : 0;
-
-    // Source of tile row tr: window rows first, then the staged rows in list
-    // order; rows past the split end repeat its last row (finite data that the
-    // softmax masks).
-    auto row_src = [&](int tr0, int tr) -> const float4* {
-        const int row = min(tr0 + tr, row1 - 1);
-        if (row < kWindow) return reinterpret_cast<const float4*>(a.window + (lb * kWindow + row) * kKvDim);
-        int slot = ph[row - kWindow] - kWindow;
-        if (slot < 0 || slot >= a.G) {
-            atomicOr(a.err, kErrBounds);
-            slot = 0;
-        }
-        return reinterpret_cast<const float4*>(a.staging + (lb * (size_t)a.G + slot) * kKvDim);
+        row0 = sg.tile0 * kTileRows;
+        row1 = min(kWindow + cnt, sg.tile1 * kTileRows);
     };
-    // Ask L2 for the rows of the tile at tr0: one 2 KiB bulk prefetch per row,
-    // issued by threads 0-127. It holds no registers or shared memory, so the
-    // whole tile is requested from HBM at once and the loads below find it in L2.
-    // `first`: the segment's first tile, whose slots are already in ph0.
-    auto prefetch_tile = [&](int tr0, bool first) {
+    // Ask L2 for the rows of the tile at tr0 of pair lb (threads 0-127, one
+    // 2 KiB bulk prefetch each): no registers or shared memory, so HBM streams
+    // the whole tile while its loads and the products of the tile before run.
+    auto prefetch_tile = [&](size_t lb, int tr0, int row1) {
         const int row = tr0 + tid;
         if (tid >= kTileRows || row >= row1) return;
-        if (si == sb && row < kWindow) return;             // requested before the wait
         const float* p;
         if (row < kWindow) {
             p = a.window + (lb * kWindow + row) * kKvDim;
         } else {
-            const int slot = (first ? ph0 : ph[row - kWindow]) - kWindow;
+            const int slot = a.phys[lb * a.S + row - kWindow] - kWindow;
             if (slot < 0 || slot >= a.G) return;            // reported by the loads
             p = a.staging + (lb * (size_t)a.G + slot) * kKvDim;
         }
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(kKvDim * 4) : "memory");
     };
-    // Four rows of this warp: lane holds float4 lane + 32 j of each (d = 4 (lane + 32 j)).
-    auto load4 = [&](float4 (&v)[4][4], int tr0, int rbase) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float4* src = row_src(tr0, rbase + i);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) v[i][j] = ldg_stream(src + lane + 32 * j);
-        }
-    };
 
-    if (n_tiles > 0) prefetch_tile(row0, true);
-    for (int tile = 0; tile < n_tiles; ++tile) {
-        // ------------------------------------------------------------ load E (all warps)
-        const int tr0 = row0 + tile * kTileRows;
-        if (tile + 1 < n_tiles) prefetch_tile(tr0 + kTileRows, false);   // the next tile's rows, during this one
-        float4 b0[4][4], b1[4][4];
-        if (ok) {
-            load4(b0, tr0, rw);
-            load4(b1, tr0, rw + 4);
-            // the previous tile's pass 2 reads E: wait for it before overwriting
-            if (tile > 0 && !wait_or_abort(&ms.o_full, (gt0 + tile - 1) & 1, abort, a.err)) ok = false;
-        }
-        if (ok) {
-            store4(b0, rw);
-            load4(b0, tr0, rw + 8);
-            store4(b1, rw + 4);
-            load4(b1, tr0, rw + 12);
-            store4(b0, rw + 8);
-            store4(b1, rw + 12);
-        }
-        fence_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(!ok)) {
-            ok = false;
-            break;
-        }
-        tc_fence_after();
-        const uint32_t tmem = ms.tmem_base;
+    // the barriers, the abort flag and the TMEM address are set; every thread sees them from here on
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
 
-        // ------------------------------------------------------------ pass 1 (thread 0)
-        if (tid == 0) {
-            const uint32_t e0 = smem_u32(sm + kOffE), q0 = smem_u32(sm + kOffQ);
-#pragma unroll 1
-            for (int x = 0; x < 8; ++x)
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_f16kind(tmem + kColS, desc_sw128(e0 + x * kDBlockE + kk * 32, 16, 1024),
-                                desc_sw128(q0 + x * 8192 + kk * 32, 16, 1024), id1, (x | kk) != 0);
-            mma_commit(&ms.s_full);
-        }
-        if (tid >= kSoftThreads) continue;   // warps 4-7: on to the next tile's loads
+    // The first segment's queries are this call's own input: their copy is
+    // issued before the dependency wait.
+    int q_lb = -1;
+    if (sb < se) {
+        if (tid == 0) fetch_q(a.segs[sb].lb);
+        q_lb = a.segs[sb].lb;
+    }
 
-        // ------------------------------------------------------------ softmax (warps 0-3)
-        const int r = tid;                                // tile row = TMEM lane
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        const bool got = wait_or_abort(&ms.s_full, (gt0 + tile) & 1, abort, a.err);
-        if (named_sync_or(1, kSoftThreads, !got)) {
-            ok = false;
-            *abort = 1;
-            continue;                                     // leaves at the next block barrier
-        }
-        tc_fence_after();
-        float v[64];
-#pragma unroll
-        for (int c = 0; c < H; c += 16) {
-            float t16[16];
-            tmem_ld16(tmem + lane_base + kColS + c, t16);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[c + i] = t16[i];
-        }
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < H; c += 16) tmem_regs_ready(v + c);
-        const bool valid = tr0 + r < row1;
-#pragma unroll
-        for (int h = 0; h < 64; ++h) v[h] = (h < H && valid) ? v[h] * a.sl2 : -INFINITY;
-        // per-head tile max over the 128 rows: warp butterflies, then the 4 warps
-#pragma unroll
-        for (int hh = 0; hh < H; hh += 32) {
-            float red[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) red[i] = hh + i < H ? v[hh + i] : -INFINITY;
-            ms.red[warp][hh + lane] = butterfly32<true>(red, lane);
-        }
-        named_sync(1, kSoftThreads);
-        if (tid < H) {
-            const int h = tid;
-            const float mt = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
-            const float mu = ms.m_used[h];
-            float al = 1.f;
-            if (mt > mu + kLazy || (mu == -INFINITY && mt > -INFINITY)) {
-                al = exp2f(mu - mt);                      // 0 when mu = -inf
-                ms.m_used[h] = mt;
-                ms.l_run[h] *= al;
-                if (tile > 0 && al != 1.f) ms.rescale = 1;
+    pdl_wait();   // slots, counts and staged rows come from earlier kernels; partial buffers are reused
+    bool q_pending = sb < se;   // a queries' copy into the E area is issued and not yet converted
+
+    constexpr uint32_t id1 = idesc_f16(0, 0, H);   // pass 1: K-major E and Q
+    constexpr uint32_t id2 = idesc_f16(1, 1, H);   // pass 2: MN-major E^T and P
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    uint32_t gt = 0;            // tiles this CTA has run (mbarrier phases of s_full / o_full)
+    bool failed = false;        // block-uniform: a wait gave up (the abort flag, OR-ed at a barrier)
+
+    int si = sb;
+    for (; si < se; ++si) {
+        const AttnSeg sg = a.segs[si];
+        const size_t lb = (size_t)sg.lb;
+        int row0, row1;
+        seg_rows(sg, row0, row1);
+        const int n_tiles = row1 > row0 ? (row1 - row0 + kTileRows - 1) / kTileRows : 0;
+        const int32_t* ph = a.phys + lb * a.S;
+        if (si > sb && n_tiles > 0 && sg.lb != q_lb) {
+            // the previous segment drained its MMAs before its epilogue: Q and E are
+            // free; a copy that an earlier segment without rows left unused lands first
+            if (q_pending && block_wait(&ms.q_full, q_uses & 1)) {
+                failed = true;
+                break;
             }
-            ms.alpha[h] = al;
+            if (q_pending) ++q_uses;
+            if (tid == 0) fetch_q(sg.lb);
+            q_lb = sg.lb;
+            q_pending = true;
         }
-        named_sync(1, kSoftThreads);
-#pragma unroll
-        for (int h = 0; h < 64; ++h) v[h] = (h < H) ? exp2f(v[h] - ms.m_used[h]) : 0.f;
-#pragma unroll
-        for (int hh = 0; hh < H; hh += 32) {
-            float red[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) red[i] = v[hh + i];
-            ms.red[warp][hh + lane] = butterfly32<false>(red, lane);
+        if (tid < 64) {
+            ms.m_used[0][tid] = -INFINITY;
+            ms.l_run[0][tid] = 0.f;
         }
-        named_sync(1, kSoftThreads);
-        if (tid < H) ms.l_run[tid] += (ms.red[0][tid] + ms.red[1][tid]) + (ms.red[2][tid] + ms.red[3][tid]);
-        // pass 2 of the previous tile completed before E was overwritten, so O
-        // and P are free here
-        if (ms.rescale) {
-            // O^T[d, h] *= alpha[h]: this thread owns TMEM lane r of each d-block
-#pragma unroll 1
-            for (int mb = 0; mb < 4; ++mb) {
+
+        // Sources of this warp's rows w + 16 i (lane i < 8) of the tile at tr0:
+        // -1 - row for a window row, else the row's phys entry (window + slot).
+        auto fetch_src = [&](int tr0) -> int {
+            const int row = tr0 + warp + kWarps * (lane & 7);
+            if (lane >= kRowsPerWarp || row >= row1) return -1;
+            return row < kWindow ? -1 - row : ph[row - kWindow];
+        };
+        auto src_ptr = [&](int src) -> const float4* {
+            if (src < 0) return reinterpret_cast<const float4*>(a.window + (lb * kWindow + (-1 - src)) * kKvDim);
+            int slot = src - kWindow;
+            if (slot < 0 || slot >= a.G) {
+                atomicOr(a.err, kErrBounds);
+                slot = 0;
+            }
+            return reinterpret_cast<const float4*>(a.staging + (lb * (size_t)a.G + slot) * kKvDim);
+        };
+        // rows w + 16 (4 k + i), i < 4, of the tile at tr0: whole rows, 512
+        // contiguous bytes per load instruction
+        auto load_rows = [&](float4 (&v)[4][4], int tr0, int k, int src) {
 #pragma unroll
-                for (int c = 0; c < H; c += 16) {
-                    float t16[16];
-                    const uint32_t ta = tmem + lane_base + kColO + 64 * mb + c;
-                    tmem_ld16(ta, t16);
-                    tmem_ld_wait();
-                    tmem_regs_ready(t16);
+            for (int i = 0; i < 4; ++i) {
+                const int s = __shfl_sync(0xffffffffu, src, 4 * k + i);
+                if (tr0 + warp + kWarps * (4 * k + i) < row1) {
+                    const float4* p = src_ptr(s);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) t16[i] *= ms.alpha[c + i];
-                    tmem_st16(ta, t16);
+                    for (int j = 0; j < 4; ++j) v[i][j] = ldg_stream(p + lane + 32 * j);
                 }
             }
-            tmem_st_wait();
-        }
-        // P row r: 64 fp16 heads = 128 B, MN-major (heads contiguous), swizzled
-        unsigned char* prow = sm + kOffP;
+        };
+        auto store_rows = [&](const float4 (&v)[4][4], int tr0, int k) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            uint4 w;
-            w.x = pack_f16x2(v[8 * c + 0], v[8 * c + 1]);
-            w.y = pack_f16x2(v[8 * c + 2], v[8 * c + 3]);
-            w.z = pack_f16x2(v[8 * c + 4], v[8 * c + 5]);
-            w.w = pack_f16x2(v[8 * c + 6], v[8 * c + 7]);
-            *reinterpret_cast<uint4*>(prow + sw128(r, c)) = w;
-        }
-        fence_async_smem();
-        tc_fence_before();
-        named_sync(1, kSoftThreads);
-        if (tid == 0) {
-            // ------------------------------------------------------------ pass 2 (thread 0)
-            ms.rescale = 0;
+            for (int i = 0; i < 4; ++i) {
+                const int r = warp + kWarps * (4 * k + i);
+                if (tr0 + r < row1) {
+                    store_half(*reinterpret_cast<const float4(*)[2]>(&v[i][0]), r, 0);
+                    store_half(*reinterpret_cast<const float4(*)[2]>(&v[i][2]), r, 1);
+                } else {
+                    zero_half(r, 0);
+                    zero_half(r, 1);
+                }
+            }
+        };
+        auto issue_pass1 = [&](int x0) {   // d-blocks x0 .. x0 + 3 (thread 0)
+            const uint32_t e0 = smem_u32(sm + kOffE), q0 = smem_u32(sm + kOffQ);
+#pragma unroll 1
+            for (int x = x0; x < x0 + 4; ++x)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f16kind(ms.tmem_base + kColS, desc_sw128(e0 + x * kDBlockE + kk * 32, 16, 1024),
+                                desc_sw128(q0 + x * 8192 + kk * 32, 16, 1024), id1, (x | kk) != 0);
+        };
+
+        for (int tile = 0; tile < n_tiles; ++tile) {
+            const int tr0 = row0 + tile * kTileRows;
+            const int par = tile & 1;
+            if (tile + 1 < n_tiles) prefetch_tile(lb, tr0 + kTileRows, row1);
+            // ------------------------------------------------------------ E (all warps)
+            const int src = fetch_src(tr0);          // this tile's row sources (lanes 0-7)
+            float4 v[4][4];
+            load_rows(v, tr0, 0, src);
+            if (q_pending) {
+                // the queries' copy has landed in the E area: convert it while the rows arrive
+                if (block_wait(&ms.q_full, q_uses & 1)) {
+                    failed = true;
+                    break;
+                }
+                ++q_uses;
+                convert_q();
+                __syncthreads();   // every thread is done reading the E area
+                q_pending = false;
+            }
+            // the previous tile's pass 2 reads E: wait for it before overwriting
+            if (tile > 0 && block_wait(&ms.o_full, (gt - 1) & 1)) {
+                failed = true;
+                break;
+            }
+            store_rows(v, tr0, 0);
+            load_rows(v, tr0, 1, src);
+            store_rows(v, tr0, 1);
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
             tc_fence_after();
-            const uint32_t e0 = smem_u32(sm + kOffE), p0 = smem_u32(sm + kOffP);
-#pragma unroll 1
-            for (int mb = 0; mb < 4; ++mb)
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_f16kind(tmem + kColO + 64 * mb, desc_sw128(e0 + 2 * mb * kDBlockE + kk * 2048, kDBlockE, 1024),
-                                desc_sw128(p0 + kk * 2048, 8192, 1024), id2, (tile > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&ms.o_full);
-        }
-    }
+            // ------------------------------------------------------------ pass 1 (thread 0)
+            if (tid == 0) {
+                issue_pass1(0);
+                issue_pass1(4);
+                mma_commit(&ms.s_full);
+            }
+            const uint32_t tmem = ms.tmem_base;
 
-    // ---------------------------------------------------------------- drain
-    if (tid == 0 && n_tiles > 0) {
-        // completes once every MMA issued above has completed
-        mma_commit(&ms.drain);
-        if (!mbar_wait(&ms.drain, n_drain & 1)) {
-            atomicOr(a.err, kErrTimeout);
-            ok = false;
-        }
-    }
-    if (n_tiles > 0) ++n_drain;
-    gt0 += (uint32_t)n_tiles;
-    tc_fence_before();
-    const bool failed = __syncthreads_or(!ok);
-    tc_fence_after();
-    if (tid < H) ms.alpha[tid] = 1.f / ms.l_run[tid];
-    if (tid == 0) ms.epi_ok = failed ? 0 : 1;
-    __syncthreads();
-
-    // ---------------------------------------------------------------- epilogue: all 8 warps
-    const bool single = sg.slot < 0;
-    float* dst = single ? a.out + lb * H * kKvDim : a.part_o + (size_t)sg.slot * H * kKvDim;
-    if (n_tiles > 0 && ms.epi_ok) {
-        const uint32_t tmem = ms.tmem_base;
-        // warp w reads TMEM lanes 32 (w & 3).. of d-blocks 2 (w >> 2) and 2 (w >> 2) + 1
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-#pragma unroll 1
-        for (int mm = 0; mm < 2; ++mm) {
-            const int mb = 2 * (warp >> 2) + mm;
-            const int d = mb * 128 + (warp & 3) * 32 + lane;
-            // all H columns of this d-block in one TMEM round trip
-            float t[H];
-#pragma unroll
-            for (int c = 0; c < H; c += 16) tmem_ld16(tmem + lane_base + kColO + 64 * mb + c, *reinterpret_cast<float(*)[16]>(t + c));
+            // ------------------------------------------------------------ softmax (all warps)
+            const int r = quad * 32 + lane;               // tile row = TMEM lane
+            if (block_wait(&ms.s_full, gt & 1)) {
+                failed = true;
+                break;
+            }
+            const uint32_t ts = tmem + lane_base + kColS + HPG * grp;
+            const bool valid = tr0 + r < row1;
+            float sv[HPG], t[HPG];
+            tmem_ld<HPG>(ts, sv);                            // stale after an abort, then unused
             tmem_ld_wait();
+            tmem_regs_ready_n(sv);
 #pragma unroll
-            for (int c = 0; c < H; c += 16) tmem_regs_ready(t + c);
+            for (int i = 0; i < HPG; ++i) {
+                sv[i] = valid ? sv[i] * a.sl2 : -INFINITY;
+                t[i] = sv[i];
+            }
+            {
+                const float m = reduce_cols<HPG, true>(t, lane);
+                if ((lane & (32 / HPG - 1)) == 0) ms.red[quad][HPG * grp + lane / (32 / HPG)] = m;
+            }
+            named_sync(1 + grp, 128);
+            bool moved = false;
 #pragma unroll
-            for (int h = 0; h < H; ++h) {
-                if (single) dst[h * kKvDim + d] = t[h] * ms.alpha[h];
-                else __stcg(&dst[h * kKvDim + d], t[h]);
+            for (int c = 0; c < HPG / 4; ++c) {
+                // heads HPG * grp + 4 c .. + 3: the four quadrants' tile maxima and the reference max
+                const int h4 = HPG * grp + 4 * c;
+                const float4 a0 = *reinterpret_cast<const float4*>(&ms.red[0][h4]);
+                const float4 a1 = *reinterpret_cast<const float4*>(&ms.red[1][h4]);
+                const float4 a2 = *reinterpret_cast<const float4*>(&ms.red[2][h4]);
+                const float4 a3 = *reinterpret_cast<const float4*>(&ms.red[3][h4]);
+                const float4 m4 = *reinterpret_cast<const float4*>(&ms.m_used[par][h4]);
+                const float mts[4] = {fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x)), fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y)),
+                                      fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z)), fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w))};
+                const float mus[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = 4 * c + u, h = h4 + u;
+                    const float mt = mts[u];
+                    const float mu = mus[u];
+                    float mn = mu;
+                    const bool mv = mt > mu + kLazy || (mu == -INFINITY && mt > -INFINITY);
+                    if (mv) {
+                        mn = mt;
+                        moved = true;
+                    }
+                    if (quad == 0) {                         // a warp-uniform branch: every lane writes the same
+                        ms.alpha[h] = mv ? ex2_approx(mu - mt) : 1.f;   // 0 when mu = -inf
+                        ms.m_used[par ^ 1][h] = mn;
+                    }
+                    sv[i] = ex2_approx(sv[i] - mn);            // 0 for a row past the end
+                }
+            }
+            // P row r, heads HPG * grp ..: fp16, MN-major (heads contiguous), swizzled
+            {
+                if constexpr (HPG >= 8) {
+#pragma unroll
+                    for (int c = 0; c < HPG / 8; ++c)
+                        *reinterpret_cast<uint4*>(sm + kOffP + sw128(r, (HPG * grp) / 8 + c)) =
+                            make_uint4(pack_f16x2(sv[8 * c + 0], sv[8 * c + 1]), pack_f16x2(sv[8 * c + 2], sv[8 * c + 3]),
+                                       pack_f16x2(sv[8 * c + 4], sv[8 * c + 5]), pack_f16x2(sv[8 * c + 6], sv[8 * c + 7]));
+                } else {
+                    *reinterpret_cast<uint2*>(sm + kOffP + sw128(r, (HPG * grp) >> 3) + 2 * ((HPG * grp) & 7)) =
+                        make_uint2(pack_f16x2(sv[0], sv[1]), pack_f16x2(sv[2], sv[3]));
+                }
+            }
+            {
+                const float sum = reduce_cols<HPG, false>(sv, lane);   // sv is consumed
+                if ((lane & (32 / HPG - 1)) == 0) ms.red2[quad][HPG * grp + lane / (32 / HPG)] = sum;
+            }
+            named_sync(1 + grp, 128);
+            if (quad == 0 && (lane & (32 / HPG - 1)) == 0) {
+                const int h = HPG * grp + lane / (32 / HPG);
+                const float l = ms.l_run[par][h] * ms.alpha[h] +
+                                ((ms.red2[0][h] + ms.red2[1][h]) + (ms.red2[2][h] + ms.red2[3][h]));
+                ms.l_run[par ^ 1][h] = l;
+                ms.inv_l[h] = __fdividef(1.f, l);   // used after the segment's last tile; l >= 1
+            }
+            // the previous tile's pass 2 completed before E was overwritten, so
+            // O is free here: O^T[d, h] *= alpha[h] for this group's heads
+            if (moved && tile > 0) {
+#pragma unroll 1
+                for (int mb = 0; mb < 4; ++mb) {
+                    float o[HPG];
+                    const uint32_t ta = tmem + lane_base + kColO + 64 * mb + HPG * grp;
+                    tmem_ld<HPG>(ta, o);
+                    tmem_ld_wait();
+                    tmem_regs_ready_n(o);
+#pragma unroll
+                    for (int i = 0; i < HPG; ++i) o[i] *= ms.alpha[HPG * grp + i];
+                    tmem_st<HPG>(ta, o);
+                }
+                tmem_st_wait();
+            }
+            fence_async_smem();
+            tc_fence_before();
+            failed = __syncthreads_or(*abort != 0);
+            if (tid == 0 && !failed) {
+                // ------------------------------------------------------------ pass 2 (thread 0)
+                tc_fence_after();
+                const uint32_t e0 = smem_u32(sm + kOffE), p0 = smem_u32(sm + kOffP);
+#pragma unroll 1
+                for (int mb = 0; mb < 4; ++mb)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_f16kind(tmem + kColO + 64 * mb, desc_sw128(e0 + 2 * mb * kDBlockE + kk * 2048, kDBlockE, 1024),
+                                    desc_sw128(p0 + kk * 2048, 8192, 1024), id2, (tile > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&ms.o_full);
+            }
+            ++gt;
+            if (failed) break;
+        }
+        if (failed) break;
+
+        // ---------------------------------------------------------------- epilogue: all warps
+        // warp w reads TMEM lanes 32 (w % 4).. of d-block w / 4, all heads in
+        // chunks of 16 columns
+        const int fpar = n_tiles & 1;
+        const bool single = sg.slot < 0;
+        const int mb = grp;
+        if (n_tiles > 0 && block_wait(&ms.o_full, (gt - 1) & 1)) {
+            failed = true;
+            break;
+        }
+        if (n_tiles > 0) {
+            const int d = mb * 128 + quad * 32 + lane;
+#pragma unroll 1
+            for (int h0 = 0; h0 < H; h0 += 16) {
+                float o[16];
+                tmem_ld<16>(ms.tmem_base + lane_base + kColO + 64 * mb + h0, o);
+                tmem_ld_wait();
+                tmem_regs_ready_n(o);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float4 il = reinterpret_cast<const float4*>(&ms.inv_l[h0])[c];
+                    o[4 * c + 0] *= il.x;
+                    o[4 * c + 1] *= il.y;
+                    o[4 * c + 2] *= il.z;
+                    o[4 * c + 3] *= il.w;
+                }
+                if (single) {
+                    float* dst = a.out + (lb * H + h0) * kKvDim + d;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) dst[(size_t)i * kKvDim] = o[i];
+                } else {
+                    // lanes 2k and 2k + 1 hold d and d + 1: the even lane stores both
+                    // values of head i, the odd lane both of head i + 1 (4-byte stores)
+                    const bool odd = lane & 1;
+                    uint32_t* dst = reinterpret_cast<uint32_t*>(a.part_o + ((size_t)sg.slot * H + h0) * kKvDim +
+                                                                (d & ~1));
+#pragma unroll
+                    for (int i = 0; i < 16; i += 2) {
+                        const float other = __shfl_xor_sync(0xffffffffu, odd ? o[i] : o[i + 1], 1);
+                        const uint32_t w = odd ? pack_f16x2(other, o[i + 1]) : pack_f16x2(o[i], other);
+                        __stcg(&dst[(size_t)(i + (odd ? 1 : 0)) * (kKvDim / 2)], w);
+                    }
+                }
             }
         }
-    } else if (!single) {
-        for (int i = tid; i < H * kKvDim; i += kThreads) __stcg(&dst[i], 0.f);
-    }
-    if (!single && tid < H) {
-        float* pml = a.part_ml + (size_t)sg.slot * 2 * H;
-        __stcg(&pml[tid], ms.m_used[tid]);
-        __stcg(&pml[H + tid], n_tiles > 0 && ms.epi_ok ? ms.l_run[tid] : 0.f);
-    }
-    // the next segment overwrites O, S, E, P and the softmax state: every
-    // thread is done with this one's TMEM reads and shared values first
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (!ms.epi_ok && n_tiles > 0) *abort = 1;
+        if (!single && tid < H) {
+            float* pml = a.part_ml + (size_t)sg.slot * 2 * H;
+            __stcg(&pml[tid], ms.m_used[fpar][tid]);
+            __stcg(&pml[H + tid], n_tiles > 0 ? ms.l_run[fpar][tid] : 0.f);
+        }
+        // the next segment overwrites O, S, E, P, Q and the softmax state: every
+        // thread is done with this one's TMEM reads and shared values first
+        tc_fence_before();
+        failed = __syncthreads_or(*abort != 0);
+        tc_fence_after();
+        if (failed) break;
+        if (!single && tid == 0) {
+            // this segment's partial is written (every thread's stores precede the
+            // barrier; the fence makes them visible GPU-wide before the count):
+            // count it, and note the share of the pair this CTA merges at the end
+            const MergeItem mi = a.merges[sg.merge];
+            __threadfence();
+            const unsigned long long old = atomicAdd(&a.merge_cnt[sg.merge], 1ull);
+            const int k = ms.n_duties;
+            if (k < kMaxDuties) {
+                ms.duty_merge[k] = sg.merge;
+                ms.duty_part[k] = sg.part;
+                ms.duty_target[k] = (old / (unsigned long long)mi.ns + 1ull) * (unsigned long long)mi.ns;
+                ms.n_duties = k + 1;
+            } else {
+                atomicOr(a.err, kErrBounds);
+            }
+        }
     }   // segments
 
+    if (q_pending) {
+        // a queries' copy still lands in the E area: wait for it before leaving
+        if (tid == 0 && !mbar_wait(&ms.q_full, q_uses & 1)) atomicOr(a.err, kErrTimeout);
+        __syncthreads();
+    }
+    if (failed) {
+        // the split pairs of the segments not finished: a zero-weight partial
+        // each, counted, so that the other CTAs of those pairs do not wait
+        for (int sj = si; sj < se; ++sj) {
+            const AttnSeg sg = a.segs[sj];
+            if (sg.slot < 0) continue;
+            if (tid < H) __stcg(&a.part_ml[(size_t)sg.slot * 2 * H + H + tid], 0.f);
+            __syncthreads();
+            if (tid == 0) {
+                __threadfence();
+                atomicAdd(&a.merge_cnt[sg.merge], 1ull);
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- range guard
+    if (__any_sync(0xffffffffu, !(amax <= 65504.f)) && lane == 0) atomicOr(a.err, kErrRange);
+
+    // ---------------------------------------------------------------- merges
+    __syncthreads();
+    const int n_duties = failed ? 0 : ms.n_duties;
+    for (int k = 0; k < n_duties; ++k) {
+        const MergeItem mi = a.merges[ms.duty_merge[k]];
+        const int ns = min(mi.ns, kMaxSplits);
+        if (tid == 0) {
+            const unsigned long long* c = &a.merge_cnt[ms.duty_merge[k]];
+            const unsigned long long target = ms.duty_target[k];
+            bool ok = ld_acquire_u64(c) >= target;
+            if (!ok) {
+                const uint64_t t0 = global_ns();
+                while (!(ok = ld_acquire_u64(c) >= target)) {
+                    __nanosleep(32);
+                    if (global_ns() - t0 > kWaitLimitNs) break;
+                }
+            }
+            if (!ok) {
+                atomicOr(a.err, kErrTimeout);
+                ms.abort = 1;
+            }
+        }
+        if (__syncthreads_or(*abort != 0)) break;
+        // this CTA's share: 8-value chunks [c0, c1) of the pair's H x 512 outputs.
+        // Each thread loads, for its chunk, every split's 8 values and the
+        // head's (m, l) statistics in one round and combines them itself.
+        constexpr int kChunks = H * kKvDim / 8;
+        const int j = ms.duty_part[k];
+        const int c0 = (int)((long long)j * kChunks / ns), c1 = (int)((long long)(j + 1) * kChunks / ns);
+        const float* ml = a.part_ml + (size_t)mi.first * 2 * H;
+        // two chunks per thread and iteration, every load of both issued at once
+        for (int cb = c0 + tid; cb < c1; cb += 2 * kThreads) {
+            uint4 pv[2][kMergeBatch];
+            float mv[2][kMergeBatch], lv[2][kMergeBatch];
+            float acc[2][8], M[2], L[2];
+            for (int s0 = 0; s0 < ns; s0 += kMergeBatch) {
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int c = cb + q * kThreads;
+                    if (c >= c1) continue;
+                    const int h = c >> 6;
+                    const uint16_t* src = a.part_o + ((size_t)mi.first * H + h) * kKvDim + (c & 63) * 8;
+#pragma unroll
+                    for (int s = 0; s < kMergeBatch; ++s) {
+                        if (s0 + s < ns) {
+                            pv[q][s] = ld_cg_u4(src + (size_t)(s0 + s) * H * kKvDim);
+                            mv[q][s] = ld_cg_f(&ml[(size_t)(s0 + s) * 2 * H + h]);
+                            lv[q][s] = ld_cg_f(&ml[(size_t)(s0 + s) * 2 * H + H + h]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    if (cb + q * kThreads >= c1) continue;
+                    if (s0 == 0) {
+                        M[q] = -INFINITY;
+                        L[q] = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[q][e] = 0.f;
+                    }
+                    // online combination over the splits, in split order
+#pragma unroll
+                    for (int s = 0; s < kMergeBatch; ++s) {
+                        if (s0 + s < ns && lv[q][s] > 0.f) {
+                            const float Mn = fmaxf(M[q], mv[q][s]);
+                            const float a0 = ex2_approx(M[q] - Mn), w = lv[q][s] * ex2_approx(mv[q][s] - Mn);
+                            L[q] = L[q] * a0 + w;
+                            const uint32_t x[4] = {pv[q][s].x, pv[q][s].y, pv[q][s].z, pv[q][s].w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                acc[q][2 * e] = acc[q][2 * e] * a0 + w * f16_to_f32(x[e] & 0xffffu);
+                                acc[q][2 * e + 1] = acc[q][2 * e + 1] * a0 + w * f16_to_f32(x[e] >> 16);
+                            }
+                            M[q] = Mn;
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int c = cb + q * kThreads;
+                if (c >= c1) continue;
+                const float inv = L[q] > 0.f ? 1.f / L[q] : 0.f;
+                float4* dst = reinterpret_cast<float4*>(a.out + ((size_t)mi.lb * H + (c >> 6)) * kKvDim + (c & 63) * 8);
+                dst[0] = make_float4(acc[q][0] * inv, acc[q][1] * inv, acc[q][2] * inv, acc[q][3] * inv);
+                dst[1] = make_float4(acc[q][4] * inv, acc[q][5] * inv, acc[q][6] * inv, acc[q][7] * inv);
+            }
+        }
+        __syncthreads();
+    }
+
     // ---------------------------------------------------------------- teardown
+    if (tid == 0 && gt > 0) {
+        // completes once every MMA issued above has completed
+        mma_commit(&ms.drain);
+        if (!mbar_wait(&ms.drain, 0)) atomicOr(a.err, kErrTimeout);
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -573,131 +777,37 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     }
 }
 
-// Merge the split partials of one (layer, sequence), one head per CTA (thread
-// i owns float4 i of the head's 512 values):
-//     o_h = sum_s w_s O_s[h] / sum_s w_s l_s,   w_s = 2^(m_s - max_s m_s),
-// over the splits with l_s > 0, in split order. A split with l_s = 0 (no rows,
-// or a failed CTA) wrote zeros and gets weight 0. Every thread loads the
-// splits' statistics itself, together with its values of the first splits, so
-// the merge costs one round of loads and no barrier.
-// L2 loads of data an earlier kernel wrote: volatile with a memory clobber, so
-// the compiler keeps them after pdl_wait().
-__device__ __forceinline__ float ld_dep(const float* p) {
-    float v;
-    asm volatile("ld.global.cg.f32 %0, [%1];\n" : "=f"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ float4 ld_dep4(const float4* p) {
-    float4 v;
-    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];\n"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(p)
-                 : "memory");
-    return v;
-}
-
 template <int H>
-__global__ void __launch_bounds__(kKvDim / 4) merge_kernel(const MergeItem* __restrict__ merges, int merge0,
-                                                           const float* part_o, const float* part_ml,
-                                                           float* __restrict__ out) {
-    constexpr int kFirst = 5;   // splits loaded in the first round (a 640-row pair has 5)
-    const MergeItem mi = merges[merge0 + blockIdx.x];   // the plan: written once, at creation
-    const int h = blockIdx.y;
-    const int ns = min(mi.ns, kMaxSplits);
-    const int t = threadIdx.x;
-    const float* ml = part_ml + (size_t)mi.first * 2 * H;
-    const float4* src = reinterpret_cast<const float4*>(part_o + ((size_t)mi.first * H + h) * kKvDim) + t;
-    const size_t split_stride = (size_t)H * kKvDim / 4;   // float4s between consecutive splits
-    pdl_wait();   // the partials come from the attention kernel
-    float4 v[kFirst];
-    float mv[kFirst], lv[kFirst];
-#pragma unroll
-    for (int j = 0; j < kFirst; ++j) {
-        if (j < ns) {
-            v[j] = ld_dep4(src + (size_t)j * split_stride);
-            mv[j] = ld_dep(&ml[(size_t)j * 2 * H + h]);
-            lv[j] = ld_dep(&ml[(size_t)j * 2 * H + H + h]);
-        }
-    }
-    float M = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kFirst; ++j)
-        if (j < ns && lv[j] > 0.f) M = fmaxf(M, mv[j]);
-    for (int s = kFirst; s < ns; ++s) {
-        const float ls = ld_dep(&ml[(size_t)s * 2 * H + H + h]);
-        if (ls > 0.f) M = fmaxf(M, ld_dep(&ml[(size_t)s * 2 * H + h]));
-    }
-    float L = 0.f;
-#pragma unroll
-    for (int j = 0; j < kFirst; ++j) {
-        if (j < ns) {
-            mv[j] = lv[j] > 0.f ? exp2f(mv[j] - M) : 0.f;   // the weight w_j
-            L += mv[j] * lv[j];
-        }
-    }
-    for (int s = kFirst; s < ns; ++s) {
-        const float ls = ld_dep(&ml[(size_t)s * 2 * H + H + h]);
-        const float w = ls > 0.f ? exp2f(ld_dep(&ml[(size_t)s * 2 * H + h]) - M) : 0.f;
-        L += w * ls;
-    }
-    const float inv = 1.f / L;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int j = 0; j < kFirst; ++j) {
-        if (j < ns) {
-            const float w = mv[j] * inv;
-            acc.x += w * v[j].x;
-            acc.y += w * v[j].y;
-            acc.z += w * v[j].z;
-            acc.w += w * v[j].w;
-        }
-    }
-    for (int s = kFirst; s < ns; ++s) {
-        const float ls = ld_dep(&ml[(size_t)s * 2 * H + H + h]);
-        const float w = (ls > 0.f ? exp2f(ld_dep(&ml[(size_t)s * 2 * H + h]) - M) : 0.f) * inv;
-        const float4 x = ld_dep4(src + (size_t)s * split_stride);
-        acc.x += w * x.x;
-        acc.y += w * x.y;
-        acc.z += w * x.z;
-        acc.w += w * x.w;
-    }
-    reinterpret_cast<float4*>(out + ((size_t)mi.lb * H + h) * kKvDim)[t] = acc;
-}
-
-template <int H>
-cudaError_t launch_h(const AttnArgs& args, int n_ctas, const MergeItem* merges, int n_merges,
-                     cudaStream_t st, bool chained) {
-    cudaError_t e = launch_k(attend_tc_kernel<H>, dim3(n_ctas), dim3(kThreads), kSmemBytes, st, chained, args);
-    if (e != cudaSuccess || n_merges <= 0) return e;
-    // the merge follows its own attention kernel: always chained
-    return launch_k(merge_kernel<H>, dim3((unsigned)n_merges, H), dim3(kKvDim / 4), 0, st, true, merges, 0,
-                    (const float*)args.part_o, (const float*)args.part_ml, args.out);
+cudaError_t launch_h(const AttnArgs& args, int n_ctas, cudaStream_t st, bool chained) {
+    return launch_coop(attend_kernel<H>, dim3(n_ctas), dim3(kThreads), kSmemBytes, st, chained, args);
 }
 
 }  // namespace
 
 int attend_max_splits() { return kMaxSplits; }
+int attend_max_duties() { return kMaxDuties; }
 
 cudaError_t set_attend_attrs() {
-    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(attend_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(attend_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        e = cudaFuncSetAttribute(attend_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(attend_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        e = cudaFuncSetAttribute(attend_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     return e;
 }
 
 cudaError_t launch_attend(const AttnSeg* segs, const int* cta_begin, int n_ctas, const MergeItem* merges,
-                          int n_merges, int n_heads, int B, int G, int S, const uint16_t* q, const float* window,
-                          const float* staging, const int32_t* phys, const int32_t* count_l, float* out,
-                          float* part_o, float* part_ml, uint32_t* err, cudaStream_t st, bool chained) {
+                          unsigned long long* merge_cnt, int n_heads, int B, int G, int S, const uint16_t* q,
+                          const float* window, const float* staging, const int32_t* phys, const int32_t* count_l,
+                          float* out, uint16_t* part_o, float* part_ml, uint32_t* err, cudaStream_t st,
+                          bool chained) {
     if (n_ctas <= 0) return cudaSuccess;
-    AttnArgs args{segs, cta_begin, B, G, S, q, window, staging, phys, count_l,
+    AttnArgs args{segs, cta_begin, merges, merge_cnt, B, G, S, q, window, staging, phys, count_l,
                   out, part_o, part_ml, err, (float)(1.4426950408889634 / std::sqrt((double)kKvDim))};
     switch (n_heads) {
-        case 16: return launch_h<16>(args, n_ctas, merges, n_merges, st, chained);
-        case 32: return launch_h<32>(args, n_ctas, merges, n_merges, st, chained);
-        case 64: return launch_h<64>(args, n_ctas, merges, n_merges, st, chained);
+        case 16: return launch_h<16>(args, n_ctas, st, chained);
+        case 32: return launch_h<32>(args, n_ctas, st, chained);
+        case 64: return launch_h<64>(args, n_ctas, st, chained);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -32,6 +32,7 @@ const char* kErrText[] = {
     "device wait timed out",
     "out of memory",
     "index out of bounds on the device",
+    "attention operand beyond the fp16 range",
 };
 
 int fail(srh_ctx* ctx, int code, const std::string& msg) {
@@ -125,6 +126,7 @@ void free_ctx(srh_ctx* ctx) {
     cudaFree(ctx->d_part_o);
     cudaFree(ctx->d_part_ml);
     cudaFree(ctx->d_merges);
+    cudaFree(ctx->d_merge_cnt);
     if (ctx->ev_resolved) cudaEventDestroy(ctx->ev_resolved);
     if (ctx->ev_gathered) cudaEventDestroy(ctx->ev_gathered);
     delete ctx;
@@ -132,14 +134,15 @@ void free_ctx(srh_ctx* ctx) {
 
 // The static attention plan of one lsa_attend scope (the pairs (layer, seq)
 // of `layers`). A pair holds 128 window rows plus at most min(S, cap) staged
-// rows, in 128-row tiles; a CTA holds ~200 KB of shared memory, so one runs
-// per SM. With T tiles in the scope, no plan can give a CTA fewer than
-// ceil(T / SMs) tiles; when cutting every pair into chunks of that many tiles
-// fits one wave, each CTA runs one chunk; otherwise the T tiles, in (layer,
-// seq, row) order, are cut into min(SMs, T) contiguous ranges of equal size
-// (+-1 tile), one CTA each. A pair spread over several CTAs is merged
-// afterwards from their partials. The plan depends only on the configuration,
-// so the same rows give the same bits whichever slots hold them.
+// rows, in 128-row tiles; an attention CTA holds ~210 KB of shared memory and
+// 1024 threads, so one runs per SM. With T tiles in the scope, no plan can give
+// a CTA fewer than ceil(T / SMs) tiles; when cutting every pair into chunks of
+// that many tiles fits one wave, each CTA runs one chunk; otherwise the T
+// tiles, in (layer, seq, row) order, are cut into min(SMs, T) contiguous
+// ranges of equal size (+-1 tile), one CTA each. A pair spread over several
+// CTAs is merged by those CTAs, each taking one share, once all its partials
+// are written. The plan depends only on the configuration, so the same rows
+// give the same bits whichever slots hold them.
 void plan_scope(srh_ctx* ctx, const std::vector<int>& layers, std::vector<AttnSeg>* segs,
                 std::vector<int>* cta_begin, std::vector<MergeItem>* merges, AttnPlan* plan) {
     const int B = ctx->B;
@@ -152,70 +155,71 @@ void plan_scope(srh_ctx* ctx, const std::vector<int>& layers, std::vector<AttnSe
             tiles.push_back((int)((rows + kAttnTile - 1) / kAttnTile));
             T += tiles.back();
         }
-    plan->seg0 = (int)segs->size();
-    plan->cta0 = (int)cta_begin->size();
-    plan->merge0 = (int)merges->size();
-    std::vector<int> first_slot(lbs.size(), -1), n_parts(lbs.size(), 0);
-    int slot = 0;
-    // Pair-aligned when it fits one wave: each pair is cut into chunks of at
-    // most m = ceil(T / SMs) tiles, one CTA per chunk, so no CTA starts a second
-    // pair (which would cost it a second query load and epilogue).
+    // raw segments (pair, tile range) and the first segment of each CTA
+    struct Raw { size_t r; int t0, t1; };
+    std::vector<Raw> raw;
+    std::vector<int> begin;
     const long long m = (T + ctx->sm_count - 1) / ctx->sm_count;
     long long n_chunks = 0;
     for (int t : tiles) n_chunks += (t + m - 1) / m;
     if (n_chunks <= ctx->sm_count) {
+        // one wave: each pair cut into chunks of at most m tiles, one CTA per
+        // chunk, so no CTA starts a second pair (a second query load and epilogue)
         for (size_t r = 0; r < lbs.size(); ++r) {
             const int nc = (int)((tiles[r] + m - 1) / m);
             for (int c = 0; c < nc; ++c) {
-                cta_begin->push_back((int)segs->size() - plan->seg0);
-                int sl = -1;
-                if (nc > 1) {
-                    sl = slot++;
-                    if (first_slot[r] < 0) first_slot[r] = sl;
-                    ++n_parts[r];
-                }
-                segs->push_back(AttnSeg{lbs[r], (int)(c * m), (int)std::min<long long>((c + 1) * m, tiles[r]), sl});
+                begin.push_back((int)raw.size());
+                raw.push_back(Raw{r, (int)(c * m), (int)std::min<long long>((c + 1) * m, tiles[r])});
             }
         }
-        plan->n_ctas = (int)n_chunks;
-        cta_begin->push_back((int)segs->size() - plan->seg0);
-        for (size_t r = 0; r < lbs.size(); ++r)
-            if (n_parts[r] > 0) merges->push_back(MergeItem{lbs[r], first_slot[r], n_parts[r], 0});
-        plan->n_segs = (int)segs->size() - plan->seg0;
-        plan->n_merges = (int)merges->size() - plan->merge0;
-        plan->n_slots = slot;
-        return;
-    }
-    // Otherwise stream-K: min(SMs, T) CTAs over contiguous tile ranges.
-    const int n = (int)std::min<long long>(ctx->sm_count, T);
-    plan->n_ctas = n;
-    size_t q = 0;
-    long long qs = 0;                           // first tile of pair q
-    for (int k = 0; k < n; ++k) {
-        cta_begin->push_back((int)segs->size() - plan->seg0);
-        const long long t0 = (long long)k * T / n, t1 = (long long)(k + 1) * T / n;
-        while (qs + tiles[q] <= t0) qs += tiles[q++];
-        long long t = t0;
-        size_t r = q;
-        long long rs = qs;
-        while (t < t1) {
-            const long long re = rs + tiles[r];
-            const long long e = std::min(re, t1);
-            int sl = -1;
-            if (!(t == rs && e == re)) {        // part of the pair: a partial
-                sl = slot++;
-                if (first_slot[r] < 0) first_slot[r] = sl;
-                ++n_parts[r];
+    } else {
+        // stream-K: min(SMs, T) CTAs over contiguous tile ranges
+        const int n = (int)std::min<long long>(ctx->sm_count, T);
+        size_t q = 0;
+        long long qs = 0;                       // first tile of pair q
+        for (int k = 0; k < n; ++k) {
+            begin.push_back((int)raw.size());
+            const long long t0 = (long long)k * T / n, t1 = (long long)(k + 1) * T / n;
+            while (qs + tiles[q] <= t0) qs += tiles[q++];
+            long long t = t0;
+            size_t r = q;
+            long long rs = qs;
+            while (t < t1) {
+                const long long re = rs + tiles[r];
+                const long long e = std::min(re, t1);
+                raw.push_back(Raw{r, (int)(t - rs), (int)(e - rs)});
+                t = e;
+                if (e == re) rs += tiles[r++];
             }
-            segs->push_back(AttnSeg{lbs[r], (int)(t - rs), (int)(e - rs), sl});
-            t = e;
-            if (e == re) rs += tiles[r++];
         }
     }
-    cta_begin->push_back((int)segs->size() - plan->seg0);
-    for (size_t r = 0; r < lbs.size(); ++r)
-        if (n_parts[r] > 0) merges->push_back(MergeItem{lbs[r], first_slot[r], n_parts[r], 0});
-    plan->n_segs = (int)segs->size() - plan->seg0;
+    plan->seg0 = (int)segs->size();
+    plan->cta0 = (int)cta_begin->size();
+    plan->merge0 = (int)merges->size();
+    plan->n_ctas = (int)begin.size();
+    // pairs with more than one segment write partials, in row order
+    std::vector<int> n_parts(lbs.size(), 0), merge_of(lbs.size(), -1), seen(lbs.size(), 0);
+    for (const Raw& x : raw) ++n_parts[x.r];
+    int slot = 0;
+    for (const Raw& x : raw) {
+        if (n_parts[x.r] > 1 && merge_of[x.r] < 0) {
+            merge_of[x.r] = (int)merges->size() - plan->merge0;
+            merges->push_back(MergeItem{lbs[x.r], slot, n_parts[x.r], 0});
+            slot += n_parts[x.r];
+        }
+    }
+    for (const Raw& x : raw) {
+        const int mi = merge_of[x.r];
+        int sl = -1, part = 0;
+        if (mi >= 0) {
+            part = seen[x.r]++;
+            sl = (*merges)[plan->merge0 + mi].first + part;
+        }
+        segs->push_back(AttnSeg{lbs[x.r], x.t0, x.t1, sl, mi, part});
+    }
+    for (int k : begin) cta_begin->push_back(k);
+    cta_begin->push_back((int)raw.size());
+    plan->n_segs = (int)raw.size();
     plan->n_merges = (int)merges->size() - plan->merge0;
     plan->n_slots = slot;
 }
@@ -237,7 +241,7 @@ void plan_attention(srh_ctx* ctx, std::vector<AttnSeg>* segs, std::vector<int>* 
 extern "C" {
 
 const char* srh_error_string(int code) {
-    if (code > 0 || code < -7) return "unknown error";
+    if (code > 0 || code < -8) return "unknown error";
     return kErrText[-code];
 }
 
@@ -380,11 +384,15 @@ int srh_create(const srh_config* cfg, srh_ctx** out) {
     if (e == cudaSuccess)
         e = cudaMemcpy(ctx->d_cta_begin, cta_begin.data(), sizeof(int) * cta_begin.size(), cudaMemcpyHostToDevice);
     const size_t slots = (size_t)std::max(ctx->max_slots, 1);
-    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_part_o, sizeof(float) * slots * SRH_MAX_HEADS * kKvDim);
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_part_o, sizeof(uint16_t) * slots * SRH_MAX_HEADS * kKvDim);
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_part_ml, sizeof(float) * slots * 2 * SRH_MAX_HEADS);
     if (e == cudaSuccess && !merges.empty()) e = cudaMalloc(&ctx->d_merges, sizeof(MergeItem) * merges.size());
     if (e == cudaSuccess && !merges.empty())
         e = cudaMemcpy(ctx->d_merges, merges.data(), sizeof(MergeItem) * merges.size(), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !merges.empty())
+        e = cudaMalloc(&ctx->d_merge_cnt, sizeof(unsigned long long) * merges.size());
+    if (e == cudaSuccess && !merges.empty())
+        e = cudaMemset(ctx->d_merge_cnt, 0, sizeof(unsigned long long) * merges.size());
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_resolved, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_gathered, cudaEventDisableTiming);
     if (e != cudaSuccess) return bail(SRH_ERR_NOMEM, std::string("attention scratch: ") + cudaGetErrorString(e));
@@ -627,9 +635,10 @@ int lsa_attend(srh_ctx* ctx, int layer, const uint16_t* d_q, int n_heads, const 
         return fail(ctx, SRH_ERR_INVALID, "q/window/staging/out must be 16-byte aligned");
     const AttnPlan& pl = ctx->plans[layer + 1];
     const cudaError_t e = launch_attend(ctx->d_segs + pl.seg0, ctx->d_cta_begin + pl.cta0, pl.n_ctas,
-                                        ctx->d_merges + pl.merge0, pl.n_merges, n_heads, ctx->B, ctx->G, ctx->S,
-                                        d_q, d_window, d_staging, d_phys, d_count_l, d_out, ctx->d_part_o,
-                                        ctx->d_part_ml, ctx->d_err, (cudaStream_t)stream, ctx->chained);
+                                        ctx->d_merges + pl.merge0, ctx->d_merge_cnt + pl.merge0, n_heads, ctx->B,
+                                        ctx->G, ctx->S, d_q, d_window, d_staging, d_phys, d_count_l, d_out,
+                                        ctx->d_part_o, ctx->d_part_ml, ctx->d_err, (cudaStream_t)stream,
+                                        ctx->chained);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "lsa_attend launch");
     return SRH_OK;
 }
@@ -741,6 +750,8 @@ int srh_check_error(srh_ctx* ctx) {
     if (w & kErrNotStored) return fail(ctx, SRH_ERR_NOT_STORED, "GGUF KV swap selected chunk before it was stored");
     if (w & kErrBounds) return fail(ctx, SRH_ERR_BOUNDS, "a device index was out of bounds");
     if (w & kErrTimeout) return fail(ctx, SRH_ERR_TIMEOUT, "a device wait timed out");
+    if (w & kErrRange)
+        return fail(ctx, SRH_ERR_RANGE, "an attention query or latent value is beyond +-65504 (fp16 range)");
     return SRH_OK;
 }
 

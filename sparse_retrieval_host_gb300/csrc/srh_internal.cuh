@@ -36,6 +36,26 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// A cooperative launch (every CTA of the grid resident at once, or the launch
+// fails): for kernels whose CTAs wait on one another. `chained` as above.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_coop(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                               bool chained, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = chained ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 constexpr int kKvDim = SRH_KV_DIM;
 constexpr int kWindow = SRH_WINDOW;
 constexpr int kIdx = SRH_N_INDEXERS;
@@ -51,6 +71,7 @@ enum : uint32_t {
     kErrNotStored = 1u,
     kErrBounds = 2u,
     kErrTimeout = 4u,
+    kErrRange = 8u,      // an attention operand beyond fp16's finite range
 };
 
 // Device-side counters (one array of unsigned long long).
@@ -97,16 +118,19 @@ struct LayerDev {
 // One segment of the attention plan: tiles [tile0, tile1) (128 rows each) of
 // one (layer, seq). A CTA runs a contiguous range of the plan's tiles, so its
 // segments are the pairs that range touches. A segment holding every tile of
-// its pair writes the output; the others write partials to `slot`.
+// its pair writes the output; the others write partials to `slot`, and the
+// CTA merges share `part` of the pair's output once every partial is in.
 struct AttnSeg {
     int lb;      // layer * B + seq
     int tile0;
     int tile1;
     int slot;    // partial slot, or -1
+    int merge;   // index of the pair's MergeItem in its plan, or -1
+    int part;    // this segment's place among the pair's partials (its merge share)
 };
 
-// One (layer, seq) whose tiles were cut across ns > 1 CTAs: the merge pass
-// combines partial slots first .. first + ns - 1, in row order.
+// One (layer, seq) whose tiles were cut across ns > 1 CTAs: its partial
+// slots first .. first + ns - 1 are combined in row order.
 struct MergeItem {
     int lb;      // layer * B + seq
     int first;
@@ -166,8 +190,9 @@ struct Ctx {
     int* d_cta_begin = nullptr;
     MergeItem* d_merges = nullptr;
     int max_slots = 0;
-    float* d_part_o = nullptr;          // [max_slots][SRH_MAX_HEADS][D]
+    uint16_t* d_part_o = nullptr;       // fp16 [max_slots][SRH_MAX_HEADS][D]
     float* d_part_ml = nullptr;         // [max_slots][2][SRH_MAX_HEADS]
+    unsigned long long* d_merge_cnt = nullptr;   // arrivals per split pair, all plans
     // bookkeeping
     float* staging = nullptr;           // the staging buffer bound to this context
     cudaEvent_t ev_resolved = nullptr;
@@ -232,11 +257,13 @@ cudaError_t launch_store(const LayerDev* layers, int l, int B, int G, int seq, l
 cudaError_t launch_resident_fill(const float* pool_dev, const uint8_t* ready, long long cap,
                                  int layer, int B, int G, float* staging, cudaStream_t st);
 cudaError_t launch_attend(const AttnSeg* segs, const int* cta_begin, int n_ctas, const MergeItem* merges,
-                          int n_merges, int n_heads, int B, int G, int S, const uint16_t* q, const float* window,
-                          const float* staging, const int32_t* phys, const int32_t* count_l, float* out,
-                          float* part_o, float* part_ml, uint32_t* err, cudaStream_t st, bool chained);
+                          unsigned long long* merge_cnt, int n_heads, int B, int G, int S, const uint16_t* q,
+                          const float* window, const float* staging, const int32_t* phys, const int32_t* count_l,
+                          float* out, uint16_t* part_o, float* part_ml, uint32_t* err, cudaStream_t st,
+                          bool chained);
 size_t lru_smem_bytes(int S, int G);
 int attend_max_splits();
+int attend_max_duties();   // split pairs one attention CTA may take part in
 // One CTA waits (limit_ns) on an mbarrier phase nothing completes and records
 // kErrTimeout in err: the self-test of the kernels' bounded waits.
 cudaError_t launch_wait_selftest(uint32_t* err, unsigned long long limit_ns, cudaStream_t st);
