@@ -88,7 +88,10 @@ extern "C" {
 #define SRH_SELECT_THRESH 1    /* sigmoid(s) > tau, taken as s > ln(tau/(1-tau)) ([P2] LSA) */
 
 /* srh_config.flags */
-#define SRH_FLAG_TEST_FAIL_HOST_ALLOC 1u  /* testing only: make the pinned allocation fail */
+#define SRH_FLAG_TEST_FAIL_HOST_ALLOC 1u  /* testing only: the last layer's pinned pool allocation
+                                             fails (after every earlier layer's pool and device
+                                             state were allocated): srh_create returns
+                                             SRH_ERR_NOMEM and frees all of it */
 
 typedef void* srh_stream_t;
 typedef struct srh_ctx srh_ctx;

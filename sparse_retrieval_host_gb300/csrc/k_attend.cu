@@ -79,6 +79,7 @@ constexpr uint32_t kColO = 64;                      // O^T[mb]: 64 columns each
 constexpr float kLazy = 8.0f;                       // reference max moves past 2^8 growth
 constexpr int kMaxSplits = (kWindow + kMaxSelect + kTileRows - 1) / kTileRows;
 constexpr int kMaxDuties = 4;                       // split pairs one CTA takes part in
+constexpr int kMlStride = kAttnMlStride;            // floats per partial's statistics: m, l, scale
 constexpr int kMergeBatch = 5;                      // splits whose values a merging thread loads at once
 
 struct Misc {
@@ -94,6 +95,7 @@ struct Misc {
     float red[4][64];       // per-quadrant tile maxima
     float red2[4][64];      // per-quadrant tile sums
     float alpha[64];        // this tile's rescale factor per head
+    uint32_t wmax[kWarps];  // per-warp max |row value| (bits) of the segment
     float inv_l[64];        // 1 / l per head at a segment's end
 };
 constexpr int kSmemBytes = kOffMisc + (int)sizeof(Misc) + 1024;   // + base alignment slack
@@ -117,8 +119,8 @@ struct AttnArgs {
     const int32_t* phys;
     const int32_t* count_l;
     float* out;
-    uint16_t* part_o;       // fp16 [slot][H][512]: O / l of one segment
-    float* part_ml;         // [slot][2][H]: m, l
+    uint16_t* part_o;       // fp16 [slot][H][512]: (O / l) / sc of one segment
+    float* part_ml;         // [slot][kMlStride]: m [H], l [H], sc
     uint32_t* err;
     float sl2;              // log2(e) / sqrt(kv_dim)
 };
@@ -231,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     }
     if (warp == 0) tmem_alloc(&ms.tmem_base, kTmemCols);
     float amax = 0.f;   // largest |value| converted to fp16 by this thread (range guard)
+    float ramax = 0.f;  // largest |row value| of the current segment (scale of its partial)
 
     // Wait for an mbarrier phase: thread 0 polls, every other thread waits at
     // the block barrier that follows (a waiting warp issues nothing). Returns
@@ -284,7 +287,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         unsigned char* e = sm + kOffE + ((lane >> 4) + 4 * h2) * kDBlockE + 8 * (lane & 1) + sw128(r, (lane & 15) >> 1);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+            const float t = fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w)));
+            amax = fmaxf(amax, t);
+            ramax = fmaxf(ramax, t);
             *reinterpret_cast<uint2*>(e + 2 * j * kDBlockE) =
                 make_uint2(pack_f16x2(v[j].x, v[j].y), pack_f16x2(v[j].z, v[j].w));
         }
@@ -368,6 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             ms.m_used[0][tid] = -INFINITY;
             ms.l_run[0][tid] = 0.f;
         }
+        ramax = 0.f;
 
         // Sources of this warp's rows w + 16 i (lane i < 8) of the tile at tr0:
         // -1 - row for a window row, else the row's phys entry (window + slot).
@@ -580,9 +586,26 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         const int fpar = n_tiles & 1;
         const bool single = sg.slot < 0;
         const int mb = grp;
+        if (!single) {
+            // the partial is stored as (O / l) / sc, sc = 2^floor(log2 max |row value|),
+            // so that it stays in fp16's normal range whatever the rows' magnitude
+            const uint32_t wm = __reduce_max_sync(0xffffffffu, __float_as_uint(ramax));   // ramax >= 0
+            if (lane == 0) ms.wmax[warp] = wm;
+        }
         if (n_tiles > 0 && block_wait(&ms.o_full, (gt - 1) & 1)) {
             failed = true;
             break;
+        }
+        float inv_sc = 1.f, sc = 1.f;
+        if (!single) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) m = max(m, ms.wmax[w]);
+            const uint32_t e = m & 0x7f800000u;          // 2^floor(log2 m) for a normal m
+            if (e != 0u && e != 0x7f800000u) {
+                sc = __uint_as_float(e);
+                inv_sc = __uint_as_float(0x7f000000u - e);   // 1 / sc, exact
+            }
         }
         if (n_tiles > 0) {
             const int d = mb * 128 + quad * 32 + lane;
@@ -595,10 +618,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const float4 il = reinterpret_cast<const float4*>(&ms.inv_l[h0])[c];
-                    o[4 * c + 0] *= il.x;
-                    o[4 * c + 1] *= il.y;
-                    o[4 * c + 2] *= il.z;
-                    o[4 * c + 3] *= il.w;
+                    o[4 * c + 0] *= il.x * inv_sc;
+                    o[4 * c + 1] *= il.y * inv_sc;
+                    o[4 * c + 2] *= il.z * inv_sc;
+                    o[4 * c + 3] *= il.w * inv_sc;
                 }
                 if (single) {
                     float* dst = a.out + (lb * H + h0) * kKvDim + d;
@@ -619,10 +642,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                 }
             }
         }
-        if (!single && tid < H) {
-            float* pml = a.part_ml + (size_t)sg.slot * 2 * H;
-            __stcg(&pml[tid], ms.m_used[fpar][tid]);
-            __stcg(&pml[H + tid], n_tiles > 0 ? ms.l_run[fpar][tid] : 0.f);
+        if (!single && tid <= H) {
+            float* pml = a.part_ml + (size_t)sg.slot * kMlStride;
+            if (tid < H) {
+                __stcg(&pml[tid], ms.m_used[fpar][tid]);
+                __stcg(&pml[H + tid], n_tiles > 0 ? ms.l_run[fpar][tid] : 0.f);
+            } else {
+                __stcg(&pml[2 * H], sc);
+            }
         }
         // the next segment overwrites O, S, E, P, Q and the softmax state: every
         // thread is done with this one's TMEM reads and shared values first
@@ -660,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         for (int sj = si; sj < se; ++sj) {
             const AttnSeg sg = a.segs[sj];
             if (sg.slot < 0) continue;
-            if (tid < H) __stcg(&a.part_ml[(size_t)sg.slot * 2 * H + H + tid], 0.f);
+            if (tid < H) __stcg(&a.part_ml[(size_t)sg.slot * kMlStride + H + tid], 0.f);
             __syncthreads();
             if (tid == 0) {
                 __threadfence();
@@ -701,11 +728,11 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         constexpr int kChunks = H * kKvDim / 8;
         const int j = ms.duty_part[k];
         const int c0 = (int)((long long)j * kChunks / ns), c1 = (int)((long long)(j + 1) * kChunks / ns);
-        const float* ml = a.part_ml + (size_t)mi.first * 2 * H;
+        const float* ml = a.part_ml + (size_t)mi.first * kMlStride;
         // two chunks per thread and iteration, every load of both issued at once
         for (int cb = c0 + tid; cb < c1; cb += 2 * kThreads) {
             uint4 pv[2][kMergeBatch];
-            float mv[2][kMergeBatch], lv[2][kMergeBatch];
+            float mv[2][kMergeBatch], lv[2][kMergeBatch], sv[2][kMergeBatch];
             float acc[2][8], M[2], L[2];
             for (int s0 = 0; s0 < ns; s0 += kMergeBatch) {
 #pragma unroll
@@ -718,8 +745,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                     for (int s = 0; s < kMergeBatch; ++s) {
                         if (s0 + s < ns) {
                             pv[q][s] = ld_cg_u4(src + (size_t)(s0 + s) * H * kKvDim);
-                            mv[q][s] = ld_cg_f(&ml[(size_t)(s0 + s) * 2 * H + h]);
-                            lv[q][s] = ld_cg_f(&ml[(size_t)(s0 + s) * 2 * H + H + h]);
+                            mv[q][s] = ld_cg_f(&ml[(size_t)(s0 + s) * kMlStride + h]);
+                            lv[q][s] = ld_cg_f(&ml[(size_t)(s0 + s) * kMlStride + H + h]);
+                            sv[q][s] = ld_cg_f(&ml[(size_t)(s0 + s) * kMlStride + 2 * H]);
                         }
                     }
                 }
@@ -737,8 +765,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                     for (int s = 0; s < kMergeBatch; ++s) {
                         if (s0 + s < ns && lv[q][s] > 0.f) {
                             const float Mn = fmaxf(M[q], mv[q][s]);
-                            const float a0 = ex2_approx(M[q] - Mn), w = lv[q][s] * ex2_approx(mv[q][s] - Mn);
-                            L[q] = L[q] * a0 + w;
+                            const float a0 = ex2_approx(M[q] - Mn), wl = lv[q][s] * ex2_approx(mv[q][s] - Mn);
+                            const float w = wl * sv[q][s];           // the partial's values were divided by its scale
+                            L[q] = L[q] * a0 + wl;
                             const uint32_t x[4] = {pv[q][s].x, pv[q][s].y, pv[q][s].z, pv[q][s].w};
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {

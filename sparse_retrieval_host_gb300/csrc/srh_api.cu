@@ -318,7 +318,7 @@ int srh_create(const srh_config* cfg, srh_ctx** out) {
         ld.swap = cap > G ? 1 : 0;
         const size_t pool_bytes = (size_t)B * cap * kKvDim * sizeof(float);
         void* hp = nullptr;
-        if (cfg->flags & SRH_FLAG_TEST_FAIL_HOST_ALLOC) {
+        if ((cfg->flags & SRH_FLAG_TEST_FAIL_HOST_ALLOC) && l == ctx->L - 1) {
             return bail(SRH_ERR_NOMEM, "cudaHostAlloc failed (injected by SRH_FLAG_TEST_FAIL_HOST_ALLOC)");
         }
         e = cudaHostAlloc(&hp, pool_bytes, cudaHostAllocMapped | cudaHostAllocPortable);
@@ -385,7 +385,7 @@ int srh_create(const srh_config* cfg, srh_ctx** out) {
         e = cudaMemcpy(ctx->d_cta_begin, cta_begin.data(), sizeof(int) * cta_begin.size(), cudaMemcpyHostToDevice);
     const size_t slots = (size_t)std::max(ctx->max_slots, 1);
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_part_o, sizeof(uint16_t) * slots * SRH_MAX_HEADS * kKvDim);
-    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_part_ml, sizeof(float) * slots * 2 * SRH_MAX_HEADS);
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_part_ml, sizeof(float) * slots * kAttnMlStride);
     if (e == cudaSuccess && !merges.empty()) e = cudaMalloc(&ctx->d_merges, sizeof(MergeItem) * merges.size());
     if (e == cudaSuccess && !merges.empty())
         e = cudaMemcpy(ctx->d_merges, merges.data(), sizeof(MergeItem) * merges.size(), cudaMemcpyHostToDevice);

@@ -65,6 +65,7 @@ constexpr int kHistBins = 4096;        // score histogram: top 12 bits of the or
 constexpr int kMaxSelect = 4096;       // largest S
 constexpr int kMaxGpuChunks = 4096;    // largest G
 constexpr int kAttnTile = 128;         // rows per attention tile
+constexpr int kAttnMlStride = 2 * SRH_MAX_HEADS + 4;   // floats per attention partial's statistics: m, l, scale
 
 // Bits of the sticky device error word.
 enum : uint32_t {
@@ -191,7 +192,7 @@ struct Ctx {
     MergeItem* d_merges = nullptr;
     int max_slots = 0;
     uint16_t* d_part_o = nullptr;       // fp16 [max_slots][SRH_MAX_HEADS][D]
-    float* d_part_ml = nullptr;         // [max_slots][2][SRH_MAX_HEADS]
+    float* d_part_ml = nullptr;         // [max_slots][kAttnMlStride]
     unsigned long long* d_merge_cnt = nullptr;   // arrivals per split pair, all plans
     // bookkeeping
     float* staging = nullptr;           // the staging buffer bound to this context

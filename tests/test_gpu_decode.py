@@ -22,9 +22,11 @@ def _built():
     torch.cuda.set_device(0)
 
 
-def _run_decode(w, steps, attend_layers=None, pools=None, policy=None):
+def _run_decode(w, steps, attend_layers=None, pools=None, policy=None, attend_seqs=None):
     """Run ``steps`` decode steps on GPU and oracle; returns (n_matched_steps, worst_attn_rel).
-    With ``policy`` both sides run the adaptive staging capacity."""
+    With ``policy`` both sides run the adaptive staging capacity. Attention and
+    staged rows are checked on ``attend_layers`` x ``attend_seqs`` (all by
+    default); selections, slots and counters on every sequence and layer."""
     ds = make_ds(w)
     try:
         if pools is None and w.n_chunks <= 8192:
@@ -50,11 +52,12 @@ def _run_decode(w, steps, attend_layers=None, pools=None, policy=None):
         else:
             rows_of = lambda l, b, idx: G.pool_rows(w, l, b, idx)
         layers = range(w.n_layers) if attend_layers is None else attend_layers
+        seqs = range(w.batch) if attend_seqs is None else attend_seqs
         for t in range(steps):
             load_step_inputs(ds, w, t)
             ds.step(spec)
             torch.cuda.synchronize()
-            pairs = [(l, b) for l in layers for b in range(w.batch)]
+            pairs = [(l, b) for l in layers for b in seqs]
             ref = ora.step(lambda b: keys[b], lambda b: G.fm_queries(w, t, b),
                            lambda l, b: G.attn_q(w, t, l, b), lambda l, b: G.window(w, l, b),
                            rows_of, attend_pairs=pairs)
@@ -86,7 +89,7 @@ def _run_decode(w, steps, attend_layers=None, pools=None, policy=None):
             # staged rows always hold the pool rows of the GPU's own selection
             stg = ds.staging
             for l in list(layers)[:3]:
-                for b in range(w.batch):
+                for b in seqs:
                     n_l = int(cl[l, b])
                     got = stg[l, b][torch.from_numpy(phys[l, b, :n_l] - 128).long().cuda()].cpu().numpy()
                     lst = np.asarray(sorted(set(sel[b, :cnt[b]] * 4 // w.layer_ratios[l])), dtype=np.int64)
@@ -127,6 +130,20 @@ def test_decode_batch_sweep_b4():
     w = C.batch_sweep(4)
     matched, worst = _run_decode(w, 20, attend_layers=[0, 7, 19])
     assert matched == 20
+    assert worst <= ATTN_TOL, worst
+
+
+@pytest.mark.skipif(os.environ.get("SRH_SKIP_LARGE") == "1", reason="large configs skipped")
+@pytest.mark.parametrize("batch,steps,seqs", [(16, 4, (0, 9, 15)), (32, 3, (0, 17, 31))])
+def test_decode_batch_sweep_large(batch, steps, seqs):
+    """The batch rows where one step runs the tensor-core scoring kernel (2^19
+    chunks and more per call) and the stream-K attention plan (more tiles than
+    SMs) together: selections, slots and counters of every sequence and layer;
+    attention and staged rows on sampled layers and sequences."""
+    w = C.batch_sweep(batch)
+    assert w.batch * w.n_chunks >= 1 << 19
+    matched, worst = _run_decode(w, steps, attend_layers=[0, 11, 19], attend_seqs=seqs)
+    assert matched == steps
     assert worst <= ATTN_TOL, worst
 
 

@@ -471,3 +471,111 @@ def test_lsa_attend_matches_oracle(H, counts, batch_layers, per_layer):
         assert ds.check_error() == 0
     finally:
         ds.close()
+
+
+def _attend_case(H, counts, L, scales, seed):
+    """lsa_attend on random rows, row block (l, b) scaled by scales[(l * B + b) % len]."""
+    from sparse_retrieval_host_gb300.runtime import bits_to_i16
+    B = len(counts)
+    w = _w(context_len=8192, layer_ratios=(4,) * L, gpu_chunks=600, index_topk=512, n_heads=H, batch=B, code=63)
+    ds = make_ds(w, max_select=512)
+    rng = np.random.default_rng(seed)
+    stg = rng.standard_normal((L, B, 600, 512), dtype=np.float32)
+    win = rng.standard_normal((L, B, 128, 512), dtype=np.float32)
+    for l in range(L):
+        for b in range(B):
+            f = np.float32(scales[(l * B + b) % len(scales)])
+            stg[l, b] *= f
+            win[l, b] *= f
+    q = G.f32_to_bf16_bits(rng.standard_normal((L, B, H, 512), dtype=np.float32))
+    phys = np.zeros((L, B, ds.S), np.int32)
+    for l in range(L):
+        for b in range(B):
+            phys[l, b, :counts[b]] = 128 + rng.choice(600, size=counts[b], replace=False)
+    ds.staging.copy_(torch.from_numpy(stg))
+    ds.window.copy_(torch.from_numpy(win))
+    ds.q.copy_(bits_to_i16(q))
+    ds.phys.copy_(torch.from_numpy(phys))
+    ds.count_l.copy_(torch.from_numpy(np.tile(np.int32(counts), (L, 1))))
+    return ds, stg, win, q, phys
+
+
+@pytest.mark.parametrize("scales", [(8e3,), (1e-4,), (8e3, 1e-4, 1.0)], ids=["large", "small", "mixed"])
+def test_lsa_attend_rows_far_from_unit_scale(scales):
+    """Latent rows far from O(1): |e| around 1e4 (near fp16's top) and around
+    1e-4 (partly fp16-subnormal), within one call and mixed across pairs; the
+    pairs are split over several CTAs, so the fp16 partials and the merge run."""
+    H, counts, L = 64, (512, 300, 33), 2
+    ds, stg, win, q, phys = _attend_case(H, counts, L, scales, seed=5)
+    try:
+        ds.attend()
+        out = ds.out.cpu().numpy()
+        worst = 0.0
+        for l in range(L):
+            for b in range(len(counts)):
+                rows = np.concatenate([win[l, b], stg[l, b][phys[l, b, :counts[b]] - 128]])
+                _, rel = attn_err(out[l, b], O.attend(q[l, b], rows))
+                worst = max(worst, rel)
+        assert worst <= ATTN_TOL, worst
+        assert ds.check_error() == 0
+    finally:
+        ds.close()
+
+
+@pytest.mark.parametrize("where", ["staged_row", "window_row", "query"])
+def test_lsa_attend_reports_values_beyond_fp16(where):
+    """A latent or query value beyond +-65504 cannot become an fp16 tensor-core
+    operand: the call reports SRH_ERR_RANGE (the word clears once read), and a
+    later call on finite-range inputs is clean."""
+    from sparse_retrieval_host_gb300 import abi
+    from sparse_retrieval_host_gb300.runtime import bits_to_i16
+    ds, stg, win, q, phys = _attend_case(32, (200, 7), 1, (1.0,), seed=9)
+    try:
+        ds.attend()
+        assert ds.check_error() == abi.SRH_OK
+        if where == "staged_row":
+            ds.staging[0, 1, int(phys[0, 1, 3]) - 128, 17] = 1e5
+        elif where == "window_row":
+            ds.window[0, 0, 5, 300] = -7e4
+        else:
+            qq = q.copy()
+            qq[0, 1, 2, 9] = G.f32_to_bf16_bits(np.array([2e5], np.float32))[0]
+            ds.q.copy_(bits_to_i16(qq))
+        ds.attend()
+        assert ds.check_error() == abi.SRH_ERR_RANGE
+        assert ds.check_error() == abi.SRH_OK
+        ds.staging.copy_(torch.from_numpy(stg))
+        ds.window.copy_(torch.from_numpy(win))
+        ds.q.copy_(bits_to_i16(q))
+        ds.attend()
+        assert ds.check_error() == abi.SRH_OK
+    finally:
+        ds.close()
+
+
+def test_create_host_alloc_failure_frees_everything():
+    """An injected pinned-pool allocation failure (the last layer's, after the
+    earlier layers' pools and device tables exist) gives SRH_ERR_NOMEM, and the
+    failed creations leave neither device memory nor pinned host memory behind."""
+    import os
+    from sparse_retrieval_host_gb300 import abi
+
+    def rss_bytes():
+        with open("/proc/self/statm") as f:
+            return int(f.read().split()[1]) * os.sysconf("SC_PAGE_SIZE")
+
+    ratios = [4, 4, 128]
+    kw = dict(batch=2, layer_ratios=ratios, gpu_chunks=1024, index_topk=512, context_len=1 << 20)
+    ok = abi.srh_create(abi.make_config(**kw))            # a context of this shape can be made
+    abi.srh_destroy(ok)
+    torch.cuda.synchronize()
+    free0, rss0 = torch.cuda.mem_get_info()[0], rss_bytes()
+    for _ in range(4):   # each attempt pins 2 pools of 1 GiB before it fails
+        with pytest.raises(abi.SrhError) as ei:
+            abi.srh_create(abi.make_config(flags=abi.SRH_FLAG_TEST_FAIL_HOST_ALLOC, **kw))
+        assert ei.value.code == abi.SRH_ERR_NOMEM
+        assert "injected" in str(ei.value)
+    torch.cuda.synchronize()
+    free1, rss1 = torch.cuda.mem_get_info()[0], rss_bytes()
+    assert abs(free1 - free0) < (8 << 20), (free0, free1)
+    assert rss1 - rss0 < (256 << 20), (rss0, rss1)       # four leaks would be 8 GiB
