@@ -44,6 +44,8 @@ COLLECT_MIN_N = 16384         # fm_select runs its candidate pass above this man
 Q_CYCLE = 16                  # distinct attention-query sets cycled through the steps
 FLUSH_BYTES = 256 << 20       # > 2x the 126 MiB L2
 METRIC = "decode steps/s"
+SWEEP = ("ctx256k", "ctx1m", "batch128k_b1", "batch128k_b4", "batch128k_b8", "batch128k_b16", "batch128k_b32")
+DTYPE = "bf16 scoring / fp16 attention operands / fp32 accumulate"
 
 
 def parse():
@@ -57,6 +59,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-steps", type=int, default=0, help="0 = auto")
     ap.add_argument("--quiet", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the other workloads' sub-records")
+    ap.add_argument("--sweep", default=",".join(SWEEP), help="workloads measured beside the headline")
+    ap.add_argument("--oracle-seconds", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -284,6 +289,15 @@ def run_ours(args, dist, rank, world, local):
     assert ds.check_error() == 0, "device error during the timed steps"
     step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     st = ds.stats()
+    # the same steps with a warm L2 (no flush between them), for comparison only
+    evw = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        bind(args.warmup + i)
+        evw[i][0].record(stream)
+        graph.replay()
+        evw[i][1].record(stream)
+    torch.cuda.synchronize()
+    warm_ms = [e0.elapsed_time(e1) for e0, e1 in evw]
 
     # periodic selection: the memory indexer scores once per lookahead window and
     # the steps in between reuse the selection (same outputs for these inputs)
@@ -481,8 +495,9 @@ def run_ours(args, dist, rank, world, local):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "f32",
-            "precision": "bf16 keys/queries, f32 latents; fp16 attention MMA operands (tcgen05 kind::f16), f32 accumulate",
+            "dtype": DTYPE,
+            "precision": "bf16 keys/queries scored on bf16 MMAs; f32 latents rounded to fp16 attention MMA operands "
+                         "(tcgen05 kind::f16); f32 accumulate and softmax; fp16 split partials",
             "data": "synthetic (seeded PCG64; shapes of the pages' workloads)",
             "config": {
                 "workload": w.name, "context_len": w.context_len,
@@ -537,6 +552,8 @@ def run_ours(args, dist, rank, world, local):
                 "note": "fm_score_multi, three key sets (one per memory indexer), L2 flushed, eager call queued "
                         "behind a device-side wait"},
             "step_hbm_gbs": step_bytes / (statistics.mean(step_ms) / 1e3) / 1e9,
+            "warm_l2": {"value": K / (sum(warm_ms) / 1e3), "unit": "steps/s", "ms_per_step": statistics.mean(warm_ms),
+                        "note": "the same graph-replayed steps without the L2 flush between them"},
             "lru_hit_rate": (st["hits"] / sel_total) if sel_total else None,
             "staged_bytes_per_step": st["h2d_bytes"] / K,
             "selected_per_step": st["selected"] / K,
@@ -559,49 +576,34 @@ def run_ours(args, dist, rank, world, local):
         e2e = run_e2e(args, w, ds, spec, graph)
         if result is not None:
             result["e2e"] = e2e
-    gather = run_miss_gather(w, ds, stream)
+    link = host_link_gbs(device)
+    gather = run_miss_gather(w, ds, stream, cold=False, link=link)
+    gather_cold = run_miss_gather(w, ds, stream, cold=True, link=link)
     if result is not None:
         result["miss_gather"] = gather
+        result["miss_gather_cold"] = gather_cold
     ds.close()
+    del flush, fm_q_all, q_all
+    torch.cuda.synchronize()
+    if result is not None and world == 1 and not args.no_sweep:
+        # the other workloads of the metric, one compact record each
+        sweep = {}
+        for name in [x for x in args.sweep.split(",") if x and x != w.name]:
+            try:
+                sweep[name] = sweep_record(name, args, device, link)
+            except Exception as exc:   # a failed workload is reported, the headline stands
+                sweep[name] = {"error": f"{type(exc).__name__}: {exc}"}
+            torch.cuda.empty_cache()
+        result["workloads"] = sweep
     return result
 
 
-def run_miss_gather(w, ds, stream):
-    """Host-link roofline of the miss gather: kvswap_stage calls in which every
-    selected chunk of a swapped layer misses (disjoint chunk sets in turn, so the
-    LRU always evicts a set staged earlier), timed after every row's host pages
-    were read once, against a plain pinned H2D copy of 256 MiB in the same run."""
+def host_link_gbs(device):
+    """A plain pinned H2D copy of 256 MiB, best of 3: the host link's measured rate."""
     import torch
-    if not any(ds.swap):
-        return None
-    m = w.index_topk if w.select_mode == C.SELECT_TOPK else w.clamp
-    n_sets = 3 if w.gpu_chunks >= 2 * m else 2
-    if w.n_chunks < n_sets * m:
-        return None
-    sets = [torch.arange(i * m, (i + 1) * m, dtype=torch.int32, device=ds.sel.device) for i in range(n_sets)]
-
-    def select_set(i):
-        ds.sel[:, :m] = sets[i % n_sets]
-        ds.count.fill_(m)
-
-    for i in range(2 * n_sets):                         # fill the slots, then read every row once more
-        select_set(i)
-        ds.stage(-1, stream)
-    torch.cuda.synchronize()
-    ds.reset_stats()
-    R = 6
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(R)]
-    for i in range(R):
-        select_set(2 * n_sets + i)                      # outside the timed span
-        ev[i][0].record(stream)
-        ds.stage(-1, stream)
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    assert ds.check_error() == 0, "device error during the miss-gather measurement"
-    st = ds.stats()
-    secs = sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3
     src = torch.empty(64 << 20, dtype=torch.float32).pin_memory()
-    dst = torch.empty(src.shape, dtype=torch.float32, device=ds.sel.device)
+    dst = torch.empty(src.shape, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
     link = 0.0
     for _ in range(3):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -610,11 +612,159 @@ def run_miss_gather(w, ds, stream):
         b.record(stream)
         b.synchronize()
         link = max(link, src.numel() * 4 / (a.elapsed_time(b) / 1e3) / 1e9)
+    return link
+
+
+def run_miss_gather(w, ds, stream, cold=False, link=None):
+    """Host-link roofline of the miss gather: kvswap_stage calls in which every
+    selected chunk of a swapped layer misses (disjoint chunk sets in turn, so the
+    LRU always evicts a set staged earlier). Warm: every row's host pages were
+    read once just before (the rows of the first chunk sets, read twice in
+    turn). Cold: chunk sets from the top of the context that no step selected,
+    read for the first time since their store (only where the context has
+    room for them). Compared with a plain pinned H2D copy of 256 MiB."""
+    import torch
+    if not any(ds.swap):
+        return None
+    m = w.index_topk if w.select_mode == C.SELECT_TOPK else w.clamp
+    n_sets = 3 if w.gpu_chunks >= 2 * m else 2
+    R = 4 if cold else 6
+    if cold and w.n_chunks < 64 * m:
+        return {"value": None, "note": "context too small for rows unread since their store"}
+    if w.n_chunks < n_sets * m:
+        return None
+    dev = ds.sel.device
+    if cold:
+        sets = [torch.arange(w.n_chunks - (i + 1) * m, w.n_chunks - i * m, dtype=torch.int32, device=dev)
+                for i in range(R)]
+    else:
+        sets = [torch.arange(i * m, (i + 1) * m, dtype=torch.int32, device=dev) for i in range(n_sets)]
+
+    def select_set(i):
+        ds.sel[:, :m] = sets[i % len(sets)]
+        ds.count.fill_(m)
+
+    if not cold:
+        for i in range(2 * n_sets):                     # fill the slots, then read every row once more
+            select_set(i)
+            ds.stage(-1, stream)
+    torch.cuda.synchronize()
+    ds.reset_stats()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(R)]
+    for i in range(R):
+        select_set(i if cold else 2 * n_sets + i)       # outside the timed span
+        ev[i][0].record(stream)
+        ds.stage(-1, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert ds.check_error() == 0, "device error during the miss-gather measurement"
+    st = ds.stats()
+    secs = sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3
+    link = link if link is not None else host_link_gbs(dev)
     gbs = st["h2d_bytes"] / secs / 1e9
     return {"gbs": gbs, "host_link_gbs": link, "frac": gbs / link, "misses_per_call": st["misses"] / R,
             "hits": st["hits"], "us_per_call": secs / R * 1e6,
             "note": f"kvswap_stage (resolve + zero-copy gather) of {m} chunks per sequence, all missing in every "
-                    f"swapped layer, rows read once before; host link = pinned cudaMemcpyAsync H2D of 256 MiB"}
+                    f"swapped layer, {'rows not read since their store' if cold else 'rows read once before'}; "
+                    f"host link = pinned cudaMemcpyAsync H2D of 256 MiB"}
+
+
+def sweep_record(name, args, device, link):
+    """A compact record of one more workload: graph-replayed steps with the L2
+    flushed and warm, per-call device times (attention roofline, scoring +
+    selection pass), the swap counters, and the miss gather on warm and cold rows."""
+    import torch
+    w = C.get(name)
+    t0 = time.perf_counter()
+    ds, spec, fm_q_all, q_all = setup(w, device)
+    setup_s = time.perf_counter() - t0
+    try:
+        stream = torch.cuda.current_stream()
+        flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+        def bind(t):
+            ds.fm_q.copy_(fm_q_all[(t % w.steps) // w.lookahead])
+            ds.q.copy_(q_all[t % q_all.shape[0]])
+
+        W, K = 3, 10
+        for t in range(W):
+            bind(t)
+            ds.step(spec, stream)
+        torch.cuda.synchronize()
+        assert ds.check_error() == 0, "device error during warm-up"
+        (graph,) = ds.capture(spec)
+        ds.reset_stats()
+        cold_ms, warm_ms = [], []
+        # the timed steps straddle a lookahead boundary (new needles: misses)
+        t_first = max(W, w.lookahead - K // 2)
+        for flushed, out in ((True, cold_ms), (False, warm_ms)):
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+            for i in range(K):
+                bind(t_first + i + (0 if flushed else w.lookahead))
+                if flushed:
+                    flush.zero_()
+                    flush.sum()
+                ev[i][0].record(stream)
+                graph.replay()
+                ev[i][1].record(stream)
+            torch.cuda.synchronize()
+            out.extend(e0.elapsed_time(e1) for e0, e1 in ev)
+            if flushed:
+                st = ds.stats()
+        assert ds.check_error() == 0, "device error during the timed steps"
+        sp = {"score": [], "select": [], "stage": [], "attend": []}
+        counts, sel_counts = [], []
+        for i in range(6):
+            bind(t_first + 2 * w.lookahead + i)
+            flush.zero_()
+            flush.sum()
+            torch.cuda._sleep(HOLD_CYCLES)
+            q = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            q[0].record(stream)
+            ds.score(spec, stream)
+            q[1].record(stream)
+            ds.select(spec, stream)
+            q[2].record(stream)
+            ds.stage(-1, stream)
+            q[3].record(stream)
+            ds.attend(-1, stream)
+            q[4].record(stream)
+            q[4].synchronize()
+            if i >= 1:
+                for j, key in enumerate(("score", "select", "stage", "attend")):
+                    sp[key].append(q[j].elapsed_time(q[j + 1]))
+                counts.append(ds.count_l.cpu().numpy().copy())
+                sel_counts.extend(int(c) for c in ds.count.cpu().numpy())
+        assert ds.check_error() == 0, "device error during the per-call timing"
+        peak, _ = measured_peaks()
+        a_us = statistics.median(sp["attend"]) * 1e3
+        a_bytes = statistics.mean(attn_bytes(w, c) for c in counts)
+        p_us = (statistics.median(sp["score"]) + statistics.median(sp["select"])) * 1e3
+        sel_total = st["hits"] + st["misses"]
+        rec = {
+            "value": K / (sum(cold_ms) / 1e3), "unit": "steps/s", "ms_per_step": statistics.mean(cold_ms),
+            "warm_l2": {"value": K / (sum(warm_ms) / 1e3), "ms_per_step": statistics.mean(warm_ms)},
+            "batch": w.batch, "context_len": w.context_len, "n_chunks": w.n_chunks,
+            "lsa_attend": {"us": a_us, "algorithmic_bytes": a_bytes, "gbs": a_bytes / a_us / 1e3,
+                           "frac": a_bytes / a_us / 1e3 / peak},
+            "score_select_pass": {"us": p_us, "score_us": statistics.median(sp["score"]) * 1e3,
+                                  "select_us": statistics.median(sp["select"]) * 1e3,
+                                  "score_kernel": scoring_kernel(w), "bytes": pass_bytes(w),
+                                  "gbs": pass_bytes(w) / p_us / 1e3, "frac": pass_bytes(w) / p_us / 1e3 / peak},
+            "kvswap_stage_us": statistics.median(sp["stage"]) * 1e3,
+            "lru_hit_rate": (st["hits"] / sel_total) if sel_total else None,
+            "staged_bytes_per_step": st["h2d_bytes"] / K,
+            "selected_count": {"min": min(sel_counts), "median": statistics.median(sel_counts),
+                               "max": max(sel_counts)},
+            "setup_s": setup_s,
+            "steps": K, "warmup": W,
+        }
+        rec["miss_gather_warm"] = run_miss_gather(w, ds, stream, cold=False, link=link)
+        rec["miss_gather_cold"] = run_miss_gather(w, ds, stream, cold=True, link=link)
+        return rec
+    finally:
+        ds.close()
+        torch.cuda.synchronize()
 
 
 def run_e2e(args, w, ds, spec, graph):
@@ -710,15 +860,46 @@ def blas_threads():
         n = max((i.get("num_threads", 1) for i in info), default=1)
         return int(n)
     except Exception:
+        return None
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
         return os.cpu_count() or 1
 
 
+ONE_THREAD_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1",
+                  "BLIS_NUM_THREADS": "1", "VECLIB_MAXIMUM_THREADS": "1"}
+
+
+def oracle_seconds_subprocess(name, n_steps, one_thread):
+    """Seconds of the oracle on the first ``n_steps`` steps of workload ``name``,
+    timed in a fresh interpreter (its BLAS pinned to one thread when asked; the
+    GPU is not touched)."""
+    env = dict(os.environ)
+    if one_thread:
+        env.update(ONE_THREAD_ENV)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--config", name, "--oracle-seconds",
+                        str(n_steps)], capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr.strip()[-300:])
+    return float(r.stdout.strip().splitlines()[-1])
+
+
 def cpu_baseline(w, sample_steps=0):
-    n = sample_steps or {"tiny": 256, "ctx8k": 128}.get(w.name, 8)
-    secs = oracle_sample(w, n)
-    return {"value": n / secs, "unit": "steps/s", "cores": blas_threads(), "kind": "oracle",
-            "sample": f"first {n} decode steps of {w.name} (fp64 numpy oracle, host cores; "
-                      f"input generation excluded)", "seconds": secs}
+    n = sample_steps or {"tiny": 256, "ctx8k": 96}.get(w.name, 8)
+    cores = host_cores()
+    secs_all = oracle_seconds_subprocess(w.name, n, one_thread=False)
+    secs_one = oracle_seconds_subprocess(w.name, n, one_thread=True)
+    return {"value": n / secs_all, "unit": "steps/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n} decode steps of {w.name} (fp64 numpy oracle; input generation excluded)",
+            "seconds": secs_all,
+            "threading": "numpy's BLAS on every host core for the matrix products; selection, LRU and the step "
+                         "loop are single-threaded Python",
+            "blas_threads": blas_threads(),
+            "single_thread": {"value": n / secs_one, "unit": "steps/s", "seconds": secs_one, "cores": 1}}
 
 
 def run_reference(args, rank):
@@ -735,13 +916,17 @@ def run_reference(args, rank):
             "steps": n, "warmup": args.warmup, "ms_per_step": secs / n * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name},
-            "cpu_baseline": {"value": v, "unit": "steps/s", "cores": blas_threads(), "kind": "oracle",
+            "cpu_baseline": {"value": v, "unit": "steps/s", "cores": host_cores(), "kind": "oracle",
+                             "blas_threads": blas_threads(),
                              "sample": f"{n} decode steps of {w.name} per timed run"},
             "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 def main():
     args = parse()
+    if args.oracle_seconds:
+        print(oracle_sample(C.get(args.config), args.oracle_seconds))
+        return
     dist, rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":
         res = run_reference(args, rank)
