@@ -273,7 +273,10 @@ int fm_select(srh_ctx* ctx, const float* d_scores, int n, int mode, int k, float
  * other streams by synchronizing the device. Creating an srh_ctx allocates, so
  * such a caller uses this instead of fm_select.
  *
- * It computes exactly what fm_select computes (same kernels, same results).
+ * It computes exactly what fm_select computes (the same histogram and
+ * selection kernels, the same results). It skips fm_select's candidate pass
+ * for n above 16384, so each sequence's selection scans all n scores in one
+ * CTA: calls with n far above 16384 are much slower than fm_select's.
  * The caller owns every input and output buffer; the only scratch is the
  * per-sequence first-digit histogram, held in a fixed array compiled into the
  * library: SRH_NOALLOC_MAX_BATCH x 4096 uint32 (1 MiB). Every GPU that loads
@@ -296,7 +299,9 @@ int fm_select(srh_ctx* ctx, const float* d_scores, int n, int mode, int k, float
  * last call's histogram (each call clears it first on its stream). Calls whose
  * GPU work overlaps -- on different streams, or from threads that do not order
  * them -- race on the array and may return wrong selections: order them on
- * one stream.
+ * one stream. The scratch address found by the first call is kept for the
+ * life of the process: calls after cudaDeviceReset() on that device are not
+ * supported.
  */
 #define SRH_NOALLOC_MAX_BATCH 64
 #define SRH_NOALLOC_MAX_N (1 << 30)

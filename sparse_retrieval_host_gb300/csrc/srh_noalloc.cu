@@ -11,8 +11,16 @@
 // zeroes the rows it uses on its own stream before filling them, so calls in
 // stream order are independent, while calls whose GPU work overlaps race.
 //
-// The kernels are the ones fm_select launches; only where the histogram lives
-// differs, so results are identical to fm_select's on the same inputs.
+// It launches fm_select's histogram and selection kernels, with the histogram
+// in the fixed array, so its results are identical to fm_select's on the same
+// inputs. It does not run fm_select's candidate pass for n above 16384 (that
+// pass needs a candidate buffer): each sequence's selection then scans all n
+// scores in one CTA, so calls with n far above 16384 are much slower than
+// fm_select's.
+//
+// The array's device address is looked up once per device ordinal and kept for
+// the life of the process; calls after cudaDeviceReset() on that device (which
+// unloads the library's device code) are not supported.
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>

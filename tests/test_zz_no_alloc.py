@@ -101,3 +101,24 @@ def test_noalloc_matches_fm_select_on_consecutive_calls(abi):
             assert np.array_equal(outs[0][0][r, :512].cpu().numpy(), O.select_topk(s0[r].astype(np.float64), 512))
     finally:
         abi.srh_destroy(ctx)
+
+
+@pytest.mark.gpu
+def test_noalloc_full_batch_reaches_the_last_scratch_row(abi):
+    """At batch = SRH_NOALLOC_MAX_BATCH every row of the fixed scratch is used:
+    two calls in a row (the second with other scores) against the oracle."""
+    import torch
+    torch.cuda.set_device(0)
+    B, n, S, k = abi.SRH_NOALLOC_MAX_BATCH, 4097, 64, 16
+    rng = np.random.default_rng(64)
+    dev = torch.device("cuda", 0)
+    for kind in ("random", "ties"):
+        s_np = _scores(kind, B, n, rng)
+        sel = torch.full((B, S), -1, dtype=torch.int32, device=dev)
+        cnt = torch.full((B,), -1, dtype=torch.int32, device=dev)
+        abi.fm_select_noalloc(torch.from_numpy(s_np).to(dev), B, n, abi.SRH_SELECT_TOPK, k, 0.5, 0, S, sel, cnt)
+        torch.cuda.synchronize()
+        got, got_c = sel.cpu().numpy(), cnt.cpu().numpy()
+        assert np.all(got_c == k)
+        for r in range(B):
+            assert np.array_equal(got[r, :k], O.select_topk(s_np[r].astype(np.float64), k)), (kind, r)
