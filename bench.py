@@ -436,6 +436,8 @@ def run_ours(args, dist, rank, world, local):
             sp_attn.append(q[3].elapsed_time(q[4]))
             sp_counts.append(ds.count_l.cpu().numpy().copy())
 
+    ch_us = chained_pass_us(ds, spec, stream, flush, bind, args.warmup + K + KP + KB + 10)
+
     # one key set per memory indexer (fm_score_multi): the scoring call alone
     from sparse_retrieval_host_gb300 import abi
     keys3 = torch.empty((3,) + tuple(ds.keys.shape), dtype=ds.keys.dtype, device=device)
@@ -539,8 +541,13 @@ def run_ours(args, dist, rank, world, local):
                 "score_kernel": scoring_kernel(w),
                 "frac": pass_bytes(w) / ((statistics.median(sp_score) + statistics.median(sp_select)) / 1e3) / 1e9
                 / peak,
-                "note": "fm_score then fm_select, eager, queued behind the L2 flush; bytes = keys + score write + "
-                        "selection reads (256 + 12 per chunk and sequence)"},
+                "chained": {"us": ch_us, "gbs": pass_bytes(w) / ch_us / 1e3,
+                            "frac": pass_bytes(w) / ch_us / 1e3 / peak,
+                            "note": "as the decode step issues them: fm_select chained to fm_score (its kernel "
+                                    "launched while the scoring kernel runs), one span"},
+                "note": "fm_score then fm_select, eager and unchained (each call pays its launch), queued behind "
+                        "the L2 flush; bytes = keys + score write + selection reads (256 + 12 per chunk and "
+                        "sequence)"},
             "score_fp8_keys": {
                 "us": statistics.median(fp8_ms) * 1e3,
                 "gbs": w.batch * w.n_chunks * (C.INDEXER_DIM + 4 + 4) / (statistics.median(fp8_ms) / 1e3) / 1e9,
@@ -669,6 +676,32 @@ def run_miss_gather(w, ds, stream, cold=False, link=None):
                     f"host link = pinned cudaMemcpyAsync H2D of 256 MiB"}
 
 
+def chained_pass_us(ds, spec, stream, flush, bind, t0, reps=6):
+    """The scoring + selection pass as the decode step issues it: fm_score, then
+    fm_select chained to it (its kernel launched while the scoring kernel runs),
+    queued behind the L2 flush and a device-side wait; median span in us."""
+    import torch
+    from sparse_retrieval_host_gb300 import abi
+    spans = []
+    for i in range(reps):
+        bind(t0 + i)
+        flush.zero_()
+        flush.sum()
+        torch.cuda._sleep(HOLD_CYCLES)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ds.score(spec, stream)
+        abi.srh_set_chained(ds.ctx, True)
+        ds.select(spec, stream)
+        abi.srh_set_chained(ds.ctx, False)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= 1:
+            spans.append(e0.elapsed_time(e1) * 1e3)
+    assert ds.check_error() == 0, "device error during the chained pass"
+    return statistics.median(spans)
+
+
 def sweep_record(name, args, device, link):
     """A compact record of one more workload: graph-replayed steps with the L2
     flushed and warm, per-call device times (attention roofline, scoring +
@@ -736,6 +769,7 @@ def sweep_record(name, args, device, link):
                 counts.append(ds.count_l.cpu().numpy().copy())
                 sel_counts.extend(int(c) for c in ds.count.cpu().numpy())
         assert ds.check_error() == 0, "device error during the per-call timing"
+        ch_us = chained_pass_us(ds, spec, stream, flush, bind, t_first + 3 * w.lookahead)
         peak, _ = measured_peaks()
         a_us = statistics.median(sp["attend"]) * 1e3
         a_bytes = statistics.mean(attn_bytes(w, c) for c in counts)
@@ -750,7 +784,9 @@ def sweep_record(name, args, device, link):
             "score_select_pass": {"us": p_us, "score_us": statistics.median(sp["score"]) * 1e3,
                                   "select_us": statistics.median(sp["select"]) * 1e3,
                                   "score_kernel": scoring_kernel(w), "bytes": pass_bytes(w),
-                                  "gbs": pass_bytes(w) / p_us / 1e3, "frac": pass_bytes(w) / p_us / 1e3 / peak},
+                                  "gbs": pass_bytes(w) / p_us / 1e3, "frac": pass_bytes(w) / p_us / 1e3 / peak,
+                                  "chained": {"us": ch_us, "gbs": pass_bytes(w) / ch_us / 1e3,
+                                              "frac": pass_bytes(w) / ch_us / 1e3 / peak}},
             "kvswap_stage_us": statistics.median(sp["stage"]) * 1e3,
             "lru_hit_rate": (st["hits"] / sel_total) if sel_total else None,
             "staged_bytes_per_step": st["h2d_bytes"] / K,

@@ -76,13 +76,14 @@ template <int kSets>
 __global__ void __launch_bounds__(kScoreWarps * 32, kSets == 1 ? 2 : 1)
 score_kernel(const uint16_t* __restrict__ keys, long long set_stride, int n, const uint16_t* __restrict__ q,
              float scale, float b0, float b1, float b2, int ensemble, float* __restrict__ scores,
-             uint32_t* __restrict__ hist) {
+             uint32_t* __restrict__ hist, const CandSink sink) {
     __shared__ uint32_t h_s[kHistBins];
     pdl_trigger();
     const int b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h_s[i] = 0;
+    if (hist)
+        for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h_s[i] = 0;
 
     // B fragments: bq[i][k-step][2]; indexer i = n-tile i, head = g.
     uint32_t bq[kIdx][8][2];
@@ -154,16 +155,19 @@ score_kernel(const uint16_t* __restrict__ keys, long long set_stride, int n, con
             ea = (sa[0] + sa[1] + sa[2]) / 3.0f;
             eb = (sb[0] + sb[1] + sb[2]) / 3.0f;
         }
-        const long long c0 = tile * 16;
-        if (t == 0 && c0 + g < n) {
-            scores_b[c0 + g] = ea;
-            atomicAdd(&h_s[ordered_key(ea) >> 20], 1u);
-        } else if (t == 1 && c0 + g + 8 < n) {
-            scores_b[c0 + g + 8] = eb;
-            atomicAdd(&h_s[ordered_key(eb) >> 20], 1u);
+        // lane t = 0 writes chunk c0 + g, lane t = 1 chunk c0 + g + 8
+        const long long c = tile * 16 + g + (t == 1 ? 8 : 0);
+        const float e = t == 0 ? ea : eb;
+        const bool wr = t < 2 && c < n;
+        const uint32_t key = ordered_key(e);
+        if (wr) {
+            scores_b[c] = e;
+            if (hist) atomicAdd(&h_s[key >> 20], 1u);
         }
+        if (sink.cand) append_candidate(sink, b, wr && key > sink.key, key, (uint32_t)c);
         cur = nxt;
     }
+    if (!hist) return;
     __syncthreads();
     uint32_t* hb = hist + (size_t)b * kHistBins;
     for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
@@ -190,9 +194,14 @@ __global__ void hist_kernel(const float* __restrict__ scores, int n, uint32_t* _
 
 cudaError_t launch_score(const uint16_t* keys, int n, int B, const uint16_t* q, float scale,
                          const float* bias3, int ensemble, float* scores, uint32_t* hist, uint32_t* err,
-                         int sm_count, cudaStream_t st, int key_sets, bool clear_hist) {
-    if (clear_hist) {
+                         int sm_count, cudaStream_t st, int key_sets, bool clear_hist, CandSink sink,
+                         bool clear_cand) {
+    if (clear_hist && hist) {
         const cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(uint32_t) * kHistBins * B, st);
+        if (e != cudaSuccess) return e;
+    }
+    if (clear_cand && sink.cand) {
+        const cudaError_t e = cudaMemsetAsync(sink.cnt, 0, sizeof(int) * B, st);
         if (e != cudaSuccess) return e;
     }
     // One key set over many tiles: the tensor-core stream (k_score_tc.cu). Its
@@ -200,7 +209,7 @@ cudaError_t launch_score(const uint16_t* keys, int n, int B, const uint16_t* q, 
     // this kernel's, which its higher streaming rate repays only on long streams:
     // measured 16.8 against 15.0 us at 2^18 chunks, 47 against 60 us at 2^20.
     if (key_sets == 1 && (long long)B * n >= kTcMinChunks)
-        return launch_score_tc(keys, n, B, q, scale, bias3, ensemble, scores, hist, err, sm_count, st);
+        return launch_score_tc(keys, n, B, q, scale, bias3, ensemble, scores, hist, err, sm_count, st, sink);
     const long long tiles = (n + 15) / 16;
     long long bx = (tiles + kScoreWarps - 1) / kScoreWarps;
     const long long cap = (2LL * sm_count + B - 1) / B;
@@ -210,10 +219,10 @@ cudaError_t launch_score(const uint16_t* keys, int n, int B, const uint16_t* q, 
     const long long set_stride = (long long)B * n * kIdxDim;
     if (key_sets == 3)
         score_kernel<3><<<grid, kScoreWarps * 32, 0, st>>>(keys, set_stride, n, q, scale, bias3[0], bias3[1],
-                                                           bias3[2], ensemble, scores, hist);
+                                                           bias3[2], ensemble, scores, hist, sink);
     else
         score_kernel<1><<<grid, kScoreWarps * 32, 0, st>>>(keys, 0, n, q, scale, bias3[0], bias3[1], bias3[2],
-                                                           ensemble, scores, hist);
+                                                           ensemble, scores, hist, sink);
     return cudaGetLastError();
 }
 

@@ -71,8 +71,9 @@ struct ScoreTcArgs {
     float bias[3];
     int ensemble;
     float* scores;
-    uint32_t* hist;
+    uint32_t* hist;           // nullptr: no histogram
     uint32_t* err;
+    CandSink sink;            // sink.cand == nullptr: no candidate list
 };
 
 // Bounded wait that also leaves when another role has aborted the CTA.
@@ -110,7 +111,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(&bs.tmem_base, kAcc * kN);
-    for (int i = tid; i < kHistBins; i += kThreadsTc) h_s[i] = 0;
+    if (a.hist)
+        for (int i = tid; i < kHistBins; i += kThreadsTc) h_s[i] = 0;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -179,7 +181,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         float* scores_b = a.scores + (size_t)b * a.n;
         for (int i = 0; i < nt; ++i) {
             const int x = i % kAcc;
-            if (!wait_tc(&bs.tfull[x], (i / kAcc) & 1, abort)) {
+            // warp-uniform: the candidate append below is a warp collective
+            const bool got = wait_tc(&bs.tfull[x], (i / kAcc) & 1, abort);
+            if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
             }
@@ -203,10 +207,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             const float e = a.ensemble == SRH_ENSEMBLE_MAX ? fmaxf(fmaxf(si[0], si[1]), si[2])
                                                            : (si[0] + si[1] + si[2]) / 3.0f;
             const int c = (t0 + i) * kTile + r;
+            const uint32_t key = ordered_key(e);
             if (c < a.n) {
                 scores_b[c] = e;
-                atomicAdd(&h_s[ordered_key(e) >> 20], 1u);
+                if (a.hist) atomicAdd(&h_s[key >> 20], 1u);
             }
+            if (a.sink.cand) append_candidate(a.sink, b, c < a.n && key > a.sink.key, key, (uint32_t)c);
         }
     }
 
@@ -214,9 +220,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     tc_fence_before();
     const bool failed = __syncthreads_or(!ok);
     if (failed && tid == 0) atomicOr(a.err, kErrTimeout);
-    uint32_t* hb = a.hist + (size_t)b * kHistBins;
-    for (int i = tid; i < kHistBins; i += kThreadsTc)
-        if (h_s[i]) atomicAdd(&hb[i], h_s[i]);
+    if (a.hist) {
+        uint32_t* hb = a.hist + (size_t)b * kHistBins;
+        for (int i = tid; i < kHistBins; i += kThreadsTc)
+            if (h_s[i]) atomicAdd(&hb[i], h_s[i]);
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(bs.tmem_base, kAcc * kN);
@@ -281,7 +289,7 @@ cudaError_t set_score_tc_attrs() {
 
 cudaError_t launch_score_tc(const uint16_t* keys, int n, int B, const uint16_t* q, float scale, const float* bias3,
                             int ensemble, float* scores, uint32_t* hist, uint32_t* err, int sm_count,
-                            cudaStream_t st) {
+                            cudaStream_t st, CandSink sink) {
     CUtensorMap kmap, qmap;
     if (!encode_rows(&kmap, keys, n, B, kTile) || !encode_rows(&qmap, q, kIdx * kIdxHeads, B, kN))
         return cudaErrorNotSupported;
@@ -301,6 +309,7 @@ cudaError_t launch_score_tc(const uint16_t* keys, int n, int B, const uint16_t* 
     args.scores = scores;
     args.hist = hist;
     args.err = err;
+    args.sink = sink;
     score_tc_kernel<<<dim3((unsigned)parts, (unsigned)B), kThreadsTc, kSmemTc, st>>>(kmap, qmap, args);
     return cudaGetLastError();
 }

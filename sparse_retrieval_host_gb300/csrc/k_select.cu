@@ -45,7 +45,7 @@ constexpr int kCollectThreads = 256;
 constexpr int kCollectPer = 16;                         // scores per collect thread
 
 __device__ __forceinline__ unsigned long long composite(uint32_t key, uint32_t idx) {
-    return ((unsigned long long)key << 32) | (unsigned long long)(~idx);
+    return candidate_key(key, idx);
 }
 
 // Inclusive block scan of one int per thread (blockDim.x == kSelThreads).

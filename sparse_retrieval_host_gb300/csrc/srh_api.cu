@@ -468,12 +468,31 @@ int score_impl(srh_ctx* ctx, const uint16_t* d_keys, int key_sets, int n, const 
         return fail(ctx, SRH_ERR_INVALID, "unknown ensemble");
     if (((uintptr_t)d_keys | (uintptr_t)d_q) & 15) return fail(ctx, SRH_ERR_INVALID, "keys/queries must be 16-byte aligned");
     if (!std::isfinite(scale)) return fail(ctx, SRH_ERR_INVALID, "scale must be finite");
-    const cudaError_t e = launch_score(d_keys, n, ctx->B, d_q, scale, bias3, ensemble, d_scores, ctx->d_hist,
-                                       ctx->d_err, ctx->sm_count, (cudaStream_t)stream, key_sets, !ctx->hist_clean);
+    // After a threshold selection, the pass also appends the chunks above that
+    // threshold to the candidate list, and builds no histogram: the next
+    // selection with the same threshold uses the list and skips its own pass
+    // over the scores (a top-k selection rebuilds the histogram).
+    const bool fused = ctx->thresh_hint_valid;
+    CandSink sink{0u, nullptr, nullptr, 0};
+    if (fused) sink = CandSink{ordered_key(ctx->thresh_hint), ctx->d_cand, ctx->d_cand_cnt, select_cand_cap()};
+    const cudaError_t e = launch_score(d_keys, n, ctx->B, d_q, scale, bias3, ensemble, d_scores,
+                                       fused ? nullptr : ctx->d_hist, ctx->d_err, ctx->sm_count,
+                                       (cudaStream_t)stream, key_sets, !fused && !ctx->hist_clean, sink,
+                                       fused && !ctx->cand_clean);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "fm_score launch");
-    ctx->hist_clean = false;
-    ctx->hist_scores = d_scores;
-    ctx->hist_n = n;
+    if (fused) {
+        ctx->cand_clean = false;
+        ctx->cand_scores = d_scores;
+        ctx->cand_n = n;
+        ctx->cand_thresh = ctx->thresh_hint;
+        ctx->hist_scores = nullptr;
+        ctx->hist_n = -1;
+    } else {
+        ctx->hist_clean = false;
+        ctx->hist_scores = d_scores;
+        ctx->hist_n = n;
+        ctx->cand_scores = nullptr;
+    }
     return SRH_OK;
 }
 }  // namespace
@@ -517,6 +536,7 @@ int fm_score_fp8(srh_ctx* ctx, const uint8_t* d_codes, const float* d_kscale, in
     ctx->hist_clean = false;
     ctx->hist_scores = d_scores;
     ctx->hist_n = n;
+    ctx->cand_scores = nullptr;   // this pass builds no candidate list
     return SRH_OK;
 }
 
@@ -537,6 +557,24 @@ int fm_select(srh_ctx* ctx, const float* d_scores, int n, int mode, int k, float
         return fail(ctx, SRH_ERR_INVALID, "unknown selection mode");
     }
     cudaStream_t st = (cudaStream_t)stream;
+    if (mode == SRH_SELECT_THRESH) {
+        const bool have_list = ctx->cand_scores == d_scores && ctx->cand_n == n && ctx->cand_thresh == thresh;
+        ctx->thresh_hint_valid = true;     // the next scoring pass builds the list for this threshold
+        ctx->thresh_hint = thresh;
+        if (have_list) {
+            // the scoring pass appended every chunk above the threshold: select from that list
+            ctx->cand_scores = nullptr;
+            const cudaError_t e = launch_select(d_scores, n, ctx->B, mode, k, thresh, clamp, ctx->S, nullptr, d_sel,
+                                                d_count, st, ctx->d_cand, ctx->d_cand_cnt, select_cand_cap(),
+                                                ctx->chained);
+            if (e != cudaSuccess) return cuda_fail(ctx, e, "fm_select launch");
+            ctx->cand_clean = true;   // the select kernel zeroes the counts it reads
+            return SRH_OK;
+        }
+    } else {
+        ctx->thresh_hint_valid = false;
+    }
+    ctx->cand_scores = nullptr;
     uint32_t* hist = nullptr;
     bool chained = ctx->chained;   // the select kernel follows a kernel of this call or of fm_score
     if (mode == SRH_SELECT_TOPK || clamp > 0) {

@@ -5,6 +5,7 @@
 #include <cuda_fp8.h>
 
 #include <cstdint>
+#include <cstring>
 #include <string>
 #include <vector>
 
@@ -180,6 +181,14 @@ struct Ctx {
     unsigned long long* d_cand = nullptr; // [B][select_cand_cap()] candidate composites
     int* d_cand_cnt = nullptr;          // [B]
     bool cand_clean = true;             // d_cand_cnt is zero (cleared, or consumed by a selection)
+    // threshold selection: the threshold of the last fm_select in that mode; the
+    // next scoring pass appends the chunks above it to d_cand, and a selection
+    // with that threshold on those scores uses the list (no candidate pass)
+    bool thresh_hint_valid = false;
+    float thresh_hint = 0.f;
+    const float* cand_scores = nullptr; // the d_scores d_cand was built from by a scoring pass
+    int cand_n = -1;
+    float cand_thresh = 0.f;
     const float* hist_scores = nullptr; // the d_scores the histogram describes
     int hist_n = -1;
     int2* d_miss = nullptr;             // [L][B][S] (chunk, slot)
@@ -207,10 +216,43 @@ struct Ctx {
 #ifdef __CUDACC__
 // Order-preserving 32-bit key of a score: a larger score gives a larger key and
 // -0 maps like +0, so equal scores give equal keys.
-__device__ __forceinline__ uint32_t ordered_key(float s) {
+__host__ __device__ __forceinline__ uint32_t ordered_key(float s) {
     s = (s == 0.0f) ? 0.0f : s;
-    const uint32_t u = __float_as_uint(s);
+    uint32_t u;
+    memcpy(&u, &s, sizeof u);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+// The selection's unique 64-bit key of chunk idx: larger = (score descending,
+// index ascending).
+__host__ __device__ __forceinline__ unsigned long long candidate_key(uint32_t key, uint32_t idx) {
+    return ((unsigned long long)key << 32) | (unsigned long long)(~idx);
+}
+
+// Where a scoring pass appends the chunks whose key exceeds `key` (the
+// selection's threshold): the candidate list [B][cap] and counts [B] that the
+// select kernel consumes. A count past `cap` means the list overflowed (the
+// select kernel then scans all the scores). cand == nullptr: no list.
+struct CandSink {
+    uint32_t key;
+    unsigned long long* cand;
+    int* cnt;
+    int cap;
+};
+
+// Appends (key, idx) to the sequence's list when `pass`; every lane of the warp
+// calls it (one atomic per warp).
+__device__ __forceinline__ void append_candidate(const CandSink& sk, int b, bool pass, uint32_t key,
+                                                 uint32_t idx) {
+    const unsigned m = __ballot_sync(0xffffffffu, pass);
+    if (!m) return;
+    const int lane = threadIdx.x & 31, leader = __ffs(m) - 1;
+    int base = 0;
+    if (lane == leader) base = atomicAdd(&sk.cnt[b], __popc(m));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    if (pass) {
+        const int pos = base + __popc(m & ((1u << lane) - 1u));
+        if (pos < sk.cap) sk.cand[(size_t)b * sk.cap + pos] = candidate_key(key, idx);
+    }
 }
 #endif
 
@@ -218,15 +260,19 @@ __device__ __forceinline__ uint32_t ordered_key(float s) {
 // The scoring launchers add into the first-digit histogram `hist`; with
 // `clear_hist` they zero it first (the select kernel leaves the rows it reads
 // zeroed, so a histogram consumed by a selection needs no clearing).
+// With sink.cand set, the scoring kernels also append the chunks above
+// sink.key to the candidate list (the counts are zeroed first with
+// clear_cand); hist may be nullptr (no histogram).
 cudaError_t launch_score(const uint16_t* keys, int n, int B, const uint16_t* q, float scale,
                          const float* bias3, int ensemble, float* scores, uint32_t* hist, uint32_t* err,
-                         int sm_count, cudaStream_t st, int key_sets, bool clear_hist);
+                         int sm_count, cudaStream_t st, int key_sets, bool clear_hist, CandSink sink,
+                         bool clear_cand);
 // One key set on the tensor cores (TMA-streamed key tiles, tcgen05, TMEM);
 // launch_score uses it from this many chunks per call (all sequences) up.
 constexpr long long kTcMinChunks = 1LL << 19;
 cudaError_t launch_score_tc(const uint16_t* keys, int n, int B, const uint16_t* q, float scale, const float* bias3,
                             int ensemble, float* scores, uint32_t* hist, uint32_t* err, int sm_count,
-                            cudaStream_t st);
+                            cudaStream_t st, CandSink sink);
 cudaError_t launch_hist(const float* scores, int n, int B, uint32_t* hist, cudaStream_t st, bool clear_hist);
 cudaError_t launch_quantize_keys(const uint16_t* keys, long long total, uint8_t* codes, float* kscale,
                                  int sm_count, cudaStream_t st);
