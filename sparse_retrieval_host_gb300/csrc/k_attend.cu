@@ -55,6 +55,7 @@
 // configuration, so identical rows give identical bits whatever slots hold
 // them.
 #include <cmath>
+#include <cstddef>
 
 #include "srh_internal.cuh"
 #include "umma.cuh"
@@ -80,24 +81,36 @@ constexpr float kLazy = 8.0f;                       // reference max moves past 
 constexpr int kMaxSplits = (kWindow + kMaxSelect + kTileRows - 1) / kTileRows;
 constexpr int kMaxDuties = 4;                       // split pairs one CTA takes part in
 constexpr int kMlStride = kAttnMlStride;            // floats per partial's statistics: m, l, scale
-constexpr int kMergeBatch = 5;                      // splits whose values a merging thread loads at once
+// A merge's inputs in the E area: each split's share of the partial (16 bytes
+// per 8 values), then the splits' statistics.
+constexpr int kMergeMlOff = 72 * 1024;
+constexpr int kMergeWOff = 92 * 1024;                // the combined weights [split][head]
+static_assert(64 * kKvDim * 2 + kMaxSplits * (16 + 127) <= kMergeMlOff, "merge shares overlap the statistics");
+static_assert(kMergeMlOff + kMaxSplits * kMlStride * 4 <= kMergeWOff, "merge statistics overlap the weights");
+static_assert(kMergeWOff + kMaxSplits * 64 * 4 <= 8 * kDBlockE, "merge inputs exceed the E area");
+static_assert((kMlStride * 4) % 16 == 0, "partial statistics rows must be 16-byte multiples");
 
 struct Misc {
-    uint64_t s_full, o_full, drain, q_full;
+    uint64_t s_full, o_full, drain, q_full, m_full;
     uint32_t tmem_base;
     int abort;
     int n_duties;
     int duty_merge[kMaxDuties];
     int duty_part[kMaxDuties];
     unsigned long long duty_target[kMaxDuties];
-    float m_used[2][64];    // reference max per head (parity of the segment's tile)
-    float l_run[2][64];     // running sum per head
-    float red[4][64];       // per-quadrant tile maxima
-    float red2[4][64];      // per-quadrant tile sums
-    float alpha[64];        // this tile's rescale factor per head
-    uint32_t wmax[kWarps];  // per-warp max |row value| (bits) of the segment
-    float inv_l[64];        // 1 / l per head at a segment's end
+    // read and written as float4: 16-byte aligned
+    alignas(16) float m_used[2][64];    // reference max per head (parity of the segment's tile)
+    alignas(16) float l_run[2][64];     // running sum per head
+    alignas(16) float red[4][64];       // per-quadrant tile maxima
+    alignas(16) float red2[4][64];      // per-quadrant tile sums
+    alignas(16) float alpha[64];        // this tile's rescale factor per head
+    alignas(16) uint32_t wmax[kWarps];  // per-warp max |row value| (bits) of the segment
+    alignas(16) float inv_l[64];        // 1 / l per head at a segment's end
 };
+static_assert(offsetof(Misc, m_used) % 16 == 0 && offsetof(Misc, red) % 16 == 0 && offsetof(Misc, inv_l) % 16 == 0 &&
+                  offsetof(Misc, l_run) % 16 == 0 && offsetof(Misc, red2) % 16 == 0 && offsetof(Misc, alpha) % 16 == 0,
+              "float4-accessed softmax state must be 16-byte aligned");
+static_assert(kOffMisc % 16 == 0, "Misc must start 16-byte aligned");
 constexpr int kSmemBytes = kOffMisc + (int)sizeof(Misc) + 1024;   // + base alignment slack
 static_assert(kSmemBytes <= 232448, "attention shared memory exceeds 227 KB");
 
@@ -135,28 +148,25 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return r;
 }
 
-// Read-only streaming load of 16 bytes (no L1 allocation).
-__device__ __forceinline__ float4 ldg_stream(const float4* p) {
-    float4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];\n"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+// Read-only streaming load of 32 bytes (no L1 allocation); p is 32-byte aligned.
+__device__ __forceinline__ void ldg_stream8(const float* p, float4& lo, float4& hi) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n"
+                 : "=f"(lo.x), "=f"(lo.y), "=f"(lo.z), "=f"(lo.w), "=f"(hi.x), "=f"(hi.y), "=f"(hi.z), "=f"(hi.w)
                  : "l"(p));
-    return v;
 }
 
-// Loads of data written earlier in this kernel by other CTAs (partials) or by
-// an earlier kernel: L2, and volatile so they stay after the waits.
-__device__ __forceinline__ uint4 ld_cg_u4(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];\n"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p)
+// Bulk copy of bytes (a multiple of 16, both addresses 16-byte aligned) from
+// global memory into shared memory, completing on bar's transaction count.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
-    return v;
 }
-__device__ __forceinline__ float ld_cg_f(const float* p) {
-    float v;
-    asm volatile("ld.global.cg.f32 %0, [%1];\n" : "=f"(v) : "l"(p) : "memory");
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];\n" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
@@ -180,11 +190,19 @@ __device__ __forceinline__ float f16_to_f32(uint32_t h) {
     return f;
 }
 
-// Max / sum over the 32 lanes of a warp for N per-lane columns at once. The
+// Maximum over the 32 lanes of a warp (every lane receives it); -inf lanes
+// take part like any other value.
+__device__ __forceinline__ float warp_max(float v) {
+    float r;
+    asm("redux.sync.max.f32 %0, %1, 0xffffffff;\n" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// Sum over the 32 lanes of a warp for N per-lane columns at once. The
 // first log2(N) steps hand half of the columns to the partner lane; afterwards
 // lane l holds column l / (32 / N), reduced over every lane.
-template <int N, bool kMax>
-__device__ __forceinline__ float reduce_cols(float (&v)[N], int lane) {
+template <int N>
+__device__ __forceinline__ float sum_cols(float (&v)[N], int lane) {
 #pragma unroll
     for (int s = 0; (1 << s) < N; ++s) {
         const int bit = 16 >> s;
@@ -195,13 +213,13 @@ __device__ __forceinline__ float reduce_cols(float (&v)[N], int lane) {
             const float send = upper ? v[i] : v[i + half];
             const float keep = upper ? v[i + half] : v[i];
             const float recv = __shfl_xor_sync(0xffffffffu, send, bit);
-            v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+            v[i] = keep + recv;
         }
     }
 #pragma unroll
     for (int bit = 16 / N; bit >= 1; bit >>= 1) {
         const float recv = __shfl_xor_sync(0xffffffffu, v[0], bit);
-        v[0] = kMax ? fmaxf(v[0], recv) : v[0] + recv;
+        v[0] += recv;
     }
     return v[0];
 }
@@ -227,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         mbar_init(&ms.o_full, 1);
         mbar_init(&ms.drain, 1);
         mbar_init(&ms.q_full, 1);
+        mbar_init(&ms.m_full, 1);
         ms.abort = 0;
         ms.n_duties = 0;
         fence_mbar_init();
@@ -280,24 +299,20 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             *reinterpret_cast<uint4*>(sm + kOffQ + (c8 >> 3) * 8192 + sw128(h, c8 & 7)) = w;
         }
     };
-    // Half h2 (d 256 h2 .. +255) of a tile row: this lane's float4s lane + 32 j
-    // (j = 0, 1) of that half, as fp16 into E row r: d-block (lane >> 4) + 2 j
-    // + 4 h2, 16-byte chunk (lane & 15) >> 1, 8-byte half lane & 1.
-    auto store_half = [&](const float4 (&v)[2], int r, int h2) {
-        unsigned char* e = sm + kOffE + ((lane >> 4) + 4 * h2) * kDBlockE + 8 * (lane & 1) + sw128(r, (lane & 15) >> 1);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const float t = fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w)));
-            amax = fmaxf(amax, t);
-            ramax = fmaxf(ramax, t);
-            *reinterpret_cast<uint2*>(e + 2 * j * kDBlockE) =
-                make_uint2(pack_f16x2(v[j].x, v[j].y), pack_f16x2(v[j].z, v[j].w));
-        }
+    // Half h2 (d 256 h2 .. +255) of a tile row: this lane's 8 values d = 8 lane
+    // + 256 h2 .. + 7, as fp16 into E row r: d-block (lane >> 3) + 4 h2, 16-byte
+    // chunk lane & 7.
+    auto store_half = [&](const float4& lo, const float4& hi, int r, int h2) {
+        const float t = fmaxf(fmaxf(fmaxf(fabsf(lo.x), fabsf(lo.y)), fmaxf(fabsf(lo.z), fabsf(lo.w))),
+                              fmaxf(fmaxf(fabsf(hi.x), fabsf(hi.y)), fmaxf(fabsf(hi.z), fabsf(hi.w))));
+        amax = fmaxf(amax, t);
+        ramax = fmaxf(ramax, t);
+        *reinterpret_cast<uint4*>(sm + kOffE + ((lane >> 3) + 4 * h2) * kDBlockE + sw128(r, lane & 7)) =
+            make_uint4(pack_f16x2(lo.x, lo.y), pack_f16x2(lo.z, lo.w), pack_f16x2(hi.x, hi.y), pack_f16x2(hi.z, hi.w));
     };
     auto zero_half = [&](int r, int h2) {
-        unsigned char* e = sm + kOffE + ((lane >> 4) + 4 * h2) * kDBlockE + 8 * (lane & 1) + sw128(r, (lane & 15) >> 1);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) *reinterpret_cast<uint2*>(e + 2 * j * kDBlockE) = make_uint2(0u, 0u);
+        *reinterpret_cast<uint4*>(sm + kOffE + ((lane >> 3) + 4 * h2) * kDBlockE + sw128(r, lane & 7)) =
+            make_uint4(0u, 0u, 0u, 0u);
     };
 
     // Rows [row0, row1) of segment sg: the count comes from the resolve kernel.
@@ -340,7 +355,18 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         q_lb = a.segs[sb].lb;
     }
 
-    pdl_wait();   // slots, counts and staged rows come from earlier kernels; partial buffers are reused
+    // Slots, counts and staged rows come from earlier kernels, and the partial
+    // buffers and arrival counts are shared with the previous call: all of them
+    // are touched only after the dependency wait. A CTA whose first segment
+    // starts with the window tile runs that tile (rows, queries, both products)
+    // before the wait, while the earlier kernels still run.
+    bool dep_ready = false;
+    auto dep_wait = [&]() {
+        if (!dep_ready) {
+            pdl_wait();
+            dep_ready = true;
+        }
+    };
     bool q_pending = sb < se;   // a queries' copy into the E area is issued and not yet converted
 
     constexpr uint32_t id1 = idesc_f16(0, 0, H);   // pass 1: K-major E and Q
@@ -353,9 +379,23 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     for (; si < se; ++si) {
         const AttnSeg sg = a.segs[si];
         const size_t lb = (size_t)sg.lb;
-        int row0, row1;
-        seg_rows(sg, row0, row1);
-        const int n_tiles = row1 > row0 ? (row1 - row0 + kTileRows - 1) / kTileRows : 0;
+        // the window tile (rows 0-127, always full) of the CTA's first segment
+        // runs before the wait; the segment's other rows are known after it
+        const bool early = !dep_ready && sg.tile0 == 0 && sg.tile1 > 0;
+        int row0 = 0, row1 = kWindow, n_tiles = 1;
+        // A split pair's arrival count before this CTA's own arrival (read after
+        // the dependency wait: every earlier call's arrivals are in). The pair is
+        // complete when it reaches the next multiple of its split count.
+        unsigned long long seen = 0;
+        auto seg_after_wait = [&]() {
+            seg_rows(sg, row0, row1);
+            n_tiles = row1 > row0 ? (row1 - row0 + kTileRows - 1) / kTileRows : 0;
+            if (sg.slot >= 0 && tid == 0) seen = ld_relaxed_u64(&a.merge_cnt[sg.merge]);
+        };
+        if (!early) {
+            dep_wait();
+            seg_after_wait();
+        }
         const int32_t* ph = a.phys + lb * a.S;
         if (si > sb && n_tiles > 0 && sg.lb != q_lb) {
             // the previous segment drained its MMAs before its epilogue: Q and E are
@@ -382,39 +422,33 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             if (lane >= kRowsPerWarp || row >= row1) return -1;
             return row < kWindow ? -1 - row : ph[row - kWindow];
         };
-        auto src_ptr = [&](int src) -> const float4* {
-            if (src < 0) return reinterpret_cast<const float4*>(a.window + (lb * kWindow + (-1 - src)) * kKvDim);
+        auto src_ptr = [&](int src) -> const float* {
+            if (src < 0) return a.window + (lb * kWindow + (-1 - src)) * kKvDim;
             int slot = src - kWindow;
             if (slot < 0 || slot >= a.G) {
                 atomicOr(a.err, kErrBounds);
                 slot = 0;
             }
-            return reinterpret_cast<const float4*>(a.staging + (lb * (size_t)a.G + slot) * kKvDim);
+            return a.staging + (lb * (size_t)a.G + slot) * kKvDim;
         };
-        // rows w + 16 (4 k + i), i < 4, of the tile at tr0: whole rows, 512
+        // row w + 16 j (j < 8) of the tile at tr0: the whole row, 1 KiB of
         // contiguous bytes per load instruction
-        auto load_rows = [&](float4 (&v)[4][4], int tr0, int k, int src) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int s = __shfl_sync(0xffffffffu, src, 4 * k + i);
-                if (tr0 + warp + kWarps * (4 * k + i) < row1) {
-                    const float4* p = src_ptr(s);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) v[i][j] = ldg_stream(p + lane + 32 * j);
-                }
+        auto load_row = [&](float4 (&v)[4], int tr0, int j, int src) {
+            const int s = __shfl_sync(0xffffffffu, src, j);
+            if (tr0 + warp + kWarps * j < row1) {
+                const float* p = src_ptr(s) + 8 * lane;
+                ldg_stream8(p, v[0], v[1]);
+                ldg_stream8(p + 256, v[2], v[3]);
             }
         };
-        auto store_rows = [&](const float4 (&v)[4][4], int tr0, int k) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = warp + kWarps * (4 * k + i);
-                if (tr0 + r < row1) {
-                    store_half(*reinterpret_cast<const float4(*)[2]>(&v[i][0]), r, 0);
-                    store_half(*reinterpret_cast<const float4(*)[2]>(&v[i][2]), r, 1);
-                } else {
-                    zero_half(r, 0);
-                    zero_half(r, 1);
-                }
+        auto store_row = [&](const float4 (&v)[4], int tr0, int j) {
+            const int r = warp + kWarps * j;
+            if (tr0 + r < row1) {
+                store_half(v[0], v[1], r, 0);
+                store_half(v[2], v[3], r, 1);
+            } else {
+                zero_half(r, 0);
+                zero_half(r, 1);
             }
         };
         auto issue_pass1 = [&](int x0) {   // d-blocks x0 .. x0 + 3 (thread 0)
@@ -433,8 +467,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             if (tile + 1 < n_tiles) prefetch_tile(lb, tr0 + kTileRows, row1);
             // ------------------------------------------------------------ E (all warps)
             const int src = fetch_src(tr0);          // this tile's row sources (lanes 0-7)
+            // four rows in flight per warp (128 KB per CTA); each row's registers
+            // take the next row's loads as soon as they are stored, so the
+            // stream does not drain between the tile's two halves
             float4 v[4][4];
-            load_rows(v, tr0, 0, src);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) load_row(v[i], tr0, i, src);
             if (q_pending) {
                 // the queries' copy has landed in the E area: convert it while the rows arrive
                 if (block_wait(&ms.q_full, q_uses & 1)) {
@@ -451,9 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                 failed = true;
                 break;
             }
-            store_rows(v, tr0, 0);
-            load_rows(v, tr0, 1, src);
-            store_rows(v, tr0, 1);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                store_row(v[i], tr0, i);
+                load_row(v[i], tr0, 4 + i, src);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) store_row(v[i], tr0, 4 + i);
             fence_async_smem();
             tc_fence_before();
             __syncthreads();
@@ -474,51 +516,45 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             }
             const uint32_t ts = tmem + lane_base + kColS + HPG * grp;
             const bool valid = tr0 + r < row1;
-            float sv[HPG], t[HPG];
+            float sv[HPG];
             tmem_ld<HPG>(ts, sv);                            // stale after an abort, then unused
             tmem_ld_wait();
             tmem_regs_ready_n(sv);
 #pragma unroll
-            for (int i = 0; i < HPG; ++i) {
-                sv[i] = valid ? sv[i] * a.sl2 : -INFINITY;
-                t[i] = sv[i];
-            }
+            for (int i = 0; i < HPG; ++i) sv[i] = valid ? sv[i] * a.sl2 : -INFINITY;
             {
-                const float m = reduce_cols<HPG, true>(t, lane);
-                if ((lane & (32 / HPG - 1)) == 0) ms.red[quad][HPG * grp + lane / (32 / HPG)] = m;
-            }
-            named_sync(1 + grp, 128);
-            bool moved = false;
+                // each head's maximum over this warp's 32 rows: one warp reduction per column
+                float mx[HPG];
 #pragma unroll
-            for (int c = 0; c < HPG / 4; ++c) {
-                // heads HPG * grp + 4 c .. + 3: the four quadrants' tile maxima and the reference max
-                const int h4 = HPG * grp + 4 * c;
-                const float4 a0 = *reinterpret_cast<const float4*>(&ms.red[0][h4]);
-                const float4 a1 = *reinterpret_cast<const float4*>(&ms.red[1][h4]);
-                const float4 a2 = *reinterpret_cast<const float4*>(&ms.red[2][h4]);
-                const float4 a3 = *reinterpret_cast<const float4*>(&ms.red[3][h4]);
-                const float4 m4 = *reinterpret_cast<const float4*>(&ms.m_used[par][h4]);
-                const float mts[4] = {fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x)), fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y)),
-                                      fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z)), fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w))};
-                const float mus[4] = {m4.x, m4.y, m4.z, m4.w};
+                for (int i = 0; i < HPG; ++i) mx[i] = warp_max(sv[i]);
+                if (lane == 0) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int i = 4 * c + u, h = h4 + u;
-                    const float mt = mts[u];
-                    const float mu = mus[u];
-                    float mn = mu;
-                    const bool mv = mt > mu + kLazy || (mu == -INFINITY && mt > -INFINITY);
-                    if (mv) {
-                        mn = mt;
-                        moved = true;
-                    }
-                    if (quad == 0) {                         // a warp-uniform branch: every lane writes the same
-                        ms.alpha[h] = mv ? ex2_approx(mu - mt) : 1.f;   // 0 when mu = -inf
-                        ms.m_used[par ^ 1][h] = mn;
-                    }
-                    sv[i] = ex2_approx(sv[i] - mn);            // 0 for a row past the end
+                    for (int c = 0; c < HPG / 4; ++c)
+                        *reinterpret_cast<float4*>(&ms.red[quad][HPG * grp + 4 * c]) =
+                            make_float4(mx[4 * c], mx[4 * c + 1], mx[4 * c + 2], mx[4 * c + 3]);
                 }
             }
+            named_sync(1 + grp, 128);
+            // lane i < HPG: head HPG * grp + i's tile maximum over the four quadrants
+            // and its reference max (every warp of the group computes the same)
+            float mn = 0.f, al = 1.f;   // reference max, rescale of the running sums
+            bool mv = false;
+            if (lane < HPG) {
+                const int h = HPG * grp + lane;
+                const float mt = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
+                const float mu = ms.m_used[par][h];
+                mv = mt > mu + kLazy || (mu == -INFINITY && mt > -INFINITY);
+                mn = mv ? mt : mu;
+                al = mv ? ex2_approx(mu - mt) : 1.f;   // 0 when mu = -inf
+                if (quad == 0) {
+                    ms.alpha[h] = al;
+                    ms.m_used[par ^ 1][h] = mn;
+                }
+            }
+            const bool moved = __any_sync(0xffffffffu, mv);
+#pragma unroll
+            for (int i = 0; i < HPG; ++i)
+                sv[i] = ex2_approx(sv[i] - __shfl_sync(0xffffffffu, mn, i));   // 0 for a row past the end
             // P row r, heads HPG * grp ..: fp16, MN-major (heads contiguous), swizzled
             {
                 if constexpr (HPG >= 8) {
@@ -533,16 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                 }
             }
             {
-                const float sum = reduce_cols<HPG, false>(sv, lane);   // sv is consumed
+                const float sum = sum_cols<HPG>(sv, lane);   // sv is consumed
                 if ((lane & (32 / HPG - 1)) == 0) ms.red2[quad][HPG * grp + lane / (32 / HPG)] = sum;
-            }
-            named_sync(1 + grp, 128);
-            if (quad == 0 && (lane & (32 / HPG - 1)) == 0) {
-                const int h = HPG * grp + lane / (32 / HPG);
-                const float l = ms.l_run[par][h] * ms.alpha[h] +
-                                ((ms.red2[0][h] + ms.red2[1][h]) + (ms.red2[2][h] + ms.red2[3][h]));
-                ms.l_run[par ^ 1][h] = l;
-                ms.inv_l[h] = __fdividef(1.f, l);   // used after the segment's last tile; l >= 1
             }
             // the previous tile's pass 2 completed before E was overwritten, so
             // O is free here: O^T[d, h] *= alpha[h] for this group's heads
@@ -555,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                     tmem_ld_wait();
                     tmem_regs_ready_n(o);
 #pragma unroll
-                    for (int i = 0; i < HPG; ++i) o[i] *= ms.alpha[HPG * grp + i];
+                    for (int i = 0; i < HPG; ++i) o[i] *= __shfl_sync(0xffffffffu, al, i);
                     tmem_st<HPG>(ta, o);
                 }
                 tmem_st_wait();
@@ -575,7 +603,21 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                                     desc_sw128(p0 + kk * 2048, 8192, 1024), id2, (tile > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&ms.o_full);
             }
+            if (quad == 0 && lane < HPG && !failed) {
+                // this tile's running sums (the barrier above ordered every quadrant's sums);
+                // read at the next tile's update or in the epilogue, after further barriers
+                const int h = HPG * grp + lane;
+                const float l = ms.l_run[par][h] * ms.alpha[h] +
+                                ((ms.red2[0][h] + ms.red2[1][h]) + (ms.red2[2][h] + ms.red2[3][h]));
+                ms.l_run[par ^ 1][h] = l;
+                ms.inv_l[h] = __fdividef(1.f, l);   // used after the segment's last tile; l >= 1
+            }
             ++gt;
+            if (early && tile == 0) {
+                // the window tile's products are issued: the selection's rows next
+                dep_wait();
+                seg_after_wait();   // n_tiles >= 1: the window tile is in range
+            }
             if (failed) break;
         }
         if (failed) break;
@@ -609,14 +651,16 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         }
         if (n_tiles > 0) {
             const int d = mb * 128 + quad * 32 + lane;
+            // 32 heads' columns per round of TMEM loads (16 when H = 16)
+            constexpr int kEpi = H >= 32 ? 32 : 16;
 #pragma unroll 1
-            for (int h0 = 0; h0 < H; h0 += 16) {
-                float o[16];
-                tmem_ld<16>(ms.tmem_base + lane_base + kColO + 64 * mb + h0, o);
+            for (int h0 = 0; h0 < H; h0 += kEpi) {
+                float o[kEpi];
+                tmem_ld<kEpi>(ms.tmem_base + lane_base + kColO + 64 * mb + h0, o);
                 tmem_ld_wait();
                 tmem_regs_ready_n(o);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < kEpi / 4; ++c) {
                     const float4 il = reinterpret_cast<const float4*>(&ms.inv_l[h0])[c];
                     o[4 * c + 0] *= il.x * inv_sc;
                     o[4 * c + 1] *= il.y * inv_sc;
@@ -626,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                 if (single) {
                     float* dst = a.out + (lb * H + h0) * kKvDim + d;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) dst[(size_t)i * kKvDim] = o[i];
+                    for (int i = 0; i < kEpi; ++i) dst[(size_t)i * kKvDim] = o[i];
                 } else {
                     // lanes 2k and 2k + 1 hold d and d + 1: the even lane stores both
                     // values of head i, the odd lane both of head i + 1 (4-byte stores)
@@ -634,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                     uint32_t* dst = reinterpret_cast<uint32_t*>(a.part_o + ((size_t)sg.slot * H + h0) * kKvDim +
                                                                 (d & ~1));
 #pragma unroll
-                    for (int i = 0; i < 16; i += 2) {
+                    for (int i = 0; i < kEpi; i += 2) {
                         const float other = __shfl_xor_sync(0xffffffffu, odd ? o[i] : o[i + 1], 1);
                         const uint32_t w = odd ? pack_f16x2(other, o[i + 1]) : pack_f16x2(o[i], other);
                         __stcg(&dst[(size_t)(i + (odd ? 1 : 0)) * (kKvDim / 2)], w);
@@ -659,16 +703,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         if (failed) break;
         if (!single && tid == 0) {
             // this segment's partial is written (every thread's stores precede the
-            // barrier; the fence makes them visible GPU-wide before the count):
+            // barrier; the release makes them visible GPU-wide with the count):
             // count it, and note the share of the pair this CTA merges at the end
             const MergeItem mi = a.merges[sg.merge];
-            __threadfence();
-            const unsigned long long old = atomicAdd(&a.merge_cnt[sg.merge], 1ull);
+            asm volatile("red.release.gpu.global.add.u64 [%0], 1;\n" ::"l"(&a.merge_cnt[sg.merge]) : "memory");
             const int k = ms.n_duties;
             if (k < kMaxDuties) {
                 ms.duty_merge[k] = sg.merge;
                 ms.duty_part[k] = sg.part;
-                ms.duty_target[k] = (old / (unsigned long long)mi.ns + 1ull) * (unsigned long long)mi.ns;
+                ms.duty_target[k] = (seen / (unsigned long long)mi.ns + 1ull) * (unsigned long long)mi.ns;
                 ms.n_duties = k + 1;
             } else {
                 atomicOr(a.err, kErrBounds);
@@ -676,6 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         }
     }   // segments
 
+    dep_wait();   // a CTA without segments, or one that stopped early
     if (q_pending) {
         // a queries' copy still lands in the E area: wait for it before leaving
         if (tid == 0 && !mbar_wait(&ms.q_full, q_uses & 1)) atomicOr(a.err, kErrTimeout);
@@ -702,9 +746,17 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     // ---------------------------------------------------------------- merges
     __syncthreads();
     const int n_duties = failed ? 0 : ms.n_duties;
+    uint32_t m_uses = 0;   // phases of m_full
     for (int k = 0; k < n_duties; ++k) {
         const MergeItem mi = a.merges[ms.duty_merge[k]];
         const int ns = min(mi.ns, kMaxSplits);
+        // this CTA's share: 8-value chunks [c0, c1) of the pair's H x 512
+        // outputs, contiguous in every split's partial and in the output
+        constexpr int kChunks = H * kKvDim / 8;
+        const int j = ms.duty_part[k];
+        const int c0 = j * kChunks / ns, c1 = (j + 1) * kChunks / ns;
+        const uint32_t share = (uint32_t)(c1 - c0) * 16u;
+        const uint32_t stride = (share + 127u) & ~127u;   // bytes per split in shared memory
         if (tid == 0) {
             const unsigned long long* c = &a.merge_cnt[ms.duty_merge[k]];
             const unsigned long long target = ms.duty_target[k];
@@ -716,80 +768,70 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                     if (global_ns() - t0 > kWaitLimitNs) break;
                 }
             }
-            if (!ok) {
+            if (ok) {
+                // every split's share of the partial and the splits' statistics,
+                // by bulk copies into the E area (free: no MMA reads it any more)
+                asm volatile("fence.proxy.async.global;\n" ::: "memory");
+                fence_async_smem();
+                const uint32_t ml_bytes = (uint32_t)ns * kMlStride * 4u;
+                mbar_arrive_expect_tx(&ms.m_full, (uint32_t)ns * share + ml_bytes);
+                for (int sp = 0; sp < ns; ++sp)
+                    bulk_g2s(sm + kOffE + sp * stride,
+                             a.part_o + ((size_t)(mi.first + sp) * H * kKvDim + (size_t)c0 * 8), share, &ms.m_full);
+                bulk_g2s(sm + kOffE + kMergeMlOff, a.part_ml + (size_t)mi.first * kMlStride, ml_bytes, &ms.m_full);
+            } else {
                 atomicOr(a.err, kErrTimeout);
                 ms.abort = 1;
             }
         }
         if (__syncthreads_or(*abort != 0)) break;
-        // this CTA's share: 8-value chunks [c0, c1) of the pair's H x 512 outputs.
-        // Each thread loads, for its chunk, every split's 8 values and the
-        // head's (m, l) statistics in one round and combines them itself.
-        constexpr int kChunks = H * kKvDim / 8;
-        const int j = ms.duty_part[k];
-        const int c0 = (int)((long long)j * kChunks / ns), c1 = (int)((long long)(j + 1) * kChunks / ns);
-        const float* ml = a.part_ml + (size_t)mi.first * kMlStride;
-        // two chunks per thread and iteration, every load of both issued at once
-        for (int cb = c0 + tid; cb < c1; cb += 2 * kThreads) {
-            uint4 pv[2][kMergeBatch];
-            float mv[2][kMergeBatch], lv[2][kMergeBatch], sv[2][kMergeBatch];
-            float acc[2][8], M[2], L[2];
-            for (int s0 = 0; s0 < ns; s0 += kMergeBatch) {
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int c = cb + q * kThreads;
-                    if (c >= c1) continue;
-                    const int h = c >> 6;
-                    const uint16_t* src = a.part_o + ((size_t)mi.first * H + h) * kKvDim + (c & 63) * 8;
-#pragma unroll
-                    for (int s = 0; s < kMergeBatch; ++s) {
-                        if (s0 + s < ns) {
-                            pv[q][s] = ld_cg_u4(src + (size_t)(s0 + s) * H * kKvDim);
-                            mv[q][s] = ld_cg_f(&ml[(size_t)(s0 + s) * kMlStride + h]);
-                            lv[q][s] = ld_cg_f(&ml[(size_t)(s0 + s) * kMlStride + H + h]);
-                            sv[q][s] = ld_cg_f(&ml[(size_t)(s0 + s) * kMlStride + 2 * H]);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    if (cb + q * kThreads >= c1) continue;
-                    if (s0 == 0) {
-                        M[q] = -INFINITY;
-                        L[q] = 0.f;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[q][e] = 0.f;
-                    }
-                    // online combination over the splits, in split order
-#pragma unroll
-                    for (int s = 0; s < kMergeBatch; ++s) {
-                        if (s0 + s < ns && lv[q][s] > 0.f) {
-                            const float Mn = fmaxf(M[q], mv[q][s]);
-                            const float a0 = ex2_approx(M[q] - Mn), wl = lv[q][s] * ex2_approx(mv[q][s] - Mn);
-                            const float w = wl * sv[q][s];           // the partial's values were divided by its scale
-                            L[q] = L[q] * a0 + wl;
-                            const uint32_t x[4] = {pv[q][s].x, pv[q][s].y, pv[q][s].z, pv[q][s].w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                acc[q][2 * e] = acc[q][2 * e] * a0 + w * f16_to_f32(x[e] & 0xffffu);
-                                acc[q][2 * e + 1] = acc[q][2 * e + 1] * a0 + w * f16_to_f32(x[e] >> 16);
-                            }
-                            M[q] = Mn;
-                        }
-                    }
-                }
+        if (block_wait(&ms.m_full, m_uses & 1)) break;
+        ++m_uses;
+        // each head's weights over the splits, once:
+        //   w_s = l_s 2^(m_s - M) sc_s / sum_s' l_s' 2^(m_s' - M),  M = max m_s over splits with rows
+        const float* mls = reinterpret_cast<const float*>(sm + kOffE + kMergeMlOff);
+        float* wts = reinterpret_cast<float*>(sm + kOffE + kMergeWOff);
+        if (tid < H) {
+            float M = -INFINITY;
+            for (int sp = 0; sp < ns; ++sp)
+                if (mls[sp * kMlStride + H + tid] > 0.f) M = fmaxf(M, mls[sp * kMlStride + tid]);
+            float L = 0.f;
+            for (int sp = 0; sp < ns; ++sp) {
+                const float l = mls[sp * kMlStride + H + tid];
+                const float wl = l > 0.f ? l * ex2_approx(mls[sp * kMlStride + tid] - M) : 0.f;
+                wts[sp * 64 + tid] = wl;
+                L += wl;
             }
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int c = cb + q * kThreads;
-                if (c >= c1) continue;
-                const float inv = L[q] > 0.f ? 1.f / L[q] : 0.f;
-                float4* dst = reinterpret_cast<float4*>(a.out + ((size_t)mi.lb * H + (c >> 6)) * kKvDim + (c & 63) * 8);
-                dst[0] = make_float4(acc[q][0] * inv, acc[q][1] * inv, acc[q][2] * inv, acc[q][3] * inv);
-                dst[1] = make_float4(acc[q][4] * inv, acc[q][5] * inv, acc[q][6] * inv, acc[q][7] * inv);
-            }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            for (int sp = 0; sp < ns; ++sp) wts[sp * 64 + tid] *= mls[sp * kMlStride + 2 * H] * inv;
         }
         __syncthreads();
+        // every thread combines its chunks over the splits, in split order; a
+        // split without rows (weight 0) is skipped: its partial was not written
+        for (int c = c0 + tid; c < c1; c += kThreads) {
+            const int h = c >> 6;
+            const unsigned char* pv = sm + kOffE + (size_t)(c - c0) * 16;
+            float acc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll 4
+            for (int sp = 0; sp < ns; ++sp) {
+                const float w = wts[sp * 64 + h];
+                if (w != 0.f) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(pv + (size_t)sp * stride);
+                    const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        acc[2 * e] += w * f16_to_f32(x[e] & 0xffffu);
+                        acc[2 * e + 1] += w * f16_to_f32(x[e] >> 16);
+                    }
+                }
+            }
+            float4* dst = reinterpret_cast<float4*>(a.out + (size_t)mi.lb * H * kKvDim + (size_t)c * 8);
+            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+        __syncthreads();   // the E area is read before the next merge's copies land
     }
 
     // ---------------------------------------------------------------- teardown
@@ -808,7 +850,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
 
 template <int H>
 cudaError_t launch_h(const AttnArgs& args, int n_ctas, cudaStream_t st, bool chained) {
-    return launch_coop(attend_kernel<H>, dim3(n_ctas), dim3(kThreads), kSmemBytes, st, chained, args);
+    return launch_k(attend_kernel<H>, dim3(n_ctas), dim3(kThreads), kSmemBytes, st, chained, args);
 }
 
 }  // namespace

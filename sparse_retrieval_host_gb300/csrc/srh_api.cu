@@ -134,15 +134,18 @@ void free_ctx(srh_ctx* ctx) {
 
 // The static attention plan of one lsa_attend scope (the pairs (layer, seq)
 // of `layers`). A pair holds 128 window rows plus at most min(S, cap) staged
-// rows, in 128-row tiles; an attention CTA holds ~210 KB of shared memory and
-// 1024 threads, so one runs per SM. With T tiles in the scope, no plan can give
+// rows, in 128-row tiles; an attention CTA holds ~218 KB of shared memory and
+// 512 threads of 128 registers, so one runs per SM, and a plan never has more
+// CTAs than SMs (every CTA becomes resident, which the merge waits rely on). With T tiles in the scope, no plan can give
 // a CTA fewer than ceil(T / SMs) tiles; when cutting every pair into chunks of
 // that many tiles fits one wave, each CTA runs one chunk; otherwise the T
 // tiles, in (layer, seq, row) order, are cut into min(SMs, T) contiguous
 // ranges of equal size (+-1 tile), one CTA each. A pair spread over several
 // CTAs is merged by those CTAs, each taking one share, once all its partials
-// are written. The plan depends only on the configuration, so the same rows
-// give the same bits whichever slots hold them.
+// are written. CTAs whose first segment starts with a pair's window tile come
+// first: that tile needs no earlier kernel's output, and the CTAs launched
+// first run it while those kernels finish. The plan depends only on the
+// configuration, so the same rows give the same bits whichever slots hold them.
 void plan_scope(srh_ctx* ctx, const std::vector<int>& layers, std::vector<AttnSeg>* segs,
                 std::vector<int>* cta_begin, std::vector<MergeItem>* merges, AttnPlan* plan) {
     const int B = ctx->B;
@@ -208,6 +211,7 @@ void plan_scope(srh_ctx* ctx, const std::vector<int>& layers, std::vector<AttnSe
             slot += n_parts[x.r];
         }
     }
+    std::vector<AttnSeg> tmp;
     for (const Raw& x : raw) {
         const int mi = merge_of[x.r];
         int sl = -1, part = 0;
@@ -215,10 +219,20 @@ void plan_scope(srh_ctx* ctx, const std::vector<int>& layers, std::vector<AttnSe
             part = seen[x.r]++;
             sl = (*merges)[plan->merge0 + mi].first + part;
         }
-        segs->push_back(AttnSeg{lbs[x.r], x.t0, x.t1, sl, mi, part});
+        tmp.push_back(AttnSeg{lbs[x.r], x.t0, x.t1, sl, mi, part});
     }
-    for (int k : begin) cta_begin->push_back(k);
-    cta_begin->push_back((int)raw.size());
+    // CTAs that start with a window tile first, otherwise in plan order
+    const int nct = (int)begin.size();
+    std::vector<int> order;
+    for (int pass = 0; pass < 2; ++pass)
+        for (int k = 0; k < nct; ++k)
+            if ((raw[begin[k]].t0 == 0) == (pass == 0)) order.push_back(k);
+    for (int k : order) {
+        const int e = k + 1 < nct ? begin[k + 1] : (int)raw.size();
+        cta_begin->push_back((int)segs->size() - plan->seg0);
+        for (int i = begin[k]; i < e; ++i) segs->push_back(tmp[i]);
+    }
+    cta_begin->push_back((int)segs->size() - plan->seg0);
     plan->n_segs = (int)raw.size();
     plan->n_merges = (int)merges->size() - plan->merge0;
     plan->n_slots = slot;
