@@ -313,8 +313,14 @@ int fm_select_noalloc(const float* d_scores, int batch, int n, int mode, int k, 
  * a4+a5: KV_SWAP staging ([P1] KV_SWAP 实现细节, Swap-in flow).
  *   layer      one sparse layer, or -1 for all layers
  *   d_sel, d_count  the fm_select outputs ([batch][S], [batch])
- *   d_staging  [L][batch][G][kv_dim] fp32: the GPU staging slots. This buffer is
- *              part of the cache state: pass the same buffer to every call on a
+ *   d_staging  [L][batch][G][kv_dim] fp16 (IEEE binary16 bits), 32-byte
+ *              aligned: the GPU staging slots. A staged row is the pool's fp32
+ *              row rounded to nearest fp16: lsa_attend rounds every row to fp16
+ *              for its tensor-core products, so its results are the same as
+ *              from fp32 slots, from half the bytes (a departure from the page's
+ *              fp32 slot layout). A pool value beyond +-65504 sets
+ *              SRH_ERR_RANGE at the next srh_check_error. This buffer is part
+ *              of the cache state: pass the same buffer to every call on a
  *              context (a different one is rejected with SRH_ERR_INVALID).
  *              Swap-disabled layers keep their chunk c in row c.
  *   d_phys     [L][batch][S] int32 output: physical row of each selected chunk of
@@ -335,31 +341,32 @@ int fm_select_noalloc(const float* d_scores, int batch, int n, int mode, int k, 
  * previous list's slots are then the most recently used and none is evicted.
  */
 int kvswap_stage(srh_ctx* ctx, int layer, const int32_t* d_sel, const int32_t* d_count,
-                 float* d_staging, int32_t* d_phys, int32_t* d_count_l, srh_stream_t main,
+                 uint16_t* d_staging, int32_t* d_phys, int32_t* d_count_l, srh_stream_t main,
                  srh_stream_t side);
 
 /*
  * a6: sparse attention ([P1] 架构概览, per-layer box step 3; Memory Layout).
  *   layer      one sparse layer, or -1 for all layers
- *   d_q        [L][batch][n_heads][kv_dim] bf16 queries
+ *   d_q        [L][batch][n_heads][kv_dim] bf16 queries (16-byte aligned)
  *   n_heads    16, 32 or 64
- *   d_window   [L][batch][128][kv_dim] fp32 window rows
+ *   d_window   [L][batch][128][kv_dim] fp32 window rows (32-byte aligned)
  *   d_staging, d_phys, d_count_l  as written by kvswap_stage
- *   d_out      [L][batch][n_heads][kv_dim] fp32 output:
+ *   d_out      [L][batch][n_heads][kv_dim] fp32 output (16-byte aligned):
  *              o_h = sum_j softmax_j(<q_h, e_j> / sqrt(kv_dim)) e_j over the 128
  *              window rows and the layer's staged rows (K = V = the latent row).
  * Precision: the products run on the tensor cores with fp16 operands (11
  * significant bits) and fp32 accumulation; a pair split over several CTAs is
  * combined from fp16 partial outputs (each a softmax-weighted mean of rows).
  * Query and latent values must lie within +-65504 (else SRH_ERR_RANGE at the
- * next srh_check_error); values below 2^-14 (about 6.1e-5) in magnitude keep
- * an absolute precision of 2^-25 instead of 11 significant bits.
+ * next srh_check_error; a staged value that is not finite fp16 counts too);
+ * values below 2^-14 (about 6.1e-5) in magnitude keep an absolute precision of
+ * 2^-25 instead of 11 significant bits.
  * Calls on one context must not overlap in time: they share the context's
  * partial buffers and arrival counters. Asynchronous; returns SRH_OK,
  * SRH_ERR_INVALID or SRH_ERR_CUDA.
  */
 int lsa_attend(srh_ctx* ctx, int layer, const uint16_t* d_q, int n_heads, const float* d_window,
-               const float* d_staging, const int32_t* d_phys, const int32_t* d_count_l,
+               const uint16_t* d_staging, const int32_t* d_phys, const int32_t* d_count_l,
                float* d_out, srh_stream_t stream);
 
 /*

@@ -66,6 +66,7 @@ namespace {
 using namespace umma;
 
 constexpr int kTileRows = kAttnTile;                // 128
+static_assert(kWindow == kTileRows, "a pair's first tile is exactly its window rows");
 constexpr int kThreads = 512;                       // 16 warps
 constexpr int kWarps = kThreads / 32;
 constexpr int kRowsPerWarp = kTileRows / kWarps;    // 8 tile rows per warp
@@ -128,7 +129,7 @@ struct AttnArgs {
     int B, G, S;
     const uint16_t* q;
     const float* window;
-    const float* staging;
+    const uint16_t* staging;   // fp16 staged rows
     const int32_t* phys;
     const int32_t* count_l;
     float* out;
@@ -253,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     if (warp == 0) tmem_alloc(&ms.tmem_base, kTmemCols);
     float amax = 0.f;   // largest |value| converted to fp16 by this thread (range guard)
     float ramax = 0.f;  // largest |row value| of the current segment (scale of its partial)
+    uint32_t rbits = 0; // ... of its fp16 staged rows: two maxima of |fp16| bit patterns
 
     // Wait for an mbarrier phase: thread 0 polls, every other thread waits at
     // the block barrier that follows (a waiting warp issues nothing). Returns
@@ -331,15 +333,18 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     auto prefetch_tile = [&](size_t lb, int tr0, int row1) {
         const int row = tr0 + tid;
         if (tid >= kTileRows || row >= row1) return;
-        const float* p;
+        const void* p;
+        uint32_t bytes;
         if (row < kWindow) {
             p = a.window + (lb * kWindow + row) * kKvDim;
+            bytes = kKvDim * 4;
         } else {
             const int slot = a.phys[lb * a.S + row - kWindow] - kWindow;
             if (slot < 0 || slot >= a.G) return;            // reported by the loads
             p = a.staging + (lb * (size_t)a.G + slot) * kKvDim;
+            bytes = kKvDim * 2;
         }
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(kKvDim * 4) : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
     };
 
     // the barriers, the abort flag and the TMEM address are set; every thread sees them from here on
@@ -414,6 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             ms.l_run[0][tid] = 0.f;
         }
         ramax = 0.f;
+        rbits = 0u;
 
         // Sources of this warp's rows w + 16 i (lane i < 8) of the tile at tr0:
         // -1 - row for a window row, else the row's phys entry (window + slot).
@@ -422,8 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             if (lane >= kRowsPerWarp || row >= row1) return -1;
             return row < kWindow ? -1 - row : ph[row - kWindow];
         };
-        auto src_ptr = [&](int src) -> const float* {
-            if (src < 0) return a.window + (lb * kWindow + (-1 - src)) * kKvDim;
+        auto staged_ptr = [&](int src) -> const uint16_t* {
             int slot = src - kWindow;
             if (slot < 0 || slot >= a.G) {
                 atomicOr(a.err, kErrBounds);
@@ -431,15 +436,39 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             }
             return a.staging + (lb * (size_t)a.G + slot) * kKvDim;
         };
-        // row w + 16 j (j < 8) of the tile at tr0: the whole row, 1 KiB of
-        // contiguous bytes per load instruction
+        // window row w + 16 j (j < 8) of the tile at tr0 (fp32): the whole row,
+        // 1 KiB of contiguous bytes per load instruction
         auto load_row = [&](float4 (&v)[4], int tr0, int j, int src) {
             const int s = __shfl_sync(0xffffffffu, src, j);
             if (tr0 + warp + kWarps * j < row1) {
-                const float* p = src_ptr(s) + 8 * lane;
+                const float* p = a.window + (lb * kWindow + (-1 - s)) * kKvDim + 8 * lane;
                 ldg_stream8(p, v[0], v[1]);
                 ldg_stream8(p + 256, v[2], v[3]);
             }
+        };
+        // staged row w + 16 j (fp16, 1 KiB): this lane's 16 values d = 16 lane ..
+        auto load_row_h = [&](float4& lo, float4& hi, int tr0, int j, int src) {
+            const int s = __shfl_sync(0xffffffffu, src, j);
+            if (tr0 + warp + kWarps * j < row1)
+                ldg_stream8(reinterpret_cast<const float*>(staged_ptr(s) + 16 * lane), lo, hi);
+        };
+        // as they are into E row r: d-block lane / 4, 16-byte chunks 2 (lane % 4) and + 1
+        auto store_row_h = [&](const float4& lo, const float4& hi, int tr0, int j) {
+            const int r = warp + kWarps * j;
+            unsigned char* e = sm + kOffE + (lane >> 2) * kDBlockE;
+            const int c = 2 * (lane & 3);
+            uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;
+            if (tr0 + r < row1) {
+                w0 = make_uint4(__float_as_uint(lo.x), __float_as_uint(lo.y), __float_as_uint(lo.z), __float_as_uint(lo.w));
+                w1 = make_uint4(__float_as_uint(hi.x), __float_as_uint(hi.y), __float_as_uint(hi.z), __float_as_uint(hi.w));
+                const uint32_t m = __vmaxu2(__vmaxu2(__vmaxu2(w0.x & 0x7fff7fffu, w0.y & 0x7fff7fffu),
+                                                     __vmaxu2(w0.z & 0x7fff7fffu, w0.w & 0x7fff7fffu)),
+                                            __vmaxu2(__vmaxu2(w1.x & 0x7fff7fffu, w1.y & 0x7fff7fffu),
+                                                     __vmaxu2(w1.z & 0x7fff7fffu, w1.w & 0x7fff7fffu)));
+                rbits = __vmaxu2(rbits, m);
+            }
+            *reinterpret_cast<uint4*>(e + sw128(r, c)) = w0;
+            *reinterpret_cast<uint4*>(e + sw128(r, c + 1)) = w1;
         };
         auto store_row = [&](const float4 (&v)[4], int tr0, int j) {
             const int r = warp + kWarps * j;
@@ -467,12 +496,19 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             if (tile + 1 < n_tiles) prefetch_tile(lb, tr0 + kTileRows, row1);
             // ------------------------------------------------------------ E (all warps)
             const int src = fetch_src(tr0);          // this tile's row sources (lanes 0-7)
-            // four rows in flight per warp (128 KB per CTA); each row's registers
-            // take the next row's loads as soon as they are stored, so the
-            // stream does not drain between the tile's two halves
+            const bool win = tr0 < kWindow;           // a pair's first tile: its window rows, fp32
             float4 v[4][4];
+            if (win) {
+                // four rows in flight per warp (128 KB per CTA); each row's registers
+                // take the next row's loads as soon as they are stored, so the
+                // stream does not drain between the tile's two halves
 #pragma unroll
-            for (int i = 0; i < 4; ++i) load_row(v[i], tr0, i, src);
+                for (int i = 0; i < 4; ++i) load_row(v[i], tr0, i, src);
+            } else {
+                // staged rows, fp16: all eight of this warp's rows in flight at once
+#pragma unroll
+                for (int j = 0; j < 8; ++j) load_row_h(v[j >> 1][2 * (j & 1)], v[j >> 1][2 * (j & 1) + 1], tr0, j, src);
+            }
             if (q_pending) {
                 // the queries' copy has landed in the E area: convert it while the rows arrive
                 if (block_wait(&ms.q_full, q_uses & 1)) {
@@ -489,13 +525,18 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                 failed = true;
                 break;
             }
+            if (win) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                store_row(v[i], tr0, i);
-                load_row(v[i], tr0, 4 + i, src);
+                for (int i = 0; i < 4; ++i) {
+                    store_row(v[i], tr0, i);
+                    load_row(v[i], tr0, 4 + i, src);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) store_row(v[i], tr0, 4 + i);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) store_row_h(v[j >> 1][2 * (j & 1)], v[j >> 1][2 * (j & 1) + 1], tr0, j);
             }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) store_row(v[i], tr0, 4 + i);
             fence_async_smem();
             tc_fence_before();
             __syncthreads();
@@ -628,6 +669,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         const int fpar = n_tiles & 1;
         const bool single = sg.slot < 0;
         const int mb = grp;
+        {
+            // the staged rows' largest |value|; one that is not finite fp16 is out of range
+            const uint32_t hb = max(rbits & 0xffffu, rbits >> 16);
+            if (hb >= 0x7c00u) amax = INFINITY;
+            else ramax = fmaxf(ramax, f16_to_f32(hb));
+        }
         if (!single) {
             // the partial is stored as (O / l) / sc, sc = 2^floor(log2 max |row value|),
             // so that it stays in fp16's normal range whatever the rows' magnitude
@@ -869,7 +916,7 @@ cudaError_t set_attend_attrs() {
 
 cudaError_t launch_attend(const AttnSeg* segs, const int* cta_begin, int n_ctas, const MergeItem* merges,
                           unsigned long long* merge_cnt, int n_heads, int B, int G, int S, const uint16_t* q,
-                          const float* window, const float* staging, const int32_t* phys, const int32_t* count_l,
+                          const float* window, const uint16_t* staging, const int32_t* phys, const int32_t* count_l,
                           float* out, uint16_t* part_o, float* part_ml, uint32_t* err, cudaStream_t st,
                           bool chained) {
     if (n_ctas <= 0) return cudaSuccess;

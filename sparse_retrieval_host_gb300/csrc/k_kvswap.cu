@@ -21,7 +21,10 @@
 // produce the state and outputs of the sequential list.
 //
 // The miss gather reads the mapped pinned pool directly (zero-copy over the
-// host link), one warp per 2 KiB chunk, 16-byte loads.
+// host link), one warp per 2 KiB chunk, 16-byte loads. A staged row is kept
+// as fp16 (1 KiB): the attention rounds every row to fp16 for its tensor-core
+// products anyway, so staging the rounded row gives the same results from half
+// the bytes. A pool value beyond fp16's finite range (65504) sets kErrRange.
 #include <climits>
 
 #include "srh_internal.cuh"
@@ -83,14 +86,33 @@ __device__ int block_scan_excl_array(int* a, int len, int* warp_buf) {
     return total;
 }
 
-__device__ __forceinline__ void copy_row(float* __restrict__ dst, const float* __restrict__ src, int lane) {
+__device__ __forceinline__ void load_row(float4 (&v)[4], const float* __restrict__ src, int lane) {
     const float4* s = reinterpret_cast<const float4*>(src);
-    float4* d = reinterpret_cast<float4*>(dst);
-    float4 v[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) v[k] = s[k * 32 + lane];
+}
+__device__ __forceinline__ void store_row(float* __restrict__ dst, const float4 (&v)[4], int lane) {
+    float4* d = reinterpret_cast<float4*>(dst);
 #pragma unroll
     for (int k = 0; k < 4; ++k) d[k * 32 + lane] = v[k];
+}
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// The row as fp16 (round to nearest even) into a staging row; a value beyond
+// fp16's finite range sets kErrRange.
+__device__ __forceinline__ void store_row_h(uint16_t* __restrict__ dst, const float4 (&v)[4], int lane,
+                                            uint32_t* __restrict__ err) {
+    uint2* d = reinterpret_cast<uint2*>(dst);
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)), fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
+        d[k * 32 + lane] = make_uint2(pack_h2(v[k].x, v[k].y), pack_h2(v[k].z, v[k].w));
+    }
+    if (__any_sync(0xffffffffu, !(amax <= 65504.f)) && lane == 0) atomicOr(err, kErrRange);
 }
 
 struct LruShared {
@@ -515,7 +537,7 @@ constexpr int kGatherWarps = 8;
 __global__ void __launch_bounds__(kGatherWarps * 32)
 gather_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S,
               const int2* miss, const int* miss_count,
-              float* __restrict__ staging, uint32_t* __restrict__ err) {
+              uint16_t* __restrict__ staging, uint32_t* __restrict__ err) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
     pdl_wait();                        // the miss lists come from the resolve kernel
@@ -530,21 +552,24 @@ gather_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S,
             if (lane == 0) atomicOr(err, kErrBounds);
             continue;
         }
-        copy_row(staging + (((size_t)l * B + b) * G + e.y) * kKvDim,
-                 ld.pool + ((size_t)b * ld.cap + e.x) * kKvDim, lane);
+        float4 v[4];
+        load_row(v, ld.pool + ((size_t)b * ld.cap + e.x) * kKvDim, lane);
+        store_row_h(staging + (((size_t)l * B + b) * G + e.y) * kKvDim, v, lane, err);
     }
 }
 
 __global__ void __launch_bounds__(kGatherWarps * 32)
 resident_fill_kernel(const float* __restrict__ pool, const uint8_t* __restrict__ ready,
-                     long long cap, int layer, int B, int G, float* __restrict__ staging) {
+                     long long cap, int layer, int B, int G, uint16_t* __restrict__ staging,
+                     uint32_t* __restrict__ err) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.y;
     for (long long c = (long long)blockIdx.x * kGatherWarps + warp; c < cap;
          c += (long long)gridDim.x * kGatherWarps) {
         if (!ready[(size_t)b * cap + c]) continue;
-        copy_row(staging + (((size_t)layer * B + b) * G + c) * kKvDim,
-                 pool + ((size_t)b * cap + c) * kKvDim, lane);
+        float4 v[4];
+        load_row(v, pool + ((size_t)b * cap + c) * kKvDim, lane);
+        store_row_h(staging + (((size_t)layer * B + b) * G + c) * kKvDim, v, lane, err);
     }
 }
 
@@ -555,19 +580,20 @@ resident_fill_kernel(const float* __restrict__ pool, const uint8_t* __restrict__
 // that does not swap gets row c. One warp per row.
 __global__ void __launch_bounds__(kGatherWarps * 32)
 store_kernel(const LayerDev* __restrict__ layers, int l, int B, int G, int seq, long long c0, int n,
-             const float* __restrict__ rows, float* __restrict__ staging, uint32_t* __restrict__ err) {
+             const float* __restrict__ rows, uint16_t* __restrict__ staging, uint32_t* __restrict__ err) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const LayerDev ld = layers[l];
     float* pool = const_cast<float*>(ld.pool) + (size_t)seq * ld.cap * kKvDim;
-    float* stg = staging ? staging + ((size_t)l * B + seq) * G * kKvDim : nullptr;
+    uint16_t* stg = staging ? staging + ((size_t)l * B + seq) * G * kKvDim : nullptr;
     for (int i = blockIdx.x * kGatherWarps + warp; i < n; i += gridDim.x * kGatherWarps) {
         const long long c = c0 + i;
         if (c < 0 || c >= ld.cap) {
             if (lane == 0) atomicOr(err, kErrBounds);
             continue;
         }
-        const float* src = rows + (size_t)i * kKvDim;
-        copy_row(pool + c * kKvDim, src, lane);
+        float4 v[4];
+        load_row(v, rows + (size_t)i * kKvDim, lane);
+        store_row(pool + c * kKvDim, v, lane);
         if (stg) {
             long long row = -1;
             if (ld.swap) {
@@ -576,7 +602,7 @@ store_kernel(const LayerDev* __restrict__ layers, int l, int B, int G, int seq, 
             } else if (c < G) {
                 row = c;
             }
-            if (row >= 0) copy_row(stg + row * kKvDim, src, lane);
+            if (row >= 0) store_row_h(stg + row * kKvDim, v, lane, err);
         }
         __syncwarp();
         if (lane == 0) ld.host_ready[(size_t)seq * ld.cap + c] = 1;
@@ -621,7 +647,7 @@ cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int
 }
 
 cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, int S,
-                          const int2* miss, const int* miss_count, float* staging, uint32_t* err,
+                          const int2* miss, const int* miss_count, uint16_t* staging, uint32_t* err,
                           int sm_count, cudaStream_t st, bool chained) {
     int bx = (4 * sm_count + nl * B - 1) / (nl * B);
     if (bx < 1) bx = 1;
@@ -640,7 +666,7 @@ cudaError_t launch_touch(const float* p, long long n_floats, uint32_t* sink, int
 }
 
 cudaError_t launch_store(const LayerDev* layers, int l, int B, int G, int seq, long long c0, int n,
-                         const float* rows, float* staging, uint32_t* err, cudaStream_t st) {
+                         const float* rows, uint16_t* staging, uint32_t* err, cudaStream_t st) {
     int bx = (n + kGatherWarps - 1) / kGatherWarps;
     if (bx > 1024) bx = 1024;
     store_kernel<<<bx, kGatherWarps * 32, 0, st>>>(layers, l, B, G, seq, c0, n, rows, staging, err);
@@ -648,12 +674,12 @@ cudaError_t launch_store(const LayerDev* layers, int l, int B, int G, int seq, l
 }
 
 cudaError_t launch_resident_fill(const float* pool_dev, const uint8_t* ready, long long cap,
-                                 int layer, int B, int G, float* staging, cudaStream_t st) {
+                                 int layer, int B, int G, uint16_t* staging, uint32_t* err, cudaStream_t st) {
     long long bx = (cap + kGatherWarps - 1) / kGatherWarps;
     if (bx > 256) bx = 256;
     if (bx < 1) bx = 1;
     resident_fill_kernel<<<dim3((unsigned)bx, B), kGatherWarps * 32, 0, st>>>(pool_dev, ready, cap,
-                                                                              layer, B, G, staging);
+                                                                              layer, B, G, staging, err);
     return cudaGetLastError();
 }
 

@@ -623,12 +623,12 @@ int fm_select(srh_ctx* ctx, const float* d_scores, int n, int mode, int k, float
 }
 
 int kvswap_stage(srh_ctx* ctx, int layer, const int32_t* d_sel, const int32_t* d_count,
-                 float* d_staging, int32_t* d_phys, int32_t* d_count_l, srh_stream_t main,
+                 uint16_t* d_staging, int32_t* d_phys, int32_t* d_count_l, srh_stream_t main,
                  srh_stream_t side) {
     if (!ctx) return SRH_ERR_INVALID;
     if (!d_sel || !d_count || !d_staging || !d_phys || !d_count_l) return fail(ctx, SRH_ERR_INVALID, "NULL pointer");
     if (layer < -1 || layer >= ctx->L) return fail(ctx, SRH_ERR_INVALID, "layer out of range");
-    if (((uintptr_t)d_staging) & 15) return fail(ctx, SRH_ERR_INVALID, "staging must be 16-byte aligned");
+    if (((uintptr_t)d_staging) & 31) return fail(ctx, SRH_ERR_INVALID, "staging must be 32-byte aligned");
     if (ctx->staging && ctx->staging != d_staging)
         return fail(ctx, SRH_ERR_INVALID, "d_staging differs from the buffer bound on the first call");
     ctx->staging = d_staging;
@@ -639,7 +639,7 @@ int kvswap_stage(srh_ctx* ctx, int layer, const int32_t* d_sel, const int32_t* d
     for (int l = l0; l < l0 + nl; ++l) {
         if (ctx->swap[l] || !ctx->resident_dirty[l]) continue;
         cudaError_t e = launch_resident_fill(ctx->pool_dev[l], ctx->h_layers[l].host_ready, ctx->caps[l], l,
-                                             ctx->B, ctx->G, d_staging, sm);
+                                             ctx->B, ctx->G, d_staging, ctx->d_err, sm);
         if (e != cudaSuccess) return cuda_fail(ctx, e, "resident fill");
         ctx->resident_dirty[l] = 0;
         unsigned long long ready = 0;
@@ -675,7 +675,7 @@ int kvswap_stage(srh_ctx* ctx, int layer, const int32_t* d_sel, const int32_t* d
 }
 
 int lsa_attend(srh_ctx* ctx, int layer, const uint16_t* d_q, int n_heads, const float* d_window,
-               const float* d_staging, const int32_t* d_phys, const int32_t* d_count_l, float* d_out,
+               const uint16_t* d_staging, const int32_t* d_phys, const int32_t* d_count_l, float* d_out,
                srh_stream_t stream) {
     if (!ctx) return SRH_ERR_INVALID;
     if (!d_q || !d_window || !d_staging || !d_phys || !d_count_l || !d_out)
@@ -683,8 +683,8 @@ int lsa_attend(srh_ctx* ctx, int layer, const uint16_t* d_q, int n_heads, const 
     if (layer < -1 || layer >= ctx->L) return fail(ctx, SRH_ERR_INVALID, "layer out of range");
     if (n_heads != 16 && n_heads != 32 && n_heads != 64)
         return fail(ctx, SRH_ERR_INVALID, "n_heads must be 16, 32 or 64");
-    if (((uintptr_t)d_q | (uintptr_t)d_window | (uintptr_t)d_staging | (uintptr_t)d_out) & 15)
-        return fail(ctx, SRH_ERR_INVALID, "q/window/staging/out must be 16-byte aligned");
+    if (((uintptr_t)d_q | (uintptr_t)d_out) & 15 || ((uintptr_t)d_window | (uintptr_t)d_staging) & 31)
+        return fail(ctx, SRH_ERR_INVALID, "q/out must be 16-byte aligned, window/staging 32-byte aligned");
     const AttnPlan& pl = ctx->plans[layer + 1];
     const cudaError_t e = launch_attend(ctx->d_segs + pl.seg0, ctx->d_cta_begin + pl.cta0, pl.n_ctas,
                                         ctx->d_merges + pl.merge0, ctx->d_merge_cnt + pl.merge0, n_heads, ctx->B,

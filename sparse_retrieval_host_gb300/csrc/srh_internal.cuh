@@ -204,7 +204,7 @@ struct Ctx {
     float* d_part_ml = nullptr;         // [max_slots][kAttnMlStride]
     unsigned long long* d_merge_cnt = nullptr;   // arrivals per split pair, all plans
     // bookkeeping
-    float* staging = nullptr;           // the staging buffer bound to this context
+    uint16_t* staging = nullptr;        // the staging buffer (fp16 rows) bound to this context
     cudaEvent_t ev_resolved = nullptr;
     cudaEvent_t ev_gathered = nullptr;
     unsigned long long stage_calls = 0;
@@ -296,16 +296,16 @@ cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int
                        unsigned long long* stats, uint32_t* err, AdaptParams ap, cudaStream_t st,
                        bool chained);
 cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, int S,
-                          const int2* miss, const int* miss_count, float* staging,
+                          const int2* miss, const int* miss_count, uint16_t* staging,
                           uint32_t* err, int sm_count, cudaStream_t st, bool chained);
 cudaError_t launch_touch(const float* p, long long n_floats, uint32_t* sink, int sm_count, cudaStream_t st);
 cudaError_t launch_store(const LayerDev* layers, int l, int B, int G, int seq, long long c0, int n,
-                         const float* rows, float* staging, uint32_t* err, cudaStream_t st);
+                         const float* rows, uint16_t* staging, uint32_t* err, cudaStream_t st);
 cudaError_t launch_resident_fill(const float* pool_dev, const uint8_t* ready, long long cap,
-                                 int layer, int B, int G, float* staging, cudaStream_t st);
+                                 int layer, int B, int G, uint16_t* staging, uint32_t* err, cudaStream_t st);
 cudaError_t launch_attend(const AttnSeg* segs, const int* cta_begin, int n_ctas, const MergeItem* merges,
                           unsigned long long* merge_cnt, int n_heads, int B, int G, int S, const uint16_t* q,
-                          const float* window, const float* staging, const int32_t* phys, const int32_t* count_l,
+                          const float* window, const uint16_t* staging, const int32_t* phys, const int32_t* count_l,
                           float* out, uint16_t* part_o, float* part_ml, uint32_t* err, cudaStream_t st,
                           bool chained);
 size_t lru_smem_bytes(int S, int G);

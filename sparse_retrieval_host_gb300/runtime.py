@@ -68,7 +68,7 @@ class DecodeStep:
         self.scores = torch.zeros((B, n), dtype=f32, device=dev)
         self.sel = torch.zeros((B, S), dtype=i32, device=dev)
         self.count = torch.zeros((B,), dtype=i32, device=dev)
-        self.staging = torch.zeros((L, B, G, abi.KV_DIM), dtype=f32, device=dev)
+        self.staging = torch.zeros((L, B, G, abi.KV_DIM), dtype=torch.float16, device=dev)   # fp16 staged rows
         self.phys = torch.zeros((L, B, S), dtype=i32, device=dev)
         self.count_l = torch.zeros((L, B), dtype=i32, device=dev)
         self.window = torch.zeros((L, B, abi.WINDOW, abi.KV_DIM), dtype=f32, device=dev)

@@ -86,14 +86,14 @@ def _run_decode(w, steps, attend_layers=None, pools=None, policy=None, attend_se
                         if ds.swap[l]:
                             hits += ref.swap[l][b].hits
                             misses += len(ref.swap[l][b].misses)
-            # staged rows always hold the pool rows of the GPU's own selection
+            # staged rows always hold the pool rows of the GPU's own selection, rounded to fp16
             stg = ds.staging
             for l in list(layers)[:3]:
                 for b in seqs:
                     n_l = int(cl[l, b])
                     got = stg[l, b][torch.from_numpy(phys[l, b, :n_l] - 128).long().cuda()].cpu().numpy()
                     lst = np.asarray(sorted(set(sel[b, :cnt[b]] * 4 // w.layer_ratios[l])), dtype=np.int64)
-                    want_rows = rows_of(l, b, lst)
+                    want_rows = np.asarray(rows_of(l, b, lst), dtype=np.float32).astype(np.float16)   # fp16 staging
                     assert sorted(map(bytes, got)) == sorted(map(bytes, want_rows))
             if same:
                 matched += 1

@@ -52,7 +52,7 @@ def test_store_updates_pool_and_the_staged_row_and_keeps_the_slot():
         torch.cuda.synchronize()
         view = ds.pool_view(0, 0)
         assert np.array_equal(view[staged], new[0]) and np.array_equal(view[fresh], new[1])
-        assert np.array_equal(ds.staging[0, 0, slot].cpu().numpy(), new[0])
+        assert np.array_equal(ds.staging[0, 0, slot].cpu().numpy(), new[0].astype(np.float16))   # fp16 staging
         pools[(0, 0)][staged] = new[0]
         pools[(0, 0)][fresh] = new[1]
         ora.store(0, 0, staged, 1)
@@ -98,7 +98,7 @@ def test_store_on_a_layer_that_does_not_swap(before_first_stage):
         ds.step(spec)
         torch.cuda.synchronize()
         ref = _ref_step(ora, w, keys, 1, pools)
-        assert np.array_equal(ds.staging[0, 0, 100:103].cpu().numpy(), new)
+        assert np.array_equal(ds.staging[0, 0, 100:103].cpu().numpy(), new.astype(np.float16))
         err, rel = attn_err(ds.out[0, 0].cpu().numpy(), ref.out[(0, 0)])
         assert rel <= ATTN_TOL, (err, rel)
         assert ds.check_error() == 0
@@ -166,3 +166,47 @@ def test_periodic_selection_matches_scoring_every_step():
     for xa, xb in zip(sa, sb):
         for a, b in zip(xa, xb):
             assert torch.equal(a, b)
+
+
+def test_fp16_staging_reports_pool_values_beyond_its_range():
+    """Staged rows are kept as fp16: a pool value beyond +-65504 that reaches a
+    staging slot -- by a store into a staged chunk, or by the miss gather of a
+    chunk stored earlier -- is reported as SRH_ERR_RANGE; finite rows are not."""
+    from sparse_retrieval_host_gb300 import abi
+    w = C.TINY
+    pools = {(0, 0): G.pool(w, 0, 0)}
+    ds = make_ds(w)
+    try:
+        fill(ds, w, pools)
+        load_step_inputs(ds, w, 0)
+        ds.step(spec_of(w))
+        torch.cuda.synchronize()
+        assert ds.check_error() == abi.SRH_OK
+        sel = ds.sel[0, :int(ds.count[0])].cpu().numpy()
+        staged = int(sel[0])
+        big = pools[(0, 0)][staged:staged + 1].copy()
+        big[0, 7] = 1e5
+        ds.store(0, 0, staged, torch.from_numpy(big).cuda())      # the staged row gets it
+        torch.cuda.synchronize()
+        assert ds.check_error() == abi.SRH_ERR_RANGE
+        assert ds.check_error() == abi.SRH_OK
+        ds.store(0, 0, staged, torch.from_numpy(pools[(0, 0)][staged:staged + 1].copy()).cuda())
+        torch.cuda.synchronize()
+        assert ds.check_error() == abi.SRH_OK
+        # a chunk in no slot: the store writes the pool only, its miss gather converts the row
+        fresh = int(np.setdiff1d(np.arange(w.n_chunks), sel)[0])
+        big = pools[(0, 0)][fresh:fresh + 1].copy()
+        big[0, 300] = -7e4
+        ds.store(0, 0, fresh, torch.from_numpy(big).cuda())
+        torch.cuda.synchronize()
+        assert ds.check_error() == abi.SRH_OK
+        s = np.zeros(tuple(ds.sel.shape), np.int32)
+        s[0, 0] = fresh
+        ds.sel.copy_(torch.from_numpy(s))
+        ds.count.copy_(torch.ones_like(ds.count))
+        ds.stage()
+        torch.cuda.synchronize()
+        assert ds.check_error() == abi.SRH_ERR_RANGE
+        assert ds.check_error() == abi.SRH_OK
+    finally:
+        ds.close()
