@@ -167,6 +167,22 @@ void srh_destroy(srh_ctx* ctx);
  * batch * ceil(context_len / ratio) * kv_dim * 4 ([P1] 关键参数调优, item 2). */
 int srh_pinned_required_bytes(const srh_config* cfg, unsigned long long* out);
 
+/*
+ * The attention work split of a configuration, computed on the host without
+ * a GPU (no counterpart on the pages: a check of lsa_attend's static plan).
+ *   cfg       a configuration, validated as srh_create does
+ *   sm_count  SMs to plan for (> 0)
+ *   layer     -1: the plan of lsa_attend(layer = -1); else that layer's plan
+ *   info      [6] out: CTAs, segments, split pairs, the largest CTA's rows in
+ *             KiB (window rows 2 KiB, staged rows 1 KiB, at max_select rows
+ *             per pair), 1 if each pair is cut into chunks of equal bytes (one
+ *             wave) or 0 for stream-K tile ranges, 1 if the plan keeps its
+ *             invariants (at most one CTA per SM, every pair covered once in
+ *             row order, merge limits) -- srh_create fails otherwise.
+ * Returns SRH_OK, SRH_ERR_INVALID or SRH_ERR_NOMEM.
+ */
+int srh_attend_plan_info(const srh_config* cfg, int sm_count, int layer, long long* info);
+
 /* Host pointer to the pinned pool of (layer, seq): [cap][kv_dim] fp32, owned by
  * the context, valid until srh_destroy(). The caller writes chunks here and then
  * calls srh_mark_stored(). NULL on a bad argument. */

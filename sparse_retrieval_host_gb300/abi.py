@@ -93,6 +93,7 @@ SIGNATURES = [
     ("srh_create", _i, [ctypes.POINTER(SrhConfig), ctypes.POINTER(_vp)]),
     ("srh_destroy", None, [_vp]),
     ("srh_pinned_required_bytes", _i, [ctypes.POINTER(SrhConfig), ctypes.POINTER(ctypes.c_ulonglong)]),
+    ("srh_attend_plan_info", _i, [ctypes.POINTER(SrhConfig), _i, _i, ctypes.POINTER(_ll)]),
     ("srh_pool_host_ptr", ctypes.POINTER(_f), [_vp, _i, _i]),
     ("srh_mark_stored", _i, [_vp, _i, _i, _ll, _ll]),
     ("kvswap_store", _i, [_vp, _i, _i, _ll, _i, _vp, _vp]),
@@ -193,6 +194,14 @@ def srh_pinned_required_bytes(cfg: SrhConfig) -> int:
     out = ctypes.c_ulonglong()
     _check(load().srh_pinned_required_bytes(ctypes.byref(cfg), ctypes.byref(out)), "srh_pinned_required_bytes")
     return out.value
+
+
+def srh_attend_plan_info(cfg: SrhConfig, sm_count: int, layer: int = -1) -> dict:
+    """srh_attend_plan_info: lsa_attend's work split for this configuration (host only)."""
+    info = (_ll * 6)()
+    _check(load().srh_attend_plan_info(ctypes.byref(cfg), sm_count, layer, info), "srh_attend_plan_info")
+    return {"ctas": info[0], "segments": info[1], "split_pairs": info[2], "max_cta_kib": info[3],
+            "one_wave": bool(info[4]), "valid": bool(info[5])}
 
 
 def srh_pool_host_ptr(ctx: int, layer: int, seq: int) -> int:

@@ -324,8 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             if (tid == 0) atomicOr(a.err, kErrBounds);
             cnt = cnt < 0 ? 0 : a.S;
         }
-        row0 = sg.tile0 * kTileRows;
-        row1 = min(kWindow + cnt, sg.tile1 * kTileRows);
+        row0 = sg.r0;
+        row1 = min(kWindow + cnt, sg.r1);
     };
     // Ask L2 for the rows of the tile at tr0 of pair lb (threads 0-127, one
     // 2 KiB bulk prefetch each): no registers or shared memory, so HBM streams
@@ -384,10 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     for (; si < se; ++si) {
         const AttnSeg sg = a.segs[si];
         const size_t lb = (size_t)sg.lb;
-        // the window tile (rows 0-127, always full) of the CTA's first segment
-        // runs before the wait; the segment's other rows are known after it
-        const bool early = !dep_ready && sg.tile0 == 0 && sg.tile1 > 0;
-        int row0 = 0, row1 = kWindow, n_tiles = 1;
+        // a first tile of window rows only (always present) of the CTA's first
+        // segment runs before the wait; the segment's other rows are known after it
+        const bool early = !dep_ready && sg.r0 < kWindow && sg.r1 > sg.r0 && (sg.r0 == 0 || sg.r1 <= kWindow);
+        int row0 = sg.r0, row1 = min(sg.r1, kWindow), n_tiles = 1;
         // A split pair's arrival count before this CTA's own arrival (read after
         // the dependency wait: every earlier call's arrivals are in). The pair is
         // complete when it reaches the next multiple of its split count.
@@ -480,6 +480,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                 zero_half(r, 1);
             }
         };
+        // row w + 16 j of a tile that holds window rows: fp32 or fp16 by its place
+        auto load_any = [&](float4 (&v)[4], int tr0, int j, int src) {
+            if (tr0 + warp + kWarps * j < kWindow) load_row(v, tr0, j, src);
+            else load_row_h(v[0], v[1], tr0, j, src);
+        };
+        auto store_any = [&](const float4 (&v)[4], int tr0, int j) {
+            if (tr0 + warp + kWarps * j < kWindow) store_row(v, tr0, j);
+            else store_row_h(v[0], v[1], tr0, j);
+        };
         auto issue_pass1 = [&](int x0) {   // d-blocks x0 .. x0 + 3 (thread 0)
             const uint32_t e0 = smem_u32(sm + kOffE), q0 = smem_u32(sm + kOffQ);
 #pragma unroll 1
@@ -496,14 +505,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             if (tile + 1 < n_tiles) prefetch_tile(lb, tr0 + kTileRows, row1);
             // ------------------------------------------------------------ E (all warps)
             const int src = fetch_src(tr0);          // this tile's row sources (lanes 0-7)
-            const bool win = tr0 < kWindow;           // a pair's first tile: its window rows, fp32
+            const bool mixed = tr0 < kWindow;         // window rows (fp32) in the tile
             float4 v[4][4];
-            if (win) {
+            if (mixed) {
                 // four rows in flight per warp (128 KB per CTA); each row's registers
                 // take the next row's loads as soon as they are stored, so the
                 // stream does not drain between the tile's two halves
 #pragma unroll
-                for (int i = 0; i < 4; ++i) load_row(v[i], tr0, i, src);
+                for (int i = 0; i < 4; ++i) load_any(v[i], tr0, i, src);
             } else {
                 // staged rows, fp16: all eight of this warp's rows in flight at once
 #pragma unroll
@@ -525,14 +534,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                 failed = true;
                 break;
             }
-            if (win) {
+            if (mixed) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    store_row(v[i], tr0, i);
-                    load_row(v[i], tr0, 4 + i, src);
+                    store_any(v[i], tr0, i);
+                    load_any(v[i], tr0, 4 + i, src);
                 }
 #pragma unroll
-                for (int i = 0; i < 4; ++i) store_row(v[i], tr0, 4 + i);
+                for (int i = 0; i < 4; ++i) store_any(v[i], tr0, 4 + i);
             } else {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) store_row_h(v[j >> 1][2 * (j & 1)], v[j >> 1][2 * (j & 1) + 1], tr0, j);

@@ -133,104 +133,190 @@ void free_ctx(srh_ctx* ctx) {
 }
 
 // The static attention plan of one lsa_attend scope (the pairs (layer, seq)
-// of `layers`). A pair holds 128 window rows plus at most min(S, cap) staged
-// rows, in 128-row tiles; an attention CTA holds ~218 KB of shared memory and
-// 512 threads of 128 registers, so one runs per SM, and a plan never has more
-// CTAs than SMs (every CTA becomes resident, which the merge waits rely on). With T tiles in the scope, no plan can give
-// a CTA fewer than ceil(T / SMs) tiles; when cutting every pair into chunks of
-// that many tiles fits one wave, each CTA runs one chunk; otherwise the T
-// tiles, in (layer, seq, row) order, are cut into min(SMs, T) contiguous
-// ranges of equal size (+-1 tile), one CTA each. A pair spread over several
-// CTAs is merged by those CTAs, each taking one share, once all its partials
-// are written. CTAs whose first segment starts with a pair's window tile come
-// first: that tile needs no earlier kernel's output, and the CTAs launched
-// first run it while those kernels finish. The plan depends only on the
-// configuration, so the same rows give the same bits whichever slots hold them.
+// of `layers`). A pair holds 128 window rows (fp32, 2 KiB each) plus at most
+// min(S, cap) staged rows (fp16, 1 KiB each). A CTA runs its rows in tiles of
+// up to 128 rows, each tile a serial chain (rows in, two products, softmax);
+// it holds ~218 KB of shared memory and 512 threads of 128 registers, so one
+// runs per SM, and a plan never has more CTAs than SMs (every CTA becomes
+// resident, which the merge waits rely on).
+//   * One wave, when every pair's tiles fit on CTAs of their own: each pair is
+//     cut into k chunks of at most one tile, balanced by bytes (the largest
+//     chunk as small as k chunks of <= 128 rows allow); k starts at the pair's
+//     tile count and the pairs with the largest chunks get one more CTA each,
+//     all together, while the SMs last. No CTA starts a second pair (a second
+//     query load and epilogue).
+//   * Otherwise stream-K: the scope's tiles, in (layer, seq, row) order and
+//     weighted by their bytes, cut into at most SMs contiguous ranges of
+//     equal bytes to the nearest tile.
+// A pair spread over several CTAs is merged by those CTAs, each taking one
+// share, once all its partials are written. CTAs whose first tile holds only
+// window rows come first: that tile needs no earlier kernel's output, and the
+// CTAs launched first run it while those kernels finish. The plan depends only
+// on the configuration, so the same rows give the same bits whichever slots
+// hold them.
 void plan_scope(srh_ctx* ctx, const std::vector<int>& layers, std::vector<AttnSeg>* segs,
                 std::vector<int>* cta_begin, std::vector<MergeItem>* merges, AttnPlan* plan) {
     const int B = ctx->B;
-    std::vector<int> lbs, tiles;
-    long long T = 0;
+    const long long N = ctx->sm_count;
+    constexpr long long kT = kAttnTile;
+    std::vector<int> lbs;
+    std::vector<long long> rows;
     for (int l : layers)
         for (int b = 0; b < B; ++b) {
-            const long long rows = kWindow + std::min<long long>(ctx->S, ctx->caps[l]);
             lbs.push_back(l * B + b);
-            tiles.push_back((int)((rows + kAttnTile - 1) / kAttnTile));
-            T += tiles.back();
+            rows.push_back(kWindow + std::min<long long>(ctx->S, ctx->caps[l]));
         }
-    // raw segments (pair, tile range) and the first segment of each CTA
-    struct Raw { size_t r; int t0, t1; };
+    const size_t P = lbs.size();
+    // KiB of rows [0, r) of a pair: window rows 2, staged rows 1
+    auto cost_to = [](long long r) { return r <= kWindow ? 2 * r : 2LL * kWindow + (r - kWindow); };
+    // Cut rows [0, n) into chunks of at most kT rows and M KiB, each as long as
+    // it can be; returns the chunk count (or -1 if a row exceeds M) and the ends.
+    auto pack = [&](long long n, long long M, std::vector<long long>* ends) -> long long {
+        long long r = 0, c = 0;
+        while (r < n) {
+            const long long w = r < kWindow ? std::min({kWindow - r, M / 2, kT, n - r}) : 0;
+            long long e = r + w, room = M - 2 * w;
+            if (e >= kWindow && e - r < kT) e += std::min({n - e, room, kT - (e - r)});
+            if (e == r) return -1;
+            if (ends) ends->push_back(e);
+            r = e;
+            ++c;
+        }
+        return c;
+    };
+    // the smallest largest-chunk of a pair cut into at most k such chunks
+    auto best = [&](long long n, long long k) {
+        long long lo = 2, hi = 2 * kT;
+        while (lo < hi) {
+            const long long m = (lo + hi) / 2;
+            const long long c = pack(n, m, nullptr);
+            if (c >= 0 && c <= k) hi = m;
+            else lo = m + 1;
+        }
+        return lo;
+    };
+    struct Raw { size_t p; int r0, r1; };
     std::vector<Raw> raw;
     std::vector<int> begin;
-    const long long m = (T + ctx->sm_count - 1) / ctx->sm_count;
-    long long n_chunks = 0;
-    for (int t : tiles) n_chunks += (t + m - 1) / m;
-    if (n_chunks <= ctx->sm_count) {
-        // one wave: each pair cut into chunks of at most m tiles, one CTA per
-        // chunk, so no CTA starts a second pair (a second query load and epilogue)
-        for (size_t r = 0; r < lbs.size(); ++r) {
-            const int nc = (int)((tiles[r] + m - 1) / m);
-            for (int c = 0; c < nc; ++c) {
+    long long tiles_all = 0;
+    for (long long r : rows) tiles_all += (r + kT - 1) / kT;
+    const bool one_wave = tiles_all <= N;
+    if (one_wave) {
+        // A CTA's fixed costs (its queries, the dependent-load chain, the epilogue
+        // and the merge wait) outweigh the rows below about one staged tile: a
+        // pair gets more chunks than tiles only down to 128 KiB each, and at most
+        // attend_max_splits() chunks (what a merge combines).
+        std::vector<long long> k(P), kmax(P), top(P);
+        long long used = 0;
+        for (size_t p = 0; p < P; ++p) {
+            k[p] = (rows[p] + kT - 1) / kT;
+            kmax[p] = std::max(k[p], std::min<long long>(attend_max_splits(), cost_to(rows[p]) / 128));
+            top[p] = best(rows[p], k[p]);
+            used += k[p];
+        }
+        for (;;) {
+            long long mx = 0;
+            for (size_t p = 0; p < P; ++p) mx = std::max(mx, top[p]);
+            std::vector<size_t> at;
+            bool room = true;
+            for (size_t p = 0; p < P; ++p)
+                if (top[p] == mx) {
+                    at.push_back(p);
+                    room = room && k[p] < kmax[p];
+                }
+            if (!room || used + (long long)at.size() > N) break;
+            for (size_t p : at) top[p] = best(rows[p], ++k[p]);
+            used += (long long)at.size();
+        }
+        for (size_t p = 0; p < P; ++p) {
+            std::vector<long long> ends;
+            pack(rows[p], top[p], &ends);
+            long long prev = 0;
+            for (long long e : ends) {
                 begin.push_back((int)raw.size());
-                raw.push_back(Raw{r, (int)(c * m), (int)std::min<long long>((c + 1) * m, tiles[r])});
+                raw.push_back(Raw{p, (int)prev, (int)e});
+                prev = e;
             }
         }
     } else {
-        // stream-K: min(SMs, T) CTAs over contiguous tile ranges
-        const int n = (int)std::min<long long>(ctx->sm_count, T);
-        size_t q = 0;
-        long long qs = 0;                       // first tile of pair q
-        for (int k = 0; k < n; ++k) {
-            begin.push_back((int)raw.size());
-            const long long t0 = (long long)k * T / n, t1 = (long long)(k + 1) * T / n;
-            while (qs + tiles[q] <= t0) qs += tiles[q++];
-            long long t = t0;
-            size_t r = q;
-            long long rs = qs;
-            while (t < t1) {
-                const long long re = rs + tiles[r];
-                const long long e = std::min(re, t1);
-                raw.push_back(Raw{r, (int)(t - rs), (int)(e - rs)});
-                t = e;
-                if (e == re) rs += tiles[r++];
+        // stream-K over whole tiles, weighted by bytes
+        struct Tile { size_t p; long long r0, r1, c; };
+        std::vector<Tile> tl;
+        long long total = 0;
+        for (size_t p = 0; p < P; ++p)
+            for (long long r0 = 0; r0 < rows[p]; r0 += kT) {
+                const long long r1 = std::min(r0 + kT, rows[p]);
+                tl.push_back(Tile{p, r0, r1, cost_to(r1) - cost_to(r0)});
+                total += tl.back().c;
             }
+        const long long n = std::min<long long>(N, (long long)tl.size());
+        size_t t = 0;
+        long long acc = 0;
+        for (long long j = 0; j < n && t < tl.size(); ++j) {
+            // the range ends at the tile boundary nearest to (j + 1) / n of the bytes,
+            // leaving at least one tile for each remaining range
+            const long long goal = (j + 1) * total / n;
+            size_t e = t + 1;
+            long long a = acc + tl[t].c;
+            while (e < tl.size() && (long long)(tl.size() - e) > n - j - 1 && 2 * (a + tl[e].c) <= 2 * goal + tl[e].c) {
+                a += tl[e].c;
+                ++e;
+            }
+            if (j == n - 1) {
+                for (; e < tl.size(); ++e) a += tl[e].c;
+            }
+            begin.push_back((int)raw.size());
+            for (size_t i = t; i < e; ++i) {
+                if (!raw.empty() && (int)raw.size() > begin.back() && raw.back().p == tl[i].p &&
+                    raw.back().r1 == tl[i].r0)
+                    raw.back().r1 = (int)tl[i].r1;
+                else
+                    raw.push_back(Raw{tl[i].p, (int)tl[i].r0, (int)tl[i].r1});
+            }
+            t = e;
+            acc = a;
         }
     }
     plan->seg0 = (int)segs->size();
     plan->cta0 = (int)cta_begin->size();
     plan->merge0 = (int)merges->size();
     plan->n_ctas = (int)begin.size();
+    plan->one_wave = one_wave ? 1 : 0;
     // pairs with more than one segment write partials, in row order
-    std::vector<int> n_parts(lbs.size(), 0), merge_of(lbs.size(), -1), seen(lbs.size(), 0);
-    for (const Raw& x : raw) ++n_parts[x.r];
+    std::vector<int> n_parts(P, 0), merge_of(P, -1), seen(P, 0);
+    for (const Raw& x : raw) ++n_parts[x.p];
     int slot = 0;
     for (const Raw& x : raw) {
-        if (n_parts[x.r] > 1 && merge_of[x.r] < 0) {
-            merge_of[x.r] = (int)merges->size() - plan->merge0;
-            merges->push_back(MergeItem{lbs[x.r], slot, n_parts[x.r], 0});
-            slot += n_parts[x.r];
+        if (n_parts[x.p] > 1 && merge_of[x.p] < 0) {
+            merge_of[x.p] = (int)merges->size() - plan->merge0;
+            merges->push_back(MergeItem{lbs[x.p], slot, n_parts[x.p], 0});
+            slot += n_parts[x.p];
         }
     }
     std::vector<AttnSeg> tmp;
     for (const Raw& x : raw) {
-        const int mi = merge_of[x.r];
+        const int mi = merge_of[x.p];
         int sl = -1, part = 0;
         if (mi >= 0) {
-            part = seen[x.r]++;
+            part = seen[x.p]++;
             sl = (*merges)[plan->merge0 + mi].first + part;
         }
-        tmp.push_back(AttnSeg{lbs[x.r], x.t0, x.t1, sl, mi, part});
+        tmp.push_back(AttnSeg{lbs[x.p], x.r0, x.r1, sl, mi, part});
     }
-    // CTAs that start with a window tile first, otherwise in plan order
+    // CTAs whose first tile holds only window rows first, otherwise in plan order
     const int nct = (int)begin.size();
+    auto window_first = [&](int j) {
+        const Raw& x = raw[begin[j]];
+        return x.r0 < kWindow && (x.r0 == 0 || x.r1 <= kWindow);
+    };
     std::vector<int> order;
     for (int pass = 0; pass < 2; ++pass)
-        for (int k = 0; k < nct; ++k)
-            if ((raw[begin[k]].t0 == 0) == (pass == 0)) order.push_back(k);
-    for (int k : order) {
-        const int e = k + 1 < nct ? begin[k + 1] : (int)raw.size();
+        for (int j = 0; j < nct; ++j)
+            if (window_first(j) == (pass == 0)) order.push_back(j);
+    for (int j : order) {
+        const int e = j + 1 < nct ? begin[j + 1] : (int)raw.size();
         cta_begin->push_back((int)segs->size() - plan->seg0);
-        for (int i = begin[k]; i < e; ++i) segs->push_back(tmp[i]);
+        for (int i = begin[j]; i < e; ++i) segs->push_back(tmp[i]);
     }
     cta_begin->push_back((int)segs->size() - plan->seg0);
     plan->n_segs = (int)raw.size();
@@ -238,8 +324,52 @@ void plan_scope(srh_ctx* ctx, const std::vector<int>& layers, std::vector<AttnSe
     plan->n_slots = slot;
 }
 
+// The plan's invariants, which the kernel relies on: at most one CTA per SM;
+// every pair of the scope covered once, in row order, by its segments (parts
+// 0 .. ns-1 of a split pair contiguous from row 0, within the merge limit); a
+// CTA takes part in at most attend_max_duties() split pairs.
+bool plan_valid(const srh_ctx* ctx, const std::vector<int>& layers, const std::vector<AttnSeg>& segs,
+                const std::vector<int>& cta_begin, const std::vector<MergeItem>& merges, const AttnPlan& pl) {
+    if (pl.n_ctas < 1 || pl.n_ctas > ctx->sm_count) return false;
+    std::vector<std::vector<AttnSeg>> by_lb((size_t)ctx->L * ctx->B);
+    for (int j = 0; j < pl.n_ctas; ++j) {
+        const int a = cta_begin[pl.cta0 + j], b = cta_begin[pl.cta0 + j + 1];
+        if (a < 0 || b < a || b > pl.n_segs) return false;
+        int duties = 0;
+        for (int i = a; i < b; ++i) {
+            const AttnSeg& g = segs[pl.seg0 + i];
+            if (g.lb < 0 || g.lb >= ctx->L * ctx->B || g.r1 <= g.r0) return false;
+            if (g.slot >= 0) ++duties;
+            by_lb[g.lb].push_back(g);
+        }
+        if (duties > attend_max_duties()) return false;
+    }
+    if (cta_begin[pl.cta0] != 0 || cta_begin[pl.cta0 + pl.n_ctas] != pl.n_segs) return false;
+    for (int l : layers)
+        for (int b = 0; b < ctx->B; ++b) {
+            std::vector<AttnSeg>& v = by_lb[(size_t)l * ctx->B + b];
+            const long long rows = kWindow + std::min<long long>(ctx->S, ctx->caps[l]);
+            if (v.empty()) return false;
+            std::sort(v.begin(), v.end(), [](const AttnSeg& x, const AttnSeg& y) { return x.r0 < y.r0; });
+            const int ns = (int)v.size();
+            if (ns > attend_max_splits()) return false;
+            for (int i = 0; i < ns; ++i) {
+                if (v[i].r0 != (i == 0 ? 0 : v[i - 1].r1)) return false;
+                if (ns == 1) {
+                    if (v[i].slot >= 0) return false;
+                    continue;
+                }
+                if (v[i].merge < 0 || v[i].merge >= pl.n_merges || v[i].part != i) return false;
+                const MergeItem& m = merges[pl.merge0 + v[i].merge];
+                if (m.ns != ns || m.lb != v[i].lb || v[i].slot != m.first + i || m.first + ns > pl.n_slots) return false;
+            }
+            if (v[ns - 1].r1 != rows) return false;
+        }
+    return true;
+}
+
 // Plans [0] for all layers and [1 + l] for layer l alone.
-void plan_attention(srh_ctx* ctx, std::vector<AttnSeg>* segs, std::vector<int>* cta_begin,
+bool plan_attention(srh_ctx* ctx, std::vector<AttnSeg>* segs, std::vector<int>* cta_begin,
                     std::vector<MergeItem>* merges) {
     ctx->plans.assign(ctx->L + 1, AttnPlan{});
     std::vector<int> all(ctx->L);
@@ -248,6 +378,9 @@ void plan_attention(srh_ctx* ctx, std::vector<AttnSeg>* segs, std::vector<int>* 
     for (int l = 0; l < ctx->L; ++l) plan_scope(ctx, {l}, segs, cta_begin, merges, &ctx->plans[1 + l]);
     ctx->max_slots = 0;
     for (const AttnPlan& p : ctx->plans) ctx->max_slots = std::max(ctx->max_slots, p.n_slots);
+    bool ok = plan_valid(ctx, all, *segs, *cta_begin, *merges, ctx->plans[0]);
+    for (int l = 0; ok && l < ctx->L; ++l) ok = plan_valid(ctx, {l}, *segs, *cta_begin, *merges, ctx->plans[1 + l]);
+    return ok;
 }
 
 }  // namespace
@@ -269,6 +402,45 @@ int srh_pinned_required_bytes(const srh_config* cfg, unsigned long long* out) {
     const int rc = validate_config(cfg, &why);
     if (rc != SRH_OK) return fail(nullptr, rc, why);
     *out = pinned_bytes(cfg);
+    return SRH_OK;
+}
+
+int srh_attend_plan_info(const srh_config* cfg, int sm_count, int layer, long long* info) {
+    std::string why;
+    if (!info || sm_count <= 0) return fail(nullptr, SRH_ERR_INVALID, "info is NULL or sm_count <= 0");
+    const int rc = validate_config(cfg, &why);
+    if (rc != SRH_OK) return fail(nullptr, rc, why);
+    if (layer < -1 || layer >= cfg->n_layers) return fail(nullptr, SRH_ERR_INVALID, "layer out of range");
+    srh_ctx* ctx = new (std::nothrow) srh_ctx();
+    if (!ctx) return fail(nullptr, SRH_ERR_NOMEM, "host allocation failed");
+    ctx->B = cfg->batch;
+    ctx->L = cfg->n_layers;
+    ctx->G = cfg->gpu_chunks;
+    ctx->S = cfg->max_select > 0 ? cfg->max_select : cfg->index_topk;
+    ctx->sm_count = sm_count;
+    for (int l = 0; l < ctx->L; ++l) ctx->caps.push_back(cap_of(cfg->context_len, cfg->layer_ratio[l]));
+    std::vector<AttnSeg> segs;
+    std::vector<int> cta_begin;
+    std::vector<MergeItem> merges;
+    const bool ok = plan_attention(ctx, &segs, &cta_begin, &merges);
+    const AttnPlan& pl = ctx->plans[layer + 1];
+    long long worst = 0;
+    for (int j = 0; j < pl.n_ctas; ++j) {
+        long long c = 0;
+        for (int i = cta_begin[pl.cta0 + j]; i < cta_begin[pl.cta0 + j + 1]; ++i) {
+            const AttnSeg& g = segs[pl.seg0 + i];
+            auto to = [](long long r) { return r <= kWindow ? 2 * r : 2LL * kWindow + (r - kWindow); };
+            c += to(g.r1) - to(g.r0);
+        }
+        worst = std::max(worst, c);
+    }
+    info[0] = pl.n_ctas;
+    info[1] = pl.n_segs;
+    info[2] = pl.n_merges;
+    info[3] = worst;
+    info[4] = pl.one_wave;
+    info[5] = ok ? 1 : 0;
+    delete ctx;
     return SRH_OK;
 }
 
@@ -390,7 +562,8 @@ int srh_create(const srh_config* cfg, srh_ctx** out) {
     std::vector<AttnSeg> segs;
     std::vector<int> cta_begin;
     std::vector<MergeItem> merges;
-    plan_attention(ctx, &segs, &cta_begin, &merges);
+    if (!plan_attention(ctx, &segs, &cta_begin, &merges))
+        return bail(SRH_ERR_INVALID, "internal: the attention plan breaks its invariants for this configuration");
     e = cudaMalloc(&ctx->d_segs, sizeof(AttnSeg) * segs.size());
     if (e == cudaSuccess)
         e = cudaMemcpy(ctx->d_segs, segs.data(), sizeof(AttnSeg) * segs.size(), cudaMemcpyHostToDevice);

@@ -117,15 +117,16 @@ struct LayerDev {
     AdaptState* adapt;       // [B] (swap layers)
 };
 
-// One segment of the attention plan: tiles [tile0, tile1) (128 rows each) of
-// one (layer, seq). A CTA runs a contiguous range of the plan's tiles, so its
-// segments are the pairs that range touches. A segment holding every tile of
-// its pair writes the output; the others write partials to `slot`, and the
-// CTA merges share `part` of the pair's output once every partial is in.
+// One segment of the attention plan: rows [r0, r1) of one (layer, seq) (rows
+// 0-127 are the window rows, then the staged rows in selection order), run in
+// tiles of up to 128 rows from r0. A CTA runs one or more segments. A segment
+// holding every row of its pair writes the output; the others write partials
+// to `slot`, and the CTA merges share `part` of the pair's output once every
+// partial is in.
 struct AttnSeg {
     int lb;      // layer * B + seq
-    int tile0;
-    int tile1;
+    int r0;
+    int r1;
     int slot;    // partial slot, or -1
     int merge;   // index of the pair's MergeItem in its plan, or -1
     int part;    // this segment's place among the pair's partials (its merge share)
@@ -146,6 +147,7 @@ struct AttnPlan {
     int cta0, n_ctas;      // into Ctx::d_cta_begin (n_ctas + 1 entries from cta0)
     int merge0, n_merges;  // into Ctx::d_merges
     int n_slots;
+    int one_wave;          // 1: each pair cut into chunks of equal bytes; 0: stream-K tile ranges
 };
 
 struct Ctx {
