@@ -504,6 +504,12 @@ def run_ours(args, dist, rank, world, local):
             "steps": K,
             "warmup": args.warmup,
             "ms_per_step": statistics.mean(step_ms),
+            "step_ms_spread": {
+                "p50": statistics.median(step_ms), "max": max(step_ms),
+                "lookahead_boundary": [[args.warmup + i, step_ms[i]] for i in range(K)
+                                       if (args.warmup + i) % w.lookahead == 0],
+                "note": "per-step device time; a lookahead-boundary step (new indexer queries) gathers "
+                        "the new selection's misses from the pinned pool"},
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
