@@ -37,7 +37,7 @@ import numpy as np  # noqa: E402
 from srh_workload import configs as C  # noqa: E402
 from srh_workload import generate as G  # noqa: E402
 
-TC_SCORE_MIN_CHUNKS = 1 << 19  # fm_score's tensor-core kernel from this many chunks per call (all sequences)
+TC_SCORE_MIN_CHUNKS = 1 << 18  # fm_score's tensor-core kernel from this many chunks per call (all sequences)
 HOLD_CYCLES = 400_000          # ~0.2 ms device-side wait before eagerly timed calls
 BASE_KERNELS = 5              # score, select, lru, gather, attend (+ the candidate pass)
 COLLECT_MIN_N = 16384         # fm_select runs its candidate pass above this many chunks

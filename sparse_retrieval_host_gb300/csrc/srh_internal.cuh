@@ -271,7 +271,7 @@ cudaError_t launch_score(const uint16_t* keys, int n, int B, const uint16_t* q, 
                          bool clear_cand);
 // One key set on the tensor cores (TMA-streamed key tiles, tcgen05, TMEM);
 // launch_score uses it from this many chunks per call (all sequences) up.
-constexpr long long kTcMinChunks = 1LL << 19;
+constexpr long long kTcMinChunks = 1LL << 18;
 cudaError_t launch_score_tc(const uint16_t* keys, int n, int B, const uint16_t* q, float scale, const float* bias3,
                             int ensemble, float* scores, uint32_t* hist, uint32_t* err, int sm_count,
                             cudaStream_t st, CandSink sink);

@@ -33,7 +33,7 @@ def _w(**kw):
     _w(context_len=4 * 1001 + 3, code=51),                          # ragged tail: n = 1002
     _w(context_len=4, code=52, index_topk=1, gpu_chunks=1),         # n = 1
     _w(context_len=131072, batch=3, code=53, ensemble=C.ENSEMBLE_MEAN, bias=-7.0),
-    # 2^19 chunks in one call: the tensor-core kernel (smaller calls use the mma.sync one)
+    # 2^19 chunks in one call: the tensor-core kernel (from 2^18; smaller calls use the mma.sync one)
     _w(context_len=131072, batch=16, code=61, layer_ratios=(128,)),
     _w(context_len=4 * (4 * 32768 + 37), batch=4, code=62, layer_ratios=(128,), ensemble=C.ENSEMBLE_MEAN,
        bias=-7.0),
