@@ -76,5 +76,5 @@ def test_bench_names_the_scoring_kernel_the_library_picks():
     txt = open(os.path.join(root, "sparse_retrieval_host_gb300", "csrc", "srh_internal.cuh")).read()
     m = re.search(r"kTcMinChunks\s*=\s*1LL\s*<<\s*(\d+)", txt)
     assert m and bench.TC_SCORE_MIN_CHUNKS == 1 << int(m.group(1))
-    assert "mma.sync" in bench.scoring_kernel(C.CTX8K) and "mma.sync" in bench.scoring_kernel(C.CTX1M)
-    assert "tcgen05" in bench.scoring_kernel(C.batch_sweep(16))
+    assert "mma.sync" in bench.scoring_kernel(C.CTX8K) and "mma.sync" in bench.scoring_kernel(C.CTX256K)
+    assert "tcgen05" in bench.scoring_kernel(C.CTX1M) and "tcgen05" in bench.scoring_kernel(C.batch_sweep(16))
