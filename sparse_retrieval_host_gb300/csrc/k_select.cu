@@ -25,11 +25,16 @@
 //     or above the threshold) to a candidate list; the per-sequence CTA then
 //     works on that list instead of all n scores (if the list overflows its
 //     capacity, the CTA scans all n scores as before);
-//   * when the first digit already isolates the selection and every digit
-//     bucket at or above the cut-off is small, the output is placed without a
-//     sort: candidates are scattered into their buckets (buckets are ordered by
-//     digit), and each one's position is its bucket's start plus the number of
-//     larger keys inside its bucket.
+//   * when the first digit already isolates the selection, the output is
+//     placed without a sort. The keys at or above the cut-off digit are
+//     counted into 4096 fine buckets: a shift of the 32-bit score key over the
+//     digits from the cut-off to the highest one present, so bucket order is
+//     key order and a bucket holds a few keys. A prefix sum gives each bucket's
+//     first output position; the keys are scattered into their buckets, and a
+//     key's position is its bucket's start plus the number of larger keys in
+//     its bucket.
+// Histograms are owned four bins per thread, highest digit first (thread t:
+// digits 4095-4t .. 4092-4t), read and written with one 16-byte access.
 #include "srh_internal.cuh"
 
 namespace srh {
@@ -39,7 +44,7 @@ constexpr int kSelThreads = 1024;
 constexpr int kCandCap = 8192;
 constexpr int kDigit = 12;
 constexpr int kArr = kCandCap + kMaxSelect;             // cand + outk, contiguous in shared memory
-constexpr long long kBucketWork = 256LL * kSelThreads;  // bound on sum of squared bucket sizes
+constexpr unsigned kBucketWork = 256u * kSelThreads;   // bound on sum of squared bucket sizes
 constexpr int kPre = 8;                                 // keys per thread held in registers
 constexpr int kCollectThreads = 256;
 constexpr int kCollectPer = 16;                         // scores per collect thread
@@ -71,6 +76,24 @@ __device__ int block_inclusive_scan(int v, int* warp_buf) {
     const int r = v + (warp > 0 ? warp_buf[warp - 1] : 0);
     __syncthreads();
     return r;
+}
+
+// Inclusive block scan of one int per thread with a single barrier
+// (blockDim.x == kSelThreads, 32 warps): each warp adds up the totals of the
+// warps before it itself. `total` receives the block's sum. Two calls on the
+// same warp_buf must be separated by another barrier.
+__device__ __forceinline__ int block_scan_1bar(int v, int* warp_buf, int& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+    }
+    if (lane == 31) warp_buf[warp] = v;
+    __syncthreads();
+    const int w = warp_buf[lane];
+    total = __reduce_add_sync(0xffffffffu, w);
+    return v + __reduce_add_sync(0xffffffffu, lane < warp ? w : 0);
 }
 
 // Descending bitonic sort of a[0..m) in shared memory (pads to a power of two
@@ -128,17 +151,23 @@ __device__ __forceinline__ int pow2_at_least(int m) {
     return m2;
 }
 
-struct SelShared {
-    uint32_t hist[kHistBins];
-    int bbase[kHistBins];    // first level: keys in higher digits (then: bucket ends)
+// 16-byte aligned size: the 64-bit key arrays follow it in shared memory
+struct alignas(16) SelShared {
+    uint32_t hist[kHistBins];   // digit histogram of the rounds not handed in
+    uint32_t fcnt[kHistBins];   // fine-bucket sizes
+    int fpos[kHistBins];        // fine-bucket starts; after the scatter, ends
     int warp_buf[32];
     int n_out;
     int n_cand;
     int found_digit;
     int found_above;
-    int hist_total;          // sum of the handed-in histogram row
-    unsigned long long sq;   // sum of squared bucket sizes at or above the cut-off
+    int found_cls;
+    int top_digit;              // highest non-empty first digit
+    unsigned sq;                // sum of squared fine-bucket sizes (saturating)
 };
+static_assert(sizeof(SelShared) % 16 == 0, "key arrays after SelShared need 8-byte alignment");
+static_assert(offsetof(SelShared, fcnt) % 16 == 0 && offsetof(SelShared, fpos) % 16 == 0,
+              "histograms are accessed 16 bytes at a time");
 
 // The keys the selection runs over: all n scores of the sequence, or a
 // candidate list of composites made by collect_kernel.
@@ -170,13 +199,11 @@ select_kernel(const float* scores, int n, int mode, int k, float thresh, int cla
     // The handed-in first-digit histogram is read once and left zeroed, so the
     // next scoring pass can add into it without clearing it first. Its loads
     // and the first keys of every thread are issued together: one round trip.
-    constexpr int kHv = kHistBins / kSelThreads;
+    static_assert(kHistBins == 4 * kSelThreads, "four histogram bins per thread");
+    const int own = kHistBins - 4 - 4 * tid;   // bins own .. own + 3 belong to this thread
     uint32_t* hb = hist_in ? hist_in + (size_t)b * kHistBins : nullptr;
-    uint32_t hv[kHv];
-    if (hb) {
-#pragma unroll
-        for (int k = 0; k < kHv; ++k) hv[k] = hb[tid + k * kSelThreads];
-    }
+    uint4 h4 = make_uint4(0u, 0u, 0u, 0u);
+    if (hb) h4 = *reinterpret_cast<const uint4*>(hb + own);
 
     // the key universe: a candidate list when one was made and did not overflow
     Src src{scores + (size_t)b * n, nullptr, n};
@@ -200,18 +227,15 @@ select_kernel(const float* scores, int n, int mode, int k, float thresh, int cla
             if (tid + k * kSelThreads < src.n) body(pre[k]);
         for (int i = tid + kPre * kSelThreads; i < src.n; i += kSelThreads) body(src.get(i));
     };
-    if (hb) {
-#pragma unroll
-        for (int k = 0; k < kHv; ++k) {
-            sh.hist[tid + k * kSelThreads] = hv[k];
-            hb[tid + k * kSelThreads] = 0u;
-        }
-    }
+    const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+    if (hb) *reinterpret_cast<uint4*>(hb + own) = zero4;
+    *reinterpret_cast<uint4*>(sh.fcnt + own) = zero4;
 
     if (tid == 0) {
         sh.n_out = 0;
         sh.n_cand = 0;
-        sh.sq = 0ull;
+        sh.sq = 0u;
+        sh.top_digit = 0;
     }
     __syncthreads();
     // every thread has read the candidate count: leave it zeroed for the next
@@ -264,38 +288,39 @@ select_kernel(const float* scores, int n, int mode, int k, float thresh, int cla
         const int shift = 64 - pbits - D;
         const unsigned long long mask = (1ull << D) - 1ull;
         if (tid == 0) sh.found_digit = -1;
+        uint4 c4;
         if (pbits == 0 && use_hist_in) {
-            // sh.hist holds the handed-in histogram (copied at the start)
+            c4 = h4;
         } else {
-            for (int i = tid; i < kHistBins; i += kSelThreads) sh.hist[i] = 0;
+            *reinterpret_cast<uint4*>(sh.hist + own) = zero4;
             __syncthreads();
             each_key([&](unsigned long long c) {
                 if (pbits == 0 || (c >> (64 - pbits)) == (prefix >> (64 - pbits)))
                     atomicAdd(&sh.hist[(c >> shift) & mask], 1u);
             });
+            __syncthreads();
+            c4 = *reinterpret_cast<const uint4*>(sh.hist + own);
         }
-        __syncthreads();
-        // thread tid owns bins 4095-4*tid .. 4092-4*tid (descending)
-        int local = 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) local += (int)sh.hist[kHistBins - 1 - 4 * tid - j];
-        const int incl = block_inclusive_scan(local, sh.warp_buf);
-        if (tid == kSelThreads - 1) sh.hist_total = incl;
+        const uint32_t cb[4] = {c4.w, c4.z, c4.y, c4.x};   // digits own + 3 .. own
+        const int local = (int)(cb[0] + cb[1] + cb[2] + cb[3]);
+        int hist_total;
+        const int incl = block_scan_1bar(local, sh.warp_buf, hist_total);
         int cum = incl - local;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int bin = kHistBins - 1 - 4 * tid - j;
-            const int c = (int)sh.hist[bin];
-            sh.bbase[bin] = cum;
+            const int bin = own + 3 - j;
+            const int c = (int)cb[j];
             if (c > 0 && cum < remaining && remaining <= cum + c) {
                 sh.found_digit = bin;
                 sh.found_above = cum;
+                sh.found_cls = c;
             }
+            if (pbits == 0 && c > 0 && cum == 0) sh.top_digit = bin;   // the first non-empty digit
             cum += c;
         }
         __syncthreads();
         const int digit = sh.found_digit;
-        if (digit < 0 || (pbits == 0 && use_hist_in && sh.hist_total != n)) {
+        if (digit < 0 || (pbits == 0 && use_hist_in && hist_total != n)) {
             // the histogram handed in does not describe these scores (a count
             // that is not n means it was not cleared or not filled): rebuild it
             if (pbits == 0 && use_hist_in) {
@@ -306,48 +331,70 @@ select_kernel(const float* scores, int n, int mode, int k, float thresh, int cla
             if (tid == 0) count[b] = 0;   // unreachable for consistent inputs
             return;
         }
-        const int cls = (int)sh.hist[digit];
+        const int cls = sh.found_cls;
         remaining -= sh.found_above;
         prefix |= ((unsigned long long)digit) << shift;
         pbits += D;
-        __syncthreads();
         if (cls <= kCandCap || pbits >= 64) break;
+        __syncthreads();
     }
 
-    if (pbits == kDigit && mode == SRH_SELECT_TOPK) {
-        // ---- first digit decided: try placing by buckets (no sort)
-        const int digit = (int)(prefix >> (64 - kDigit));
+    if (pbits == kDigit) {
+        // ---- the first digit decides the class: place by fine buckets (no sort).
+        // Keys at or above the cut-off digit span digits cut .. top, i.e. key32
+        // in [cut << 20, (top + 1) << 20); a shift of fs = 8 + ceil(log2(top -
+        // cut + 1)) maps that range onto 4096 ordered buckets.
+        const uint32_t cut = (uint32_t)(prefix >> (64 - kDigit));
+        const int nb = max(sh.top_digit - (int)cut + 1, 1);
+        const int fs = 8 + (nb > 1 ? 32 - __clz(nb - 1) : 0);
+        auto fine = [&](unsigned long long c) -> int {
+            const uint32_t f = ((uint32_t)(c >> 32) - (cut << 20)) >> fs;
+            return (int)min(f, (uint32_t)(kHistBins - 1));   // in range for consistent inputs
+        };
+        each_key([&](unsigned long long c) {
+            if ((uint32_t)(c >> 52) >= cut) atomicAdd(&sh.fcnt[fine(c)], 1u);
+        });
+        __syncthreads();
+        const uint4 f4 = *reinterpret_cast<const uint4*>(sh.fcnt + own);
+        const uint32_t fb[4] = {f4.w, f4.z, f4.y, f4.x};   // buckets own + 3 .. own
         unsigned long long sq = 0ull;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int bin = kHistBins - 1 - 4 * tid - j;
-            if (bin >= digit) sq += (unsigned long long)sh.hist[bin] * sh.hist[bin];
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-        if ((tid & 31) == 0 && sq) atomicAdd(&sh.sq, sq);
+        for (int j = 0; j < 4; ++j) sq += (unsigned long long)fb[j] * fb[j];
+        const unsigned wsq = __reduce_add_sync(0xffffffffu, (unsigned)min(sq, (unsigned long long)(1u << 26)));
+        if ((tid & 31) == 0 && wsq) atomicAdd(&sh.sq, min(wsq, 1u << 26));   // at most 2^31 in all
+        const int flocal = (int)(fb[0] + fb[1] + fb[2] + fb[3]);
+        int total;
+        const int fincl = block_scan_1bar(flocal, sh.warp_buf, total);
+        int fc = fincl - flocal;
+        int4 st;
+        st.w = fc;
+        fc += (int)fb[0];
+        st.z = fc;
+        fc += (int)fb[1];
+        st.y = fc;
+        fc += (int)fb[2];
+        st.x = fc;
+        *reinterpret_cast<int4*>(sh.fpos + own) = st;
         __syncthreads();
-        const int total = (K - remaining) + (int)sh.hist[digit];
-        if (sh.sq <= (unsigned long long)kBucketWork && total <= kArr) {
+        if (sh.sq <= kBucketWork && total <= kArr) {
             unsigned long long* arr = cand;               // cand and outk: kArr entries
             each_key([&](unsigned long long c) {
-                const int bin = (int)(c >> (64 - kDigit));
-                if (bin >= digit) {
-                    const int slot = atomicAdd(&sh.bbase[bin], 1);
+                if ((uint32_t)(c >> 52) >= cut) {
+                    const int slot = atomicAdd(&sh.fpos[fine(c)], 1);
                     if (slot < kArr) arr[slot] = c;
                 }
             });
             __syncthreads();
-            // bucket of digit d: [bbase[d] - hist[d], bbase[d]); keys in higher
-            // buckets are larger, so a key's position is its bucket start plus
-            // the number of larger keys in its bucket
+            // bucket f: [fpos[f] - fcnt[f], fpos[f]); keys in earlier buckets
+            // are larger, so a key's position is its bucket start plus the
+            // number of larger keys in its bucket
             for (int j = tid; j < total; j += kSelThreads) {
                 const unsigned long long c = arr[j];
-                const int bin = (int)(c >> (64 - kDigit));
-                const int e = min(sh.bbase[bin], total);
-                const int s0 = max(e - (int)sh.hist[bin], 0);
+                const int f = fine(c);
+                const int e = min(sh.fpos[f], total);
+                const int s0 = max(e - (int)sh.fcnt[f], 0);
+                if (s0 >= K) continue;
                 int rank = 0;
-#pragma unroll 4
                 for (int q = s0; q < e; ++q) rank += arr[q] > c ? 1 : 0;
                 const int pos = s0 + rank;
                 if (pos < K) sel_b[pos] = (int32_t)(~(uint32_t)c);

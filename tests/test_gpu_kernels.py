@@ -174,11 +174,13 @@ def _select_case(name, n, rng):
         return -np.abs(rng.standard_normal(n)).astype(np.float32)
     if name == "coarse":      # 64 distinct values: mid-sized digit buckets full of exact ties
         return (rng.integers(0, 64, n) * 0.125).astype(np.float32)
+    if name == "wide":        # magnitudes from 1e-30 to 1e30: the fine buckets span thousands of digits
+        return (rng.standard_normal(n) * 10.0 ** rng.integers(-30, 31, n)).astype(np.float32)
     raise ValueError(name)
 
 
 @pytest.mark.parametrize("n", [1, 37, 2048, 65536, 262144])
-@pytest.mark.parametrize("case", ["random", "ties", "equal", "one_bin", "neg", "coarse"])
+@pytest.mark.parametrize("case", ["random", "ties", "equal", "one_bin", "neg", "coarse", "wide"])
 def test_fm_select_topk_exact(n, case):
     from sparse_retrieval_host_gb300 import abi
     rng = np.random.default_rng(n + len(case))
