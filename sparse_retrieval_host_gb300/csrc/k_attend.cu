@@ -185,6 +185,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// The fp16 value in the low half of x times 2^-112, exactly: its sign, and its
+// exponent and mantissa bits moved to the fp32 positions (an fp16 subnormal
+// becomes an fp32 subnormal; no flush to zero is in force). Finite inputs only.
+__device__ __forceinline__ float f16_bits_scaled(uint32_t x) {
+    return __uint_as_float(((x & 0x8000u) << 16) | ((x & 0x7fffu) << 13));
+}
+
 __device__ __forceinline__ float f16_to_f32(uint32_t h) {
     float f;
     asm("{\n .reg .f16 t;\n mov.b16 t, %1;\n cvt.f32.f16 %0, t;\n}\n" : "=f"(f) : "h"((unsigned short)h));
@@ -847,19 +854,28 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         //   w_s = l_s 2^(m_s - M) sc_s / sum_s' l_s' 2^(m_s' - M),  M = max m_s over splits with rows
         const float* mls = reinterpret_cast<const float*>(sm + kOffE + kMergeMlOff);
         float* wts = reinterpret_cast<float*>(sm + kOffE + kMergeWOff);
-        if (tid < H) {
+        // eight lanes per head, each taking splits j, j + 8, ...: maximum and
+        // sum over the splits by shuffles within the eight lanes
+        {
+            const int h = tid >> 3, j = tid & 7;
+            const bool hv = h < H;
             float M = -INFINITY;
-            for (int sp = 0; sp < ns; ++sp)
-                if (mls[sp * kMlStride + H + tid] > 0.f) M = fmaxf(M, mls[sp * kMlStride + tid]);
+            for (int sp = j; hv && sp < ns; sp += 8)
+                if (mls[sp * kMlStride + H + h] > 0.f) M = fmaxf(M, mls[sp * kMlStride + h]);
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
             float L = 0.f;
-            for (int sp = 0; sp < ns; ++sp) {
-                const float l = mls[sp * kMlStride + H + tid];
-                const float wl = l > 0.f ? l * ex2_approx(mls[sp * kMlStride + tid] - M) : 0.f;
-                wts[sp * 64 + tid] = wl;
+            for (int sp = j; hv && sp < ns; sp += 8) {
+                const float l = mls[sp * kMlStride + H + h];
+                const float wl = l > 0.f ? l * ex2_approx(mls[sp * kMlStride + h] - M) : 0.f;
+                wts[sp * 64 + h] = wl;
                 L += wl;
             }
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-            for (int sp = 0; sp < ns; ++sp) wts[sp * 64 + tid] *= mls[sp * kMlStride + 2 * H] * inv;
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+            // 2^112 undoes the exponent offset of the fp16 bits read as fp32 below
+            const float inv = L > 0.f ? 0x1p112f / L : 0.f;
+            for (int sp = j; hv && sp < ns; sp += 8) wts[sp * 64 + h] *= mls[sp * kMlStride + 2 * H] * inv;
         }
         __syncthreads();
         // every thread combines its chunks over the splits, in split order; a
@@ -878,8 +894,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                     const uint32_t x[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        acc[2 * e] += w * f16_to_f32(x[e] & 0xffffu);
-                        acc[2 * e + 1] += w * f16_to_f32(x[e] >> 16);
+                        acc[2 * e] = fmaf(w, f16_bits_scaled(x[e]), acc[2 * e]);
+                        acc[2 * e + 1] = fmaf(w, f16_bits_scaled(x[e] >> 16), acc[2 * e + 1]);
                     }
                 }
             }
