@@ -399,6 +399,18 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         // the dependency wait: every earlier call's arrivals are in). The pair is
         // complete when it reaches the next multiple of its split count.
         unsigned long long seen = 0;
+        const int32_t* ph = a.phys + lb * a.S;
+        // Sources of this warp's rows w + 16 i (lane i < 8) of the tile at tr0:
+        // -1 - row for a window row, else the row's phys entry (window + slot).
+        // Bounded by the plan's rows, not by the count: the first tile's entries
+        // are loaded together with the count (an entry past the count is never
+        // used: every row load, store and slot check is bounded by row1).
+        auto fetch_src = [&](int tr0) -> int {
+            const int row = tr0 + warp + kWarps * (lane & 7);
+            if (lane >= kRowsPerWarp || row >= sg.r1) return -1;
+            return row < kWindow ? -1 - row : ph[row - kWindow];
+        };
+        int src0 = INT_MIN;           // the first tile's sources, when taken beside the count
         auto seg_after_wait = [&]() {
             seg_rows(sg, row0, row1);
             n_tiles = row1 > row0 ? (row1 - row0 + kTileRows - 1) / kTileRows : 0;
@@ -406,9 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         };
         if (!early) {
             dep_wait();
+            src0 = fetch_src(row0);   // issued before the count is used (no loads for window rows)
             seg_after_wait();
         }
-        const int32_t* ph = a.phys + lb * a.S;
         if (si > sb && n_tiles > 0 && sg.lb != q_lb) {
             // the previous segment drained its MMAs before its epilogue: Q and E are
             // free; a copy that an earlier segment without rows left unused lands first
@@ -428,13 +440,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         ramax = 0.f;
         rbits = 0u;
 
-        // Sources of this warp's rows w + 16 i (lane i < 8) of the tile at tr0:
-        // -1 - row for a window row, else the row's phys entry (window + slot).
-        auto fetch_src = [&](int tr0) -> int {
-            const int row = tr0 + warp + kWarps * (lane & 7);
-            if (lane >= kRowsPerWarp || row >= row1) return -1;
-            return row < kWindow ? -1 - row : ph[row - kWindow];
-        };
         auto staged_ptr = [&](int src) -> const uint16_t* {
             int slot = src - kWindow;
             if (slot < 0 || slot >= a.G) {
@@ -511,7 +516,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             const int par = tile & 1;
             if (tile + 1 < n_tiles) prefetch_tile(lb, tr0 + kTileRows, row1);
             // ------------------------------------------------------------ E (all warps)
-            const int src = fetch_src(tr0);          // this tile's row sources (lanes 0-7)
+            int src;                                  // this tile's row sources (lanes 0-7)
+            if (src0 != INT_MIN) {
+                src = src0;
+                src0 = INT_MIN;
+            } else {
+                src = fetch_src(tr0);
+            }
             const bool mixed = tr0 < kWindow;         // window rows (fp32) in the tile
             float4 v[4][4];
             if (mixed) {
