@@ -441,27 +441,85 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
             lru[g - m + p] = s;
         }
     } else {
-        // replay the list one id at a time (flag: 0 untouched, 1 hit, 2 refilled)
-        for (int q = tid; q < g; q += blockDim.x) flag[q] = 0;
+        // Replay the list in order, visiting only the misses (warp 0). The LRU
+        // pointer skips the slot at queue position q exactly when that slot's
+        // listed position T[q] comes before the current miss (it was hit
+        // already); otherwise it pops it, and a popped slot's later listed
+        // position T[q] becomes a miss too. The next miss is the smaller of the
+        // next initial miss and the earliest pending induced one (kept sorted
+        // in mr[hs..he)). A run of initial misses that all come before the
+        // earliest pending one, at queue positions whose slots are not listed
+        // (T = INT_MAX), pops those positions in order: up to 32 of them are
+        // placed at once; every other miss is taken one at a time. All lanes
+        // hold the same state; lane 0 writes the pending list.
+        for (int q = tid; q < g; q += blockDim.x) flag[q] = hit_time[queue[q]];   // T[q]
+        for (int p = tid; p < m; p += blockDim.x) {
+            assign[p] = init_slot[p];
+            is_miss[p] = 0;
+        }
         __syncthreads();
-        if (tid == 0) {
-            int ptr = 0, nm = 0;
-            for (int p = 0; p < m; ++p) {
-                const int j = init_slot[p];
-                if (j >= 0 && flag[j] != 2) {
-                    flag[j] = 1;
-                    assign[p] = j;
-                    is_miss[p] = 0;
+        if (tid < 32) {
+            const int lane = tid;
+            int i0 = 0, hs = 0, he = 0, nm = 0, ptr = 0;
+            int hmin = INT_MAX;   // earliest pending induced miss
+            for (;;) {
+                // a run of misses i0 + j popping positions ptr + j (j < 32)
+                const int q = ptr + lane;
+                const int pj = i0 + lane < nmiss0 ? tk[i0 + lane] : INT_MAX;
+                const bool ok = q < g && pj < hmin && flag[q] == INT_MAX;
+                const unsigned run = __ballot_sync(0xffffffffu, ok);
+                const int k = run == 0xffffffffu ? 32 : __ffs(~run) - 1;
+                if (k > 0) {
+                    if (lane < k) {
+                        assign[pj] = queue[q];
+                        is_miss[pj] = 1;
+                    }
+                    nm += k;
+                    ptr += k;
+                    i0 += k;
+                    continue;
+                }
+                // one miss: the next initial or pending one
+                const int ni = i0 < nmiss0 ? tk[i0] : INT_MAX;
+                int P;
+                if (ni < hmin) {
+                    P = ni;
+                    ++i0;
+                } else if (hmin != INT_MAX) {
+                    P = hmin;
+                    ++hs;
+                    hmin = hs < he ? mr[hs] : INT_MAX;
                 } else {
-                    while (ptr < g && flag[queue[ptr]] != 0) ++ptr;
-                    const int s = ptr < g ? queue[ptr++] : 0;
-                    flag[s] = 2;
-                    assign[p] = s;
-                    is_miss[p] = 1;
-                    ++nm;
+                    break;
+                }
+                while (ptr < g && flag[ptr] < P) ++ptr;   // hit before P: skipped
+                if (ptr >= g) {   // no slot left: unreachable (at most g misses among g slots)
+                    if (lane == 0) atomicOr(err, kErrBounds);
+                    break;
+                }
+                const int tv = flag[ptr];
+                if (lane == 0) {
+                    assign[P] = queue[ptr];
+                    is_miss[P] = 1;
+                }
+                ++nm;
+                ++ptr;
+                if (tv != INT_MAX) {
+                    // the popped slot's own listed position (> P) misses too
+                    if (lane == 0) {
+                        int j = he;
+                        while (j > hs && mr[j - 1] > tv) {
+                            mr[j] = mr[j - 1];
+                            --j;
+                        }
+                        mr[j] = tv;
+                    }
+                    ++he;
+                    __syncwarp();
+                    hmin = mr[hs];
                 }
             }
-            sh.nmiss = nm;
+            if (lane == 0) sh.nmiss = nm;
         }
         __syncthreads();
         nmiss = sh.nmiss;

@@ -318,6 +318,41 @@ def test_kvswap_stage_matches_list_lru(G_, k, ctx_len):
         ds.close()
 
 
+def test_kvswap_stage_replays_evictions_of_later_listed_chunks():
+    """Lists whose new chunks come first and whose last entries are the chunks
+    in the least recently used slots: each of those slots is popped before its
+    chunk's turn, which then misses too. Step 2 has 60 such evictions pending at
+    once (more than the warp replay holds: the one-thread replay), step 3 has
+    ten (the warp replay); both match the oracle's list LRU, rows included."""
+    G_, k = 128, 128
+    w = _w(context_len=4 * 1024, layer_ratios=(4,), gpu_chunks=G_, index_topk=k, code=57)
+    ds = make_ds(w, max_select=k)
+    try:
+        pool = G.pool(w, 0, 0)
+        fill(ds, w, {(0, 0): pool})
+        st = O.KvSwapLayerState(w.layer_cap(0), G_)
+        st.host_ready[:] = 1
+        lists = [list(range(128)), list(range(200, 260)) + list(range(60)),
+                 list(range(300, 310)) + list(range(60, 70)) + list(range(200, 230))]
+        for t, ids in enumerate(lists):
+            sel = np.zeros((1, ds.S), np.int32)
+            sel[0, :len(ids)] = ids
+            ds.sel.copy_(torch.from_numpy(sel))
+            ds.count.copy_(torch.from_numpy(np.array([len(ids)], np.int32)))
+            ds.stage()
+            torch.cuda.synchronize()
+            r = st.swap_in_selected(ids)
+            phys = ds.phys.cpu().numpy()[0, 0, :len(ids)]
+            assert phys.tolist() == r.phys, t
+            rows = ds.staging.cpu().numpy()[0, 0][phys - 128]
+            assert np.array_equal(rows, pool[ids].astype(np.float16)), t
+        s_ = ds.stats()
+        assert s_["misses"] == st.misses and s_["hits"] == st.hits
+        assert ds.check_error() == 0
+    finally:
+        ds.close()
+
+
 @pytest.mark.parametrize("G_,k,policy", [
     (64, 24, dict(g_min=24, g_max=64, g_init=32, epoch=2, lo_permille=600, hi_permille=850, delta=8)),
     (96, 32, dict(g_min=32, g_max=80, g_init=80, epoch=1, lo_permille=300, hi_permille=500, delta=16)),
