@@ -115,14 +115,49 @@ __device__ __forceinline__ void store_row_h(uint16_t* __restrict__ dst, const fl
     if (__any_sync(0xffffffffu, !(amax <= 65504.f)) && lane == 0) atomicOr(err, kErrRange);
 }
 
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 struct LruShared {
     int warp_buf[32];
     int nmiss;
     int conflict;
+    unsigned version;   // the state's version read before the dependency wait
+    int stale;          // it changed by the time the wait returned: state read again
 };
 
+constexpr int kLruPer = kMaxGpuChunks / kLruThreads;   // LRU entries per thread
+
+// A swapped (layer, sequence)'s state into registers (thread t: entries
+// t + k * kLruThreads of the LRU order and slot contents) and, when it fits,
+// its slot map into shared memory.
+__device__ __forceinline__ void lru_read_state(const AdaptState* as, const int* lru, const int* slot_logical,
+                                               const int* slot_of, int* smap, bool mirror, long long cap, int G,
+                                               int& g0, int& g, int (&lruv)[kLruPer], int (&slv)[kLruPer]) {
+    g0 = as->g;
+    g = as->g_next;
+#pragma unroll
+    for (int k = 0; k < kLruPer; ++k) {
+        const int q = threadIdx.x + k * kLruThreads;
+        lruv[k] = q < G ? lru[q] : 0;
+        slv[k] = q < G ? slot_logical[q] : -1;
+    }
+    if (mirror)
+        for (long long c = threadIdx.x; c < cap; c += blockDim.x) smap[c] = slot_of[c];
+}
+__device__ __forceinline__ void lru_keep_contents(int* sls, const int (&slv)[kLruPer], int G) {
+#pragma unroll
+    for (int k = 0; k < kLruPer; ++k) {
+        const int q = threadIdx.x + k * kLruThreads;
+        if (q < G) sls[q] = slv[k];
+    }
+}
+
 __global__ void __launch_bounds__(kLruThreads)
-lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int src_ratio, int dedup_tbl,
+lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int src_ratio, int dedup_tbl, int mirror_tbl,
            const int32_t* sel, const int32_t* count,
            int32_t* __restrict__ phys, int32_t* __restrict__ count_l, int2* __restrict__ miss,
            int* __restrict__ miss_count, unsigned long long* __restrict__ stats,
@@ -141,9 +176,9 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
     int* nh = hit_time + G;      // [G]
     int* victim = nh + G;        // [G]
     int* flag = victim + G;      // [G]
-    int* ready = flag + G;       // [S] host_ready of each listed chunk
-    int* sls = ready + S;        // [G] chunk held by each slot before this step
+    int* sls = flag + G;         // [G] chunk held by each slot before this step
     int* first = sls + G;        // [dedup_tbl]: first list position of each mapped chunk
+    int* smap = first + dedup_tbl;   // [mirror_tbl]: the slot map, when it fits
 
     const int tid = threadIdx.x;
     const int l = l0 + blockIdx.x / B;
@@ -155,26 +190,30 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
     int* lru = ld.swap ? ld.lru_order + (size_t)b * G : nullptr;   // swap layers only
     AdaptState* as = ld.swap ? ld.adapt + b : nullptr;
     pdl_trigger();                     // the gather kernel may launch (it waits for this one)
-    // While the earlier kernels finish: shared state that needs no input, and
-    // L2 prefetches of this layer's tables (a prefetch reads nothing into the
-    // kernel, so it is safe whoever writes the tables; the loads after the wait
-    // then find them in L2). slot_of is prefetched only when it is small.
+    // The layer's own state (capacity, LRU order, slot contents and, when it
+    // fits in shared memory, the whole slot map) is written only by resolve
+    // kernels of this (layer, sequence). It is read before the dependency wait,
+    // while the earlier kernels finish, after a read of the state's version;
+    // every resolve raises the version (release) after its last write. A
+    // resolve still running at the first read (one chained right before this
+    // one) has raised it by the time the wait returns, and the state is then
+    // read again. host_ready is read only after the wait (for misses).
     for (int q = tid; q < G; q += blockDim.x) hit_time[q] = INT_MAX;
-    if (ld.swap && tid < 4) {
+    const bool mirror = ld.swap && cap <= mirror_tbl;
+    int* slot_of = ld.swap ? ld.slot_of + (size_t)b * cap : nullptr;
+    int* slot_logical = ld.swap ? ld.slot_logical + (size_t)b * G : nullptr;
+    if (ld.swap && tid == 0) sh.version = ld_acquire_u32(&as->version);
+    if (ld.swap && tid < 2 && cap <= kPrefetchCap) {
+        // L2 prefetches of the tables read after the wait: the host_ready bits
+        // (for misses) and a slot map not copied into shared memory
         const void* base = nullptr;
         long long bytes = 0;
         if (tid == 0) {
-            base = lru;
-            bytes = 4LL * G;
-        } else if (tid == 1) {
-            base = ld.slot_logical + (size_t)b * G;
-            bytes = 4LL * G;
-        } else if (tid == 2 && cap <= kPrefetchCap) {
-            base = ld.slot_of + (size_t)b * cap;
-            bytes = 4LL * cap;
-        } else if (tid == 3 && cap <= kPrefetchCap) {
             base = ld.host_ready + (size_t)b * cap;
             bytes = cap;
+        } else if (!mirror) {
+            base = slot_of;
+            bytes = 4LL * cap;
         }
         // whole 16-byte units inside the range, from its first 16-byte boundary
         const uintptr_t a0 = ((uintptr_t)base + 15) & ~(uintptr_t)15;
@@ -184,40 +223,28 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
             asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(a), "r"(len) : "memory");
         }
     }
-    __syncthreads();
-    pdl_wait();                        // the selection comes from earlier kernels
+    __syncthreads();   // orders the version's acquire before every thread's state reads
 
-    // One round of independent loads: the count, the whole selection row
-    // (entries past the count are ignored) and, for a swapped layer, its
-    // capacity state, LRU order and slot contents. Thread t holds entries t + k * 1024.
-    constexpr int kPer = kMaxGpuChunks / kLruThreads;
+    // Thread t holds entries t + k * 1024 of the selection row, the LRU order
+    // and the slot contents.
+    constexpr int kPer = kLruPer;
     static_assert(kMaxSelect <= kMaxGpuChunks, "selection entries per thread");
     int selv[kPer], lruv[kPer], slv[kPer];
+    int g0 = G, g = G;
+    if (ld.swap) lru_read_state(as, lru, slot_logical, slot_of, smap, mirror, cap, G, g0, g, lruv, slv);
+    pdl_wait();                        // the selection comes from earlier kernels
+
+    // one round of loads: the count and the whole selection row (entries past
+    // the count are ignored), and the state's version again
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
         const int p = tid + k * kLruThreads;
         selv[k] = p < S ? sel_b[p] : 0;
     }
-    int g0 = G, g = G;
-    if (ld.swap) {
-        g0 = as->g;
-        g = as->g_next;
-        const int* slg = ld.slot_logical + (size_t)b * G;
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int q = tid + k * kLruThreads;
-            lruv[k] = q < G ? lru[q] : 0;
-            slv[k] = q < G ? slg[q] : -1;
-        }
-    }
     int m0 = count[b];
     if (ld.swap) {
-        // visible to every thread after the barrier of step 1
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int q = tid + k * kLruThreads;
-            if (q < G) sls[q] = slv[k];
-        }
+        if (tid == 0) sh.stale = ld_acquire_u32(&as->version) != sh.version;
+        lru_keep_contents(sls, slv, G);   // visible to every thread after the barrier of step 1
     }
 
     // ---- 1. the layer's ordered chunk list: c -> floor(c * src_ratio / ratio), first kept
@@ -275,6 +302,14 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
         __syncthreads();
     }
 
+    if (ld.swap && sh.stale) {
+        // a resolve of this state ran past the first read: read it again
+        __syncthreads();
+        lru_read_state(as, lru, slot_logical, slot_of, smap, mirror, cap, G, g0, g, lruv, slv);
+        lru_keep_contents(sls, slv, G);
+        __syncthreads();
+    }
+
     int32_t* phys_lb = phys + lb * S;
     if (!ld.swap) {
         // swap disabled: every chunk is resident at its own row
@@ -291,9 +326,6 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
         return;
     }
 
-    int* slot_of = ld.slot_of + (size_t)b * cap;
-    int* slot_logical = ld.slot_logical + (size_t)b * G;
-
     // ---- 2a. slots in use: the last step's range g0, resized to g when the
     // hit-rate policy (or the host) asked for it. No staged row moves.
     if (g0 < 1 || g0 > G || g < 1 || g > G) {
@@ -307,7 +339,10 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
         for (int q = tid; q < add; q += blockDim.x) {
             const int s = g0 + q;
             const int c = sls[s];
-            if (c >= 0 && c < cap && slot_of[c] == s) slot_of[c] = -1;
+            if (c >= 0 && c < cap && (mirror ? smap[c] : slot_of[c]) == s) {
+                slot_of[c] = -1;
+                if (mirror) smap[c] = -1;
+            }
             slot_logical[s] = -1;
             sls[s] = -1;
             queue[q] = s;
@@ -348,7 +383,10 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
                 queue[nh[q]] = s;
             } else {
                 const int c = sls[s];
-                if (c >= 0 && c < cap && slot_of[c] == s) slot_of[c] = -1;
+                if (c >= 0 && c < cap && (mirror ? smap[c] : slot_of[c]) == s) {
+                    slot_of[c] = -1;
+                    if (mirror) smap[c] = -1;
+                }
                 slot_logical[s] = -1;
             }
         }
@@ -374,8 +412,7 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
     // ---- 2b. resident lookups (hit_time was set to INT_MAX before the wait)
     for (int p = tid; p < m; p += blockDim.x) {
         const int c = r[p];
-        int s = slot_of[c];
-        ready[p] = ld.host_ready[(size_t)b * cap + c];   // read with the slot, used for misses
+        int s = mirror ? smap[c] : slot_of[c];
         if (s >= g) {
             atomicOr(err, kErrBounds);
             s = -1;
@@ -435,7 +472,7 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
                 slot_of[c] = s;
                 slot_logical[s] = c;
                 miss_lb[i] = make_int2(c, s);
-                if (!ready[p]) atomicOr(err, kErrNotStored);
+                if (!ld.host_ready[(size_t)b * cap + c]) atomicOr(err, kErrNotStored);
             }
             phys_lb[p] = kWindow + s;
             lru[g - m + p] = s;
@@ -554,10 +591,11 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
                 slot_of[c] = s;
                 slot_logical[s] = c;
                 miss_lb[mr[p]] = make_int2(c, s);
-                if (!ready[p]) atomicOr(err, kErrNotStored);
+                if (!ld.host_ready[(size_t)b * cap + c]) atomicOr(err, kErrNotStored);
             }
         }
     }
+    __syncthreads();   // every thread's state writes precede the version's release below
     if (tid == 0) {
         count_l[lb] = m;
         miss_count[lb] = nmiss;
@@ -586,6 +624,7 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
         } else {
             as->g_next = g;
         }
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;\n" ::"l"(&as->version) : "memory");
     }
 }
 
@@ -685,11 +724,11 @@ cudaError_t set_lru_attrs() {
 }
 
 size_t lru_smem_bytes(int S, int G) {
-    return sizeof(LruShared) + sizeof(int) * (7 * (size_t)S + 7 * (size_t)G);
+    return sizeof(LruShared) + sizeof(int) * (6 * (size_t)S + 7 * (size_t)G);
 }
 
 cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int S, int src_ratio,
-                       long long max_dedup_cap, const int32_t* sel, const int32_t* count,
+                       long long max_dedup_cap, long long max_mirror_cap, const int32_t* sel, const int32_t* count,
                        int32_t* phys, int32_t* count_l, int2* miss, int* miss_count,
                        unsigned long long* stats, uint32_t* err, AdaptParams ap, cudaStream_t st,
                        bool chained) {
@@ -699,9 +738,17 @@ cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int
     if (max_dedup_cap > 0 &&
         lru_smem_bytes(S, G) + sizeof(int) * (size_t)max_dedup_cap <= 227 * 1024)
         tbl = (int)max_dedup_cap;
-    const size_t smem = lru_smem_bytes(S, G) + sizeof(int) * (size_t)tbl;   // <= 227 KB (set_lru_attrs)
+    // a shared-memory copy of the slot map for swapped layers of at most
+    // kLruMirrorMax chunks, when it fits beside the rest and the launch is
+    // chained (the copy then overlaps the earlier kernels; unchained it would
+    // only add its reads ahead of the lookups)
+    int mir = 0;
+    if (chained && max_mirror_cap > 0 && max_mirror_cap <= kLruMirrorMax &&
+        lru_smem_bytes(S, G) + sizeof(int) * ((size_t)tbl + (size_t)max_mirror_cap) <= 227 * 1024)
+        mir = (int)max_mirror_cap;
+    const size_t smem = lru_smem_bytes(S, G) + sizeof(int) * ((size_t)tbl + (size_t)mir);   // <= 227 KB
     return launch_k(lru_kernel, dim3(nl * B), dim3(kLruThreads), smem, st, chained, layers, l0, B, G, S, src_ratio,
-                    tbl, sel, count, phys, count_l, miss, miss_count, stats, err, ap);
+                    tbl, mir, sel, count, phys, count_l, miss, miss_count, stats, err, ap);
 }
 
 cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, int S,

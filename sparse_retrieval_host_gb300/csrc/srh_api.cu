@@ -819,10 +819,12 @@ int kvswap_stage(srh_ctx* ctx, int layer, const int32_t* d_sel, const int32_t* d
         for (uint8_t v : ctx->ready_host[l]) ready += v;
         ctx->resident_fill_bytes += ready * kKvDim * sizeof(float);
     }
-    long long dedup_cap = 0;
-    for (int l = l0; l < l0 + nl; ++l)
+    long long dedup_cap = 0, mirror_cap = 0;
+    for (int l = l0; l < l0 + nl; ++l) {
         if (ctx->ratios[l] != ctx->cfg.src_ratio) dedup_cap = std::max(dedup_cap, ctx->caps[l]);
-    cudaError_t e = launch_lru(ctx->d_layers, l0, nl, ctx->B, ctx->G, ctx->S, ctx->cfg.src_ratio, dedup_cap,
+        if (ctx->swap[l] && ctx->caps[l] <= kLruMirrorMax) mirror_cap = std::max(mirror_cap, ctx->caps[l]);
+    }
+    cudaError_t e = launch_lru(ctx->d_layers, l0, nl, ctx->B, ctx->G, ctx->S, ctx->cfg.src_ratio, dedup_cap, mirror_cap,
                                d_sel, d_count, d_phys, d_count_l, ctx->d_miss, ctx->d_miss_count, ctx->d_stats,
                                ctx->d_err, ctx->adapt, sm, ctx->chained);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "kvswap_stage LRU launch");

@@ -90,7 +90,7 @@ struct AdaptState {
     int g;               // slots used by the last resolve
     int g_next;          // slots the next resolve uses (policy decision or host setting)
     int ep_steps;        // swap steps in the current hit-rate window
-    int pad;
+    unsigned version;    // resolves of this (layer, sequence) so far (raised by each, with release)
     long long ep_hits;   // hits in the window
     long long ep_sel;    // chunks resolved in the window
 };
@@ -292,8 +292,11 @@ cudaError_t launch_select(const float* scores, int n, int B, int mode, int k, fl
                           int clamp, int S, uint32_t* hist, int32_t* sel, int32_t* count,
                           cudaStream_t st, const unsigned long long* cand = nullptr,
                           int* cand_cnt = nullptr, int cand_cap = 0, bool chained = false);
+// Swapped layers of at most this many chunks keep a shared-memory copy of their
+// slot map in the resolve kernel (read before its dependency wait).
+constexpr long long kLruMirrorMax = 1 << 13;
 cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int S, int src_ratio,
-                       long long max_dedup_cap, const int32_t* sel, const int32_t* count,
+                       long long max_dedup_cap, long long max_mirror_cap, const int32_t* sel, const int32_t* count,
                        int32_t* phys, int32_t* count_l, int2* miss, int* miss_count,
                        unsigned long long* stats, uint32_t* err, AdaptParams ap, cudaStream_t st,
                        bool chained);

@@ -353,6 +353,58 @@ def test_kvswap_stage_replays_evictions_of_later_listed_chunks():
         ds.close()
 
 
+def test_kvswap_stage_chained_back_to_back_matches_list_lru():
+    """Two kvswap_stage calls chained back to back on one stream (each with its
+    own selection and outputs, written before the first is issued): the second
+    resolve may start while the first still runs, and reads the LRU state again
+    if it changed after its early read. Both calls' phys match the oracle's list
+    LRU, applied in order, over eight rounds with in-step evictions."""
+    from sparse_retrieval_host_gb300 import abi
+    G_, k = 64, 48
+    w = _w(context_len=4 * 600, layer_ratios=(4, 4, 8), gpu_chunks=G_, index_topk=k, batch=2, code=58)
+    ds = make_ds(w, max_select=k)
+    try:
+        fill(ds, w)
+        states = [[O.KvSwapLayerState(w.layer_cap(l), G_) for b in range(w.batch)] for l in range(w.n_layers)]
+        for row in states:
+            for st in row:
+                st.host_ready[:] = 1
+        rng = np.random.default_rng(58)
+        traces = [_trace(rng, 16, w.n_chunks, k, G_) for _ in range(w.batch)]
+        sels = [torch.zeros_like(ds.sel) for _ in range(2)]
+        cnts = [torch.zeros_like(ds.count) for _ in range(2)]
+        phys = [torch.zeros_like(ds.phys) for _ in range(2)]
+        cls = [torch.zeros_like(ds.count_l) for _ in range(2)]
+        for r in range(8):
+            for i in range(2):
+                sel = np.zeros(tuple(ds.sel.shape), np.int32)
+                cnt = np.zeros(w.batch, np.int32)
+                for b in range(w.batch):
+                    ids = traces[b][2 * r + i]
+                    sel[b, :len(ids)] = ids
+                    cnt[b] = len(ids)
+                sels[i].copy_(torch.from_numpy(sel))
+                cnts[i].copy_(torch.from_numpy(cnt))
+            torch.cuda.synchronize()
+            abi.srh_set_chained(ds.ctx, True)
+            try:
+                for i in range(2):
+                    abi.kvswap_stage(ds.ctx, -1, sels[i], cnts[i], ds.staging, phys[i], cls[i])
+            finally:
+                abi.srh_set_chained(ds.ctx, False)
+            torch.cuda.synchronize()
+            for i in range(2):
+                ph = phys[i].cpu().numpy()
+                for l in range(w.n_layers):
+                    for b in range(w.batch):
+                        lst = O.layer_chunks(traces[b][2 * r + i], 4, w.layer_ratios[l])
+                        res = states[l][b].swap_in_selected(lst)
+                        assert ph[l, b, :len(lst)].tolist() == res.phys, (r, i, l, b)
+        assert ds.check_error() == 0
+    finally:
+        ds.close()
+
+
 @pytest.mark.parametrize("G_,k,policy", [
     (64, 24, dict(g_min=24, g_max=64, g_init=32, epoch=2, lo_permille=600, hi_permille=850, delta=8)),
     (96, 32, dict(g_min=32, g_max=80, g_init=80, epoch=1, lo_permille=300, hi_permille=500, delta=16)),
