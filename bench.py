@@ -223,9 +223,11 @@ def scoring_kernel(w) -> str:
 def launches_per_step(w, sm_count):
     """Our kernels per step: score, select, resolve, gather and attend (the
     attention kernel merges split pairs itself), plus fm_select's candidate
-    pass when the workload scores more than COLLECT_MIN_N chunks."""
+    pass when the workload scores more than COLLECT_MIN_N chunks; the gather
+    runs only when some layer swaps (its capacity exceeds GPU_CHUNKS)."""
     collect = 1 if w.n_chunks > COLLECT_MIN_N else 0
-    return BASE_KERNELS + collect
+    swapped = any(-(-w.context_len // r) > w.gpu_chunks for r in w.layer_ratios)
+    return BASE_KERNELS + collect - (0 if swapped else 1)
 
 
 def adaptive_policy(w):

@@ -632,14 +632,15 @@ constexpr int kGatherWarps = 8;
 
 
 __global__ void __launch_bounds__(kGatherWarps * 32)
-gather_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S,
+gather_kernel(const LayerDev* __restrict__ layers, const int* __restrict__ swap_layers, int B, int G, int S,
               const int2* miss, const int* miss_count,
               uint16_t* __restrict__ staging, uint32_t* __restrict__ err) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
+    // blockIdx.y: (swapped layer, sequence); the list is written once, at creation
+    const int l = swap_layers[blockIdx.y / B], b = (int)(blockIdx.y % B);
+    const size_t lb = (size_t)l * B + b;
     pdl_wait();                        // the miss lists come from the resolve kernel
-    const size_t lb = (size_t)l0 * B + blockIdx.y;
-    const int l = (int)(lb / B), b = (int)(lb % B);
     const int nm = miss_count[lb];
     const LayerDev ld = layers[l];
     const int2* ml = miss + lb * S;
@@ -751,14 +752,17 @@ cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int
                     tbl, mir, sel, count, phys, count_l, miss, miss_count, stats, err, ap);
 }
 
-cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, int S,
+cudaError_t launch_gather(const LayerDev* layers, const int* swap_layers, int n_sw, int nl_call, int B, int G, int S,
                           const int2* miss, const int* miss_count, uint16_t* staging, uint32_t* err,
                           int sm_count, cudaStream_t st, bool chained) {
-    int bx = (4 * sm_count + nl * B - 1) / (nl * B);
+    if (n_sw <= 0) return cudaSuccess;
+    // CTAs per (layer, sequence) as if every layer of the call swapped: a
+    // lookahead boundary's misses keep that many rows in flight per layer
+    int bx = (4 * sm_count + nl_call * B - 1) / (nl_call * B);
     if (bx < 1) bx = 1;
     if (bx > 64) bx = 64;
-    return launch_k(gather_kernel, dim3(bx, nl * B), dim3(kGatherWarps * 32), 0, st, chained, layers, l0, B, G, S,
-                    miss, miss_count, staging, err);
+    return launch_k(gather_kernel, dim3(bx, n_sw * B), dim3(kGatherWarps * 32), 0, st, chained, layers, swap_layers, B,
+                    G, S, miss, miss_count, staging, err);
 }
 
 cudaError_t launch_touch(const float* p, long long n_floats, uint32_t* sink, int sm_count, cudaStream_t st) {

@@ -113,6 +113,7 @@ void free_ctx(srh_ctx* ctx) {
         cudaFree(ld.adapt);
     }
     cudaFree(ctx->d_layers);
+    cudaFree(ctx->d_swap_layers);
     cudaFree(ctx->d_stats);
     cudaFree(ctx->d_err);
     cudaFree(ctx->d_hist);
@@ -541,6 +542,18 @@ int srh_create(const srh_config* cfg, srh_ctx** out) {
         if (e != cudaSuccess) return bail(SRH_ERR_NOMEM, std::string("device state: ") + cudaGetErrorString(e));
     }
 
+    std::vector<int> swl;
+    ctx->swap_pos.assign(ctx->L, -1);
+    for (int l = 0; l < ctx->L; ++l)
+        if (ctx->swap[l]) {
+            ctx->swap_pos[l] = (int)swl.size();
+            swl.push_back(l);
+        }
+    ctx->n_swap = (int)swl.size();
+    e = cudaMalloc(&ctx->d_swap_layers, sizeof(int) * std::max<size_t>(swl.size(), 1));
+    if (e == cudaSuccess && !swl.empty())
+        e = cudaMemcpy(ctx->d_swap_layers, swl.data(), sizeof(int) * swl.size(), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return bail(SRH_ERR_NOMEM, std::string("device state: ") + cudaGetErrorString(e));
     e = cudaMalloc(&ctx->d_layers, sizeof(LayerDev) * ctx->L);
     if (e == cudaSuccess)
         e = cudaMemcpy(ctx->d_layers, ctx->h_layers.data(), sizeof(LayerDev) * ctx->L, cudaMemcpyHostToDevice);
@@ -828,22 +841,27 @@ int kvswap_stage(srh_ctx* ctx, int layer, const int32_t* d_sel, const int32_t* d
                                d_sel, d_count, d_phys, d_count_l, ctx->d_miss, ctx->d_miss_count, ctx->d_stats,
                                ctx->d_err, ctx->adapt, sm, ctx->chained);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "kvswap_stage LRU launch");
-    // The gather is a wide kernel of its own: a boundary step's misses are rows
-    // of host pages the GPU may not have read recently, so many must be in
-    // flight at once. On the main stream it directly follows the resolve
-    // kernel (chained); with a side stream it runs there, joined by events.
-    if (ss && ss != sm) {
-        SRH_CUDA(ctx, cudaEventRecord(ctx->ev_resolved, sm));
-        SRH_CUDA(ctx, cudaStreamWaitEvent(ss, ctx->ev_resolved, 0));
-    } else {
-        ss = sm;
-    }
-    e = launch_gather(ctx->d_layers, l0, nl, ctx->B, ctx->G, ctx->S, ctx->d_miss, ctx->d_miss_count, d_staging,
-                      ctx->d_err, ctx->sm_count, ss, ss == sm);
-    if (e != cudaSuccess) return cuda_fail(ctx, e, "kvswap_stage gather launch");
-    if (ss != sm) {
-        SRH_CUDA(ctx, cudaEventRecord(ctx->ev_gathered, ss));
-        SRH_CUDA(ctx, cudaStreamWaitEvent(sm, ctx->ev_gathered, 0));
+    // The gather is a wide kernel of its own, over the swapped layers only: a
+    // boundary step's misses are rows of host pages the GPU may not have read
+    // recently, so many must be in flight at once. On the main stream it
+    // directly follows the resolve kernel (chained); with a side stream it
+    // runs there, joined by events. A call with no swapped layer has none.
+    const int sw0 = layer < 0 ? 0 : ctx->swap_pos[layer];
+    const int n_sw = layer < 0 ? ctx->n_swap : (sw0 >= 0 ? 1 : 0);
+    if (n_sw > 0) {
+        if (ss && ss != sm) {
+            SRH_CUDA(ctx, cudaEventRecord(ctx->ev_resolved, sm));
+            SRH_CUDA(ctx, cudaStreamWaitEvent(ss, ctx->ev_resolved, 0));
+        } else {
+            ss = sm;
+        }
+        e = launch_gather(ctx->d_layers, ctx->d_swap_layers + sw0, n_sw, nl, ctx->B, ctx->G, ctx->S, ctx->d_miss,
+                          ctx->d_miss_count, d_staging, ctx->d_err, ctx->sm_count, ss, ss == sm);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "kvswap_stage gather launch");
+        if (ss != sm) {
+            SRH_CUDA(ctx, cudaEventRecord(ctx->ev_gathered, ss));
+            SRH_CUDA(ctx, cudaStreamWaitEvent(sm, ctx->ev_gathered, 0));
+        }
     }
     ++ctx->stage_calls;
     return SRH_OK;

@@ -173,6 +173,9 @@ struct Ctx {
 
     // device state
     LayerDev* d_layers = nullptr;
+    int* d_swap_layers = nullptr;       // the swapped layers' indices, ascending (the gather's rows)
+    std::vector<int> swap_pos;          // each layer's place in that list, -1 if it does not swap
+    int n_swap = 0;
     std::vector<LayerDev> h_layers;
     unsigned long long* d_stats = nullptr;
     uint32_t* d_err = nullptr;
@@ -300,7 +303,9 @@ cudaError_t launch_lru(const LayerDev* layers, int l0, int nl, int B, int G, int
                        int32_t* phys, int32_t* count_l, int2* miss, int* miss_count,
                        unsigned long long* stats, uint32_t* err, AdaptParams ap, cudaStream_t st,
                        bool chained);
-cudaError_t launch_gather(const LayerDev* layers, int l0, int nl, int B, int G, int S,
+// Gathers the misses of the swapped layers swap_layers[0 .. n_sw) (every
+// sequence); nl_call is the call's layer count, which sizes the grid per layer.
+cudaError_t launch_gather(const LayerDev* layers, const int* swap_layers, int n_sw, int nl_call, int B, int G, int S,
                           const int2* miss, const int* miss_count, uint16_t* staging,
                           uint32_t* err, int sm_count, cudaStream_t st, bool chained);
 cudaError_t launch_touch(const float* p, long long n_floats, uint32_t* sink, int sm_count, cudaStream_t st);
