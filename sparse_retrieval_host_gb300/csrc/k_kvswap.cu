@@ -66,6 +66,25 @@ __device__ __forceinline__ int block_scan_incl(int v, int* warp_buf, int* total)
     return v + (warp > 0 ? warp_buf[warp - 1] : 0);
 }
 
+// Exclusive block scan of one int per thread with a single barrier
+// (blockDim.x == kLruThreads, 32 warps): each warp adds up the totals of the
+// warps before it itself. `total` receives the block's sum. warp_buf must not
+// be written again before the caller's next barrier.
+__device__ __forceinline__ int block_scan_excl_1bar(int v, int* warp_buf, int& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += u;
+    }
+    if (lane == 31) warp_buf[warp] = x;
+    __syncthreads();
+    const int w = warp_buf[lane];
+    total = __reduce_add_sync(0xffffffffu, w);
+    return x - v + __reduce_add_sync(0xffffffffu, lane < warp ? w : 0);
+}
+
 // In-place exclusive scan of a[0..len) in shared memory; returns the total.
 // Three barriers; on return every thread sees the whole scanned array.
 __device__ int block_scan_excl_array(int* a, int len, int* warp_buf) {
@@ -428,15 +447,29 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
     // the i-th non-hit slot in LRU order. One scan ranks both: the non-hit slots
     // (high 16 bits) and the misses (low 16 bits); both counts are <= 4096.
     const int nk = max(g, m);
-    for (int i = tid; i < nk; i += blockDim.x)
-        nh[i] = ((i < g && hit_time[queue[i]] == INT_MAX) ? (1 << 16) : 0) | ((i < m && init_slot[i] < 0) ? 1 : 0);
-    __syncthreads();
-    const int both = block_scan_excl_array(nh, nk, sh.warp_buf);
-    const int nmiss0 = both & 0xffff;
-    for (int q = tid; q < g; q += blockDim.x)
-        if (hit_time[queue[q]] == INT_MAX) victim[nh[q] >> 16] = queue[q];
-    for (int p = tid; p < m; p += blockDim.x)
-        if (init_slot[p] < 0) tk[nh[p] & 0xffff] = p;
+    int nmiss0;
+    if (nk <= kLruThreads) {
+        // one entry per thread: one scan with a single barrier, ranks used in place
+        const bool free_q = tid < g && hit_time[queue[tid]] == INT_MAX;
+        const bool miss_p = tid < m && init_slot[tid] < 0;
+        const int v = (free_q ? (1 << 16) : 0) | (miss_p ? 1 : 0);
+        int both;
+        const int ex = block_scan_excl_1bar(v, sh.warp_buf, both);
+        nmiss0 = both & 0xffff;
+        if (tid < nk) nh[tid] = ex;
+        if (free_q) victim[ex >> 16] = queue[tid];
+        if (miss_p) tk[ex & 0xffff] = tid;
+    } else {
+        for (int i = tid; i < nk; i += blockDim.x)
+            nh[i] = ((i < g && hit_time[queue[i]] == INT_MAX) ? (1 << 16) : 0) | ((i < m && init_slot[i] < 0) ? 1 : 0);
+        __syncthreads();
+        const int both = block_scan_excl_array(nh, nk, sh.warp_buf);
+        nmiss0 = both & 0xffff;
+        for (int q = tid; q < g; q += blockDim.x)
+            if (hit_time[queue[q]] == INT_MAX) victim[nh[q] >> 16] = queue[q];
+        for (int p = tid; p < m; p += blockDim.x)
+            if (init_slot[p] < 0) tk[nh[p] & 0xffff] = p;
+    }
     __syncthreads();
     // a hit slot j lying before the kj-th non-hit slot is reached by that pop if
     // the pop happens before j is touched: the sequential list would take j
