@@ -452,6 +452,64 @@ int srh_get_stats(srh_ctx* ctx, srh_stats* out);
 /* Zero the swap counters (waits for the device). */
 int srh_reset_stats(srh_ctx* ctx);
 
+/*
+ * Native host loop (no counterpart on the pages: the serving loop around the
+ * four calls, in native code so that issuing a step costs a few microseconds
+ * of host time). Decode steps fed from host memory and read back into it, with
+ * the copies of neighbouring steps overlapping the step in flight. Two sets of
+ * device step buffers alternate; each set has its own CUDA graph of one decode
+ * step over all layers -- fm_score, then fm_select, kvswap_stage and
+ * lsa_attend chained (srh_set_chained) -- captured at creation on the loop's
+ * compute stream (nothing runs then). Step i copies its indexer and attention
+ * queries from host memory into set i % 2 on a copy-in stream, replays that
+ * set's graph on the compute stream and copies the attention output, the
+ * selection and the count back on a copy-out stream; events order each set's
+ * reuse after its previous step's outputs have left the device. Steps run in
+ * issue order, so the LRU state advances as with srh calls on one stream.
+ *
+ *   d_keys, n, d_scores                      as for fm_score / fm_select
+ *   d_staging, d_phys, d_count_l, d_window   as for kvswap_stage / lsa_attend
+ *   n_heads                                  16, 32 or 64
+ *   scale, bias3[3], ensemble                as for fm_score
+ *   mode, k, tau, clamp                      as for fm_select
+ *   d_fm_q[2]   [B][3][8][128] bf16, d_q[2] [L][B][n_heads][512] bf16 (inputs)
+ *   d_out[2]    [L][B][n_heads][512] fp32, d_sel[2] [B][max_select] int32,
+ *   d_count[2]  [B] int32 (outputs); every set's buffers distinct
+ *   stream      GPU work already issued on it precedes the loop's first step
+ *   out         receives the loop (NULL on failure)
+ * The loop keeps the pointers: the buffers must outlive it. The context's
+ * chaining flag is off when the call returns. Returns SRH_OK, SRH_ERR_INVALID,
+ * SRH_ERR_NOMEM or SRH_ERR_CUDA (details in srh_last_error(ctx)).
+ */
+typedef struct srh_hostloop srh_hostloop;
+int srh_hostloop_create(srh_ctx* ctx, const uint16_t* d_keys, int n, float* d_scores, uint16_t* d_staging,
+                        int32_t* d_phys, int32_t* d_count_l, const float* d_window, int n_heads, float scale,
+                        const float* bias3, int ensemble, int mode, int k, float tau, int clamp,
+                        uint16_t* const d_fm_q[2], uint16_t* const d_q[2], float* const d_out[2],
+                        int32_t* const d_sel[2], int32_t* const d_count[2], srh_stream_t stream,
+                        srh_hostloop** out);
+
+/*
+ * Issues step i (i = 0, 1, 2, ...; consecutive): h_fm_q [B][3][8][128] bf16 and
+ * h_q [L][B][n_heads][512] bf16 are read, h_out / h_sel [B][max_select] /
+ * h_count [B] written -- host memory, page-locked for the copies to be
+ * asynchronous. Asynchronous: the outputs are complete once srh_hostloop_wait
+ * for step i (or srh_hostloop_sync) returns, and the host buffers must not be
+ * reused before then. Returns SRH_OK, SRH_ERR_INVALID or SRH_ERR_CUDA.
+ */
+int srh_hostloop_step(srh_hostloop* lp, long long i, const uint16_t* h_fm_q, const uint16_t* h_q, float* h_out,
+                      int32_t* h_sel, int32_t* h_count);
+
+/* Blocks until step i's outputs are in host memory. Valid for the last two
+ * steps issued (an earlier step's outputs are complete already). */
+int srh_hostloop_wait(srh_hostloop* lp, long long i);
+
+/* Blocks until every step issued so far has finished. */
+int srh_hostloop_sync(srh_hostloop* lp);
+
+/* Waits for the loop's work and frees it (its streams, events and graphs). */
+void srh_hostloop_destroy(srh_hostloop* lp);
+
 /* Wait for the device and report the sticky device error word: SRH_OK,
  * SRH_ERR_NOT_STORED, SRH_ERR_BOUNDS, SRH_ERR_TIMEOUT or SRH_ERR_RANGE (first
  * match in that order), or SRH_ERR_CUDA. The word is cleared after it is read. */

@@ -114,6 +114,13 @@ SIGNATURES = [
     ("srh_reset_stats", _i, [_vp]),
     ("srh_check_error", _i, [_vp]),
     ("srh_selftest_wait_timeout", _i, [_vp, _i, _vp]),
+    ("srh_hostloop_create", _i, [_vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _f, ctypes.POINTER(_f), _i, _i, _i, _f, _i,
+                                 ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                 ctypes.POINTER(_vp), _vp, ctypes.POINTER(_vp)]),
+    ("srh_hostloop_step", _i, [_vp, _ll, _vp, _vp, _vp, _vp, _vp]),
+    ("srh_hostloop_wait", _i, [_vp, _ll]),
+    ("srh_hostloop_sync", _i, [_vp]),
+    ("srh_hostloop_destroy", None, [_vp]),
     ("srh_error_string", ctypes.c_char_p, [_i]),
     ("srh_last_error", ctypes.c_char_p, [_vp]),
 ]
@@ -310,6 +317,38 @@ def srh_get_stats(ctx) -> dict:
 
 def srh_reset_stats(ctx) -> None:
     _check(load().srh_reset_stats(ctx), "srh_reset_stats", ctx)
+
+
+def srh_hostloop_create(ctx, keys, n, scores, staging, phys, count_l, window, n_heads, scale, bias3, ensemble,
+                        mode, k, tau, clamp, fm_q2, q2, out2, sel2, count2, stream=None) -> int:
+    """The native host loop over two sets of step buffers (each argument ending
+    in 2 is a pair of tensors). Returns its handle."""
+    pair = lambda xs: (_vp * 2)(*[_ptr(x) for x in xs])
+    b3 = (_f * 3)(*[float(v) for v in bias3])
+    out = _vp()
+    rc = load().srh_hostloop_create(ctx, _ptr(keys), n, _ptr(scores), _ptr(staging), _ptr(phys), _ptr(count_l),
+                                    _ptr(window), n_heads, float(scale), b3, ensemble, mode, k, float(tau), clamp,
+                                    pair(fm_q2), pair(q2), pair(out2), pair(sel2), pair(count2), _stream(stream),
+                                    ctypes.byref(out))
+    _check(rc, "srh_hostloop_create", ctx)
+    return out.value
+
+
+def srh_hostloop_step(ctx, lp, i, h_fm_q, h_q, h_out, h_sel, h_count) -> None:
+    _check(load().srh_hostloop_step(lp, i, _ptr(h_fm_q), _ptr(h_q), _ptr(h_out), _ptr(h_sel), _ptr(h_count)),
+           "srh_hostloop_step", ctx)
+
+
+def srh_hostloop_wait(ctx, lp, i) -> None:
+    _check(load().srh_hostloop_wait(lp, i), "srh_hostloop_wait", ctx)
+
+
+def srh_hostloop_sync(ctx, lp) -> None:
+    _check(load().srh_hostloop_sync(lp), "srh_hostloop_sync", ctx)
+
+
+def srh_hostloop_destroy(lp) -> None:
+    load().srh_hostloop_destroy(lp)
 
 
 def srh_check_error(ctx) -> int:

@@ -985,6 +985,157 @@ int srh_selftest_wait_timeout(srh_ctx* ctx, int limit_us, srh_stream_t stream) {
     return SRH_OK;
 }
 
+}  // extern "C"
+
+struct srh_hostloop {
+    srh_ctx* ctx = nullptr;
+    cudaStream_t s_in = nullptr, s_comp = nullptr, s_out = nullptr;
+    cudaEvent_t ev_in[2] = {}, ev_done[2] = {}, ev_out[2] = {};
+    cudaGraph_t graph[2] = {};
+    cudaGraphExec_t exec[2] = {};
+    uint16_t* fm_q[2] = {};
+    uint16_t* q[2] = {};
+    float* out[2] = {};
+    int32_t* sel[2] = {};
+    int32_t* count[2] = {};
+    size_t fmq_bytes = 0, q_bytes = 0, out_bytes = 0, sel_bytes = 0, count_bytes = 0;
+};
+
+namespace {
+
+void hostloop_free(srh_hostloop* lp) {
+    if (!lp) return;
+    for (cudaStream_t s : {lp->s_in, lp->s_comp, lp->s_out})
+        if (s) cudaStreamSynchronize(s);
+    for (int k = 0; k < 2; ++k) {
+        if (lp->exec[k]) cudaGraphExecDestroy(lp->exec[k]);
+        if (lp->graph[k]) cudaGraphDestroy(lp->graph[k]);
+        for (cudaEvent_t e : {lp->ev_in[k], lp->ev_done[k], lp->ev_out[k]})
+            if (e) cudaEventDestroy(e);
+    }
+    for (cudaStream_t s : {lp->s_in, lp->s_comp, lp->s_out})
+        if (s) cudaStreamDestroy(s);
+    delete lp;
+}
+
+}  // namespace
+
+extern "C" {
+
+int srh_hostloop_create(srh_ctx* ctx, const uint16_t* d_keys, int n, float* d_scores, uint16_t* d_staging,
+                        int32_t* d_phys, int32_t* d_count_l, const float* d_window, int n_heads, float scale,
+                        const float* bias3, int ensemble, int mode, int k, float tau, int clamp,
+                        uint16_t* const d_fm_q[2], uint16_t* const d_q[2], float* const d_out[2],
+                        int32_t* const d_sel[2], int32_t* const d_count[2], srh_stream_t stream,
+                        srh_hostloop** out) {
+    if (!ctx || !out) return SRH_ERR_INVALID;
+    *out = nullptr;
+    if (!d_keys || !d_scores || !d_staging || !d_phys || !d_count_l || !d_window || !bias3 || !d_fm_q || !d_q ||
+        !d_out || !d_sel || !d_count)
+        return fail(ctx, SRH_ERR_INVALID, "NULL pointer");
+    for (int s = 0; s < 2; ++s)
+        if (!d_fm_q[s] || !d_q[s] || !d_out[s] || !d_sel[s] || !d_count[s])
+            return fail(ctx, SRH_ERR_INVALID, "NULL step buffer");
+    if (n_heads != 16 && n_heads != 32 && n_heads != 64) return fail(ctx, SRH_ERR_INVALID, "n_heads must be 16, 32 or 64");
+    srh_hostloop* lp = new (std::nothrow) srh_hostloop;
+    if (!lp) return fail(ctx, SRH_ERR_NOMEM, "host loop");
+    lp->ctx = ctx;
+    const size_t LB = (size_t)ctx->L * ctx->B;
+    lp->fmq_bytes = (size_t)ctx->B * 3 * 8 * 128 * sizeof(uint16_t);
+    lp->q_bytes = LB * n_heads * kKvDim * sizeof(uint16_t);
+    lp->out_bytes = LB * n_heads * kKvDim * sizeof(float);
+    lp->sel_bytes = (size_t)ctx->B * ctx->S * sizeof(int32_t);
+    lp->count_bytes = (size_t)ctx->B * sizeof(int32_t);
+    for (int s = 0; s < 2; ++s) {
+        lp->fm_q[s] = d_fm_q[s];
+        lp->q[s] = d_q[s];
+        lp->out[s] = d_out[s];
+        lp->sel[s] = d_sel[s];
+        lp->count[s] = d_count[s];
+    }
+    auto bail = [&](int code) {
+        hostloop_free(lp);
+        return code;
+    };
+    cudaError_t e = cudaSuccess;
+    for (cudaStream_t* s : {&lp->s_in, &lp->s_comp, &lp->s_out})
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(s, cudaStreamNonBlocking);
+    for (int s = 0; s < 2 && e == cudaSuccess; ++s)
+        for (cudaEvent_t* ev : {&lp->ev_in[s], &lp->ev_done[s], &lp->ev_out[s]})
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "host loop streams and events"));
+    // the work already on the caller's stream comes first
+    if (e == cudaSuccess) e = cudaEventRecord(lp->ev_in[0], (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(lp->s_comp, lp->ev_in[0], 0);
+    if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "host loop start"));
+    for (int s = 0; s < 2; ++s) {
+        e = cudaStreamBeginCapture(lp->s_comp, cudaStreamCaptureModeThreadLocal);
+        if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "host loop capture"));
+        int rc = fm_score(ctx, d_keys, n, lp->fm_q[s], scale, bias3, ensemble, d_scores, lp->s_comp);
+        if (rc == SRH_OK) {
+            ctx->chained = true;
+            rc = fm_select(ctx, d_scores, n, mode, k, tau, clamp, lp->sel[s], lp->count[s], lp->s_comp);
+            if (rc == SRH_OK)
+                rc = kvswap_stage(ctx, -1, lp->sel[s], lp->count[s], d_staging, d_phys, d_count_l, lp->s_comp,
+                                  nullptr);
+            if (rc == SRH_OK)
+                rc = lsa_attend(ctx, -1, lp->q[s], n_heads, d_window, d_staging, d_phys, d_count_l, lp->out[s],
+                                lp->s_comp);
+            ctx->chained = false;
+        }
+        cudaGraph_t g = nullptr;
+        const cudaError_t ec = cudaStreamEndCapture(lp->s_comp, &g);
+        if (rc != SRH_OK) {
+            if (g) cudaGraphDestroy(g);
+            return bail(rc);
+        }
+        if (ec != cudaSuccess) return bail(cuda_fail(ctx, ec, "host loop capture"));
+        lp->graph[s] = g;
+        e = cudaGraphInstantiate(&lp->exec[s], g, 0);
+        if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "host loop graph instantiate"));
+    }
+    *out = lp;
+    return SRH_OK;
+}
+
+int srh_hostloop_step(srh_hostloop* lp, long long i, const uint16_t* h_fm_q, const uint16_t* h_q, float* h_out,
+                      int32_t* h_sel, int32_t* h_count) {
+    if (!lp) return SRH_ERR_INVALID;
+    srh_ctx* ctx = lp->ctx;
+    if (i < 0 || !h_fm_q || !h_q || !h_out || !h_sel || !h_count) return fail(ctx, SRH_ERR_INVALID, "host loop step arguments");
+    const int s = (int)(i & 1);
+    // set s was last read by step i - 2: its inputs are refilled after that step finished
+    SRH_CUDA(ctx, cudaStreamWaitEvent(lp->s_in, lp->ev_done[s], 0));
+    SRH_CUDA(ctx, cudaMemcpyAsync(lp->fm_q[s], h_fm_q, lp->fmq_bytes, cudaMemcpyHostToDevice, lp->s_in));
+    SRH_CUDA(ctx, cudaMemcpyAsync(lp->q[s], h_q, lp->q_bytes, cudaMemcpyHostToDevice, lp->s_in));
+    SRH_CUDA(ctx, cudaEventRecord(lp->ev_in[s], lp->s_in));
+    // and its outputs are overwritten after step i - 2's outputs left the device
+    SRH_CUDA(ctx, cudaStreamWaitEvent(lp->s_comp, lp->ev_in[s], 0));
+    SRH_CUDA(ctx, cudaStreamWaitEvent(lp->s_comp, lp->ev_out[s], 0));
+    SRH_CUDA(ctx, cudaGraphLaunch(lp->exec[s], lp->s_comp));
+    SRH_CUDA(ctx, cudaEventRecord(lp->ev_done[s], lp->s_comp));
+    SRH_CUDA(ctx, cudaStreamWaitEvent(lp->s_out, lp->ev_done[s], 0));
+    SRH_CUDA(ctx, cudaMemcpyAsync(h_out, lp->out[s], lp->out_bytes, cudaMemcpyDeviceToHost, lp->s_out));
+    SRH_CUDA(ctx, cudaMemcpyAsync(h_sel, lp->sel[s], lp->sel_bytes, cudaMemcpyDeviceToHost, lp->s_out));
+    SRH_CUDA(ctx, cudaMemcpyAsync(h_count, lp->count[s], lp->count_bytes, cudaMemcpyDeviceToHost, lp->s_out));
+    SRH_CUDA(ctx, cudaEventRecord(lp->ev_out[s], lp->s_out));
+    return SRH_OK;
+}
+
+int srh_hostloop_wait(srh_hostloop* lp, long long i) {
+    if (!lp || i < 0) return SRH_ERR_INVALID;
+    SRH_CUDA(lp->ctx, cudaEventSynchronize(lp->ev_out[i & 1]));
+    return SRH_OK;
+}
+
+int srh_hostloop_sync(srh_hostloop* lp) {
+    if (!lp) return SRH_ERR_INVALID;
+    for (cudaStream_t s : {lp->s_in, lp->s_comp, lp->s_out}) SRH_CUDA(lp->ctx, cudaStreamSynchronize(s));
+    return SRH_OK;
+}
+
+void srh_hostloop_destroy(srh_hostloop* lp) { hostloop_free(lp); }
+
 int srh_check_error(srh_ctx* ctx) {
     if (!ctx) return SRH_ERR_INVALID;
     SRH_CUDA(ctx, cudaDeviceSynchronize());

@@ -352,6 +352,50 @@ class HostLoop:
             s.synchronize()
 
 
+class NativeHostLoop:
+    """The same pipelined loop as HostLoop, issued by the library in native code
+    (srh_hostloop_*): two sets of device step buffers, each with a CUDA graph
+    of one step captured by the library, copy-in and copy-out streams ordered by
+    events. One call per step from Python. Single key set, bf16 keys."""
+
+    def __init__(self, ds: "DecodeStep", spec: StepSpec):
+        if ds.key_format != "bf16" or ds.key_sets != 1:
+            raise ValueError("the native host loop scores one bf16 key set")
+        self.ds = ds
+        self.fm_q = [torch.zeros_like(ds.fm_q) for _ in range(2)]
+        self.q = [torch.zeros_like(ds.q) for _ in range(2)]
+        self.out = [torch.zeros_like(ds.out) for _ in range(2)]
+        self.sel = [torch.zeros_like(ds.sel) for _ in range(2)]
+        self.count = [torch.zeros_like(ds.count) for _ in range(2)]
+        self.lp = abi.srh_hostloop_create(ds.ctx, ds.keys, ds.n, ds.scores, ds.staging, ds.phys, ds.count_l,
+                                          ds.window, ds.H, spec.scale, spec.bias, spec.ensemble, spec.select_mode,
+                                          spec.k, spec.tau, spec.clamp, self.fm_q, self.q, self.out, self.sel,
+                                          self.count, torch.cuda.current_stream(ds.keys.device))
+
+    def step(self, i: int, h_fm_q: torch.Tensor, h_q: torch.Tensor, h_out: torch.Tensor, h_sel: torch.Tensor,
+             h_count: torch.Tensor) -> None:
+        """Issue step i (consecutive i from 0): pinned host inputs and outputs,
+        complete after ``wait(i)`` or ``synchronize()``. Asynchronous."""
+        abi.srh_hostloop_step(self.ds.ctx, self.lp, i, h_fm_q, h_q, h_out, h_sel, h_count)
+
+    def wait(self, i: int) -> None:
+        abi.srh_hostloop_wait(self.ds.ctx, self.lp, i)
+
+    def synchronize(self) -> None:
+        abi.srh_hostloop_sync(self.ds.ctx, self.lp)
+
+    def close(self) -> None:
+        if self.lp:
+            abi.srh_hostloop_destroy(self.lp)
+            self.lp = None
+
+    def __del__(self):  # pragma: no cover
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 def bits_to_i16(a: np.ndarray) -> torch.Tensor:
     """uint16 bf16 bit patterns as an int16 tensor (same bytes)."""
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16))

@@ -438,17 +438,18 @@ def test_replay_after_unconsumed_scoring_selects_right(ctx_len):
 
 
 def test_host_loop_matches_eager_steps():
-    """runtime.HostLoop (pinned host inputs and outputs, copies of neighbouring
-    steps overlapping the step in flight) gives, step for step, the bits of
-    eager steps fed through the bound buffers."""
-    from sparse_retrieval_host_gb300.runtime import HostLoop, bits_to_i16
+    """runtime.HostLoop and the library's native loop (srh_hostloop_*, through
+    runtime.NativeHostLoop) -- pinned host inputs and outputs, copies of
+    neighbouring steps overlapping the step in flight -- give, step for step,
+    the bits of eager steps fed through the bound buffers."""
+    from sparse_retrieval_host_gb300.runtime import HostLoop, NativeHostLoop, bits_to_i16
     w = C.TINY.with_(steps=10)
     n = 9
     h_fmq = [bits_to_i16(np.stack([G.fm_queries(w, t, b) for b in range(w.batch)])).pin_memory() for t in range(n)]
     h_q = [bits_to_i16(np.stack([np.stack([G.attn_q(w, t, l, b) for b in range(w.batch)])
                                  for l in range(w.n_layers)])).pin_memory() for t in range(n)]
     runs = []
-    for mode in ("eager", "loop"):
+    for mode in ("eager", "loop", "native"):
         ds = make_ds(w)
         try:
             fill(ds, w)
@@ -463,17 +464,22 @@ def test_host_loop_matches_eager_steps():
                     ds.step(spec)
                     outs.append((ds.out.cpu(), ds.sel.cpu(), ds.count.cpu()))
             else:
-                loop = HostLoop(ds, spec)
+                loop = HostLoop(ds, spec) if mode == "loop" else NativeHostLoop(ds, spec)
                 bufs = [(torch.empty(ds.out.shape).pin_memory(), torch.empty(ds.sel.shape, dtype=torch.int32).pin_memory(),
                          torch.empty(ds.count.shape, dtype=torch.int32).pin_memory()) for _ in range(1, n)]
                 for i, t in enumerate(range(1, n)):
                     loop.step(i, h_fmq[t], h_q[t], *bufs[i])
+                if mode == "native":
+                    loop.wait(n - 3)                        # the second-to-last step's outputs
                 loop.synchronize()
+                if mode == "native":
+                    loop.close()
                 outs = bufs
             assert ds.check_error() == 0
             runs.append(outs)
         finally:
             ds.close()
-    for a, b in zip(*runs):
-        for x, y in zip(a, b):
-            assert torch.equal(x, y)
+    for run in runs[1:]:                                     # each loop against the eager steps
+        for a, b in zip(runs[0], run):
+            for x, y in zip(a, b):
+                assert torch.equal(x, y)
