@@ -662,6 +662,7 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
 }
 
 constexpr int kGatherWarps = 8;
+constexpr int kGatherRows = 4;   // rows in flight per gather warp
 
 
 __global__ void __launch_bounds__(kGatherWarps * 32)
@@ -677,15 +678,27 @@ gather_kernel(const LayerDev* __restrict__ layers, const int* __restrict__ swap_
     const int nm = miss_count[lb];
     const LayerDev ld = layers[l];
     const int2* ml = miss + lb * S;
-    for (int i = blockIdx.x * kGatherWarps + warp; i < nm; i += gridDim.x * kGatherWarps) {
-        const int2 e = ml[i];
-        if (e.x < 0 || e.x >= ld.cap || e.y < 0 || e.y >= G) {
-            if (lane == 0) atomicOr(err, kErrBounds);
-            continue;
+    // up to kGatherRows rows per warp in flight: their loads are all issued
+    // before the first store (a host row's first read may wait on the
+    // translation of its page)
+    const int step = gridDim.x * kGatherWarps;
+    for (int i0 = blockIdx.x * kGatherWarps + warp; i0 < nm; i0 += kGatherRows * step) {
+        int2 e[kGatherRows];
+        bool ok[kGatherRows];
+#pragma unroll
+        for (int r = 0; r < kGatherRows; ++r) {
+            const int i = i0 + r * step;
+            e[r] = i < nm ? ml[i] : make_int2(-1, -1);
+            ok[r] = i < nm && e[r].x >= 0 && e[r].x < ld.cap && e[r].y >= 0 && e[r].y < G;
+            if (i < nm && !ok[r] && lane == 0) atomicOr(err, kErrBounds);
         }
-        float4 v[4];
-        load_row(v, ld.pool + ((size_t)b * ld.cap + e.x) * kKvDim, lane);
-        store_row_h(staging + (((size_t)l * B + b) * G + e.y) * kKvDim, v, lane, err);
+        float4 v[kGatherRows][4];
+#pragma unroll
+        for (int r = 0; r < kGatherRows; ++r)
+            if (ok[r]) load_row(v[r], ld.pool + ((size_t)b * ld.cap + e[r].x) * kKvDim, lane);
+#pragma unroll
+        for (int r = 0; r < kGatherRows; ++r)
+            if (ok[r]) store_row_h(staging + (((size_t)l * B + b) * G + e[r].y) * kKvDim, v[r], lane, err);
     }
 }
 
