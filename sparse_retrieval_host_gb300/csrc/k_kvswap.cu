@@ -662,10 +662,12 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
 }
 
 constexpr int kGatherWarps = 8;
-constexpr int kGatherRows = 4;   // rows in flight per gather warp
+constexpr int kGatherRows = 3;   // rows in flight per gather warp
 
 
-__global__ void __launch_bounds__(kGatherWarps * 32)
+// at most 85 registers: three gather CTAs per SM, so that the whole grid is
+// resident beside the resolve CTAs and the attention behind it can launch
+__global__ void __launch_bounds__(kGatherWarps * 32, 3)
 gather_kernel(const LayerDev* __restrict__ layers, const int* __restrict__ swap_layers, int B, int G, int S,
               const int2* miss, const int* miss_count,
               uint16_t* __restrict__ staging, uint32_t* __restrict__ err) {
