@@ -14,7 +14,9 @@
 // memory stages. Roles (192 threads, two CTAs per SM):
 //   warp 0   one thread issues the TMA loads: the sequence's query block once
 //            (24 rows, padded to 32 with zeros by the tensor map), then every
-//            tile, each as two 128B-swizzled boxes of 128 chunks x 64 d;
+//            tile, each as two 128B-swizzled boxes of 128 chunks x 64 d; the
+//            query block and the first two tiles as soon as the barriers are
+//            initialized, before the CTA's set-up barrier;
 //   warp 1   allocates TMEM; one thread issues, per tile, the eight
 //            tcgen05.mma kind::f16 (bf16) steps S[c, i*8+h] = K[c, :] . Q[i,h, :]
 //            (M = 128 chunks, N = 32, K = 128) into one of two TMEM
@@ -95,6 +97,15 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     const int t1 = (int)((long long)(blockIdx.x + 1) * a.tiles / a.parts);
     const int nt = t1 - t0;
     pdl_trigger();
+    // tile i of this CTA's range into stage i % kStages (thread 0)
+    auto issue_tile = [&](int i) {
+        const int s = i % kStages;
+        const uint32_t dst = smem_u32(sm + s * kStageBytes);
+        const int y = (t0 + i) * kTile;
+        mbar_arrive_expect_tx(&bs.full[s], kStageBytes);
+        tma_load_3d(dst, &kmap, 0, y, b, &bs.full[s]);
+        tma_load_3d(dst + kHalfBytes, &kmap, 64, y, b, &bs.full[s]);
+    };
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -109,6 +120,19 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         mbar_init(&bs.drain, 1);
         bs.abort = 0;
         fence_mbar_init();
+        if (nt > 0) {
+            // the queries and the first tiles are requested before the set-up
+            // barrier, so that HBM starts streaming while TMEM and the histogram
+            // are set up (the barriers' initialization is ordered before the
+            // copies' completions by the proxy fence)
+            fence_async_smem();
+            asm volatile("prefetch.tensormap [%0];\n" ::"l"(&kmap) : "memory");
+            const uint32_t q0 = smem_u32(sm + kOffQ);
+            mbar_arrive_expect_tx(&bs.qfull, kQBytes);
+            tma_load_3d(q0, &qmap, 0, 0, b, &bs.qfull);
+            tma_load_3d(q0 + kQBytes / 2, &qmap, 64, 0, b, &bs.qfull);
+            for (int i = 0; i < nt && i < kStages; ++i) issue_tile(i);
+        }
     }
     if (warp == 1) tmem_alloc(&bs.tmem_base, kAcc * kN);
     if (a.hist)
@@ -121,23 +145,15 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && nt > 0) {
-            asm volatile("prefetch.tensormap [%0];\n" ::"l"(&kmap) : "memory");
-            const uint32_t q0 = smem_u32(sm + kOffQ);
-            mbar_arrive_expect_tx(&bs.qfull, kQBytes);
-            tma_load_3d(q0, &qmap, 0, 0, b, &bs.qfull);
-            tma_load_3d(q0 + kQBytes / 2, &qmap, 64, 0, b, &bs.qfull);
-            int issued = 0;
-            for (int i = 0; i < nt; ++i) {
+            // the queries and tiles 0 .. kStages - 1 were issued before the set-up barrier
+            int issued = nt < kStages ? nt : kStages;
+            for (int i = issued; i < nt; ++i) {
                 const int s = i % kStages;
-                if (i >= kStages && !wait_tc(&bs.empty[s], ((i / kStages) + 1) & 1, abort)) {
+                if (!wait_tc(&bs.empty[s], ((i / kStages) + 1) & 1, abort)) {
                     ok = false;
                     break;
                 }
-                const uint32_t dst = smem_u32(sm + s * kStageBytes);
-                const int y = (t0 + i) * kTile;
-                mbar_arrive_expect_tx(&bs.full[s], kStageBytes);
-                tma_load_3d(dst, &kmap, 0, y, b, &bs.full[s]);
-                tma_load_3d(dst + kHalfBytes, &kmap, 64, y, b, &bs.full[s]);
+                issue_tile(i);
                 issued = i + 1;
             }
             if (!ok) {
