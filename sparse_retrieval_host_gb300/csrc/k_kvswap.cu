@@ -16,12 +16,15 @@
 // The walk is sequential on the pages, so a miss may pop the slot of a chunk
 // that is selected later in the same list. The kernel first assumes that never
 // happens (hits are the resident chunks; the i-th miss takes the i-th non-hit
-// slot in LRU order), checks that assumption exactly in parallel, and replays
-// the list one id at a time in shared memory only when it fails. Both paths
-// produce the state and outputs of the sequential list.
+// slot in LRU order), checks that assumption exactly in parallel, and only
+// when it fails replays the list in order in shared memory, visiting just the
+// misses (one warp: runs of up to 32 misses that pop unlisted slots at once,
+// every other miss one at a time). Both paths produce the state and outputs of
+// the sequential list.
 //
 // The miss gather reads the mapped pinned pool directly (zero-copy over the
-// host link), one warp per 2 KiB chunk, 16-byte loads. A staged row is kept
+// host link): each warp moves 2 KiB chunks with 16-byte loads, up to three
+// chunks in flight, only for the layers that swap. A staged row is kept
 // as fp16 (1 KiB): the attention rounds every row to fp16 for its tensor-core
 // products anyway, so staging the rounded row gives the same results from half
 // the bytes. A pool value beyond fp16's finite range (65504) sets kErrRange.
@@ -663,7 +666,6 @@ lru_kernel(const LayerDev* __restrict__ layers, int l0, int B, int G, int S, int
 
 constexpr int kGatherWarps = 8;
 constexpr int kGatherRows = 3;   // rows in flight per gather warp
-
 
 // at most 85 registers: three gather CTAs per SM, so that the whole grid is
 // resident beside the resolve CTAs and the attention behind it can launch
