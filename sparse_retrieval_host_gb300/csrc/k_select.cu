@@ -20,11 +20,13 @@
 // global top-`clamp`, so it falls through to the top-k path with k = clamp.
 //
 // Two accelerations, both exact:
-//   * for large n, a multi-CTA collect pass first appends the chunks that can
-//     be selected (first digit at or above the cut-off digit of the k-th key,
-//     or above the threshold) to a candidate list; the per-sequence CTA then
-//     works on that list instead of all n scores (if the list overflows its
-//     capacity, the CTA scans all n scores as before);
+//   * for large n, the per-sequence CTA works on a candidate list instead of
+//     all n scores: the chunks that can be selected (first digit at or above
+//     the cut-off digit of the k-th key, or above the threshold). A multi-CTA
+//     collect pass appends them; in threshold mode the scoring pass after a
+//     threshold selection has already appended the chunks above that same
+//     threshold, and the collect pass is skipped. If the list overflows its
+//     capacity, the CTA scans all n scores as before;
 //   * when the first digit already isolates the selection, the output is
 //     placed without a sort. The keys at or above the cut-off digit are
 //     counted into 4096 fine buckets: a shift of the 32-bit score key over the
