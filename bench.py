@@ -156,10 +156,37 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def code_hash(path: str) -> str:
+    """sha256 (first 16 hex digits) of a C++/CUDA source with its comments and
+    whitespace removed: a change to the code changes it, a change to the
+    comments does not. String and character literals are kept as they are."""
+    src = open(path, encoding="utf-8").read()
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            if not c.isspace():
+                out.append(c)
+            i += 1
+    return hashlib.sha256("".join(out).encode("utf-8")).hexdigest()[:16]
+
+
 def traffic_record(kernel: str, workload: str):
     """Measured DRAM bytes per launch from an ncu capture of this workload, if the
-    kernel source is unchanged since (profiles/traffic.json keys it by a hash of
-    the source and names the workload it was taken on)."""
+    kernel's code is unchanged since (profiles/traffic.json keys it by
+    code_hash of the source and names the workload it was taken on)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -168,8 +195,7 @@ def traffic_record(kernel: str, workload: str):
     if not rec or rec.get("workload") != workload:
         return None
     src = os.path.join(ROOT, "sparse_retrieval_host_gb300", "csrc", rec["source"])
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return rec if h == rec.get("source_sha") else None
+    return rec if code_hash(src) == rec.get("source_code_hash") else None
 
 
 # --------------------------------------------------------------------------- setup

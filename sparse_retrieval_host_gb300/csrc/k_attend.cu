@@ -1,5 +1,5 @@
 // K-attend: split-K flash-decode on the 5th-generation tensor cores, with the
-// split merge inside the same (cooperative) kernel.
+// split merge inside the same kernel.
 //
 // PocketLLM "FlashMemory 1M 上下文显存优化使用文档", section 技术细节 / 架构概览,
 // per-layer box step 3 (indexed_cached_attention over window + selected rows)
@@ -15,17 +15,20 @@
 // one wave, otherwise a contiguous range of the whole call's tiles. Each row
 // is read from HBM once per call.
 //
-// One CTA of 32 warps per SM. A CTA's row stream is bound by the bytes it
-// keeps in flight, so every warp streams rows: warp w owns tile rows w, w+32,
-// w+64, w+96 and loads two whole 2 KiB rows at a time (512 contiguous bytes
-// per load instruction, 128 KB in flight per CTA), converts them to fp16 and
-// stores them into one resident 128B-swizzled tile E [128 rows x 512 d]
-// (8 d-blocks of 64). Rows past the segment's end are zero-filled, not loaded.
+// One CTA of 16 warps per SM. A CTA's row stream is bound by the bytes it
+// keeps in flight, so every warp streams rows: warp w owns tile rows w + 16 j
+// (j < 8), 1 KiB of contiguous bytes per load instruction (32-byte loads).
+// A tile of fp16 staged rows has all eight of a warp's rows in flight; a tile
+// holding fp32 window rows (2 KiB each) four, each row's registers taking the
+// next row once stored: 128 KB in flight per CTA either way. Every row is
+// stored once, as fp16, into one resident 128B-swizzled tile E [128 rows x
+// 512 d] (8 d-blocks of 64). Rows past the segment's end are zero-filled, not
+// loaded.
 //   pass 1  S^T[r, h] = E[r, :] . Q[h, :]   (M = 128 rows, N = heads, K = 512),
 //           E and Q K-major;
 //   softmax every warp: warp w reads TMEM lanes 32 (w % 4) (its rows) and the
-//           H/8 head columns of group w / 4; per-head tile max and sum by warp
-//           butterflies and a 4-warp exchange in shared memory; base-2 online
+//           H/4 head columns of group w / 4; per-head tile max and sum by warp
+//           reductions and a 4-warp exchange in shared memory; base-2 online
 //           softmax with a lazily moved reference max (moved only when the tile
 //           max exceeds it by 2^8); P written as fp16 [rows x heads];
 //   pass 2  O^T[d, h] += E^T[d, r] P[r, h]   (M = 128 d, N = heads, K = rows),
@@ -39,21 +42,24 @@
 // normal fp16 range convert exactly.
 //
 // With more than one tile in a segment, the next tile's rows are requested
-// into L2 (one 2 KiB bulk prefetch per row) when a tile starts, so HBM keeps
+// into L2 (one bulk prefetch per row) when a tile starts, so HBM keeps
 // streaming while the tile's products and softmax run; its loads then find the
 // rows in L2. Every wait is bounded; on a timeout the CTA records kErrTimeout,
 // drains its MMAs, frees TMEM and returns.
 //
 // A pair spread over several segments: each segment writes its normalized
-// output O / l as fp16 with its (m, l) statistics, and raises the pair's
-// arrival counter. When a CTA has run all its segments, it waits (bounded) for
+// output as fp16, (O / l) / sc with sc the power of two at or below the
+// largest |row value| it read (so the values stay in fp16's normal range),
+// with its statistics (m, l, sc), and raises the pair's arrival counter. When a CTA has run all its segments, it waits (bounded) for
 // the counters of the split pairs it took part in and merges its share of each
 // such pair's output, in split order:
-//     o_h = sum_s w_s O_s[h] / l_s,   w_s = l_s 2^(m_s - M) / sum_s' l_s' 2^(m_s' - M).
-// The CTAs of the grid wait on one another only there, so the kernel is
-// launched cooperatively (every CTA resident). The plan depends only on the
-// configuration, so identical rows give identical bits whatever slots hold
-// them.
+//     o_h = sum_s w_s O_s[h] / l_s,   w_s = l_s 2^(m_s - M) / sum_s' l_s' 2^(m_s' - M),
+// each stored partial multiplied back by its sc_s (folded into w_s).
+// The CTAs of the grid wait on one another only there. A plan never has more
+// CTAs than SMs and a CTA takes a whole SM, so every CTA of the grid becomes
+// resident once the kernels ahead of it leave their SMs; the wait is bounded
+// all the same. The plan depends only on the configuration, so identical rows
+// give identical bits whatever slots hold them.
 #include <cmath>
 #include <cstddef>
 
