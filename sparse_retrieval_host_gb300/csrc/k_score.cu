@@ -16,7 +16,9 @@
 // one n-tile of 8 columns is exactly one indexer's 8 heads, so the head max is
 // a 4-lane shuffle. The epilogue writes the fp32 score and bumps a 4096-bin
 // histogram of its order-preserving key (top 12 bits) that the selector uses
-// to skip its first radix pass.
+// to skip its first radix pass; a pass that follows a threshold selection
+// builds no histogram and instead appends the chunks above that threshold to
+// the selection's candidate list (warp-aggregated).
 //
 // The reduction dimension is permuted inside every 32-wide block of d so each
 // lane reads 16 contiguous bytes of a key row; A and B use the same

@@ -1,4 +1,5 @@
-// Host side of the C ABI: context creation, validation, pinned pools, launches.
+// Host side of the C ABI: context creation, validation, pinned pools, launches,
+// the attention's static work plan and the native host loop (srh_hostloop_*).
 //
 // Guards restated from PocketLLM "FlashMemory 1M 上下文显存优化使用文档":
 //   * section 关键参数调优 item 1 and 故障排查 error 2: GPU_CHUNKS must be >=

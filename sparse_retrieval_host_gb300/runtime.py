@@ -3,8 +3,12 @@
 ``DecodeStep`` owns a library context (pinned pools, slot tables, scratch) and
 the caller-side device tensors the C ABI reads and writes. ``step()`` issues
 fm_score -> fm_select -> kvswap_stage -> lsa_attend on one stream (the miss
-gathers go to a side stream when one is given). PyTorch is used only to
-allocate device memory and to name streams.
+gathers go to a side stream when one is given), and ``capture()`` records the
+step into CUDA graphs. ``HostLoop`` and ``NativeHostLoop`` run steps from pinned
+host buffers: queries copied in, outputs and the selection copied out, the
+copies of neighbouring steps overlapping the step (issued from Python, or by one
+library call per step). PyTorch is used only to allocate device memory and to
+name streams.
 """
 from __future__ import annotations
 
