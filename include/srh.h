@@ -230,7 +230,12 @@ int srh_max_select(srh_ctx* ctx);
  *   d_scores [batch][n] fp32 output: s(c), where
  *            s_i(c) = scale * max_h <Q[i,h], K[c]> + b_i and s = max_i or mean_i.
  * Also fills a per-sequence score histogram inside the context that fm_select
- * uses when it is called on the same d_scores.
+ * uses when it is called on the same d_scores. After a threshold selection
+ * (fm_select with SRH_SELECT_THRESH) the next fm_score instead appends every
+ * chunk above that threshold to a candidate list inside the context; the next
+ * threshold selection with the same tau on the same d_scores selects from that
+ * list and skips its own pass over the scores. Either way the outputs are
+ * those of the definitions above; only the work fm_select does changes.
  */
 int fm_score(srh_ctx* ctx, const uint16_t* d_keys, int n, const uint16_t* d_q, float scale,
              const float* bias3, int ensemble, float* d_scores, srh_stream_t stream);
