@@ -483,7 +483,9 @@ int srh_reset_stats(srh_ctx* ctx);
  *   stream      GPU work already issued on it precedes the loop's first step
  *   out         receives the loop (NULL on failure)
  * The loop keeps the pointers: the buffers must outlive it. The context's
- * chaining flag is off when the call returns. Returns SRH_OK, SRH_ERR_INVALID,
+ * chaining flag (srh_set_chained) is as the caller left it when the call
+ * returns; inside the graphs the first kernel is never chained and the others
+ * always are. Returns SRH_OK, SRH_ERR_INVALID,
  * SRH_ERR_NOMEM or SRH_ERR_CUDA (details in srh_last_error(ctx)).
  */
 typedef struct srh_hostloop srh_hostloop;

@@ -1069,9 +1069,11 @@ int srh_hostloop_create(srh_ctx* ctx, const uint16_t* d_keys, int n, float* d_sc
     if (e == cudaSuccess) e = cudaEventRecord(lp->ev_in[0], (cudaStream_t)stream);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(lp->s_comp, lp->ev_in[0], 0);
     if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "host loop start"));
+    const bool was_chained = ctx->chained;   // the caller's setting, restored after each capture
     for (int s = 0; s < 2; ++s) {
         e = cudaStreamBeginCapture(lp->s_comp, cudaStreamCaptureModeThreadLocal);
         if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "host loop capture"));
+        ctx->chained = false;                 // the graph's first kernel has no predecessor
         int rc = fm_score(ctx, d_keys, n, lp->fm_q[s], scale, bias3, ensemble, d_scores, lp->s_comp);
         if (rc == SRH_OK) {
             ctx->chained = true;
@@ -1082,8 +1084,8 @@ int srh_hostloop_create(srh_ctx* ctx, const uint16_t* d_keys, int n, float* d_sc
             if (rc == SRH_OK)
                 rc = lsa_attend(ctx, -1, lp->q[s], n_heads, d_window, d_staging, d_phys, d_count_l, lp->out[s],
                                 lp->s_comp);
-            ctx->chained = false;
         }
+        ctx->chained = was_chained;
         cudaGraph_t g = nullptr;
         const cudaError_t ec = cudaStreamEndCapture(lp->s_comp, &g);
         if (rc != SRH_OK) {
