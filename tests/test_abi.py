@@ -96,3 +96,21 @@ def test_null_context_calls_are_invalid(abi):
     assert lib.fm_score(None, None, 1, None, ctypes.c_float(1.0), None, 0, None, None) == abi.SRH_ERR_INVALID
     assert lib.lsa_attend(None, -1, None, 64, None, None, None, None, None, None) == abi.SRH_ERR_INVALID
     lib.srh_destroy(None)
+
+
+def test_null_host_loop_calls_are_invalid(abi):
+    """The native host loop's entry points refuse a missing context or loop
+    before any GPU call, and its destroy accepts NULL."""
+    lib = abi.load()
+    out = ctypes.c_void_p(12345)
+    bias = (ctypes.c_float * 3)(0.0, 0.0, 0.0)
+    rc = lib.srh_hostloop_create(None, None, 1, None, None, None, None, None, 64, ctypes.c_float(1.0), bias, 0, 0,
+                                 1, ctypes.c_float(0.5), 0, None, None, None, None, None, None, ctypes.byref(out))
+    assert rc == abi.SRH_ERR_INVALID
+    assert lib.srh_hostloop_create(None, None, 1, None, None, None, None, None, 64, ctypes.c_float(1.0), bias, 0, 0,
+                                   1, ctypes.c_float(0.5), 0, None, None, None, None, None, None,
+                                   None) == abi.SRH_ERR_INVALID
+    assert lib.srh_hostloop_step(None, 0, None, None, None, None, None) == abi.SRH_ERR_INVALID
+    assert lib.srh_hostloop_wait(None, 0) == abi.SRH_ERR_INVALID
+    assert lib.srh_hostloop_sync(None) == abi.SRH_ERR_INVALID
+    lib.srh_hostloop_destroy(None)
