@@ -114,3 +114,22 @@ def test_null_host_loop_calls_are_invalid(abi):
     assert lib.srh_hostloop_wait(None, 0) == abi.SRH_ERR_INVALID
     assert lib.srh_hostloop_sync(None) == abi.SRH_ERR_INVALID
     lib.srh_hostloop_destroy(None)
+
+
+def test_every_entry_point_refuses_null_arguments(abi):
+    """Every int-returning export, called with every pointer NULL and every
+    number zero, returns SRH_ERR_INVALID before any GPU call; the pointer
+    getter returns NULL and the destroy calls accept NULL (the header's error
+    behaviour, checked for each function the binding declares)."""
+    lib = abi.load()
+    numbers = (ctypes.c_int, ctypes.c_long, ctypes.c_longlong, ctypes.c_uint, ctypes.c_ulonglong, ctypes.c_size_t)
+    checked = []
+    for name, res, argtypes in abi.SIGNATURES:
+        args = [0 if t in numbers else 0.0 if t in (ctypes.c_float, ctypes.c_double) else None for t in argtypes]
+        r = getattr(lib, name)(*args)
+        if res is ctypes.c_int:
+            assert r == abi.SRH_ERR_INVALID, (name, r)
+            checked.append(name)
+        elif isinstance(res, type) and issubclass(res, ctypes._Pointer):
+            assert not r, name
+    assert len(checked) >= 25 and {"fm_score", "fm_select", "kvswap_stage", "lsa_attend"} <= set(checked)
